@@ -1,0 +1,235 @@
+/*
+ * libidx -- sparse-attention indexer hot path on one GB300 (sm_103a).
+ *
+ * Plain C ABI.  Every pointer named "device" is a CUDA device pointer owned by
+ * the caller; the library never allocates device memory on these paths and
+ * never synchronises the host: all work is enqueued on the caller's stream
+ * (`stream` is a cudaStream_t; NULL is the legacy default stream).  Entry points
+ * that need scratch memory take (ws, ws_bytes) and have a *_workspace_size()
+ * query; the workspace is caller-owned device memory, at least 256-byte
+ * aligned, and may be reused across calls that do not overlap on the GPU.
+ *
+ * Every argument that the host can see is validated before anything is
+ * launched; a call that returns an error has enqueued nothing and written
+ * nothing.  Values that live in device memory (key_len, key_off, context
+ * lengths, query positions) cannot be checked by the host: a row whose extent
+ * falls outside the key buffer or above max_key_len is treated as a row with
+ * no visible keys and sets IDX_DEVERR_BAD_ROW in the device error word
+ * (idx_device_error()).  Inputs are assumed finite; NaN scores are undefined.
+ *
+ * Notation follows the pages: M query rows, H index heads, D head dim, K the
+ * top-K, L_r the visible keys of row r, S the segment count.
+ */
+#ifndef IDX_H_
+#define IDX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------- status codes */
+typedef int32_t idx_status;
+enum {
+  IDX_OK = 0,
+  /* The three refusals of the segment-witness merge ("Segment Witnesses",
+   * section "Refusals"): context lengths do not cover every row; segment count
+   * zero (where there is no off switch) or above 64; retained prefix wider
+   * than the row. */
+  IDX_ERR_ROWS_MISMATCH = 1,
+  IDX_ERR_SEGMENTS_OUT_OF_RANGE = 2,
+  IDX_ERR_KEEP_OUT_OF_RANGE = 3,
+  IDX_ERR_INVALID_ARG = 4,          /* null pointer, negative size, K too large, ... */
+  IDX_ERR_UNSUPPORTED = 5,          /* dtype / shape combination not implemented */
+  IDX_ERR_WORKSPACE_TOO_SMALL = 6,
+  IDX_ERR_CUDA = 7                  /* a CUDA call failed; see idx_last_error_string() */
+};
+
+/* Device error word bits (idx_device_error). */
+enum {
+  IDX_DEVERR_WAIT_TIMEOUT = 1,      /* a pipeline wait hit its time limit; the kernel returned early */
+  IDX_DEVERR_BAD_ROW = 2,           /* a row's key extent was outside the key buffer */
+  IDX_DEVERR_CAPACITY = 4           /* an internal buffer overflowed; affected rows were recomputed */
+};
+
+/* Element types. */
+enum { IDX_F32 = 0, IDX_BF16 = 1, IDX_FP8_E4M3 = 2 };
+
+enum { IDX_MAX_SEGMENTS = 64, IDX_MAX_K = 4096 };
+
+/* Human-readable text of the last host-side error of this thread. */
+const char* idx_last_error_string(void);
+
+/* Synchronises the device, returns the device error word and clears it. */
+uint32_t idx_device_error(void);
+
+/* ----------------------------------------------------------- the problem ---
+ * One batch of indexer rows ("DoSA：用安全上界减少 Indexer 的完整打分",
+ * section 3: one index key per position, shared by every head of a query).
+ *
+ *   q        device [M, H, D], q_dtype IDX_F32 or IDX_BF16, row-major.
+ *   w        device [M, H] float32 head weights (either sign).
+ *   keys     device [n_keys, D], k_dtype IDX_F32, IDX_BF16 or IDX_FP8_E4M3,
+ *            row-major, rows 16-byte aligned for the bf16/fp8 paths.
+ *   key_scale device [n_keys] float32 per-token dequantisation scale (> 0),
+ *            required for IDX_FP8_E4M3 and NULL otherwise; the score of an FP8
+ *            key k = scale * code is scale * sum_h w_h ReLU(q_h . code).
+ *   key_off  device [M] int64, or NULL.  NULL: every row reads one shared key
+ *            sequence starting at keys[0] (causal prefill; row m sees keys
+ *            0..key_len[m]-1).  Non-NULL: row m reads its own keys
+ *            keys[key_off[m] .. key_off[m]+key_len[m]-1] (decode).
+ *   key_len  device [M] int32, L_r >= 0; key ids are row-relative, 0..L_r-1.
+ *   max_key_len host-side bound on every key_len[m] (sizes grids/workspaces).
+ *
+ * Supported: (F32 q, F32 keys) any H <= 128, D <= 256 on CUDA cores;
+ * (BF16 q, BF16 keys) and (BF16 q, FP8 keys) with D = 128 and H in
+ * {16, 32, 64, 128} on the tensor cores; (BF16 q, BF16 keys) other shapes on
+ * CUDA cores.  The same combination always takes the same kernels, so every
+ * exact score of a (query, key) pair has the same bits on every path.
+ */
+typedef struct idx_problem {
+  const void* q;
+  int32_t q_dtype;
+  const float* w;
+  int64_t M;
+  int32_t H;
+  int32_t D;
+  const void* keys;
+  int32_t k_dtype;
+  const float* key_scale;
+  int64_t n_keys;
+  const int64_t* key_off;
+  const int32_t* key_len;
+  int32_t max_key_len;
+} idx_problem;
+
+/* ---------------------------------------------------------------- idx_score
+ * Indexer score s(k) = sum_h w_h ReLU(q_h . k) for every visible key
+ * ("DoSA：用安全上界减少 Indexer 的完整打分", section 3, the equation for s(k)).
+ * scores: device [M, ld_scores] float32; row m receives s for ids
+ * 0..key_len[m]-1; entries at and beyond key_len[m] are not written.
+ * ld_scores >= max_key_len.  No workspace. */
+idx_status idx_score(const idx_problem* p, float* scores, int64_t ld_scores, void* stream);
+
+/* ---------------------------------------------------------------- idx_topk
+ * Exact top-K of every row under the total order (score desc, key id asc)
+ * (same page, section 1 and the note after section 2: the final choice is by
+ * the original scorer, and equal ids need one consistent total order).
+ * out_ids: device [M, K] int32, sorted in that order; rows with fewer than K
+ * visible keys are padded with -1.  out_scores: device [M, K] float32 or NULL,
+ * padded with -inf; -0.0 is reported as +0.0.  1 <= K <= IDX_MAX_K. */
+size_t idx_topk_workspace_size(const idx_problem* p, int32_t K);
+idx_status idx_topk(const idx_problem* p, int32_t K, int32_t* out_ids, float* out_scores, void* ws,
+                    size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------- idx_topk_scores
+ * The top-K step alone, on score rows the caller already has: row m is
+ * scores[m*ld .. m*ld + lens[m]-1] (device float32, lens device int32), ids
+ * are positions in the row.  Same order, padding and K limit as idx_topk.
+ * No workspace. */
+idx_status idx_topk_scores(const float* scores, int64_t ld, const int32_t* lens, int64_t M, int32_t max_len,
+                           int32_t K, int32_t* out_ids, float* out_scores, void* stream);
+
+/* --------------------------------------------------------------- dosa_topk
+ * DoSA safe-upper-bound pruning ("DoSA：用安全上界减少 Indexer 的完整打分",
+ * sections 2, 3.1, 3.2 and 4): per row, seeds fully scored give the threshold
+ * tau (K-th best seed score) and the seed top-K; every other visible key gets
+ * an upper bound U from R retained heads (omitted positive heads bounded via an
+ * anchor and residual norm, section 3.1; omitted negative heads active on at
+ * least act_freq_min of n_sample seed samples deducted through the ReLU of
+ * their |w|-weighted aggregate, section 3.2) plus a rounding margin; keys with
+ * U < tau are dropped; the rest are scored exactly, those with s >= tau merged
+ * with the seed top-K and the final K chosen by (score desc, id asc).
+ * Output contract: identical, bit for bit, to idx_topk on the same inputs.
+ *
+ * seed_ids: device [M, seed_ld] int32 (row-relative ids, -1 padded) or NULL:
+ * NULL selects the built-in rule -- with key_off == NULL (shared keys) the
+ * cold rule of section 4 (four evenly spaced representative queries, keys
+ * ranked by how many representative top-K lists hold them, then by their best
+ * representative score, then id; n_seed seeds from the common visible prefix),
+ * otherwise floor(i L_r / n) for i < n = min(L_r, n_seed).  A row with fewer
+ * than K distinct visible seeds, or whose candidate list overflows
+ * candidate_capacity, is computed on the unpruned path (row_status 1 resp. 2).
+ * row_status: device [M] int32 or NULL.  stats: device dosa_stats or NULL
+ * (counters are added to, not overwritten). */
+typedef struct dosa_params {
+  int32_t n_seed;             /* seeds per row (12288 for prefill) */
+  int32_t retained_heads;     /* R (16 / 20) */
+  int32_t n_sample;           /* seed samples for the activation statistics (128) */
+  float act_freq_min;         /* 0.5 */
+  float margin_gamma;         /* relative rounding margin (2^-10) */
+  int32_t candidate_capacity; /* per-row candidate list length */
+} dosa_params;
+
+typedef struct dosa_stats {
+  unsigned long long pairs;       /* visible (query, key) pairs decided */
+  unsigned long long seeds;       /* seed pairs fully scored */
+  unsigned long long candidates;  /* keys with U >= tau (rescored) */
+  unsigned long long survivors;   /* rescored keys with s >= tau */
+  unsigned long long fallback_rows;
+} dosa_stats;
+
+size_t dosa_topk_workspace_size(const idx_problem* p, int32_t K, const dosa_params* dp, int32_t seed_ld);
+idx_status dosa_topk(const idx_problem* p, int32_t K, const dosa_params* dp, const int32_t* seed_ids,
+                     int32_t seed_ld, int32_t* out_ids, float* out_scores, int32_t* row_status,
+                     dosa_stats* stats, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ witness_merge
+ * Segment-witness covering pass, in place ("Segment Witnesses", sections
+ * "Object" and "Implementation rule and contracts").  Row r of topk_ids
+ * (device [rows, topk] int32, row-relative offsets, negative = padding) with
+ * context length L_r = context_lens[r] (device int32): S_eff = min(S, L_r);
+ * occupancy O = {min(floor(x S_eff / L_r), S-1) : x >= 0 in the row};
+ * witnesses e_s = ceil(s L_r / S_eff) for s < S_eff not in O, in ascending s,
+ * overwrite slots keep, keep+1, ... up to B = min(max_replacements,
+ * topk - keep) slots; further witnesses are dropped, slots without a witness
+ * keep their value; rows with L_r <= 0 are unchanged.  The serving form is
+ * keep = max(topk - S, 0), max_replacements = S.
+ * Checks in order: S == 0 -> no-op (the off switch); S > 64 ->
+ * IDX_ERR_SEGMENTS_OUT_OF_RANGE; keep > topk or keep < 0 ->
+ * IDX_ERR_KEEP_OUT_OF_RANGE; n_context_lens < rows -> IDX_ERR_ROWS_MISMATCH;
+ * B <= 0 or rows == 0 -> no-op.  A refused call leaves the buffer untouched. */
+idx_status witness_merge(int32_t* topk_ids, int64_t rows, int32_t topk, const int32_t* context_lens,
+                         int64_t n_context_lens, int32_t keep, int32_t num_segments, int32_t max_replacements,
+                         void* stream);
+
+/* The witness table alone ("Segment Witnesses", Rust API
+ * topology_witness_indices): out device [rows, S] int32, out[r][s] = e_s when
+ * segment s < S_eff of row r is unoccupied, else -1.  S == 0 or S > 64 ->
+ * IDX_ERR_SEGMENTS_OUT_OF_RANGE; n_context_lens < rows -> ROWS_MISMATCH. */
+idx_status witness_indices(const int32_t* learned, int64_t rows, int32_t topk, const int32_t* context_lens,
+                           int64_t n_context_lens, int32_t num_segments, int32_t* out, void* stream);
+
+/* ------------------------------------------------------------- block_select
+ * MiniMax-M3 block-sparse selection ("ferrox_core/block_sparse.rs":
+ * block_sparse_select, select_for_head, dot).  For query i at position
+ * query_pos[i] (device int32 >= 0) and KV head h: n_blocks = min(pos/bs + 1,
+ * ceil(L/bs)) (0 when bs == 0); blocks [0, init) and [n_blocks - local,
+ * n_blocks) are forced; budget = max(top, #forced); every other block scores
+ * the max over its positions p < min((b+1) bs, L, pos+1) of the raw dot
+ * q.k_p, summed in sequence in f32 (products and sums rounded one by one);
+ * the best budget - #forced of them by (score desc, block asc) join the forced
+ * ones; the selection is written ascending.
+ *   index_q device [Q, n_kv, D] float32, index_k device [L, D] float32.
+ *   out device [Q, n_kv, out_width] int32, -1 padded; out_count device
+ *   [Q, n_kv] int32 or NULL.  out_width >= max(top, init + local).
+ * Block size 0 gives empty selections. */
+typedef struct block_sparse_config {
+  int32_t block_size;   /* 128: also the KV page size */
+  int32_t top_blocks;   /* 32 */
+  int32_t init_blocks;  /* 1 */
+  int32_t local_blocks; /* 2 */
+} block_sparse_config;
+
+size_t block_select_workspace_size(int64_t Q, int32_t n_kv, int64_t L, const block_sparse_config* cfg);
+idx_status block_select(const float* index_q, const float* index_k, const int32_t* query_pos, int64_t Q,
+                        int32_t n_kv, int32_t D, int64_t L, const block_sparse_config* cfg, int32_t* out,
+                        int32_t out_width, int32_t* out_count, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDX_H_ */

@@ -1,0 +1,258 @@
+// MiniMax-M3 block-sparse selection ("ferrox_core/block_sparse.rs":
+// block_sparse_select, select_for_head, dot).
+//
+// Two kernels:
+//  1. block_score_kernel: for each (query, KV head) pair and each visible,
+//     non-forced block, the max over the block's causally visible positions of
+//     the raw dot q.k_p, with the page's summation order: acc starts at 0 and
+//     acc = acc + q[d]*k[d] for d = 0..D-1, each product and each sum rounded
+//     to fp32 on its own (__fmul_rn / __fadd_rn, no FMA).  That order is what
+//     makes the selected block indices bit-exact, so this runs on the fp32
+//     CUDA-core pipes, not the tensor cores.  A thread block stages a chunk of
+//     the key block in shared memory (row-major, float4 broadcast reads) and
+//     every thread owns one pair, its query in registers (D = 128 path), and
+//     runs four positions at once for instruction-level parallelism.
+//  2. block_pick_kernel: per pair, forced blocks get the largest key, then the
+//     exact top-`budget` of (score desc, block asc) is taken and written in
+//     ascending block order.
+#include "internal.h"
+#include "topk.cuh"
+
+namespace idx {
+
+constexpr int kBsThreads = 128;   // pairs per thread block
+constexpr int kBsChunk = 64;      // key positions staged per round
+
+struct BlockGeom {
+  int64_t n_blocks;
+  int64_t n_forced;
+  int64_t budget;
+  bool scoring;  // false when the forced blocks already decide the selection
+};
+
+__device__ __forceinline__ BlockGeom block_geom(int64_t pos, int64_t L, const block_sparse_config& c) {
+  BlockGeom g{0, 0, 0, false};
+  if (c.block_size <= 0 || pos < 0) return g;
+  int64_t causal = pos / c.block_size + 1;
+  int64_t exist = (L + c.block_size - 1) / c.block_size;
+  g.n_blocks = causal < exist ? causal : exist;
+  const int64_t n = g.n_blocks;
+  int64_t a = c.init_blocks < n ? c.init_blocks : n;              // [0, a) forced
+  int64_t z = n - c.local_blocks;                                  // [max(z,0), n) forced
+  z = z < 0 ? 0 : z;
+  int64_t overlap = a > z ? a - z : 0;
+  g.n_forced = a + (n - z) - overlap;
+  g.budget = c.top_blocks > g.n_forced ? c.top_blocks : g.n_forced;
+  g.scoring = !(g.n_forced >= g.budget || g.n_forced == n);
+  return g;
+}
+
+__device__ __forceinline__ bool block_forced(int64_t b, int64_t n, const block_sparse_config& c) {
+  int64_t z = n - c.local_blocks;
+  return b < c.init_blocks || b >= (z < 0 ? 0 : z);
+}
+
+// D == 128: query in registers.  D == 0: any D, query read from global.
+template <int DC>
+__global__ void __launch_bounds__(kBsThreads) block_score_kernel(const float* __restrict__ q,
+                                                                  const float* __restrict__ k,
+                                                                  const int32_t* __restrict__ qpos, int64_t Q,
+                                                                  int n_kv, int D, int64_t L,
+                                                                  block_sparse_config c, int64_t nbm,
+                                                                  uint32_t* __restrict__ bkey) {
+  extern __shared__ __align__(16) float ks[];   // [chunk][D]
+  const int64_t n_pairs = Q * n_kv;
+  const int64_t pair = (int64_t)blockIdx.x * kBsThreads + threadIdx.x;
+  const bool live = pair < n_pairs;
+  const int64_t qi = live ? pair / n_kv : 0;
+  const int64_t pos = live ? (int64_t)qpos[qi] : -1;
+  const BlockGeom g = block_geom(pos, L, c);
+  const int chunk = (DC == 128) ? kBsChunk : (int)max(1, min(kBsChunk, 16384 / D));
+  const float* qrow = q + pair * (int64_t)D;
+
+  float qr[DC == 128 ? 128 : 1];
+  if (DC == 128 && live) {
+#pragma unroll
+    for (int d4 = 0; d4 < 32; ++d4) {
+      float4 v = __ldg(reinterpret_cast<const float4*>(qrow) + d4);
+      qr[4 * d4 + 0] = v.x;
+      qr[4 * d4 + 1] = v.y;
+      qr[4 * d4 + 2] = v.z;
+      qr[4 * d4 + 3] = v.w;
+    }
+  }
+
+  for (int64_t b = blockIdx.y; b < nbm; b += gridDim.y) {
+    const bool need = live && g.scoring && b < g.n_blocks && !block_forced(b, g.n_blocks, c);
+    if (!__syncthreads_or(need)) continue;
+    const int64_t start = b * c.block_size;
+    int64_t bend = start + c.block_size;
+    bend = bend < L ? bend : L;
+    int64_t vend = pos + 1 < bend ? pos + 1 : bend;   // this thread's visible end
+    float best = -__int_as_float(0x7f800000);
+    for (int64_t c0 = start; c0 < bend; c0 += chunk) {
+      const int cl = (int)((bend - c0) < chunk ? (bend - c0) : chunk);
+      __syncthreads();
+      if (DC == 128) {
+        const float4* src = reinterpret_cast<const float4*>(k + c0 * 128);
+        float4* dst = reinterpret_cast<float4*>(ks);
+        for (int i = threadIdx.x; i < cl * 32; i += kBsThreads) dst[i] = __ldg(src + i);
+      } else {
+        for (int i = threadIdx.x; i < cl * D; i += kBsThreads) ks[i] = __ldg(k + c0 * D + i);
+      }
+      __syncthreads();
+      if (!need) continue;
+      int nv = (int)(vend - c0);
+      nv = nv < 0 ? 0 : (nv > cl ? cl : nv);
+      if (DC == 128) {
+        int p = 0;
+        for (; p + 4 <= nv; p += 4) {
+          float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+          const float4* r0 = reinterpret_cast<const float4*>(ks + (p + 0) * 128);
+          const float4* r1 = reinterpret_cast<const float4*>(ks + (p + 1) * 128);
+          const float4* r2 = reinterpret_cast<const float4*>(ks + (p + 2) * 128);
+          const float4* r3 = reinterpret_cast<const float4*>(ks + (p + 3) * 128);
+#pragma unroll
+          for (int d4 = 0; d4 < 32; ++d4) {
+            const float4 k0 = r0[d4], k1 = r1[d4], k2 = r2[d4], k3 = r3[d4];
+            const float x0 = qr[4 * d4], x1 = qr[4 * d4 + 1], x2 = qr[4 * d4 + 2], x3 = qr[4 * d4 + 3];
+            a0 = __fadd_rn(a0, __fmul_rn(x0, k0.x));
+            a1 = __fadd_rn(a1, __fmul_rn(x0, k1.x));
+            a2 = __fadd_rn(a2, __fmul_rn(x0, k2.x));
+            a3 = __fadd_rn(a3, __fmul_rn(x0, k3.x));
+            a0 = __fadd_rn(a0, __fmul_rn(x1, k0.y));
+            a1 = __fadd_rn(a1, __fmul_rn(x1, k1.y));
+            a2 = __fadd_rn(a2, __fmul_rn(x1, k2.y));
+            a3 = __fadd_rn(a3, __fmul_rn(x1, k3.y));
+            a0 = __fadd_rn(a0, __fmul_rn(x2, k0.z));
+            a1 = __fadd_rn(a1, __fmul_rn(x2, k1.z));
+            a2 = __fadd_rn(a2, __fmul_rn(x2, k2.z));
+            a3 = __fadd_rn(a3, __fmul_rn(x2, k3.z));
+            a0 = __fadd_rn(a0, __fmul_rn(x3, k0.w));
+            a1 = __fadd_rn(a1, __fmul_rn(x3, k1.w));
+            a2 = __fadd_rn(a2, __fmul_rn(x3, k2.w));
+            a3 = __fadd_rn(a3, __fmul_rn(x3, k3.w));
+          }
+          best = fmaxf(best, __fadd_rn(a0, 0.0f));
+          best = fmaxf(best, __fadd_rn(a1, 0.0f));
+          best = fmaxf(best, __fadd_rn(a2, 0.0f));
+          best = fmaxf(best, __fadd_rn(a3, 0.0f));
+        }
+        for (; p < nv; ++p) {
+          float a = 0.0f;
+          const float4* r = reinterpret_cast<const float4*>(ks + p * 128);
+#pragma unroll
+          for (int d4 = 0; d4 < 32; ++d4) {
+            const float4 kv = r[d4];
+            a = __fadd_rn(a, __fmul_rn(qr[4 * d4], kv.x));
+            a = __fadd_rn(a, __fmul_rn(qr[4 * d4 + 1], kv.y));
+            a = __fadd_rn(a, __fmul_rn(qr[4 * d4 + 2], kv.z));
+            a = __fadd_rn(a, __fmul_rn(qr[4 * d4 + 3], kv.w));
+          }
+          best = fmaxf(best, __fadd_rn(a, 0.0f));
+        }
+      } else {
+        for (int p = 0; p < nv; ++p) {
+          float a = 0.0f;
+          for (int d = 0; d < D; ++d) a = __fadd_rn(a, __fmul_rn(__ldg(qrow + d), ks[p * D + d]));
+          best = fmaxf(best, __fadd_rn(a, 0.0f));
+        }
+      }
+    }
+    if (need) bkey[pair * nbm + b] = score_key(best);
+  }
+}
+
+constexpr int kPickThreads = 256;
+
+struct BlockKeyRow {
+  const uint32_t* k;
+  int64_t n_blocks;
+  block_sparse_config c;
+  __device__ int n() const { return (int)n_blocks; }
+  __device__ uint32_t key(int b) const { return block_forced(b, n_blocks, c) ? 0xffffffffu : k[b]; }
+  __device__ int32_t id(int b) const { return b; }
+};
+
+__global__ void __launch_bounds__(kPickThreads) block_pick_kernel(const int32_t* __restrict__ qpos, int64_t Q,
+                                                                   int n_kv, int64_t L, block_sparse_config c,
+                                                                   int64_t nbm, const uint32_t* __restrict__ bkey,
+                                                                   int32_t* __restrict__ out, int W,
+                                                                   int32_t* __restrict__ out_count) {
+  __shared__ TopkShared<kPickThreads> sh;
+  extern __shared__ uint64_t sel[];
+  const int64_t pair = blockIdx.x;
+  const int64_t qi = pair / n_kv;
+  const BlockGeom g = block_geom(qpos[qi], L, c);
+  int32_t* o = out + pair * (int64_t)W;
+  int count;
+  if (g.n_blocks == 0) {
+    count = 0;
+    for (int j = threadIdx.x; j < W; j += kPickThreads) o[j] = -1;
+  } else if (!g.scoring) {
+    // the forced blocks are the whole selection: [0, a) then [max(n-local,0), n)
+    const int64_t n = g.n_blocks;
+    const int64_t a = c.init_blocks < n ? c.init_blocks : n;
+    int64_t z = n - c.local_blocks;
+    z = z < 0 ? 0 : z;
+    const int64_t zs = z > a ? z : a;          // skip the overlap
+    count = (int)(a + (n - zs));
+    for (int j = threadIdx.x; j < W; j += kPickThreads) {
+      int64_t v = -1;
+      if (j < a) v = j;
+      else if (j < count) v = zs + (j - a);
+      o[j] = (int32_t)v;
+    }
+  } else {
+    BlockKeyRow row{bkey + pair * nbm, g.n_blocks, c};
+    count = block_topk<kPickThreads>(sh, sel, row, (int)g.budget, o, nullptr, true);
+    for (int j = (int)g.budget + threadIdx.x; j < W; j += kPickThreads) o[j] = -1;
+  }
+  if (out_count && threadIdx.x == 0) out_count[pair] = count;
+}
+
+size_t block_select_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c) {
+  if (c.block_size <= 0) return 0;
+  int64_t nbm = (L + c.block_size - 1) / c.block_size;
+  return (size_t)(Q * n_kv) * (size_t)nbm * sizeof(uint32_t);
+}
+
+cudaError_t launch_block_select(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv, int D,
+                                int64_t L, const block_sparse_config& c, int32_t* out, int out_width,
+                                int32_t* out_count, void* ws, cudaStream_t st) {
+  const int64_t pairs = Q * n_kv;
+  if (pairs <= 0) return cudaSuccess;
+  const int64_t nbm = c.block_size > 0 ? (L + c.block_size - 1) / c.block_size : 0;
+  uint32_t* bkey = (uint32_t*)ws;
+  cudaError_t e;
+  if (nbm > 0) {
+    dim3 grid((unsigned)((pairs + kBsThreads - 1) / kBsThreads), (unsigned)(nbm < 65535 ? nbm : 65535));
+    if (D == 128) {
+      size_t smem = (size_t)kBsChunk * 128 * sizeof(float);
+      e = cudaFuncSetAttribute(block_score_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      block_score_kernel<128><<<grid, kBsThreads, smem, st>>>(q, k, pos, Q, n_kv, D, L, c, nbm, bkey);
+    } else {
+      int chunk = D > 0 ? (16384 / D < kBsChunk ? 16384 / D : kBsChunk) : 1;
+      chunk = chunk < 1 ? 1 : chunk;
+      size_t smem = (size_t)chunk * D * sizeof(float);
+      e = cudaFuncSetAttribute(block_score_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      block_score_kernel<0><<<grid, kBsThreads, smem, st>>>(q, k, pos, Q, n_kv, D, L, c, nbm, bkey);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  int Kmax = c.top_blocks > c.init_blocks + c.local_blocks ? c.top_blocks : c.init_blocks + c.local_blocks;
+  int P = 1;
+  while (P < Kmax) P <<= 1;
+  size_t smem = (size_t)P * sizeof(uint64_t);
+  e = cudaFuncSetAttribute(block_pick_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(IDX_MAX_K * sizeof(uint64_t)));
+  if (e != cudaSuccess) return e;
+  block_pick_kernel<<<(unsigned)pairs, kPickThreads, smem, st>>>(pos, Q, n_kv, L, c, nbm, bkey, out, out_width,
+                                                                out_count);
+  return cudaGetLastError();
+}
+
+}  // namespace idx

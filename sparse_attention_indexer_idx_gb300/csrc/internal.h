@@ -1,0 +1,67 @@
+// Library-internal declarations shared by the .cu files of libidx.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/idx.h"
+#include "common.cuh"
+
+namespace idx {
+
+constexpr int kTile = 128;  // keys per tensor-core tile (one TMEM lane each)
+
+// Number of streaming multiprocessors of the current device (cached).
+int sm_count();
+
+// Visible extent of row m: false (and len 0) when the extent does not fit the
+// key buffer or exceeds max_key_len.
+__device__ __forceinline__ bool row_extent(const idx_problem& p, int64_t m, int64_t* off, int* len) {
+  int32_t L = p.key_len[m];
+  int64_t o = p.key_off ? p.key_off[m] : 0;
+  bool ok = L >= 0 && L <= p.max_key_len && o >= 0 && o + (int64_t)L <= p.n_keys;
+  *off = ok ? o : 0;
+  *len = ok ? L : 0;
+  return ok;
+}
+
+// ---- launchers (host) -------------------------------------------------------
+cudaError_t launch_witness_merge(int32_t* ids, int64_t rows, int topk, const int32_t* ctx, int keep, int S, int B,
+                                 cudaStream_t st);
+cudaError_t launch_witness_indices(const int32_t* ids, int64_t rows, int topk, const int32_t* ctx, int S,
+                                   int32_t* out, cudaStream_t st);
+
+cudaError_t launch_topk_dense(const float* scores, int64_t ld, const int32_t* lens, const idx_problem* p_or_null,
+                              int64_t M, int max_len, int K, int32_t* out_ids, float* out_scores, cudaStream_t st);
+
+// Scores of every visible key (the kernel family depends only on dtype/H/D).
+cudaError_t launch_score(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st);
+bool score_uses_tensor_cores(const idx_problem& p);
+cudaError_t launch_score_simt(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st);
+cudaError_t launch_score_tc(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st);
+
+size_t block_select_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c);
+cudaError_t launch_block_select(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv, int D,
+                                int64_t L, const block_sparse_config& c, int32_t* out, int out_width,
+                                int32_t* out_count, void* ws, cudaStream_t st);
+
+size_t dosa_ws(const idx_problem& p, int K, const dosa_params& dp, int seed_ld);
+cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, const int32_t* seed_ids, int seed_ld,
+                        int32_t* out_ids, float* out_scores, int32_t* row_status, dosa_stats* stats, void* ws,
+                        size_t ws_bytes, cudaStream_t st);
+
+// ---- workspace carving -------------------------------------------------------
+struct WsCarver {
+  char* base;
+  size_t used = 0;
+  explicit WsCarver(void* b) : base((char*)b) {}
+  template <class T>
+  T* take(size_t count) {
+    size_t off = (used + 255) & ~size_t(255);
+    used = off + count * sizeof(T);
+    return base ? (T*)(base + off) : nullptr;
+  }
+};
+
+}  // namespace idx

@@ -289,3 +289,16 @@ def witness_rows(seed: int, rows: int, topk: int, L_min: int = 1, L_max: int = 4
         oob = rng.random(topk) < oob_frac
         out[r, oob] = L + rng.integers(0, 1000, int(oob.sum()))
     return out, ctx
+
+
+def score_rows(seed: int, M: int, L_max: int, ties: bool = False, ragged: bool = True):
+    """Random float32 score rows [M, L_max] with row lengths in [0, L_max];
+    `ties` draws small integers (many exact ties, signed zeros)."""
+    rng = np.random.default_rng(seed)
+    if ties:
+        s = rng.integers(-4, 5, (M, L_max)).astype(np.float32)
+        s[rng.random((M, L_max)) < 0.1] = np.float32(-0.0)
+    else:
+        s = rng.standard_normal((M, L_max), dtype=np.float32)
+    lens = rng.integers(0, L_max + 1, M).astype(np.int32) if ragged else np.full(M, L_max, dtype=np.int32)
+    return s, lens

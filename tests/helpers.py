@@ -1,0 +1,57 @@
+"""Comparison helpers shared by the GPU parity tests (test-side only)."""
+import re
+
+import numpy as np
+
+# Tolerance of a score, relative to a(k) = sum_h |w_h| ReLU(q_h.k): 1e-3 for
+# fp32 / bf16 inputs, 2e-2 for FP8 keys.
+EPS = {"f32": 1e-3, "bf16": 1e-3, "fp8": 2e-2}
+
+
+def header_functions(path):
+    """Names of the functions declared in a C header."""
+    src = open(path).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+([A-Za-z_][A-Za-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "return", "sizeof")))
+
+
+def check_scores(s_gpu, s_ref, a_ref, eps):
+    s_gpu = np.asarray(s_gpu, dtype=np.float64)
+    err = np.abs(s_gpu - s_ref)
+    tol = eps * (a_ref + 1e-30)
+    bad = np.nonzero(err > tol)[0]
+    assert bad.size == 0, f"{bad.size} scores out of tolerance, e.g. id {bad[0]}: gpu {s_gpu[bad[0]]} ref {s_ref[bad[0]]} a {a_ref[bad[0]]}"
+
+
+def check_topk_row(g_ids, g_sc, s_ref, a_ref, K, eps):
+    """GPU top-K row vs the oracle's full score row (ids 0..L-1).
+
+    * ids distinct, in range, -1 padding exactly when L < K;
+    * reported scores within tolerance of the oracle score of that id;
+    * order: non-increasing score, ties by ascending id;
+    * the id set equals the oracle's except for keys whose oracle score lies
+      within tolerance of the oracle's K-th score.
+    """
+    L = s_ref.shape[0]
+    n = min(L, K)
+    g_ids = np.asarray(g_ids)
+    assert (g_ids[n:] == -1).all(), "padding"
+    real = g_ids[:n]
+    assert (real >= 0).all() and (real < L).all(), "id range"
+    assert len(set(real.tolist())) == n, "distinct"
+    if g_sc is not None:
+        g_sc = np.asarray(g_sc, dtype=np.float64)
+        assert np.isneginf(g_sc[n:]).all()
+        check_scores(g_sc[:n], s_ref[real], a_ref[real], eps)
+        for j in range(n - 1):
+            assert g_sc[j] > g_sc[j + 1] or (g_sc[j] == g_sc[j + 1] and real[j] < real[j + 1]), f"order at {j}"
+    if n == 0:
+        return
+    order = np.lexsort((np.arange(L), -s_ref))
+    o_ids = order[:n]
+    kth = o_ids[-1]
+    s_k, a_k = s_ref[kth], a_ref[kth]
+    diff = set(real.tolist()) ^ set(o_ids.tolist())
+    for x in diff:
+        assert abs(s_ref[x] - s_k) <= eps * (a_ref[x] + a_k) + 1e-30, f"id {x} differs and is not near the K-th score"

@@ -1,0 +1,109 @@
+"""GPU parity of the integer / selection kernels against the oracle, through
+the C ABI: witness merge and witness table (bit-exact), top-K of given score
+rows (bit-exact ids and scores)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import dsa as odsa
+from oracle import witness as ow
+from sparse_attention_indexer_idx_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "witness_examples.json")))
+
+
+@pytest.fixture(scope="module")
+def B():
+    from sparse_attention_indexer_idx_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _dev(a, dtype=torch.int32):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda", dtype)
+
+
+def test_printed_examples(B):
+    c = GOLD["merge"][0]
+    ids = _dev(np.array([c["learned"]], dtype=np.int32))
+    B.witness_merge(ids, _dev(np.array([c["L"]])), c["keep"], c["S"], c["max_replacements"])
+    assert ids.cpu().numpy()[0].tolist() == c["expected"]
+    c = GOLD["serving"][0]
+    ids = _dev(np.array([c["learned"]], dtype=np.int32))
+    topk = len(c["learned"])
+    B.witness_merge(ids, _dev(np.array([c["L"]])), topk - c["S"], c["S"], c["S"])
+    assert ids.cpu().numpy()[0].tolist() == c["expected"]
+    c = GOLD["witness_indices"][0]
+    out = torch.empty((1, c["S"]), dtype=torch.int32, device="cuda")
+    B.witness_indices(_dev(np.array([c["learned"]])), _dev(np.array([c["L"]])), c["S"], out)
+    assert out.cpu().numpy()[0].tolist() == c["expected"]
+    assert B.device_error() == 0
+
+
+@pytest.mark.parametrize("seed,rows,topk,S,keep_mode", [
+    (1, 64, 2048, 16, "serving"), (2, 128, 2048, 32, "serving"), (3, 37, 100, 64, "serving"),
+    (4, 50, 33, 7, "random"), (5, 300, 8, 4, "random"), (6, 20, 64, 64, "random"), (7, 9, 5, 40, "serving")])
+def test_merge_random_rows(B, seed, rows, topk, S, keep_mode):
+    learned, ctx = wl.witness_rows(seed, rows, topk, L_min=-2, L_max=5000)
+    rng = np.random.default_rng(seed + 100)
+    if keep_mode == "serving":
+        keep, maxr = max(topk - S, 0), S
+    else:
+        keep, maxr = int(rng.integers(0, topk + 1)), int(rng.integers(0, S + 3))
+    ids = _dev(learned)
+    B.witness_merge(ids, _dev(ctx), keep, S, maxr)
+    ref = ow.apply_topology_witnesses(learned, topk, ctx, keep, S, maxr)
+    assert np.array_equal(ids.cpu().numpy(), ref)
+    tab = torch.empty((rows, S), dtype=torch.int32, device="cuda")
+    B.witness_indices(_dev(learned), _dev(ctx), S, tab)
+    assert np.array_equal(tab.cpu().numpy(), ow.topology_witness_indices(learned, topk, ctx, S))
+    assert B.device_error() == 0
+
+
+def test_decode_shaped_rows_with_padding(B):
+    """64 rows x 2048 with 5% of slots set to -1, S = 16, serving form."""
+    wp = wl.decode_bf16(M=64, H=2, D=8, L=32768, K=2048)
+    rng = np.random.default_rng(9)
+    learned = np.stack([rng.choice(32768, 2048, replace=False) for _ in range(64)]).astype(np.int32)
+    learned[wp.extras["pad_mask"]] = -1
+    ctx = np.full(64, 32768, dtype=np.int32)
+    ids = _dev(learned)
+    B.witness_merge(ids, _dev(ctx), 2048 - 16, 16, 16)
+    ref = ow.apply_topology_witnesses(learned, 2048, ctx, 2048 - 16, 16, 16)
+    assert np.array_equal(ids.cpu().numpy(), ref)
+
+
+def test_refused_calls_leave_the_buffer(B):
+    learned = np.array([[0, 5, 9, -1]], dtype=np.int32)
+    ids = _dev(learned)
+    for args, name in [((_dev(np.array([16])), 2, 65, 2), "SEGMENTS_OUT_OF_RANGE"),
+                       ((_dev(np.array([16])), 5, 4, 2), "KEEP_OUT_OF_RANGE"),
+                       ((_dev(np.zeros(0)), 2, 4, 2), "ROWS_MISMATCH")]:
+        with pytest.raises(B.IdxError) as e:
+            B.witness_merge(ids, *args)
+        assert e.value.name == name
+    assert ids.cpu().numpy().tolist() == learned.tolist()
+
+
+@pytest.mark.parametrize("seed,M,L,K,ties", [
+    (1, 16, 5000, 32, False), (2, 16, 5000, 2048, False), (3, 8, 40000, 2048, False), (4, 33, 3000, 100, True),
+    (5, 7, 9000, 4096, True), (6, 12, 300, 1, True), (7, 5, 131072, 2048, False), (8, 40, 64, 64, True)])
+def test_topk_scores_bit_exact(B, seed, M, L, K, ties):
+    s, lens = wl.score_rows(seed, M, L, ties=ties)
+    lens[0] = 0
+    lens[-1] = L
+    ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    sc = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    B.idx_topk_scores(_dev(s, torch.float32), _dev(lens), L, K, ids, sc)
+    g_ids, g_sc = ids.cpu().numpy(), sc.cpu().numpy()
+    for m in range(M):
+        o_ids, o_sc = odsa.topk(s[m, :lens[m]].astype(np.float64), K)
+        assert g_ids[m].tolist() == o_ids.tolist(), m
+        o32 = o_sc.astype(np.float32) + np.float32(0.0)    # the kernel reports -0.0 as +0.0
+        assert np.array_equal(g_sc[m].view(np.uint32), o32.view(np.uint32)), m
+    assert B.device_error() == 0
