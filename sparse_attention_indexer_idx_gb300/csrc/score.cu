@@ -5,7 +5,7 @@
 
 namespace idx {
 
-constexpr bool kTensorScoreEnabled = false;
+constexpr bool kTensorScoreEnabled = true;
 
 bool score_uses_tensor_cores(const idx_problem& p) {
   const bool dt = p.q_dtype == IDX_BF16 && (p.k_dtype == IDX_BF16 || p.k_dtype == IDX_FP8_E4M3);

@@ -1,0 +1,529 @@
+// Indexer score on the 5th-generation tensor cores (tcgen05, sm_103a):
+// s(k) = sum_h w_h ReLU(q_h . k) ("DoSA：用安全上界减少 Indexer 的完整打分",
+// section 3), for bf16 queries with bf16 keys or FP8 e4m3 keys (+ per-token
+// scale), D = 128.
+//
+// Mapping.  One MMA tile is 128 keys (the M axis: key i of the tile lives in
+// TMEM lane i) times N = NQ*H columns (NQ queries x H heads, all K-major), with
+// the full D = 128 as 8 MMAs of K = 16.  So each epilogue thread owns one key
+// and reduces its own TMEM columns, head by head, with no shuffles:
+//   s = fma(w_{H-1}, max(x_{H-1}, 0), ... fma(w_0, max(x_0, 0), 0)).
+// A (query, key) score therefore has the same bits wherever it is computed
+// (dense tile, gathered seed or survivor tile): same instruction shape, same
+// K order, same epilogue chain.
+//
+// Work units are (query group g, key tile t).  Shared keys (causal prefill):
+// a group is NQ = 256/H consecutive rows over one key sequence, N = 256.
+// Per-row keys (decode): a group is one row, N = H.  The units are split into
+// one contiguous range per CTA (persistent, one CTA per SM), balanced by the
+// exact tile count of every group, which a prologue warp scans from key_len.
+//
+// Warp roles:  warp 0  TMA producer (key tiles, query tiles)
+//              warp 1  TMEM allocation + MMA issue (one thread)
+//              warps 2-5  epilogue: tcgen05.ld -> ReLU.w chain -> global
+//              warps 6-9  (FP8 only) e4m3 -> f16 conversion of key tiles into
+//                         the swizzled MMA layout, bf16 -> f16 of query tiles
+// Rings: A (MMA-ready key tiles), RAW (FP8 tiles as loaded), B (query tiles),
+// ACC (TMEM accumulators).  Every wait is bounded (see common.cuh); on a
+// timeout all roles stop, the producer and the MMA thread drain what they
+// issued, and TMEM is released before exit.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace idx {
+
+struct TcArgs {
+  idx_problem p;
+  float* scores;
+  int64_t ld;
+  int64_t G;                  // groups
+};
+
+__host__ __device__ constexpr int tc_pow2_cols(int c) {
+  return c <= 32 ? 32 : (c <= 64 ? 64 : (c <= 128 ? 128 : (c <= 256 ? 256 : 512)));
+}
+
+template <int KDT_, int H_, int NQ_>
+struct TcCfg {
+  static constexpr int KDT = KDT_;
+  static constexpr int H = H_;
+  static constexpr int NQ = NQ_;
+  static constexpr bool FP8 = (KDT == IDX_FP8_E4M3);
+  static constexpr int N = NQ * H;
+  static constexpr int A_BYTES = 128 * 128 * 2;
+  static constexpr int B_BYTES = N * 128 * 2;
+  static constexpr int RAW_BYTES = 128 * 128;
+  static constexpr int SB = (NQ > 1) ? 1 : 2;
+  static constexpr int SA = FP8 ? 3 : ((B_BYTES * SB <= 32768) ? 5 : 4);
+  static constexpr int SRAW = FP8 ? ((B_BYTES * SB <= 32768) ? 4 : 3) : 0;
+  static constexpr int SRAW_MOD = SRAW > 0 ? SRAW : 1;   // ring index arithmetic
+  static constexpr int SACC = (N >= 256) ? 2 : 4;
+  static constexpr int TMEM_COLS = tc_pow2_cols(SACC * N);
+  static constexpr int NTHREADS = FP8 ? 320 : 192;
+  // shared memory layout (offsets from a 1024-aligned base)
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + SA * A_BYTES;
+  static constexpr int OFF_RAW = OFF_B + SB * B_BYTES;
+  // per epilogue warp (4 private copies, so the warps never wait on each other)
+  static constexpr int OFF_W = OFF_RAW + SRAW * RAW_BYTES;
+  static constexpr int OFF_BASE = OFF_W + 4 * N * 4;
+  static constexpr int OFF_LEN = OFF_BASE + 4 * NQ * 8;
+  static constexpr int OFF_BAR = ((OFF_LEN + 4 * NQ * 4) + 7) & ~7;
+  static constexpr int NBARS = 2 * SA + 3 * SB + 2 * SRAW + 2 * SACC + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
+  static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+struct TcSched {
+  int64_t g0;       // first group
+  int64_t t0;       // first tile in it
+  int64_t count;    // units in this CTA's range
+};
+
+// ------------------------------------------------------------ group helpers --
+template <class C>
+__device__ __forceinline__ int64_t tc_group_tiles(const TcArgs& A, int64_t g, bool report = false) {
+  int mx = 0;
+#pragma unroll 1
+  for (int q = 0; q < C::NQ; ++q) {
+    int64_t m = g * C::NQ + q;
+    if (m >= A.p.M) break;
+    int64_t off;
+    int len;
+    if (!row_extent(A.p, m, &off, &len) && report) atomicOr(&g_device_error, DEVERR_BAD_ROW);
+    mx = len > mx ? len : mx;
+  }
+  return (mx + 127) / 128;
+}
+
+__device__ __forceinline__ int64_t warp_incl_scan(int64_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int64_t u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
+// One warp: total units, this CTA's [start, end), and its first (g, t).
+template <class C>
+__device__ void tc_schedule(const TcArgs& A, TcSched* out) {
+  const int lane = threadIdx.x & 31;
+  int64_t total = 0;
+  for (int64_t b = 0; b < A.G; b += 32) {
+    int64_t g = b + lane;
+    int64_t t = g < A.G ? tc_group_tiles<C>(A, g, blockIdx.x == 0) : 0;
+    total += __shfl_sync(0xffffffffu, warp_incl_scan(t), 31);
+  }
+  const int64_t start = total * (int64_t)blockIdx.x / gridDim.x;
+  const int64_t end = total * (int64_t)(blockIdx.x + 1) / gridDim.x;
+  int64_t g0 = 0, t0 = 0;
+  if (end > start) {
+    int64_t run = 0;
+    for (int64_t b = 0; b < A.G; b += 32) {
+      int64_t g = b + lane;
+      int64_t t = g < A.G ? tc_group_tiles<C>(A, g) : 0;
+      int64_t incl = warp_incl_scan(t);
+      int64_t chunk = __shfl_sync(0xffffffffu, incl, 31);
+      if (run + chunk > start) {
+        unsigned hit = __ballot_sync(0xffffffffu, run + incl > start);
+        int first = __ffs(hit) - 1;
+        int64_t incl_f = __shfl_sync(0xffffffffu, incl, first);
+        int64_t t_f = __shfl_sync(0xffffffffu, t, first);
+        g0 = b + first;
+        t0 = start - (run + incl_f - t_f);
+        break;
+      }
+      run += chunk;
+    }
+  }
+  if (lane == 0) {
+    out->g0 = g0;
+    out->t0 = t0;
+    out->count = end - start;
+  }
+}
+
+// Walks this CTA's units in order.
+template <class C>
+struct TcUnits {
+  const TcArgs* A;
+  int64_t g, t, left, tiles_g;
+  __device__ void init(const TcArgs& a, const TcSched& s) {
+    A = &a;
+    g = s.g0;
+    t = s.t0;
+    left = s.count;
+    tiles_g = left > 0 ? tc_group_tiles<C>(a, g) : 0;
+  }
+  __device__ bool valid() const { return left > 0; }
+  __device__ void advance() {
+    --left;
+    if (left <= 0) return;
+    ++t;
+    while (t >= tiles_g) {
+      ++g;
+      t = 0;
+      tiles_g = tc_group_tiles<C>(*A, g);
+    }
+  }
+};
+
+// ------------------------------------------------------------- the kernel ---
+template <class C>
+__global__ void __launch_bounds__(C::NTHREADS, 1)
+    score_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                    const TcArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint8_t* sA = smem + C::OFF_A;
+  uint8_t* sB = smem + C::OFF_B;
+  uint8_t* sRaw = smem + C::OFF_RAW;
+  float* sW_all = reinterpret_cast<float*>(smem + C::OFF_W);
+  int32_t* sLen_all = reinterpret_cast<int32_t*>(smem + C::OFF_LEN);
+  int64_t* sBase_all = reinterpret_cast<int64_t*>(smem + C::OFF_BASE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* a_full = bars;
+  uint64_t* a_empty = a_full + C::SA;
+  uint64_t* b_full = a_empty + C::SA;
+  uint64_t* b_empty = b_full + C::SB;
+  uint64_t* b_loaded = b_empty + C::SB;
+  uint64_t* raw_full = b_loaded + C::SB;
+  uint64_t* raw_empty = raw_full + C::SRAW;
+  uint64_t* acc_full = raw_empty + C::SRAW;
+  uint64_t* acc_empty = acc_full + C::SACC;
+  uint64_t* drain_bar = acc_empty + C::SACC;
+  uint8_t* misc = smem + C::OFF_MISC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  TcSched* sched = reinterpret_cast<TcSched*>(misc + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr int kConvThreads = 128;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::SA; ++i) {
+      mbar_init(&a_full[i], C::FP8 ? kConvThreads : 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < C::SB; ++i) {
+      mbar_init(&b_full[i], C::FP8 ? kConvThreads : 1);
+      mbar_init(&b_empty[i], 1);
+      mbar_init(&b_loaded[i], 1);
+    }
+    for (int i = 0; i < C::SRAW; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], kConvThreads);
+    }
+    for (int i = 0; i < C::SACC; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_q);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == 2) tc_schedule<C>(args, sched);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const TcSched s = *sched;
+  volatile int no_abort_storage = 0;
+  volatile int* no_abort = &no_abort_storage;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      TcUnits<C> u;
+      u.init(args, s);
+      int64_t cur_g = -1;
+      uint32_t na = 0, nb = 0, nr = 0;
+      while (u.valid()) {
+        if (u.g != cur_g) {
+          cur_g = u.g;
+          const int bs = nb % C::SB;
+          if (!mbar_wait(&b_empty[bs], ((nb / C::SB) & 1) ^ 1, abort_flag)) break;
+          uint64_t* bar = C::FP8 ? &b_loaded[bs] : &b_full[bs];
+          mbar_arrive_expect_tx(bar, C::B_BYTES);
+          const int32_t y = (int32_t)(cur_g * C::N);
+          tma_load_2d(sB + bs * C::B_BYTES, &tmap_q, bar, 0, y);
+          tma_load_2d(sB + bs * C::B_BYTES + C::B_BYTES / 2, &tmap_q, bar, 64, y);
+          ++nb;
+        }
+        {
+          int64_t base = 0;
+          if (args.p.key_off) {
+            int64_t off;
+            int len;
+            row_extent(args.p, u.g, &off, &len);
+            base = off;
+          }
+          const int32_t y = (int32_t)(base + u.t * 128);
+          if (C::FP8) {
+            const int rs = nr % C::SRAW_MOD;
+            if (!mbar_wait(&raw_empty[rs], ((nr / C::SRAW_MOD) & 1) ^ 1, abort_flag)) break;
+            mbar_arrive_expect_tx(&raw_full[rs], C::RAW_BYTES);
+            tma_load_2d(sRaw + rs * C::RAW_BYTES, &tmap_k, &raw_full[rs], 0, y);
+            ++nr;
+          } else {
+            const int as = na % C::SA;
+            if (!mbar_wait(&a_empty[as], ((na / C::SA) & 1) ^ 1, abort_flag)) break;
+            mbar_arrive_expect_tx(&a_full[as], C::A_BYTES);
+            tma_load_2d(sA + as * C::A_BYTES, &tmap_k, &a_full[as], 0, y);
+            tma_load_2d(sA + as * C::A_BYTES + C::A_BYTES / 2, &tmap_k, &a_full[as], 64, y);
+            ++na;
+          }
+        }
+        u.advance();
+      }
+      // drain: the last phase issued on every ring slot has landed
+      for (uint32_t i = 0; i < (uint32_t)C::SB && i < nb; ++i) {
+        uint32_t j = nb - 1 - i;
+        mbar_wait(C::FP8 ? &b_loaded[j % C::SB] : &b_full[j % C::SB], (j / C::SB) & 1, no_abort);
+      }
+      if (!C::FP8) {
+        for (uint32_t i = 0; i < (uint32_t)C::SA && i < na; ++i) {
+          uint32_t j = na - 1 - i;
+          mbar_wait(&a_full[j % C::SA], (j / C::SA) & 1, no_abort);
+        }
+      }
+      if constexpr (C::FP8) {
+        for (uint32_t i = 0; i < (uint32_t)C::SRAW_MOD && i < nr; ++i) {
+          uint32_t j = nr - 1 - i;
+          mbar_wait(&raw_full[j % C::SRAW_MOD], (j / C::SRAW_MOD) & 1, no_abort);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(128, C::N, C::FP8 ? 0u : 1u);
+      TcUnits<C> u;
+      u.init(args, s);
+      int64_t cur_g = -1;
+      int cur_bs = 0;
+      uint32_t na = 0, nb = 0, nacc = 0;
+      bool issued = false;
+      while (u.valid()) {
+        if (u.g != cur_g) {
+          cur_g = u.g;
+          cur_bs = nb % C::SB;
+          if (!mbar_wait(&b_full[cur_bs], (nb / C::SB) & 1, abort_flag)) break;
+          ++nb;
+        }
+        const int as = na % C::SA;
+        if (!mbar_wait(&a_full[as], (na / C::SA) & 1, abort_flag)) break;
+        const int acc = nacc % C::SACC;
+        if (!mbar_wait(&acc_empty[acc], ((nacc / C::SACC) & 1) ^ 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + as * C::A_BYTES);
+        const uint32_t b0 = smem_u32(sB + cur_bs * C::B_BYTES);
+        const uint32_t d = tmem_base + (uint32_t)(acc * C::N);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t ao = a0 + (k >> 2) * (C::A_BYTES / 2) + (k & 3) * 32;
+          const uint32_t bo = b0 + (k >> 2) * (C::B_BYTES / 2) + (k & 3) * 32;
+          tc_mma_f16(d, smem_desc_sw128(ao), smem_desc_sw128(bo), idesc, k > 0 ? 1u : 0u);
+        }
+        issued = true;
+        tc_commit(&a_empty[as]);
+        tc_commit(&acc_full[acc]);
+        ++na;
+        ++nacc;
+        const int64_t g_this = u.g;
+        u.advance();
+        if (!u.valid() || u.g != g_this) tc_commit(&b_empty[cur_bs]);
+      }
+      if (issued) {
+        tc_commit(drain_bar);
+        mbar_wait(drain_bar, 0, no_abort);
+      }
+    }
+  } else if (warp >= 2 && warp < 6) {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;              // TMEM lanes this warp may read
+    const int row_in_tile = quarter * 32 + lane;
+    float* sW = sW_all + quarter * C::N;
+    int32_t* sLen = sLen_all + quarter * C::NQ;
+    int64_t* sBase = sBase_all + quarter * C::NQ;
+    TcUnits<C> u;
+    u.init(args, s);
+    int64_t cur_g = -1;
+    uint32_t nacc = 0;
+    while (u.valid()) {
+      if (u.g != cur_g) {
+        cur_g = u.g;
+        __syncwarp();
+        for (int i = lane; i < C::N; i += 32) {
+          const int64_t m = cur_g * C::NQ + i / C::H;
+          sW[i] = (m < args.p.M) ? args.p.w[m * C::H + (i % C::H)] : 0.0f;
+        }
+        if (lane < C::NQ) {
+          const int64_t m = cur_g * C::NQ + lane;
+          int64_t off = 0;
+          int len = 0;
+          if (m < args.p.M) row_extent(args.p, m, &off, &len);
+          sLen[lane] = len;
+          sBase[lane] = off;
+        }
+        __syncwarp();
+      }
+      const int acc = nacc % C::SACC;
+      const bool got = mbar_wait(&acc_full[acc], (nacc / C::SACC) & 1, abort_flag);
+      __syncwarp();                           // tcgen05.ld below is warp-collective
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const int key = (int)(u.t * 128) + row_in_tile;
+#pragma unroll 1
+      for (int qi = 0; qi < C::NQ; ++qi) {
+        const int64_t m = cur_g * C::NQ + qi;
+        if (m >= args.p.M) break;
+        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::N + qi * C::H);
+        const float* wq = sW + qi * C::H;
+        float sc = 0.0f;
+#pragma unroll
+        for (int c = 0; c < C::H; c += 32) {
+          uint32_t v[32];
+          if (C::H >= 32) {
+            tmem_ld_32x32b_x32(tcol + c, v);
+          } else {
+            tmem_ld_32x32b_x16(tcol + c, v);
+          }
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < (C::H < 32 ? C::H : 32); ++j)
+            sc = __fmaf_rn(wq[c + j], fmaxf(__uint_as_float(v[j]), 0.0f), sc);
+        }
+        const int len = sLen[qi];
+        if (key < len) {
+          float outv = sc;
+          if (C::FP8) outv = sc * args.p.key_scale[sBase[qi] + key];
+          args.scores[m * args.ld + key] = outv;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[acc]);
+      ++nacc;
+      u.advance();
+    }
+  } else if (C::FP8) {
+    // ------------------------------------------------------------ converters
+    const int ct = threadIdx.x - 192;          // 0..127
+    TcUnits<C> u;
+    u.init(args, s);
+    int64_t cur_g = -1;
+    uint32_t na = 0, nb = 0, nr = 0;
+    while (u.valid()) {
+      if (u.g != cur_g) {
+        cur_g = u.g;
+        const int bs = nb % C::SB;
+        if (!mbar_wait(&b_loaded[bs], (nb / C::SB) & 1, abort_flag)) break;
+        uint4* bp = reinterpret_cast<uint4*>(sB + bs * C::B_BYTES);
+        for (int i = ct; i < C::B_BYTES / 16; i += kConvThreads) {
+          uint4 v = bp[i];
+          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16);
+            const float hi = __uint_as_float(w[j] & 0xffff0000u);
+            __half2 h2 = __floats2half2_rn(lo, hi);
+            w[j] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          bp[i] = v;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&b_full[bs]);
+        ++nb;
+      }
+      const int rs = nr % C::SRAW_MOD;
+      if (!mbar_wait(&raw_full[rs], (nr / C::SRAW_MOD) & 1, abort_flag)) break;
+      const int as = na % C::SA;
+      if (!mbar_wait(&a_empty[as], ((na / C::SA) & 1) ^ 1, abort_flag)) break;
+      const uint8_t* src = sRaw + rs * C::RAW_BYTES;
+      uint8_t* dst = sA + as * C::A_BYTES;
+#pragma unroll 2
+      for (int it = 0; it < 8; ++it) {
+        const int item = it * kConvThreads + ct;   // (row r, 16-byte source chunk j)
+        const int r = item >> 3, j = item & 7;
+        const uint4 raw = *reinterpret_cast<const uint4*>(src + r * 128 + ((j ^ (r & 7)) << 4));
+        const uint32_t* rw = reinterpret_cast<const uint32_t*>(&raw);
+        uint32_t o[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t lo, hi;
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((unsigned short)(rw[q] & 0xffffu)));
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((unsigned short)(rw[q] >> 16)));
+          o[2 * q] = lo;
+          o[2 * q + 1] = hi;
+        }
+        // elements 16j..16j+15 of row r -> half j/4, 16-byte chunks 2j%8 and 2j%8+1
+        uint8_t* hbase = dst + (j >> 2) * (C::A_BYTES / 2) + r * 128;
+        const int c0 = (2 * j) & 7;
+        *reinterpret_cast<uint4*>(hbase + ((c0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(hbase + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&raw_empty[rs]);
+      mbar_arrive(&a_full[as]);
+      ++nr;
+      ++na;
+      u.advance();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace idx
+
+namespace idx {
+
+// 2-D tensor map over a row-major [rows, inner] matrix, 128-byte swizzle.
+bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
+
+template <class C>
+cudaError_t launch_tc(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st) {
+  if (p.M <= 0 || p.n_keys <= 0 || p.max_key_len <= 0) return cudaSuccess;
+  if (p.n_keys >= ((int64_t)1 << 31) || p.M * p.H >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+  CUtensorMap tk, tq;
+  bool ok;
+  if (C::FP8)
+    ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.keys, 128, (uint64_t)p.n_keys, 128, 128, 128);
+  else
+    ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.keys, 128, (uint64_t)p.n_keys, 256, 64, 128);
+  ok = ok && make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, 128, (uint64_t)(p.M * p.H), 256, 64, C::N);
+  if (!ok) return cudaErrorInvalidValue;
+  TcArgs a;
+  a.p = p;
+  a.scores = scores;
+  a.ld = ld;
+  a.G = (p.M + C::NQ - 1) / C::NQ;
+  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  score_tc_kernel<C><<<sm_count(), C::NTHREADS, C::SMEM_BYTES, st>>>(tk, tq, a);
+  return cudaGetLastError();
+}
+
+}  // namespace idx
