@@ -1,0 +1,493 @@
+"""Benchmark of the indexer hot path on GB300.
+
+Default workload (the decode indexer batch): 64 query rows, each with its own
+32768 bf16 index keys, H=32 heads, D=128, exact top-K=2048, then the
+segment-witness merge (S=16, keep=K-S, max_replacements=S) after 5% of the
+learned slots are set to -1 padding.  One step = score every visible key
+(idx_score) -> exact top-K (idx_topk_scores) -> padding -> witness_merge.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload decode|prefill|prefill_dosa|ragged_fp8|block_select|tiny]
+
+Prints ONE JSON line (rank 0).  `value` is queries*keys scored per second over
+the whole job (inputs resident in HBM); `e2e` is the same metric through the
+C ABI with the inputs copied from pinned host memory and the top-K ids copied
+back inside the timed region.  `roofline` is for the dominant kernel, timed
+with CUDA events on its own stream inside the timed region.  `cpu_baseline`
+times the CPU oracle on a bounded sample of the same workload on this host.
+--impl reference times the oracle alone (the reference arm of this build).
+Multi-GPU (torchrun): every rank runs its own independent batch (weak
+scaling, no data-path collective); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle leg runs single-threaded so its core count is exact
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_attention_indexer_idx_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "indexer queries*keys scored/sec"
+UNIT = "pairs/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        hi = max(sm)
+        under = [x for x in sm if x >= 0.5 * hi] or sm
+        return {"sm_mhz": statistics.median(under), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- workloads --
+
+def make_workload(name: str, rank: int):
+    seed_shift = 1000 * rank
+    if name == "decode":
+        return wl.decode_bf16(seed=2 + seed_shift)
+    if name in ("prefill", "prefill_dosa"):
+        return wl.prefill_bf16(seed=3 + seed_shift)
+    if name == "ragged_fp8":
+        return wl.ragged_fp8(seed=5 + seed_shift)
+    if name == "tiny":
+        return wl.tiny_fp32(seed=0 + seed_shift)
+    if name == "block_select":
+        return wl.block_select(seed=4 + seed_shift)
+    raise ValueError(name)
+
+
+WORKLOAD_TEXT = {
+    "decode": "decode indexer bf16: 64 rows x 32768 own keys, H32 D128, top-2048, witness_merge S=16 (5% padding)",
+    "prefill": "causal prefill bf16: 4096 queries over 65536 shared keys, H64 D128, top-2048 (unpruned)",
+    "prefill_dosa": "causal prefill bf16 with DoSA pruning: 4096 queries, 65536 keys, H64 D128, K2048, 12288 seeds, R16",
+    "ragged_fp8": "ragged decode FP8 e4m3 keys + scale: 128 rows, L_r~U[4096,131072], H64 D128, top-2048, witness_merge S=32",
+    "tiny": "tiny fp32 indexer: 8 rows, H4 D16, L512, K32, witness_merge S=4",
+    "block_select": "MiniMax block select fp32: 1024 queries, 8 KV heads, D128, L131072, block 128, top 32, init 1, local 2",
+}
+
+
+# ---------------------------------------------------------------- our arm ----
+
+class IndexerStep:
+    """score -> top-K -> padding -> witness merge on device-resident inputs."""
+
+    def __init__(self, B, wp, dev):
+        self.B = B
+        self.wp = wp
+        self.dev = dev
+        self.p = B.problem_to_device(wp, dev)
+        self.K = wp.K
+        self.ld = self.p.max_key_len
+        self.scores = torch.empty((wp.M, self.ld), dtype=torch.float32, device=dev)
+        self.ids = torch.empty((wp.M, self.K), dtype=torch.int32, device=dev)
+        self.S = wp.extras.get("S", 0)
+        pm = wp.extras.get("pad_mask")
+        self.pad = None if pm is None else torch.from_numpy(pm).to(dev)
+        self.ctx = self.p.key_len
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        self.score_ms = []
+        self.launches = 3 if self.S else 2
+
+    def run(self, timed=False):
+        B, p = self.B, self.p
+        if timed:
+            self.ev[0].record()
+        B.idx_score(p, self.scores, self.ld)
+        if timed:
+            self.ev[1].record()
+        B.idx_topk_scores(self.scores, p.key_len, self.ld, self.K, self.ids, None, ld=self.ld)
+        if self.S:
+            if self.pad is not None:
+                self.ids.masked_fill_(self.pad, -1)
+            B.witness_merge(self.ids, self.ctx, max(self.K - self.S, 0), self.S, self.S)
+        if timed:
+            self.ev[2].record()
+
+    def collect(self):
+        self.score_ms.append(self.ev[0].elapsed_time(self.ev[1]))
+
+    def algorithmic_bytes(self):
+        """Score kernel: every visible key row once, queries, weights, one fp32 score per pair."""
+        wp = self.wp
+        kb = {"bf16": 2, "f32": 4, "fp8": 1}[wp.dtype] * wp.D
+        if wp.dtype == "fp8":
+            kb += 4
+        pairs = wp.pairs()
+        if wp.key_off is None:
+            key_bytes = int(np.max(wp.key_len)) * kb
+        else:
+            key_bytes = pairs * kb
+        qb = wp.M * wp.H * wp.D * (4 if wp.dtype == "f32" else 2) + wp.M * wp.H * 4
+        return key_bytes + qb + pairs * 4
+
+    def flops(self):
+        return 2.0 * self.wp.pairs() * self.wp.H * self.wp.D
+
+
+class DosaStep:
+    """DoSA-pruned top-K (dosa_topk) on device-resident inputs."""
+
+    def __init__(self, B, wp, dev, R, n_seed):
+        self.B = B
+        self.wp = wp
+        self.p = B.problem_to_device(wp, dev)
+        self.K = wp.K
+        self.dp = B.make_dosa_params(n_seed=n_seed, retained_heads=R)
+        self.ids = torch.empty((wp.M, self.K), dtype=torch.int32, device=dev)
+        self.sc = torch.empty((wp.M, self.K), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(B.dosa_topk_workspace_size(self.p, self.K, self.dp), dtype=torch.uint8, device=dev)
+        self.stats = torch.zeros(5, dtype=torch.int64, device=dev)
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        self.score_ms = []
+        self.launches = 0
+
+    def run(self, timed=False):
+        if timed:
+            self.ev[0].record()
+        self.B.dosa_topk(self.p, self.K, self.dp, self.ids, self.sc, self.ws, stats=self.stats)
+        if timed:
+            self.ev[1].record()
+
+    def collect(self):
+        self.score_ms.append(self.ev[0].elapsed_time(self.ev[1]))
+
+
+class BlockSelectStep:
+    def __init__(self, B, bp, dev):
+        self.B = B
+        self.bp = bp
+        self.q = torch.from_numpy(bp.index_q).to(dev)
+        self.k = torch.from_numpy(bp.index_k).to(dev)
+        self.pos = torch.from_numpy(bp.query_pos).to(dev)
+        self.cfg = B.block_sparse_config(bp.block_size, bp.top_blocks, bp.init_blocks, bp.local_blocks)
+        Q, n_kv, _ = bp.index_q.shape
+        self.out = torch.empty((Q, n_kv, max(bp.top_blocks, bp.init_blocks + bp.local_blocks)), dtype=torch.int32,
+                               device=dev)
+        self.cnt = torch.empty((Q, n_kv), dtype=torch.int32, device=dev)
+        self.ws = torch.empty(B.block_select_workspace_size(Q, n_kv, bp.index_k.shape[0], self.cfg),
+                              dtype=torch.uint8, device=dev)
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        self.score_ms = []
+        self.launches = 2
+
+    def run(self, timed=False):
+        if timed:
+            self.ev[0].record()
+        self.B.block_select(self.q, self.k, self.pos, self.cfg, self.out, self.cnt, self.ws)
+        if timed:
+            self.ev[1].record()
+
+    def collect(self):
+        self.score_ms.append(self.ev[0].elapsed_time(self.ev[1]))
+
+    def pairs(self):
+        bs = self.bp.block_size
+        L = self.bp.index_k.shape[0]
+        return int(sum(min(int(p) + 1, L) for p in self.bp.query_pos)) * self.bp.index_q.shape[1]
+
+
+def e2e_run(B, wp, dev, steps):
+    """Same step through the C ABI from pinned host buffers: H2D of the step's
+    inputs, score -> top-K -> witness merge, D2H of the top-K ids."""
+    host = {}
+    p_dev = B.problem_to_device(wp, dev)
+    tens = {"q": p_dev.q, "w": p_dev.w, "keys": p_dev.keys, "key_len": p_dev.key_len}
+    if p_dev.key_off is not None:
+        tens["key_off"] = p_dev.key_off
+    if p_dev.key_scale is not None:
+        tens["key_scale"] = p_dev.key_scale
+    for k, t in tens.items():
+        host[k] = t.cpu().pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    ids = torch.empty((wp.M, wp.K), dtype=torch.int32, device=dev)
+    ids_host = torch.empty((wp.M, wp.K), dtype=torch.int32).pin_memory()
+    d2h = ids_host.numel() * 4
+    ws = torch.empty(B.idx_topk_workspace_size(p_dev, wp.K), dtype=torch.uint8, device=dev)
+    S = wp.extras.get("S", 0)
+
+    def one():
+        for k, t in tens.items():
+            t.copy_(host[k], non_blocking=True)
+        B.idx_topk(p_dev, wp.K, ids, None, ws)
+        if S:
+            B.witness_merge(ids, p_dev.key_len, max(wp.K - S, 0), S, S)
+        ids_host.copy_(ids, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+# ------------------------------------------------------------- CPU baseline --
+
+def cpu_baseline(wl_name, wp, budget_s=12.0):
+    """The oracle as it stands, single-threaded, on a bounded sample of rows."""
+    from oracle import dsa as odsa
+    from oracle import witness as ow
+    if wl_name == "block_select":
+        from oracle import block_select as obs
+        bp = wp
+        t0 = time.perf_counter()
+        done_pairs, done_q = 0, 0
+        for i in range(bp.index_q.shape[0] - 1, -1, -37):
+            obs.block_sparse_select(bp.index_q[i], bp.index_k, int(bp.query_pos[i]), bp.block_size,
+                                    bp.top_blocks, bp.init_blocks, bp.local_blocks)
+            done_pairs += min(int(bp.query_pos[i]) + 1, bp.index_k.shape[0]) * bp.index_q.shape[1]
+            done_q += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return {"value": done_pairs / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{done_q} queries (all 8 KV heads) of the workload, oracle.block_select"}
+    t0 = time.perf_counter()
+    pairs, rows = 0, 0
+    S = wp.extras.get("S", 0)
+    for m in range(wp.M):
+        ids, _, _, _ = odsa.row_topk(wp, m, wp.K)
+        if S:
+            ow.apply_topology_witnesses(ids, wp.K, [int(wp.key_len[m])], max(wp.K - S, 0), S, S)
+        pairs += int(wp.key_len[m])
+        rows += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": pairs / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {wp.M} rows (score + top-K{' + witness merge' if S else ''}), oracle.dsa fp64"}
+
+
+# --------------------------------------------------------------------- main --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=list(WORKLOAD_TEXT))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    if args.impl == "reference":
+        if rank != 0:
+            if dist:
+                dist.destroy_process_group()
+            return
+        wp = make_workload(args.workload, 0)
+        samples = []
+        for _ in range(args.warmup):
+            pass
+        for _ in range(args.steps):
+            samples.append(cpu_baseline(args.workload, wp, budget_s=4.0))
+        v = statistics.median(s["value"] for s in samples)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": WORKLOAD_TEXT[args.workload]},
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                 "sample": samples[0]["sample"] + " per step"},
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    from sparse_attention_indexer_idx_gb300 import binding as B
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B.lib()
+    wp = make_workload(args.workload, rank)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        if args.workload == "block_select":
+            step = BlockSelectStep(B, wp, dev)
+            pairs_per_step = step.pairs()
+            rows_per_step = wp.index_q.shape[0] * wp.index_q.shape[1]
+        elif args.workload == "prefill_dosa":
+            step = DosaStep(B, wp, dev, R=wp.extras["R"], n_seed=wp.extras["n_seed"])
+            pairs_per_step = wp.pairs()
+            rows_per_step = wp.M
+        else:
+            step = IndexerStep(B, wp, dev)
+            pairs_per_step = wp.pairs()
+            rows_per_step = wp.M
+        for _ in range(args.warmup):
+            step.run()
+        torch.cuda.synchronize()
+        assert B.device_error() == 0, "device error during warm-up"
+        clocks = Clocks(torch.cuda.current_device())
+        clocks.start()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        # one event pair per step around the dominant kernel, on the launching stream
+        per_step = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        t_start.record(stream)
+        for i in range(args.steps):
+            step.ev = per_step[i]
+            step.run(timed=True)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        ms_total = t_start.elapsed_time(t_end)
+        clock_info = clocks.stop()
+    for i in range(args.steps):
+        step.ev = per_step[i]
+        step.collect()
+    kernel_ms = step.score_ms
+    ms_step = ms_total / args.steps
+    if dist:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = pairs_per_step * world / (ms_step * 1e-3)
+
+    hbm, bf16, bf16_sus, peak_src = _peaks()
+    roof = None
+    if isinstance(step, IndexerStep):
+        k_ms = statistics.median(kernel_ms)
+        if wp.dtype in ("bf16", "fp8") and wp.key_off is None:
+            ach = step.flops() / (k_ms * 1e-3) / 1e12
+            roof = {"kernel": "score_tc_kernel", "bound": "tensor", "achieved": ach, "peak": bf16, "unit": "TFLOP/s",
+                    "frac": ach / bf16, "traffic": None, "peak_source": f"{peak_src} bf16 burst",
+                    "kernel_ms": k_ms}
+        else:
+            ach = step.algorithmic_bytes() / (k_ms * 1e-3) / 1e9
+            roof = {"kernel": "score_tc_kernel" if wp.dtype != "f32" else "score_simt_kernel", "bound": "hbm",
+                    "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                    "peak_source": f"{peak_src} hbm copy", "kernel_ms": k_ms,
+                    "algorithmic_bytes": step.algorithmic_bytes()}
+    elif isinstance(step, BlockSelectStep):
+        k_ms = statistics.median(kernel_ms)
+        # fp32 ALU: 2 instructions (mul, add) per multiply-add, 152 SMs x 128 lanes x clock
+        macs = step.pairs() * wp.index_q.shape[2]
+        sm_mhz = clock_info.get("sm_mhz") or 2070.0
+        peak_alu = 152 * 128 * sm_mhz * 1e6 / 1e12
+        ach = 2.0 * macs / (k_ms * 1e-3) / 1e12
+        roof = {"kernel": "block_score_kernel + block_pick_kernel", "bound": "alu", "achieved": ach,
+                "peak": peak_alu, "unit": "Tinst/s", "frac": ach / peak_alu, "traffic": None,
+                "peak_source": "152 SMs x 128 fp32 lanes x median SM clock", "kernel_ms": k_ms}
+    else:
+        k_ms = statistics.median(kernel_ms)
+        roof = {"kernel": "dosa_topk (all kernels)", "bound": "tensor", "achieved": None, "peak": bf16,
+                "unit": "TFLOP/s", "frac": None, "traffic": None, "kernel_ms": k_ms}
+
+    e2e = None
+    if isinstance(step, IndexerStep):
+        with torch.cuda.stream(stream):
+            e_ms, h2d, d2h = e2e_run(B, wp, dev, max(3, min(args.steps, 10)))
+        e2e = {"value": pairs_per_step * world / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    assert B.device_error() == 0, "device error during the timed region"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "fp8": "fp8e4m3"}.get(
+                getattr(wp, "dtype", "f32"), "f32"),
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "l2": "inputs larger than L2 (no flush)"
+                       if args.workload in ("decode", "ragged_fp8") else "keys L2-resident (no flush)"},
+            "rows_per_s": rows_per_step * world / (ms_step * 1e-3),
+            "roofline": roof, "e2e": e2e, "clocks": clock_info,
+            "gpu_launches": step.launches * args.steps}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, wp)
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -43,7 +43,7 @@ def dequantised_keys(problem, m: int) -> np.ndarray:
     """The visible keys of row m as fp64 values (FP8 keys times their scale)."""
     off = problem.row_offset(m)
     n = int(problem.key_len[m])
-    k = problem.keys_f32()[off:off + n].astype(np.float64)
+    k = problem.keys_f32(off, off + n).astype(np.float64)
     if problem.key_scale is not None:
         k = k * problem.key_scale[off:off + n].astype(np.float64)[:, None]
     return k

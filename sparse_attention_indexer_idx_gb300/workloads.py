@@ -93,6 +93,22 @@ def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
     return bits.astype(np.uint8)
 
 
+def _bulk_bf16(x: np.ndarray) -> np.ndarray:
+    """f32_to_bf16_bits for large arrays (torch's cast: same round-to-nearest-even,
+    checked equal by the generator tests)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bulk_e4m3(x: np.ndarray) -> np.ndarray:
+    """f32_to_e4m3_bits for large arrays with |x| <= 448 (torch's cast, checked
+    equal by the generator tests)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
 # ----------------------------------------------------------------------------
 # problem containers
 # ----------------------------------------------------------------------------
@@ -137,12 +153,14 @@ class IndexerProblem:
     def q_f32(self) -> np.ndarray:
         return self.q if self.dtype == "f32" else bf16_bits_to_f32(self.q)
 
-    def keys_f32(self) -> np.ndarray:
+    def keys_f32(self, start: int = 0, stop: Optional[int] = None) -> np.ndarray:
+        """Stored keys [start, stop) widened exactly to float32 (codes only for FP8)."""
+        k = self.keys[start:stop]
         if self.dtype == "f32":
-            return self.keys
+            return k
         if self.dtype == "bf16":
-            return bf16_bits_to_f32(self.keys)
-        return e4m3_bits_to_f32(self.keys)
+            return bf16_bits_to_f32(k)
+        return e4m3_bits_to_f32(k)
 
     def row_offset(self, m: int) -> int:
         return 0 if self.key_off is None else int(self.key_off[m])
@@ -191,12 +209,12 @@ def decode_bf16(seed: int = 2, M: int = 64, H: int = 32, D: int = 128, L: int = 
                 K: int = 2048, S: int = 16, pad_frac: float = 0.05) -> IndexerProblem:
     """Decode batch: every row owns L bf16 keys; w ~ N(0, 1/H) (variance 1/H)."""
     rng = np.random.default_rng(seed)
-    q = f32_to_bf16_bits(_normal(rng, (M, H, D)))
+    q = _bulk_bf16(_normal(rng, (M, H, D)))
     keys = np.empty((M * L, D), dtype=np.uint16)
     chunk = max(1, (1 << 22) // D)
     for s in range(0, M * L, chunk):
         e = min(M * L, s + chunk)
-        keys[s:e] = f32_to_bf16_bits(_normal(rng, (e - s, D)))
+        keys[s:e] = _bulk_bf16(_normal(rng, (e - s, D)))
     w = _normal(rng, (M, H), std=float(np.sqrt(1.0 / H)))
     key_len = np.full(M, L, dtype=np.int32)
     key_off = (np.arange(M, dtype=np.int64) * L)
@@ -220,8 +238,8 @@ def prefill_bf16(seed: int = 3, n_queries: int = 4096, H: int = 64, D: int = 128
     z = rng.integers(0, n_centres, L)
     eps = _normal(rng, (L, D))
     kf = np.where(is_cluster[:, None], centres[z] + np.float32(sigma) * eps, eps).astype(np.float32)
-    keys = f32_to_bf16_bits(kf)
-    q = f32_to_bf16_bits(_normal(rng, (n_queries, H, D)))
+    keys = _bulk_bf16(kf)
+    q = _bulk_bf16(_normal(rng, (n_queries, H, D)))
     w = _normal(rng, (n_queries, H), std=float(np.sqrt(1.0 / H)))
     pos = np.arange(L - n_queries, L, dtype=np.int64)
     key_len = (pos + 1).astype(np.int32)
@@ -244,15 +262,17 @@ def ragged_fp8(seed: int = 5, M: int = 128, H: int = 64, D: int = 128, L_min: in
     n_keys = int(key_len.astype(np.int64).sum())
     keys = np.empty((n_keys, D), dtype=np.uint8)
     scale = np.empty(n_keys, dtype=np.float32)
-    chunk = max(1, (1 << 21) // D)
+    chunk = max(1, (1 << 23) // D)
     for s in range(0, n_keys, chunk):
         e = min(n_keys, s + chunk)
         k = _normal(rng, (e - s, D))
         amax = np.abs(k).max(axis=1)
         sc = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-        keys[s:e] = f32_to_e4m3_bits(k / sc[:, None])
+        k /= sc[:, None]
+        np.clip(k, -E4M3_MAX, E4M3_MAX, out=k)
+        keys[s:e] = _bulk_e4m3(k)
         scale[s:e] = sc
-    q = f32_to_bf16_bits(_normal(rng, (M, H, D)))
+    q = _bulk_bf16(_normal(rng, (M, H, D)))
     w = _normal(rng, (M, H), std=float(np.sqrt(1.0 / H)))
     return IndexerProblem("ragged_fp8", "fp8", q, w, keys, key_len, key_off, K,
                           key_scale=scale,

@@ -33,3 +33,11 @@ def test_generators_are_seeded():
     assert p.keys.dtype == np.uint8 and p.key_scale.shape[0] == p.n_keys
     assert int(p.key_off[-1] + p.key_len[-1]) == p.n_keys
     assert np.abs(p.keys_f32()).max() <= 448
+
+
+def test_bulk_casts_equal_the_reference_encoders():
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(50000) * 60).astype(np.float32)
+    assert np.array_equal(wl._bulk_bf16(x), wl.f32_to_bf16_bits(x))
+    y = np.clip(x, -448, 448)
+    assert np.array_equal(wl._bulk_e4m3(y), wl.f32_to_e4m3_bits(y))
