@@ -153,6 +153,8 @@ class IndexerStep:
         self.K = wp.K
         self.ld = self.p.max_key_len
         self.scores = torch.empty((wp.M, self.ld), dtype=torch.float32, device=dev)
+        self.tk_ws = torch.empty(max(1, B.idx_topk_scores_workspace_size(wp.M, self.ld, wp.K)), dtype=torch.uint8,
+                                 device=dev)
         self.ids = torch.empty((wp.M, self.K), dtype=torch.int32, device=dev)
         self.S = wp.extras.get("S", 0)
         pm = wp.extras.get("pad_mask")
@@ -169,7 +171,7 @@ class IndexerStep:
         B.idx_score(p, self.scores, self.ld)
         if timed:
             self.ev[1].record()
-        B.idx_topk_scores(self.scores, p.key_len, self.ld, self.K, self.ids, None, ld=self.ld)
+        B.idx_topk_scores(self.scores, p.key_len, self.ld, self.K, self.ids, None, ld=self.ld, ws=self.tk_ws)
         if self.S:
             if self.pad is not None:
                 self.ids.masked_fill_(self.pad, -1)

@@ -126,11 +126,14 @@ idx_status idx_topk(const idx_problem* p, int32_t K, int32_t* out_ids, float* ou
 
 /* ---------------------------------------------------------- idx_topk_scores
  * The top-K step alone, on score rows the caller already has: row m is
- * scores[m*ld .. m*ld + lens[m]-1] (device float32, lens device int32), ids
- * are positions in the row.  Same order, padding and K limit as idx_topk.
- * No workspace. */
+ * scores[m*ld .. m*ld + lens[m]-1] (device float32, lens device int32, clamped
+ * to [0, max_len]), ids are positions in the row.  Same order, padding and K
+ * limit as idx_topk.  The workspace is only needed for rows longer than 32768
+ * (the per-chunk candidate lists); its size is 0 otherwise. */
+size_t idx_topk_scores_workspace_size(int64_t M, int32_t max_len, int32_t K);
 idx_status idx_topk_scores(const float* scores, int64_t ld, const int32_t* lens, int64_t M, int32_t max_len,
-                           int32_t K, int32_t* out_ids, float* out_scores, void* stream);
+                           int32_t K, int32_t* out_ids, float* out_scores, void* ws, size_t ws_bytes,
+                           void* stream);
 
 /* --------------------------------------------------------------- dosa_topk
  * DoSA safe-upper-bound pruning ("DoSA：用安全上界减少 Indexer 的完整打分",

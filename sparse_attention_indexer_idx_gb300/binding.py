@@ -65,9 +65,10 @@ EXPORTS = {
     "idx_topk_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(idx_problem), ctypes.c_int32]),
     "idx_topk": (ctypes.c_int32, [ctypes.POINTER(idx_problem), ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "idx_topk_scores_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
     "idx_topk_scores": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
-                                         ctypes.c_void_p]),
+                                         ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "dosa_topk_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(idx_problem), ctypes.c_int32,
                                                    ctypes.POINTER(dosa_params), ctypes.c_int32]),
     "dosa_topk": (ctypes.c_int32, [ctypes.POINTER(idx_problem), ctypes.c_int32, ctypes.POINTER(dosa_params),
@@ -172,11 +173,18 @@ def idx_topk(p: Problem, K: int, out_ids: torch.Tensor, out_scores: Optional[tor
     return out_ids, out_scores
 
 
+def idx_topk_scores_workspace_size(M: int, max_len: int, K: int) -> int:
+    return int(lib().idx_topk_scores_workspace_size(M, max_len, K))
+
+
 def idx_topk_scores(scores: torch.Tensor, lens: torch.Tensor, max_len: int, K: int, out_ids: torch.Tensor,
-                    out_scores: Optional[torch.Tensor] = None, ld: Optional[int] = None, stream=None):
+                    out_scores: Optional[torch.Tensor] = None, ld: Optional[int] = None,
+                    ws: Optional[torch.Tensor] = None, stream=None):
     M = lens.shape[0]
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().idx_topk_scores(_ptr(scores), int(ld if ld is not None else scores.shape[-1]), _ptr(lens), M,
-                                 int(max_len), K, _ptr(out_ids), _ptr(out_scores), _stream(stream)))
+                                 int(max_len), K, _ptr(out_ids), _ptr(out_scores), _ptr(ws), ws_bytes,
+                                 _stream(stream)))
     return out_ids, out_scores
 
 

@@ -101,9 +101,11 @@ idx_status idx_score(const idx_problem* p, float* scores, int64_t ld_scores, voi
 }
 
 size_t idx_topk_workspace_size(const idx_problem* p, int32_t K) {
-  (void)K;
   if (!p || p->M <= 0) return 0;
-  return (size_t)p->M * (size_t)(p->max_key_len > 0 ? p->max_key_len : 1) * sizeof(float) + 256;
+  WsCarver c(nullptr);
+  c.take<float>((size_t)p->M * (size_t)(p->max_key_len > 0 ? p->max_key_len : 1));
+  c.take<char>(topk_dense_ws(p->M, p->max_key_len, K < 1 ? 1 : K));
+  return c.used + 256;
 }
 
 idx_status idx_topk(const idx_problem* p, int32_t K, int32_t* out_ids, float* out_scores, void* ws, size_t ws_bytes,
@@ -117,20 +119,31 @@ idx_status idx_topk(const idx_problem* p, int32_t K, int32_t* out_ids, float* ou
   if (p->M == 0) return IDX_OK;
   cudaStream_t s = (cudaStream_t)stream;
   const int64_t ld = p->max_key_len > 0 ? p->max_key_len : 1;
-  float* scores = (float*)ws;
+  WsCarver c(ws);
+  float* scores = c.take<float>((size_t)p->M * (size_t)ld);
+  char* lists = c.take<char>(topk_dense_ws(p->M, p->max_key_len, K));
   cudaError_t e = launch_score(*p, scores, ld, s);
   if (e != cudaSuccess) return cuda_status(e, "idx_topk/score");
-  e = launch_topk_dense(scores, ld, nullptr, p, p->M, p->max_key_len, K, out_ids, out_scores, s);
+  e = launch_topk_dense(scores, ld, nullptr, p, p->M, p->max_key_len, K, out_ids, out_scores, lists, s);
   return cuda_status(e, "idx_topk/select");
 }
 
+size_t idx_topk_scores_workspace_size(int64_t M, int32_t max_len, int32_t K) {
+  if (M <= 0 || max_len <= 0) return 0;
+  return topk_dense_ws(M, max_len, K < 1 ? 1 : K);
+}
+
 idx_status idx_topk_scores(const float* scores, int64_t ld, const int32_t* lens, int64_t M, int32_t max_len,
-                           int32_t K, int32_t* out_ids, float* out_scores, void* stream) {
+                           int32_t K, int32_t* out_ids, float* out_scores, void* ws, size_t ws_bytes,
+                           void* stream) {
   if (M < 0 || max_len < 0 || ld < max_len) return fail(IDX_ERR_INVALID_ARG, "bad sizes");
   if (K < 1 || K > IDX_MAX_K) return fail(IDX_ERR_INVALID_ARG, "K=%d outside [1, %d]", K, IDX_MAX_K);
   if (M > 0 && (!lens || !out_ids || (max_len > 0 && !scores))) return fail(IDX_ERR_INVALID_ARG, "NULL pointer");
+  const size_t need = idx_topk_scores_workspace_size(M, max_len, K);
+  if (ws_bytes < need) return fail(IDX_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  if (need > 0 && !ws) return fail(IDX_ERR_INVALID_ARG, "workspace is NULL");
   if (M == 0) return IDX_OK;
-  return cuda_status(launch_topk_dense(scores, ld, lens, nullptr, M, max_len, K, out_ids, out_scores,
+  return cuda_status(launch_topk_dense(scores, ld, lens, nullptr, M, max_len, K, out_ids, out_scores, ws,
                                        (cudaStream_t)stream),
                      "idx_topk_scores");
 }

@@ -32,8 +32,13 @@ cudaError_t launch_witness_merge(int32_t* ids, int64_t rows, int topk, const int
 cudaError_t launch_witness_indices(const int32_t* ids, int64_t rows, int topk, const int32_t* ctx, int S,
                                    int32_t* out, cudaStream_t st);
 
+// Exact top-K of dense score rows; ws holds topk_dense_ws() bytes (0 when every
+// row fits one chunk).  Rows come from lens[m] (clamped to [0, max_len]) or,
+// when p_or_null is given, from the problem's visible extents.
+size_t topk_dense_ws(int64_t M, int max_len, int K);
 cudaError_t launch_topk_dense(const float* scores, int64_t ld, const int32_t* lens, const idx_problem* p_or_null,
-                              int64_t M, int max_len, int K, int32_t* out_ids, float* out_scores, cudaStream_t st);
+                              int64_t M, int max_len, int K, int32_t* out_ids, float* out_scores, void* ws,
+                              cudaStream_t st);
 
 // Scores of every visible key (the kernel family depends only on dtype/H/D).
 cudaError_t launch_score(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st);

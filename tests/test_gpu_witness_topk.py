@@ -92,18 +92,41 @@ def test_refused_calls_leave_the_buffer(B):
 
 @pytest.mark.parametrize("seed,M,L,K,ties", [
     (1, 16, 5000, 32, False), (2, 16, 5000, 2048, False), (3, 8, 40000, 2048, False), (4, 33, 3000, 100, True),
-    (5, 7, 9000, 4096, True), (6, 12, 300, 1, True), (7, 5, 131072, 2048, False), (8, 40, 64, 64, True)])
+    (5, 7, 9000, 4096, True), (6, 12, 300, 1, True), (7, 5, 131072, 2048, False), (8, 40, 64, 64, True),
+    (9, 6, 32768, 2048, False), (10, 6, 32769, 2048, True), (11, 4, 100000, 4096, True), (12, 9, 70000, 3, False),
+    (13, 3, 32768, 2048, True)])
 def test_topk_scores_bit_exact(B, seed, M, L, K, ties):
     s, lens = wl.score_rows(seed, M, L, ties=ties)
     lens[0] = 0
     lens[-1] = L
     ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
     sc = torch.empty((M, K), dtype=torch.float32, device="cuda")
-    B.idx_topk_scores(_dev(s, torch.float32), _dev(lens), L, K, ids, sc)
+    ws = torch.empty(max(1, B.idx_topk_scores_workspace_size(M, L, K)), dtype=torch.uint8, device="cuda")
+    B.idx_topk_scores(_dev(s, torch.float32), _dev(lens), L, K, ids, sc, ws=ws)
     g_ids, g_sc = ids.cpu().numpy(), sc.cpu().numpy()
     for m in range(M):
         o_ids, o_sc = odsa.topk(s[m, :lens[m]].astype(np.float64), K)
         assert g_ids[m].tolist() == o_ids.tolist(), m
         o32 = o_sc.astype(np.float32) + np.float32(0.0)    # the kernel reports -0.0 as +0.0
         assert np.array_equal(g_sc[m].view(np.uint32), o32.view(np.uint32)), m
+    assert B.device_error() == 0
+
+
+def test_topk_all_equal_and_two_valued_rows(B):
+    """All scores equal (the sample threshold cannot separate anything: exact
+    fallback) and two-valued rows: ties resolve to the lowest ids."""
+    M, L, K = 4, 50000, 2048
+    s = np.zeros((M, L), dtype=np.float32)
+    s[1] = 1.0
+    s[2, ::3] = 2.0
+    s[3] = -0.0
+    lens = np.full(M, L, dtype=np.int32)
+    ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    sc = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(1, B.idx_topk_scores_workspace_size(M, L, K)), dtype=torch.uint8, device="cuda")
+    B.idx_topk_scores(_dev(s, torch.float32), _dev(lens), L, K, ids, sc, ws=ws)
+    g = ids.cpu().numpy()
+    for m in range(M):
+        o_ids, _ = odsa.topk(s[m].astype(np.float64), K)
+        assert g[m].tolist() == o_ids.tolist(), m
     assert B.device_error() == 0
