@@ -13,22 +13,25 @@
 //      key << 32 | ~id, whose descending order is exactly (score desc, id asc);
 //      otherwise T is lowered (or, failing that, an exact radix select on the
 //      registers takes over);
-//   3. the candidates are bitonic-sorted and the first K are the chunk's top-K.
-// A row of one chunk writes its result directly.  Longer rows write every
-// chunk's sorted top-K list to the workspace, and a merge kernel folds the
-// lists pairwise with bitonic merges, keeping the best K each time.
+//   3. the K winners are bitonic-sorted (in-thread and warp-shuffle stages,
+//      shared memory only for strides that cross warps).
+// The candidates are cut to exactly K by two radix selects (key, then id among
+// ties) and only then sorted, in registers.  A row of one chunk writes its
+// result directly; longer rows write every chunk's (unsorted) top-K set to the
+// workspace, and a merge kernel folds the sets into a running best-K and sorts
+// once.
 #include "internal.h"
 #include "topk.cuh"
 
 namespace idx {
 
-constexpr int TK_NT = 512;
-constexpr int TK_E = 64;
-constexpr int TK_CH = TK_NT * TK_E;
+constexpr int TK_NT = 1024;
+constexpr int TK_CH = 32768;
 constexpr int TK_NS = 1024;
 constexpr int TK_CAP = 8192;
 
 struct TkShared {
+  uint32_t keys[TK_CH];       // the chunk's ordered keys
   uint64_t cand[TK_CAP];
   uint32_t samp[TK_NS];
   uint32_t hist[kTopkBins];
@@ -51,6 +54,32 @@ __device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* red) {
   return t;
 }
 
+// Exclusive prefix sum over the block (thread order); *total = block sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  __syncthreads();
+  if (lane == 31) red[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t x = red[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += u;
+    }
+    red[lane] = x;
+  }
+  __syncthreads();
+  *total = red[31];
+  return (wid ? red[wid - 1] : 0u) + incl - v;
+}
+
 template <class T>
 __device__ void bitonic_desc(T* v, int n, int nt) {
   for (int size = 2; size <= n; size <<= 1) {
@@ -70,19 +99,91 @@ __device__ void bitonic_desc(T* v, int n, int nt) {
   }
 }
 
-// Bitonic merge of a bitonic sequence of n (power of two) values, descending.
-__device__ void bitonic_merge_desc(uint64_t* v, int n) {
-  for (int stride = n >> 1; stride > 0; stride >>= 1) {
-    for (int t = threadIdx.x; t < (n >> 1); t += TK_NT) {
-      const int lo = 2 * t - (t & (stride - 1));
-      const int hi = lo + stride;
-      const uint64_t a = v[lo], b = v[hi];
-      if (a < b) {
-        v[lo] = b;
-        v[hi] = a;
+// ---- register-resident bitonic sort --------------------------------------
+// S = TK_NT * EPT values, thread t holding elements t*EPT .. t*EPT+EPT-1.
+// Strides below EPT are swaps inside a thread, strides below 32*EPT are warp
+// shuffles, only the larger ones go through shared memory (with barriers).
+template <class T>
+__device__ __forceinline__ T shfl_xor_t(T v, int m) {
+  if constexpr (sizeof(T) == 8) {
+    uint32_t lo = (uint32_t)v, hi = (uint32_t)(v >> 32);
+    lo = __shfl_xor_sync(0xffffffffu, lo, m);
+    hi = __shfl_xor_sync(0xffffffffu, hi, m);
+    return ((T)hi << 32) | lo;
+  } else {
+    return (T)__shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+  }
+}
+
+template <class T>
+__device__ __forceinline__ T cmpx(T a, T o, int e, int stride, int size) {
+  // keep the larger value when (lower half) == (descending block)
+  const bool keep_max = (((e & stride) == 0) == ((e & size) == 0));
+  return ((a < o) == keep_max) ? o : a;
+}
+
+template <int EPT, int STRIDE, class T>
+__device__ __forceinline__ void thread_stage(T (&v)[EPT], int size) {
+  T n[EPT];
+#pragma unroll
+  for (int r = 0; r < EPT; ++r) n[r] = cmpx(v[r], v[r ^ STRIDE], threadIdx.x * EPT + r, STRIDE, size);
+#pragma unroll
+  for (int r = 0; r < EPT; ++r) v[r] = n[r];
+}
+
+template <int EPT, class T>
+__device__ void reg_bitonic_desc(T (&v)[EPT], T* xchg) {
+  constexpr int S = TK_NT * EPT;
+  const int tid = threadIdx.x;
+#pragma unroll 1
+  for (int size = 2; size <= S; size <<= 1) {
+#pragma unroll 1
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 32 * EPT) {
+#pragma unroll
+        for (int r = 0; r < EPT; ++r) xchg[tid * EPT + r] = v[r];
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < EPT; ++r) {
+          const int e = tid * EPT + r;
+          v[r] = cmpx(v[r], xchg[e ^ stride], e, stride, size);
+        }
+        __syncthreads();
+      } else if (stride >= EPT) {
+        const int lx = stride / EPT;
+#pragma unroll
+        for (int r = 0; r < EPT; ++r) v[r] = cmpx(v[r], shfl_xor_t(v[r], lx), tid * EPT + r, stride, size);
+      } else {
+        if constexpr (EPT > 8) { if (stride == 8) thread_stage<EPT, 8>(v, size); }
+        if constexpr (EPT > 4) { if (stride == 4) thread_stage<EPT, 4>(v, size); }
+        if constexpr (EPT > 2) { if (stride == 2) thread_stage<EPT, 2>(v, size); }
+        if constexpr (EPT > 1) { if (stride == 1) thread_stage<EPT, 1>(v, size); }
       }
     }
-    __syncthreads();
+  }
+}
+
+// Sorts buf[0..S) descending (S a power of two, >= TK_NT) through registers.
+template <int EPT>
+__device__ void sort_smem_via_regs(uint64_t* buf) {
+  uint64_t v[EPT];
+#pragma unroll
+  for (int r = 0; r < EPT; ++r) v[r] = buf[threadIdx.x * EPT + r];
+  __syncthreads();
+  reg_bitonic_desc<EPT>(v, buf);
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < EPT; ++r) buf[threadIdx.x * EPT + r] = v[r];
+  __syncthreads();
+}
+
+__device__ void sort_candidates(uint64_t* buf, int S) {
+  switch (S / TK_NT) {
+    case 0: bitonic_desc<uint64_t>(buf, S, TK_NT); break;
+    case 1: sort_smem_via_regs<1>(buf); break;
+    case 2: sort_smem_via_regs<2>(buf); break;
+    case 4: sort_smem_via_regs<4>(buf); break;
+    default: sort_smem_via_regs<8>(buf); break;
   }
 }
 
@@ -90,75 +191,95 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, int32_t id) {
   return ((uint64_t)key << 32) | id_key(id);
 }
 
-// Warp-aggregated append of the flagged composite to sh.cand.
-__device__ __forceinline__ void append(TkShared& sh, bool take, uint64_t v) {
-  const unsigned mask = __ballot_sync(0xffffffffu, take);
-  if (!mask) return;
-  const int lane = threadIdx.x & 31;
-  uint32_t base = 0;
-  if (lane == 0) base = atomicAdd(&sh.cnt, (uint32_t)__popc(mask));
-  base = __shfl_sync(0xffffffffu, base, 0);
-  if (take) {
-    const uint32_t pos = base + __popc(mask & ((1u << lane) - 1u));
-    if (pos < TK_CAP) sh.cand[pos] = v;
+template <class F, class Flag>
+__device__ uint32_t smem_radix_select(TkShared& sh, int cn, uint32_t want, F f, Flag flag, uint32_t* above_out,
+                                      uint32_t* eq_out);
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total);
+
+// Keeps exactly the K largest of the n nonzero composites src[0..n) (n >= K),
+// appending them to dst (unsorted).  Two radix selects: the K-th key, then,
+// among the keys equal to it, the ids.
+__device__ void select_exact_k(TkShared& sh, const uint64_t* src, int n, int K, uint64_t* dst) {
+  uint32_t above, eq;
+  auto hi = [&](int i) { return (uint32_t)(src[i] >> 32); };
+  auto real = [&](int i) { return src[i] != 0ull; };
+  const uint32_t KT = smem_radix_select(sh, n, (uint32_t)K, hi, real, &above, &eq);
+  const uint32_t need = (uint32_t)K - above;
+  uint32_t IT = 0;   // with no surplus ties every element at KT is taken
+  if (eq != need) {
+    auto lo = [&](int i) { return (uint32_t)src[i]; };
+    auto tie = [&](int i) { return src[i] != 0ull && (uint32_t)(src[i] >> 32) == KT; };
+    uint32_t above2, eq2;
+    IT = smem_radix_select(sh, n, need, lo, tie, &above2, &eq2);
   }
+  auto take = [&](int i) {
+    const uint64_t v = src[i];
+    const uint32_t k = (uint32_t)(v >> 32);
+    return v != 0ull && (k > KT || (k == KT && (uint32_t)v >= IT));
+  };
+  uint32_t local = 0;
+  for (int i = threadIdx.x; i < n; i += TK_NT) local += take(i) ? 1u : 0u;
+  uint32_t total;
+  uint32_t off = block_excl_scan(local, sh.red, &total);
+  for (int i = threadIdx.x; i < n; i += TK_NT)
+    if (take(i)) dst[off++] = src[i];
+  __syncthreads();
 }
 
-// Exact radix select over the register-resident keys: the `want`-th largest
-// value of f (11+11+10-bit digits) among the flagged elements.
+// Suffix search over sh.hist[0..nb) (bins high to low): the bin b with
+// (#in bins > b) < remaining <= (#in bins >= b) -> sh.found_bin/found_above.
+__device__ __forceinline__ void hist_suffix_find(TkShared& sh, int nb, uint32_t remaining) {
+  constexpr int PER = kTopkBins / TK_NT;
+  uint32_t loc[PER], sum = 0;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int bin = nb - 1 - (threadIdx.x * PER + q);
+    loc[q] = bin >= 0 ? sh.hist[bin] : 0u;
+    sum += loc[q];
+  }
+  uint32_t total;
+  uint32_t run = block_excl_scan(sum, sh.red, &total);
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int bin = nb - 1 - (threadIdx.x * PER + q);
+    if (bin >= 0 && run < remaining && run + loc[q] >= remaining) {
+      sh.found_bin = (uint32_t)bin;
+      sh.found_above = run;
+    }
+    run += loc[q];
+  }
+  __syncthreads();
+}
+
+// Exact radix select over n elements in shared memory: the `want`-th largest
+// value of f(i) (11+11+10-bit digits) among the flagged elements; *eq_out =
+// how many flagged elements equal it.
 template <class F, class Flag>
-__device__ uint32_t reg_radix_select(TkShared& sh, uint32_t want, F f, Flag flag, uint32_t* above_out) {
-  uint32_t prefix = 0, mask = 0, remaining = want;
+__device__ uint32_t smem_radix_select(TkShared& sh, int cn, uint32_t want, F f, Flag flag, uint32_t* above_out,
+                                      uint32_t* eq_out) {
+  uint32_t prefix = 0, mask = 0, remaining = want, eq = 0;
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const uint32_t dmask = pass == 2 ? 0x3ffu : 0x7ffu;
     for (int b = threadIdx.x; b < kTopkBins; b += TK_NT) sh.hist[b] = 0;
     __syncthreads();
-#pragma unroll
-    for (int j = 0; j < TK_E; ++j) {
-      if (flag(j)) {
-        const uint32_t k = f(j);
+    for (int i = threadIdx.x; i < cn; i += TK_NT) {
+      if (flag(i)) {
+        const uint32_t k = f(i);
         if ((k & mask) == prefix) atomicAdd(&sh.hist[(k >> shift) & dmask], 1u);
       }
     }
     __syncthreads();
-    // suffix search over the bins, high to low (4 bins per thread)
-    const int nb = (int)dmask + 1;
-    uint32_t loc[4], sum = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int bin = nb - 1 - (threadIdx.x * 4 + q);
-      loc[q] = bin >= 0 ? sh.hist[bin] : 0u;
-      sum += loc[q];
-    }
-    uint32_t incl = sum;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) sh.red[wid] = incl;
-    __syncthreads();
-    uint32_t run = incl - sum;
-    for (int w = 0; w < wid; ++w) run += sh.red[w];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int bin = nb - 1 - (threadIdx.x * 4 + q);
-      if (bin >= 0 && run < remaining && run + loc[q] >= remaining) {
-        sh.found_bin = (uint32_t)bin;
-        sh.found_above = run;
-      }
-      run += loc[q];
-    }
-    __syncthreads();
+    hist_suffix_find(sh, (int)dmask + 1, remaining);
     remaining -= sh.found_above;
+    eq = sh.hist[sh.found_bin];
     prefix |= sh.found_bin << shift;
     mask |= dmask << shift;
     __syncthreads();
   }
   *above_out = want - remaining;
+  *eq_out = eq;
   return prefix;
 }
 
@@ -187,40 +308,74 @@ __global__ void __launch_bounds__(TK_NT, 1)
   const float* row = scores + m * ld + base;
   const int tid = threadIdx.x;
 
-  uint32_t k[TK_E];
+  // stage the chunk as ordered keys in shared memory (8 loads in flight per thread)
+  uint32_t* K_ = sh.keys;
+  for (int i0 = 0; i0 < cn; i0 += 8 * TK_NT) {
+    float f[8];
 #pragma unroll
-  for (int j = 0; j < TK_E; ++j) {
-    const int i = tid + j * TK_NT;
-    k[j] = i < cn ? score_key(__ldg(row + i)) : 0u;   // 0 sorts below every finite score
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * TK_NT + tid;
+      f[u] = i < cn ? __ldg(row + i) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * TK_NT + tid;
+      if (i < cn) K_[i] = score_key(f[u]);
+    }
   }
-  if (tid == 0) sh.cnt = 0;
   __syncthreads();
 
-  if (cn <= K) {
-#pragma unroll
-    for (int j = 0; j < TK_E; ++j) {
-      const int i = tid + j * TK_NT;
-      append(sh, i < cn, composite(k[j], (int32_t)(base + i)));
-    }
-  } else {
-    // 1. sample threshold
-    sh.samp[tid] = k[0];
-    sh.samp[tid + TK_NT] = k[TK_E / 2];
+  // Candidates: every key >= T, written through a block prefix sum (no atomics).
+  auto compact = [&](uint32_t T, uint32_t KT, uint32_t IT, bool exact_ids) {
+    auto take = [&](int i) {
+      const uint32_t kk = K_[i];
+      return exact_ids ? (kk > KT || (kk == KT && id_key((int32_t)(base + i)) >= IT)) : kk >= T;
+    };
+    uint32_t local = 0;
+    for (int i = tid; i < cn; i += TK_NT) local += take(i) ? 1u : 0u;
+    uint32_t total;
+    uint32_t off = block_excl_scan(local, sh.red, &total);
+    for (int i = tid; i < cn; i += TK_NT)
+      if (take(i) && off < TK_CAP) sh.cand[off++] = composite(K_[i], (int32_t)(base + i));
+    if (tid == 0) sh.cnt = total;
     __syncthreads();
-    bitonic_desc<uint32_t>(sh.samp, TK_NS, TK_NT);
-    const int nvalid = min(TK_NT, cn) + max(0, min(TK_NT, cn - (TK_E / 2) * TK_NT));
+  };
+
+  if (cn <= K) {
+    compact(0u, 0u, 0u, false);          // every key (keys are >= 1)
+  } else {
+    // 1. threshold from 1024 evenly spaced sample keys: the sample rank r that
+    //    should leave ~1.15 K + 3 sigma keys above, located by a two-level
+    //    histogram of the samples (top 11 bits, then the next 11)
+    const int step = cn / TK_NS > 0 ? cn / TK_NS : 1;
+    const int si = tid * step;
+    const uint32_t sv = si < cn ? K_[si] : 0u;
+    const int nvalid = min(TK_NS, cn);
     const float expect = (float)nvalid * (float)K / (float)cn;
-    int r = (int)ceilf(1.2f * expect + 3.0f * sqrtf(expect)) + 1;
+    int r = (int)ceilf(1.15f * expect + 3.0f * sqrtf(expect)) + 1;
     r = r < 1 ? 1 : (r > nvalid ? nvalid : r);
-    uint32_t T = 0;
+    uint32_t T = 0, count = 0;
     bool ok = false;
 #pragma unroll 1
-    for (int attempt = 0; attempt < 4; ++attempt) {
-      T = sh.samp[r - 1];
+    for (int attempt = 0; attempt < 3; ++attempt) {
+      for (int b2 = tid; b2 < kTopkBins; b2 += TK_NT) sh.hist[b2] = 0;
+      __syncthreads();
+      if (sv) atomicAdd(&sh.hist[sv >> 21], 1u);
+      __syncthreads();
+      hist_suffix_find(sh, kTopkBins, (uint32_t)r);
+      const uint32_t b1 = sh.found_bin, a1 = sh.found_above;
+      __syncthreads();
+      for (int b2 = tid; b2 < kTopkBins; b2 += TK_NT) sh.hist[b2] = 0;
+      __syncthreads();
+      if (sv && (sv >> 21) == b1) atomicAdd(&sh.hist[(sv >> 10) & 0x7ffu], 1u);
+      __syncthreads();
+      hist_suffix_find(sh, kTopkBins, (uint32_t)r - a1);
+      T = (b1 << 21) | (sh.found_bin << 10);
+      if (T == 0u) T = 1u;
+      __syncthreads();
       uint32_t local = 0;
-#pragma unroll
-      for (int j = 0; j < TK_E; ++j) local += (k[j] >= T && k[j] != 0u) ? 1u : 0u;
-      const uint32_t count = block_sum_u32(local, sh.red);
+      for (int i = tid; i < cn; i += TK_NT) local += (K_[i] >= T) ? 1u : 0u;
+      count = block_sum_u32(local, sh.red);
       if (count > (uint32_t)TK_CAP) break;
       if (count >= (uint32_t)K) {
         ok = true;
@@ -230,56 +385,61 @@ __global__ void __launch_bounds__(TK_NT, 1)
       r = min(nvalid, 2 * r);
     }
     if (ok) {
-#pragma unroll
-      for (int j = 0; j < TK_E; ++j) {
-        const int i = tid + j * TK_NT;
-        append(sh, k[j] >= T && k[j] != 0u, composite(k[j], (int32_t)(base + i)));
-      }
+      compact(T, 0u, 0u, false);
     } else {
-      // 2'. exact: radix select of the K-th key, then of the ids among its ties
-      uint32_t above;
-      auto key_f = [&](int j) { return k[j]; };
-      auto valid = [&](int j) { return tid + j * TK_NT < cn; };
-      const uint32_t KT = reg_radix_select(sh, (uint32_t)K, key_f, valid, &above);
+      // exact: radix select of the K-th key, then of the ids among its ties
+      uint32_t above, eq;
+      auto key_f = [&](int i) { return K_[i]; };
+      auto all = [&](int) { return true; };
+      const uint32_t KT = smem_radix_select(sh, cn, (uint32_t)K, key_f, all, &above, &eq);
       const uint32_t need = (uint32_t)K - above;
-      auto tie = [&](int j) { return tid + j * TK_NT < cn && k[j] == KT; };
-      auto idk = [&](int j) { return id_key((int32_t)(base + tid + j * TK_NT)); };
-      uint32_t above2;
-      const uint32_t IT = reg_radix_select(sh, need, idk, tie, &above2);
-#pragma unroll
-      for (int j = 0; j < TK_E; ++j) {
-        const int i = tid + j * TK_NT;
-        const bool take = i < cn && (k[j] > KT || (k[j] == KT && id_key((int32_t)(base + i)) >= IT));
-        append(sh, take, composite(k[j], (int32_t)(base + i)));
+      uint32_t IT = 0;
+      if (eq != need) {
+        auto tie = [&](int i) { return K_[i] == KT; };
+        auto idk = [&](int i) { return id_key((int32_t)(base + i)); };
+        uint32_t above2, eq2;
+        IT = smem_radix_select(sh, cn, need, idk, tie, &above2, &eq2);
       }
+      compact(0u, KT, IT, true);
     }
   }
   __syncthreads();
-  const int cnt = (int)min(sh.cnt, (uint32_t)TK_CAP);
-  int S = 1;
-  while (S < cnt) S <<= 1;
-  for (int i = cnt + tid; i < S; i += TK_NT) sh.cand[i] = 0ull;
-  __syncthreads();
-  if (S > 1) bitonic_desc<uint64_t>(sh.cand, S, TK_NT);
-  if (single) {
-    for (int j = tid; j < K; j += TK_NT) {
-      const uint64_t v = j < cnt ? sh.cand[j] : 0ull;
-      out_ids[m * K + j] = v ? key_id((uint32_t)v) : -1;
-      if (out_scores) out_scores[m * K + j] = v ? key_score((uint32_t)(v >> 32)) : -__int_as_float(0x7f800000);
-    }
+  int cnt = (int)min(sh.cnt, (uint32_t)TK_CAP);
+  // exactly min(K, cn) composites, into the (now free) key area
+  uint64_t* best = reinterpret_cast<uint64_t*>(sh.keys);
+  if (cnt > K) {
+    select_exact_k(sh, sh.cand, cnt, K, best);
+    cnt = K;
   } else {
+    for (int i = tid; i < cnt; i += TK_NT) best[i] = sh.cand[i];
+    __syncthreads();
+  }
+  if (!single) {
     uint64_t* dst = lists + ((int64_t)m * n_chunks + c) * P;
-    for (int j = tid; j < P; j += TK_NT) dst[j] = (j < K && j < cnt) ? sh.cand[j] : 0ull;
+    for (int j = tid; j < P; j += TK_NT) dst[j] = j < cnt ? best[j] : 0ull;
+    return;
+  }
+  for (int i = cnt + tid; i < P; i += TK_NT) best[i] = 0ull;
+  __syncthreads();
+  if (P > 1) sort_candidates(best, P);
+  for (int j = tid; j < K; j += TK_NT) {
+    const uint64_t v = best[j];
+    out_ids[m * K + j] = v ? key_id((uint32_t)v) : -1;
+    if (out_scores) out_scores[m * K + j] = v ? key_score((uint32_t)(v >> 32)) : -__int_as_float(0x7f800000);
   }
 }
 
-// Folds the sorted chunk lists of every multi-chunk row into its top-K.
+// Folds the chunk candidate sets of every multi-chunk row into its top-K:
+// a running best-K set meets each chunk's set, an exact selection keeps the K
+// largest, and one sort orders the result.
 __global__ void __launch_bounds__(TK_NT, 1)
     topk_merge_kernel(const int32_t* __restrict__ lens, idx_problem p, int use_p, int max_len, int K, int P,
                       const uint64_t* __restrict__ lists, int n_chunks, int32_t* __restrict__ out_ids,
                       float* __restrict__ out_scores) {
   extern __shared__ __align__(16) uint8_t tk_smem[];
-  uint64_t* buf = reinterpret_cast<uint64_t*>(tk_smem);   // 2P
+  TkShared& sh = *reinterpret_cast<TkShared*>(tk_smem);
+  uint64_t* pair = reinterpret_cast<uint64_t*>(sh.keys);   // [best P | chunk P]
+  uint64_t* best = sh.cand;
   const int64_t m = blockIdx.x;
   int n;
   if (use_p) {
@@ -292,16 +452,18 @@ __global__ void __launch_bounds__(TK_NT, 1)
   if (n <= TK_CH) return;   // written by the chunk kernel
   const int chunks = (int)((n + TK_CH - 1) / TK_CH);
   const uint64_t* src = lists + (int64_t)m * n_chunks * P;
-  for (int i = threadIdx.x; i < P; i += TK_NT) buf[i] = src[i];
+  for (int i = threadIdx.x; i < P; i += TK_NT) pair[i] = src[i];
   for (int c = 1; c < chunks; ++c) {
     const uint64_t* s2 = src + (int64_t)c * P;
-    for (int i = threadIdx.x; i < P; i += TK_NT) buf[P + i] = s2[P - 1 - i];   // reversed: bitonic
+    for (int i = threadIdx.x; i < P; i += TK_NT) pair[P + i] = s2[i];
     __syncthreads();
-    bitonic_merge_desc(buf, 2 * P);
+    select_exact_k(sh, pair, 2 * P, K, best);     // at least K real entries: chunk 0 alone has K
+    for (int i = threadIdx.x; i < P; i += TK_NT) pair[i] = i < K ? best[i] : 0ull;
+    __syncthreads();
   }
-  __syncthreads();
+  if (P > 1) sort_candidates(pair, P);
   for (int j = threadIdx.x; j < K; j += TK_NT) {
-    const uint64_t v = buf[j];
+    const uint64_t v = pair[j];
     out_ids[m * K + j] = v ? key_id((uint32_t)v) : -1;
     if (out_scores) out_scores[m * K + j] = v ? key_score((uint32_t)(v >> 32)) : -__int_as_float(0x7f800000);
   }
@@ -336,7 +498,7 @@ cudaError_t launch_topk_dense(const float* scores, int64_t ld, const int32_t* le
                                                out_scores, (uint64_t*)ws, n_chunks);
   e = cudaGetLastError();
   if (e != cudaSuccess || n_chunks == 1) return e;
-  const size_t msmem = 2 * (size_t)P * sizeof(uint64_t);
+  const size_t msmem = sizeof(TkShared);
   e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
   if (e != cudaSuccess) return e;
   topk_merge_kernel<<<(unsigned)M, TK_NT, msmem, st>>>(lens, p, p_or_null ? 1 : 0, max_len, K, P, (const uint64_t*)ws,
