@@ -1,8 +1,793 @@
+// DoSA safe-upper-bound pruning of the indexer top-K
+// ("DoSA：用安全上界减少 Indexer 的完整打分", sections 2, 3.1, 3.2, 4).
+//
+// Pipeline (one stream, no host synchronisation):
+//   seeds      per row a set of distinct visible seed keys, as a bitmap and an
+//              ascending list: the caller's lists, the cold rule of section 4
+//              for one shared key sequence (four evenly spaced representative
+//              queries fully scored; keys ranked by how many representative
+//              top-K lists hold them, then their best representative score,
+//              then id), or floor(i L / n) for per-row keys;
+//   seed top-K the seeds scored with every head by the same tensor-core score
+//              kernel as the unpruned path, then the exact top-K; tau = the
+//              K-th seed score (section 2 step 1);
+//   planner    per query: R retained heads (largest |w_h| ||q_h||), an anchor
+//              q_j, beta = max(0, q_h.q_j/||q_j||^2) and ||q_h - beta q_j|| for
+//              every omitted positive head (section 3.1), folded weights
+//              w'_j = w_j + sum beta_h w_h, c = sum w_h ||d_h||, the omitted
+//              negative heads active (q_h.k > 0) on at least act_freq_min of the
+//              seed samples and their |w|-weighted aggregate a_A (section 3.2),
+//              a_A rounded to bf16 with the rounding distance added to the
+//              margin, plus gamma * (sum_h |w_h| ||q_h|| + ||a_A||);
+//   bound scan the tensor-core kernel in bound mode: U >= tau keeps a key;
+//   rescoring  the candidates scored exactly (gathered tiles, same MMA shape
+//              per pair); survivors have s >= tau (section 2 step 3);
+//   merge      exact top-K of the seed top-K plus the survivors;
+//   fallback   rows with too few seeds or an overflowing candidate list are
+//              recomputed on the unpruned path.
+// The output equals idx_topk bit for bit: every exact score comes from the
+// same kernel family, the bound exceeds the computed score (margin), ties at
+// tau are kept, and the final selection uses the same total order.
+#include <cstring>
+
 #include "internal.h"
+#include "topk.cuh"
+
 namespace idx {
-size_t dosa_ws(const idx_problem&, int, const dosa_params&, int) { return 0; }
-cudaError_t launch_dosa(const idx_problem&, int, const dosa_params&, const int32_t*, int, int32_t*, float*, int32_t*,
-                        dosa_stats*, void*, size_t, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+constexpr int kVec = 32;          // prepared vectors per query: R retained + aggregate at row 31
+constexpr int kPlanThreads = 256;
+
+__global__ void fill_i32_kernel(int32_t* p, int64_t n, int32_t v) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) p[i] = v;
 }
+
+static cudaError_t fill_i32(void* p, int64_t n, int32_t v, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  fill_i32_kernel<<<(unsigned)blocks, 256, 0, st>>>((int32_t*)p, n, v);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ seeds --
+
+__global__ void min_len_kernel(idx_problem p, int32_t* out) {
+  __shared__ int32_t red[32];
+  int32_t mn = 0x7fffffff;
+  for (int64_t m = threadIdx.x; m < p.M; m += blockDim.x) {
+    int64_t off;
+    int len;
+    row_extent(p, m, &off, &len);
+    mn = len < mn ? len : mn;
+  }
+  for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mn;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t v = 0x7fffffff;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) v = min(v, red[w]);
+    *out = p.M > 0 ? v : 0;
+  }
+}
+
+struct Reps {
+  int64_t m[4];
+  int n;
+};
+
+__global__ void gather_reps_kernel(idx_problem p, Reps r, const int32_t* common_len, uint16_t* q_out, float* w_out,
+                                   int32_t* len_out) {
+  const int i = blockIdx.x;
+  const int64_t m = r.m[i];
+  const int64_t hd = (int64_t)p.H * p.D;
+  const uint16_t* q = (const uint16_t*)p.q + m * hd;
+  for (int64_t e = threadIdx.x; e < hd; e += blockDim.x) q_out[i * hd + e] = q[e];
+  for (int h = threadIdx.x; h < p.H; h += blockDim.x) w_out[i * p.H + h] = p.w[m * p.H + h];
+  if (threadIdx.x == 0) len_out[i] = *common_len;
+}
+
+__global__ void rep_count_kernel(const int32_t* rep_ids, int nrep, int K, uint32_t* count) {
+  const int64_t n = (int64_t)nrep * K;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t id = rep_ids[i];
+    if (id >= 0) atomicAdd(&count[id], 1u);
+  }
+}
+
+// Cold rule: the n_seed best keys of [0, Lc) by (count desc, best rep score
+// desc, id asc) are marked in the shared seed bitmap.
+constexpr int kColdThreads = 1024;
+struct DummyRow {};
+
+__global__ void __launch_bounds__(kColdThreads) cold_select_kernel(const uint32_t* count, const float* rep_sc,
+                                                                   int64_t ld, int nrep, const int32_t* common_len,
+                                                                   int n_seed, uint32_t* seedbits) {
+  __shared__ TopkShared<kColdThreads> sh;
+  __shared__ uint32_t cnt_hist[8];
+  const int Lc = *common_len;
+  auto best_key = [&](int k) {
+    float b = rep_sc[k];
+    for (int r = 1; r < nrep; ++r) b = fmaxf(b, rep_sc[r * ld + k]);
+    return score_key(b);
+  };
+  if (Lc <= n_seed) {
+    for (int k = threadIdx.x; k < Lc; k += kColdThreads) atomicOr(&seedbits[k >> 5], 1u << (k & 31));
+    return;
+  }
+  if (threadIdx.x < 8) cnt_hist[threadIdx.x] = 0;
+  __syncthreads();
+  for (int k = threadIdx.x; k < Lc; k += kColdThreads) atomicAdd(&cnt_hist[min(count[k], 7u)], 1u);
+  __syncthreads();
+  // c*: the count level where the cumulative number of keys (from the top) reaches n_seed
+  int cstar = 0;
+  uint32_t above = 0;
+  {
+    uint32_t cum = 0;
+    for (int c = 7; c >= 0; --c) {
+      if (cum + cnt_hist[c] >= (uint32_t)n_seed) {
+        cstar = c;
+        above = cum;
+        break;
+      }
+      cum += cnt_hist[c];
+    }
+  }
+  const uint32_t need = (uint32_t)n_seed - above;
+  DummyRow dr;
+  auto at_c = [&](int k) { return (int)min(count[k], 7u) == cstar; };
+  uint32_t above_b, eq_b;
+  const uint32_t T = topk_radix_select<kColdThreads>(sh, dr, Lc, need, best_key, at_c, &above_b, &eq_b);
+  const uint32_t need_t = need - above_b;
+  uint32_t I = 0;
+  if (eq_b != need_t) {
+    auto idk = [&](int k) { return id_key(k); };
+    auto tie = [&](int k) { return at_c(k) && best_key(k) == T; };
+    uint32_t a2, e2;
+    I = topk_radix_select<kColdThreads>(sh, dr, Lc, need_t, idk, tie, &a2, &e2);
+  }
+  for (int k = threadIdx.x; k < Lc; k += kColdThreads) {
+    const int c = (int)min(count[k], 7u);
+    bool take = c > cstar;
+    if (c == cstar) {
+      const uint32_t bk = best_key(k);
+      take = bk > T || (bk == T && id_key(k) >= I);
+    }
+    if (take) atomicOr(&seedbits[k >> 5], 1u << (k & 31));
+  }
+}
+
+__global__ void strided_seeds_kernel(idx_problem p, int n_seed, uint32_t* bits, int64_t W) {
+  const int64_t m = blockIdx.x;
+  int64_t off;
+  int L;
+  row_extent(p, m, &off, &L);
+  const int n = L < n_seed ? L : n_seed;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int64_t x = ((int64_t)i * L) / n;
+    atomicOr(&bits[m * W + (x >> 5)], 1u << (x & 31));
+  }
+}
+
+__global__ void caller_seeds_kernel(idx_problem p, const int32_t* seed_ids, int seed_ld, uint32_t* bits, int64_t W) {
+  const int64_t m = blockIdx.x;
+  int64_t off;
+  int L;
+  row_extent(p, m, &off, &L);
+  for (int j = threadIdx.x; j < seed_ld; j += blockDim.x) {
+    const int32_t id = seed_ids[m * seed_ld + j];
+    if (id >= 0 && id < L) atomicOr(&bits[m * W + (id >> 5)], 1u << (id & 31));
+  }
+}
+
+// Seed bitmap row -> ascending id list (at most cap entries) and its count.
+constexpr int kListThreads = 1024;
+__global__ void __launch_bounds__(kListThreads) bits_to_list_kernel(const uint32_t* bits, int64_t W, int32_t* list,
+                                                                     int64_t cap, int32_t* cnt) {
+  __shared__ uint32_t wsum[32];
+  const int64_t r = blockIdx.x;
+  const uint32_t* b = bits + r * W;
+  int32_t* out = list + r * cap;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int64_t run = 0;
+  for (int64_t w0 = 0; w0 < W; w0 += kListThreads) {
+    const int64_t w = w0 + threadIdx.x;
+    const uint32_t word = w < W ? b[w] : 0u;
+    const uint32_t pc = __popc(word);
+    uint32_t incl = pc;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[wid] = incl;
+    __syncthreads();
+    uint32_t woff = 0, tot = 0;
+    for (int i = 0; i < kListThreads / 32; ++i) {
+      if (i < wid) woff += wsum[i];
+      tot += wsum[i];
+    }
+    int64_t pos = run + woff + incl - pc;
+    uint32_t v = word;
+    while (v) {
+      const int bit = __ffs(v) - 1;
+      v &= v - 1;
+      if (pos < cap) out[pos] = (int32_t)(w * 32 + bit);
+      ++pos;
+    }
+    run += tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) cnt[r] = (int32_t)(run < cap ? run : cap);
+}
+
+// Copies the shared seed keys (and scales) into a contiguous buffer.
+__global__ void gather_keys_kernel(idx_problem p, const int32_t* list, const int32_t* cnt, void* out_keys,
+                                   float* out_scale) {
+  const int n = *cnt;
+  const int row_bytes = p.k_dtype == IDX_FP8_E4M3 ? 128 : 256;
+  const int words = row_bytes / 16;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < (int64_t)n * words;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = t / words, c = t % words;
+    const int64_t id = list[i];
+    const uint4* src = (const uint4*)((const char*)p.keys + id * row_bytes);
+    ((uint4*)((char*)out_keys + i * row_bytes))[c] = src[c];
+    if (c == 0 && out_scale) out_scale[i] = p.key_scale[id];
+  }
+}
+
+__global__ void broadcast_i32_kernel(const int32_t* src, int32_t* dst, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = *src;
+}
+
+// tau, status and the active-row mask after the seed top-K.
+__global__ void seed_status_kernel(int64_t M, int K, const int32_t* seed_cnt, int shared, const float* stop_sc,
+                                   float* tau, int32_t* status, int32_t* active) {
+  for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < M; m += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t c = seed_cnt[shared ? 0 : m];
+    const bool ok = c >= K;
+    tau[m] = ok ? stop_sc[m * K + K - 1] : 0.0f;
+    status[m] = ok ? 0 : 1;
+    active[m] = ok ? 1 : 0;
+  }
+}
+
+// ---------------------------------------------------------------- planner --
+
+struct PlanArgs {
+  idx_problem p;
+  int R;
+  int n_sample;
+  float act_min;
+  float gamma;
+  const int32_t* seed_list;   // [rows, list_ld]
+  int64_t list_ld;
+  const int32_t* seed_cnt;
+  int shared_seeds;
+  const int32_t* active;
+  uint16_t* qprep;            // [M, 32, D] bf16
+  float* wfold;               // [M, 32]
+  float* coef;                // [M]
+};
+
+__device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ uint16_t f_to_bf16_rn(float x) {
+  uint32_t u = __float_as_uint(x);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+__device__ __forceinline__ float e4m3_to_f(uint8_t b) {
+  const int s = b >> 7, e = (b >> 3) & 0xf, m = b & 7;
+  float v = e == 0 ? (float)m * 0.001953125f : ldexpf(1.0f + (float)m * 0.125f, e - 7);
+  return s ? -v : v;
+}
+
+// One thread block per query.  Shared memory: q [H][D] f32, sample keys
+// [ns][D] f32, and per-head scratch.
+__global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
+  extern __shared__ __align__(16) float pl[];
+  const idx_problem& p = a.p;
+  const int64_t m = blockIdx.x;
+  const int H = p.H, D = p.D, R = a.R;
+  float* q = pl;                       // H*D
+  float* ks = q + H * D;               // n_sample*D
+  float* qn2 = ks + a.n_sample * D;    // H: ||q_h||^2
+  float* beta = qn2 + H;               // H
+  float* dn = beta + H;                // H: ||d_h||
+  float* aggv = dn + H;                // D: a_A
+  int* anchor = (int*)(aggv + D);      // H
+  int* ret_pos = anchor + H;           // H: position among retained, -1 if omitted
+  int* act = ret_pos + H;              // H: activation counts
+  int* rlist = act + H;                // 32: retained heads ascending
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int nw = kPlanThreads / 32;
+
+  uint16_t* qout = a.qprep + m * kVec * D;
+  float* wout = a.wfold + m * kVec;
+  if (!a.active[m]) {
+    for (int i = tid; i < kVec * D; i += kPlanThreads) qout[i] = 0;
+    for (int i = tid; i < kVec; i += kPlanThreads) wout[i] = 0.0f;
+    if (tid == 0) a.coef[m] = 0.0f;
+    return;
+  }
+  const uint16_t* qsrc = (const uint16_t*)p.q + m * (int64_t)H * D;
+  for (int i = tid; i < H * D; i += kPlanThreads) q[i] = bf16_to_f(qsrc[i]);
+  // sample keys: seed[floor(i n / ns)], i < ns = min(n_sample, n)
+  const int32_t* sl = a.seed_list + (a.shared_seeds ? 0 : m * a.list_ld);
+  const int n = a.seed_cnt[a.shared_seeds ? 0 : m];
+  const int ns = n < a.n_sample ? n : a.n_sample;
+  const int64_t kbase = p.key_off ? p.key_off[m] : 0;
+  for (int i = tid; i < ns * D; i += kPlanThreads) {
+    const int si = i / D, d = i % D;
+    const int64_t id = sl[n <= a.n_sample ? si : (int)(((int64_t)si * n) / a.n_sample)];
+    const int64_t e = (kbase + id) * D + d;
+    ks[i] = p.k_dtype == IDX_FP8_E4M3 ? e4m3_to_f(((const uint8_t*)p.keys)[e]) : bf16_to_f(((const uint16_t*)p.keys)[e]);
+  }
+  __syncthreads();
+  // ||q_h||^2, one warp per head, fixed order
+  for (int h = wid; h < H; h += nw) {
+    float s = 0.0f;
+    for (int d = lane; d < D; d += 32) s = __fmaf_rn(q[h * D + d], q[h * D + d], s);
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) qn2[h] = s;
+  }
+  __syncthreads();
+  // retained heads: the R largest |w_h| ||q_h||, ties to the lower head
+  for (int h = tid; h < H; h += kPlanThreads) {
+    const float mh = fabsf(p.w[m * H + h]) * sqrtf(qn2[h]);
+    int rank = 0;
+    for (int g = 0; g < H; ++g) {
+      const float mg = fabsf(p.w[m * H + g]) * sqrtf(qn2[g]);
+      rank += (mg > mh || (mg == mh && g < h)) ? 1 : 0;
+    }
+    ret_pos[h] = rank < R ? 1 : -1;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int c = 0;
+    for (int h = 0; h < H; ++h)
+      if (ret_pos[h] > 0) {
+        rlist[c] = h;
+        ret_pos[h] = c++;
+      }
+  }
+  __syncthreads();
+  // anchors of the omitted positive heads (section 3.1)
+  for (int h = tid; h < H; h += kPlanThreads) {
+    const float wh = p.w[m * H + h];
+    anchor[h] = -1;
+    beta[h] = 0.0f;
+    dn[h] = 0.0f;
+    if (ret_pos[h] >= 0 || !(wh > 0.0f)) continue;
+    float best = 0.0f;
+    int bj = -1;
+    float bb = 0.0f;
+    for (int r = 0; r < R; ++r) {
+      const int j = rlist[r];
+      float dot = 0.0f;
+      for (int d = 0; d < D; ++d) dot = __fmaf_rn(q[h * D + d], q[j * D + d], dot);
+      const float b = qn2[j] > 0.0f ? fmaxf(0.0f, dot / qn2[j]) : 0.0f;
+      const float r2 = qn2[h] - 2.0f * b * dot + b * b * qn2[j];
+      if (bj < 0 || r2 < best) {
+        best = r2;
+        bj = j;
+        bb = b;
+      }
+    }
+    // residual norm of the chosen decomposition, computed directly and rounded up
+    float s = 0.0f;
+    for (int d = 0; d < D; ++d) {
+      const float x = q[h * D + d] - bb * q[bj * D + d];
+      s = __fmaf_rn(x, x, s);
+    }
+    anchor[h] = bj;
+    beta[h] = bb;
+    dn[h] = __fsqrt_ru(s) * (1.0f + 1.0e-6f);
+  }
+  // activation counts of the omitted negative heads on the samples (section 3.2)
+  for (int h = wid; h < H; h += nw) {
+    int count = 0;
+    const float wh = p.w[m * H + h];
+    if (ret_pos[h] < 0 && wh < 0.0f) {
+      for (int si = lane; si < ns; si += 32) {
+        float dot = 0.0f;
+        for (int d = 0; d < D; ++d) dot = __fmaf_rn(q[h * D + d], ks[si * D + d], dot);
+        count += dot > 0.0f ? 1 : 0;
+      }
+      for (int o = 16; o > 0; o >>= 1) count += __shfl_xor_sync(0xffffffffu, count, o);
+    }
+    if (lane == 0) act[h] = count;
+  }
+  __syncthreads();
+  // aggregate a_A = sum_{h in A} |w_h| q_h, prepared rows, folded weights
+  const float need_act = a.act_min * (float)ns;
+  for (int d = tid; d < D; d += kPlanThreads) {
+    float s = 0.0f;
+    for (int h = 0; h < H; ++h) {
+      const float wh = p.w[m * H + h];
+      if (ret_pos[h] < 0 && wh < 0.0f && ns > 0 && (float)act[h] >= need_act) s = __fmaf_rn(-wh, q[h * D + d], s);
+    }
+    aggv[d] = s;
+    qout[31 * D + d] = f_to_bf16_rn(s);
+  }
+  for (int i = tid; i < (kVec - 1) * D; i += kPlanThreads) {
+    const int r = i / D, d = i % D;
+    qout[i] = r < R ? qsrc[rlist[r] * D + d] : (uint16_t)0;
+  }
+  for (int r = tid; r < kVec; r += kPlanThreads) {
+    float wf = 0.0f;
+    if (r < R) {
+      const int j = rlist[r];
+      wf = p.w[m * H + j];
+      for (int h = 0; h < H; ++h)
+        if (anchor[h] == j) wf = __fmaf_rn(p.w[m * H + h], beta[h], wf);
+    }
+    wout[r] = wf;
+  }
+  __syncthreads();
+  // margin: bf16 rounding distance of a_A, plus gamma * (sum |w_h| ||q_h|| + ||a_A||)
+  float e2 = 0.0f, a2 = 0.0f;
+  for (int d = tid; d < D; d += kPlanThreads) {
+    const float ad = bf16_to_f(f_to_bf16_rn(aggv[d])) - aggv[d];
+    e2 = __fmaf_rn(ad, ad, e2);
+    a2 = __fmaf_rn(aggv[d], aggv[d], a2);
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    e2 += __shfl_xor_sync(0xffffffffu, e2, o);
+    a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+  }
+  __shared__ float e2s[kPlanThreads / 32], a2s[kPlanThreads / 32];
+  if (lane == 0) {
+    e2s[wid] = e2;
+    a2s[wid] = a2;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float E2 = 0.0f, A2 = 0.0f;
+    for (int w = 0; w < nw; ++w) {
+      E2 += e2s[w];
+      A2 += a2s[w];
+    }
+    float c = 0.0f, W = 0.0f;
+    for (int h = 0; h < H; ++h) {
+      const float wh = p.w[m * H + h];
+      if (anchor[h] >= 0) c = __fmaf_rn(wh, dn[h], c);
+      W = __fmaf_rn(fabsf(wh), sqrtf(qn2[h]), W);
+    }
+    const float margin = __fsqrt_ru(E2) * (1.0f + 0.0009765625f) + a.gamma * (W + sqrtf(A2) * 1.01f);
+    a.coef[m] = (c + margin) * (1.0f + 1.0e-6f);
+  }
+}
+
+// --------------------------------------------------------------- merging --
+
+__global__ void clamp_cnt_kernel(const int32_t* cand_cnt, int32_t* cand_n, int64_t M, int64_t cap) {
+  for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < M; m += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t c = cand_cnt[m];
+    cand_n[m] = c < cap ? c : (int32_t)cap;
+  }
+}
+
+// Row m of the merge input: the seed top-K then the rescored candidates (those
+// below tau become -inf); also the fallback mask and the survivor count.
+__global__ void merge_rows_kernel(int64_t M, int K, int64_t cap, const int32_t* stop_ids, const float* stop_sc,
+                                  const int32_t* cand, const int32_t* cand_n, const float* cand_sc, const float* tau,
+                                  const int32_t* status, float* mrg_sc, int32_t* mrg_id, int32_t* mrg_len,
+                                  int32_t* fbmask, unsigned long long* survivors) {
+  const int64_t m = blockIdx.x;
+  const int64_t ld = K + cap;
+  const bool ok = status[m] == 0;
+  if (threadIdx.x == 0) {
+    mrg_len[m] = ok ? K + cand_n[m] : 0;
+    fbmask[m] = ok ? 0 : 1;
+  }
+  if (!ok) return;
+  for (int j = threadIdx.x; j < K; j += blockDim.x) {
+    mrg_sc[m * ld + j] = stop_sc[m * K + j];
+    mrg_id[m * ld + j] = stop_ids[m * K + j];
+  }
+  const float t = tau[m];
+  const int n = cand_n[m];
+  unsigned long long surv = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float s = cand_sc[m * cap + i];
+    const bool keep = s >= t;
+    surv += keep ? 1ull : 0ull;
+    mrg_sc[m * ld + K + i] = keep ? s : -__int_as_float(0x7f800000);
+    mrg_id[m * ld + K + i] = cand[m * cap + i];
+  }
+  for (int o = 16; o > 0; o >>= 1) surv += __shfl_xor_sync(0xffffffffu, surv, o);
+  if ((threadIdx.x & 31) == 0 && surv) atomicAdd(survivors, surv);
+}
+
+__global__ void stats_kernel(idx_problem p, const int32_t* seed_cnt, int shared_seeds, const int32_t* cand_cnt,
+                             const int32_t* status, const int32_t* active, dosa_stats* st, int32_t* row_status) {
+  unsigned long long pairs = 0, seeds = 0, cands = 0, fb = 0;
+  for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < p.M; m += (int64_t)gridDim.x * blockDim.x) {
+    int64_t off;
+    int len;
+    row_extent(p, m, &off, &len);
+    pairs += (unsigned long long)len;
+    if (active[m]) {
+      seeds += (unsigned long long)seed_cnt[shared_seeds ? 0 : m];
+      cands += (unsigned long long)cand_cnt[m];
+    }
+    const int s = status[m];
+    fb += s != 0 ? 1ull : 0ull;
+    if (row_status) row_status[m] = (s & 1) ? 1 : ((s & 2) ? 2 : 0);
+  }
+  if (!st) return;
+  for (int o = 16; o > 0; o >>= 1) {
+    pairs += __shfl_xor_sync(0xffffffffu, pairs, o);
+    seeds += __shfl_xor_sync(0xffffffffu, seeds, o);
+    cands += __shfl_xor_sync(0xffffffffu, cands, o);
+    fb += __shfl_xor_sync(0xffffffffu, fb, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&st->pairs, pairs);
+    atomicAdd(&st->seeds, seeds);
+    atomicAdd(&st->candidates, cands);
+    atomicAdd(&st->fallback_rows, fb);
+  }
+}
+
+// ------------------------------------------------------------- workspace --
+
+struct DosaWs {
+  uint32_t* bits;
+  int32_t* list;
+  int32_t* seed_cnt;
+  int32_t* seed_len;       // [M]: per-row seed count (the shared count broadcast)
+  int32_t* common;         // [1]
+  uint16_t* rep_q;
+  float* rep_w;
+  int32_t* rep_len;
+  float* rep_sc;
+  int32_t* rep_ids;
+  uint32_t* rep_count;
+  void* seed_keys;
+  float* seed_scale;
+  float* seed_sc;
+  int32_t* stop_ids;
+  float* stop_sc;
+  float* tau;
+  int32_t* status;
+  int32_t* active;
+  uint16_t* qprep;
+  float* wfold;
+  float* coef;
+  int32_t* cand;
+  int32_t* cand_cnt;
+  int32_t* cand_n;
+  float* cand_sc;
+  float* mrg_sc;
+  int32_t* mrg_id;
+  int32_t* mrg_len;
+  int32_t* fbmask;
+  unsigned long long* surv;
+  float* fb_scores;
+  char* tk_ws;
+  // (surv is the survivor counter used when the caller passes no stats)
+  size_t used;
+};
+
+struct DosaShape {
+  bool shared_keys, shared_seeds;
+  int64_t W;          // bitmap words per row
+  int64_t NS;         // seed list capacity per row
+  int64_t cap;        // candidate capacity per row
+  int64_t ldmax;      // max_key_len (>= 1)
+};
+
+static DosaShape dosa_shape(const idx_problem& p, int K, const dosa_params& dp, int seed_ld) {
+  DosaShape s;
+  s.shared_keys = p.key_off == nullptr;
+  s.shared_seeds = s.shared_keys && seed_ld == 0;
+  s.ldmax = p.max_key_len > 0 ? p.max_key_len : 1;
+  s.W = (s.ldmax + 31) / 32;
+  int64_t ns = seed_ld > 0 ? seed_ld : dp.n_seed;
+  if (ns < K) ns = K;
+  s.NS = ns < s.ldmax ? ns : s.ldmax;
+  if (s.NS < 1) s.NS = 1;
+  s.cap = dp.candidate_capacity > 0 ? dp.candidate_capacity : 1;
+  return s;
+}
+
+static DosaWs carve(void* base, const idx_problem& p, int K, const dosa_params& dp, int seed_ld) {
+  const DosaShape s = dosa_shape(p, K, dp, seed_ld);
+  const int64_t M = p.M;
+  const int64_t seed_rows = s.shared_seeds ? 1 : M;
+  WsCarver c(base);
+  DosaWs w;
+  w.bits = c.take<uint32_t>(seed_rows * s.W);
+  w.list = c.take<int32_t>(seed_rows * s.NS);
+  w.seed_cnt = c.take<int32_t>(seed_rows);
+  w.seed_len = c.take<int32_t>(M);
+  w.common = c.take<int32_t>(1);
+  w.rep_q = c.take<uint16_t>((size_t)4 * p.H * p.D);
+  w.rep_w = c.take<float>((size_t)4 * p.H);
+  w.rep_len = c.take<int32_t>(4);
+  w.rep_sc = c.take<float>((size_t)4 * s.ldmax);
+  w.rep_ids = c.take<int32_t>((size_t)4 * K);
+  w.rep_count = c.take<uint32_t>(s.ldmax);
+  const int row_bytes = p.k_dtype == IDX_FP8_E4M3 ? 128 : 256;
+  w.seed_keys = c.take<char>(s.shared_seeds ? (size_t)s.NS * row_bytes : 16);
+  w.seed_scale = c.take<float>(s.shared_seeds ? (size_t)s.NS : 1);
+  w.seed_sc = c.take<float>((size_t)M * s.NS);
+  w.stop_ids = c.take<int32_t>((size_t)M * K);
+  w.stop_sc = c.take<float>((size_t)M * K);
+  w.tau = c.take<float>(M);
+  w.status = c.take<int32_t>(M);
+  w.active = c.take<int32_t>(M);
+  w.qprep = c.take<uint16_t>((size_t)M * kVec * p.D);
+  w.wfold = c.take<float>((size_t)M * kVec);
+  w.coef = c.take<float>(M);
+  w.cand = c.take<int32_t>((size_t)M * s.cap);
+  w.cand_cnt = c.take<int32_t>(M);
+  w.cand_n = c.take<int32_t>(M);
+  w.cand_sc = c.take<float>((size_t)M * s.cap);
+  w.mrg_sc = c.take<float>((size_t)M * (K + s.cap));
+  w.mrg_id = c.take<int32_t>((size_t)M * (K + s.cap));
+  w.mrg_len = c.take<int32_t>(M);
+  w.fbmask = c.take<int32_t>(M);
+  w.surv = c.take<unsigned long long>(1);
+  w.fb_scores = c.take<float>((size_t)M * s.ldmax);
+  size_t tk = topk_dense_ws(M, (int)s.ldmax, K);
+  size_t tk2 = topk_dense_ws(M, (int)(K + s.cap), K);
+  size_t tk3 = topk_dense_ws(M, (int)s.NS, K);
+  tk = tk > tk2 ? tk : tk2;
+  tk = tk > tk3 ? tk : tk3;
+  w.tk_ws = c.take<char>(tk > 0 ? tk : 16);
+  w.used = c.used + 256;
+  return w;
+}
+
+bool dosa_supported(const idx_problem& p, const dosa_params& dp) {
+  return score_uses_tensor_cores(p) && dp.retained_heads < 32 && dp.retained_heads < p.H && dp.n_sample <= 128;
+}
+
+size_t dosa_ws(const idx_problem& p, int K, const dosa_params& dp, int seed_ld) {
+  if (!dosa_supported(p, dp)) return idx_topk_workspace_size(&p, K);
+  return carve(nullptr, p, K, dp, seed_ld).used;
+}
+
+static int grid_for(int64_t n, int threads) {
+  int64_t g = (n + threads - 1) / threads;
+  return (int)(g < 1 ? 1 : (g > 4096 ? 4096 : g));
+}
+
+#define DOSA_CHECK(x)                   \
+  do {                                  \
+    cudaError_t e_ = (x);               \
+    if (e_ != cudaSuccess) return e_;   \
+  } while (0)
+
+cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, const int32_t* seed_ids, int seed_ld,
+                        int32_t* out_ids, float* out_scores, int32_t* row_status, dosa_stats* stats, void* ws,
+                        size_t ws_bytes, cudaStream_t st) {
+  const int64_t M = p.M;
+  if (!dosa_supported(p, dp)) {
+    // exact path (the output contract is the unpruned top-K); every row counts as a fallback row
+    const int64_t ld = p.max_key_len > 0 ? p.max_key_len : 1;
+    WsCarver c(ws);
+    float* scores = c.take<float>((size_t)M * ld);
+    char* lists = c.take<char>(topk_dense_ws(M, p.max_key_len, K));
+    DOSA_CHECK(launch_score(p, scores, ld, st));
+    DOSA_CHECK(launch_topk_dense(scores, ld, nullptr, &p, M, p.max_key_len, K, out_ids, out_scores, lists, st));
+    if (row_status) DOSA_CHECK(fill_i32(row_status, M, 1, st));
+    return cudaSuccess;
+  }
+  const DosaShape s = dosa_shape(p, K, dp, seed_ld);
+  DosaWs w = carve(ws, p, K, dp, seed_ld);
+  if (w.used > ws_bytes) return cudaErrorInvalidValue;
+  const int64_t seed_rows = s.shared_seeds ? 1 : M;
+
+  // ---- seeds
+  DOSA_CHECK(fill_i32(w.bits, seed_rows * s.W, 0, st));
+  if (seed_ids) {
+    caller_seeds_kernel<<<(unsigned)M, 256, 0, st>>>(p, seed_ids, seed_ld, w.bits, s.W);
+  } else if (!s.shared_seeds) {
+    strided_seeds_kernel<<<(unsigned)M, 256, 0, st>>>(p, dp.n_seed, w.bits, s.W);
+  } else {
+    // cold rule over the common visible prefix
+    min_len_kernel<<<1, 1024, 0, st>>>(p, w.common);
+    Reps r{};
+    for (int i = 0; i < 4; ++i) {
+      const int64_t m = M > 1 ? ((int64_t)i * (M - 1)) / 3 : 0;
+      bool dup = false;
+      for (int j = 0; j < r.n; ++j) dup |= r.m[j] == m;
+      if (!dup) r.m[r.n++] = m;
+    }
+    gather_reps_kernel<<<(unsigned)r.n, 256, 0, st>>>(p, r, w.common, w.rep_q, w.rep_w, w.rep_len);
+    idx_problem sub = p;
+    sub.q = w.rep_q;
+    sub.w = w.rep_w;
+    sub.M = r.n;
+    sub.key_len = w.rep_len;
+    DOSA_CHECK(launch_score(sub, w.rep_sc, s.ldmax, st));
+    DOSA_CHECK(launch_topk_dense(w.rep_sc, s.ldmax, w.rep_len, nullptr, r.n, (int)s.ldmax, K, w.rep_ids, nullptr,
+                                 w.tk_ws, st));
+    DOSA_CHECK(fill_i32(w.rep_count, s.ldmax, 0, st));
+    rep_count_kernel<<<grid_for((int64_t)r.n * K, 256), 256, 0, st>>>(w.rep_ids, r.n, K, w.rep_count);
+    cold_select_kernel<<<1, kColdThreads, 0, st>>>(w.rep_count, w.rep_sc, s.ldmax, r.n, w.common, dp.n_seed, w.bits);
+  }
+  DOSA_CHECK(cudaGetLastError());
+  bits_to_list_kernel<<<(unsigned)seed_rows, kListThreads, 0, st>>>(w.bits, s.W, w.list, s.NS, w.seed_cnt);
+  DOSA_CHECK(cudaGetLastError());
+
+  // ---- seed scores, seed top-K, tau
+  if (s.shared_seeds) {
+    gather_keys_kernel<<<grid_for(s.NS * 16, 256), 256, 0, st>>>(p, w.list, w.seed_cnt, w.seed_keys,
+                                                                  p.key_scale ? w.seed_scale : nullptr);
+    broadcast_i32_kernel<<<grid_for(M, 256), 256, 0, st>>>(w.seed_cnt, w.seed_len, M);
+    idx_problem sp = p;
+    sp.keys = w.seed_keys;
+    sp.key_scale = p.key_scale ? w.seed_scale : nullptr;
+    sp.n_keys = s.NS;
+    sp.key_off = nullptr;
+    sp.key_len = w.seed_len;
+    sp.max_key_len = (int32_t)s.NS;
+    DOSA_CHECK(launch_score(sp, w.seed_sc, s.NS, st));
+  } else {
+    DOSA_CHECK(cudaMemcpyAsync(w.seed_len, w.seed_cnt, M * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    DOSA_CHECK(launch_score_gather(p, w.list, w.seed_cnt, s.NS, w.seed_sc, s.NS, nullptr, st));
+  }
+  DOSA_CHECK(launch_topk_dense(w.seed_sc, s.NS, w.seed_len, nullptr, M, (int)s.NS, K, w.stop_ids, w.stop_sc,
+                               w.tk_ws, st, w.list, s.shared_seeds ? 0 : s.NS));
+  seed_status_kernel<<<grid_for(M, 256), 256, 0, st>>>(M, K, w.seed_cnt, s.shared_seeds ? 1 : 0, w.stop_sc, w.tau,
+                                                       w.status, w.active);
+  DOSA_CHECK(cudaGetLastError());
+
+  // ---- planner
+  PlanArgs pa;
+  pa.p = p;
+  pa.R = dp.retained_heads;
+  pa.n_sample = dp.n_sample;
+  pa.act_min = dp.act_freq_min;
+  pa.gamma = dp.margin_gamma;
+  pa.seed_list = w.list;
+  pa.list_ld = s.NS;
+  pa.seed_cnt = w.seed_cnt;
+  pa.shared_seeds = s.shared_seeds ? 1 : 0;
+  pa.active = w.active;
+  pa.qprep = w.qprep;
+  pa.wfold = w.wfold;
+  pa.coef = w.coef;
+  const size_t psmem = ((size_t)p.H * p.D + (size_t)dp.n_sample * p.D + 4 * (size_t)p.H + p.D) * sizeof(float) +
+                       (3 * (size_t)p.H + 32) * sizeof(int);
+  DOSA_CHECK(cudaFuncSetAttribute(dosa_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem));
+  dosa_plan_kernel<<<(unsigned)M, kPlanThreads, psmem, st>>>(pa);
+  DOSA_CHECK(cudaGetLastError());
+
+  // ---- bound scan
+  DOSA_CHECK(fill_i32(w.cand_cnt, M, 0, st));
+  idx_problem prep = p;
+  prep.q = w.qprep;
+  prep.H = kVec;
+  DOSA_CHECK(launch_bound(prep, w.wfold, w.coef, w.tau, w.bits, s.shared_seeds ? 0 : s.W, w.cand, w.cand_cnt, s.cap,
+                          w.status, dp.retained_heads, w.active, st));
+
+  // ---- exact rescoring of the candidates, merge with the seed top-K
+  clamp_cnt_kernel<<<grid_for(M, 256), 256, 0, st>>>(w.cand_cnt, w.cand_n, M, s.cap);
+  DOSA_CHECK(launch_score_gather(p, w.cand, w.cand_n, s.cap, w.cand_sc, s.cap, w.active, st));
+  merge_rows_kernel<<<(unsigned)M, 256, 0, st>>>(M, K, s.cap, w.stop_ids, w.stop_sc, w.cand, w.cand_n, w.cand_sc,
+                                                  w.tau, w.status, w.mrg_sc, w.mrg_id, w.mrg_len, w.fbmask,
+                                                  stats ? &stats->survivors : w.surv);
+  DOSA_CHECK(cudaGetLastError());
+  DOSA_CHECK(launch_topk_dense(w.mrg_sc, K + s.cap, w.mrg_len, nullptr, M, (int)(K + s.cap), K, out_ids, out_scores,
+                               w.tk_ws, st, w.mrg_id, K + s.cap));
+
+  // ---- rows that could not be pruned: the unpruned path, only for them
+  DOSA_CHECK(launch_score(p, w.fb_scores, s.ldmax, st, w.fbmask));
+  DOSA_CHECK(launch_topk_dense(w.fb_scores, s.ldmax, nullptr, &p, M, (int)s.ldmax, K, out_ids, out_scores, w.tk_ws,
+                               st, nullptr, 0, w.fbmask));
+
+  stats_kernel<<<grid_for(M, 256), 256, 0, st>>>(p, w.seed_cnt, s.shared_seeds ? 1 : 0, w.cand_cnt, w.status,
+                                                 w.active, stats, row_status);
+  return cudaGetLastError();
+}
+
 }  // namespace idx

@@ -36,15 +36,31 @@ cudaError_t launch_witness_indices(const int32_t* ids, int64_t rows, int topk, c
 // row fits one chunk).  Rows come from lens[m] (clamped to [0, max_len]) or,
 // when p_or_null is given, from the problem's visible extents.
 size_t topk_dense_ws(int64_t M, int max_len, int K);
+// id_map (optional, [M, id_ld]): position i of row m stands for key id
+// id_map[m*id_ld + i] (id_ld 0: one map shared by all rows).  row_mask
+// (optional): rows with row_mask[m] == 0 are neither read nor written.
 cudaError_t launch_topk_dense(const float* scores, int64_t ld, const int32_t* lens, const idx_problem* p_or_null,
                               int64_t M, int max_len, int K, int32_t* out_ids, float* out_scores, void* ws,
-                              cudaStream_t st);
+                              cudaStream_t st, const int32_t* id_map = nullptr, int64_t id_ld = 0,
+                              const int32_t* row_mask = nullptr);
 
 // Scores of every visible key (the kernel family depends only on dtype/H/D).
-cudaError_t launch_score(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st);
+// row_mask (optional, device [M]): rows with row_mask[m] == 0 are skipped.
+cudaError_t launch_score(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st,
+                         const int32_t* row_mask = nullptr);
 bool score_uses_tensor_cores(const idx_problem& p);
-cudaError_t launch_score_simt(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st);
-cudaError_t launch_score_tc(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st);
+cudaError_t launch_score_simt(const idx_problem& p, float* scores, int64_t ld, const int32_t* row_mask,
+                              cudaStream_t st);
+cudaError_t launch_score_tc(const idx_problem& p, float* scores, int64_t ld, const int32_t* row_mask,
+                            cudaStream_t st);
+// Exact scores of per-row key lists (tensor-core shapes only): scores[m*ld + i]
+// for list position i < cnt[m] of row m, keys key_off[m] + list[m*gld + i].
+cudaError_t launch_score_gather(const idx_problem& p, const int32_t* list, const int32_t* cnt, int64_t gld,
+                                float* scores, int64_t ld, const int32_t* row_mask, cudaStream_t st);
+// DoSA bound scan over prepared vectors prep.q = [M, 32, 128] bf16.
+cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const float* coef, const float* tau,
+                         const uint32_t* seedbits, int64_t seed_stride, int32_t* cand, int32_t* cand_cnt,
+                         int64_t cap, int32_t* status, int R, const int32_t* row_mask, cudaStream_t st);
 
 size_t block_select_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c);
 cudaError_t launch_block_select(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv, int D,

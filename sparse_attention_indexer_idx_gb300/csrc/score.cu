@@ -13,9 +13,9 @@ bool score_uses_tensor_cores(const idx_problem& p) {
   return dt && hs && p.D == 128 && kTensorScoreEnabled;
 }
 
-cudaError_t launch_score(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st) {
-  if (score_uses_tensor_cores(p)) return launch_score_tc(p, scores, ld, st);
-  return launch_score_simt(p, scores, ld, st);
+cudaError_t launch_score(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st, const int32_t* row_mask) {
+  if (score_uses_tensor_cores(p)) return launch_score_tc(p, scores, ld, row_mask, st);
+  return launch_score_simt(p, scores, ld, row_mask, st);
 }
 
 }  // namespace idx

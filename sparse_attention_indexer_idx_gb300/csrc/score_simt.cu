@@ -50,13 +50,14 @@ __device__ __forceinline__ void stage_query(const idx_problem& p, int64_t m, flo
 
 template <int QDT, int KDT>
 __global__ void __launch_bounds__(kSimtThreads) score_simt_kernel(idx_problem p, float* __restrict__ scores,
-                                                                   int64_t ld) {
+                                                                   int64_t ld, const int32_t* __restrict__ row_mask) {
   extern __shared__ float qs[];   // [H*D] queries then [H] weights
   for (int64_t m = blockIdx.y; m < p.M; m += gridDim.y) {
     int64_t off;
     int len;
     bool ok = row_extent(p, m, &off, &len);
     if (!ok && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&g_device_error, DEVERR_BAD_ROW);
+    if (row_mask && !row_mask[m]) len = 0;
     if ((int64_t)blockIdx.x * kSimtThreads >= len) continue;   // uniform over the block
     __syncthreads();
     stage_query<QDT>(p, m, qs);
@@ -66,7 +67,8 @@ __global__ void __launch_bounds__(kSimtThreads) score_simt_kernel(idx_problem p,
   }
 }
 
-cudaError_t launch_score_simt(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st) {
+cudaError_t launch_score_simt(const idx_problem& p, float* scores, int64_t ld, const int32_t* row_mask,
+                              cudaStream_t st) {
   if (p.M <= 0 || p.max_key_len <= 0) return cudaSuccess;
   dim3 grid((unsigned)((p.max_key_len + kSimtThreads - 1) / kSimtThreads), (unsigned)(p.M < 65535 ? p.M : 65535));
   size_t smem = (size_t)(p.H * p.D + p.H) * sizeof(float);
@@ -75,12 +77,12 @@ cudaError_t launch_score_simt(const idx_problem& p, float* scores, int64_t ld, c
     e = cudaFuncSetAttribute(score_simt_kernel<IDX_F32, IDX_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    score_simt_kernel<IDX_F32, IDX_F32><<<grid, kSimtThreads, smem, st>>>(p, scores, ld);
+    score_simt_kernel<IDX_F32, IDX_F32><<<grid, kSimtThreads, smem, st>>>(p, scores, ld, row_mask);
   } else {
     e = cudaFuncSetAttribute(score_simt_kernel<IDX_BF16, IDX_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    score_simt_kernel<IDX_BF16, IDX_BF16><<<grid, kSimtThreads, smem, st>>>(p, scores, ld);
+    score_simt_kernel<IDX_BF16, IDX_BF16><<<grid, kSimtThreads, smem, st>>>(p, scores, ld, row_mask);
   }
   return cudaGetLastError();
 }

@@ -1,5 +1,5 @@
-// bf16-key instantiations of the tensor-core score kernel (score_tc.cuh) and
-// the tensor-map helper shared with the FP8 instantiations.
+// bf16-key dense instantiations of the tensor-core score kernel (score_tc.cuh)
+// and the tensor-map helper shared with the other instantiations.
 #include <cudaTypedefs.h>
 
 #include "score_tc.cuh"
@@ -32,20 +32,26 @@ bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, ui
   return r == CUDA_SUCCESS;
 }
 
-cudaError_t launch_score_tc_fp8(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st);
+cudaError_t launch_score_tc_fp8(const TcArgs& a, cudaStream_t st);
 
-cudaError_t launch_score_tc(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st) {
-  if (p.k_dtype == IDX_FP8_E4M3) return launch_score_tc_fp8(p, scores, ld, st);
+cudaError_t launch_score_tc(const idx_problem& p, float* scores, int64_t ld, const int32_t* row_mask,
+                            cudaStream_t st) {
+  TcArgs a{};
+  a.p = p;
+  a.scores = scores;
+  a.ld = ld;
+  a.row_mask = row_mask;
+  if (p.k_dtype == IDX_FP8_E4M3) return launch_score_tc_fp8(a, st);
   const bool shared = p.key_off == nullptr;
   switch (p.H) {
-    case 16: return shared ? launch_tc<TcCfg<IDX_BF16, 16, 16>>(p, scores, ld, st)
-                           : launch_tc<TcCfg<IDX_BF16, 16, 1>>(p, scores, ld, st);
-    case 32: return shared ? launch_tc<TcCfg<IDX_BF16, 32, 8>>(p, scores, ld, st)
-                           : launch_tc<TcCfg<IDX_BF16, 32, 1>>(p, scores, ld, st);
-    case 64: return shared ? launch_tc<TcCfg<IDX_BF16, 64, 4>>(p, scores, ld, st)
-                           : launch_tc<TcCfg<IDX_BF16, 64, 1>>(p, scores, ld, st);
-    case 128: return shared ? launch_tc<TcCfg<IDX_BF16, 128, 2>>(p, scores, ld, st)
-                            : launch_tc<TcCfg<IDX_BF16, 128, 1>>(p, scores, ld, st);
+    case 16: return shared ? launch_tc<TcCfg<IDX_BF16, 16, 16, kScore>>(a, st)
+                           : launch_tc<TcCfg<IDX_BF16, 16, 1, kScore>>(a, st);
+    case 32: return shared ? launch_tc<TcCfg<IDX_BF16, 32, 8, kScore>>(a, st)
+                           : launch_tc<TcCfg<IDX_BF16, 32, 1, kScore>>(a, st);
+    case 64: return shared ? launch_tc<TcCfg<IDX_BF16, 64, 4, kScore>>(a, st)
+                           : launch_tc<TcCfg<IDX_BF16, 64, 1, kScore>>(a, st);
+    case 128: return shared ? launch_tc<TcCfg<IDX_BF16, 128, 2, kScore>>(a, st)
+                            : launch_tc<TcCfg<IDX_BF16, 128, 1, kScore>>(a, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,32 +1,43 @@
-// Indexer score on the 5th-generation tensor cores (tcgen05, sm_103a):
-// s(k) = sum_h w_h ReLU(q_h . k) ("DoSA：用安全上界减少 Indexer 的完整打分",
-// section 3), for bf16 queries with bf16 keys or FP8 e4m3 keys (+ per-token
-// scale), D = 128.
+// Indexer score and DoSA bound on the 5th-generation tensor cores (tcgen05,
+// sm_103a), bf16 queries with bf16 keys or FP8 e4m3 keys (+ per-token scale),
+// D = 128.
 //
 // Mapping.  One MMA tile is 128 keys (the M axis: key i of the tile lives in
-// TMEM lane i) times N = NQ*H columns (NQ queries x H heads, all K-major), with
-// the full D = 128 as 8 MMAs of K = 16.  So each epilogue thread owns one key
-// and reduces its own TMEM columns, head by head, with no shuffles:
-//   s = fma(w_{H-1}, max(x_{H-1}, 0), ... fma(w_0, max(x_0, 0), 0)).
-// A (query, key) score therefore has the same bits wherever it is computed
-// (dense tile, gathered seed or survivor tile): same instruction shape, same
-// K order, same epilogue chain.
+// TMEM lane i) times N = NQ*NCOL columns (NQ queries x NCOL vectors each, all
+// K-major), the full D = 128 as 8 MMAs of K = 16.  Each epilogue thread owns
+// one key and reduces its own TMEM columns with no shuffles.
 //
-// Work units are (query group g, key tile t).  Shared keys (causal prefill):
-// a group is NQ = 256/H consecutive rows over one key sequence, N = 256.
-// Per-row keys (decode): a group is one row, N = H.  The units are split into
-// one contiguous range per CTA (persistent, one CTA per SM), balanced by the
-// exact tile count of every group, which a prologue warp scans from key_len.
+// Modes:
+//  kScore   s(k) = sum_h w_h ReLU(q_h . k) ("DoSA：用安全上界减少 Indexer 的完整
+//           打分", section 3), NCOL = H; the head sum is one fused-multiply-add
+//           chain h = 0..H-1, so a (query, key) score has the same bits
+//           wherever it is computed -- same instruction shape, same K order,
+//           same chain.
+//  kGather  the same score over per-row key lists: tile t of row m holds the
+//           keys list[m][t*128 + i], fetched by TMA tile::gather4 (four rows
+//           per instruction) straight into the swizzled tile.  Used to rescore
+//           DoSA candidates; output is indexed by list position.
+//  kBound   DoSA's safe upper bound (same page, sections 2, 3.1, 3.2): B holds
+//           per query R retained head vectors (rows 0..R-1) and the |w|-folded
+//           negative aggregate (row 31); the epilogue evaluates
+//             U = sum_j w'_j ReLU(q_j . k) + coef ||k|| - ReLU(a . k)
+//           (times the FP8 scale), with ||k|| read from the key tile in shared
+//           memory, and appends every visible non-seed key with U >= tau to the
+//           row's candidate list (drop only when U < tau).
+//
+// Work units are (query group g, key tile t).  Shared keys (causal prefill): a
+// group is NQ consecutive rows over one key sequence.  Per-row keys (decode,
+// gathered lists): a group is one row.  The units are split into one
+// contiguous range per CTA (persistent, one CTA per SM), balanced by the exact
+// tile count of every group, which a prologue warp scans from the lengths.
 //
 // Warp roles:  warp 0  TMA producer (key tiles, query tiles)
 //              warp 1  TMEM allocation + MMA issue (one thread)
-//              warps 2-5  epilogue: tcgen05.ld -> ReLU.w chain -> global
+//              warps 2-5  epilogue: tcgen05.ld -> score / bound -> global
 //              warps 6-9  (FP8 only) e4m3 -> f16 conversion of key tiles into
 //                         the swizzled MMA layout, bf16 -> f16 of query tiles
-// Rings: A (MMA-ready key tiles), RAW (FP8 tiles as loaded), B (query tiles),
-// ACC (TMEM accumulators).  Every wait is bounded (see common.cuh); on a
-// timeout all roles stop, the producer and the MMA thread drain what they
-// issued, and TMEM is released before exit.
+// Every wait is bounded (see common.cuh); on a timeout all roles stop, the
+// producer and the MMA thread drain what they issued, and TMEM is released.
 #pragma once
 
 #include <cuda.h>
@@ -36,24 +47,46 @@
 
 namespace idx {
 
+enum TcMode { kScore = 0, kGather = 1, kBound = 2 };
+
 struct TcArgs {
-  idx_problem p;
+  idx_problem p;              // p.q is the B source: queries, or prepared vectors (kBound)
   float* scores;
   int64_t ld;
   int64_t G;                  // groups
+  // kGather: row m's keys are key_base(m) + list[m*gld + i], i < cnt[m]
+  const int32_t* list;
+  const int32_t* cnt;
+  int64_t gld;
+  // kBound
+  const float* wfold;         // [M, 32] folded retained weights (j < R)
+  const float* coef;          // [M] c + margin, multiplies ||k||
+  const float* tau;           // [M]
+  const uint32_t* seedbits;   // seed bitmap, row stride seed_stride words (0: one shared bitmap)
+  int64_t seed_stride;
+  int32_t* cand;              // [M, cap] candidate ids
+  int32_t* cand_cnt;          // [M]
+  int64_t cap;
+  int32_t* status;            // [M] bit 1: candidate overflow
+  const int32_t* row_mask;    // optional [M]: rows with row_mask[m] == 0 are skipped
+  int R;
 };
 
 __host__ __device__ constexpr int tc_pow2_cols(int c) {
   return c <= 32 ? 32 : (c <= 64 ? 64 : (c <= 128 ? 128 : (c <= 256 ? 256 : 512)));
 }
 
-template <int KDT_, int H_, int NQ_>
+template <int KDT_, int NCOL_, int NQ_, int MODE_>
 struct TcCfg {
   static constexpr int KDT = KDT_;
-  static constexpr int H = H_;
+  static constexpr int NCOL = NCOL_;          // H (score) or 32 (bound)
+  static constexpr int H = NCOL_;
   static constexpr int NQ = NQ_;
+  static constexpr int MODE = MODE_;
   static constexpr bool FP8 = (KDT == IDX_FP8_E4M3);
-  static constexpr int N = NQ * H;
+  static constexpr bool GATHER = (MODE == kGather);
+  static constexpr bool BOUND = (MODE == kBound);
+  static constexpr int N = NQ * NCOL;
   static constexpr int A_BYTES = 128 * 128 * 2;
   static constexpr int B_BYTES = N * 128 * 2;
   static constexpr int RAW_BYTES = 128 * 128;
@@ -72,7 +105,8 @@ struct TcCfg {
   static constexpr int OFF_W = OFF_RAW + SRAW * RAW_BYTES;
   static constexpr int OFF_BASE = OFF_W + 4 * N * 4;
   static constexpr int OFF_LEN = OFF_BASE + 4 * NQ * 8;
-  static constexpr int OFF_BAR = ((OFF_LEN + 4 * NQ * 4) + 7) & ~7;
+  static constexpr int OFF_AUX = OFF_LEN + 4 * NQ * 4;         // coef, tau per query (bound)
+  static constexpr int OFF_BAR = ((OFF_AUX + 4 * NQ * 8) + 7) & ~7;
   static constexpr int NBARS = 2 * SA + 3 * SB + 2 * SRAW + 2 * SACC + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
@@ -89,6 +123,11 @@ struct TcSched {
 // ------------------------------------------------------------ group helpers --
 template <class C>
 __device__ __forceinline__ int64_t tc_group_tiles(const TcArgs& A, int64_t g, bool report = false) {
+  if (C::GATHER) {
+    if (A.row_mask && !A.row_mask[g]) return 0;
+    const int32_t c = A.cnt[g];
+    return c > 0 ? (c + 127) / 128 : 0;
+  }
   int mx = 0;
 #pragma unroll 1
   for (int q = 0; q < C::NQ; ++q) {
@@ -97,6 +136,7 @@ __device__ __forceinline__ int64_t tc_group_tiles(const TcArgs& A, int64_t g, bo
     int64_t off;
     int len;
     if (!row_extent(A.p, m, &off, &len) && report) atomicOr(&g_device_error, DEVERR_BAD_ROW);
+    if (A.row_mask && !A.row_mask[m]) len = 0;
     mx = len > mx ? len : mx;
   }
   return (mx + 127) / 128;
@@ -176,6 +216,24 @@ struct TcUnits {
   }
 };
 
+// Key-row base of row m's key sequence (per-row keys: key_off, else 0).
+__device__ __forceinline__ int64_t tc_key_base(const TcArgs& A, int64_t m) {
+  if (!A.p.key_off) return 0;
+  int64_t off;
+  int len;
+  row_extent(A.p, m, &off, &len);
+  return off;
+}
+
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y0,
+                                            int32_t y1, int32_t y2, int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+      "%5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
 // ------------------------------------------------------------- the kernel ---
 template <class C>
 __global__ void __launch_bounds__(C::NTHREADS, 1)
@@ -190,6 +248,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   float* sW_all = reinterpret_cast<float*>(smem + C::OFF_W);
   int32_t* sLen_all = reinterpret_cast<int32_t*>(smem + C::OFF_LEN);
   int64_t* sBase_all = reinterpret_cast<int64_t*>(smem + C::OFF_BASE);
+  float* sAux_all = reinterpret_cast<float*>(smem + C::OFF_AUX);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* a_full = bars;
   uint64_t* a_empty = a_full + C::SA;
@@ -213,7 +272,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::SA; ++i) {
       mbar_init(&a_full[i], C::FP8 ? kConvThreads : 1);
-      mbar_init(&a_empty[i], 1);
+      // the bound epilogue reads ||k|| from the key tile, so its 4 warps also release it
+      mbar_init(&a_empty[i], C::BOUND ? 5 : 1);
     }
     for (int i = 0; i < C::SB; ++i) {
       mbar_init(&b_full[i], C::FP8 ? kConvThreads : 1);
@@ -248,50 +308,77 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      TcUnits<C> u;
-      u.init(args, s);
-      int64_t cur_g = -1;
-      uint32_t na = 0, nb = 0, nr = 0;
-      while (u.valid()) {
-        if (u.g != cur_g) {
-          cur_g = u.g;
-          const int bs = nb % C::SB;
-          if (!mbar_wait(&b_empty[bs], ((nb / C::SB) & 1) ^ 1, abort_flag)) break;
-          uint64_t* bar = C::FP8 ? &b_loaded[bs] : &b_full[bs];
-          mbar_arrive_expect_tx(bar, C::B_BYTES);
-          const int32_t y = (int32_t)(cur_g * C::N);
-          tma_load_2d(sB + bs * C::B_BYTES, &tmap_q, bar, 0, y);
-          tma_load_2d(sB + bs * C::B_BYTES + C::B_BYTES / 2, &tmap_q, bar, 64, y);
-          ++nb;
-        }
-        {
-          int64_t base = 0;
-          if (args.p.key_off) {
-            int64_t off;
-            int len;
-            row_extent(args.p, u.g, &off, &len);
-            base = off;
-          }
-          const int32_t y = (int32_t)(base + u.t * 128);
-          if (C::FP8) {
-            const int rs = nr % C::SRAW_MOD;
-            if (!mbar_wait(&raw_empty[rs], ((nr / C::SRAW_MOD) & 1) ^ 1, abort_flag)) break;
-            mbar_arrive_expect_tx(&raw_full[rs], C::RAW_BYTES);
-            tma_load_2d(sRaw + rs * C::RAW_BYTES, &tmap_k, &raw_full[rs], 0, y);
-            ++nr;
-          } else {
-            const int as = na % C::SA;
-            if (!mbar_wait(&a_empty[as], ((na / C::SA) & 1) ^ 1, abort_flag)) break;
-            mbar_arrive_expect_tx(&a_full[as], C::A_BYTES);
-            tma_load_2d(sA + as * C::A_BYTES, &tmap_k, &a_full[as], 0, y);
-            tma_load_2d(sA + as * C::A_BYTES + C::A_BYTES / 2, &tmap_k, &a_full[as], 64, y);
-            ++na;
+    TcUnits<C> u;
+    u.init(args, s);
+    int64_t cur_g = -1;
+    uint32_t na = 0, nb = 0, nr = 0;
+    while (u.valid()) {
+      if (u.g != cur_g) {
+        cur_g = u.g;
+        const int bs = nb % C::SB;
+        bool ok = true;
+        if (lane == 0) {
+          ok = mbar_wait(&b_empty[bs], ((nb / C::SB) & 1) ^ 1, abort_flag);
+          if (ok) {
+            uint64_t* bar = C::FP8 ? &b_loaded[bs] : &b_full[bs];
+            mbar_arrive_expect_tx(bar, C::B_BYTES);
+            const int32_t y = (int32_t)(cur_g * C::N);
+            tma_load_2d(sB + bs * C::B_BYTES, &tmap_q, bar, 0, y);
+            tma_load_2d(sB + bs * C::B_BYTES + C::B_BYTES / 2, &tmap_q, bar, 64, y);
           }
         }
-        u.advance();
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        ++nb;
       }
-      // drain: the last phase issued on every ring slot has landed
+      // the ring slot this tile goes to, and its barrier
+      uint8_t* dst;
+      uint64_t* fbar;
+      bool ok = true;
+      if (C::FP8) {
+        const int rs = nr % C::SRAW_MOD;
+        if (lane == 0) ok = mbar_wait(&raw_empty[rs], ((nr / C::SRAW_MOD) & 1) ^ 1, abort_flag);
+        dst = sRaw + rs * C::RAW_BYTES;
+        fbar = &raw_full[rs];
+      } else {
+        const int as = na % C::SA;
+        if (lane == 0) ok = mbar_wait(&a_empty[as], ((na / C::SA) & 1) ^ 1, abort_flag);
+        dst = sA + as * C::A_BYTES;
+        fbar = &a_full[as];
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const uint32_t tile_bytes = C::FP8 ? C::RAW_BYTES : C::A_BYTES;
+      if (C::GATHER) {
+        // lane l fetches tile rows 4l..4l+3 (list positions t*128 + 4l + i)
+        const int64_t m = u.g;
+        const int64_t base = tc_key_base(args, m);
+        const int32_t cntm = args.cnt[m];
+        const int32_t* lst = args.list + m * args.gld + u.t * 128;
+        int32_t y[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int pos = (int)(u.t * 128) + 4 * lane + i;
+          int64_t id = pos < cntm ? (int64_t)lst[4 * lane + i] : 0;
+          int64_t row = base + id;
+          row = row < 0 ? 0 : (row >= args.p.n_keys ? args.p.n_keys - 1 : row);
+          y[i] = (int32_t)row;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(fbar, tile_bytes);
+        __syncwarp();
+        tma_gather4(dst + lane * 512, &tmap_k, fbar, 0, y[0], y[1], y[2], y[3]);
+        if (!C::FP8) tma_gather4(dst + C::A_BYTES / 2 + lane * 512, &tmap_k, fbar, 64, y[0], y[1], y[2], y[3]);
+      } else if (lane == 0) {
+        const int32_t y = (int32_t)(tc_key_base(args, u.g) + u.t * 128);
+        mbar_arrive_expect_tx(fbar, tile_bytes);
+        tma_load_2d(dst, &tmap_k, fbar, 0, y);
+        if (!C::FP8) tma_load_2d(dst + C::A_BYTES / 2, &tmap_k, fbar, 64, y);
+      }
+      __syncwarp();
+      if (C::FP8) ++nr;
+      else ++na;
+      u.advance();
+    }
+    // drain: the last phase issued on every ring slot has landed
+    if (lane == 0) {
       for (uint32_t i = 0; i < (uint32_t)C::SB && i < nb; ++i) {
         uint32_t j = nb - 1 - i;
         mbar_wait(C::FP8 ? &b_loaded[j % C::SB] : &b_full[j % C::SB], (j / C::SB) & 1, no_abort);
@@ -361,6 +448,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     float* sW = sW_all + quarter * C::N;
     int32_t* sLen = sLen_all + quarter * C::NQ;
     int64_t* sBase = sBase_all + quarter * C::NQ;
+    float* sAux = sAux_all + quarter * C::NQ * 2;
     TcUnits<C> u;
     u.init(args, s);
     int64_t cur_g = -1;
@@ -370,16 +458,30 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         cur_g = u.g;
         __syncwarp();
         for (int i = lane; i < C::N; i += 32) {
-          const int64_t m = cur_g * C::NQ + i / C::H;
-          sW[i] = (m < args.p.M) ? args.p.w[m * C::H + (i % C::H)] : 0.0f;
+          const int64_t m = cur_g * C::NQ + i / C::NCOL;
+          float wv = 0.0f;
+          if (m < args.p.M) wv = C::BOUND ? args.wfold[m * 32 + (i % 32)] : args.p.w[m * C::H + (i % C::H)];
+          sW[i] = wv;
         }
         if (lane < C::NQ) {
           const int64_t m = cur_g * C::NQ + lane;
           int64_t off = 0;
           int len = 0;
-          if (m < args.p.M) row_extent(args.p, m, &off, &len);
+          if (m < args.p.M) {
+            if (C::GATHER) {
+              len = args.cnt[m];
+              off = tc_key_base(args, m);
+            } else {
+              row_extent(args.p, m, &off, &len);
+            }
+            if (args.row_mask && !args.row_mask[m]) len = 0;
+          }
           sLen[lane] = len;
           sBase[lane] = off;
+          if (C::BOUND) {
+            sAux[2 * lane] = m < args.p.M ? args.coef[m] : 0.0f;
+            sAux[2 * lane + 1] = m < args.p.M ? args.tau[m] : 0.0f;
+          }
         }
         __syncwarp();
       }
@@ -389,31 +491,97 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const int key = (int)(u.t * 128) + row_in_tile;
+      float knorm = 0.0f;
+      if (C::BOUND) {
+        // ||k|| of this lane's key from the MMA-ready tile (128-byte swizzle), then release the tile
+        const uint8_t* at = sA + (nacc % C::SA) * C::A_BYTES;
+        float ss = 0.0f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(at + h * (C::A_BYTES / 2) + row_in_tile * 128 +
+                                                            ((c ^ (row_in_tile & 7)) << 4));
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float lo, hi;
+              if (C::FP8) {
+                const __half2 h2 = *reinterpret_cast<const __half2*>(&w4[e]);
+                lo = __low2float(h2);
+                hi = __high2float(h2);
+              } else {
+                lo = __uint_as_float(w4[e] << 16);
+                hi = __uint_as_float(w4[e] & 0xffff0000u);
+              }
+              ss = __fmaf_rn(lo, lo, ss);
+              ss = __fmaf_rn(hi, hi, ss);
+            }
+          }
+        }
+        knorm = __fsqrt_ru(ss);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_empty[nacc % C::SA]);
+      }
 #pragma unroll 1
       for (int qi = 0; qi < C::NQ; ++qi) {
         const int64_t m = cur_g * C::NQ + qi;
         if (m >= args.p.M) break;
-        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::N + qi * C::H);
-        const float* wq = sW + qi * C::H;
-        float sc = 0.0f;
-#pragma unroll
-        for (int c = 0; c < C::H; c += 32) {
-          uint32_t v[32];
-          if (C::H >= 32) {
-            tmem_ld_32x32b_x32(tcol + c, v);
-          } else {
-            tmem_ld_32x32b_x16(tcol + c, v);
-          }
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < (C::H < 32 ? C::H : 32); ++j)
-            sc = __fmaf_rn(wq[c + j], fmaxf(__uint_as_float(v[j]), 0.0f), sc);
-        }
+        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::N + qi * C::NCOL);
+        const float* wq = sW + qi * C::NCOL;
         const int len = sLen[qi];
-        if (key < len) {
-          float outv = sc;
-          if (C::FP8) outv = sc * args.p.key_scale[sBase[qi] + key];
-          args.scores[m * args.ld + key] = outv;
+        if (!C::BOUND) {
+          float sc = 0.0f;
+#pragma unroll
+          for (int c = 0; c < C::H; c += 32) {
+            uint32_t v[32];
+            if (C::H >= 32) {
+              tmem_ld_32x32b_x32(tcol + c, v);
+            } else {
+              tmem_ld_32x32b_x16(tcol + c, v);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < (C::H < 32 ? C::H : 32); ++j)
+              sc = __fmaf_rn(wq[c + j], fmaxf(__uint_as_float(v[j]), 0.0f), sc);
+          }
+          if (key < len) {
+            float outv = sc;
+            if (C::FP8) {
+              const int64_t kid = C::GATHER ? (int64_t)args.list[m * args.gld + key] : (int64_t)key;
+              outv = sc * args.p.key_scale[sBase[qi] + kid];
+            }
+            args.scores[m * args.ld + key] = outv;
+          }
+        } else {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tcol, v);
+          tmem_ld_wait();
+          const int R = args.R;
+          float ub = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 31; ++j)
+            if (j < R) ub = __fmaf_rn(wq[j], fmaxf(__uint_as_float(v[j]), 0.0f), ub);
+          ub = __fmaf_rn(sAux[2 * qi], knorm, ub);
+          ub = ub - fmaxf(__uint_as_float(v[31]), 0.0f);
+          bool is_cand = false;
+          if (key < len) {
+            if (C::FP8) ub = ub * args.p.key_scale[sBase[qi] + key];
+            const uint32_t* bits = args.seedbits + (args.seed_stride ? m * args.seed_stride : 0);
+            const bool seed = (bits[key >> 5] >> (key & 31)) & 1u;
+            is_cand = !seed && !(ub < sAux[2 * qi + 1]);
+          }
+          const unsigned mask = __ballot_sync(0xffffffffu, is_cand);
+          if (mask) {
+            int32_t basepos = 0;
+            if (lane == 0) basepos = atomicAdd(&args.cand_cnt[m], __popc(mask));
+            basepos = __shfl_sync(0xffffffffu, basepos, 0);
+            if (lane == 0 && basepos + __popc(mask) > args.cap) atomicOr(&args.status[m], 2);
+            if (is_cand) {
+              const int64_t pos = basepos + __popc(mask & ((1u << lane) - 1u));
+              if (pos < args.cap) args.cand[m * args.cap + pos] = key;
+            }
+          }
         }
       }
       tc_fence_before();
@@ -495,30 +663,27 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   }
 }
 
-}  // namespace idx
-
-namespace idx {
-
 // 2-D tensor map over a row-major [rows, inner] matrix, 128-byte swizzle.
 bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
 
+// Launches one configuration.  B rows are a.p.q viewed as [M * NCOL, 128] bf16.
 template <class C>
-cudaError_t launch_tc(const idx_problem& p, float* scores, int64_t ld, cudaStream_t st) {
-  if (p.M <= 0 || p.n_keys <= 0 || p.max_key_len <= 0) return cudaSuccess;
-  if (p.n_keys >= ((int64_t)1 << 31) || p.M * p.H >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+cudaError_t launch_tc(const TcArgs& a_in, cudaStream_t st) {
+  TcArgs a = a_in;
+  const idx_problem& p = a.p;
+  if (p.M <= 0 || p.n_keys <= 0) return cudaSuccess;
+  if (!C::GATHER && p.max_key_len <= 0) return cudaSuccess;
+  if (p.n_keys >= ((int64_t)1 << 31) || p.M * C::NCOL >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
   CUtensorMap tk, tq;
   bool ok;
+  const uint32_t krows = C::GATHER ? 1u : 128u;     // gather4 wants a one-row box
   if (C::FP8)
-    ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.keys, 128, (uint64_t)p.n_keys, 128, 128, 128);
+    ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.keys, 128, (uint64_t)p.n_keys, 128, 128, krows);
   else
-    ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.keys, 128, (uint64_t)p.n_keys, 256, 64, 128);
-  ok = ok && make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, 128, (uint64_t)(p.M * p.H), 256, 64, C::N);
+    ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.keys, 128, (uint64_t)p.n_keys, 256, 64, krows);
+  ok = ok && make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, 128, (uint64_t)(p.M * C::NCOL), 256, 64, C::N);
   if (!ok) return cudaErrorInvalidValue;
-  TcArgs a;
-  a.p = p;
-  a.scores = scores;
-  a.ld = ld;
   a.G = (p.M + C::NQ - 1) / C::NQ;
   cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;

@@ -1,0 +1,31 @@
+// DoSA bound-scan instantiations of the tensor-core kernel (score_tc.cuh):
+// 32 prepared vectors per query (R retained heads + the negative aggregate),
+// 8 queries per tile over shared keys, one query per tile over per-row keys.
+#include "score_tc.cuh"
+
+namespace idx {
+
+cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const float* coef, const float* tau,
+                         const uint32_t* seedbits, int64_t seed_stride, int32_t* cand, int32_t* cand_cnt,
+                         int64_t cap, int32_t* status, int R, const int32_t* row_mask, cudaStream_t st) {
+  TcArgs a{};
+  a.p = prep;
+  a.wfold = wfold;
+  a.coef = coef;
+  a.tau = tau;
+  a.seedbits = seedbits;
+  a.seed_stride = seed_stride;
+  a.cand = cand;
+  a.cand_cnt = cand_cnt;
+  a.cap = cap;
+  a.status = status;
+  a.R = R;
+  a.row_mask = row_mask;
+  const bool shared = prep.key_off == nullptr;
+  if (prep.k_dtype == IDX_FP8_E4M3)
+    return shared ? launch_tc<TcCfg<IDX_FP8_E4M3, 32, 8, kBound>>(a, st)
+                  : launch_tc<TcCfg<IDX_FP8_E4M3, 32, 1, kBound>>(a, st);
+  return shared ? launch_tc<TcCfg<IDX_BF16, 32, 8, kBound>>(a, st) : launch_tc<TcCfg<IDX_BF16, 32, 1, kBound>>(a, st);
+}
+
+}  // namespace idx

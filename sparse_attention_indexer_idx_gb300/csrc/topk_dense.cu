@@ -288,11 +288,13 @@ __device__ uint32_t smem_radix_select(TkShared& sh, int cn, uint32_t want, F f, 
 __global__ void __launch_bounds__(TK_NT, 1)
     topk_chunk_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ lens,
                       idx_problem p, int use_p, int max_len, int K, int P, int32_t* __restrict__ out_ids,
-                      float* __restrict__ out_scores, uint64_t* __restrict__ lists, int n_chunks) {
+                      float* __restrict__ out_scores, uint64_t* __restrict__ lists, int n_chunks,
+                      const int32_t* __restrict__ id_map, int64_t id_ld, const int32_t* __restrict__ row_mask) {
   extern __shared__ __align__(16) uint8_t tk_smem[];
   TkShared& sh = *reinterpret_cast<TkShared*>(tk_smem);
   const int64_t m = blockIdx.x;
   const int c = blockIdx.y;
+  if (row_mask && !row_mask[m]) return;
   int n;
   if (use_p) {
     int64_t off;
@@ -307,6 +309,8 @@ __global__ void __launch_bounds__(TK_NT, 1)
   const int cn = (int)min((int64_t)TK_CH, (int64_t)n - base > 0 ? (int64_t)n - base : 0);
   const float* row = scores + m * ld + base;
   const int tid = threadIdx.x;
+  const int32_t* idm = id_map ? id_map + m * id_ld + base : nullptr;
+  auto idof = [&](int i) { return idm ? idm[i] : (int32_t)(base + i); };
 
   // stage the chunk as ordered keys in shared memory (8 loads in flight per thread)
   uint32_t* K_ = sh.keys;
@@ -329,14 +333,14 @@ __global__ void __launch_bounds__(TK_NT, 1)
   auto compact = [&](uint32_t T, uint32_t KT, uint32_t IT, bool exact_ids) {
     auto take = [&](int i) {
       const uint32_t kk = K_[i];
-      return exact_ids ? (kk > KT || (kk == KT && id_key((int32_t)(base + i)) >= IT)) : kk >= T;
+      return exact_ids ? (kk > KT || (kk == KT && id_key(idof(i)) >= IT)) : kk >= T;
     };
     uint32_t local = 0;
     for (int i = tid; i < cn; i += TK_NT) local += take(i) ? 1u : 0u;
     uint32_t total;
     uint32_t off = block_excl_scan(local, sh.red, &total);
     for (int i = tid; i < cn; i += TK_NT)
-      if (take(i) && off < TK_CAP) sh.cand[off++] = composite(K_[i], (int32_t)(base + i));
+      if (take(i) && off < TK_CAP) sh.cand[off++] = composite(K_[i], idof(i));
     if (tid == 0) sh.cnt = total;
     __syncthreads();
   };
@@ -396,7 +400,7 @@ __global__ void __launch_bounds__(TK_NT, 1)
       uint32_t IT = 0;
       if (eq != need) {
         auto tie = [&](int i) { return K_[i] == KT; };
-        auto idk = [&](int i) { return id_key((int32_t)(base + i)); };
+        auto idk = [&](int i) { return id_key(idof(i)); };
         uint32_t above2, eq2;
         IT = smem_radix_select(sh, cn, need, idk, tie, &above2, &eq2);
       }
@@ -435,12 +439,13 @@ __global__ void __launch_bounds__(TK_NT, 1)
 __global__ void __launch_bounds__(TK_NT, 1)
     topk_merge_kernel(const int32_t* __restrict__ lens, idx_problem p, int use_p, int max_len, int K, int P,
                       const uint64_t* __restrict__ lists, int n_chunks, int32_t* __restrict__ out_ids,
-                      float* __restrict__ out_scores) {
+                      float* __restrict__ out_scores, const int32_t* __restrict__ row_mask) {
   extern __shared__ __align__(16) uint8_t tk_smem[];
   TkShared& sh = *reinterpret_cast<TkShared*>(tk_smem);
   uint64_t* pair = reinterpret_cast<uint64_t*>(sh.keys);   // [best P | chunk P]
   uint64_t* best = sh.cand;
   const int64_t m = blockIdx.x;
+  if (row_mask && !row_mask[m]) return;
   int n;
   if (use_p) {
     int64_t off;
@@ -483,7 +488,7 @@ size_t topk_dense_ws(int64_t M, int max_len, int K) {
 
 cudaError_t launch_topk_dense(const float* scores, int64_t ld, const int32_t* lens, const idx_problem* p_or_null,
                               int64_t M, int max_len, int K, int32_t* out_ids, float* out_scores, void* ws,
-                              cudaStream_t st) {
+                              cudaStream_t st, const int32_t* id_map, int64_t id_ld, const int32_t* row_mask) {
   if (M <= 0) return cudaSuccess;
   const int P = pow2_at_least(K);
   const int n_chunks = max_len > 0 ? (max_len + TK_CH - 1) / TK_CH : 1;
@@ -495,14 +500,13 @@ cudaError_t launch_topk_dense(const float* scores, int64_t ld, const int32_t* le
   if (n_chunks > 65535) return cudaErrorInvalidValue;
   dim3 grid((unsigned)M, (unsigned)n_chunks);
   topk_chunk_kernel<<<grid, TK_NT, smem, st>>>(scores, ld, lens, p, p_or_null ? 1 : 0, max_len, K, P, out_ids,
-                                               out_scores, (uint64_t*)ws, n_chunks);
+                                               out_scores, (uint64_t*)ws, n_chunks, id_map, id_ld, row_mask);
   e = cudaGetLastError();
   if (e != cudaSuccess || n_chunks == 1) return e;
-  const size_t msmem = sizeof(TkShared);
-  e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+  e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  topk_merge_kernel<<<(unsigned)M, TK_NT, msmem, st>>>(lens, p, p_or_null ? 1 : 0, max_len, K, P, (const uint64_t*)ws,
-                                                       n_chunks, out_ids, out_scores);
+  topk_merge_kernel<<<(unsigned)M, TK_NT, smem, st>>>(lens, p, p_or_null ? 1 : 0, max_len, K, P, (const uint64_t*)ws,
+                                                      n_chunks, out_ids, out_scores, row_mask);
   return cudaGetLastError();
 }
 

@@ -225,12 +225,15 @@ def decode_bf16(seed: int = 2, M: int = 64, H: int = 32, D: int = 128, L: int = 
 
 def prefill_bf16(seed: int = 3, n_queries: int = 4096, H: int = 64, D: int = 128,
                  L: int = 65536, K: int = 2048, n_centres: int = 64, sigma: float = 0.3,
-                 n_seed: int = 12288, R: int = 16) -> IndexerProblem:
+                 n_seed: int = 12288, R: int = 16, q_noise: Optional[float] = None) -> IndexerProblem:
     """Causal prefill: queries at positions L-n..L-1 over one shared key sequence.
 
     Keys: with probability 1/2 a cluster key c_z + sigma*eps (z uniform over
-    n_centres centres c ~ N(0, I)), otherwise N(0, I) noise.  q ~ N(0, 1),
-    w ~ N(0, 1/H).
+    n_centres centres c ~ N(0, I)), otherwise N(0, I) noise.  w ~ N(0, 1/H).
+    Queries: q ~ N(0, 1) when q_noise is None; otherwise the heads of query m
+    share one direction, q_{m,h} = a_{m,h} c_{z_m} + q_noise * eps with
+    a ~ N(0, 1) and z_m uniform over the centres (heads of a trained indexer
+    are strongly correlated; this is the structure the anchor bound uses).
     """
     rng = np.random.default_rng(seed)
     centres = _normal(rng, (n_centres, D))
@@ -239,12 +242,18 @@ def prefill_bf16(seed: int = 3, n_queries: int = 4096, H: int = 64, D: int = 128
     eps = _normal(rng, (L, D))
     kf = np.where(is_cluster[:, None], centres[z] + np.float32(sigma) * eps, eps).astype(np.float32)
     keys = _bulk_bf16(kf)
-    q = _bulk_bf16(_normal(rng, (n_queries, H, D)))
+    if q_noise is None:
+        q = _bulk_bf16(_normal(rng, (n_queries, H, D)))
+    else:
+        zq = rng.integers(0, n_centres, n_queries)
+        amp = _normal(rng, (n_queries, H))
+        qf = amp[:, :, None] * centres[zq][:, None, :] + np.float32(q_noise) * _normal(rng, (n_queries, H, D))
+        q = _bulk_bf16(qf.astype(np.float32))
     w = _normal(rng, (n_queries, H), std=float(np.sqrt(1.0 / H)))
     pos = np.arange(L - n_queries, L, dtype=np.int64)
     key_len = (pos + 1).astype(np.int32)
     return IndexerProblem("prefill_bf16", "bf16", q, w, keys, key_len, None, K,
-                          extras=dict(n_seed=n_seed, R=R, pos=pos))
+                          extras=dict(n_seed=n_seed, R=R, pos=pos, q_noise=q_noise))
 
 
 def ragged_fp8(seed: int = 5, M: int = 128, H: int = 64, D: int = 128, L_min: int = 4096,

@@ -1,0 +1,140 @@
+"""DoSA pruning on the GPU: dosa_topk must equal idx_topk bit for bit (ids and
+score bits) on the same inputs, on every path (cold / strided / caller seeds,
+bf16 / FP8 keys, shared / per-row keys, overflow and too-few-seed fallbacks,
+exact ties at tau); and both agree with the fp64 oracle up to the score
+tolerance."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import EPS, check_topk_row
+from oracle import dsa as odsa
+from sparse_attention_indexer_idx_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from sparse_attention_indexer_idx_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _unpruned(B, p, K):
+    ids = torch.empty((p.q.shape[0], K), dtype=torch.int32, device="cuda")
+    sc = torch.empty((p.q.shape[0], K), dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.idx_topk_workspace_size(p, K), dtype=torch.uint8, device="cuda")
+    B.idx_topk(p, K, ids, sc, ws)
+    return ids.cpu().numpy(), sc.cpu().numpy()
+
+
+def _pruned(B, p, K, seed_ids=None, **kw):
+    dp = B.make_dosa_params(**kw)
+    M = p.q.shape[0]
+    ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    sc = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    st = torch.full((M,), -7, dtype=torch.int32, device="cuda")
+    stats = torch.zeros(5, dtype=torch.int64, device="cuda")
+    sld = 0 if seed_ids is None else seed_ids.shape[1]
+    ws = torch.empty(B.dosa_topk_workspace_size(p, K, dp, sld), dtype=torch.uint8, device="cuda")
+    B.dosa_topk(p, K, dp, ids, sc, ws, seed_ids=seed_ids, row_status=st, stats=stats)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), sc.cpu().numpy(), st.cpu().numpy(), stats.cpu().numpy()
+
+
+def _same(a_ids, a_sc, b_ids, b_sc):
+    assert np.array_equal(a_ids, b_ids)
+    assert np.array_equal(a_sc.view(np.uint32), b_sc.view(np.uint32))
+
+
+def _check_oracle(wp, ids, sc, rows):
+    for m in rows:
+        s_ref, a_ref = odsa.row_scores(wp, m)
+        check_topk_row(ids[m], sc[m], s_ref, a_ref, wp.K, EPS[wp.dtype])
+
+
+@pytest.mark.parametrize("q_noise", [0.1, None])
+def test_prefill_cold_seeds(B, q_noise):
+    wp = wl.prefill_bf16(seed=11, n_queries=40, H=64, D=128, L=6000, K=256, n_seed=1024, R=16, q_noise=q_noise)
+    p = B.problem_to_device(wp)
+    u_ids, u_sc = _unpruned(B, p, wp.K)
+    d_ids, d_sc, st, stats = _pruned(B, p, wp.K, n_seed=1024, retained_heads=16, candidate_capacity=6000)
+    _same(u_ids, u_sc, d_ids, d_sc)
+    assert (st == 0).all(), st
+    assert stats[0] == wp.pairs() and stats[1] == 1024 * wp.M
+    assert stats[3] <= stats[2]
+    _check_oracle(wp, d_ids, d_sc, [0, 17, 39])
+    if q_noise is not None:
+        assert stats[2] < 0.5 * (stats[0] - stats[1]), stats    # the bound prunes on structured heads
+    assert B.device_error() == 0
+
+
+@pytest.mark.parametrize("H,R", [(32, 16), (64, 20), (16, 8)])
+def test_decode_strided_seeds(B, H, R):
+    wp = wl.decode_bf16(seed=H + R, M=6, H=H, D=128, L=3000, K=128)
+    p = B.problem_to_device(wp)
+    u = _unpruned(B, p, wp.K)
+    d_ids, d_sc, st, stats = _pruned(B, p, wp.K, n_seed=512, retained_heads=R, candidate_capacity=3000)
+    _same(*u, d_ids, d_sc)
+    assert (st == 0).all()
+    assert B.device_error() == 0
+
+
+def test_ragged_fp8(B):
+    wp = wl.ragged_fp8(seed=8, M=7, H=64, D=128, L_min=300, L_max=5000, K=128, R=20)
+    p = B.problem_to_device(wp)
+    u = _unpruned(B, p, wp.K)
+    d_ids, d_sc, st, _ = _pruned(B, p, wp.K, n_seed=1024, retained_heads=20, candidate_capacity=5000)
+    _same(*u, d_ids, d_sc)
+    _check_oracle(wp, d_ids, d_sc, [0, 6])
+    assert B.device_error() == 0
+
+
+def test_caller_seeds_with_duplicates_and_junk(B):
+    wp = wl.decode_bf16(seed=5, M=4, H=32, D=128, L=2000, K=64)
+    p = B.problem_to_device(wp)
+    rng = np.random.default_rng(5)
+    seeds = rng.integers(-5, 2100, (4, 700)).astype(np.int32)      # duplicates, negatives, beyond L
+    u = _unpruned(B, p, wp.K)
+    d_ids, d_sc, st, stats = _pruned(B, p, wp.K, seed_ids=torch.from_numpy(seeds).cuda(), retained_heads=16,
+                                     candidate_capacity=2000)
+    _same(*u, d_ids, d_sc)
+    distinct = sum(len(set(x for x in row if 0 <= x < 2000)) for row in seeds)
+    assert stats[1] == distinct
+
+
+def test_overflow_and_too_few_seeds_fall_back(B):
+    wp = wl.decode_bf16(seed=6, M=5, H=32, D=128, L=2500, K=100)
+    p = B.problem_to_device(wp)
+    u = _unpruned(B, p, wp.K)
+    d_ids, d_sc, st, stats = _pruned(B, p, wp.K, n_seed=300, retained_heads=16, candidate_capacity=4)
+    _same(*u, d_ids, d_sc)
+    assert (st == 2).all() and stats[4] == 5
+    d_ids, d_sc, st, stats = _pruned(B, p, wp.K, n_seed=50, retained_heads=16, candidate_capacity=4000)
+    _same(*u, d_ids, d_sc)             # n_seed < K: every row on the unpruned path
+    assert (st == 1).all()
+
+
+def test_exact_ties_at_tau(B):
+    """Keys duplicated many times so that scores tie exactly at the threshold."""
+    wp = wl.decode_bf16(seed=9, M=3, H=32, D=128, L=1500, K=200)
+    rng = np.random.default_rng(9)
+    for m in range(3):
+        base = m * 1500
+        src = rng.integers(0, 1500, 60)
+        for k in range(1500):
+            wp.keys[base + k] = wp.keys[base + src[k % 60]]
+    p = B.problem_to_device(wp)
+    u = _unpruned(B, p, wp.K)
+    d_ids, d_sc, st, _ = _pruned(B, p, wp.K, n_seed=400, retained_heads=16, candidate_capacity=1500)
+    _same(*u, d_ids, d_sc)
+
+
+def test_unsupported_shape_takes_the_exact_path(B):
+    wp = wl.tiny_fp32()
+    p = B.problem_to_device(wp)
+    u = _unpruned(B, p, wp.K)
+    d_ids, d_sc, st, _ = _pruned(B, p, wp.K, n_seed=64, retained_heads=2)
+    _same(*u, d_ids, d_sc)
+    assert (st == 1).all()
