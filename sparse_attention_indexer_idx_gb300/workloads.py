@@ -232,7 +232,7 @@ def prefill_bf16(seed: int = 3, n_queries: int = 4096, H: int = 64, D: int = 128
     n_centres centres c ~ N(0, I)), otherwise N(0, I) noise.  w ~ N(0, 1/H).
     Queries: q ~ N(0, 1) when q_noise is None; otherwise the heads of query m
     share one direction, q_{m,h} = a_{m,h} c_{z_m} + q_noise * eps with
-    a ~ N(0, 1) and z_m uniform over the centres (heads of a trained indexer
+    a = |N(0, 1)| and z_m uniform over the centres (heads of a trained indexer
     are strongly correlated; this is the structure the anchor bound uses).
     """
     rng = np.random.default_rng(seed)
@@ -246,7 +246,7 @@ def prefill_bf16(seed: int = 3, n_queries: int = 4096, H: int = 64, D: int = 128
         q = _bulk_bf16(_normal(rng, (n_queries, H, D)))
     else:
         zq = rng.integers(0, n_centres, n_queries)
-        amp = _normal(rng, (n_queries, H))
+        amp = np.abs(_normal(rng, (n_queries, H)))
         qf = amp[:, :, None] * centres[zq][:, None, :] + np.float32(q_noise) * _normal(rng, (n_queries, H, D))
         q = _bulk_bf16(qf.astype(np.float32))
     w = _normal(rng, (n_queries, H), std=float(np.sqrt(1.0 / H)))
