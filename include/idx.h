@@ -231,6 +231,30 @@ idx_status block_select(const float* index_q, const float* index_k, const int32_
                         int32_t n_kv, int32_t D, int64_t L, const block_sparse_config* cfg, int32_t* out,
                         int32_t out_width, int32_t* out_count, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------ block_select_static
+ * block_select for callers that cannot allocate device memory: code that runs
+ * inside a host framework which owns every device allocation (and offers no
+ * allocator handle to plug-ins), or on a latency-critical path where a
+ * cudaMalloc could stall on the driver or fail under memory pressure.  No
+ * source page has a counterpart of this entry point; it is a deployment
+ * convenience with the same result as block_select.
+ *
+ * Identical arguments and output to block_select, minus (ws, ws_bytes): the
+ * per-(query, head, block) scratch lives in a fixed device array inside the
+ * library, 2^23 words (32 MiB), which every GPU that loads the library holds
+ * until the process exits.  Calls with Q * n_kv * ceil(L / block_size) above
+ * 2^23 are refused with IDX_ERR_WORKSPACE_TOO_SMALL before anything runs.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  Nothing is allocated: no cudaMalloc, cudaFree or allocating
+ * library routine is called.  All calls share the one array and it keeps the
+ * previous call's contents (every entry a call reads it has written first, so
+ * nothing needs clearing); calls that overlap on the GPU race on it, so
+ * serialise them (one stream, or events). */
+idx_status block_select_static(const float* index_q, const float* index_k, const int32_t* query_pos, int64_t Q,
+                               int32_t n_kv, int32_t D, int64_t L, const block_sparse_config* cfg, int32_t* out,
+                               int32_t out_width, int32_t* out_count, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

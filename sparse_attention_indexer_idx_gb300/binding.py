@@ -86,6 +86,10 @@ EXPORTS = {
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                       ctypes.POINTER(block_sparse_config), ctypes.c_void_p, ctypes.c_int32,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "block_select_static": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                             ctypes.POINTER(block_sparse_config), ctypes.c_void_p, ctypes.c_int32,
+                                             ctypes.c_void_p, ctypes.c_void_p]),
 }
 
 _lib = None
@@ -258,3 +262,14 @@ def problem_to_device(wp, device="cuda") -> Problem:
     key_off = None if wp.key_off is None else torch.from_numpy(np.ascontiguousarray(wp.key_off, dtype=np.int64)).to(device)
     key_scale = None if wp.key_scale is None else torch.from_numpy(np.ascontiguousarray(wp.key_scale)).to(device)
     return Problem(q, w, keys, key_len, int(np.max(wp.key_len)) if len(wp.key_len) else 0, key_off, key_scale)
+
+
+def block_select_static(index_q: torch.Tensor, index_k: torch.Tensor, query_pos: torch.Tensor,
+                        cfg: block_sparse_config, out: torch.Tensor, out_count: Optional[torch.Tensor], stream=None):
+    """block_select without a workspace: the scratch is a fixed array inside the
+    library (for callers that cannot allocate device memory)."""
+    Q, n_kv, D = index_q.shape
+    L = index_k.shape[0]
+    _check(lib().block_select_static(_ptr(index_q), _ptr(index_k), _ptr(query_pos), Q, n_kv, D, L,
+                                     ctypes.byref(cfg), _ptr(out), out.shape[-1], _ptr(out_count), _stream(stream)))
+    return out, out_count

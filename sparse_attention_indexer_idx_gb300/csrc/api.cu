@@ -24,7 +24,7 @@ void register_error_word(uint32_t (*take)()) {
 
 static thread_local std::string g_last_error;
 
-static idx_status fail(idx_status st, const char* fmt, ...) {
+idx_status fail(idx_status st, const char* fmt, ...) {
   char buf[512];
   va_list ap;
   va_start(ap, fmt);

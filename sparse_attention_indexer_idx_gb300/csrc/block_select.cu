@@ -15,6 +15,8 @@
 //  2. block_pick_kernel: per pair, forced blocks get the largest key, then the
 //     exact top-`budget` of (score desc, block asc) is taken and written in
 //     ascending block order.
+#include <mutex>
+
 #include "internal.h"
 #include "topk.cuh"
 
@@ -256,3 +258,76 @@ cudaError_t launch_block_select(const float* q, const float* k, const int32_t* p
 }
 
 }  // namespace idx
+
+// ---------------------------------------------------------------------------
+// block_select_static: the same selection with its block-score scratch in a
+// file-scope device array instead of a caller workspace, for callers that
+// cannot allocate device memory.  The array is part of the library's device
+// image: every GPU that loads the library holds kStaticBlockScores words of it
+// until the process exits.  Its device address is looked up once per device
+// (cudaGetSymbolAddress, with that device current) on the first call made on
+// that device.
+// ---------------------------------------------------------------------------
+
+namespace idx {
+
+constexpr int64_t kStaticBlockScores = (int64_t)1 << 23;   // 8 Mi words = 32 MiB
+static __device__ __align__(256) uint32_t g_block_scores_static[kStaticBlockScores];
+
+constexpr int kMaxStaticDevices = 64;
+static std::mutex g_static_mu;
+static void* g_static_ptr[kMaxStaticDevices];
+
+static idx_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "block_select_static: cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxStaticDevices)
+    return fail(IDX_ERR_UNSUPPORTED, "block_select_static: device ordinal %d above %d", dev, kMaxStaticDevices - 1);
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_block_scores_static);
+    if (e != cudaSuccess || !p)
+      return fail(IDX_ERR_CUDA, "block_select_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return IDX_OK;
+}
+
+}  // namespace idx
+
+extern "C" idx_status block_select_static(const float* index_q, const float* index_k, const int32_t* query_pos,
+                                          int64_t Q, int32_t n_kv, int32_t D, int64_t L,
+                                          const block_sparse_config* cfg, int32_t* out, int32_t out_width,
+                                          int32_t* out_count, void* stream) {
+  using namespace idx;
+  if (!cfg) return fail(IDX_ERR_INVALID_ARG, "config is NULL");
+  if (Q < 0 || n_kv < 0 || D <= 0 || L < 0 || cfg->block_size < 0 || cfg->top_blocks < 0 || cfg->init_blocks < 0 ||
+      cfg->local_blocks < 0)
+    return fail(IDX_ERR_INVALID_ARG, "negative size or config field");
+  const int64_t need_w = cfg->top_blocks > (int64_t)cfg->init_blocks + cfg->local_blocks
+                             ? cfg->top_blocks
+                             : (int64_t)cfg->init_blocks + cfg->local_blocks;
+  if (out_width < need_w || out_width > IDX_MAX_K)
+    return fail(IDX_ERR_INVALID_ARG, "out_width=%d must be in [max(top, init+local)=%lld, %d]", out_width,
+                (long long)need_w, IDX_MAX_K);
+  if (D > 256) return fail(IDX_ERR_UNSUPPORTED, "D=%d above 256", D);
+  if (D == 128 && (((uintptr_t)index_q | (uintptr_t)index_k) & 15))
+    return fail(IDX_ERR_INVALID_ARG, "index_q/index_k must be 16-byte aligned");
+  const int64_t words = (int64_t)(block_select_ws(Q, n_kv, L, *cfg) / sizeof(uint32_t));
+  if (words > kStaticBlockScores)
+    return fail(IDX_ERR_WORKSPACE_TOO_SMALL,
+                "block_select_static: Q*n_kv*ceil(L/block_size) = %lld block scores exceed the fixed %lld",
+                (long long)words, (long long)kStaticBlockScores);
+  if (Q * n_kv == 0) return IDX_OK;
+  if (!index_q || !query_pos || !out || (L > 0 && !index_k)) return fail(IDX_ERR_INVALID_ARG, "NULL pointer");
+  void* scratch = nullptr;
+  idx_status st = static_scratch(&scratch);
+  if (st != IDX_OK) return st;
+  cudaError_t e = launch_block_select(index_q, index_k, query_pos, Q, n_kv, D, L, *cfg, out, out_width, out_count,
+                                      scratch, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "block_select_static: %s", cudaGetErrorString(e));
+  return IDX_OK;
+}

@@ -15,6 +15,9 @@ constexpr int kTile = 128;  // keys per tensor-core tile (one TMEM lane each)
 // Number of streaming multiprocessors of the current device (cached).
 int sm_count();
 
+// Records the message returned by idx_last_error_string() and returns st.
+idx_status fail(idx_status st, const char* fmt, ...);
+
 // Visible extent of row m: false (and len 0) when the extent does not fit the
 // key buffer or exceeds max_key_len.
 __device__ __forceinline__ bool row_extent(const idx_problem& p, int64_t m, int64_t* off, int* len) {
