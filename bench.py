@@ -43,6 +43,8 @@ sys.path.insert(0, ROOT)
 from sparse_attention_indexer_idx_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "indexer queries*keys scored/sec"
+# prefill queries: the heads of a query share one direction, q = |a| c_z + 0.05 eps
+PREFILL_Q_NOISE = 0.05
 UNIT = "pairs/s"
 
 
@@ -115,18 +117,29 @@ class Clocks:
 
 # ----------------------------------------------------------------- workloads --
 
-def make_workload(name: str, rank: int):
+def make_workload(name: str, rank: int, rows=None):
+    """The workload's inputs; `rows` shrinks the batch (query rows) for profiling runs."""
     seed_shift = 1000 * rank
+    kw = {}
     if name == "decode":
-        return wl.decode_bf16(seed=2 + seed_shift)
+        if rows:
+            kw["M"] = rows
+        return wl.decode_bf16(seed=2 + seed_shift, **kw)
     if name in ("prefill", "prefill_dosa"):
-        return wl.prefill_bf16(seed=3 + seed_shift)
-    if name == "ragged_fp8":
-        return wl.ragged_fp8(seed=5 + seed_shift)
+        if rows:
+            kw["n_queries"] = rows
+        return wl.prefill_bf16(seed=3 + seed_shift, q_noise=PREFILL_Q_NOISE, **kw)
+    if name in ("ragged_fp8", "ragged_fp8_dosa"):
+        if rows:
+            kw["M"] = rows
+        return wl.ragged_fp8(seed=5 + seed_shift, **kw)
     if name == "tiny":
         return wl.tiny_fp32(seed=0 + seed_shift)
     if name == "block_select":
-        return wl.block_select(seed=4 + seed_shift)
+        if rows:
+            kw["Q"] = rows
+            kw["L"] = 128 * rows
+        return wl.block_select(seed=4 + seed_shift, **kw)
     raise ValueError(name)
 
 
@@ -134,6 +147,7 @@ WORKLOAD_TEXT = {
     "decode": "decode indexer bf16: 64 rows x 32768 own keys, H32 D128, top-2048, witness_merge S=16 (5% padding)",
     "prefill": "causal prefill bf16: 4096 queries over 65536 shared keys, H64 D128, top-2048 (unpruned)",
     "prefill_dosa": "causal prefill bf16 with DoSA pruning: 4096 queries, 65536 keys, H64 D128, K2048, 12288 seeds, R16",
+    "ragged_fp8_dosa": "ragged decode FP8 with DoSA pruning: 128 rows, L_r~U[4096,131072], H64 D128, K2048, 8192 seeds/row, R20",
     "ragged_fp8": "ragged decode FP8 e4m3 keys + scale: 128 rows, L_r~U[4096,131072], H64 D128, top-2048, witness_merge S=32",
     "tiny": "tiny fp32 indexer: 8 rows, H4 D16, L512, K32, witness_merge S=4",
     "block_select": "MiniMax block select fp32: 1024 queries, 8 KV heads, D128, L131072, block 128, top 32, init 1, local 2",
@@ -162,7 +176,8 @@ class IndexerStep:
         self.ctx = self.p.key_len
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         self.score_ms = []
-        self.launches = 3 if self.S else 2
+        # score + top-K (a merge launch for rows above 32768) + witness merge
+        self.launches = 1 + (1 if self.ld <= 32768 else 2) + (1 if self.S else 0)
 
     def run(self, timed=False):
         B, p = self.B, self.p
@@ -203,19 +218,27 @@ class IndexerStep:
 class DosaStep:
     """DoSA-pruned top-K (dosa_topk) on device-resident inputs."""
 
-    def __init__(self, B, wp, dev, R, n_seed):
+    def __init__(self, B, wp, dev, R, n_seed, capacity=16384):
         self.B = B
         self.wp = wp
         self.p = B.problem_to_device(wp, dev)
         self.K = wp.K
-        self.dp = B.make_dosa_params(n_seed=n_seed, retained_heads=R)
+        self.dp = B.make_dosa_params(n_seed=n_seed, retained_heads=R, candidate_capacity=capacity)
         self.ids = torch.empty((wp.M, self.K), dtype=torch.int32, device=dev)
         self.sc = torch.empty((wp.M, self.K), dtype=torch.float32, device=dev)
         self.ws = torch.empty(B.dosa_topk_workspace_size(self.p, self.K, self.dp), dtype=torch.uint8, device=dev)
         self.stats = torch.zeros(5, dtype=torch.int64, device=dev)
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         self.score_ms = []
-        self.launches = 0
+        # kernels dosa_topk enqueues per call: seeds, seed scores and top-K, planner,
+        # bound scan, rescoring, merge, fallback and statistics (top-K stages
+        # over rows above 32768 take a second, merge launch)
+        two = lambda n: 1 if n <= 32768 else 2
+        L = int(np.max(wp.key_len))
+        if wp.key_off is None:
+            self.launches = 15 + two(L) + two(R and n_seed) + two(wp.K + capacity) + two(L) + 5
+        else:
+            self.launches = 13 + two(n_seed) + two(wp.K + capacity) + two(L)
 
     def run(self, timed=False):
         if timed:
@@ -348,6 +371,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=list(WORKLOAD_TEXT))
+    ap.add_argument("--capacity", type=int, default=16384, help="DoSA candidate capacity per row")
+    ap.add_argument("--rows", type=int, default=0, help="smaller batch (query rows) for profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -388,15 +413,16 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     B.lib()
-    wp = make_workload(args.workload, rank)
+    wp = make_workload(args.workload, rank, args.rows or None)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         if args.workload == "block_select":
             step = BlockSelectStep(B, wp, dev)
             pairs_per_step = step.pairs()
             rows_per_step = wp.index_q.shape[0] * wp.index_q.shape[1]
-        elif args.workload == "prefill_dosa":
-            step = DosaStep(B, wp, dev, R=wp.extras["R"], n_seed=wp.extras["n_seed"])
+        elif args.workload in ("prefill_dosa", "ragged_fp8_dosa"):
+            step = DosaStep(B, wp, dev, R=wp.extras["R"], n_seed=wp.extras.get("n_seed", wp.extras.get("seed_cap", 8192)),
+                            capacity=args.capacity)
             pairs_per_step = wp.pairs()
             rows_per_step = wp.M
         else:
@@ -464,6 +490,14 @@ def main():
         k_ms = statistics.median(kernel_ms)
         roof = {"kernel": "dosa_topk (all kernels)", "bound": "tensor", "achieved": None, "peak": bf16,
                 "unit": "TFLOP/s", "frac": None, "traffic": None, "kernel_ms": k_ms}
+        step.stats.zero_()
+        with torch.cuda.stream(stream):
+            step.run()
+        torch.cuda.synchronize()
+        st = step.stats.cpu().tolist()
+        nonseed = max(1, st[0] - st[1])
+        dosa_info = {"pairs": st[0], "seed_pairs": st[1], "candidates": st[2], "survivors": st[3],
+                     "fallback_rows": st[4], "candidate_rate": st[2] / nonseed, "survival_rate": st[3] / nonseed}
 
     e2e = None
     if isinstance(step, IndexerStep):
@@ -483,6 +517,8 @@ def main():
             "rows_per_s": rows_per_step * world / (ms_step * 1e-3),
             "roofline": roof, "e2e": e2e, "clocks": clock_info,
             "gpu_launches": step.launches * args.steps}
+    if isinstance(step, DosaStep):
+        line["dosa"] = dosa_info
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, wp)
     if rank == 0:

@@ -1,0 +1,100 @@
+"""Parity at the full workload sizes, in the launch configuration the
+benchmark times: sampled rows against the fp64 oracle (scores within
+tolerance, top-K sets equal away from the K-th score), every row of the
+integer witness merge bit-exact, and the DoSA-pruned top-K bit-identical to
+the unpruned one on every row."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import EPS, check_topk_row
+from oracle import dsa as odsa
+from oracle import witness as ow
+from sparse_attention_indexer_idx_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from sparse_attention_indexer_idx_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _topk(B, p, K):
+    M = p.q.shape[0]
+    ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    sc = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.idx_topk_workspace_size(p, K), dtype=torch.uint8, device="cuda")
+    B.idx_topk(p, K, ids, sc, ws)
+    return ids, sc
+
+
+def _dosa(B, p, K, **kw):
+    M = p.q.shape[0]
+    dp = B.make_dosa_params(**kw)
+    ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    sc = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    st = torch.empty((M,), dtype=torch.int32, device="cuda")
+    stats = torch.zeros(5, dtype=torch.int64, device="cuda")
+    ws = torch.empty(B.dosa_topk_workspace_size(p, K, dp), dtype=torch.uint8, device="cuda")
+    B.dosa_topk(p, K, dp, ids, sc, ws, row_status=st, stats=stats)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), sc.cpu().numpy(), st.cpu().numpy(), stats.cpu().numpy()
+
+
+def test_decode_bf16_full(B):
+    """64 rows x 32768 own keys, H32, K2048; witnesses S=16 after 5% padding."""
+    wp = wl.decode_bf16()
+    p = B.problem_to_device(wp)
+    ids, sc = _topk(B, p, wp.K)
+    g_ids, g_sc = ids.cpu().numpy(), sc.cpu().numpy()
+    for m in (0, 31, 63):
+        s_ref, a_ref = odsa.row_scores(wp, m)
+        check_topk_row(g_ids[m], g_sc[m], s_ref, a_ref, wp.K, EPS["bf16"])
+    learned = g_ids.copy()
+    learned[wp.extras["pad_mask"]] = -1
+    t = torch.from_numpy(learned).cuda()
+    S = wp.extras["S"]
+    B.witness_merge(t, p.key_len, wp.K - S, S, S)
+    ref = ow.apply_topology_witnesses(learned, wp.K, wp.key_len, wp.K - S, S, S)
+    assert np.array_equal(t.cpu().numpy(), ref)
+    assert B.device_error() == 0
+
+
+@pytest.mark.parametrize("q_noise", [None, 0.05])
+def test_prefill_full_pruned_equals_unpruned(B, q_noise):
+    """4096 causal queries over 65536 keys, H64, K2048, 12288 seeds, R16."""
+    wp = wl.prefill_bf16(q_noise=q_noise)
+    p = B.problem_to_device(wp)
+    ids, sc = _topk(B, p, wp.K)
+    u_ids, u_sc = ids.cpu().numpy(), sc.cpu().numpy()
+    d_ids, d_sc, st, stats = _dosa(B, p, wp.K, n_seed=12288, retained_heads=16)
+    assert np.array_equal(u_ids, d_ids)
+    assert np.array_equal(u_sc.view(np.uint32), d_sc.view(np.uint32))
+    assert stats[0] == wp.pairs()
+    for m in (0, 2047, 4095):
+        s_ref, a_ref = odsa.row_scores(wp, m)
+        check_topk_row(u_ids[m], u_sc[m], s_ref, a_ref, wp.K, EPS["bf16"])
+    assert B.device_error() == 0
+
+
+def test_ragged_fp8_full(B):
+    """128 rows, L_r ~ U[4096, 131072], FP8 keys; DoSA R=20 == unpruned; witnesses S=32."""
+    wp = wl.ragged_fp8()
+    p = B.problem_to_device(wp)
+    ids, sc = _topk(B, p, wp.K)
+    u_ids, u_sc = ids.cpu().numpy(), sc.cpu().numpy()
+    for m in (0, 77, 127):
+        s_ref, a_ref = odsa.row_scores(wp, m)
+        check_topk_row(u_ids[m], u_sc[m], s_ref, a_ref, wp.K, EPS["fp8"])
+    d_ids, d_sc, st, stats = _dosa(B, p, wp.K, n_seed=8192, retained_heads=20)
+    assert np.array_equal(u_ids, d_ids)
+    assert np.array_equal(u_sc.view(np.uint32), d_sc.view(np.uint32))
+    S = wp.extras["S"]
+    t = torch.from_numpy(u_ids.copy()).cuda()
+    B.witness_merge(t, p.key_len, wp.K - S, S, S)
+    ref = ow.apply_topology_witnesses(u_ids, wp.K, wp.key_len, wp.K - S, S, S)
+    assert np.array_equal(t.cpu().numpy(), ref)
+    assert B.device_error() == 0
