@@ -235,10 +235,11 @@ class DosaStep:
         # over rows above 32768 take a second, merge launch)
         two = lambda n: 1 if n <= 32768 else 2
         L = int(np.max(wp.key_len))
+        NS = min(max(n_seed, wp.K), L)
         if wp.key_off is None:
-            self.launches = 15 + two(L) + two(R and n_seed) + two(wp.K + capacity) + two(L) + 5
+            self.launches = 20 + two(L) + two(NS) + two(wp.K + capacity) + two(L)
         else:
-            self.launches = 13 + two(n_seed) + two(wp.K + capacity) + two(L)
+            self.launches = 13 + two(NS) + two(wp.K + capacity) + two(L)
 
     def run(self, timed=False):
         if timed:
