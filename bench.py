@@ -41,6 +41,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from sparse_attention_indexer_idx_gb300 import workloads as wl  # noqa: E402
+from sparse_attention_indexer_idx_gb300.dist import job_step_ms, job_value, rank_seed  # noqa: E402
 
 METRIC = "indexer queries*keys scored/sec"
 # prefill queries: the heads of a query share one direction, q = |a| c_z + 0.05 eps
@@ -119,7 +120,7 @@ class Clocks:
 
 def make_workload(name: str, rank: int, rows=None):
     """The workload's inputs; `rows` shrinks the batch (query rows) for profiling runs."""
-    seed_shift = 1000 * rank
+    seed_shift = rank_seed(0, rank)
     kw = {}
     if name == "decode":
         if rows:
@@ -455,12 +456,8 @@ def main():
         step.ev = per_step[i]
         step.collect()
     kernel_ms = step.score_ms
-    ms_step = ms_total / args.steps
-    if dist:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = pairs_per_step * world / (ms_step * 1e-3)
+    ms_step = job_step_ms(ms_total / args.steps, device=dev)
+    value = job_value(pairs_per_step, ms_step, world)
 
     hbm, bf16, bf16_sus, peak_src = _peaks()
     roof = None
