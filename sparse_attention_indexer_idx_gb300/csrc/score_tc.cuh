@@ -33,8 +33,10 @@
 //
 // Warp roles:  warp 0  TMA producer (key tiles, query tiles)
 //              warp 1  TMEM allocation + MMA issue (one thread)
-//              warps 2-5  epilogue: tcgen05.ld -> score / bound -> global
-//              warps 6-9  (FP8 only) e4m3 -> f16 conversion of key tiles into
+//              warps 2..  epilogue (4, or 8 when a tile holds several queries:
+//                         two per TMEM lane quarter, alternating queries):
+//                         tcgen05.ld -> score / bound -> global
+//              last 4     (FP8 only) e4m3 -> f16 conversion of key tiles into
 //                         the swizzled MMA layout, bf16 -> f16 of query tiles
 // Every wait is bounded (see common.cuh); on a timeout all roles stop, the
 // producer and the MMA thread drain what they issued, and TMEM is released.
@@ -91,22 +93,28 @@ struct TcCfg {
   static constexpr int B_BYTES = N * 128 * 2;
   static constexpr int RAW_BYTES = 128 * 128;
   static constexpr int SB = (NQ > 1) ? 1 : 2;
-  static constexpr int SA = FP8 ? 3 : ((B_BYTES * SB <= 32768) ? 5 : 4);
-  static constexpr int SRAW = FP8 ? ((B_BYTES * SB <= 32768) ? 4 : 3) : 0;
+  // FP8: two converted (f16) tiles are enough for the MMA; every other byte of
+  // shared memory holds raw tiles in flight from HBM
+  static constexpr int SA = FP8 ? 2 : ((B_BYTES * SB <= 32768) ? 5 : 4);
+  static constexpr int SRAW_FIT = (212 * 1024 - SA * A_BYTES - SB * B_BYTES) / RAW_BYTES;
+  static constexpr int SRAW = FP8 ? (SRAW_FIT > 8 ? 8 : SRAW_FIT) : 0;
   static constexpr int SRAW_MOD = SRAW > 0 ? SRAW : 1;   // ring index arithmetic
   static constexpr int SACC = (N >= 256) ? 2 : 4;
   static constexpr int TMEM_COLS = tc_pow2_cols(SACC * N);
-  static constexpr int NTHREADS = FP8 ? 320 : 192;
+  // epilogue warps: two per TMEM lane quarter when a tile holds several queries
+  // (each takes every other query), else one
+  static constexpr int NE = (NQ > 1) ? 8 : 4;
+  static constexpr int NTHREADS = 32 * (2 + NE + (FP8 ? 4 : 0));
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + SA * A_BYTES;
   static constexpr int OFF_RAW = OFF_B + SB * B_BYTES;
-  // per epilogue warp (4 private copies, so the warps never wait on each other)
+  // per epilogue warp (NE private copies, so the warps never wait on each other)
   static constexpr int OFF_W = OFF_RAW + SRAW * RAW_BYTES;
-  static constexpr int OFF_BASE = OFF_W + 4 * N * 4;
-  static constexpr int OFF_LEN = OFF_BASE + 4 * NQ * 8;
-  static constexpr int OFF_AUX = OFF_LEN + 4 * NQ * 4;         // coef, tau per query (bound)
-  static constexpr int OFF_BAR = ((OFF_AUX + 4 * NQ * 8) + 7) & ~7;
+  static constexpr int OFF_BASE = OFF_W + NE * N * 4;
+  static constexpr int OFF_LEN = OFF_BASE + NE * NQ * 8;
+  static constexpr int OFF_AUX = OFF_LEN + NE * NQ * 4;        // coef, tau per query (bound)
+  static constexpr int OFF_BAR = ((OFF_AUX + NE * NQ * 8) + 7) & ~7;
   static constexpr int NBARS = 2 * SA + 3 * SB + 2 * SRAW + 2 * SACC + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
@@ -273,7 +281,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     for (int i = 0; i < C::SA; ++i) {
       mbar_init(&a_full[i], C::FP8 ? kConvThreads : 1);
       // the bound epilogue reads ||k|| from the key tile, so its 4 warps also release it
-      mbar_init(&a_empty[i], C::BOUND ? 5 : 1);
+      mbar_init(&a_empty[i], C::BOUND ? 1 + C::NE : 1);
     }
     for (int i = 0; i < C::SB; ++i) {
       mbar_init(&b_full[i], C::FP8 ? kConvThreads : 1);
@@ -286,7 +294,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     }
     for (int i = 0; i < C::SACC; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
+      mbar_init(&acc_empty[i], 32 * C::NE);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -441,14 +449,17 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         mbar_wait(drain_bar, 0, no_abort);
       }
     }
-  } else if (warp >= 2 && warp < 6) {
+  } else if (warp >= 2 && warp < 2 + C::NE) {
     // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;                   // epilogue warp index
     const int quarter = warp & 3;              // TMEM lanes this warp may read
+    const int qfirst = ew >> 2;                // first query of this warp in a tile
+    constexpr int QSTEP = C::NE / 4;
     const int row_in_tile = quarter * 32 + lane;
-    float* sW = sW_all + quarter * C::N;
-    int32_t* sLen = sLen_all + quarter * C::NQ;
-    int64_t* sBase = sBase_all + quarter * C::NQ;
-    float* sAux = sAux_all + quarter * C::NQ * 2;
+    float* sW = sW_all + ew * C::N;
+    int32_t* sLen = sLen_all + ew * C::NQ;
+    int64_t* sBase = sBase_all + ew * C::NQ;
+    float* sAux = sAux_all + ew * C::NQ * 2;
     TcUnits<C> u;
     u.init(args, s);
     int64_t cur_g = -1;
@@ -486,11 +497,24 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         __syncwarp();
       }
       const int acc = nacc % C::SACC;
+      const int key = (int)(u.t * 128) + row_in_tile;
+      // FP8: fetch this key's dequantisation scale before waiting for the
+      // accumulator, so the global load overlaps the wait (all queries of a
+      // group read the same key sequence, so one scale serves them all)
+      float kscale = 1.0f;
+      if constexpr (C::FP8) {
+        const int64_t m0 = cur_g * C::NQ + qfirst;
+        if (m0 < args.p.M) {
+          int64_t kid = key;
+          if (C::GATHER) kid = key < sLen[qfirst] ? (int64_t)args.list[m0 * args.gld + key] : -1;
+          const int64_t row = sBase[qfirst] + kid;
+          if (kid >= 0 && row < args.p.n_keys) kscale = __ldg(args.p.key_scale + row);
+        }
+      }
       const bool got = mbar_wait(&acc_full[acc], (nacc / C::SACC) & 1, abort_flag);
       __syncwarp();                           // tcgen05.ld below is warp-collective
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      const int key = (int)(u.t * 128) + row_in_tile;
       float knorm = 0.0f;
       if (C::BOUND) {
         // ||k|| of this lane's key from the MMA-ready tile (128-byte swizzle), then release the tile
@@ -524,7 +548,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         if (lane == 0) mbar_arrive(&a_empty[nacc % C::SA]);
       }
 #pragma unroll 1
-      for (int qi = 0; qi < C::NQ; ++qi) {
+      for (int qi = qfirst; qi < C::NQ; qi += QSTEP) {
         const int64_t m = cur_g * C::NQ + qi;
         if (m >= args.p.M) break;
         const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::N + qi * C::NCOL);
@@ -532,27 +556,36 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         const int len = sLen[qi];
         if (!C::BOUND) {
           float sc = 0.0f;
+          constexpr int NCH = (C::H + 31) / 32;      // 32-column TMEM loads per query
+          constexpr int CW = C::H < 32 ? C::H : 32;  // columns per load
+          constexpr int GRP = NCH < 2 ? NCH : 2;     // loads in flight before one wait
+          // head chain h = 0 .. H-1, weights four at a time (broadcast loads)
 #pragma unroll
-          for (int c = 0; c < C::H; c += 32) {
-            uint32_t v[32];
-            if (C::H >= 32) {
-              tmem_ld_32x32b_x32(tcol + c, v);
-            } else {
-              tmem_ld_32x32b_x16(tcol + c, v);
+          for (int c0 = 0; c0 < NCH; c0 += GRP) {
+            uint32_t v[GRP][32];
+#pragma unroll
+            for (int c = 0; c < GRP; ++c) {
+              if (C::H >= 32) {
+                tmem_ld_32x32b_x32(tcol + 32 * (c0 + c), v[c]);
+              } else {
+                tmem_ld_32x32b_x16(tcol, v[c]);
+              }
             }
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < (C::H < 32 ? C::H : 32); ++j)
-              sc = __fmaf_rn(wq[c + j], fmaxf(__uint_as_float(v[j]), 0.0f), sc);
-          }
-          if (key < len) {
-            float outv = sc;
-            if (C::FP8) {
-              const int64_t kid = C::GATHER ? (int64_t)args.list[m * args.gld + key] : (int64_t)key;
-              outv = sc * args.p.key_scale[sBase[qi] + kid];
+            for (int c = 0; c < GRP; ++c) {
+              const float4* w4 = reinterpret_cast<const float4*>(wq + 32 * (c0 + c));
+#pragma unroll
+              for (int j4 = 0; j4 < CW / 4; ++j4) {
+                const float4 ww = w4[j4];
+                sc = __fmaf_rn(ww.x, fmaxf(__uint_as_float(v[c][4 * j4 + 0]), 0.0f), sc);
+                sc = __fmaf_rn(ww.y, fmaxf(__uint_as_float(v[c][4 * j4 + 1]), 0.0f), sc);
+                sc = __fmaf_rn(ww.z, fmaxf(__uint_as_float(v[c][4 * j4 + 2]), 0.0f), sc);
+                sc = __fmaf_rn(ww.w, fmaxf(__uint_as_float(v[c][4 * j4 + 3]), 0.0f), sc);
+              }
             }
-            args.scores[m * args.ld + key] = outv;
           }
+          if (key < len) args.scores[m * args.ld + key] = C::FP8 ? sc * kscale : sc;
         } else {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tcol, v);
@@ -566,7 +599,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           ub = ub - fmaxf(__uint_as_float(v[31]), 0.0f);
           bool is_cand = false;
           if (key < len) {
-            if (C::FP8) ub = ub * args.p.key_scale[sBase[qi] + key];
+            if (C::FP8) ub = ub * kscale;
             const uint32_t* bits = args.seedbits + (args.seed_stride ? m * args.seed_stride : 0);
             const bool seed = (bits[key >> 5] >> (key & 31)) & 1u;
             is_cand = !seed && !(ub < sAux[2 * qi + 1]);
@@ -591,7 +624,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     }
   } else if (C::FP8) {
     // ------------------------------------------------------------ converters
-    const int ct = threadIdx.x - 192;          // 0..127
+    const int ct = threadIdx.x - 32 * (2 + C::NE);   // 0..127
     TcUnits<C> u;
     u.init(args, s);
     int64_t cur_g = -1;
