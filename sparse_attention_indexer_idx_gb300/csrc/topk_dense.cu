@@ -35,10 +35,12 @@ struct TkShared {
   uint64_t cand[TK_CAP];
   uint32_t samp[TK_NS];
   uint32_t hist[kTopkBins];
+  uint32_t bstart[kTopkBins];
   uint32_t red[TK_NT / 32];
   uint32_t cnt;
   uint32_t found_bin;
   uint32_t found_above;
+  uint32_t kmin, kmax, bmax;
 };
 
 __device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* red) {
@@ -185,6 +187,98 @@ __device__ void sort_candidates(uint64_t* buf, int S) {
     case 4: sort_smem_via_regs<4>(buf); break;
     default: sort_smem_via_regs<8>(buf); break;
   }
+}
+
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total);
+
+// Sorts the n nonzero, distinct composites src[0..n) descending into dst by one
+// bucket pass on the 11 key bits just below the common prefix of the smallest
+// and largest key (monotone in the key), then an insertion sort inside each
+// bucket (one thread per bucket).  Returns false, with src untouched, when a
+// bucket would hold more than kBucketMax entries (heavy ties): the caller then
+// uses the bitonic network.
+constexpr uint32_t kBucketMax = 32;
+__device__ bool bucket_sort_desc(TkShared& sh, const uint64_t* src, int n, uint64_t* dst) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    sh.kmin = 0xffffffffu;
+    sh.kmax = 0u;
+    sh.bmax = 0u;
+  }
+  for (int b = tid; b < kTopkBins; b += TK_NT) sh.hist[b] = 0;
+  __syncthreads();
+  uint32_t mn = 0xffffffffu, mx = 0u;
+  for (int i = tid; i < n; i += TK_NT) {
+    const uint32_t k = (uint32_t)(src[i] >> 32);
+    mn = min(mn, k);
+    mx = max(mx, k);
+  }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if ((tid & 31) == 0) {
+    atomicMin(&sh.kmin, mn);
+    atomicMax(&sh.kmax, mx);
+  }
+  __syncthreads();
+  const uint32_t diff = sh.kmin ^ sh.kmax;
+  const int top = diff ? 31 - __clz((int)diff) : 0;
+  const int shift = top >= 10 ? top - 10 : 0;
+  for (int i = tid; i < n; i += TK_NT) atomicAdd(&sh.hist[((uint32_t)(src[i] >> 32) >> shift) & 0x7ffu], 1u);
+  __syncthreads();
+  // exclusive scan over the buckets, highest bucket first; largest bucket
+  constexpr int PER = kTopkBins / TK_NT;
+  uint32_t loc[PER], sum = 0, big = 0;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    loc[q] = sh.hist[kTopkBins - 1 - (tid * PER + q)];
+    sum += loc[q];
+    big = max(big, loc[q]);
+  }
+  uint32_t total;
+  uint32_t run = block_excl_scan(sum, sh.red, &total);
+  big = __reduce_max_sync(0xffffffffu, big);
+  if ((tid & 31) == 0) atomicMax(&sh.bmax, big);
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int b = kTopkBins - 1 - (tid * PER + q);
+    sh.bstart[b] = run;
+    sh.hist[b] = run;          // becomes the scatter cursor
+    run += loc[q];
+  }
+  __syncthreads();
+  if (sh.bmax > kBucketMax) return false;
+  for (int i = tid; i < n; i += TK_NT) {
+    const uint64_t v = src[i];
+    const uint32_t pos = atomicAdd(&sh.hist[((uint32_t)(v >> 32) >> shift) & 0x7ffu], 1u);
+    dst[pos] = v;
+  }
+  __syncthreads();
+  for (int b = tid; b < kTopkBins; b += TK_NT) {
+    const int s0 = (int)sh.bstart[b], e = (int)sh.hist[b];
+    for (int i = s0 + 1; i < e; ++i) {
+      const uint64_t v = dst[i];
+      int j = i - 1;
+      while (j >= s0 && dst[j] < v) {
+        dst[j + 1] = dst[j];
+        --j;
+      }
+      dst[j + 1] = v;
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
+// Descending order of src[0..cnt) (nonzero, distinct): returns the buffer that
+// holds it -- dst after the bucket pass, or src itself (zero-padded to P and
+// bitonic-sorted) when the buckets are too uneven.
+__device__ const uint64_t* order_desc(TkShared& sh, uint64_t* src, int cnt, int P, uint64_t* dst) {
+  if (cnt <= 1) return src;
+  if (bucket_sort_desc(sh, src, cnt, dst)) return dst;
+  for (int i = cnt + threadIdx.x; i < P; i += TK_NT) src[i] = 0ull;
+  __syncthreads();
+  sort_candidates(src, P);
+  return src;
 }
 
 __device__ __forceinline__ uint64_t composite(uint32_t key, int32_t id) {
@@ -423,11 +517,9 @@ __global__ void __launch_bounds__(TK_NT, 1)
     for (int j = tid; j < P; j += TK_NT) dst[j] = j < cnt ? best[j] : 0ull;
     return;
   }
-  for (int i = cnt + tid; i < P; i += TK_NT) best[i] = 0ull;
-  __syncthreads();
-  if (P > 1) sort_candidates(best, P);
+  const uint64_t* sorted = order_desc(sh, best, cnt, P, sh.cand);
   for (int j = tid; j < K; j += TK_NT) {
-    const uint64_t v = best[j];
+    const uint64_t v = j < cnt ? sorted[j] : 0ull;
     out_ids[m * K + j] = v ? key_id((uint32_t)v) : -1;
     if (out_scores) out_scores[m * K + j] = v ? key_score((uint32_t)(v >> 32)) : -__int_as_float(0x7f800000);
   }
@@ -466,9 +558,10 @@ __global__ void __launch_bounds__(TK_NT, 1)
     for (int i = threadIdx.x; i < P; i += TK_NT) pair[i] = i < K ? best[i] : 0ull;
     __syncthreads();
   }
-  if (P > 1) sort_candidates(pair, P);
+  // the running set holds exactly K real entries (chunk 0 alone has K)
+  const uint64_t* sorted = order_desc(sh, pair, K, P, best);
   for (int j = threadIdx.x; j < K; j += TK_NT) {
-    const uint64_t v = pair[j];
+    const uint64_t v = sorted[j];
     out_ids[m * K + j] = v ? key_id((uint32_t)v) : -1;
     if (out_scores) out_scores[m * K + j] = v ? key_score((uint32_t)(v >> 32)) : -__int_as_float(0x7f800000);
   }
