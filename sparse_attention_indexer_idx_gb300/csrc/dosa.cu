@@ -457,7 +457,22 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
       if (anchor[h] >= 0) c = __fmaf_rn(wh, dn[h], c);
       W = __fmaf_rn(fabsf(wh), sqrtf(qn2[h]), W);
     }
-    const float margin = __fsqrt_ru(E2) * (1.0f + 0.0009765625f) + a.gamma * (W + sqrtf(A2) * 1.01f);
+    float margin = __fsqrt_ru(E2) * (1.0f + 0.0009765625f) + a.gamma * (W + sqrtf(A2) * 1.01f);
+    if (p.k_dtype == IDX_FP8_E4M3) {
+      // FP8 keys: the tensor cores see every query-side vector v as sigma (hi + lo),
+      // two e4m3 vectors with a power-of-two sigma <= max|v| / 128 over the query's
+      // vectors; each element is off by at most 2^-10 sigma, so a vector by at most
+      // sqrt(D) 2^-17 max_i ||v_i||.  Both the exact scores (H query heads) and the
+      // bound (R retained vectors, folded weights, the aggregate) carry that error.
+      float qmax = 0.0f, sw = 0.0f, swf = 1.0f;
+      for (int h = 0; h < H; ++h) {
+        qmax = fmaxf(qmax, sqrtf(qn2[h]));
+        sw += fabsf(p.w[m * H + h]);
+      }
+      for (int r = 0; r < kVec; ++r) swf += fabsf(wout[r]);
+      const float vmax = fmaxf(qmax, sqrtf(A2) * 1.01f + sqrtf(E2) * 1.01f);
+      margin += 2.0f * sqrtf((float)D) * 7.62939453125e-6f * (sw * qmax + swf * vmax);
+    }
     a.coef[m] = (c + margin) * (1.0f + 1.0e-6f);
   }
 }

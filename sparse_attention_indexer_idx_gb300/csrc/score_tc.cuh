@@ -2,9 +2,20 @@
 // sm_103a), bf16 queries with bf16 keys or FP8 e4m3 keys (+ per-token scale),
 // D = 128.
 //
+// FP8 keys go to the MMA as they are loaded (kind::f8f6f4, e4m3 x e4m3): the
+// bf16 query row is split once per query group into two e4m3 vectors with one
+// exact power-of-two scale sigma per row, q = sigma (hi + lo) (bf16 holds 8
+// significant bits, hi takes the top 4, lo the next 4; only elements below
+// 2^-2 sigma lose low bits, by less than 2^-10 sigma); hi and lo are
+// separate B rows (N = 2 x vectors, so a key tile takes four MMAs of K = 32)
+// and the epilogue forms sigma (acc_hi + acc_lo).  The per-key dequantisation scales travel with the key
+// tile (cp.async into a shared ring, completion on the tile's barrier), so the
+// epilogue never waits on a global load.
+//
 // Mapping.  One MMA tile is 128 keys (the M axis: key i of the tile lives in
 // TMEM lane i) times N = NQ*NCOL columns (NQ queries x NCOL vectors each, all
-// K-major), the full D = 128 as 8 MMAs of K = 16.  Each epilogue thread owns
+// K-major), the full D = 128 as 8 MMAs of K = 16 (bf16) or 4 MMAs of K = 32
+// (FP8, with the hi and lo rows of every vector among the N columns).  Each epilogue thread owns
 // one key and reduces its own TMEM columns with no shuffles.
 //
 // Modes:
@@ -33,11 +44,12 @@
 //
 // Warp roles:  warp 0  TMA producer (key tiles, query tiles)
 //              warp 1  TMEM allocation + MMA issue (one thread)
-//              warps 2..  epilogue (4, or 8 when a tile holds several queries:
-//                         two per TMEM lane quarter, alternating queries):
+//              warps 2..9 epilogue, two per TMEM lane quarter: they take
+//                         alternate queries of a tile (several queries per
+//                         tile) or alternate tiles (one query per tile):
 //                         tcgen05.ld -> score / bound -> global
-//              last 4     (FP8 only) e4m3 -> f16 conversion of key tiles into
-//                         the swizzled MMA layout, bf16 -> f16 of query tiles
+//              last 2     (FP8 only) split of each query group's bf16 rows
+//                         into the e4m3 hi and lo tiles
 // Every wait is bounded (see common.cuh); on a timeout all roles stop, the
 // producer and the MMA thread drain what they issued, and TMEM is released.
 #pragma once
@@ -81,41 +93,56 @@ __host__ __device__ constexpr int tc_pow2_cols(int c) {
 template <int KDT_, int NCOL_, int NQ_, int MODE_>
 struct TcCfg {
   static constexpr int KDT = KDT_;
-  static constexpr int NCOL = NCOL_;          // H (score) or 32 (bound)
+  static constexpr int NCOL = NCOL_;          // query vectors per query: H (score) or 32 (bound)
   static constexpr int H = NCOL_;
   static constexpr int NQ = NQ_;
   static constexpr int MODE = MODE_;
   static constexpr bool FP8 = (KDT == IDX_FP8_E4M3);
   static constexpr bool GATHER = (MODE == kGather);
   static constexpr bool BOUND = (MODE == kBound);
-  static constexpr int N = NQ * NCOL;
-  static constexpr int A_BYTES = 128 * 128 * 2;
-  static constexpr int B_BYTES = N * 128 * 2;
-  static constexpr int RAW_BYTES = 128 * 128;
+  static constexpr int NCOLX = FP8 ? 2 * NCOL : NCOL;   // MMA columns per query (hi, lo for FP8)
+  static constexpr int N = NQ * NCOLX;
+  static constexpr int A_BYTES = FP8 ? 128 * 128 : 128 * 128 * 2;   // one key tile
+  static constexpr int BQ_BYTES = FP8 ? 0 : NQ * NCOL * 256;         // bf16 query rows as loaded
+  static constexpr int B8_BYTES = FP8 ? N * 128 : 0;                 // e4m3 hi and lo rows (FP8)
+  static constexpr int B_BYTES = BQ_BYTES + B8_BYTES;                // one query buffer
   static constexpr int SB = (NQ > 1) ? 1 : 2;
-  // FP8: two converted (f16) tiles are enough for the MMA; every other byte of
-  // shared memory holds raw tiles in flight from HBM
-  static constexpr int SA = FP8 ? 2 : ((B_BYTES * SB <= 32768) ? 5 : 4);
-  static constexpr int SRAW_FIT = (212 * 1024 - SA * A_BYTES - SB * B_BYTES) / RAW_BYTES;
-  static constexpr int SRAW = FP8 ? (SRAW_FIT > 8 ? 8 : SRAW_FIT) : 0;
-  static constexpr int SRAW_MOD = SRAW > 0 ? SRAW : 1;   // ring index arithmetic
   static constexpr int SACC = (N >= 256) ? 2 : 4;
+  // FP8: key scales of one tile; their ring is deeper than the key ring by the
+  // tiles that can sit between the MMA and the epilogue, so a key slot is free
+  // as soon as its MMAs complete
+  static constexpr int SC_BYTES = FP8 ? 512 : 0;
+  static constexpr int SA_FIT = (220 * 1024 - SB * B_BYTES - (SACC + 2) * SC_BYTES) / (A_BYTES + SC_BYTES);
+  static constexpr int SA = FP8 ? (SA_FIT > 12 ? 12 : SA_FIT) : ((BQ_BYTES * SB <= 32768) ? 5 : 4);
+  static constexpr int SSC = FP8 ? SA + SACC + 2 : 0;
+  static constexpr int SSC_MOD = SSC > 0 ? SSC : 1;
+  static constexpr int IL = (N <= 128) ? 2 : 1;   // MMA chains interleaved (tiles per issue round)
   static constexpr int TMEM_COLS = tc_pow2_cols(SACC * N);
   // epilogue warps: two per TMEM lane quarter when a tile holds several queries
   // (each takes every other query), else one
-  static constexpr int NE = (NQ > 1) ? 8 : 4;
-  static constexpr int NTHREADS = 32 * (2 + NE + (FP8 ? 4 : 0));
+  static constexpr int NE = 8;
+  // epilogue warps that read one tile: all 8 when a tile holds several queries
+  // (two per TMEM lane quarter, alternating queries), else 4 (the two warps of a
+  // quarter take alternate tiles)
+  static constexpr int EPT = (NQ > 1) ? 8 : 4;
+  static constexpr int NCONV = FP8 ? 2 : 0;   // warps that split the query rows (FP8)
+  static constexpr int NTHREADS = 32 * (2 + NE + NCONV);
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + SA * A_BYTES;
-  static constexpr int OFF_RAW = OFF_B + SB * B_BYTES;
   // per epilogue warp (NE private copies, so the warps never wait on each other)
-  static constexpr int OFF_W = OFF_RAW + SRAW * RAW_BYTES;
-  static constexpr int OFF_BASE = OFF_W + NE * N * 4;
+  static constexpr int OFF_SC = OFF_B + SB * B_BYTES;
+  static constexpr int OFF_W = OFF_SC + SSC * SC_BYTES;
+  static constexpr int OFF_BASE = OFF_W + NE * NQ * NCOL * 4;
   static constexpr int OFF_LEN = OFF_BASE + NE * NQ * 8;
-  static constexpr int OFF_AUX = OFF_LEN + NE * NQ * 4;        // coef, tau per query (bound)
-  static constexpr int OFF_BAR = ((OFF_AUX + NE * NQ * 8) + 7) & ~7;
-  static constexpr int NBARS = 2 * SA + 3 * SB + 2 * SRAW + 2 * SACC + 1;
+  static constexpr int OFF_AUX = OFF_LEN + NE * NQ * 4;        // coef, tau, sigma per query
+  // FP8: ring of the per-query scales sigma, split warps -> epilogue, deeper
+  // than the groups that can lie between them (SB + SACC + 1)
+  static constexpr int SIGR = FP8 ? 8 : 0;
+  static constexpr int SIGR_MOD = SIGR > 0 ? SIGR : 1;
+  static constexpr int OFF_SIG = OFF_AUX + NE * NQ * 16;
+  static constexpr int OFF_BAR = ((OFF_SIG + SIGR * NQ * 4) + 7) & ~7;
+  static constexpr int NBARS = 2 * SA + 2 * SB + 2 * SACC + 1 + 2 * SIGR + 2 * SSC;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N");
@@ -242,6 +269,53 @@ __device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, uint64_
       : "memory");
 }
 
+// ----------------------------------------------------------- FP8 helpers ---
+// Power-of-two scale of a query row: max|q| / sigma lies in [128, 256).
+__device__ __forceinline__ void row_sigma(float amax, float* sigma, float* inv) {
+  if (!(amax > 0.0f)) {
+    *sigma = 1.0f;
+    *inv = 1.0f;
+    return;
+  }
+  int ex;
+  frexpf(amax, &ex);                      // amax = f 2^ex, f in [0.5, 1)
+  *sigma = ldexpf(1.0f, ex - 8);
+  *inv = ldexpf(1.0f, 8 - ex);
+}
+
+// Two floats -> two e4m3 codes (round to nearest even, saturating), x0 in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(x1), "f"(x0));
+  return r;
+}
+// Two e4m3 codes (low byte first) -> two floats, exactly.
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t codes, float* lo, float* hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)(codes & 0xffffu)));
+  const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+  *lo = __low2float(hv);
+  *hi = __high2float(hv);
+}
+
+// max |q| over a query's NCOL rows of 128 bf16 values (global memory): the
+// epilogue's copy of the value the split used.
+template <int NCOL>
+__device__ __forceinline__ float query_amax(const uint16_t* q) {
+  const int lane = threadIdx.x & 31;
+  float mx = 0.0f;
+  for (int i = lane; i < NCOL * 32; i += 32) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(q) + i);
+    mx = fmaxf(mx, fabsf(__uint_as_float(v.x << 16)));
+    mx = fmaxf(mx, fabsf(__uint_as_float(v.x & 0xffff0000u)));
+    mx = fmaxf(mx, fabsf(__uint_as_float(v.y << 16)));
+    mx = fmaxf(mx, fabsf(__uint_as_float(v.y & 0xffff0000u)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  return mx;
+}
+
 // ------------------------------------------------------------- the kernel ---
 template <class C>
 __global__ void __launch_bounds__(C::NTHREADS, 1)
@@ -252,7 +326,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
   uint8_t* sA = smem + C::OFF_A;
   uint8_t* sB = smem + C::OFF_B;
-  uint8_t* sRaw = smem + C::OFF_RAW;
+  float* sScale = reinterpret_cast<float*>(smem + C::OFF_SC);
   float* sW_all = reinterpret_cast<float*>(smem + C::OFF_W);
   int32_t* sLen_all = reinterpret_cast<int32_t*>(smem + C::OFF_LEN);
   int64_t* sBase_all = reinterpret_cast<int64_t*>(smem + C::OFF_BASE);
@@ -262,12 +336,14 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   uint64_t* a_empty = a_full + C::SA;
   uint64_t* b_full = a_empty + C::SA;
   uint64_t* b_empty = b_full + C::SB;
-  uint64_t* b_loaded = b_empty + C::SB;
-  uint64_t* raw_full = b_loaded + C::SB;
-  uint64_t* raw_empty = raw_full + C::SRAW;
-  uint64_t* acc_full = raw_empty + C::SRAW;
+  uint64_t* acc_full = b_empty + C::SB;
   uint64_t* acc_empty = acc_full + C::SACC;
   uint64_t* drain_bar = acc_empty + C::SACC;
+  uint64_t* sig_full = drain_bar + 1;
+  uint64_t* sig_empty = sig_full + C::SIGR;
+  float* sSig = reinterpret_cast<float*>(smem + C::OFF_SIG);
+  uint64_t* sc_full = sig_empty + C::SIGR;
+  uint64_t* sc_empty = sc_full + C::SSC;
   uint8_t* misc = smem + C::OFF_MISC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -275,28 +351,31 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr int kConvThreads = 128;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::SA; ++i) {
-      mbar_init(&a_full[i], C::FP8 ? kConvThreads : 1);
-      // the bound epilogue reads ||k|| from the key tile, so its 4 warps also release it
-      mbar_init(&a_empty[i], C::BOUND ? 1 + C::NE : 1);
+      mbar_init(&a_full[i], 1);
+      // the bound epilogue reads ||k|| from the key tile, so its warps also release the slot
+      mbar_init(&a_empty[i], C::BOUND ? 1 + C::EPT : 1);
     }
     for (int i = 0; i < C::SB; ++i) {
-      mbar_init(&b_full[i], C::FP8 ? kConvThreads : 1);
+      // FP8: every lane of the split warps arrives once its rows are written
+      mbar_init(&b_full[i], C::FP8 ? 32 * C::NCONV : 1);
       mbar_init(&b_empty[i], 1);
-      mbar_init(&b_loaded[i], 1);
-    }
-    for (int i = 0; i < C::SRAW; ++i) {
-      mbar_init(&raw_full[i], 1);
-      mbar_init(&raw_empty[i], kConvThreads);
     }
     for (int i = 0; i < C::SACC; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 32 * C::NE);
+      mbar_init(&acc_empty[i], 32 * C::EPT);
     }
     mbar_init(drain_bar, 1);
+    for (int i = 0; i < C::SIGR; ++i) {
+      mbar_init(&sig_full[i], 1);
+      mbar_init(&sig_empty[i], C::NE);
+    }
+    for (int i = 0; i < C::SSC; ++i) {
+      mbar_init(&sc_full[i], 32);               // each producer lane, once its copies landed
+      mbar_init(&sc_empty[i], C::EPT);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -319,95 +398,97 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     TcUnits<C> u;
     u.init(args, s);
     int64_t cur_g = -1;
-    uint32_t na = 0, nb = 0, nr = 0;
+    int64_t gbase = 0;                         // first key row of the group (kept: no global load per tile)
+    int32_t gcnt = 0;                          // kGather: list length of the group
+    uint32_t na = 0, nb = 0;
     while (u.valid()) {
       if (u.g != cur_g) {
         cur_g = u.g;
-        const int bs = nb % C::SB;
-        bool ok = true;
-        if (lane == 0) {
-          ok = mbar_wait(&b_empty[bs], ((nb / C::SB) & 1) ^ 1, abort_flag);
-          if (ok) {
-            uint64_t* bar = C::FP8 ? &b_loaded[bs] : &b_full[bs];
-            mbar_arrive_expect_tx(bar, C::B_BYTES);
-            const int32_t y = (int32_t)(cur_g * C::N);
-            tma_load_2d(sB + bs * C::B_BYTES, &tmap_q, bar, 0, y);
-            tma_load_2d(sB + bs * C::B_BYTES + C::B_BYTES / 2, &tmap_q, bar, 64, y);
+        gbase = tc_key_base(args, cur_g);
+        if (C::GATHER) gcnt = args.cnt[cur_g];
+        if (!C::FP8) {
+          // bf16: the group's query rows (FP8: the split warps read them from global memory)
+          const int bs = nb % C::SB;
+          bool ok = true;
+          if (lane == 0) {
+            ok = mbar_wait(&b_empty[bs], ((nb / C::SB) & 1) ^ 1, abort_flag);
+            if (ok) {
+              uint64_t* bar = &b_full[bs];
+              mbar_arrive_expect_tx(bar, C::BQ_BYTES);
+              const int32_t y = (int32_t)(cur_g * C::NQ * C::NCOL);
+              tma_load_2d(sB + bs * C::B_BYTES, &tmap_q, bar, 0, y);
+              tma_load_2d(sB + bs * C::B_BYTES + C::BQ_BYTES / 2, &tmap_q, bar, 64, y);
+            }
           }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+          ++nb;
         }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        ++nb;
       }
-      // the ring slot this tile goes to, and its barrier
-      uint8_t* dst;
-      uint64_t* fbar;
+      const int as = na % C::SA;
       bool ok = true;
-      if (C::FP8) {
-        const int rs = nr % C::SRAW_MOD;
-        if (lane == 0) ok = mbar_wait(&raw_empty[rs], ((nr / C::SRAW_MOD) & 1) ^ 1, abort_flag);
-        dst = sRaw + rs * C::RAW_BYTES;
-        fbar = &raw_full[rs];
-      } else {
-        const int as = na % C::SA;
-        if (lane == 0) ok = mbar_wait(&a_empty[as], ((na / C::SA) & 1) ^ 1, abort_flag);
-        dst = sA + as * C::A_BYTES;
-        fbar = &a_full[as];
-      }
+      if (lane == 0) ok = mbar_wait(&a_empty[as], ((na / C::SA) & 1) ^ 1, abort_flag);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const uint32_t tile_bytes = C::FP8 ? C::RAW_BYTES : C::A_BYTES;
+      uint8_t* dst = sA + as * C::A_BYTES;
+      uint64_t* fbar = &a_full[as];
+      if constexpr (C::FP8) {
+        // key scales: lane l copies those of tile rows 4l..4l+3 (rows clamped into
+        // the buffer; a scale past the row's end is never used)
+        const int ss = na % C::SSC_MOD;
+        bool sok = true;
+        if (lane == 0) sok = mbar_wait(&sc_empty[ss], ((na / C::SSC_MOD) & 1) ^ 1, abort_flag);
+        if (!__shfl_sync(0xffffffffu, sok, 0)) break;
+        float* sdst = sScale + ss * 128 + 4 * lane;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int pos = (int)(u.t * 128) + 4 * lane + i;
+          int64_t row = gbase + pos;
+          if (C::GATHER) row = gbase + (pos < gcnt ? (int64_t)args.list[u.g * args.gld + pos] : 0);
+          row = row < 0 ? 0 : (row >= args.p.n_keys ? args.p.n_keys - 1 : row);
+          cp_async_4(sdst + i, args.p.key_scale + row);
+        }
+        cp_async_arrive_noinc(&sc_full[ss]);
+      }
       if (C::GATHER) {
         // lane l fetches tile rows 4l..4l+3 (list positions t*128 + 4l + i)
-        const int64_t m = u.g;
-        const int64_t base = tc_key_base(args, m);
-        const int32_t cntm = args.cnt[m];
-        const int32_t* lst = args.list + m * args.gld + u.t * 128;
+        const int32_t* lst = args.list + u.g * args.gld + u.t * 128;
         int32_t y[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int pos = (int)(u.t * 128) + 4 * lane + i;
-          int64_t id = pos < cntm ? (int64_t)lst[4 * lane + i] : 0;
-          int64_t row = base + id;
+          int64_t id = pos < gcnt ? (int64_t)lst[4 * lane + i] : 0;
+          int64_t row = gbase + id;
           row = row < 0 ? 0 : (row >= args.p.n_keys ? args.p.n_keys - 1 : row);
           y[i] = (int32_t)row;
         }
-        if (lane == 0) mbar_arrive_expect_tx(fbar, tile_bytes);
+        if (lane == 0) mbar_arrive_expect_tx(fbar, C::A_BYTES);
         __syncwarp();
         tma_gather4(dst + lane * 512, &tmap_k, fbar, 0, y[0], y[1], y[2], y[3]);
         if (!C::FP8) tma_gather4(dst + C::A_BYTES / 2 + lane * 512, &tmap_k, fbar, 64, y[0], y[1], y[2], y[3]);
       } else if (lane == 0) {
-        const int32_t y = (int32_t)(tc_key_base(args, u.g) + u.t * 128);
-        mbar_arrive_expect_tx(fbar, tile_bytes);
+        const int32_t y = (int32_t)(gbase + u.t * 128);
+        mbar_arrive_expect_tx(fbar, C::A_BYTES);
         tma_load_2d(dst, &tmap_k, fbar, 0, y);
         if (!C::FP8) tma_load_2d(dst + C::A_BYTES / 2, &tmap_k, fbar, 64, y);
       }
       __syncwarp();
-      if (C::FP8) ++nr;
-      else ++na;
+      ++na;
       u.advance();
     }
     // drain: the last phase issued on every ring slot has landed
+    if (C::FP8) asm volatile("cp.async.wait_all;" ::: "memory");
     if (lane == 0) {
       for (uint32_t i = 0; i < (uint32_t)C::SB && i < nb; ++i) {
         uint32_t j = nb - 1 - i;
-        mbar_wait(C::FP8 ? &b_loaded[j % C::SB] : &b_full[j % C::SB], (j / C::SB) & 1, no_abort);
+        mbar_wait(&b_full[j % C::SB], (j / C::SB) & 1, no_abort);
       }
-      if (!C::FP8) {
-        for (uint32_t i = 0; i < (uint32_t)C::SA && i < na; ++i) {
-          uint32_t j = na - 1 - i;
-          mbar_wait(&a_full[j % C::SA], (j / C::SA) & 1, no_abort);
-        }
-      }
-      if constexpr (C::FP8) {
-        for (uint32_t i = 0; i < (uint32_t)C::SRAW_MOD && i < nr; ++i) {
-          uint32_t j = nr - 1 - i;
-          mbar_wait(&raw_full[j % C::SRAW_MOD], (j / C::SRAW_MOD) & 1, no_abort);
-        }
+      for (uint32_t i = 0; i < (uint32_t)C::SA && i < na; ++i) {
+        uint32_t j = na - 1 - i;
+        mbar_wait(&a_full[j % C::SA], (j / C::SA) & 1, no_abort);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(128, C::N, C::FP8 ? 0u : 1u);
       TcUnits<C> u;
       u.init(args, s);
       int64_t cur_g = -1;
@@ -421,26 +502,59 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           if (!mbar_wait(&b_full[cur_bs], (nb / C::SB) & 1, abort_flag)) break;
           ++nb;
         }
-        const int as = na % C::SA;
-        if (!mbar_wait(&a_full[as], (na / C::SA) & 1, abort_flag)) break;
-        const int acc = nacc % C::SACC;
-        if (!mbar_wait(&acc_empty[acc], ((nacc / C::SACC) & 1) ^ 1, abort_flag)) break;
+        // up to IL consecutive tiles of this group: their MMA chains are issued
+        // interleaved (a chain of small-N MMAs on one accumulator runs at the
+        // accumulate latency, two independent chains fill the gaps); each
+        // accumulator still sees the same instructions in the same order
+        int n = 1;
+        TcUnits<C> nx = u;
+        if (C::IL > 1) {
+          nx.advance();
+          if (nx.valid() && nx.g == u.g) n = 2;
+        }
+        bool ok = true;
+        for (int i = 0; i < n && ok; ++i) {
+          ok = mbar_wait(&a_full[(na + i) % C::SA], ((na + i) / C::SA) & 1, abort_flag);
+          if (ok) ok = mbar_wait(&acc_empty[(nacc + i) % C::SACC], (((nacc + i) / C::SACC) & 1) ^ 1, abort_flag);
+        }
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + as * C::A_BYTES);
         const uint32_t b0 = smem_u32(sB + cur_bs * C::B_BYTES);
-        const uint32_t d = tmem_base + (uint32_t)(acc * C::N);
+        uint32_t a0[2], d[2];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t ao = a0 + (k >> 2) * (C::A_BYTES / 2) + (k & 3) * 32;
-          const uint32_t bo = b0 + (k >> 2) * (C::B_BYTES / 2) + (k & 3) * 32;
-          tc_mma_f16(d, smem_desc_sw128(ao), smem_desc_sw128(bo), idesc, k > 0 ? 1u : 0u);
+        for (int i = 0; i < 2; ++i) {
+          a0[i] = smem_u32(sA + ((na + i) % C::SA) * C::A_BYTES);
+          d[i] = tmem_base + (uint32_t)(((nacc + i) % C::SACC) * C::N);
+        }
+        if constexpr (C::FP8) {
+          // e4m3 x e4m3, K = 32 per instruction: four steps of 32 bytes along the 128-byte rows
+          constexpr uint32_t idesc = idesc_f16(128, C::N, 0u);   // same layout; format 0 = E4M3 here
+          const uint32_t b8 = b0 + C::BQ_BYTES;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t bd = smem_desc_sw128(b8 + k * 32);
+            tc_mma_f8(d[0], smem_desc_sw128(a0[0] + k * 32), bd, idesc, k > 0 ? 1u : 0u);
+            if (n > 1) tc_mma_f8(d[1], smem_desc_sw128(a0[1] + k * 32), bd, idesc, k > 0 ? 1u : 0u);
+          }
+        } else {
+          constexpr uint32_t idesc = idesc_f16(128, C::N, 1u);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t ao = (k >> 2) * (C::A_BYTES / 2) + (k & 3) * 32;
+            const uint64_t bd = smem_desc_sw128(b0 + (k >> 2) * (C::BQ_BYTES / 2) + (k & 3) * 32);
+            tc_mma_f16(d[0], smem_desc_sw128(a0[0] + ao), bd, idesc, k > 0 ? 1u : 0u);
+            if (n > 1) tc_mma_f16(d[1], smem_desc_sw128(a0[1] + ao), bd, idesc, k > 0 ? 1u : 0u);
+          }
         }
         issued = true;
-        tc_commit(&a_empty[as]);
-        tc_commit(&acc_full[acc]);
-        ++na;
-        ++nacc;
+        for (int i = 0; i < n; ++i) {
+          tc_commit(&a_empty[(na + i) % C::SA]);
+          tc_commit(&acc_full[(nacc + i) % C::SACC]);
+        }
+        na += n;
+        nacc += n;
         const int64_t g_this = u.g;
+        if (n > 1) u = nx;
         u.advance();
         if (!u.valid() || u.g != g_this) tc_commit(&b_empty[cur_bs]);
       }
@@ -453,27 +567,40 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;                   // epilogue warp index
     const int quarter = warp & 3;              // TMEM lanes this warp may read
-    const int qfirst = ew >> 2;                // first query of this warp in a tile
-    constexpr int QSTEP = C::NE / 4;
+    const int qfirst = C::NQ > 1 ? (ew >> 2) : 0;   // first query of this warp in a tile
+    constexpr int QSTEP = C::NQ > 1 ? 2 : 1;
+    const int tile_par = ew >> 2;              // one query per tile: the parity of the tiles this warp takes
     const int row_in_tile = quarter * 32 + lane;
-    float* sW = sW_all + ew * C::N;
+    float* sW = sW_all + ew * C::NQ * C::NCOL;
     int32_t* sLen = sLen_all + ew * C::NQ;
     int64_t* sBase = sBase_all + ew * C::NQ;
-    float* sAux = sAux_all + ew * C::NQ * 2;
+    float* sAux = sAux_all + ew * C::NQ * 4;   // coef, tau, sigma per query
     TcUnits<C> u;
     u.init(args, s);
     int64_t cur_g = -1;
-    uint32_t nacc = 0;
+    uint32_t nacc = 0, ngrp = 0;
     while (u.valid()) {
       if (u.g != cur_g) {
         cur_g = u.g;
         __syncwarp();
-        for (int i = lane; i < C::N; i += 32) {
+        if constexpr (C::FP8) {
+          // the group's sigma per query, as the split warps used it
+          const int sl = ngrp % C::SIGR;
+          bool ok = true;
+          if (lane == 0) ok = mbar_wait(&sig_full[sl], (ngrp / C::SIGR) & 1, abort_flag);
+          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+          if (lane < C::NQ) sAux[4 * lane + 2] = sSig[sl * C::NQ + lane];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sig_empty[sl]);
+          ++ngrp;
+        }
+        for (int i = lane; i < C::NQ * C::NCOL; i += 32) {
           const int64_t m = cur_g * C::NQ + i / C::NCOL;
           float wv = 0.0f;
           if (m < args.p.M) wv = C::BOUND ? args.wfold[m * 32 + (i % 32)] : args.p.w[m * C::H + (i % C::H)];
           sW[i] = wv;
         }
+        if (!C::FP8 && lane < C::NQ) sAux[4 * lane + 2] = 1.0f;
         if (lane < C::NQ) {
           const int64_t m = cur_g * C::NQ + lane;
           int64_t off = 0;
@@ -490,38 +617,39 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           sLen[lane] = len;
           sBase[lane] = off;
           if (C::BOUND) {
-            sAux[2 * lane] = m < args.p.M ? args.coef[m] : 0.0f;
-            sAux[2 * lane + 1] = m < args.p.M ? args.tau[m] : 0.0f;
+            sAux[4 * lane] = m < args.p.M ? args.coef[m] : 0.0f;
+            sAux[4 * lane + 1] = m < args.p.M ? args.tau[m] : 0.0f;
           }
         }
         __syncwarp();
       }
+      if (C::NQ == 1 && (int)(nacc & 1) != tile_par) {
+        ++nacc;
+        u.advance();
+        continue;
+      }
       const int acc = nacc % C::SACC;
       const int key = (int)(u.t * 128) + row_in_tile;
-      // FP8: fetch this key's dequantisation scale before waiting for the
-      // accumulator, so the global load overlaps the wait (all queries of a
-      // group read the same key sequence, so one scale serves them all)
-      float kscale = 1.0f;
-      if constexpr (C::FP8) {
-        const int64_t m0 = cur_g * C::NQ + qfirst;
-        if (m0 < args.p.M) {
-          int64_t kid = key;
-          if (C::GATHER) kid = key < sLen[qfirst] ? (int64_t)args.list[m0 * args.gld + key] : -1;
-          const int64_t row = sBase[qfirst] + kid;
-          if (kid >= 0 && row < args.p.n_keys) kscale = __ldg(args.p.key_scale + row);
-        }
-      }
-      const bool got = mbar_wait(&acc_full[acc], (nacc / C::SACC) & 1, abort_flag);
+      bool got = mbar_wait(&acc_full[acc], (nacc / C::SACC) & 1, abort_flag);
+      // the key-tile slot of this unit (bound: read below for ||k||, so the slot is
+      // held until this warp releases it) and its scale slot (FP8)
+      const int slot = nacc % C::SA;
+      const int sslot = nacc % C::SSC_MOD;
+      if (C::BOUND && got) got = mbar_wait(&a_full[slot], (nacc / C::SA) & 1, abort_flag);
+      if (C::FP8 && got) got = mbar_wait(&sc_full[sslot], (nacc / C::SSC_MOD) & 1, abort_flag);
       __syncwarp();                           // tcgen05.ld below is warp-collective
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
+      // FP8: all queries of a group read the same key sequence, so one scale serves them all
+      const float kscale = C::FP8 ? sScale[sslot * 128 + row_in_tile] : 1.0f;
       float knorm = 0.0f;
       if (C::BOUND) {
-        // ||k|| of this lane's key from the MMA-ready tile (128-byte swizzle), then release the tile
-        const uint8_t* at = sA + (nacc % C::SA) * C::A_BYTES;
+        // ||k|| of this lane's key (codes for FP8) from the MMA-ready tile
+        const uint8_t* at = sA + slot * C::A_BYTES;
         float ss = 0.0f;
+        constexpr int HALVES = C::FP8 ? 1 : 2;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < HALVES; ++h) {
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 v = *reinterpret_cast<const uint4*>(at + h * (C::A_BYTES / 2) + row_in_tile * 128 +
@@ -529,80 +657,121 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              float lo, hi;
               if (C::FP8) {
-                const __half2 h2 = *reinterpret_cast<const __half2*>(&w4[e]);
-                lo = __low2float(h2);
-                hi = __high2float(h2);
+                float x0, x1, x2, x3;
+                e4m3x2_to_f32(w4[e], &x0, &x1);
+                e4m3x2_to_f32(w4[e] >> 16, &x2, &x3);
+                ss = __fmaf_rn(x0, x0, ss);
+                ss = __fmaf_rn(x1, x1, ss);
+                ss = __fmaf_rn(x2, x2, ss);
+                ss = __fmaf_rn(x3, x3, ss);
               } else {
-                lo = __uint_as_float(w4[e] << 16);
-                hi = __uint_as_float(w4[e] & 0xffff0000u);
+                const float lo = __uint_as_float(w4[e] << 16);
+                const float hi = __uint_as_float(w4[e] & 0xffff0000u);
+                ss = __fmaf_rn(lo, lo, ss);
+                ss = __fmaf_rn(hi, hi, ss);
               }
-              ss = __fmaf_rn(lo, lo, ss);
-              ss = __fmaf_rn(hi, hi, ss);
             }
           }
         }
         knorm = __fsqrt_ru(ss);
+      }
+      if (C::BOUND || C::FP8) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_empty[nacc % C::SA]);
+        if (lane == 0) {
+          if (C::BOUND) mbar_arrive(&a_empty[slot]);
+          if (C::FP8) mbar_arrive(&sc_empty[sslot]);
+        }
       }
 #pragma unroll 1
       for (int qi = qfirst; qi < C::NQ; qi += QSTEP) {
         const int64_t m = cur_g * C::NQ + qi;
         if (m >= args.p.M) break;
-        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::N + qi * C::NCOL);
+        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::N + qi * C::NCOLX);
         const float* wq = sW + qi * C::NCOL;
         const int len = sLen[qi];
         if (!C::BOUND) {
           float sc = 0.0f;
-          constexpr int NCH = (C::H + 31) / 32;      // 32-column TMEM loads per query
-          constexpr int CW = C::H < 32 ? C::H : 32;  // columns per load
-          constexpr int GRP = NCH < 2 ? NCH : 2;     // loads in flight before one wait
-          // head chain h = 0 .. H-1, weights four at a time (broadcast loads)
+          constexpr int NCH = (C::H + 31) / 32;      // 32-head chunks per query
+          constexpr int CW = C::H < 32 ? C::H : 32;  // heads per chunk
+          if constexpr (C::FP8) {
+            // head h: hi column h plus lo column H + h
 #pragma unroll
-          for (int c0 = 0; c0 < NCH; c0 += GRP) {
-            uint32_t v[GRP][32];
-#pragma unroll
-            for (int c = 0; c < GRP; ++c) {
+            for (int c = 0; c < NCH; ++c) {
+              uint32_t vh[32], vl[32];
               if (C::H >= 32) {
-                tmem_ld_32x32b_x32(tcol + 32 * (c0 + c), v[c]);
+                tmem_ld_32x32b_x32(tcol + 32 * c, vh);
+                tmem_ld_32x32b_x32(tcol + C::H + 32 * c, vl);
               } else {
-                tmem_ld_32x32b_x16(tcol, v[c]);
+                tmem_ld_32x32b_x16(tcol, vh);
+                tmem_ld_32x32b_x16(tcol + C::H, vl);
               }
-            }
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < GRP; ++c) {
-              const float4* w4 = reinterpret_cast<const float4*>(wq + 32 * (c0 + c));
+              tmem_ld_wait();
+              const float4* w4 = reinterpret_cast<const float4*>(wq + 32 * c);
 #pragma unroll
               for (int j4 = 0; j4 < CW / 4; ++j4) {
                 const float4 ww = w4[j4];
-                sc = __fmaf_rn(ww.x, fmaxf(__uint_as_float(v[c][4 * j4 + 0]), 0.0f), sc);
-                sc = __fmaf_rn(ww.y, fmaxf(__uint_as_float(v[c][4 * j4 + 1]), 0.0f), sc);
-                sc = __fmaf_rn(ww.z, fmaxf(__uint_as_float(v[c][4 * j4 + 2]), 0.0f), sc);
-                sc = __fmaf_rn(ww.w, fmaxf(__uint_as_float(v[c][4 * j4 + 3]), 0.0f), sc);
+                const float wv[4] = {ww.x, ww.y, ww.z, ww.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int j = 4 * j4 + e;
+                  sc = __fmaf_rn(wv[e], fmaxf(__uint_as_float(vh[j]) + __uint_as_float(vl[j]), 0.0f), sc);
+                }
+              }
+            }
+          } else {
+            constexpr int GRP = NCH < 2 ? NCH : 2;     // loads in flight before one wait
+            // head chain h = 0 .. H-1, weights four at a time (broadcast loads)
+#pragma unroll
+            for (int c0 = 0; c0 < NCH; c0 += GRP) {
+              uint32_t v[GRP][32];
+#pragma unroll
+              for (int c = 0; c < GRP; ++c) {
+                if (C::H >= 32) {
+                  tmem_ld_32x32b_x32(tcol + 32 * (c0 + c), v[c]);
+                } else {
+                  tmem_ld_32x32b_x16(tcol, v[c]);
+                }
+              }
+              tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < GRP; ++c) {
+                const float4* w4 = reinterpret_cast<const float4*>(wq + 32 * (c0 + c));
+#pragma unroll
+                for (int j4 = 0; j4 < CW / 4; ++j4) {
+                  const float4 ww = w4[j4];
+                  sc = __fmaf_rn(ww.x, fmaxf(__uint_as_float(v[c][4 * j4 + 0]), 0.0f), sc);
+                  sc = __fmaf_rn(ww.y, fmaxf(__uint_as_float(v[c][4 * j4 + 1]), 0.0f), sc);
+                  sc = __fmaf_rn(ww.z, fmaxf(__uint_as_float(v[c][4 * j4 + 2]), 0.0f), sc);
+                  sc = __fmaf_rn(ww.w, fmaxf(__uint_as_float(v[c][4 * j4 + 3]), 0.0f), sc);
+                }
               }
             }
           }
-          if (key < len) args.scores[m * args.ld + key] = C::FP8 ? sc * kscale : sc;
+          if (key < len) args.scores[m * args.ld + key] = C::FP8 ? (sc * sAux[4 * qi + 2]) * kscale : sc;
         } else {
-          uint32_t v[32];
+          uint32_t v[32], vl[32];
           tmem_ld_32x32b_x32(tcol, v);
+          if (C::FP8) tmem_ld_32x32b_x32(tcol + 32, vl);
           tmem_ld_wait();
+          if (C::FP8) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(vl[j]));
+          }
           const int R = args.R;
           float ub = 0.0f;
 #pragma unroll
           for (int j = 0; j < 31; ++j)
             if (j < R) ub = __fmaf_rn(wq[j], fmaxf(__uint_as_float(v[j]), 0.0f), ub);
-          ub = __fmaf_rn(sAux[2 * qi], knorm, ub);
           ub = ub - fmaxf(__uint_as_float(v[31]), 0.0f);
+          if (C::FP8) ub = ub * sAux[4 * qi + 2];
+          ub = __fmaf_rn(sAux[4 * qi], knorm, ub);
           bool is_cand = false;
           if (key < len) {
             if (C::FP8) ub = ub * kscale;
             const uint32_t* bits = args.seedbits + (args.seed_stride ? m * args.seed_stride : 0);
             const bool seed = (bits[key >> 5] >> (key & 31)) & 1u;
-            is_cand = !seed && !(ub < sAux[2 * qi + 1]);
+            is_cand = !seed && !(ub < sAux[4 * qi + 1]);
           }
           const unsigned mask = __ballot_sync(0xffffffffu, is_cand);
           if (mask) {
@@ -623,66 +792,59 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       u.advance();
     }
   } else if (C::FP8) {
-    // ------------------------------------------------------------ converters
-    const int ct = threadIdx.x - 32 * (2 + C::NE);   // 0..127
+    // ------------------------------------------------------------ query split
+    // Per query group, once the MMA has released the buffer: bf16 row v of query
+    // qi (global memory, 256 bytes, one coalesced warp load) -> e4m3 B rows
+    // qi*2*NCOL + v (hi) and qi*2*NCOL + NCOL + v (lo) (128-byte rows, 128-byte
+    // swizzle); rows of queries past M are zero.
+    const int cw = warp - 2 - C::NE;           // split warp 0..NCONV-1
     TcUnits<C> u;
     u.init(args, s);
     int64_t cur_g = -1;
-    uint32_t na = 0, nb = 0, nr = 0;
+    uint32_t nb = 0;
     while (u.valid()) {
       if (u.g != cur_g) {
         cur_g = u.g;
         const int bs = nb % C::SB;
-        if (!mbar_wait(&b_loaded[bs], (nb / C::SB) & 1, abort_flag)) break;
-        uint4* bp = reinterpret_cast<uint4*>(sB + bs * C::B_BYTES);
-        for (int i = ct; i < C::B_BYTES / 16; i += kConvThreads) {
-          uint4 v = bp[i];
-          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float lo = __uint_as_float(w[j] << 16);
-            const float hi = __uint_as_float(w[j] & 0xffff0000u);
-            __half2 h2 = __floats2half2_rn(lo, hi);
-            w[j] = *reinterpret_cast<uint32_t*>(&h2);
+        bool ok = mbar_wait(&b_empty[bs], ((nb / C::SB) & 1) ^ 1, abort_flag);
+        const int sl = nb % C::SIGR_MOD;
+        if (cw == 0 && ok && lane == 0) ok = mbar_wait(&sig_empty[sl], ((nb / C::SIGR_MOD) & 1) ^ 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        uint8_t* b8 = sB + bs * C::B_BYTES;
+        for (int qi = 0; qi < C::NQ; ++qi) {
+          const int64_t m = cur_g * C::NQ + qi;
+          const bool live = m < args.p.M;
+          const uint16_t* qrow = (const uint16_t*)args.p.q + (live ? m : 0) * C::NCOL * 128;
+          float sig = 1.0f, inv = 1.0f;
+          if (live) row_sigma(query_amax<C::NCOL>(qrow), &sig, &inv);
+          if (cw == 0 && lane == 0) sSig[sl * C::NQ + qi] = sig;
+          for (int v = cw; v < C::NCOL; v += C::NCONV) {
+            uint2 q4 = make_uint2(0u, 0u);
+            if (live) q4 = __ldg(reinterpret_cast<const uint2*>(qrow + v * 128) + lane);
+            // elements 4*lane .. 4*lane+3
+            const float x[4] = {__uint_as_float(q4.x << 16) * inv, __uint_as_float(q4.x & 0xffff0000u) * inv,
+                                __uint_as_float(q4.y << 16) * inv, __uint_as_float(q4.y & 0xffff0000u) * inv};
+            const uint32_t h01 = e4m3x2(x[0], x[1]), h23 = e4m3x2(x[2], x[3]);
+            float hv[4];
+            e4m3x2_to_f32(h01, &hv[0], &hv[1]);
+            e4m3x2_to_f32(h23, &hv[2], &hv[3]);
+            const uint32_t l01 = e4m3x2(x[0] - hv[0], x[1] - hv[1]);
+            const uint32_t l23 = e4m3x2(x[2] - hv[2], x[3] - hv[3]);
+            const uint32_t hi = h01 | (h23 << 16), lo = l01 | (l23 << 16);
+            // byte 4*lane of a 128-byte row: 16-byte chunk lane/4, offset 4*(lane%4)
+            const int rh = qi * 2 * C::NCOL + v, rl = rh + C::NCOL;
+            *reinterpret_cast<uint32_t*>(b8 + rh * 128 + (((lane >> 2) ^ (rh & 7)) << 4) + 4 * (lane & 3)) = hi;
+            *reinterpret_cast<uint32_t*>(b8 + rl * 128 + (((lane >> 2) ^ (rl & 7)) << 4) + 4 * (lane & 3)) = lo;
           }
-          bp[i] = v;
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(&b_full[bs]);
+        if (cw == 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sig_full[sl]);
+        }
         ++nb;
       }
-      const int rs = nr % C::SRAW_MOD;
-      if (!mbar_wait(&raw_full[rs], (nr / C::SRAW_MOD) & 1, abort_flag)) break;
-      const int as = na % C::SA;
-      if (!mbar_wait(&a_empty[as], ((na / C::SA) & 1) ^ 1, abort_flag)) break;
-      const uint8_t* src = sRaw + rs * C::RAW_BYTES;
-      uint8_t* dst = sA + as * C::A_BYTES;
-#pragma unroll 2
-      for (int it = 0; it < 8; ++it) {
-        const int item = it * kConvThreads + ct;   // (row r, 16-byte source chunk j)
-        const int r = item >> 3, j = item & 7;
-        const uint4 raw = *reinterpret_cast<const uint4*>(src + r * 128 + ((j ^ (r & 7)) << 4));
-        const uint32_t* rw = reinterpret_cast<const uint32_t*>(&raw);
-        uint32_t o[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t lo, hi;
-          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((unsigned short)(rw[q] & 0xffffu)));
-          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((unsigned short)(rw[q] >> 16)));
-          o[2 * q] = lo;
-          o[2 * q + 1] = hi;
-        }
-        // elements 16j..16j+15 of row r -> half j/4, 16-byte chunks 2j%8 and 2j%8+1
-        uint8_t* hbase = dst + (j >> 2) * (C::A_BYTES / 2) + r * 128;
-        const int c0 = (2 * j) & 7;
-        *reinterpret_cast<uint4*>(hbase + ((c0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(hbase + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&raw_empty[rs]);
-      mbar_arrive(&a_full[as]);
-      ++nr;
-      ++na;
       u.advance();
     }
   }
@@ -700,7 +862,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
 bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
 
-// Launches one configuration.  B rows are a.p.q viewed as [M * NCOL, 128] bf16.
+// Launches one configuration.  Query rows are a.p.q viewed as [M * NCOL, 128] bf16.
 template <class C>
 cudaError_t launch_tc(const TcArgs& a_in, cudaStream_t st) {
   TcArgs a = a_in;
@@ -715,7 +877,8 @@ cudaError_t launch_tc(const TcArgs& a_in, cudaStream_t st) {
     ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.keys, 128, (uint64_t)p.n_keys, 128, 128, krows);
   else
     ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.keys, 128, (uint64_t)p.n_keys, 256, 64, krows);
-  ok = ok && make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, 128, (uint64_t)(p.M * C::NCOL), 256, 64, C::N);
+  ok = ok && make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, 128, (uint64_t)(p.M * C::NCOL), 256, 64,
+                          C::NQ * C::NCOL);
   if (!ok) return cudaErrorInvalidValue;
   a.G = (p.M + C::NQ - 1) / C::NQ;
   cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);

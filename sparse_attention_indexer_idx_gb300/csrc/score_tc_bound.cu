@@ -23,7 +23,7 @@ cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const floa
   a.row_mask = row_mask;
   const bool shared = prep.key_off == nullptr;
   if (prep.k_dtype == IDX_FP8_E4M3)
-    return shared ? launch_tc<TcCfg<IDX_FP8_E4M3, 32, 8, kBound>>(a, st)
+    return shared ? launch_tc<TcCfg<IDX_FP8_E4M3, 32, 4, kBound>>(a, st)
                   : launch_tc<TcCfg<IDX_FP8_E4M3, 32, 1, kBound>>(a, st);
   return shared ? launch_tc<TcCfg<IDX_BF16, 32, 8, kBound>>(a, st) : launch_tc<TcCfg<IDX_BF16, 32, 1, kBound>>(a, st);
 }
