@@ -102,29 +102,33 @@ struct TcCfg {
   static constexpr bool BOUND = (MODE == kBound);
   static constexpr int NCOLX = FP8 ? 2 * NCOL : NCOL;   // MMA columns per query (hi, lo for FP8)
   static constexpr int N = NQ * NCOLX;
-  static constexpr int A_BYTES = FP8 ? 128 * 128 : 128 * 128 * 2;   // one key tile
+  // 128-key subtiles per work unit: FP8 per-row scoring takes 256 keys (32 KB,
+  // one TMA box) per unit, so every barrier round trip, commit and schedule
+  // step covers as many key bytes as a bf16 tile
+  static constexpr int SUB = (FP8 && MODE == kScore && NQ == 1 && N <= 128) ? 2 : 1;
+  static constexpr int UKEYS = 128 * SUB;
+  static constexpr int A_BYTES = SUB * (FP8 ? 128 * 128 : 128 * 128 * 2);   // one unit of keys
+  static constexpr int SUB_BYTES = A_BYTES / SUB;                           // one 128-key subtile
   static constexpr int BQ_BYTES = FP8 ? 0 : NQ * NCOL * 256;         // bf16 query rows as loaded
   static constexpr int B8_BYTES = FP8 ? N * 128 : 0;                 // e4m3 hi and lo rows (FP8)
   static constexpr int B_BYTES = BQ_BYTES + B8_BYTES;                // one query buffer
   static constexpr int SB = (NQ > 1) ? 1 : 2;
-  static constexpr int SACC = (N >= 256) ? 2 : 4;
+  static constexpr int SACC = (SUB * N >= 256) ? 2 : 4;
   // FP8: key scales of one tile; their ring is deeper than the key ring by the
   // tiles that can sit between the MMA and the epilogue, so a key slot is free
   // as soon as its MMAs complete
-  static constexpr int SC_BYTES = FP8 ? 512 : 0;
+  static constexpr int SC_BYTES = FP8 ? 512 * SUB : 0;
   static constexpr int SA_FIT = (220 * 1024 - SB * B_BYTES - (SACC + 2) * SC_BYTES) / (A_BYTES + SC_BYTES);
   static constexpr int SA = FP8 ? (SA_FIT > 12 ? 12 : SA_FIT) : ((BQ_BYTES * SB <= 32768) ? 5 : 4);
   static constexpr int SSC = FP8 ? SA + SACC + 2 : 0;
   static constexpr int SSC_MOD = SSC > 0 ? SSC : 1;
-  static constexpr int IL = (N <= 128) ? 2 : 1;   // MMA chains interleaved (tiles per issue round)
-  static constexpr int TMEM_COLS = tc_pow2_cols(SACC * N);
-  // epilogue warps: two per TMEM lane quarter when a tile holds several queries
-  // (each takes every other query), else one
-  static constexpr int NE = 8;
-  // epilogue warps that read one tile: all 8 when a tile holds several queries
-  // (two per TMEM lane quarter, alternating queries), else 4 (the two warps of a
-  // quarter take alternate tiles)
-  static constexpr int EPT = (NQ > 1) ? 8 : 4;
+  static constexpr int IL = (SUB == 1 && N <= 128) ? 2 : 1;   // units whose MMA chains are interleaved
+  static constexpr int TMEM_COLS = tc_pow2_cols(SACC * SUB * N);
+  static constexpr int NE = 8;   // epilogue warps, two per TMEM lane quarter
+  // epilogue warps that read one unit: all 8 when a unit holds several queries
+  // (alternating queries) or two subtiles (one warp of a quarter per subtile),
+  // else 4 (the two warps of a quarter take alternate units)
+  static constexpr int EPT = (NQ > 1 || SUB > 1) ? 8 : 4;
   static constexpr int NCONV = FP8 ? 2 : 0;   // warps that split the query rows (FP8)
   static constexpr int NTHREADS = 32 * (2 + NE + NCONV);
   // shared memory layout (offsets from a 1024-aligned base)
@@ -146,6 +150,7 @@ struct TcCfg {
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N");
+  static_assert(SACC * SUB * N <= 512, "TMEM columns");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -174,7 +179,7 @@ __device__ __forceinline__ int64_t tc_group_tiles(const TcArgs& A, int64_t g, bo
     if (A.row_mask && !A.row_mask[m]) len = 0;
     mx = len > mx ? len : mx;
   }
-  return (mx + 127) / 128;
+  return (mx + C::UKEYS - 1) / C::UKEYS;
 }
 
 __device__ __forceinline__ int64_t warp_incl_scan(int64_t v) {
@@ -437,14 +442,14 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         bool sok = true;
         if (lane == 0) sok = mbar_wait(&sc_empty[ss], ((na / C::SSC_MOD) & 1) ^ 1, abort_flag);
         if (!__shfl_sync(0xffffffffu, sok, 0)) break;
-        float* sdst = sScale + ss * 128 + 4 * lane;
+        float* sdst = sScale + ss * C::UKEYS + 4 * lane;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int pos = (int)(u.t * 128) + 4 * lane + i;
+        for (int i = 0; i < 4 * C::SUB; ++i) {
+          const int pos = (int)(u.t * C::UKEYS) + 128 * (i >> 2) + 4 * lane + (i & 3);
           int64_t row = gbase + pos;
           if (C::GATHER) row = gbase + (pos < gcnt ? (int64_t)args.list[u.g * args.gld + pos] : 0);
           row = row < 0 ? 0 : (row >= args.p.n_keys ? args.p.n_keys - 1 : row);
-          cp_async_4(sdst + i, args.p.key_scale + row);
+          cp_async_4(sdst + 128 * (i >> 2) + (i & 3), args.p.key_scale + row);
         }
         cp_async_arrive_noinc(&sc_full[ss]);
       }
@@ -465,7 +470,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         tma_gather4(dst + lane * 512, &tmap_k, fbar, 0, y[0], y[1], y[2], y[3]);
         if (!C::FP8) tma_gather4(dst + C::A_BYTES / 2 + lane * 512, &tmap_k, fbar, 64, y[0], y[1], y[2], y[3]);
       } else if (lane == 0) {
-        const int32_t y = (int32_t)(gbase + u.t * 128);
+        const int32_t y = (int32_t)(gbase + u.t * C::UKEYS);
         mbar_arrive_expect_tx(fbar, C::A_BYTES);
         tma_load_2d(dst, &tmap_k, fbar, 0, y);
         if (!C::FP8) tma_load_2d(dst + C::A_BYTES / 2, &tmap_k, fbar, 64, y);
@@ -520,11 +525,20 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t b0 = smem_u32(sB + cur_bs * C::B_BYTES);
+        // two independent chains: two units (IL), or the two subtiles of one unit
         uint32_t a0[2], d[2];
+        if (C::SUB > 1) {
+          n = 2;
+          a0[0] = smem_u32(sA + (na % C::SA) * C::A_BYTES);
+          a0[1] = a0[0] + C::SUB_BYTES;
+          d[0] = tmem_base + (uint32_t)((nacc % C::SACC) * C::SUB * C::N);
+          d[1] = d[0] + C::N;
+        } else {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          a0[i] = smem_u32(sA + ((na + i) % C::SA) * C::A_BYTES);
-          d[i] = tmem_base + (uint32_t)(((nacc + i) % C::SACC) * C::N);
+          for (int i = 0; i < 2; ++i) {
+            a0[i] = smem_u32(sA + ((na + i) % C::SA) * C::A_BYTES);
+            d[i] = tmem_base + (uint32_t)(((nacc + i) % C::SACC) * C::N);
+          }
         }
         if constexpr (C::FP8) {
           // e4m3 x e4m3, K = 32 per instruction: four steps of 32 bytes along the 128-byte rows
@@ -547,6 +561,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           }
         }
         issued = true;
+        if (C::SUB > 1) n = 1;                 // one unit
         for (int i = 0; i < n; ++i) {
           tc_commit(&a_empty[(na + i) % C::SA]);
           tc_commit(&acc_full[(nacc + i) % C::SACC]);
@@ -570,6 +585,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     const int qfirst = C::NQ > 1 ? (ew >> 2) : 0;   // first query of this warp in a tile
     constexpr int QSTEP = C::NQ > 1 ? 2 : 1;
     const int tile_par = ew >> 2;              // one query per tile: the parity of the tiles this warp takes
+    const int sub = C::SUB > 1 ? (ew >> 2) : 0;   // two subtiles per unit: the one this warp reads
     const int row_in_tile = quarter * 32 + lane;
     float* sW = sW_all + ew * C::NQ * C::NCOL;
     int32_t* sLen = sLen_all + ew * C::NQ;
@@ -623,13 +639,13 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         }
         __syncwarp();
       }
-      if (C::NQ == 1 && (int)(nacc & 1) != tile_par) {
+      if (C::NQ == 1 && C::SUB == 1 && (int)(nacc & 1) != tile_par) {
         ++nacc;
         u.advance();
         continue;
       }
       const int acc = nacc % C::SACC;
-      const int key = (int)(u.t * 128) + row_in_tile;
+      const int key = (int)(u.t * C::UKEYS) + sub * 128 + row_in_tile;
       bool got = mbar_wait(&acc_full[acc], (nacc / C::SACC) & 1, abort_flag);
       // the key-tile slot of this unit (bound: read below for ||k||, so the slot is
       // held until this warp releases it) and its scale slot (FP8)
@@ -641,7 +657,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       // FP8: all queries of a group read the same key sequence, so one scale serves them all
-      const float kscale = C::FP8 ? sScale[sslot * 128 + row_in_tile] : 1.0f;
+      const float kscale = C::FP8 ? sScale[sslot * C::UKEYS + sub * 128 + row_in_tile] : 1.0f;
       float knorm = 0.0f;
       if (C::BOUND) {
         // ||k|| of this lane's key (codes for FP8) from the MMA-ready tile
@@ -687,7 +703,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       for (int qi = qfirst; qi < C::NQ; qi += QSTEP) {
         const int64_t m = cur_g * C::NQ + qi;
         if (m >= args.p.M) break;
-        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::N + qi * C::NCOLX);
+        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                              (uint32_t)((acc * C::SUB + sub) * C::N + qi * C::NCOLX);
         const float* wq = sW + qi * C::NCOL;
         const int len = sLen[qi];
         if (!C::BOUND) {
@@ -872,7 +889,7 @@ cudaError_t launch_tc(const TcArgs& a_in, cudaStream_t st) {
   if (p.n_keys >= ((int64_t)1 << 31) || p.M * C::NCOL >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
   CUtensorMap tk, tq;
   bool ok;
-  const uint32_t krows = C::GATHER ? 1u : 128u;     // gather4 wants a one-row box
+  const uint32_t krows = C::GATHER ? 1u : (uint32_t)C::UKEYS;     // gather4 wants a one-row box
   if (C::FP8)
     ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.keys, 128, (uint64_t)p.n_keys, 128, 128, krows);
   else
