@@ -443,7 +443,12 @@ def main():
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         # one event pair per step around the dominant kernel, on the launching stream
+        # (created and recorded once here, so no event is created inside the timed region)
         per_step = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        for evs in per_step + [[t_start, t_end]]:
+            for e in evs:
+                e.record(stream)
+        torch.cuda.synchronize()
         t_start.record(stream)
         for i in range(args.steps):
             step.ev = per_step[i]

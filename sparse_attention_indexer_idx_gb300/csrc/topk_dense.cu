@@ -191,90 +191,109 @@ __device__ void sort_candidates(uint64_t* buf, int S) {
 
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total);
 
-// Sorts the n nonzero, distinct composites src[0..n) descending into dst by one
-// bucket pass on the 11 key bits just below the common prefix of the smallest
-// and largest key (monotone in the key), then an insertion sort inside each
-// bucket (one thread per bucket).  Returns false, with src untouched, when a
-// bucket would hold more than kBucketMax entries (heavy ties): the caller then
-// uses the bitonic network.
+// Sorts the n nonzero, distinct composites src[0..n) descending: one bucket
+// pass into dst -- 8192 buckets spread evenly over [min key, max key] (a
+// monotone map; bucket 0 holds the largest keys) -- then every element finds
+// its place inside its bucket by counting the larger ones there and is written
+// back to src.  The bucket arrays live in the upper half of the key area,
+// which every caller leaves free (src and dst hold at most 8192 composites
+// each and sit elsewhere).  have_range: sh.kmin / sh.kmax already hold the
+// keys' minimum and maximum.  Returns false, with src untouched, when a bucket
+// would hold more than kBucketMax entries (heavy ties): the caller then uses
+// the bitonic network.
 constexpr uint32_t kBucketMax = 32;
-__device__ bool bucket_sort_desc(TkShared& sh, const uint64_t* src, int n, uint64_t* dst) {
+constexpr int kSortBuckets = 8192;
+__device__ bool bucket_sort_desc(TkShared& sh, uint64_t* src, int n, uint64_t* dst, bool have_range = false) {
   const int tid = threadIdx.x;
-  if (tid == 0) {
-    sh.kmin = 0xffffffffu;
-    sh.kmax = 0u;
-    sh.bmax = 0u;
+  uint32_t* bh = sh.keys + TK_CH / 2;          // count, then cursor / end, per bucket
+  uint32_t* bs = bh + kSortBuckets;           // first slot per bucket
+  static_assert(TK_CH / 2 + 2 * kSortBuckets <= TK_CH, "bucket arrays");
+  constexpr int PER = kSortBuckets / TK_NT;   // buckets per thread (contiguous)
+  static_assert(PER == 8, "two 16-byte vectors per thread");
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  reinterpret_cast<uint4*>(bh)[2 * tid] = z;
+  reinterpret_cast<uint4*>(bh)[2 * tid + 1] = z;
+  if (!have_range) {
+    if (tid == 0) {
+      sh.kmin = 0xffffffffu;
+      sh.kmax = 0u;
+    }
+    __syncthreads();
+    uint32_t mn = 0xffffffffu, mx = 0u;
+    for (int i = tid; i < n; i += TK_NT) {
+      const uint32_t k = (uint32_t)(src[i] >> 32);
+      mn = min(mn, k);
+      mx = max(mx, k);
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((tid & 31) == 0) {
+      atomicMin(&sh.kmin, mn);
+      atomicMax(&sh.kmax, mx);
+    }
   }
-  for (int b = tid; b < kTopkBins; b += TK_NT) sh.hist[b] = 0;
+  if (tid == 0) sh.bmax = 0u;
   __syncthreads();
-  uint32_t mn = 0xffffffffu, mx = 0u;
-  for (int i = tid; i < n; i += TK_NT) {
-    const uint32_t k = (uint32_t)(src[i] >> 32);
-    mn = min(mn, k);
-    mx = max(mx, k);
-  }
-  mn = __reduce_min_sync(0xffffffffu, mn);
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  if ((tid & 31) == 0) {
-    atomicMin(&sh.kmin, mn);
-    atomicMax(&sh.kmax, mx);
-  }
+  const uint32_t kmin = sh.kmin;
+  const float scale = (float)kSortBuckets / ((float)(sh.kmax - kmin) + 1.0f);
+  auto bucket = [&](uint64_t v) {
+    uint32_t b = (uint32_t)((float)((uint32_t)(v >> 32) - kmin) * scale);
+    b = b < (uint32_t)kSortBuckets ? b : (uint32_t)kSortBuckets - 1u;
+    return (uint32_t)kSortBuckets - 1u - b;   // largest keys first
+  };
+  for (int i = tid; i < n; i += TK_NT) atomicAdd(&bh[bucket(src[i])], 1u);
   __syncthreads();
-  const uint32_t diff = sh.kmin ^ sh.kmax;
-  const int top = diff ? 31 - __clz((int)diff) : 0;
-  const int shift = top >= 10 ? top - 10 : 0;
-  for (int i = tid; i < n; i += TK_NT) atomicAdd(&sh.hist[((uint32_t)(src[i] >> 32) >> shift) & 0x7ffu], 1u);
-  __syncthreads();
-  // exclusive scan over the buckets, highest bucket first; largest bucket
-  constexpr int PER = kTopkBins / TK_NT;
-  uint32_t loc[PER], sum = 0, big = 0;
+  // exclusive scan over the buckets in order; the largest per-thread range
+  const uint4 c0 = reinterpret_cast<const uint4*>(bh)[2 * tid];
+  const uint4 c1 = reinterpret_cast<const uint4*>(bh)[2 * tid + 1];
+  const uint32_t cnt8[PER] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  uint32_t sum = 0, big = 0;
 #pragma unroll
   for (int q = 0; q < PER; ++q) {
-    loc[q] = sh.hist[kTopkBins - 1 - (tid * PER + q)];
-    sum += loc[q];
-    big = max(big, loc[q]);
+    sum += cnt8[q];
+    big = max(big, cnt8[q]);
   }
   uint32_t total;
   uint32_t run = block_excl_scan(sum, sh.red, &total);
   big = __reduce_max_sync(0xffffffffu, big);
   if ((tid & 31) == 0) atomicMax(&sh.bmax, big);
+  uint32_t st8[PER];
 #pragma unroll
   for (int q = 0; q < PER; ++q) {
-    const int b = kTopkBins - 1 - (tid * PER + q);
-    sh.bstart[b] = run;
-    sh.hist[b] = run;          // becomes the scatter cursor
-    run += loc[q];
+    st8[q] = run;
+    run += cnt8[q];
   }
+  reinterpret_cast<uint4*>(bs)[2 * tid] = make_uint4(st8[0], st8[1], st8[2], st8[3]);
+  reinterpret_cast<uint4*>(bs)[2 * tid + 1] = make_uint4(st8[4], st8[5], st8[6], st8[7]);
+  reinterpret_cast<uint4*>(bh)[2 * tid] = make_uint4(st8[0], st8[1], st8[2], st8[3]);   // scatter cursors
+  reinterpret_cast<uint4*>(bh)[2 * tid + 1] = make_uint4(st8[4], st8[5], st8[6], st8[7]);
   __syncthreads();
   if (sh.bmax > kBucketMax) return false;
   for (int i = tid; i < n; i += TK_NT) {
     const uint64_t v = src[i];
-    const uint32_t pos = atomicAdd(&sh.hist[((uint32_t)(v >> 32) >> shift) & 0x7ffu], 1u);
+    const uint32_t pos = atomicAdd(&bh[bucket(v)], 1u);
     dst[pos] = v;
   }
   __syncthreads();
-  for (int b = tid; b < kTopkBins; b += TK_NT) {
-    const int s0 = (int)sh.bstart[b], e = (int)sh.hist[b];
-    for (int i = s0 + 1; i < e; ++i) {
-      const uint64_t v = dst[i];
-      int j = i - 1;
-      while (j >= s0 && dst[j] < v) {
-        dst[j + 1] = dst[j];
-        --j;
-      }
-      dst[j + 1] = v;
-    }
+  // place: bucket start + the number of larger elements in the bucket
+  for (int i = tid; i < n; i += TK_NT) {
+    const uint64_t v = dst[i];
+    const uint32_t b = bucket(v);
+    const int b0 = (int)bs[b], b1 = (int)bh[b];
+    int r = b0;
+    for (int q = b0; q < b1; ++q) r += dst[q] > v ? 1 : 0;
+    src[r] = v;
   }
   __syncthreads();
   return true;
 }
 
-// Descending order of src[0..cnt) (nonzero, distinct): returns the buffer that
-// holds it -- dst after the bucket pass, or src itself (zero-padded to P and
-// bitonic-sorted) when the buckets are too uneven.
+// Descending order of src[0..cnt) (nonzero, distinct), in place (dst is
+// scratch): the bucket pass, or, when the buckets are too uneven, the bitonic
+// network over src zero-padded to P.
 __device__ const uint64_t* order_desc(TkShared& sh, uint64_t* src, int cnt, int P, uint64_t* dst) {
   if (cnt <= 1) return src;
-  if (bucket_sort_desc(sh, src, cnt, dst)) return dst;
+  if (bucket_sort_desc(sh, src, cnt, dst)) return src;
   for (int i = cnt + threadIdx.x; i < P; i += TK_NT) src[i] = 0ull;
   __syncthreads();
   sort_candidates(src, P);
@@ -423,24 +442,49 @@ __global__ void __launch_bounds__(TK_NT, 1)
   }
   __syncthreads();
 
-  // Candidates: every key >= T, written through a block prefix sum (no atomics).
-  auto compact = [&](uint32_t T, uint32_t KT, uint32_t IT, bool exact_ids) {
+  // Candidates: every key >= T (or, exact_ids, the exact top set), written
+  // through a block prefix sum (no atomics); their smallest and largest key go
+  // to sh.kmin / sh.kmax.  `counted`: this thread's count of them when the
+  // caller already has it.
+  auto compact = [&](uint32_t T, uint32_t KT, uint32_t IT, bool exact_ids, int counted) {
     auto take = [&](int i) {
       const uint32_t kk = K_[i];
       return exact_ids ? (kk > KT || (kk == KT && id_key(idof(i)) >= IT)) : kk >= T;
     };
     uint32_t local = 0;
-    for (int i = tid; i < cn; i += TK_NT) local += take(i) ? 1u : 0u;
+    if (counted >= 0) {
+      local = (uint32_t)counted;
+    } else {
+      for (int i = tid; i < cn; i += TK_NT) local += take(i) ? 1u : 0u;
+    }
+    if (tid == 0) {
+      sh.kmin = 0xffffffffu;
+      sh.kmax = 0u;
+    }
     uint32_t total;
     uint32_t off = block_excl_scan(local, sh.red, &total);
-    for (int i = tid; i < cn; i += TK_NT)
-      if (take(i) && off < TK_CAP) sh.cand[off++] = composite(K_[i], idof(i));
+    uint32_t mn = 0xffffffffu, mx = 0u;
+    for (int i = tid; i < cn; i += TK_NT) {
+      if (take(i)) {
+        const uint32_t kk = K_[i];
+        mn = min(mn, kk);
+        mx = max(mx, kk);
+        if (off < (uint32_t)TK_CAP) sh.cand[off] = composite(kk, idof(i));
+        ++off;
+      }
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((tid & 31) == 0) {
+      atomicMin(&sh.kmin, mn);
+      atomicMax(&sh.kmax, mx);
+    }
     if (tid == 0) sh.cnt = total;
     __syncthreads();
   };
 
   if (cn <= K) {
-    compact(0u, 0u, 0u, false);          // every key (keys are >= 1)
+    compact(0u, 0u, 0u, false, -1);      // every key (keys are >= 1)
   } else {
     // 1. threshold from 1024 evenly spaced sample keys: the sample rank r that
     //    should leave ~1.15 K + 3 sigma keys above, located by a two-level
@@ -452,7 +496,7 @@ __global__ void __launch_bounds__(TK_NT, 1)
     const float expect = (float)nvalid * (float)K / (float)cn;
     int r = (int)ceilf(1.15f * expect + 3.0f * sqrtf(expect)) + 1;
     r = r < 1 ? 1 : (r > nvalid ? nvalid : r);
-    uint32_t T = 0, count = 0;
+    uint32_t T = 0, count = 0, mine = 0;
     bool ok = false;
 #pragma unroll 1
     for (int attempt = 0; attempt < 3; ++attempt) {
@@ -473,6 +517,7 @@ __global__ void __launch_bounds__(TK_NT, 1)
       __syncthreads();
       uint32_t local = 0;
       for (int i = tid; i < cn; i += TK_NT) local += (K_[i] >= T) ? 1u : 0u;
+      mine = local;
       count = block_sum_u32(local, sh.red);
       if (count > (uint32_t)TK_CAP) break;
       if (count >= (uint32_t)K) {
@@ -483,7 +528,7 @@ __global__ void __launch_bounds__(TK_NT, 1)
       r = min(nvalid, 2 * r);
     }
     if (ok) {
-      compact(T, 0u, 0u, false);
+      compact(T, 0u, 0u, false, (int)mine);
     } else {
       // exact: radix select of the K-th key, then of the ids among its ties
       uint32_t above, eq;
@@ -498,13 +543,25 @@ __global__ void __launch_bounds__(TK_NT, 1)
         uint32_t above2, eq2;
         IT = smem_radix_select(sh, cn, need, idk, tie, &above2, &eq2);
       }
-      compact(0u, KT, IT, true);
+      compact(0u, KT, IT, true, -1);
     }
   }
   __syncthreads();
   int cnt = (int)min(sh.cnt, (uint32_t)TK_CAP);
-  // exactly min(K, cn) composites, into the (now free) key area
-  uint64_t* best = reinterpret_cast<uint64_t*>(sh.keys);
+  uint64_t* best = reinterpret_cast<uint64_t*>(sh.keys);   // the (now free) key area
+  if (single && cnt > K) {
+    // the candidates are distinct composites: when their buckets are even, one
+    // bucket sort of all of them orders the row and its first K are the answer
+    if (sh.cnt <= (uint32_t)TK_CAP && bucket_sort_desc(sh, sh.cand, cnt, best, true)) {
+      for (int j = tid; j < K; j += TK_NT) {
+        const uint64_t v = sh.cand[j];
+        out_ids[m * K + j] = key_id((uint32_t)v);
+        if (out_scores) out_scores[m * K + j] = key_score((uint32_t)(v >> 32));
+      }
+      return;
+    }
+  }
+  // exactly min(K, cn) composites
   if (cnt > K) {
     select_exact_k(sh, sh.cand, cnt, K, best);
     cnt = K;
