@@ -185,8 +185,8 @@ class IndexerStep:
         self.ctx = self.p.key_len
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         self.score_ms = []
-        # score + top-K (a merge launch for rows above 32768) + witness merge
-        self.launches = 1 + (1 if self.ld <= 32768 else 2) + (1 if self.S else 0)
+        # score + top-K (filter and finish kernels) + witness merge
+        self.launches = 1 + 2 + (1 if self.S else 0)
 
     def run(self, timed=False):
         B, p = self.B, self.p
@@ -243,9 +243,9 @@ class DosaStep:
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         self.score_ms = []
         # kernels dosa_topk enqueues per call: seeds, seed scores and top-K, planner,
-        # bound scan, rescoring, merge, fallback and statistics (top-K stages
-        # over rows above 32768 take a second, merge launch)
-        two = lambda n: 1 if n <= 32768 else 2
+        # bound scan, rescoring, merge, fallback and statistics (every top-K stage is
+        # a filter and a finish kernel)
+        two = lambda n: 2
         L = int(np.max(wp.key_len))
         NS = min(max(n_seed, wp.K), L)
         if wp.key_off is None:

@@ -128,8 +128,9 @@ idx_status idx_topk(const idx_problem* p, int32_t K, int32_t* out_ids, float* ou
  * The top-K step alone, on score rows the caller already has: row m is
  * scores[m*ld .. m*ld + lens[m]-1] (device float32, lens device int32, clamped
  * to [0, max_len]), ids are positions in the row.  Same order, padding and K
- * limit as idx_topk.  The workspace is only needed for rows longer than 32768
- * (the per-chunk candidate lists); its size is 0 otherwise. */
+ * limit as idx_topk.  The workspace holds, per row and per 16384 scores of
+ * max_len, a candidate count and 4096 candidate slots of 8 bytes: about
+ * M * max_len * 2 bytes. */
 size_t idx_topk_scores_workspace_size(int64_t M, int32_t max_len, int32_t K);
 idx_status idx_topk_scores(const float* scores, int64_t ld, const int32_t* lens, int64_t M, int32_t max_len,
                            int32_t K, int32_t* out_ids, float* out_scores, void* ws, size_t ws_bytes,

@@ -2,24 +2,18 @@
 // ("DoSA：用安全上界减少 Indexer 的完整打分", section 1 and the note after
 // section 2: selection by the original scorer with one total order for ties).
 //
-// A row is cut into chunks of TK_CH = 32768 scores; one thread block owns a
-// chunk and keeps it in registers (64 ordered keys per thread), so the row is
-// read from memory exactly once.  Selection inside a chunk:
-//   1. 1024 keys sampled from the chunk are bitonic-sorted; the sample rank
-//      that should leave ~1.2 K + 3 sigma keys above it gives a threshold T;
-//   2. one pass counts the keys >= T (block reduction, no atomics); if the
-//      count is at least K and fits the candidate buffer, a second pass
-//      compacts them (warp ballot + one atomic per warp) as 64-bit composites
-//      key << 32 | ~id, whose descending order is exactly (score desc, id asc);
-//      otherwise T is lowered (or, failing that, an exact radix select on the
-//      registers takes over);
-//   3. the K winners are bitonic-sorted (in-thread and warp-shuffle stages,
-//      shared memory only for strides that cross warps).
-// The candidates are cut to exactly K by two radix selects (key, then id among
-// ties) and only then sorted, in registers.  A row of one chunk writes its
-// result directly; longer rows write every chunk's (unsorted) top-K set to the
-// workspace, and a merge kernel folds the sets into a running best-K and sorts
-// once.
+// Two passes over a row's scores, which are read once from memory:
+//   filter  one thread block per (row, 16384 scores) takes a row threshold T
+//           from 1024 evenly spaced samples of the row (the same in every block
+//           of the row) and writes the keys >= T, as 64-bit composites
+//           key << 32 | ~id whose descending order is exactly (score desc, id
+//           asc), and their count to the chunk's own slots;
+//   finish  one thread block per row bucket-sorts the ~1.5-2.5 K candidates at
+//           once and writes the first K.  A bucket with heavy ties sends the
+//           candidates through two radix selects (key, then id among ties) that
+//           cut them to exactly K and a register bitonic sort; a threshold that
+//           missed (too few or too many candidates) sends the row through an
+//           exact radix select over its scores.
 #include "internal.h"
 #include "topk.cuh"
 
@@ -27,20 +21,18 @@ namespace idx {
 
 constexpr int TK_NT = 1024;
 constexpr int TK_CH = 32768;
-constexpr int TK_NS = 1024;
 constexpr int TK_CAP = 8192;
 
+// Shared memory of the finish pass: candidates, and a scratch area whose lower
+// half takes sorted / selected composites and upper half the bucket arrays.
 struct TkShared {
-  uint32_t keys[TK_CH];       // the chunk's ordered keys
+  uint32_t keys[TK_CH];       // scratch (128 KB)
   uint64_t cand[TK_CAP];
-  uint32_t samp[TK_NS];
   uint32_t hist[kTopkBins];
-  uint32_t bstart[kTopkBins];
   uint32_t red[TK_NT / 32];
-  uint32_t cnt;
   uint32_t found_bin;
   uint32_t found_above;
-  uint32_t kmin, kmax, bmax;
+  uint32_t kmin, kmax, bmax, kend;
 };
 
 __device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* red) {
@@ -198,12 +190,15 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, u
 // back to src.  The bucket arrays live in the upper half of the key area,
 // which every caller leaves free (src and dst hold at most 8192 composites
 // each and sit elsewhere).  have_range: sh.kmin / sh.kmax already hold the
-// keys' minimum and maximum.  Returns false, with src untouched, when a bucket
-// would hold more than kBucketMax entries (heavy ties): the caller then uses
-// the bitonic network.
-constexpr uint32_t kBucketMax = 32;
+// keys' minimum and maximum.  Only the first `limit` places are needed:
+// buckets that start at or after it are left out of the scatter and the
+// placement.  Returns false, with src untouched, when a bucket would hold more
+// than kBucketMax entries (heavy ties): the caller then uses the bitonic
+// network.
+constexpr uint32_t kBucketMax = 256;
 constexpr int kSortBuckets = 8192;
-__device__ bool bucket_sort_desc(TkShared& sh, uint64_t* src, int n, uint64_t* dst, bool have_range = false) {
+__device__ bool bucket_sort_desc(TkShared& sh, uint64_t* src, int n, uint64_t* dst, bool have_range = false,
+                                 int limit = 0x7fffffff) {
   const int tid = threadIdx.x;
   uint32_t* bh = sh.keys + TK_CH / 2;          // count, then cursor / end, per bucket
   uint32_t* bs = bh + kSortBuckets;           // first slot per bucket
@@ -232,7 +227,10 @@ __device__ bool bucket_sort_desc(TkShared& sh, uint64_t* src, int n, uint64_t* d
       atomicMax(&sh.kmax, mx);
     }
   }
-  if (tid == 0) sh.bmax = 0u;
+  if (tid == 0) {
+    sh.bmax = 0u;
+    sh.kend = (uint32_t)n;
+  }
   __syncthreads();
   const uint32_t kmin = sh.kmin;
   const float scale = (float)kSortBuckets / ((float)(sh.kmax - kmin) + 1.0f);
@@ -257,12 +255,16 @@ __device__ bool bucket_sort_desc(TkShared& sh, uint64_t* src, int n, uint64_t* d
   uint32_t run = block_excl_scan(sum, sh.red, &total);
   big = __reduce_max_sync(0xffffffffu, big);
   if ((tid & 31) == 0) atomicMax(&sh.bmax, big);
-  uint32_t st8[PER];
+  const uint32_t lim = (uint32_t)(limit < n ? limit : n);
+  uint32_t st8[PER], kend = 0xffffffffu;
 #pragma unroll
   for (int q = 0; q < PER; ++q) {
     st8[q] = run;
+    if (run >= lim && cnt8[q]) kend = min(kend, run);   // first bucket left out
     run += cnt8[q];
   }
+  kend = __reduce_min_sync(0xffffffffu, kend);
+  if ((tid & 31) == 0 && kend != 0xffffffffu) atomicMin(&sh.kend, kend);
   reinterpret_cast<uint4*>(bs)[2 * tid] = make_uint4(st8[0], st8[1], st8[2], st8[3]);
   reinterpret_cast<uint4*>(bs)[2 * tid + 1] = make_uint4(st8[4], st8[5], st8[6], st8[7]);
   reinterpret_cast<uint4*>(bh)[2 * tid] = make_uint4(st8[0], st8[1], st8[2], st8[3]);   // scatter cursors
@@ -271,12 +273,16 @@ __device__ bool bucket_sort_desc(TkShared& sh, uint64_t* src, int n, uint64_t* d
   if (sh.bmax > kBucketMax) return false;
   for (int i = tid; i < n; i += TK_NT) {
     const uint64_t v = src[i];
-    const uint32_t pos = atomicAdd(&bh[bucket(v)], 1u);
+    const uint32_t b = bucket(v);
+    if (bs[b] >= lim) continue;
+    const uint32_t pos = atomicAdd(&bh[b], 1u);
     dst[pos] = v;
   }
   __syncthreads();
-  // place: bucket start + the number of larger elements in the bucket
-  for (int i = tid; i < n; i += TK_NT) {
+  // place: bucket start + the number of larger elements in the bucket; the
+  // scattered elements fill dst[0, kend)
+  const int used = (int)sh.kend;
+  for (int i = tid; i < used; i += TK_NT) {
     const uint64_t v = dst[i];
     const uint32_t b = bucket(v);
     const int b0 = (int)bs[b], b1 = (int)bh[b];
@@ -341,7 +347,8 @@ __device__ void select_exact_k(TkShared& sh, const uint64_t* src, int n, int K, 
 
 // Suffix search over sh.hist[0..nb) (bins high to low): the bin b with
 // (#in bins > b) < remaining <= (#in bins >= b) -> sh.found_bin/found_above.
-__device__ __forceinline__ void hist_suffix_find(TkShared& sh, int nb, uint32_t remaining) {
+template <class SH>
+__device__ __forceinline__ void hist_suffix_find(SH& sh, int nb, uint32_t remaining) {
   constexpr int PER = kTopkBins / TK_NT;
   uint32_t loc[PER], sum = 0;
 #pragma unroll
@@ -396,18 +403,29 @@ __device__ uint32_t smem_radix_select(TkShared& sh, int cn, uint32_t want, F f, 
   return prefix;
 }
 
-// One chunk of one row.  Writes the final top-K when the row is one chunk,
-// else the chunk's sorted top-K list (P = next_pow2(K) composites, 0-padded).
-__global__ void __launch_bounds__(TK_NT, 1)
-    topk_chunk_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ lens,
-                      idx_problem p, int use_p, int max_len, int K, int P, int32_t* __restrict__ out_ids,
-                      float* __restrict__ out_scores, uint64_t* __restrict__ lists, int n_chunks,
-                      const int32_t* __restrict__ id_map, int64_t id_ld, const int32_t* __restrict__ row_mask) {
-  extern __shared__ __align__(16) uint8_t tk_smem[];
-  TkShared& sh = *reinterpret_cast<TkShared*>(tk_smem);
-  const int64_t m = blockIdx.x;
-  const int c = blockIdx.y;
-  if (row_mask && !row_mask[m]) return;
+// ------------------------------------------------------------ the filter --
+// Pass 1, one thread block per (row, chunk of TF_CH scores): the keys >= a row
+// threshold T go to the chunk's slots (at most TF_CAPC; the count is written
+// whole).  Every block of a row takes T from the same 1024 evenly spaced
+// samples of the row with the same code, so all of them use the same T: the
+// sample rank that should leave ~1.15 K + 3.5 sigma keys above it (a two-level
+// histogram of the samples, top 11 bits then the next 11), rounded down to its
+// 10-bit prefix.
+constexpr int TF_NT = 1024;
+constexpr int TF_PER = 16;
+constexpr int TF_CH = TF_NT * TF_PER;
+constexpr int TF_CAPC = TF_CH / 4;          // candidate slots per chunk
+constexpr int TK_ROWCAP = TK_CAP;           // candidates a row may sort
+
+struct TfShared {
+  uint32_t hist[kTopkBins];
+  uint32_t red[TF_NT / 32];
+  uint32_t found_bin;
+  uint32_t found_above;
+};
+
+__device__ __forceinline__ int row_length(const int32_t* lens, const idx_problem& p, int use_p, int max_len,
+                                          int64_t m) {
   int n;
   if (use_p) {
     int64_t off;
@@ -416,212 +434,169 @@ __global__ void __launch_bounds__(TK_NT, 1)
     n = lens[m];
     n = n < 0 ? 0 : (n > max_len ? max_len : n);
   }
-  const int64_t base = (int64_t)c * TK_CH;
-  if (c > 0 && base >= n) return;
-  const bool single = n <= TK_CH;
-  const int cn = (int)min((int64_t)TK_CH, (int64_t)n - base > 0 ? (int64_t)n - base : 0);
-  const float* row = scores + m * ld + base;
+  return n;
+}
+
+// The row threshold (n > K): see above.  Uniform across the block.
+__device__ uint32_t row_threshold(TfShared& sh, const float* row, int n, int K) {
   const int tid = threadIdx.x;
-  const int32_t* idm = id_map ? id_map + m * id_ld + base : nullptr;
-  auto idof = [&](int i) { return idm ? idm[i] : (int32_t)(base + i); };
-
-  // stage the chunk as ordered keys in shared memory (8 loads in flight per thread)
-  uint32_t* K_ = sh.keys;
-  for (int i0 = 0; i0 < cn; i0 += 8 * TK_NT) {
-    float f[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * TK_NT + tid;
-      f[u] = i < cn ? __ldg(row + i) : 0.0f;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * TK_NT + tid;
-      if (i < cn) K_[i] = score_key(f[u]);
-    }
-  }
+  constexpr int NS = TF_NT;
+  const uint32_t sv = score_key(__ldg(row + (int)(((int64_t)tid * n) / NS)));
+  const float expect = (float)NS * (float)K / (float)n;
+  int r = (int)ceilf(1.15f * expect + 3.5f * sqrtf(expect)) + 1;
+  r = r < 1 ? 1 : (r > NS ? NS : r);
+  for (int b = tid; b < kTopkBins; b += TF_NT) sh.hist[b] = 0;
   __syncthreads();
-
-  // Candidates: every key >= T (or, exact_ids, the exact top set), written
-  // through a block prefix sum (no atomics); their smallest and largest key go
-  // to sh.kmin / sh.kmax.  `counted`: this thread's count of them when the
-  // caller already has it.
-  auto compact = [&](uint32_t T, uint32_t KT, uint32_t IT, bool exact_ids, int counted) {
-    auto take = [&](int i) {
-      const uint32_t kk = K_[i];
-      return exact_ids ? (kk > KT || (kk == KT && id_key(idof(i)) >= IT)) : kk >= T;
-    };
-    uint32_t local = 0;
-    if (counted >= 0) {
-      local = (uint32_t)counted;
-    } else {
-      for (int i = tid; i < cn; i += TK_NT) local += take(i) ? 1u : 0u;
-    }
-    if (tid == 0) {
-      sh.kmin = 0xffffffffu;
-      sh.kmax = 0u;
-    }
-    uint32_t total;
-    uint32_t off = block_excl_scan(local, sh.red, &total);
-    uint32_t mn = 0xffffffffu, mx = 0u;
-    for (int i = tid; i < cn; i += TK_NT) {
-      if (take(i)) {
-        const uint32_t kk = K_[i];
-        mn = min(mn, kk);
-        mx = max(mx, kk);
-        if (off < (uint32_t)TK_CAP) sh.cand[off] = composite(kk, idof(i));
-        ++off;
-      }
-    }
-    mn = __reduce_min_sync(0xffffffffu, mn);
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if ((tid & 31) == 0) {
-      atomicMin(&sh.kmin, mn);
-      atomicMax(&sh.kmax, mx);
-    }
-    if (tid == 0) sh.cnt = total;
-    __syncthreads();
-  };
-
-  if (cn <= K) {
-    compact(0u, 0u, 0u, false, -1);      // every key (keys are >= 1)
-  } else {
-    // 1. threshold from 1024 evenly spaced sample keys: the sample rank r that
-    //    should leave ~1.15 K + 3 sigma keys above, located by a two-level
-    //    histogram of the samples (top 11 bits, then the next 11)
-    const int step = cn / TK_NS > 0 ? cn / TK_NS : 1;
-    const int si = tid * step;
-    const uint32_t sv = si < cn ? K_[si] : 0u;
-    const int nvalid = min(TK_NS, cn);
-    const float expect = (float)nvalid * (float)K / (float)cn;
-    int r = (int)ceilf(1.15f * expect + 3.0f * sqrtf(expect)) + 1;
-    r = r < 1 ? 1 : (r > nvalid ? nvalid : r);
-    uint32_t T = 0, count = 0, mine = 0;
-    bool ok = false;
-#pragma unroll 1
-    for (int attempt = 0; attempt < 3; ++attempt) {
-      for (int b2 = tid; b2 < kTopkBins; b2 += TK_NT) sh.hist[b2] = 0;
-      __syncthreads();
-      if (sv) atomicAdd(&sh.hist[sv >> 21], 1u);
-      __syncthreads();
-      hist_suffix_find(sh, kTopkBins, (uint32_t)r);
-      const uint32_t b1 = sh.found_bin, a1 = sh.found_above;
-      __syncthreads();
-      for (int b2 = tid; b2 < kTopkBins; b2 += TK_NT) sh.hist[b2] = 0;
-      __syncthreads();
-      if (sv && (sv >> 21) == b1) atomicAdd(&sh.hist[(sv >> 10) & 0x7ffu], 1u);
-      __syncthreads();
-      hist_suffix_find(sh, kTopkBins, (uint32_t)r - a1);
-      T = (b1 << 21) | (sh.found_bin << 10);
-      if (T == 0u) T = 1u;
-      __syncthreads();
-      uint32_t local = 0;
-      for (int i = tid; i < cn; i += TK_NT) local += (K_[i] >= T) ? 1u : 0u;
-      mine = local;
-      count = block_sum_u32(local, sh.red);
-      if (count > (uint32_t)TK_CAP) break;
-      if (count >= (uint32_t)K) {
-        ok = true;
-        break;
-      }
-      if (r == nvalid) break;
-      r = min(nvalid, 2 * r);
-    }
-    if (ok) {
-      compact(T, 0u, 0u, false, (int)mine);
-    } else {
-      // exact: radix select of the K-th key, then of the ids among its ties
-      uint32_t above, eq;
-      auto key_f = [&](int i) { return K_[i]; };
-      auto all = [&](int) { return true; };
-      const uint32_t KT = smem_radix_select(sh, cn, (uint32_t)K, key_f, all, &above, &eq);
-      const uint32_t need = (uint32_t)K - above;
-      uint32_t IT = 0;
-      if (eq != need) {
-        auto tie = [&](int i) { return K_[i] == KT; };
-        auto idk = [&](int i) { return id_key(idof(i)); };
-        uint32_t above2, eq2;
-        IT = smem_radix_select(sh, cn, need, idk, tie, &above2, &eq2);
-      }
-      compact(0u, KT, IT, true, -1);
-    }
-  }
+  atomicAdd(&sh.hist[sv >> 21], 1u);
   __syncthreads();
-  int cnt = (int)min(sh.cnt, (uint32_t)TK_CAP);
-  uint64_t* best = reinterpret_cast<uint64_t*>(sh.keys);   // the (now free) key area
-  if (single && cnt > K) {
-    // the candidates are distinct composites: when their buckets are even, one
-    // bucket sort of all of them orders the row and its first K are the answer
-    if (sh.cnt <= (uint32_t)TK_CAP && bucket_sort_desc(sh, sh.cand, cnt, best, true)) {
-      for (int j = tid; j < K; j += TK_NT) {
-        const uint64_t v = sh.cand[j];
-        out_ids[m * K + j] = key_id((uint32_t)v);
-        if (out_scores) out_scores[m * K + j] = key_score((uint32_t)(v >> 32));
-      }
-      return;
+  hist_suffix_find(sh, kTopkBins, (uint32_t)r);
+  const uint32_t b1 = sh.found_bin, a1 = sh.found_above;
+  __syncthreads();
+  for (int b = tid; b < kTopkBins; b += TF_NT) sh.hist[b] = 0;
+  __syncthreads();
+  if ((sv >> 21) == b1) atomicAdd(&sh.hist[(sv >> 10) & 0x7ffu], 1u);
+  __syncthreads();
+  hist_suffix_find(sh, kTopkBins, (uint32_t)r - a1);
+  const uint32_t T = (b1 << 21) | (sh.found_bin << 10);
+  __syncthreads();
+  return T ? T : 1u;
+}
+
+__global__ void __launch_bounds__(TF_NT, 2)
+    topk_filter_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ lens, idx_problem p,
+                       int use_p, int max_len, int K, const int32_t* __restrict__ id_map, int64_t id_ld,
+                       const int32_t* __restrict__ row_mask, uint64_t* __restrict__ cand,
+                       uint32_t* __restrict__ cnt) {
+  // cand / cnt: slots of chunk (row, blockIdx.y) at index m * gridDim.y + blockIdx.y
+  __shared__ TfShared sh;
+  const int64_t m = blockIdx.x;
+  const int64_t base = (int64_t)blockIdx.y * TF_CH;
+  if (row_mask && !row_mask[m]) return;
+  const int n = row_length(lens, p, use_p, max_len, m);
+  if (base >= n) return;
+  const int tid = threadIdx.x;
+  const float* row = scores + m * ld;
+  // every visible key when the row has at most K of them (ordered keys are >= 1)
+  const uint32_t T = n <= K ? 1u : row_threshold(sh, row, n, K);
+  uint32_t kv[TF_PER];
+#pragma unroll
+  for (int u = 0; u < TF_PER; ++u) {
+    const int64_t i = base + u * TF_NT + tid;
+    kv[u] = i < n ? score_key(__ldg(row + i)) : 0u;
+  }
+  uint32_t local = 0;
+#pragma unroll
+  for (int u = 0; u < TF_PER; ++u) local += kv[u] >= T ? 1u : 0u;
+  uint32_t total;
+  uint32_t pos = block_excl_scan(local, sh.red, &total);
+  const int64_t slot = m * (int64_t)gridDim.y + blockIdx.y;
+  if (tid == 0) cnt[slot] = total;
+  const int32_t* idm = id_map ? id_map + m * id_ld : nullptr;
+  uint64_t* out = cand + slot * TF_CAPC;
+#pragma unroll
+  for (int u = 0; u < TF_PER; ++u) {
+    if (kv[u] >= T) {
+      const int64_t i = base + u * TF_NT + tid;
+      if (pos < (uint32_t)TF_CAPC) out[pos] = composite(kv[u], idm ? idm[i] : (int32_t)i);
+      ++pos;
     }
-  }
-  // exactly min(K, cn) composites
-  if (cnt > K) {
-    select_exact_k(sh, sh.cand, cnt, K, best);
-    cnt = K;
-  } else {
-    for (int i = tid; i < cnt; i += TK_NT) best[i] = sh.cand[i];
-    __syncthreads();
-  }
-  if (!single) {
-    uint64_t* dst = lists + ((int64_t)m * n_chunks + c) * P;
-    for (int j = tid; j < P; j += TK_NT) dst[j] = j < cnt ? best[j] : 0ull;
-    return;
-  }
-  const uint64_t* sorted = order_desc(sh, best, cnt, P, sh.cand);
-  for (int j = tid; j < K; j += TK_NT) {
-    const uint64_t v = j < cnt ? sorted[j] : 0ull;
-    out_ids[m * K + j] = v ? key_id((uint32_t)v) : -1;
-    if (out_scores) out_scores[m * K + j] = v ? key_score((uint32_t)(v >> 32)) : -__int_as_float(0x7f800000);
   }
 }
 
-// Folds the chunk candidate sets of every multi-chunk row into its top-K:
-// a running best-K set meets each chunk's set, an exact selection keeps the K
-// largest, and one sort orders the result.
+// ------------------------------------------------------------ the finish --
+// Pass 2, one thread block per row: the candidates of the row's chunks are
+// gathered, bucket-sorted at once and the first min(K, n) written.  When they
+// are short of that or a chunk (or the row) overflowed (the threshold
+// missed), the row is selected exactly from the scores themselves: radix
+// select of the K-th key, then of the ids among its ties, compaction of
+// exactly K, sort.
 __global__ void __launch_bounds__(TK_NT, 1)
-    topk_merge_kernel(const int32_t* __restrict__ lens, idx_problem p, int use_p, int max_len, int K, int P,
-                      const uint64_t* __restrict__ lists, int n_chunks, int32_t* __restrict__ out_ids,
-                      float* __restrict__ out_scores, const int32_t* __restrict__ row_mask) {
+    topk_finish_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ lens, idx_problem p,
+                       int use_p, int max_len, int K, int P, const int32_t* __restrict__ id_map, int64_t id_ld,
+                       const int32_t* __restrict__ row_mask, const uint64_t* __restrict__ cand,
+                       const uint32_t* __restrict__ cnt, int n_chunks, int32_t* __restrict__ out_ids,
+                       float* __restrict__ out_scores) {
   extern __shared__ __align__(16) uint8_t tk_smem[];
   TkShared& sh = *reinterpret_cast<TkShared*>(tk_smem);
-  uint64_t* pair = reinterpret_cast<uint64_t*>(sh.keys);   // [best P | chunk P]
-  uint64_t* best = sh.cand;
   const int64_t m = blockIdx.x;
   if (row_mask && !row_mask[m]) return;
-  int n;
-  if (use_p) {
-    int64_t off;
-    row_extent(p, m, &off, &n);
-  } else {
-    n = lens[m];
-    n = n < 0 ? 0 : (n > max_len ? max_len : n);
+  const int n = row_length(lens, p, use_p, max_len, m);
+  const int tid = threadIdx.x;
+  const int want = n < K ? n : K;
+  uint64_t* best = reinterpret_cast<uint64_t*>(sh.keys);   // scratch, lower half of the key area
+  auto emit = [&](const uint64_t* sorted, int have) {
+    for (int j = tid; j < K; j += TK_NT) {
+      const uint64_t v = j < have ? sorted[j] : 0ull;
+      out_ids[m * K + j] = v ? key_id((uint32_t)v) : -1;
+      if (out_scores) out_scores[m * K + j] = v ? key_score((uint32_t)(v >> 32)) : -__int_as_float(0x7f800000);
+    }
+  };
+  if (want <= 0) {
+    emit(nullptr, 0);
+    return;
   }
-  if (n <= TK_CH) return;   // written by the chunk kernel
-  const int chunks = (int)((n + TK_CH - 1) / TK_CH);
-  const uint64_t* src = lists + (int64_t)m * n_chunks * P;
-  for (int i = threadIdx.x; i < P; i += TK_NT) pair[i] = src[i];
-  for (int c = 1; c < chunks; ++c) {
-    const uint64_t* s2 = src + (int64_t)c * P;
-    for (int i = threadIdx.x; i < P; i += TK_NT) pair[P + i] = s2[i];
+  // the row's chunks: their counts (an overflowed chunk forces the exact path)
+  const int rc = (int)((n + (int64_t)TF_CH - 1) / TF_CH);
+  uint32_t total = 0;
+  bool over = false;
+  for (int c = 0; c < rc; ++c) {
+    const uint32_t k = cnt[m * (int64_t)n_chunks + c];
+    over |= k > (uint32_t)TF_CAPC;
+    total += k;
+  }
+  if (!over && total >= (uint32_t)want && total <= (uint32_t)TK_ROWCAP) {
+    uint32_t pre = 0;
+    for (int c = 0; c < rc; ++c) {
+      const int64_t slot = m * (int64_t)n_chunks + c;
+      const int k = (int)cnt[slot];
+      const uint64_t* src = cand + slot * TF_CAPC;
+      for (int j = tid; j < k; j += TK_NT) sh.cand[pre + j] = src[j];
+      pre += (uint32_t)k;
+    }
     __syncthreads();
-    select_exact_k(sh, pair, 2 * P, K, best);     // at least K real entries: chunk 0 alone has K
-    for (int i = threadIdx.x; i < P; i += TK_NT) pair[i] = i < K ? best[i] : 0ull;
-    __syncthreads();
+    if (total > 1 && bucket_sort_desc(sh, sh.cand, (int)total, best, false, want)) {
+      emit(sh.cand, want);
+      return;
+    }
+    int c2 = (int)total;
+    if (c2 > want) {
+      select_exact_k(sh, sh.cand, c2, want, best);
+      c2 = want;
+    } else {
+      for (int j = tid; j < c2; j += TK_NT) best[j] = sh.cand[j];
+      __syncthreads();
+    }
+    emit(order_desc(sh, best, c2, P, sh.cand), c2);
+    return;
   }
-  // the running set holds exactly K real entries (chunk 0 alone has K)
-  const uint64_t* sorted = order_desc(sh, pair, K, P, best);
-  for (int j = threadIdx.x; j < K; j += TK_NT) {
-    const uint64_t v = sorted[j];
-    out_ids[m * K + j] = v ? key_id((uint32_t)v) : -1;
-    if (out_scores) out_scores[m * K + j] = v ? key_score((uint32_t)(v >> 32)) : -__int_as_float(0x7f800000);
+  // exact, from the scores (pathological rows only)
+  const float* row = scores + m * ld;
+  const int32_t* idm = id_map ? id_map + m * id_ld : nullptr;
+  auto idof = [&](int i) { return idm ? idm[i] : (int32_t)i; };
+  auto key_f = [&](int i) { return score_key(__ldg(row + i)); };
+  auto all = [&](int) { return true; };
+  uint32_t above, eq;
+  const uint32_t KT = smem_radix_select(sh, n, (uint32_t)want, key_f, all, &above, &eq);
+  const uint32_t need = (uint32_t)want - above;
+  uint32_t IT = 0;
+  if (eq != need) {
+    auto tie = [&](int i) { return key_f(i) == KT; };
+    auto idk = [&](int i) { return id_key(idof(i)); };
+    uint32_t above2, eq2;
+    IT = smem_radix_select(sh, n, need, idk, tie, &above2, &eq2);
   }
+  auto take = [&](int i) {
+    const uint32_t kk = key_f(i);
+    return kk > KT || (kk == KT && id_key(idof(i)) >= IT);
+  };
+  uint32_t local = 0;
+  for (int i = tid; i < n; i += TK_NT) local += take(i) ? 1u : 0u;
+  uint32_t tot2;
+  uint32_t off = block_excl_scan(local, sh.red, &tot2);
+  for (int i = tid; i < n; i += TK_NT)
+    if (take(i)) sh.cand[off++] = composite(key_f(i), idof(i));
+  __syncthreads();
+  emit(order_desc(sh, sh.cand, want, P, best), want);
 }
 
 static int pow2_at_least(int x) {
@@ -630,10 +605,17 @@ static int pow2_at_least(int x) {
   return p;
 }
 
+static int filter_chunks(int max_len) { return max_len > 0 ? (max_len + TF_CH - 1) / TF_CH : 1; }
+
+// Workspace: a candidate count per (row, chunk), then TF_CAPC candidate slots per (row, chunk).
 size_t topk_dense_ws(int64_t M, int max_len, int K) {
-  if (max_len <= TK_CH || M <= 0) return 0;
-  const int n_chunks = (max_len + TK_CH - 1) / TK_CH;
-  return (size_t)M * n_chunks * pow2_at_least(K) * sizeof(uint64_t);
+  (void)K;
+  if (M <= 0) return 0;
+  const size_t slots = (size_t)M * (size_t)filter_chunks(max_len);
+  WsCarver c(nullptr);
+  c.take<uint32_t>(slots);
+  c.take<uint64_t>(slots * TF_CAPC);
+  return c.used;
 }
 
 cudaError_t launch_topk_dense(const float* scores, int64_t ld, const int32_t* lens, const idx_problem* p_or_null,
@@ -641,22 +623,24 @@ cudaError_t launch_topk_dense(const float* scores, int64_t ld, const int32_t* le
                               cudaStream_t st, const int32_t* id_map, int64_t id_ld, const int32_t* row_mask) {
   if (M <= 0) return cudaSuccess;
   const int P = pow2_at_least(K);
-  const int n_chunks = max_len > 0 ? (max_len + TK_CH - 1) / TK_CH : 1;
+  const int n_chunks = filter_chunks(max_len);
+  if (n_chunks > 65535 || M > 0x7fffffff) return cudaErrorInvalidValue;
   idx_problem p{};
   if (p_or_null) p = *p_or_null;
-  const size_t smem = sizeof(TkShared);
-  cudaError_t e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  if (n_chunks > 65535) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)M, (unsigned)n_chunks);
-  topk_chunk_kernel<<<grid, TK_NT, smem, st>>>(scores, ld, lens, p, p_or_null ? 1 : 0, max_len, K, P, out_ids,
-                                               out_scores, (uint64_t*)ws, n_chunks, id_map, id_ld, row_mask);
+  WsCarver c(ws);
+  const size_t slots = (size_t)M * (size_t)n_chunks;
+  uint32_t* cnt = c.take<uint32_t>(slots);
+  uint64_t* cand = c.take<uint64_t>(slots * TF_CAPC);
+  cudaError_t e;
+  topk_filter_kernel<<<dim3((unsigned)M, (unsigned)n_chunks), TF_NT, 0, st>>>(
+      scores, ld, lens, p, p_or_null ? 1 : 0, max_len, K, id_map, id_ld, row_mask, cand, cnt);
   e = cudaGetLastError();
-  if (e != cudaSuccess || n_chunks == 1) return e;
-  e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  topk_merge_kernel<<<(unsigned)M, TK_NT, smem, st>>>(lens, p, p_or_null ? 1 : 0, max_len, K, P, (const uint64_t*)ws,
-                                                      n_chunks, out_ids, out_scores, row_mask);
+  const size_t smem = sizeof(TkShared);
+  e = cudaFuncSetAttribute(topk_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  topk_finish_kernel<<<(unsigned)M, TK_NT, smem, st>>>(scores, ld, lens, p, p_or_null ? 1 : 0, max_len, K, P, id_map,
+                                                       id_ld, row_mask, cand, cnt, n_chunks, out_ids, out_scores);
   return cudaGetLastError();
 }
 
