@@ -509,14 +509,17 @@ def main():
                     "algorithmic_bytes": step.algorithmic_bytes()}
     elif isinstance(step, BlockSelectStep):
         k_ms = statistics.median(kernel_ms)
-        # fp32 ALU: 2 instructions (mul, add) per multiply-add, 152 SMs x 128 lanes x clock
+        # fp32 ALU: a separately rounded multiply and add per multiply-add (no FMA, the
+        # page's order); the fp32 pipes retire 2 such operations per lane per clock
+        # with the packed f32x2 instructions: 152 SMs x 128 lanes x 2 x clock
         macs = step.pairs() * wp.index_q.shape[2]
         sm_mhz = clock_info.get("sm_mhz") or 2070.0
-        peak_alu = 152 * 128 * sm_mhz * 1e6 / 1e12
+        peak_alu = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
         ach = 2.0 * macs / (k_ms * 1e-3) / 1e12
-        roof = {"kernel": "block_score_kernel + block_pick_kernel", "bound": "alu", "achieved": ach,
-                "peak": peak_alu, "unit": "Tinst/s", "frac": ach / peak_alu, "traffic": None,
-                "peak_source": "152 SMs x 128 fp32 lanes x median SM clock", "kernel_ms": k_ms}
+        roof = {"kernel": "block_score128_kernel + block_pick_kernel", "bound": "alu", "achieved": ach,
+                "peak": peak_alu, "unit": "T fp32 ops/s", "frac": ach / peak_alu, "traffic": None,
+                "peak_source": "152 SMs x 128 fp32 lanes x 2 (packed f32x2) x median SM clock",
+                "kernel_ms": k_ms}
     else:
         k_ms = statistics.median(kernel_ms)
         roof = {"kernel": "dosa_topk (all kernels)", "bound": "tensor", "achieved": None, "peak": bf16,

@@ -2,16 +2,14 @@
 // block_sparse_select, select_for_head, dot).
 //
 // Two kernels:
-//  1. block_score_kernel: for each (query, KV head) pair and each visible,
+//  1. block scores: for each (query, KV head) pair and each visible,
 //     non-forced block, the max over the block's causally visible positions of
 //     the raw dot q.k_p, with the page's summation order: acc starts at 0 and
 //     acc = acc + q[d]*k[d] for d = 0..D-1, each product and each sum rounded
-//     to fp32 on its own (__fmul_rn / __fadd_rn, no FMA).  That order is what
-//     makes the selected block indices bit-exact, so this runs on the fp32
-//     CUDA-core pipes, not the tensor cores.  A thread block stages a chunk of
-//     the key block in shared memory (row-major, float4 broadcast reads) and
-//     every thread owns one pair, its query in registers (D = 128 path), and
-//     runs four positions at once for instruction-level parallelism.
+//     to fp32 on its own (no FMA).  That order is what makes the selected block
+//     indices bit-exact, so this runs on the fp32 CUDA-core pipes, not the
+//     tensor cores: block_score128_kernel for D = 128 (packed f32x2, two pairs
+//     per lane, see below), block_score_kernel for any other D.
 //  2. block_pick_kernel: per pair, forced blocks get the largest key, then the
 //     exact top-`budget` of (score desc, block asc) is taken and written in
 //     ascending block order.
@@ -54,8 +52,8 @@ __device__ __forceinline__ bool block_forced(int64_t b, int64_t n, const block_s
   return b < c.init_blocks || b >= (z < 0 ? 0 : z);
 }
 
-// D == 128: query in registers.  D == 0: any D, query read from global.
-template <int DC>
+// Any D: the query is read from global memory (L1), a chunk of keys is staged
+// in shared memory, one thread per pair, scalar fp32 in the page's order.
 __global__ void __launch_bounds__(kBsThreads) block_score_kernel(const float* __restrict__ q,
                                                                   const float* __restrict__ k,
                                                                   const int32_t* __restrict__ qpos, int64_t Q,
@@ -69,99 +67,184 @@ __global__ void __launch_bounds__(kBsThreads) block_score_kernel(const float* __
   const int64_t qi = live ? pair / n_kv : 0;
   const int64_t pos = live ? (int64_t)qpos[qi] : -1;
   const BlockGeom g = block_geom(pos, L, c);
-  const int chunk = (DC == 128) ? kBsChunk : (int)max(1, min(kBsChunk, 16384 / D));
+  const int chunk = (int)max(1, min(kBsChunk, 16384 / D));
   const float* qrow = q + pair * (int64_t)D;
-
-  float qr[DC == 128 ? 128 : 1];
-  if (DC == 128 && live) {
-#pragma unroll
-    for (int d4 = 0; d4 < 32; ++d4) {
-      float4 v = __ldg(reinterpret_cast<const float4*>(qrow) + d4);
-      qr[4 * d4 + 0] = v.x;
-      qr[4 * d4 + 1] = v.y;
-      qr[4 * d4 + 2] = v.z;
-      qr[4 * d4 + 3] = v.w;
-    }
-  }
-
   for (int64_t b = blockIdx.y; b < nbm; b += gridDim.y) {
     const bool need = live && g.scoring && b < g.n_blocks && !block_forced(b, g.n_blocks, c);
     if (!__syncthreads_or(need)) continue;
     const int64_t start = b * c.block_size;
     int64_t bend = start + c.block_size;
     bend = bend < L ? bend : L;
-    int64_t vend = pos + 1 < bend ? pos + 1 : bend;   // this thread's visible end
+    const int64_t vend = pos + 1 < bend ? pos + 1 : bend;   // this thread's visible end
     float best = -__int_as_float(0x7f800000);
     for (int64_t c0 = start; c0 < bend; c0 += chunk) {
       const int cl = (int)((bend - c0) < chunk ? (bend - c0) : chunk);
       __syncthreads();
-      if (DC == 128) {
-        const float4* src = reinterpret_cast<const float4*>(k + c0 * 128);
-        float4* dst = reinterpret_cast<float4*>(ks);
-        for (int i = threadIdx.x; i < cl * 32; i += kBsThreads) dst[i] = __ldg(src + i);
-      } else {
-        for (int i = threadIdx.x; i < cl * D; i += kBsThreads) ks[i] = __ldg(k + c0 * D + i);
-      }
+      for (int i = threadIdx.x; i < cl * D; i += kBsThreads) ks[i] = __ldg(k + c0 * D + i);
       __syncthreads();
       if (!need) continue;
       int nv = (int)(vend - c0);
       nv = nv < 0 ? 0 : (nv > cl ? cl : nv);
-      if (DC == 128) {
-        int p = 0;
-        for (; p + 4 <= nv; p += 4) {
-          float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-          const float4* r0 = reinterpret_cast<const float4*>(ks + (p + 0) * 128);
-          const float4* r1 = reinterpret_cast<const float4*>(ks + (p + 1) * 128);
-          const float4* r2 = reinterpret_cast<const float4*>(ks + (p + 2) * 128);
-          const float4* r3 = reinterpret_cast<const float4*>(ks + (p + 3) * 128);
-#pragma unroll
-          for (int d4 = 0; d4 < 32; ++d4) {
-            const float4 k0 = r0[d4], k1 = r1[d4], k2 = r2[d4], k3 = r3[d4];
-            const float x0 = qr[4 * d4], x1 = qr[4 * d4 + 1], x2 = qr[4 * d4 + 2], x3 = qr[4 * d4 + 3];
-            a0 = __fadd_rn(a0, __fmul_rn(x0, k0.x));
-            a1 = __fadd_rn(a1, __fmul_rn(x0, k1.x));
-            a2 = __fadd_rn(a2, __fmul_rn(x0, k2.x));
-            a3 = __fadd_rn(a3, __fmul_rn(x0, k3.x));
-            a0 = __fadd_rn(a0, __fmul_rn(x1, k0.y));
-            a1 = __fadd_rn(a1, __fmul_rn(x1, k1.y));
-            a2 = __fadd_rn(a2, __fmul_rn(x1, k2.y));
-            a3 = __fadd_rn(a3, __fmul_rn(x1, k3.y));
-            a0 = __fadd_rn(a0, __fmul_rn(x2, k0.z));
-            a1 = __fadd_rn(a1, __fmul_rn(x2, k1.z));
-            a2 = __fadd_rn(a2, __fmul_rn(x2, k2.z));
-            a3 = __fadd_rn(a3, __fmul_rn(x2, k3.z));
-            a0 = __fadd_rn(a0, __fmul_rn(x3, k0.w));
-            a1 = __fadd_rn(a1, __fmul_rn(x3, k1.w));
-            a2 = __fadd_rn(a2, __fmul_rn(x3, k2.w));
-            a3 = __fadd_rn(a3, __fmul_rn(x3, k3.w));
-          }
-          best = fmaxf(best, __fadd_rn(a0, 0.0f));
-          best = fmaxf(best, __fadd_rn(a1, 0.0f));
-          best = fmaxf(best, __fadd_rn(a2, 0.0f));
-          best = fmaxf(best, __fadd_rn(a3, 0.0f));
-        }
-        for (; p < nv; ++p) {
-          float a = 0.0f;
-          const float4* r = reinterpret_cast<const float4*>(ks + p * 128);
-#pragma unroll
-          for (int d4 = 0; d4 < 32; ++d4) {
-            const float4 kv = r[d4];
-            a = __fadd_rn(a, __fmul_rn(qr[4 * d4], kv.x));
-            a = __fadd_rn(a, __fmul_rn(qr[4 * d4 + 1], kv.y));
-            a = __fadd_rn(a, __fmul_rn(qr[4 * d4 + 2], kv.z));
-            a = __fadd_rn(a, __fmul_rn(qr[4 * d4 + 3], kv.w));
-          }
-          best = fmaxf(best, __fadd_rn(a, 0.0f));
-        }
-      } else {
-        for (int p = 0; p < nv; ++p) {
-          float a = 0.0f;
-          for (int d = 0; d < D; ++d) a = __fadd_rn(a, __fmul_rn(__ldg(qrow + d), ks[p * D + d]));
-          best = fmaxf(best, __fadd_rn(a, 0.0f));
-        }
+      for (int p = 0; p < nv; ++p) {
+        float a = 0.0f;
+        for (int d = 0; d < D; ++d) a = __fadd_rn(a, __fmul_rn(__ldg(qrow + d), ks[p * D + d]));
+        best = fmaxf(best, __fadd_rn(a, 0.0f));
       }
     }
     if (need) bkey[pair * nbm + b] = score_key(best);
+  }
+}
+
+// ------------------------------------------------------------ D == 128 --
+// Same scores, at the packed fp32 rate and half the shared-memory traffic per
+// operation:
+//  * the packed f32x2 multiply and add round each half on its own exactly as the
+//    scalar instructions do, so two keys' chains advance in one instruction;
+//  * lanes 2i and 2i+1 hold the two halves (d < 64, d >= 64) of the queries of
+//    two pairs, so every key value a lane loads serves two pairs.  Keys go in
+//    groups of 8: the even lane sums d = 0..63 of a group while the odd lane
+//    finishes d = 64..127 of the previous group from the even lane's partial
+//    sums (handed over by a shuffle), so every chain is still the page's
+//    sequential sum over d = 0..127.
+//  * a block of up to 128 keys is staged transposed ([d][key]) so that one
+//    16-byte load gives four keys' d-th elements.
+constexpr int kBs128Keys = 128;   // keys staged per round
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float* lo, float* hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(*lo), "=f"(*hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+  return ((uint64_t)hi << 32) | lo;
+}
+
+// One 8-key group, this lane's half of D: chains (keys 8g+2j, 8g+2j+1) of
+// pair A in acc[j], of pair B in acc[4+j], j < 4; kcol = kt + (64 h) * 128 + 8 g.
+__device__ __forceinline__ void bs128_group(const float* kcol, const float (&qa)[64], const float (&qb)[64],
+                                            uint64_t (&acc)[8]) {
+#pragma unroll
+  for (int dd = 0; dd < 64; ++dd) {
+    const float4 u = *reinterpret_cast<const float4*>(kcol + dd * kBs128Keys);
+    const float4 v = *reinterpret_cast<const float4*>(kcol + dd * kBs128Keys + 4);
+    const uint64_t k01 = f2_pack(u.x, u.y), k23 = f2_pack(u.z, u.w);
+    const uint64_t k45 = f2_pack(v.x, v.y), k67 = f2_pack(v.z, v.w);
+    const uint64_t xa = f2_pack(qa[dd], qa[dd]);
+    const uint64_t xb = f2_pack(qb[dd], qb[dd]);
+    acc[0] = f2_add(acc[0], f2_mul(xa, k01));
+    acc[1] = f2_add(acc[1], f2_mul(xa, k23));
+    acc[2] = f2_add(acc[2], f2_mul(xa, k45));
+    acc[3] = f2_add(acc[3], f2_mul(xa, k67));
+    acc[4] = f2_add(acc[4], f2_mul(xb, k01));
+    acc[5] = f2_add(acc[5], f2_mul(xb, k23));
+    acc[6] = f2_add(acc[6], f2_mul(xb, k45));
+    acc[7] = f2_add(acc[7], f2_mul(xb, k67));
+  }
+}
+
+__global__ void __launch_bounds__(kBsThreads) block_score128_kernel(const float* __restrict__ q,
+                                                                    const float* __restrict__ k,
+                                                                    const int32_t* __restrict__ qpos, int64_t Q,
+                                                                    int n_kv, int64_t L, block_sparse_config c,
+                                                                    int64_t nbm, uint32_t* __restrict__ bkey) {
+  extern __shared__ __align__(16) float kt[];   // [128 d][128 keys]
+  const int t = threadIdx.x, h = t & 1;
+  const int64_t n_pairs = Q * n_kv;
+  const int64_t pA = (int64_t)blockIdx.x * kBsThreads + (t & ~1), pB = pA + 1;
+  const bool liveA = pA < n_pairs, liveB = pB < n_pairs;
+  const int64_t posA = liveA ? (int64_t)qpos[pA / n_kv] : -1;
+  const int64_t posB = liveB ? (int64_t)qpos[pB / n_kv] : -1;
+  const BlockGeom gA = block_geom(posA, L, c), gB = block_geom(posB, L, c);
+  float qa[64], qb[64];
+  {
+    const float4* ra = reinterpret_cast<const float4*>(q + pA * 128 + 64 * h);
+    const float4* rb = reinterpret_cast<const float4*>(q + pB * 128 + 64 * h);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float4 va = liveA ? __ldg(ra + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 vb = liveB ? __ldg(rb + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      qa[4 * i] = va.x; qa[4 * i + 1] = va.y; qa[4 * i + 2] = va.z; qa[4 * i + 3] = va.w;
+      qb[4 * i] = vb.x; qb[4 * i + 1] = vb.y; qb[4 * i + 2] = vb.z; qb[4 * i + 3] = vb.w;
+    }
+  }
+  for (int64_t b = blockIdx.y; b < nbm; b += gridDim.y) {
+    const bool needA = liveA && gA.scoring && b < gA.n_blocks && !block_forced(b, gA.n_blocks, c);
+    const bool needB = liveB && gB.scoring && b < gB.n_blocks && !block_forced(b, gB.n_blocks, c);
+    if (!__syncthreads_or(needA || needB)) continue;
+    const int64_t start = b * c.block_size;
+    int64_t bend = start + c.block_size;
+    bend = bend < L ? bend : L;
+    const int64_t vendA = posA + 1 < bend ? posA + 1 : bend;   // visible ends
+    const int64_t vendB = posB + 1 < bend ? posB + 1 : bend;
+    float bestA = -__int_as_float(0x7f800000), bestB = bestA;
+    for (int64_t c0 = start; c0 < bend; c0 += kBs128Keys) {
+      const int cl = (int)((bend - c0) < kBs128Keys ? (bend - c0) : kBs128Keys);
+      __syncthreads();
+      {
+        // transposed staging: lanes take consecutive keys of one 16-byte column
+        const float4* src = reinterpret_cast<const float4*>(k + c0 * 128);
+        for (int i = t; i < cl * 32; i += kBsThreads) {
+          const int key = i % cl, d4 = i / cl;
+          const float4 v = __ldg(src + key * 32 + d4);
+          kt[(4 * d4 + 0) * kBs128Keys + key] = v.x;
+          kt[(4 * d4 + 1) * kBs128Keys + key] = v.y;
+          kt[(4 * d4 + 2) * kBs128Keys + key] = v.z;
+          kt[(4 * d4 + 3) * kBs128Keys + key] = v.w;
+        }
+      }
+      __syncthreads();
+      int nvA = needA ? (int)(vendA - c0) : 0, nvB = needB ? (int)(vendB - c0) : 0;
+      nvA = nvA < 0 ? 0 : (nvA > cl ? cl : nvA);
+      nvB = nvB < 0 ? 0 : (nvB > cl ? cl : nvB);
+      const int mine = ((nvA > nvB ? nvA : nvB) + 7) >> 3;
+      const int ng = __reduce_max_sync(0xffffffffu, mine);   // 8-key groups this warp runs
+      uint64_t recv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) recv[j] = 0;
+      // step s: the even lane takes group s, the odd lane group s - 1
+      for (int st = 0; st <= ng; ++st) {
+        const int g = st - h;
+        const bool active = g >= 0 && g < ng;
+        uint64_t acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = h ? recv[j] : 0ull;
+        if (active) bs128_group(kt + (64 * h) * kBs128Keys + 8 * g, qa, qb, acc);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) recv[j] = shfl_xor_u64(acc[j], 1);
+        if (h && active) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float x0, x1, y0, y1;
+            f2_unpack(acc[j], &x0, &x1);
+            f2_unpack(acc[4 + j], &y0, &y1);
+            const int key = 8 * g + 2 * j;
+            if (key < nvA) bestA = fmaxf(bestA, __fadd_rn(x0, 0.0f));
+            if (key + 1 < nvA) bestA = fmaxf(bestA, __fadd_rn(x1, 0.0f));
+            if (key < nvB) bestB = fmaxf(bestB, __fadd_rn(y0, 0.0f));
+            if (key + 1 < nvB) bestB = fmaxf(bestB, __fadd_rn(y1, 0.0f));
+          }
+        }
+      }
+    }
+    if (h) {
+      if (needA) bkey[pA * nbm + b] = score_key(bestA);
+      if (needB) bkey[pB * nbm + b] = score_key(bestB);
+    }
   }
 }
 
@@ -230,17 +313,17 @@ cudaError_t launch_block_select(const float* q, const float* k, const int32_t* p
   if (nbm > 0) {
     dim3 grid((unsigned)((pairs + kBsThreads - 1) / kBsThreads), (unsigned)(nbm < 65535 ? nbm : 65535));
     if (D == 128) {
-      size_t smem = (size_t)kBsChunk * 128 * sizeof(float);
-      e = cudaFuncSetAttribute(block_score_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      const int smem128 = 128 * kBs128Keys * (int)sizeof(float);
+      e = cudaFuncSetAttribute(block_score128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem128);
       if (e != cudaSuccess) return e;
-      block_score_kernel<128><<<grid, kBsThreads, smem, st>>>(q, k, pos, Q, n_kv, D, L, c, nbm, bkey);
+      block_score128_kernel<<<grid, kBsThreads, smem128, st>>>(q, k, pos, Q, n_kv, L, c, nbm, bkey);
     } else {
       int chunk = D > 0 ? (16384 / D < kBsChunk ? 16384 / D : kBsChunk) : 1;
       chunk = chunk < 1 ? 1 : chunk;
       size_t smem = (size_t)chunk * D * sizeof(float);
-      e = cudaFuncSetAttribute(block_score_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      e = cudaFuncSetAttribute(block_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
-      block_score_kernel<0><<<grid, kBsThreads, smem, st>>>(q, k, pos, Q, n_kv, D, L, c, nbm, bkey);
+      block_score_kernel<<<grid, kBsThreads, smem, st>>>(q, k, pos, Q, n_kv, D, L, c, nbm, bkey);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
