@@ -48,10 +48,11 @@
 //                         alternate queries of a tile (several queries per
 //                         tile) or alternate tiles (one query per tile):
 //                         tcgen05.ld -> score / bound -> global
-//              last 2     (FP8 only) split of each query group's bf16 rows
+//              next       (FP8 only) split of each query group's bf16 rows
 //                         into the e4m3 hi and lo tiles
+//              last       second MMA issue thread (alternate rounds with warp 1)
 // Every wait is bounded (see common.cuh); on a timeout all roles stop, the
-// producer and the MMA thread drain what they issued, and TMEM is released.
+// producer and the MMA threads drain what they issued, and TMEM is released.
 #pragma once
 
 #include <cuda.h>
@@ -125,12 +126,19 @@ struct TcCfg {
   static constexpr int IL = (SUB == 1 && N <= 128) ? 2 : 1;   // units whose MMA chains are interleaved
   static constexpr int TMEM_COLS = tc_pow2_cols(SACC * SUB * N);
   static constexpr int NE = 8;   // epilogue warps, two per TMEM lane quarter
+  // bf16 score tiles with at least 4 queries: an epilogue warp walks its queries
+  // two at a time, both chains in one packed fma.rn.f32x2 per head
+  static constexpr bool PAIR = (MODE != kBound) && !FP8 && NQ >= 4;
   // epilogue warps that read one unit: all 8 when a unit holds several queries
   // (alternating queries) or two subtiles (one warp of a quarter per subtile),
   // else 4 (the two warps of a quarter take alternate units)
   static constexpr int EPT = (NQ > 1 || SUB > 1) ? 8 : 4;
-  static constexpr int NCONV = FP8 ? 2 : 0;   // warps that split the query rows (FP8)
-  static constexpr int NTHREADS = 32 * (2 + NE + NCONV);
+  static constexpr int NCONV = FP8 ? 1 : 0;   // warp that splits the query rows (FP8)
+  // two MMA-issuing warps (warp 1 and the last warp) take alternate issue rounds:
+  // tcgen05.mma issue blocks while the tensor pipe is busy, so one thread's
+  // waits, commits and schedule steps overlap the other thread's MMAs
+  static constexpr int MMA2_WARP = 2 + NE + NCONV;
+  static constexpr int NTHREADS = 32 * (3 + NE + NCONV);
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + SA * A_BYTES;
@@ -146,7 +154,7 @@ struct TcCfg {
   static constexpr int SIGR_MOD = SIGR > 0 ? SIGR : 1;
   static constexpr int OFF_SIG = OFF_AUX + NE * NQ * 16;
   static constexpr int OFF_BAR = ((OFF_SIG + SIGR * NQ * 4) + 7) & ~7;
-  static constexpr int NBARS = 2 * SA + 2 * SB + 2 * SACC + 1 + 2 * SIGR + 2 * SSC;
+  static constexpr int NBARS = 2 * SA + 2 * SB + 2 * SACC + 2 + 2 * SIGR + 2 * SSC;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N");
@@ -309,12 +317,16 @@ template <int NCOL>
 __device__ __forceinline__ float query_amax(const uint16_t* q) {
   const int lane = threadIdx.x & 31;
   float mx = 0.0f;
-  for (int i = lane; i < NCOL * 32; i += 32) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2*>(q) + i);
-    mx = fmaxf(mx, fabsf(__uint_as_float(v.x << 16)));
-    mx = fmaxf(mx, fabsf(__uint_as_float(v.x & 0xffff0000u)));
-    mx = fmaxf(mx, fabsf(__uint_as_float(v.y << 16)));
-    mx = fmaxf(mx, fabsf(__uint_as_float(v.y & 0xffff0000u)));
+  // 16-byte loads, eight in flight per lane
+#pragma unroll 8
+  for (int i = lane; i < NCOL * 16; i += 32) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(q) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mx = fmaxf(mx, fabsf(__uint_as_float(w[e] << 16)));
+      mx = fmaxf(mx, fabsf(__uint_as_float(w[e] & 0xffff0000u)));
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -343,8 +355,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   uint64_t* b_empty = b_full + C::SB;
   uint64_t* acc_full = b_empty + C::SB;
   uint64_t* acc_empty = acc_full + C::SACC;
-  uint64_t* drain_bar = acc_empty + C::SACC;
-  uint64_t* sig_full = drain_bar + 1;
+  uint64_t* drain_bar = acc_empty + C::SACC;   // one per MMA-issuing thread
+  uint64_t* sig_full = drain_bar + 2;
   uint64_t* sig_empty = sig_full + C::SIGR;
   float* sSig = reinterpret_cast<float*>(smem + C::OFF_SIG);
   uint64_t* sc_full = sig_empty + C::SIGR;
@@ -366,13 +378,14 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     for (int i = 0; i < C::SB; ++i) {
       // FP8: every lane of the split warps arrives once its rows are written
       mbar_init(&b_full[i], C::FP8 ? 32 * C::NCONV : 1);
-      mbar_init(&b_empty[i], 1);
+      mbar_init(&b_empty[i], 2);                 // both MMA-issuing threads
     }
     for (int i = 0; i < C::SACC; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 32 * C::EPT);
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(&drain_bar[0], 1);
+    mbar_init(&drain_bar[1], 1);
     for (int i = 0; i < C::SIGR; ++i) {
       mbar_init(&sig_full[i], 1);
       mbar_init(&sig_empty[i], C::NE);
@@ -491,14 +504,16 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         mbar_wait(&a_full[j % C::SA], (j / C::SA) & 1, no_abort);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == C::MMA2_WARP) {
     // ------------------------------------------------------------ MMA issue
+    // Both issuing threads walk every round; each issues the rounds of its parity.
     if (lane == 0) {
+      const uint32_t me = warp == 1 ? 0u : 1u;
       TcUnits<C> u;
       u.init(args, s);
       int64_t cur_g = -1;
       int cur_bs = 0;
-      uint32_t na = 0, nb = 0, nacc = 0;
+      uint32_t na = 0, nb = 0, nacc = 0, round = 0;
       bool issued = false;
       while (u.valid()) {
         if (u.g != cur_g) {
@@ -516,6 +531,16 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         if (C::IL > 1) {
           nx.advance();
           if (nx.valid() && nx.g == u.g) n = 2;
+        }
+        const bool mine = (round++ & 1u) == me;
+        if (!mine) {
+          na += n;
+          nacc += n;
+          const int64_t g_this = u.g;
+          if (n > 1) u = nx;
+          u.advance();
+          if (!u.valid() || u.g != g_this) tc_commit(&b_empty[cur_bs]);
+          continue;
         }
         bool ok = true;
         for (int i = 0; i < n && ok; ++i) {
@@ -574,8 +599,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         if (!u.valid() || u.g != g_this) tc_commit(&b_empty[cur_bs]);
       }
       if (issued) {
-        tc_commit(drain_bar);
-        mbar_wait(drain_bar, 0, no_abort);
+        tc_commit(&drain_bar[me]);
+        mbar_wait(&drain_bar[me], 0, no_abort);
       }
     }
   } else if (warp >= 2 && warp < 2 + C::NE) {
@@ -611,10 +636,18 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           ++ngrp;
         }
         for (int i = lane; i < C::NQ * C::NCOL; i += 32) {
-          const int64_t m = cur_g * C::NQ + i / C::NCOL;
+          const int qi = i / C::NCOL, h = i % C::NCOL;
+          const int64_t m = cur_g * C::NQ + qi;
           float wv = 0.0f;
-          if (m < args.p.M) wv = C::BOUND ? args.wfold[m * 32 + (i % 32)] : args.p.w[m * C::H + (i % C::H)];
-          sW[i] = wv;
+          if (m < args.p.M) wv = C::BOUND ? args.wfold[m * 32 + h] : args.p.w[m * C::H + h];
+          if constexpr (C::PAIR) {
+            // this warp's r-th query goes to pair r/2, half r%2: [pair][h][2]
+            if ((qi - qfirst) % QSTEP != 0) continue;
+            const int r = (qi - qfirst) / QSTEP;
+            sW[(r >> 1) * 2 * C::NCOL + 2 * h + (r & 1)] = wv;
+          } else {
+            sW[i] = wv;
+          }
         }
         if (!C::FP8 && lane < C::NQ) sAux[4 * lane + 2] = 1.0f;
         if (lane < C::NQ) {
@@ -699,6 +732,48 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           if (C::FP8) mbar_arrive(&sc_empty[sslot]);
         }
       }
+      if constexpr (C::PAIR) {
+        // queries qi and qi + QSTEP, chains packed (a in the low half, b in the high half)
+#pragma unroll 1
+        for (int qi = qfirst, r = 0; qi < C::NQ; qi += 2 * QSTEP, r += 2) {
+          const int qb = qi + QSTEP;
+          const int64_t ma = cur_g * C::NQ + qi, mb = cur_g * C::NQ + qb;
+          if (ma >= args.p.M) break;
+          const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::SUB * C::N);
+          const uint32_t ta = tbase + (uint32_t)(qi * C::NCOLX), tb = tbase + (uint32_t)(qb * C::NCOLX);
+          const float* w2 = sW + (r >> 1) * 2 * C::NCOL;
+          constexpr int NCH = (C::H + 31) / 32;
+          constexpr int CW = C::H < 32 ? C::H : 32;
+          uint64_t s2 = 0;
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            uint32_t va[32], vb[32];
+            if (C::H >= 32) {
+              tmem_ld_32x32b_x32(ta + 32 * c, va);
+              tmem_ld_32x32b_x32(tb + 32 * c, vb);
+            } else {
+              tmem_ld_32x32b_x16(ta, va);
+              tmem_ld_32x32b_x16(tb, vb);
+            }
+            tmem_ld_wait();
+            const float4* w4 = reinterpret_cast<const float4*>(w2 + 2 * 32 * c);
+#pragma unroll
+            for (int j2 = 0; j2 < CW / 2; ++j2) {
+              const float4 ww = w4[j2];      // (wa[h], wb[h], wa[h+1], wb[h+1]), h = 32c + 2 j2
+              const int j = 2 * j2;
+              s2 = f2_fma(f2_pack(ww.x, ww.y),
+                          f2_pack(fmaxf(__uint_as_float(va[j]), 0.0f), fmaxf(__uint_as_float(vb[j]), 0.0f)), s2);
+              s2 = f2_fma(f2_pack(ww.z, ww.w),
+                          f2_pack(fmaxf(__uint_as_float(va[j + 1]), 0.0f), fmaxf(__uint_as_float(vb[j + 1]), 0.0f)),
+                          s2);
+            }
+          }
+          float sa, sb;
+          f2_unpack(s2, &sa, &sb);
+          if (key < sLen[qi]) args.scores[ma * args.ld + key] = sa;
+          if (mb < args.p.M && key < sLen[qb]) args.scores[mb * args.ld + key] = sb;
+        }
+      } else
 #pragma unroll 1
       for (int qi = qfirst; qi < C::NQ; qi += QSTEP) {
         const int64_t m = cur_g * C::NQ + qi;
@@ -835,6 +910,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           float sig = 1.0f, inv = 1.0f;
           if (live) row_sigma(query_amax<C::NCOL>(qrow), &sig, &inv);
           if (cw == 0 && lane == 0) sSig[sl * C::NQ + qi] = sig;
+#pragma unroll 8
           for (int v = cw; v < C::NCOL; v += C::NCONV) {
             uint2 q4 = make_uint2(0u, 0u);
             if (live) q4 = __ldg(reinterpret_cast<const uint2*>(qrow + v * 128) + lane);
