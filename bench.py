@@ -239,7 +239,7 @@ class DosaStep:
         self.ids = torch.empty((wp.M, self.K), dtype=torch.int32, device=dev)
         self.sc = torch.empty((wp.M, self.K), dtype=torch.float32, device=dev)
         self.ws = torch.empty(B.dosa_topk_workspace_size(self.p, self.K, self.dp), dtype=torch.uint8, device=dev)
-        self.stats = torch.zeros(5, dtype=torch.int64, device=dev)
+        self.stats = torch.zeros(6, dtype=torch.int64, device=dev)
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         self.score_ms = []
         # kernels dosa_topk enqueues per call: seeds, seed scores and top-K, planner,
@@ -531,7 +531,10 @@ def main():
         st = step.stats.cpu().tolist()
         nonseed = max(1, st[0] - st[1])
         dosa_info = {"pairs": st[0], "seed_pairs": st[1], "candidates": st[2], "survivors": st[3],
-                     "fallback_rows": st[4], "candidate_rate": st[2] / nonseed, "survival_rate": st[3] / nonseed}
+                     "fallback_rows": st[4], "skipped_rows": st[5],
+                     # rates over all non-seed pairs: only meaningful when no row skipped the scan
+                     "candidate_rate": st[2] / nonseed if st[5] == 0 else None,
+                     "survival_rate": st[3] / nonseed if st[5] == 0 else None}
 
     e2e = None
     if isinstance(step, IndexerStep):

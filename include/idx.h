@@ -155,7 +155,11 @@ idx_status idx_topk_scores(const float* scores, int64_t ld, const int32_t* lens,
  * representative score, then id; n_seed seeds from the common visible prefix),
  * otherwise floor(i L_r / n) for i < n = min(L_r, n_seed).  A row with fewer
  * than K distinct visible seeds, or whose candidate list overflows
- * candidate_capacity, is computed on the unpruned path (row_status 1 resp. 2).
+ * candidate_capacity, is computed on the unpruned path (row_status 1 resp. 2);
+ * so is a row whose bound, evaluated by the planner on n_sample evenly spaced
+ * visible keys, predicts more than 1.25 x candidate_capacity candidates: it
+ * skips the bound scan (row_status 3).  The output does not depend on which
+ * rows take the unpruned path.
  * row_status: device [M] int32 or NULL.  stats: device dosa_stats or NULL
  * (counters are added to, not overwritten). */
 typedef struct dosa_params {
@@ -173,6 +177,7 @@ typedef struct dosa_stats {
   unsigned long long candidates;  /* keys with U >= tau (rescored) */
   unsigned long long survivors;   /* rescored keys with s >= tau */
   unsigned long long fallback_rows;
+  unsigned long long skipped_rows;  /* rows whose bound scan was skipped (predicted overflow) */
 } dosa_stats;
 
 size_t dosa_topk_workspace_size(const idx_problem* p, int32_t K, const dosa_params* dp, int32_t seed_ld);

@@ -50,7 +50,8 @@ class dosa_params(ctypes.Structure):
 
 class dosa_stats(ctypes.Structure):
     _fields_ = [("pairs", ctypes.c_ulonglong), ("seeds", ctypes.c_ulonglong), ("candidates", ctypes.c_ulonglong),
-                ("survivors", ctypes.c_ulonglong), ("fallback_rows", ctypes.c_ulonglong)]
+                ("survivors", ctypes.c_ulonglong), ("fallback_rows", ctypes.c_ulonglong),
+                ("skipped_rows", ctypes.c_ulonglong)]
 
 
 class block_sparse_config(ctypes.Structure):

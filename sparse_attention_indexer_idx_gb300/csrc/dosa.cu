@@ -265,13 +265,26 @@ struct PlanArgs {
   int64_t list_ld;
   const int32_t* seed_cnt;
   int shared_seeds;
-  const int32_t* active;
+  int32_t* active;            // cleared for a row predicted to overflow
+  int32_t* status;            // bit 4 set for such a row
+  const float* tau;           // [M]
+  int64_t cap;                // candidate capacity per row
   uint16_t* qprep;            // [M, 32, D] bf16
   float* wfold;               // [M, 32]
   float* coef;                // [M]
 };
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// x . y over D floats in shared memory, the lanes across d; every lane gets the sum.
+__device__ __forceinline__ float warp_dot(const float* x, const float* y, int D) {
+  const int lane = threadIdx.x & 31;
+  float s = 0.0f;
+  for (int d = lane; d < D; d += 32) s = __fmaf_rn(x[d], y[d], s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
 
 __device__ __forceinline__ uint16_t f_to_bf16_rn(float x) {
   uint32_t u = __float_as_uint(x);
@@ -285,16 +298,41 @@ __device__ __forceinline__ float e4m3_to_f(uint8_t b) {
   return s ? -v : v;
 }
 
-// One thread block per query.  Shared memory: q [H][D] f32, sample keys
-// [ns][D] f32, and per-head scratch.
+// One key or query row (D values, bf16 or e4m3 codes) into dst[0..D) as fp32:
+// the warp loads it with one 8-byte (bf16) or 4-byte (e4m3) load per lane.
+__device__ __forceinline__ void warp_load_row(const void* base, int dtype, int64_t row, int D, float* dst) {
+  const int lane = threadIdx.x & 31;
+  for (int d = 4 * lane; d < D; d += 128) {
+    float v[4];
+    if (dtype == IDX_FP8_E4M3) {
+      const uint32_t c = *reinterpret_cast<const uint32_t*>((const uint8_t*)base + row * D + d);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = e4m3_to_f((uint8_t)(c >> (8 * e)));
+    } else {
+      const uint2 c = *reinterpret_cast<const uint2*>((const uint16_t*)base + row * D + d);
+      v[0] = bf16_to_f((uint16_t)(c.x & 0xffffu));
+      v[1] = bf16_to_f((uint16_t)(c.x >> 16));
+      v[2] = bf16_to_f((uint16_t)(c.y & 0xffffu));
+      v[3] = bf16_to_f((uint16_t)(c.y >> 16));
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dst[d + e] = v[e];
+  }
+}
+
+// One thread block per query.  Shared memory: q [H][D+1] f32, sample keys
+// [ns][D+1] f32, and per-head scratch.
 __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   extern __shared__ __align__(16) float pl[];
   const idx_problem& p = a.p;
   const int64_t m = blockIdx.x;
   const int H = p.H, D = p.D, R = a.R;
   float* q = pl;                       // H*D
-  float* ks = q + H * D;               // n_sample*D
-  float* qn2 = ks + a.n_sample * D;    // H: ||q_h||^2
+  // rows of q and of the sample keys are DP = D + 1 floats apart, so threads
+  // that walk different rows at the same d hit different banks
+  const int DP = D + 1;
+  float* ks = q + H * DP;              // n_sample rows
+  float* qn2 = ks + a.n_sample * DP;   // H: ||q_h||^2
   float* beta = qn2 + H;               // H
   float* dn = beta + H;                // H: ||d_h||
   float* aggv = dn + H;                // D: a_A
@@ -314,23 +352,21 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     return;
   }
   const uint16_t* qsrc = (const uint16_t*)p.q + m * (int64_t)H * D;
-  for (int i = tid; i < H * D; i += kPlanThreads) q[i] = bf16_to_f(qsrc[i]);
+  for (int h = wid; h < H; h += nw) warp_load_row(p.q, IDX_BF16, m * H + h, D, q + h * DP);
   // sample keys: seed[floor(i n / ns)], i < ns = min(n_sample, n)
   const int32_t* sl = a.seed_list + (a.shared_seeds ? 0 : m * a.list_ld);
   const int n = a.seed_cnt[a.shared_seeds ? 0 : m];
   const int ns = n < a.n_sample ? n : a.n_sample;
   const int64_t kbase = p.key_off ? p.key_off[m] : 0;
-  for (int i = tid; i < ns * D; i += kPlanThreads) {
-    const int si = i / D, d = i % D;
+  for (int si = wid; si < ns; si += nw) {
     const int64_t id = sl[n <= a.n_sample ? si : (int)(((int64_t)si * n) / a.n_sample)];
-    const int64_t e = (kbase + id) * D + d;
-    ks[i] = p.k_dtype == IDX_FP8_E4M3 ? e4m3_to_f(((const uint8_t*)p.keys)[e]) : bf16_to_f(((const uint16_t*)p.keys)[e]);
+    warp_load_row(p.keys, p.k_dtype, kbase + id, D, ks + si * DP);
   }
   __syncthreads();
   // ||q_h||^2, one warp per head, fixed order
   for (int h = wid; h < H; h += nw) {
     float s = 0.0f;
-    for (int d = lane; d < D; d += 32) s = __fmaf_rn(q[h * D + d], q[h * D + d], s);
+    for (int d = lane; d < D; d += 32) s = __fmaf_rn(q[h * DP + d], q[h * DP + d], s);
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) qn2[h] = s;
   }
@@ -355,51 +391,66 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
       }
   }
   __syncthreads();
-  // anchors of the omitted positive heads (section 3.1)
-  for (int h = tid; h < H; h += kPlanThreads) {
-    const float wh = p.w[m * H + h];
-    anchor[h] = -1;
-    beta[h] = 0.0f;
-    dn[h] = 0.0f;
-    if (ret_pos[h] >= 0 || !(wh > 0.0f)) continue;
-    float best = 0.0f;
-    int bj = -1;
-    float bb = 0.0f;
-    for (int r = 0; r < R; ++r) {
-      const int j = rlist[r];
-      float dot = 0.0f;
-      for (int d = 0; d < D; ++d) dot = __fmaf_rn(q[h * D + d], q[j * D + d], dot);
-      const float b = qn2[j] > 0.0f ? fmaxf(0.0f, dot / qn2[j]) : 0.0f;
-      const float r2 = qn2[h] - 2.0f * b * dot + b * b * qn2[j];
-      if (bj < 0 || r2 < best) {
-        best = r2;
-        bj = j;
-        bb = b;
-      }
-    }
-    // residual norm of the chosen decomposition, computed directly and rounded up
-    float s = 0.0f;
-    for (int d = 0; d < D; ++d) {
-      const float x = q[h * D + d] - bb * q[bj * D + d];
-      s = __fmaf_rn(x, x, s);
-    }
-    anchor[h] = bj;
-    beta[h] = bb;
-    dn[h] = __fsqrt_ru(s) * (1.0f + 1.0e-6f);
-  }
-  // activation counts of the omitted negative heads on the samples (section 3.2)
+  // anchors of the omitted positive heads (section 3.1): one warp per head, the
+  // dot products with the lanes across d (consecutive words: no bank conflicts)
   for (int h = wid; h < H; h += nw) {
-    int count = 0;
     const float wh = p.w[m * H + h];
-    if (ret_pos[h] < 0 && wh < 0.0f) {
-      for (int si = lane; si < ns; si += 32) {
-        float dot = 0.0f;
-        for (int d = 0; d < D; ++d) dot = __fmaf_rn(q[h * D + d], ks[si * D + d], dot);
-        count += dot > 0.0f ? 1 : 0;
+    int bj = -1;
+    float bb = 0.0f, dnh = 0.0f;
+    if (ret_pos[h] < 0 && wh > 0.0f) {
+      float best = 0.0f;
+      for (int r = 0; r < R; ++r) {
+        const int j = rlist[r];
+        const float dot = warp_dot(q + h * DP, q + j * DP, D);
+        const float b = qn2[j] > 0.0f ? fmaxf(0.0f, dot / qn2[j]) : 0.0f;
+        const float r2 = qn2[h] - 2.0f * b * dot + b * b * qn2[j];
+        if (bj < 0 || r2 < best) {
+          best = r2;
+          bj = j;
+          bb = b;
+        }
       }
-      for (int o = 16; o > 0; o >>= 1) count += __shfl_xor_sync(0xffffffffu, count, o);
+      // residual norm of the chosen decomposition, computed directly and rounded up
+      float sres = 0.0f;
+      for (int d = lane; d < D; d += 32) {
+        const float x = q[h * DP + d] - bb * q[bj * DP + d];
+        sres = __fmaf_rn(x, x, sres);
+      }
+      for (int o = 16; o > 0; o >>= 1) sres += __shfl_xor_sync(0xffffffffu, sres, o);
+      dnh = __fsqrt_ru(sres) * (1.0f + 1.0e-6f);
     }
-    if (lane == 0) act[h] = count;
+    if (lane == 0) {
+      anchor[h] = bj;
+      beta[h] = bb;
+      dn[h] = dnh;
+    }
+  }
+  // activation counts of the omitted negative heads on the samples (section
+  // 3.2): one whole dot product per thread and task (head, sample); the lanes of
+  // a warp share the head and walk different sample rows
+  for (int h = tid; h < H; h += kPlanThreads) act[h] = 0;
+  __syncthreads();
+  // (a thread takes samples sq, sq + NSQ, sq + 2 NSQ, sq + 3 NSQ of one head, so
+  // every q value it loads serves four dot products)
+  const int NSQ = (ns + 3) / 4;
+  for (int t = tid; t < H * NSQ; t += kPlanThreads) {
+    const int h = t / NSQ, sq = t % NSQ;
+    const float wh = p.w[m * H + h];
+    if (!(ret_pos[h] < 0 && wh < 0.0f)) continue;
+    const float* x = q + h * DP;
+    int rows[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) rows[j] = sq + j * NSQ < ns ? sq + j * NSQ : sq;
+    float dot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int d = 0; d < D; ++d) {
+      const float xd = x[d];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dot[j] = __fmaf_rn(xd, ks[rows[j] * DP + d], dot[j]);
+    }
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c += (sq + j * NSQ < ns && dot[j] > 0.0f) ? 1 : 0;
+    if (c) atomicAdd(&act[h], c);
   }
   __syncthreads();
   // aggregate a_A = sum_{h in A} |w_h| q_h, prepared rows, folded weights
@@ -408,7 +459,7 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     float s = 0.0f;
     for (int h = 0; h < H; ++h) {
       const float wh = p.w[m * H + h];
-      if (ret_pos[h] < 0 && wh < 0.0f && ns > 0 && (float)act[h] >= need_act) s = __fmaf_rn(-wh, q[h * D + d], s);
+      if (ret_pos[h] < 0 && wh < 0.0f && ns > 0 && (float)act[h] >= need_act) s = __fmaf_rn(-wh, q[h * DP + d], s);
     }
     aggv[d] = s;
     qout[31 * D + d] = f_to_bf16_rn(s);
@@ -474,15 +525,66 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
       margin += 2.0f * sqrtf((float)D) * 7.62939453125e-6f * (sw * qmax + swf * vmax);
     }
     a.coef[m] = (c + margin) * (1.0f + 1.0e-6f);
+    e2s[0] = (c + margin) * (1.0f + 1.0e-6f);   // coef, for the estimate below
+  }
+  // Overflow estimate: the bound U of n_sample evenly spaced visible keys of the row
+  // against tau.  A row whose candidates would clearly exceed the capacity
+  // skips the bound scan and is computed on the unpruned path (as an
+  // overflowing row would be); the output is the same either way.
+  __syncthreads();
+  const float coef = e2s[0];
+  int64_t off;
+  int len;
+  row_extent(p, m, &off, &len);
+  const int ne = len < a.n_sample ? len : a.n_sample;   // the sample area holds n_sample keys
+  if (ne <= 0) return;
+  for (int si = wid; si < ne; si += nw) warp_load_row(p.keys, p.k_dtype, off + ((int64_t)si * len) / ne, D, ks + si * DP);
+  __syncthreads();
+  const float t = a.tau[m];
+  // U of every estimate key, one key per thread (the lanes walk different key rows)
+  int pass = 0;
+  for (int si = tid; si < ne; si += kPlanThreads) {
+    const float* k = ks + si * DP;
+    float u = 0.0f;
+    for (int r = 0; r < R; ++r) {
+      const float* x = q + rlist[r] * DP;
+      float dot = 0.0f;
+      for (int d = 0; d < D; ++d) dot = __fmaf_rn(x[d], k[d], dot);
+      u = __fmaf_rn(wout[r], fmaxf(dot, 0.0f), u);
+    }
+    float da = 0.0f, dk = 0.0f;
+    for (int d = 0; d < D; ++d) {
+      da = __fmaf_rn(aggv[d], k[d], da);
+      dk = __fmaf_rn(k[d], k[d], dk);
+    }
+    u = u - fmaxf(da, 0.0f);
+    u = __fmaf_rn(coef, sqrtf(dk), u);
+    if (p.k_dtype == IDX_FP8_E4M3) u *= p.key_scale[off + ((int64_t)si * len) / ne];
+    pass += u >= t ? 1 : 0;
+  }
+  for (int o = 16; o > 0; o >>= 1) pass += __shfl_xor_sync(0xffffffffu, pass, o);
+  if (lane == 0) act[wid] = pass;   // the activation counts are no longer needed
+  __syncthreads();
+  if (tid == 0) {
+    int total = 0;
+    for (int w = 0; w < nw; ++w) total += act[w];
+    const float nonseed = (float)(len - (n < len ? n : len));
+    if ((float)total / (float)ne * nonseed > 1.25f * (float)a.cap) {
+      a.active[m] = 0;
+      a.status[m] |= 4;
+    }
   }
 }
 
 // --------------------------------------------------------------- merging --
 
-__global__ void clamp_cnt_kernel(const int32_t* cand_cnt, int32_t* cand_n, int64_t M, int64_t cap) {
+// Candidates to rescore per row: none for a row that will take the unpruned
+// path anyway (too few seeds, predicted or actual overflow).
+__global__ void clamp_cnt_kernel(const int32_t* cand_cnt, const int32_t* status, int32_t* cand_n, int64_t M,
+                                 int64_t cap) {
   for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < M; m += (int64_t)gridDim.x * blockDim.x) {
     const int32_t c = cand_cnt[m];
-    cand_n[m] = c < cap ? c : (int32_t)cap;
+    cand_n[m] = status[m] != 0 ? 0 : (c < cap ? c : (int32_t)cap);
   }
 }
 
@@ -520,7 +622,7 @@ __global__ void merge_rows_kernel(int64_t M, int K, int64_t cap, const int32_t* 
 
 __global__ void stats_kernel(idx_problem p, const int32_t* seed_cnt, int shared_seeds, const int32_t* cand_cnt,
                              const int32_t* status, const int32_t* active, dosa_stats* st, int32_t* row_status) {
-  unsigned long long pairs = 0, seeds = 0, cands = 0, fb = 0;
+  unsigned long long pairs = 0, seeds = 0, cands = 0, fb = 0, skipped = 0;
   for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < p.M; m += (int64_t)gridDim.x * blockDim.x) {
     int64_t off;
     int len;
@@ -532,7 +634,8 @@ __global__ void stats_kernel(idx_problem p, const int32_t* seed_cnt, int shared_
     }
     const int s = status[m];
     fb += s != 0 ? 1ull : 0ull;
-    if (row_status) row_status[m] = (s & 1) ? 1 : ((s & 2) ? 2 : 0);
+    skipped += (s & 4) ? 1ull : 0ull;
+    if (row_status) row_status[m] = (s & 1) ? 1 : ((s & 4) ? 3 : ((s & 2) ? 2 : 0));
   }
   if (!st) return;
   for (int o = 16; o > 0; o >>= 1) {
@@ -540,12 +643,14 @@ __global__ void stats_kernel(idx_problem p, const int32_t* seed_cnt, int shared_
     seeds += __shfl_xor_sync(0xffffffffu, seeds, o);
     cands += __shfl_xor_sync(0xffffffffu, cands, o);
     fb += __shfl_xor_sync(0xffffffffu, fb, o);
+    skipped += __shfl_xor_sync(0xffffffffu, skipped, o);
   }
   if ((threadIdx.x & 31) == 0) {
     atomicAdd(&st->pairs, pairs);
     atomicAdd(&st->seeds, seeds);
     atomicAdd(&st->candidates, cands);
     atomicAdd(&st->fallback_rows, fb);
+    atomicAdd(&st->skipped_rows, skipped);
   }
 }
 
@@ -768,10 +873,13 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
   pa.seed_cnt = w.seed_cnt;
   pa.shared_seeds = s.shared_seeds ? 1 : 0;
   pa.active = w.active;
+  pa.status = w.status;
+  pa.tau = w.tau;
+  pa.cap = s.cap;
   pa.qprep = w.qprep;
   pa.wfold = w.wfold;
   pa.coef = w.coef;
-  const size_t psmem = ((size_t)p.H * p.D + (size_t)dp.n_sample * p.D + 4 * (size_t)p.H + p.D) * sizeof(float) +
+  const size_t psmem = ((size_t)p.H * (p.D + 1) + (size_t)dp.n_sample * (p.D + 1) + 4 * (size_t)p.H + p.D) * sizeof(float) +
                        (3 * (size_t)p.H + 32) * sizeof(int);
   DOSA_CHECK(cudaFuncSetAttribute(dosa_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem));
   dosa_plan_kernel<<<(unsigned)M, kPlanThreads, psmem, st>>>(pa);
@@ -786,7 +894,7 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
                           w.status, dp.retained_heads, w.active, st));
 
   // ---- exact rescoring of the candidates, merge with the seed top-K
-  clamp_cnt_kernel<<<grid_for(M, 256), 256, 0, st>>>(w.cand_cnt, w.cand_n, M, s.cap);
+  clamp_cnt_kernel<<<grid_for(M, 256), 256, 0, st>>>(w.cand_cnt, w.status, w.cand_n, M, s.cap);
   DOSA_CHECK(launch_score_gather(p, w.cand, w.cand_n, s.cap, w.cand_sc, s.cap, w.active, st));
   merge_rows_kernel<<<(unsigned)M, 256, 0, st>>>(M, K, s.cap, w.stop_ids, w.stop_sc, w.cand, w.cand_n, w.cand_sc,
                                                   w.tau, w.status, w.mrg_sc, w.mrg_id, w.mrg_len, w.fbmask,

@@ -418,6 +418,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     int64_t cur_g = -1;
     int64_t gbase = 0;                         // first key row of the group (kept: no global load per tile)
     int32_t gcnt = 0;                          // kGather: list length of the group
+    // kGather: this lane's four list entries of the next unit, loaded one unit
+    // ahead so that the list read overlaps the previous unit's gather
+    int32_t pf[4] = {0, 0, 0, 0};
+    int64_t pf_g = -1, pf_t = -1;
     uint32_t na = 0, nb = 0;
     while (u.valid()) {
       if (u.g != cur_g) {
@@ -448,6 +452,17 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       uint8_t* dst = sA + as * C::A_BYTES;
       uint64_t* fbar = &a_full[as];
+      int32_t graw[4] = {0, 0, 0, 0};   // kGather: list entries of tile rows 4 lane .. 4 lane + 3
+      if (C::GATHER) {
+        if (pf_g == u.g && pf_t == u.t) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) graw[i] = pf[i];
+        } else {
+          const int32_t* lst = args.list + u.g * args.gld + u.t * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) graw[i] = (int)(u.t * 128) + 4 * lane + i < gcnt ? lst[4 * lane + i] : 0;
+        }
+      }
       if constexpr (C::FP8) {
         // key scales: lane l copies those of tile rows 4l..4l+3 (rows clamped into
         // the buffer; a scale past the row's end is never used)
@@ -460,7 +475,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         for (int i = 0; i < 4 * C::SUB; ++i) {
           const int pos = (int)(u.t * C::UKEYS) + 128 * (i >> 2) + 4 * lane + (i & 3);
           int64_t row = gbase + pos;
-          if (C::GATHER) row = gbase + (pos < gcnt ? (int64_t)args.list[u.g * args.gld + pos] : 0);
+          if (C::GATHER) row = gbase + (int64_t)graw[i & 3];
           row = row < 0 ? 0 : (row >= args.p.n_keys ? args.p.n_keys - 1 : row);
           cp_async_4(sdst + 128 * (i >> 2) + (i & 3), args.p.key_scale + row);
         }
@@ -468,13 +483,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       }
       if (C::GATHER) {
         // lane l fetches tile rows 4l..4l+3 (list positions t*128 + 4l + i)
-        const int32_t* lst = args.list + u.g * args.gld + u.t * 128;
         int32_t y[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int pos = (int)(u.t * 128) + 4 * lane + i;
-          int64_t id = pos < gcnt ? (int64_t)lst[4 * lane + i] : 0;
-          int64_t row = gbase + id;
+          int64_t row = gbase + (int64_t)graw[i];
           row = row < 0 ? 0 : (row >= args.p.n_keys ? args.p.n_keys - 1 : row);
           y[i] = (int32_t)row;
         }
@@ -482,6 +494,17 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         __syncwarp();
         tma_gather4(dst + lane * 512, &tmap_k, fbar, 0, y[0], y[1], y[2], y[3]);
         if (!C::FP8) tma_gather4(dst + C::A_BYTES / 2 + lane * 512, &tmap_k, fbar, 64, y[0], y[1], y[2], y[3]);
+        // the next unit's entries
+        TcUnits<C> nx = u;
+        nx.advance();
+        if (nx.valid()) {
+          const int32_t cn = nx.g == u.g ? gcnt : args.cnt[nx.g];
+          const int32_t* l2 = args.list + nx.g * args.gld + nx.t * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) pf[i] = (int)(nx.t * 128) + 4 * lane + i < cn ? l2[4 * lane + i] : 0;
+          pf_g = nx.g;
+          pf_t = nx.t;
+        }
       } else if (lane == 0) {
         const int32_t y = (int32_t)(gbase + u.t * C::UKEYS);
         mbar_arrive_expect_tx(fbar, C::A_BYTES);
@@ -679,6 +702,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       }
       const int acc = nacc % C::SACC;
       const int key = (int)(u.t * C::UKEYS) + sub * 128 + row_in_tile;
+      // kBound with one seed bitmap for all rows: this key's word, read before the
+      // wait so that the load overlaps it (words cover max_key_len keys)
+      uint32_t sword = 0;
+      if (C::BOUND && args.seed_stride == 0 && key < args.p.max_key_len) sword = __ldg(args.seedbits + (key >> 5));
       bool got = mbar_wait(&acc_full[acc], (nacc / C::SACC) & 1, abort_flag);
       // the key-tile slot of this unit (bound: read below for ||k||, so the slot is
       // held until this warp releases it) and its scale slot (FP8)
@@ -861,8 +888,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           bool is_cand = false;
           if (key < len) {
             if (C::FP8) ub = ub * kscale;
-            const uint32_t* bits = args.seedbits + (args.seed_stride ? m * args.seed_stride : 0);
-            const bool seed = (bits[key >> 5] >> (key & 31)) & 1u;
+            const uint32_t word = args.seed_stride ? args.seedbits[m * args.seed_stride + (key >> 5)] : sword;
+            const bool seed = (word >> (key & 31)) & 1u;
             is_cand = !seed && !(ub < sAux[4 * qi + 1]);
           }
           const unsigned mask = __ballot_sync(0xffffffffu, is_cand);
