@@ -130,3 +130,26 @@ def test_topk_all_equal_and_two_valued_rows(B):
         o_ids, _ = odsa.topk(s[m].astype(np.float64), K)
         assert g[m].tolist() == o_ids.tolist(), m
     assert B.device_error() == 0
+
+
+def test_topk_heavy_ties_among_candidates(B):
+    """The ~2500 best keys share three values (buckets of ~800 equal keys: the
+    candidates go through the radix cut and the bitonic sort); the rest are
+    distinct and lower.  Ties resolve to the lowest ids."""
+    M, L, K = 3, 40000, 2048
+    rng = np.random.default_rng(21)
+    s = rng.random((M, L), dtype=np.float32)
+    for m in range(M):
+        top = rng.choice(L, 2500, replace=False)
+        s[m, top] = rng.choice(np.array([10.0, 11.0, 12.0], dtype=np.float32), 2500)
+    lens = np.full(M, L, dtype=np.int32)
+    ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    sc = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(1, B.idx_topk_scores_workspace_size(M, L, K)), dtype=torch.uint8, device="cuda")
+    B.idx_topk_scores(_dev(s, torch.float32), _dev(lens), L, K, ids, sc, ws=ws)
+    g_ids, g_sc = ids.cpu().numpy(), sc.cpu().numpy()
+    for m in range(M):
+        o_ids, o_sc = odsa.topk(s[m].astype(np.float64), K)
+        assert g_ids[m].tolist() == o_ids.tolist(), m
+        assert np.array_equal(g_sc[m], o_sc.astype(np.float32)), m
+    assert B.device_error() == 0
