@@ -224,7 +224,16 @@ idx_status witness_indices(const int32_t* learned, int64_t rows, int32_t topk, c
  *   index_q device [Q, n_kv, D] float32, index_k device [L, D] float32.
  *   out device [Q, n_kv, out_width] int32, -1 padded; out_count device
  *   [Q, n_kv] int32 or NULL.  out_width >= max(top, init + local).
- * Block size 0 gives empty selections. */
+ * Block size 0 gives empty selections.
+ *
+ * With block_size 128, D = 128 and top_blocks <= 512 the block maxima are
+ * first computed on the tensor cores (tf32 operands, fp32 accumulate) with a
+ * certified error bound e_b = (2^-9 + 2^-12) ||q|| max_p ||k_p||; a block
+ * whose bound interval lies clear of the selection cut is decided by it, the
+ * others are scored in the page's order.  The selection is the same either
+ * way.  stats: device block_select_stats or NULL, added to (that route only).
+ * Workspace: block_select_workspace_size(), about Q * n_kv * ceil(L/bs) * 8
+ * bytes. */
 typedef struct block_sparse_config {
   int32_t block_size;   /* 128: also the KV page size */
   int32_t top_blocks;   /* 32 */
@@ -232,10 +241,20 @@ typedef struct block_sparse_config {
   int32_t local_blocks; /* 2 */
 } block_sparse_config;
 
+typedef struct block_select_stats {
+  unsigned long long pairs;           /* (query, head) pairs whose selection needed scores */
+  unsigned long long blocks_bounded;  /* their non-forced blocks, all bounded */
+  unsigned long long blocks_rescored; /* of those, scored in the page's order */
+  unsigned long long fallback_pairs;  /* pairs that rescored every non-forced block */
+  float max_bound_use;                /* largest |A_b - E_b| / e_b over rescored blocks (max-combined) */
+  float reserved;
+} block_select_stats;
+
 size_t block_select_workspace_size(int64_t Q, int32_t n_kv, int64_t L, const block_sparse_config* cfg);
 idx_status block_select(const float* index_q, const float* index_k, const int32_t* query_pos, int64_t Q,
                         int32_t n_kv, int32_t D, int64_t L, const block_sparse_config* cfg, int32_t* out,
-                        int32_t out_width, int32_t* out_count, void* ws, size_t ws_bytes, void* stream);
+                        int32_t out_width, int32_t* out_count, block_select_stats* stats, void* ws,
+                        size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------ block_select_static
  * block_select for callers that cannot allocate device memory: code that runs
@@ -245,7 +264,8 @@ idx_status block_select(const float* index_q, const float* index_k, const int32_
  * source page has a counterpart of this entry point; it is a deployment
  * convenience with the same result as block_select.
  *
- * Identical arguments and output to block_select, minus (ws, ws_bytes): the
+ * Identical arguments and output to block_select, minus (stats, ws,
+ * ws_bytes); every block score is computed in the page's order.  The
  * per-(query, head, block) scratch lives in a fixed device array inside the
  * library, 2^23 words (32 MiB), which every GPU that loads the library holds
  * until the process exits.  Calls with Q * n_kv * ceil(L / block_size) above

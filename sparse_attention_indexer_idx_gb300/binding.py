@@ -54,6 +54,26 @@ class dosa_stats(ctypes.Structure):
                 ("skipped_rows", ctypes.c_ulonglong)]
 
 
+class block_select_stats(ctypes.Structure):
+    _fields_ = [("pairs", ctypes.c_ulonglong), ("blocks_bounded", ctypes.c_ulonglong),
+                ("blocks_rescored", ctypes.c_ulonglong), ("fallback_pairs", ctypes.c_ulonglong),
+                ("max_bound_use", ctypes.c_float), ("reserved", ctypes.c_float)]
+
+
+def block_select_stats_tensor(device="cuda") -> torch.Tensor:
+    """Zeroed device storage for one block_select_stats (40 bytes)."""
+    return torch.zeros(5, dtype=torch.int64, device=device)
+
+
+def block_select_stats_read(t: torch.Tensor) -> dict:
+    """block_select_stats storage -> dict (copies to the host)."""
+    h = t.detach().cpu()
+    u = h.tolist()
+    f = h[4:5].view(torch.float32).tolist()
+    return {"pairs": u[0], "blocks_bounded": u[1], "blocks_rescored": u[2], "fallback_pairs": u[3],
+            "max_bound_use": f[0]}
+
+
 class block_sparse_config(ctypes.Structure):
     _fields_ = [("block_size", ctypes.c_int32), ("top_blocks", ctypes.c_int32), ("init_blocks", ctypes.c_int32),
                 ("local_blocks", ctypes.c_int32)]
@@ -86,7 +106,8 @@ EXPORTS = {
     "block_select": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                       ctypes.POINTER(block_sparse_config), ctypes.c_void_p, ctypes.c_int32,
-                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                      ctypes.c_void_p]),
     "block_select_static": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                              ctypes.POINTER(block_sparse_config), ctypes.c_void_p, ctypes.c_int32,
@@ -236,12 +257,17 @@ def block_select_workspace_size(Q: int, n_kv: int, L: int, cfg: block_sparse_con
 
 
 def block_select(index_q: torch.Tensor, index_k: torch.Tensor, query_pos: torch.Tensor, cfg: block_sparse_config,
-                 out: torch.Tensor, out_count: Optional[torch.Tensor], ws: Optional[torch.Tensor], stream=None):
+                 out: torch.Tensor, out_count: Optional[torch.Tensor], ws: Optional[torch.Tensor], stream=None,
+                 stats: Optional[torch.Tensor] = None):
+    """stats: block_select_stats_tensor() storage or None."""
     Q, n_kv, D = index_q.shape
     L = index_k.shape[0]
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    if stats is not None and stats.numel() * stats.element_size() < ctypes.sizeof(block_select_stats):
+        raise ValueError("stats needs 40 bytes")
     _check(lib().block_select(_ptr(index_q), _ptr(index_k), _ptr(query_pos), Q, n_kv, D, L, ctypes.byref(cfg),
-                              _ptr(out), out.shape[-1], _ptr(out_count), _ptr(ws), ws_bytes, _stream(stream)))
+                              _ptr(out), out.shape[-1], _ptr(out_count), _ptr(stats), _ptr(ws), ws_bytes,
+                              _stream(stream)))
     return out, out_count
 
 

@@ -215,7 +215,8 @@ size_t block_select_workspace_size(int64_t Q, int32_t n_kv, int64_t L, const blo
 
 idx_status block_select(const float* index_q, const float* index_k, const int32_t* query_pos, int64_t Q,
                         int32_t n_kv, int32_t D, int64_t L, const block_sparse_config* cfg, int32_t* out,
-                        int32_t out_width, int32_t* out_count, void* ws, size_t ws_bytes, void* stream) {
+                        int32_t out_width, int32_t* out_count, block_select_stats* stats, void* ws,
+                        size_t ws_bytes, void* stream) {
   if (!cfg) return fail(IDX_ERR_INVALID_ARG, "config is NULL");
   if (Q < 0 || n_kv < 0 || D <= 0 || L < 0 || cfg->block_size < 0 || cfg->top_blocks < 0 || cfg->init_blocks < 0 ||
       cfg->local_blocks < 0)
@@ -235,7 +236,7 @@ idx_status block_select(const float* index_q, const float* index_k, const int32_
     return fail(IDX_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
   if (block_select_workspace_size(Q, n_kv, L, cfg) > 0 && !ws) return fail(IDX_ERR_INVALID_ARG, "workspace is NULL");
   return cuda_status(launch_block_select(index_q, index_k, query_pos, Q, n_kv, D, L, *cfg, out, out_width, out_count,
-                                         ws, (cudaStream_t)stream),
+                                         ws, (cudaStream_t)stream, stats, true),
                      "block_select");
 }
 

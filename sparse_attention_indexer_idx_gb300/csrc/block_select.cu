@@ -15,42 +15,13 @@
 //     ascending block order.
 #include <mutex>
 
-#include "internal.h"
+#include "block_select.cuh"
 #include "topk.cuh"
 
 namespace idx {
 
 constexpr int kBsThreads = 128;   // pairs per thread block
 constexpr int kBsChunk = 64;      // key positions staged per round
-
-struct BlockGeom {
-  int64_t n_blocks;
-  int64_t n_forced;
-  int64_t budget;
-  bool scoring;  // false when the forced blocks already decide the selection
-};
-
-__device__ __forceinline__ BlockGeom block_geom(int64_t pos, int64_t L, const block_sparse_config& c) {
-  BlockGeom g{0, 0, 0, false};
-  if (c.block_size <= 0 || pos < 0) return g;
-  int64_t causal = pos / c.block_size + 1;
-  int64_t exist = (L + c.block_size - 1) / c.block_size;
-  g.n_blocks = causal < exist ? causal : exist;
-  const int64_t n = g.n_blocks;
-  int64_t a = c.init_blocks < n ? c.init_blocks : n;              // [0, a) forced
-  int64_t z = n - c.local_blocks;                                  // [max(z,0), n) forced
-  z = z < 0 ? 0 : z;
-  int64_t overlap = a > z ? a - z : 0;
-  g.n_forced = a + (n - z) - overlap;
-  g.budget = c.top_blocks > g.n_forced ? c.top_blocks : g.n_forced;
-  g.scoring = !(g.n_forced >= g.budget || g.n_forced == n);
-  return g;
-}
-
-__device__ __forceinline__ bool block_forced(int64_t b, int64_t n, const block_sparse_config& c) {
-  int64_t z = n - c.local_blocks;
-  return b < c.init_blocks || b >= (z < 0 ? 0 : z);
-}
 
 // Any D: the query is read from global memory (L1), a chunk of keys is staged
 // in shared memory, one thread per pair, scalar fp32 in the page's order.
@@ -109,22 +80,6 @@ __global__ void __launch_bounds__(kBsThreads) block_score_kernel(const float* __
 //  * a block of up to 128 keys is staged transposed ([d][key]) so that one
 //    16-byte load gives four keys' d-th elements.
 constexpr int kBs128Keys = 128;   // keys staged per round
-
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
-  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
-  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
-  return ((uint64_t)hi << 32) | lo;
-}
 
 // One 8-key group, this lane's half of D: chains (keys 8g+2j, 8g+2j+1) of
 // pair A in acc[j], of pair B in acc[4+j], j < 4; kcol = kt + (64 h) * 128 + 8 g.
@@ -288,17 +243,32 @@ __global__ void __launch_bounds__(kPickThreads) block_pick_kernel(const int32_t*
   if (out_count && threadIdx.x == 0) out_count[pair] = count;
 }
 
-size_t block_select_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c) {
+// Scratch of the CUDA-core route: one ordered key per (pair, block).
+static size_t block_select_core_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c) {
   if (c.block_size <= 0) return 0;
   int64_t nbm = (L + c.block_size - 1) / c.block_size;
   return (size_t)(Q * n_kv) * (size_t)nbm * sizeof(uint32_t);
 }
 
+// D is not an argument of the workspace query: a configuration the tensor-core
+// route may take (block size 128, D = 128) gets room for it.
+size_t block_select_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c) {
+  size_t w = block_select_core_ws(Q, n_kv, L, c);
+  if (block_select_tc_applies(128, c, Q, n_kv, L)) {
+    const size_t t = block_select_tc_ws(Q, n_kv, L, c);
+    w = t > w ? t : w;
+  }
+  return w;
+}
+
 cudaError_t launch_block_select(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv, int D,
                                 int64_t L, const block_sparse_config& c, int32_t* out, int out_width,
-                                int32_t* out_count, void* ws, cudaStream_t st) {
+                                int32_t* out_count, void* ws, cudaStream_t st, block_select_stats* stats,
+                                bool tensor_route) {
   const int64_t pairs = Q * n_kv;
   if (pairs <= 0) return cudaSuccess;
+  if (tensor_route && block_select_tc_applies(D, c, Q, n_kv, L))
+    return launch_block_select_tc(q, k, pos, Q, n_kv, L, c, out, out_width, out_count, ws, stats, st);
   const int64_t nbm = c.block_size > 0 ? (L + c.block_size - 1) / c.block_size : 0;
   uint32_t* bkey = (uint32_t*)ws;
   cudaError_t e;
@@ -391,7 +361,7 @@ extern "C" idx_status block_select_static(const float* index_q, const float* ind
   if (D > 256) return fail(IDX_ERR_UNSUPPORTED, "D=%d above 256", D);
   if (D == 128 && (((uintptr_t)index_q | (uintptr_t)index_k) & 15))
     return fail(IDX_ERR_INVALID_ARG, "index_q/index_k must be 16-byte aligned");
-  const int64_t words = (int64_t)(block_select_ws(Q, n_kv, L, *cfg) / sizeof(uint32_t));
+  const int64_t words = (int64_t)(block_select_core_ws(Q, n_kv, L, *cfg) / sizeof(uint32_t));
   if (words > kStaticBlockScores)
     return fail(IDX_ERR_WORKSPACE_TOO_SMALL,
                 "block_select_static: Q*n_kv*ceil(L/block_size) = %lld block scores exceed the fixed %lld",
@@ -402,7 +372,7 @@ extern "C" idx_status block_select_static(const float* index_q, const float* ind
   idx_status st = static_scratch(&scratch);
   if (st != IDX_OK) return st;
   cudaError_t e = launch_block_select(index_q, index_k, query_pos, Q, n_kv, D, L, *cfg, out, out_width, out_count,
-                                      scratch, (cudaStream_t)stream);
+                                      scratch, (cudaStream_t)stream, nullptr, false);
   if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "block_select_static: %s", cudaGetErrorString(e));
   return IDX_OK;
 }

@@ -1,0 +1,1045 @@
+// MiniMax-M3 block-sparse selection, tensor-core route for 128-token blocks and
+// D = 128 ("ferrox_core/block_sparse.rs": block_sparse_select, select_for_head,
+// dot).
+//
+// The page scores a block by the max over its positions of a dot product summed
+// in sequence in fp32, and the selected indices depend on those exact values,
+// so a tensor-core pass cannot decide the selection by itself.  It can decide
+// almost all of it: with A_b the block max computed by the tensor cores and a
+// certified bound e_b >= |A_b - E_b| (E_b the page's exact block score), a block
+// whose interval [A_b - e_b, A_b + e_b] lies clear of the cut is settled either
+// way, and only the few blocks per (query, head) pair whose intervals straddle
+// it are scored in the page's order.  The output is the page's selection bit
+// for bit.
+//
+//  1. bt_prep_kernel: queries ordered by their number of visible blocks (a
+//     counting sort; a tile of 32 queries then scans about as many blocks as
+//     each of its queries needs); an upper bound of ||q|| per (query, head)
+//     and of max ||k_p|| per block.
+//  2. bt_max_kernel: A_b over every visible block of every pair, on
+//     tcgen05.mma kind::tf32.  A CTA holds 256 (query, head) rows (two M = 128
+//     tiles, fetched by TMA gather4 in the sorted order) and streams key
+//     blocks (128 keys = N, four 32-float K chunks, one TMA box each) through a
+//     six-stage ring; each key chunk feeds eight MMAs (K = 8, both tiles).  The
+//     accumulators (two stages of 2 x 128 TMEM columns) are reduced by eight
+//     epilogue warps: a thread owns one (query, head) row, so the block max is
+//     a max over its own 128 columns (positions past the query's position or
+//     past L masked).  Units are (row tile pair, key block), split into one
+//     contiguous range per persistent CTA.
+//  3. bt_classify_kernel (one warp per pair): the n_need-th largest lower bound
+//     T; candidates are the blocks with upper bound >= T (every other block has
+//     n_need blocks certainly above it); a candidate is certainly in when fewer
+//     than n_need other candidates could reach its lower bound.  Pairs whose
+//     undecided blocks are exactly the places left are done here; the others
+//     list their undecided blocks per key block.
+//  4. bt_exact_kernel (one CTA per key block): the listed (pair, block) scores
+//     in the page's order on the fp32 pipes (packed f32x2 multiply and add,
+//     each half rounded as the scalar instructions round).
+//  5. bt_resolve_kernel (one warp per open pair): the remaining places from the
+//     exact scores by (score desc, block asc); a pair with too many undecided
+//     blocks has every non-forced block rescored and takes its whole top list
+//     here.
+//
+// The bound.  The tensor core reads an fp32 operand as tf32 (its top 19 bits),
+// an error below 2^-10 relative per operand; products of tf32 values are exact
+// in fp32, and the fp32 accumulation of 128 products (16 MMAs of K = 8) and the
+// page's own sequential sum each stay well inside 2^-14 of sum |q_d k_d|.  So
+// |A_p - E_p| <= (2^-9 + 2^-12) ||q|| ||k_p|| for every position p, and the
+// same holds for the block maxima.  ||q|| and max ||k_p|| are rounded up.
+// bt_exact_kernel measures |A_b - E_b| / e_b on every block it rescores and
+// reports the largest value through block_select_stats.
+#include <cudaTypedefs.h>
+
+#include "block_select.cuh"
+
+namespace idx {
+
+bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
+
+constexpr float kBtErr = 0.001953125f + 0.000244140625f;   // 2^-9 + 2^-12
+constexpr int kBtRowsT = 256;        // (query, head) rows per CTA tile: two MMA tiles of 128
+constexpr int kBtKStages = 6;        // key-chunk ring
+constexpr int kBtChunkBytes = 128 * 128;   // 128 keys x 32 floats
+constexpr int kBtATile = 4 * kBtChunkBytes;   // 128 rows x 128 floats
+constexpr int kBtNE = 8;             // epilogue warps
+constexpr int kBtThreads = 32 * (2 + kBtNE);
+constexpr int kBtTmemCols = 512;     // two stages x two tiles x 128 keys
+constexpr int kBtCapC = 256;         // candidates per pair held by the classifier
+constexpr int kBtCapU = 64;          // undecided blocks per pair resolved from a list
+constexpr int kBtMaxTop = 512;       // top_blocks handled by this route
+constexpr int kBtSortBins = 8192;
+
+// Per-pair state written by the classifier.
+enum BtStatus { kBtDone = 0, kBtList = 1, kBtFallback = 2 };
+
+struct BtWs {
+  int32_t* order;      // [Q] query rank -> query
+  int32_t* nbT;        // [nT] blocks scanned by row tile pair T
+  float* qn;           // [Q*n_kv] upper bound of ||q|| (original pair order)
+  float* kmax;         // [nbm] upper bound of max ||k_p|| over the block
+  float* amax;         // [slots, nbm] A_b (float), overwritten by the exact ordered key when rescored
+  int32_t* icnt;       // [nbm] listed pairs per block
+  int32_t* ilist;      // [nbm, slots] slots listed per block
+  int32_t* ulist;      // [slots, kBtCapU] undecided blocks (ascending)
+  int4* sstat;         // [slots] {status, k_in, n_u, m_need}
+};
+
+struct BtProblem {
+  const float* q;
+  const float* k;
+  const int32_t* qpos;
+  int64_t Q;
+  int n_kv;
+  int64_t L;
+  int64_t slots;   // Q * n_kv
+  int64_t nbm;     // ceil(L / 128)
+  int64_t nT;      // ceil(slots / 256)
+  block_sparse_config c;
+};
+
+__host__ __device__ inline int64_t bt_round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+static BtWs bt_carve(void* base, const BtProblem& P) {
+  WsCarver w(base);
+  BtWs s;
+  s.order = w.take<int32_t>((size_t)P.Q);
+  s.nbT = w.take<int32_t>((size_t)P.nT);
+  s.qn = w.take<float>((size_t)P.slots);
+  s.kmax = w.take<float>((size_t)P.nbm);
+  s.amax = w.take<float>((size_t)(P.slots * P.nbm));
+  s.icnt = w.take<int32_t>((size_t)P.nbm);
+  s.ilist = w.take<int32_t>((size_t)(P.nbm * P.slots));
+  s.ulist = w.take<int32_t>((size_t)(P.slots * kBtCapU));
+  s.sstat = w.take<int4>((size_t)P.slots);
+  return s;
+}
+
+static size_t bt_ws_bytes(const BtProblem& P) {
+  WsCarver w(nullptr);
+  w.take<int32_t>((size_t)P.Q);
+  w.take<int32_t>((size_t)P.nT);
+  w.take<float>((size_t)P.slots);
+  w.take<float>((size_t)P.nbm);
+  w.take<float>((size_t)(P.slots * P.nbm));
+  w.take<int32_t>((size_t)P.nbm);
+  w.take<int32_t>((size_t)(P.nbm * P.slots));
+  w.take<int32_t>((size_t)(P.slots * kBtCapU));
+  w.take<int4>((size_t)P.slots);
+  return w.used + 256;
+}
+
+__device__ __forceinline__ int64_t bt_nblocks(int64_t pos, const BtProblem& P) {
+  return block_geom(pos, P.L, P.c).n_blocks;
+}
+
+// Query of a slot (sorted rank * n_kv + head) and its row of index_q.
+__device__ __forceinline__ int64_t bt_slot_query(const BtProblem& P, const BtWs& W, int64_t slot) {
+  return (int64_t)W.order[slot / P.n_kv];
+}
+
+// Upper bound of the Euclidean norm of four 128-float rows r0..r0+3 (rows past
+// `rows` give 0): lanes 8g..8g+7 read row r0 + g, 16 floats each.
+__device__ __forceinline__ float bt_norm4(const float* base, int64_t r0, int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = r0 + (lane >> 3);
+  float ss = 0.0f;
+  if (r < rows) {
+    const float4* p = reinterpret_cast<const float4*>(base + r * 128) + (lane & 7) * 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = __ldg(p + i);
+      ss = __fmaf_rn(v.x, v.x, ss);
+      ss = __fmaf_rn(v.y, v.y, ss);
+      ss = __fmaf_rn(v.z, v.z, ss);
+      ss = __fmaf_rn(v.w, v.w, ss);
+    }
+  }
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+  // 128 squares summed in fp32 are within 2^-16 of the exact sum; sqrt rounded up, then 2^-14 on top
+  return __fmul_ru(__fsqrt_ru(ss), 1.00006103515625f);
+}
+
+constexpr int kBtPrepThreads = 256;
+
+// CTA 0: counting sort of the queries by visible block count (rank -> query),
+// the block count of every row tile pair, and the per-block list counters set
+// to zero.  Other CTAs: the norm bounds (warp tasks: key blocks, then groups of
+// four (query, head) rows).
+__global__ void __launch_bounds__(kBtPrepThreads) bt_prep_kernel(BtProblem P, BtWs W) {
+  if (blockIdx.x == 0) {
+    __shared__ int32_t hist[kBtSortBins];
+    __shared__ int32_t part[kBtPrepThreads];
+    int shift = 0;
+    while ((P.nbm >> shift) + 1 > kBtSortBins) ++shift;
+    for (int i = threadIdx.x; i < kBtSortBins; i += kBtPrepThreads) hist[i] = 0;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < P.Q; i += kBtPrepThreads)
+      atomicAdd(&hist[bt_nblocks(P.qpos[i], P) >> shift], 1);
+    __syncthreads();
+    // exclusive scan: 32 bins per thread, then the 256 partial sums
+    constexpr int PER = kBtSortBins / kBtPrepThreads;
+    int run = 0;
+    for (int j = 0; j < PER; ++j) {
+      const int v = hist[threadIdx.x * PER + j];
+      hist[threadIdx.x * PER + j] = run;
+      run += v;
+    }
+    part[threadIdx.x] = run;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int acc = 0;
+      for (int t = 0; t < kBtPrepThreads; ++t) {
+        const int v = part[t];
+        part[t] = acc;
+        acc += v;
+      }
+    }
+    __syncthreads();
+    for (int j = 0; j < PER; ++j) hist[threadIdx.x * PER + j] += part[threadIdx.x];
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < P.Q; i += kBtPrepThreads) {
+      const int r = atomicAdd(&hist[bt_nblocks(P.qpos[i], P) >> shift], 1);
+      W.order[r] = (int32_t)i;
+    }
+    __syncthreads();
+    for (int64_t T = threadIdx.x; T < P.nT; T += kBtPrepThreads) {
+      const int64_t r0 = T * kBtRowsT / P.n_kv;
+      int64_t r1 = ((T + 1) * kBtRowsT - 1) / P.n_kv;
+      r1 = r1 < P.Q - 1 ? r1 : P.Q - 1;
+      int64_t mx = 0;
+      for (int64_t r = r0; r <= r1; ++r) {
+        const int64_t nb = bt_nblocks(P.qpos[W.order[r]], P);
+        mx = nb > mx ? nb : mx;
+      }
+      W.nbT[T] = (int32_t)mx;
+    }
+    for (int64_t b = threadIdx.x; b < P.nbm; b += kBtPrepThreads) W.icnt[b] = 0;
+    return;
+  }
+  const int warps = kBtPrepThreads / 32;
+  const int64_t n_tasks = P.nbm + (P.slots + 3) / 4;
+  for (int64_t t = (int64_t)(blockIdx.x - 1) * warps + (threadIdx.x >> 5); t < n_tasks;
+       t += (int64_t)(gridDim.x - 1) * warps) {
+    const int lane = threadIdx.x & 31;
+    if (t < P.nbm) {
+      const int64_t r_end = (t + 1) * 128 < P.L ? (t + 1) * 128 : P.L;
+      float mx = 0.0f;
+      for (int64_t r = t * 128; r < r_end; r += 4) mx = fmaxf(mx, bt_norm4(P.k, r, r_end));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      if (lane == 0) W.kmax[t] = mx;
+    } else {
+      const int64_t r0 = (t - P.nbm) * 4;
+      const float n = bt_norm4(P.q, r0, P.slots);
+      if ((lane & 7) == 0 && r0 + (lane >> 3) < P.slots) W.qn[r0 + (lane >> 3)] = n;
+    }
+  }
+}
+
+// ------------------------------------------------------------ block maxima --
+// Units are (row tile pair T, key block b), b < nbT[T], T-major; a CTA takes a
+// contiguous range of them (balanced by count), so it reloads its 256 query
+// rows only when T changes.
+struct BtSched {
+  int64_t T0, b0, count;
+};
+
+__device__ void bt_schedule(const BtProblem& P, const BtWs& W, BtSched* out) {
+  const int lane = threadIdx.x & 31;
+  int64_t total = 0;
+  for (int64_t t0 = 0; t0 < P.nT; t0 += 32) {
+    const int64_t t = t0 + lane;
+    int64_t v = t < P.nT ? (int64_t)W.nbT[t] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    total += v;
+  }
+  const int64_t start = total * (int64_t)blockIdx.x / gridDim.x;
+  const int64_t end = total * (int64_t)(blockIdx.x + 1) / gridDim.x;
+  int64_t T0 = 0, b0 = 0;
+  if (end > start) {
+    int64_t run = 0;
+    for (int64_t t0 = 0; t0 < P.nT; t0 += 32) {
+      const int64_t t = t0 + lane;
+      const int64_t v = t < P.nT ? (int64_t)W.nbT[t] : 0;
+      int64_t incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      const int64_t chunk = __shfl_sync(0xffffffffu, incl, 31);
+      if (run + chunk > start) {
+        const unsigned hit = __ballot_sync(0xffffffffu, run + incl > start);
+        const int first = __ffs(hit) - 1;
+        const int64_t incl_f = __shfl_sync(0xffffffffu, incl, first);
+        const int64_t v_f = __shfl_sync(0xffffffffu, v, first);
+        T0 = t0 + first;
+        b0 = start - (run + incl_f - v_f);
+        break;
+      }
+      run += chunk;
+    }
+  }
+  if (lane == 0) {
+    out->T0 = T0;
+    out->b0 = b0;
+    out->count = end - start;
+  }
+}
+
+struct BtUnits {
+  const int32_t* nbT;
+  int64_t T, b, left, nb;
+  __device__ void init(const BtWs& W, const BtSched& s) {
+    nbT = W.nbT;
+    T = s.T0;
+    b = s.b0;
+    left = s.count;
+    nb = left > 0 ? nbT[T] : 0;
+  }
+  __device__ bool valid() const { return left > 0; }
+  __device__ void advance() {
+    --left;
+    if (left <= 0) return;
+    ++b;
+    while (b >= nb) {
+      ++T;
+      b = 0;
+      nb = nbT[T];
+    }
+  }
+};
+
+__device__ __forceinline__ void bt_gather4(void* dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y0,
+                                           int32_t y1, int32_t y2, int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+      "%5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
+constexpr int kBtOffA = 0;
+constexpr int kBtOffK = kBtOffA + 2 * kBtATile;
+constexpr int kBtOffBar = kBtOffK + kBtKStages * kBtChunkBytes;
+constexpr int kBtNBars = 2 + 2 * kBtKStages + 4 + 1;
+constexpr int kBtOffMisc = kBtOffBar + kBtNBars * 8;
+constexpr int kBtSmem = kBtOffMisc + 64 + 1024;
+static_assert(kBtSmem <= 232448, "shared memory");
+
+__global__ void __launch_bounds__(kBtThreads, 1)
+    bt_max_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                  const BtProblem P, const BtWs W) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint8_t* sA = smem + kBtOffA;
+  uint8_t* sK = smem + kBtOffK;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBtOffBar);
+  uint64_t* a_full = bars;
+  uint64_t* a_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_empty = k_full + kBtKStages;
+  uint64_t* acc_full = k_empty + kBtKStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain_bar = acc_empty + 2;
+  uint8_t* misc = smem + kBtOffMisc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  BtSched* sched = reinterpret_cast<BtSched*>(misc + 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(a_full, 1);
+    mbar_init(a_empty, 1);
+    for (int i = 0; i < kBtKStages; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kBtNE);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_q);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kBtTmemCols);
+  if (warp == 2) bt_schedule(P, W, sched);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const BtSched s = *sched;
+  volatile int no_abort_storage = 0;
+  volatile int* no_abort = &no_abort_storage;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    BtUnits u;
+    u.init(W, s);
+    int64_t cur_T = -1;
+    uint32_t na = 0, nk = 0;
+    bool live = true;
+    while (u.valid() && live) {
+      if (u.T != cur_T) {
+        cur_T = u.T;
+        bool ok = true;
+        if (lane == 0) {
+          ok = mbar_wait(a_empty, (na & 1) ^ 1, abort_flag);
+          if (ok) mbar_arrive_expect_tx(a_full, 2 * kBtATile);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        __syncwarp();
+        // lane l: rows 8l .. 8l+7 of the tile pair, four at a time, four K chunks each
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const int r0 = 8 * lane + 4 * g;
+          int32_t y[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int64_t slot = cur_T * kBtRowsT + r0 + i;
+            y[i] = slot < P.slots ? (int32_t)(bt_slot_query(P, W, slot) * P.n_kv + slot % P.n_kv) : 0;
+          }
+          uint8_t* dst = sA + (r0 >> 7) * kBtATile + (r0 & 127) * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) bt_gather4(dst + c * kBtChunkBytes, &tmap_q, a_full, 32 * c, y[0], y[1], y[2], y[3]);
+        }
+        ++na;
+      }
+      for (int c = 0; c < 4; ++c) {
+        const int st = nk % kBtKStages;
+        bool ok = true;
+        if (lane == 0) {
+          ok = mbar_wait(&k_empty[st], ((nk / kBtKStages) & 1) ^ 1, abort_flag);
+          if (ok) {
+            mbar_arrive_expect_tx(&k_full[st], kBtChunkBytes);
+            tma_load_2d(sK + st * kBtChunkBytes, &tmap_k, &k_full[st], 32 * c, (int32_t)(u.b * 128));
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          live = false;
+          break;
+        }
+        ++nk;
+      }
+      __syncwarp();
+      if (live) u.advance();
+    }
+    // drain: the last phase issued on every barrier has landed
+    if (lane == 0) {
+      if (na > 0) mbar_wait(a_full, (na - 1) & 1, no_abort);
+      for (uint32_t i = 0; i < (uint32_t)kBtKStages && i < nk; ++i) {
+        const uint32_t j = nk - 1 - i;
+        mbar_wait(&k_full[j % kBtKStages], (j / kBtKStages) & 1, no_abort);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(128, 128, 2u);   // A, B tf32; D f32
+      BtUnits u;
+      u.init(W, s);
+      int64_t cur_T = -1;
+      uint32_t na = 0, nk = 0, nacc = 0;
+      bool issued = false, ok = true;
+      while (u.valid() && ok) {
+        if (u.T != cur_T) {
+          cur_T = u.T;
+          if (!(ok = mbar_wait(a_full, na & 1, abort_flag))) break;
+          ++na;
+        }
+        const int acc = nacc & 1;
+        if (!(ok = mbar_wait(&acc_empty[acc], ((nacc >> 1) & 1) ^ 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + (uint32_t)(acc * 256);
+        for (int c = 0; c < 4; ++c) {
+          const int st = nk % kBtKStages;
+          if (!(ok = mbar_wait(&k_full[st], (nk / kBtKStages) & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t kb = smem_u32(sK + st * kBtChunkBytes);
+          const uint32_t a0 = smem_u32(sA + c * kBtChunkBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = smem_desc_sw128(kb + kk * 32);
+            const uint32_t accum = (c | kk) ? 1u : 0u;
+            tc_mma_tf32(d0, smem_desc_sw128(a0 + kk * 32), bd, idesc, accum);
+            tc_mma_tf32(d0 + 128, smem_desc_sw128(a0 + kBtATile + kk * 32), bd, idesc, accum);
+          }
+          issued = true;
+          tc_commit(&k_empty[st]);
+          ++nk;
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);
+        ++nacc;
+        const int64_t T_this = u.T;
+        u.advance();
+        if (!u.valid() || u.T != T_this) tc_commit(a_empty);
+      }
+      if (issued) {
+        tc_commit(drain_bar);
+        mbar_wait(drain_bar, 0, no_abort);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int tile = ew >> 2;
+    const int row = tile * 128 + quarter * 32 + lane;
+    BtUnits u;
+    u.init(W, s);
+    int64_t cur_T = -1, slot = 0, vis = 0;
+    uint32_t nacc = 0;
+    const float ninf = -__int_as_float(0x7f800000);
+    while (u.valid()) {
+      if (u.T != cur_T) {
+        cur_T = u.T;
+        slot = cur_T * kBtRowsT + row;
+        vis = 0;
+        if (slot < P.slots) {
+          const int64_t pos = P.qpos[bt_slot_query(P, W, slot)];
+          if (pos >= 0) vis = pos + 1 < P.L ? pos + 1 : P.L;
+        }
+      }
+      const int acc = nacc & 1;
+      const bool got = mbar_wait(&acc_full[acc], (nacc >> 1) & 1, abort_flag);
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      uint32_t v0[32], v1[32], v2[32], v3[32];
+      const uint32_t ta = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * 256 + tile * 128);
+      tmem_ld_32x32b_x32(ta, v0);
+      tmem_ld_32x32b_x32(ta + 32, v1);
+      tmem_ld_32x32b_x32(ta + 64, v2);
+      tmem_ld_32x32b_x32(ta + 96, v3);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      const int64_t nvis = vis - u.b * 128;
+      if (nvis > 0) {
+        float m0 = ninf, m1 = ninf, m2 = ninf, m3 = ninf;
+        if (nvis >= 128) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            m0 = fmaxf(m0, __uint_as_float(v0[i]));
+            m1 = fmaxf(m1, __uint_as_float(v1[i]));
+            m2 = fmaxf(m2, __uint_as_float(v2[i]));
+            m3 = fmaxf(m3, __uint_as_float(v3[i]));
+          }
+        } else {
+          const int nv = (int)nvis;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            m0 = fmaxf(m0, i < nv ? __uint_as_float(v0[i]) : ninf);
+            m1 = fmaxf(m1, i + 32 < nv ? __uint_as_float(v1[i]) : ninf);
+            m2 = fmaxf(m2, i + 64 < nv ? __uint_as_float(v2[i]) : ninf);
+            m3 = fmaxf(m3, i + 96 < nv ? __uint_as_float(v3[i]) : ninf);
+          }
+        }
+        W.amax[slot * P.nbm + u.b] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+      }
+      ++nacc;
+      u.advance();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kBtTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- selection --
+constexpr unsigned kFull = 0xffffffffu;
+
+// The n-th largest (1 <= n <= count) of the keys key(i), i in [i0, i1): four
+// 8-bit radix passes over a per-warp 256-bin histogram.  *need_eq: how many
+// keys equal to the result belong to the top n.
+template <class F>
+__device__ uint32_t bt_warp_kth(const F& key, int64_t i0, int64_t i1, int64_t n, int32_t* hist, int64_t* need_eq) {
+  const int lane = threadIdx.x & 31;
+  uint32_t prefix = 0, pmask = 0;
+  int64_t need = n;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+    for (int64_t i = i0 + lane; i < i1; i += 32) {
+      const uint32_t k = key(i);
+      if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+    }
+    __syncwarp();
+    // lane l holds digits 255 - 8l - j, j < 8 (descending)
+    int c[8], csum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c[j] = hist[255 - 8 * lane - j];
+      csum += c[j];
+    }
+    int incl = csum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(kFull, (int64_t)incl >= need);
+    const int fl = hit ? __ffs(hit) - 1 : 31;
+    int digit = 0, above = 0;
+    if (lane == fl) {
+      int run = incl - csum;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if ((int64_t)(run + c[j]) >= need) {
+          digit = 255 - 8 * lane - j;
+          above = run;
+          break;
+        }
+        run += c[j];
+      }
+    }
+    digit = __shfl_sync(kFull, digit, fl);
+    above = __shfl_sync(kFull, above, fl);
+    prefix |= (uint32_t)digit << shift;
+    pmask |= 255u << shift;
+    need -= above;
+    __syncwarp();
+  }
+  *need_eq = need;
+  return prefix;
+}
+
+// Forced head [0, a), a middle of `mid` entries (written elsewhere) at [a, a+mid),
+// the forced tail zs..n-1 after it, -1 padding; returns the count.
+__device__ __forceinline__ int64_t bt_frame(int32_t* o, int Wd, int64_t a, int64_t mid, int64_t zs, int64_t n) {
+  const int64_t cnt = a + mid + (n - zs);
+  for (int j = threadIdx.x & 31; j < Wd; j += 32) {
+    if (j < a) o[j] = j;
+    else if (j >= a + mid) o[j] = j < cnt ? (int32_t)(zs + (j - a - mid)) : -1;
+  }
+  return cnt;
+}
+
+struct BtSlotGeom {
+  int64_t qi, pair, n, a, zs, n_need;
+  BlockGeom g;
+};
+
+__device__ __forceinline__ BtSlotGeom bt_slot_geom(const BtProblem& P, const BtWs& W, int64_t slot) {
+  BtSlotGeom s;
+  s.qi = bt_slot_query(P, W, slot);
+  s.pair = s.qi * P.n_kv + slot % P.n_kv;
+  s.g = block_geom(P.qpos[s.qi], P.L, P.c);
+  s.n = s.g.n_blocks;
+  s.a = P.c.init_blocks < s.n ? P.c.init_blocks : s.n;
+  s.zs = s.n - P.c.local_blocks;
+  s.zs = s.zs < s.a ? s.a : s.zs;   // non-forced blocks: [a, zs)
+  s.n_need = s.g.budget - s.g.n_forced;
+  return s;
+}
+
+// Lists `slot` for exact rescoring of block b.
+__device__ __forceinline__ void bt_list(const BtProblem& P, const BtWs& W, int64_t slot, int64_t b) {
+  const int p = atomicAdd(&W.icnt[b], 1);
+  W.ilist[b * P.slots + p] = (int32_t)slot;
+}
+
+// counters: pairs scored, blocks bounded, blocks rescored, fallback pairs
+__device__ void bt_classify_slot(const BtProblem& P, const BtWs& W, int64_t slot, int32_t* out, int Wd,
+                                 int32_t* out_count, int32_t* cb, uint32_t* clo, uint32_t* chi, int32_t* hist,
+                                 unsigned long long* cnt) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  const BtSlotGeom s = bt_slot_geom(P, W, slot);
+  int32_t* o = out + s.pair * Wd;
+  int4 st = make_int4(kBtDone, 0, 0, 0);
+  int64_t count = 0;
+  if (s.n == 0 || !s.g.scoring) {
+    count = bt_frame(o, Wd, s.a, 0, s.zs, s.n);
+  } else {
+    const int64_t m = s.zs - s.a;
+    if (lane == 0) {
+      atomicAdd(&cnt[0], 1ull);
+      atomicAdd(&cnt[1], (unsigned long long)m);
+    }
+    if (m <= s.n_need) {
+      // every visible block is selected
+      for (int j = lane; j < Wd; j += 32) o[j] = j < s.n ? j : -1;
+      count = s.n;
+    } else {
+      const float ce = __fmul_ru(kBtErr, W.qn[s.pair]);
+      const float* arow = W.amax + slot * P.nbm;
+      const float* kmax = W.kmax;
+      auto lo_key = [&](int64_t b) { return score_key(__fsub_rd(arow[b], __fmul_ru(ce, kmax[b]))); };
+      int64_t need_eq;
+      const uint32_t T = bt_warp_kth(lo_key, s.a, s.zs, s.n_need, hist, &need_eq);
+      // candidates: upper bound >= T, ascending
+      int nc = 0;
+      for (int64_t b0 = s.a; b0 < s.zs; b0 += 32) {
+        const int64_t b = b0 + lane;
+        bool c = false;
+        uint32_t lk = 0, hk = 0;
+        if (b < s.zs) {
+          const float A = arow[b], e = __fmul_ru(ce, kmax[b]);
+          lk = score_key(__fsub_rd(A, e));
+          hk = score_key(__fadd_ru(A, e));
+          c = hk >= T;
+        }
+        const unsigned bal = __ballot_sync(kFull, c);
+        if (c) {
+          const int p = nc + __popc(bal & lt);
+          if (p < kBtCapC) {
+            cb[p] = (int32_t)b;
+            clo[p] = lk;
+            chi[p] = hk;
+          }
+        }
+        nc += __popc(bal);
+      }
+      __syncwarp();
+      bool fallback = nc > kBtCapC;
+      if (!fallback) {
+        // certainly in: fewer than n_need other candidates reach its lower bound
+        int k_in = 0;
+        for (int i0 = 0; i0 < nc; i0 += 32) {
+          const int i = i0 + lane;
+          bool in = false;
+          if (i < nc) {
+            const uint32_t li = clo[i];
+            int c = 0;
+            for (int j = 0; j < nc; ++j) c += (j != i && chi[j] >= li) ? 1 : 0;
+            in = c < s.n_need;
+          }
+          if (in) cb[i] |= (int32_t)0x80000000;
+          k_in += __popc(__ballot_sync(kFull, in));
+        }
+        __syncwarp();
+        const int nu = nc - k_in;
+        const int64_t m_need = s.n_need - k_in;
+        if (m_need == 0 || nu == m_need) {
+          // decided: the certain ones (m_need == 0) or every candidate
+          const bool all = m_need != 0;
+          int w = 0;
+          for (int i0 = 0; i0 < nc; i0 += 32) {
+            const int i = i0 + lane;
+            const bool sel = i < nc && (all || cb[i] < 0);
+            const unsigned bal = __ballot_sync(kFull, sel);
+            if (sel) o[s.a + w + __popc(bal & lt)] = cb[i] & 0x7fffffff;
+            w += __popc(bal);
+          }
+          count = bt_frame(o, Wd, s.a, s.n_need, s.zs, s.n);
+        } else if (nu > kBtCapU) {
+          fallback = true;
+        } else {
+          // certain ones to o[a, a + k_in); undecided ones to the pair's list and the blocks' lists
+          int wi = 0, wu = 0;
+          for (int i0 = 0; i0 < nc; i0 += 32) {
+            const int i = i0 + lane;
+            const bool valid = i < nc;
+            const bool in = valid && cb[i] < 0;
+            const bool un = valid && !in;
+            const unsigned bin = __ballot_sync(kFull, in), bun = __ballot_sync(kFull, un);
+            if (in) o[s.a + wi + __popc(bin & lt)] = cb[i] & 0x7fffffff;
+            if (un) {
+              const int b = cb[i];
+              W.ulist[slot * kBtCapU + wu + __popc(bun & lt)] = b;
+              bt_list(P, W, slot, b);
+            }
+            wi += __popc(bin);
+            wu += __popc(bun);
+          }
+          st = make_int4(kBtList, k_in, nu, (int)m_need);
+          if (lane == 0) atomicAdd(&cnt[2], (unsigned long long)nu);
+        }
+      }
+      if (fallback) {
+        for (int64_t b = s.a + lane; b < s.zs; b += 32) bt_list(P, W, slot, b);
+        st = make_int4(kBtFallback, 0, (int)m, (int)s.n_need);
+        if (lane == 0) {
+          atomicAdd(&cnt[2], (unsigned long long)m);
+          atomicAdd(&cnt[3], 1ull);
+        }
+      }
+    }
+  }
+  if (lane == 0) {
+    W.sstat[slot] = st;
+    if (st.x == kBtDone && out_count) out_count[s.pair] = (int32_t)count;
+  }
+}
+
+constexpr int kBtWarps = 8;   // pairs per CTA in the per-pair kernels
+
+__global__ void __launch_bounds__(32 * kBtWarps) bt_classify_kernel(BtProblem P, BtWs W, int32_t* out, int Wd,
+                                                                      int32_t* out_count, block_select_stats* stats) {
+  __shared__ int32_t s_b[kBtWarps][kBtCapC];
+  __shared__ uint32_t s_lo[kBtWarps][kBtCapC];
+  __shared__ uint32_t s_hi[kBtWarps][kBtCapC];
+  __shared__ int32_t s_hist[kBtWarps][256];
+  __shared__ unsigned long long s_cnt[4];
+  if (threadIdx.x < 4) s_cnt[threadIdx.x] = 0;
+  __syncthreads();
+  const int wi = threadIdx.x >> 5;
+  const int64_t slot = (int64_t)blockIdx.x * kBtWarps + wi;
+  if (slot < P.slots) bt_classify_slot(P, W, slot, out, Wd, out_count, s_b[wi], s_lo[wi], s_hi[wi], s_hist[wi], s_cnt);
+  __syncthreads();
+  if (stats && threadIdx.x < 4 && s_cnt[threadIdx.x])
+    atomicAdd(&stats->pairs + threadIdx.x, s_cnt[threadIdx.x]);
+}
+
+// ------------------------------------------------------------ exact scores --
+constexpr int kBtExactThreads = 256;
+constexpr int kBtExactSmem = (128 * 128 + (kBtExactThreads / 32) * 128 * 2) * 4;
+
+// One CTA per key block: its keys staged transposed ([d][key]), then each warp
+// takes two listed pairs at a time; lane l runs the page's chains of keys
+// 4l..4l+3 for both (packed: two keys of one pair per instruction).  The exact
+// block score replaces A_b in the pair's row as an ordered key.
+__global__ void __launch_bounds__(kBtExactThreads) bt_exact_kernel(BtProblem P, BtWs W, block_select_stats* stats) {
+  extern __shared__ __align__(16) float kt[];
+  __shared__ float s_worst;
+  const int64_t b = blockIdx.x;
+  const int cnt = W.icnt[b];
+  if (cnt == 0) return;
+  const int t = threadIdx.x, wi = t >> 5, lane = t & 31;
+  const int64_t k0 = b * 128;
+  const int nk = (int)(P.L - k0 < 128 ? P.L - k0 : 128);
+  {
+    const float4* src = reinterpret_cast<const float4*>(P.k + k0 * 128);
+    for (int i = t; i < nk * 32; i += kBtExactThreads) {
+      const int key = i % nk, d4 = i / nk;
+      const float4 v = __ldg(src + key * 32 + d4);
+      kt[(4 * d4 + 0) * 128 + key] = v.x;
+      kt[(4 * d4 + 1) * 128 + key] = v.y;
+      kt[(4 * d4 + 2) * 128 + key] = v.z;
+      kt[(4 * d4 + 3) * 128 + key] = v.w;
+    }
+  }
+  if (t == 0) s_worst = 0.0f;
+  __syncthreads();
+  float2* qs = reinterpret_cast<float2*>(kt + 128 * 128) + wi * 128;
+  const float km = W.kmax[b];
+  const float ninf = -__int_as_float(0x7f800000);
+  float worst = 0.0f;
+  const int32_t* items = W.ilist + b * P.slots;
+  for (int ip = wi; 2 * ip < cnt; ip += kBtExactThreads / 32) {
+    const int i0 = 2 * ip;
+    const bool two = i0 + 1 < cnt;
+    const int64_t s0 = items[i0], s1 = two ? items[i0 + 1] : s0;
+    const int64_t q0 = bt_slot_query(P, W, s0), q1 = bt_slot_query(P, W, s1);
+    const int64_t p0 = q0 * P.n_kv + s0 % P.n_kv, p1 = q1 * P.n_kv + s1 % P.n_kv;
+    {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(P.q + p0 * 128) + lane);
+      const float4 y = __ldg(reinterpret_cast<const float4*>(P.q + p1 * 128) + lane);
+      qs[4 * lane + 0] = make_float2(x.x, y.x);
+      qs[4 * lane + 1] = make_float2(x.y, y.y);
+      qs[4 * lane + 2] = make_float2(x.z, y.z);
+      qs[4 * lane + 3] = make_float2(x.w, y.w);
+    }
+    __syncwarp();
+    uint64_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;   // pair 0: keys (4l, 4l+1), (4l+2, 4l+3); pair 1: same
+#pragma unroll 8
+    for (int d = 0; d < 128; ++d) {
+      const float4 kv = *reinterpret_cast<const float4*>(kt + d * 128 + 4 * lane);
+      const float2 qq = qs[d];
+      const uint64_t k01 = f2_pack(kv.x, kv.y), k23 = f2_pack(kv.z, kv.w);
+      const uint64_t x0 = f2_pack(qq.x, qq.x), x1 = f2_pack(qq.y, qq.y);
+      c0 = f2_add(c0, f2_mul(x0, k01));
+      c1 = f2_add(c1, f2_mul(x0, k23));
+      c2 = f2_add(c2, f2_mul(x1, k01));
+      c3 = f2_add(c3, f2_mul(x1, k23));
+    }
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      if (it == 1 && !two) break;
+      const int64_t sl = it ? s1 : s0, qi = it ? q1 : q0, pr = it ? p1 : p0;
+      int64_t vis = (int64_t)P.qpos[qi] + 1;
+      vis = vis < P.L ? vis : P.L;
+      const int nv = (int)(vis - k0);
+      float e[4];
+      f2_unpack(it ? c2 : c0, &e[0], &e[1]);
+      f2_unpack(it ? c3 : c1, &e[2], &e[3]);
+      float mx = ninf;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (4 * lane + j < nv) mx = fmaxf(mx, __fadd_rn(e[j], 0.0f));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      if (lane == 0) {
+        uint32_t* cell = reinterpret_cast<uint32_t*>(W.amax) + sl * P.nbm + b;
+        const float A = __uint_as_float(*cell);
+        const float eb = __fmul_ru(__fmul_ru(kBtErr, W.qn[pr]), km);
+        if (eb > 0.0f) worst = fmaxf(worst, fabsf(A - mx) / eb);
+        *cell = score_key(mx);
+      }
+    }
+    __syncwarp();
+  }
+  if (lane == 0 && worst > 0.0f) atomicMax(reinterpret_cast<int*>(&s_worst), __float_as_int(worst));
+  __syncthreads();
+  if (t == 0 && stats && s_worst > 0.0f)
+    atomicMax(reinterpret_cast<int*>(&stats->max_bound_use), __float_as_int(s_worst));
+}
+
+// ---------------------------------------------------------------- resolve --
+__device__ __forceinline__ int bt_count_below(const int32_t* v, int n, int32_t x) {
+  int lo = 0, hi = n;   // first index with v[i] >= x (v ascending)
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (v[mid] < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(32 * kBtWarps) bt_resolve_kernel(BtProblem P, BtWs W, int32_t* out, int Wd,
+                                                                     int32_t* out_count) {
+  __shared__ uint32_t s_key[kBtWarps][kBtCapU];
+  __shared__ int32_t s_blk[kBtWarps][kBtCapU];
+  __shared__ int32_t s_win[kBtWarps][kBtCapU];
+  __shared__ int32_t s_in[kBtWarps][kBtMaxTop];
+  __shared__ int32_t s_hist[kBtWarps][256];
+  const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  const int64_t slot = (int64_t)blockIdx.x * kBtWarps + wi;
+  if (slot >= P.slots) return;
+  const int4 st = W.sstat[slot];
+  if (st.x == kBtDone) return;
+  const BtSlotGeom s = bt_slot_geom(P, W, slot);
+  const uint32_t* keys = reinterpret_cast<const uint32_t*>(W.amax) + slot * P.nbm;
+  int32_t* o = out + s.pair * Wd;
+  if (st.x == kBtList) {
+    const int k_in = st.y, nu = st.z, m_need = st.w;
+    uint32_t* sk = s_key[wi];
+    int32_t* sb = s_blk[wi];
+    int32_t* sw = s_win[wi];
+    int32_t* si = s_in[wi];
+    for (int i = lane; i < nu; i += 32) {
+      const int32_t b = W.ulist[slot * kBtCapU + i];
+      sb[i] = b;
+      sk[i] = keys[b];
+    }
+    for (int i = lane; i < k_in; i += 32) si[i] = o[s.a + i];
+    __syncwarp();
+    // winners: rank < m_need by (exact key desc, block asc); kept ascending
+    int w = 0;
+    for (int i0 = 0; i0 < nu; i0 += 32) {
+      const int i = i0 + lane;
+      bool win = false;
+      if (i < nu) {
+        const uint32_t ki = sk[i];
+        const int32_t bi = sb[i];
+        int r = 0;
+        for (int j = 0; j < nu; ++j) r += (sk[j] > ki || (sk[j] == ki && sb[j] < bi)) ? 1 : 0;
+        win = r < m_need;
+      }
+      const unsigned bal = __ballot_sync(kFull, win);
+      if (win) sw[w + __popc(bal & lt)] = sb[i];
+      w += __popc(bal);
+    }
+    __syncwarp();
+    // merge the two ascending, disjoint lists into o[a, a + n_need)
+    for (int i = lane; i < k_in; i += 32) o[s.a + i + bt_count_below(sw, m_need, si[i])] = si[i];
+    for (int i = lane; i < m_need; i += 32) o[s.a + i + bt_count_below(si, k_in, sw[i])] = sw[i];
+  } else {
+    // every non-forced block was rescored: the top n_need of [a, zs)
+    int64_t need_eq;
+    auto key = [&](int64_t b) { return keys[b]; };
+    const uint32_t K = bt_warp_kth(key, s.a, s.zs, s.n_need, s_hist[wi], &need_eq);
+    int64_t w = 0, eq_seen = 0;
+    for (int64_t b0 = s.a; b0 < s.zs; b0 += 32) {
+      const int64_t b = b0 + lane;
+      const uint32_t k = b < s.zs ? keys[b] : 0u;
+      const bool eq = b < s.zs && k == K;
+      const unsigned beq = __ballot_sync(kFull, eq);
+      const bool sel = (b < s.zs && k > K) || (eq && eq_seen + __popc(beq & lt) < need_eq);
+      const unsigned bal = __ballot_sync(kFull, sel);
+      if (sel) o[s.a + w + __popc(bal & lt)] = (int32_t)b;
+      w += __popc(bal);
+      eq_seen += __popc(beq);
+    }
+  }
+  const int64_t count = bt_frame(o, Wd, s.a, s.n_need, s.zs, s.n);
+  if (lane == 0 && out_count) out_count[s.pair] = (int32_t)count;
+}
+
+// ---------------------------------------------------------------- launcher --
+static BtProblem bt_problem(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv, int64_t L,
+                            const block_sparse_config& c) {
+  BtProblem P;
+  P.q = q;
+  P.k = k;
+  P.qpos = pos;
+  P.Q = Q;
+  P.n_kv = n_kv;
+  P.L = L;
+  P.slots = Q * n_kv;
+  P.nbm = (L + 127) / 128;
+  P.nT = (P.slots + kBtRowsT - 1) / kBtRowsT;
+  P.c = c;
+  return P;
+}
+
+bool block_select_tc_applies(int D, const block_sparse_config& c, int64_t Q, int n_kv, int64_t L) {
+  return D == 128 && c.block_size == 128 && c.top_blocks <= kBtMaxTop && n_kv > 0 &&
+         Q * (int64_t)n_kv < ((int64_t)1 << 31) && L < ((int64_t)1 << 31) &&
+         ((L + 127) / 128) * Q * (int64_t)n_kv < ((int64_t)1 << 40);
+}
+
+size_t block_select_tc_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c) {
+  return bt_ws_bytes(bt_problem(nullptr, nullptr, nullptr, Q, n_kv, L, c));
+}
+
+cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv,
+                                   int64_t L, const block_sparse_config& c, int32_t* out, int out_width,
+                                   int32_t* out_count, void* ws, block_select_stats* stats, cudaStream_t st) {
+  const BtProblem P = bt_problem(q, k, pos, Q, n_kv, L, c);
+  if (P.slots <= 0) return cudaSuccess;
+  const BtWs W = bt_carve(ws, P);
+  cudaError_t e;
+  {
+    const int64_t tasks = P.nbm + (P.slots + 3) / 4;
+    int64_t g = (tasks + 7) / 8;
+    const int64_t gmax = 8 * (int64_t)sm_count();
+    g = g < gmax ? g : gmax;
+    bt_prep_kernel<<<(unsigned)(1 + g), kBtPrepThreads, 0, st>>>(P, W);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (P.nbm > 0) {
+    CUtensorMap tk, tq;
+    bool ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, k, 128, (uint64_t)L, 512, 32, 128);
+    ok = ok && make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q, 128, (uint64_t)P.slots, 512, 32, 1);
+    if (!ok) return cudaErrorInvalidValue;
+    if ((e = cudaFuncSetAttribute(bt_max_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBtSmem)) !=
+        cudaSuccess)
+      return e;
+    bt_max_kernel<<<sm_count(), kBtThreads, kBtSmem, st>>>(tk, tq, P, W);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const unsigned gp = (unsigned)((P.slots + kBtWarps - 1) / kBtWarps);
+  bt_classify_kernel<<<gp, 32 * kBtWarps, 0, st>>>(P, W, out, out_width, out_count, stats);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (P.nbm > 0) {
+    if ((e = cudaFuncSetAttribute(bt_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBtExactSmem)) !=
+        cudaSuccess)
+      return e;
+    bt_exact_kernel<<<(unsigned)P.nbm, kBtExactThreads, kBtExactSmem, st>>>(P, W, stats);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  bt_resolve_kernel<<<gp, 32 * kBtWarps, 0, st>>>(P, W, out, out_width, out_count);
+  return cudaGetLastError();
+}
+
+}  // namespace idx

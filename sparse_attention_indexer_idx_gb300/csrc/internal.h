@@ -66,9 +66,17 @@ cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const floa
                          int64_t cap, int32_t* status, int R, const int32_t* row_mask, cudaStream_t st);
 
 size_t block_select_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c);
+// tensor_route: allow the tensor-core route (block_tc.cu) when it applies; ws
+// must then hold block_select_ws() bytes, which covers both routes.
 cudaError_t launch_block_select(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv, int D,
                                 int64_t L, const block_sparse_config& c, int32_t* out, int out_width,
-                                int32_t* out_count, void* ws, cudaStream_t st);
+                                int32_t* out_count, void* ws, cudaStream_t st, block_select_stats* stats,
+                                bool tensor_route);
+bool block_select_tc_applies(int D, const block_sparse_config& c, int64_t Q, int n_kv, int64_t L);
+size_t block_select_tc_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c);
+cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv,
+                                   int64_t L, const block_sparse_config& c, int32_t* out, int out_width,
+                                   int32_t* out_count, void* ws, block_select_stats* stats, cudaStream_t st);
 
 size_t dosa_ws(const idx_problem& p, int K, const dosa_params& dp, int seed_ld);
 cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, const int32_t* seed_ids, int seed_ld,

@@ -1,0 +1,152 @@
+"""GPU parity of the tensor-core block-selection route (block size 128, D = 128):
+bit-exact block indices against the oracle and against the CUDA-core route
+(block_select_static computes every block score in the page's order), on
+shapes that span several 256-row tiles with ragged tails, unsorted positions,
+exact ties between blocks, queries whose bounds decide nothing (every block
+rescored), and the certified-bound statistics."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import block_select as obs
+from sparse_attention_indexer_idx_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from sparse_attention_indexer_idx_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _run(B, q, k, pos, top, init, local, static=False, stats=None):
+    Q, n_kv, D = q.shape
+    L = k.shape[0]
+    cfg = B.block_sparse_config(128, top, init, local)
+    W = max(top, init + local, 1)
+    out = torch.full((Q, n_kv, W), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((Q, n_kv), -7, dtype=torch.int32, device="cuda")
+    qd = torch.from_numpy(np.ascontiguousarray(q, dtype=np.float32)).cuda()
+    kd = torch.from_numpy(np.ascontiguousarray(k, dtype=np.float32)).cuda()
+    pd = torch.from_numpy(np.asarray(pos, dtype=np.int32)).cuda()
+    if static:
+        B.block_select_static(qd, kd, pd, cfg, out, cnt)
+    else:
+        ws = torch.empty(max(1, B.block_select_workspace_size(Q, n_kv, max(L, 1), cfg)), dtype=torch.uint8,
+                         device="cuda")
+        B.block_select(qd, kd, pd, cfg, out, cnt, ws, stats=stats)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), cnt.cpu().numpy()
+
+
+def _lists(o, c):
+    Q, n_kv, _ = o.shape
+    res = []
+    for i in range(Q):
+        row = []
+        for h in range(n_kv):
+            assert (o[i, h, c[i, h]:] == -1).all()
+            row.append(o[i, h, :c[i, h]].tolist())
+        res.append(row)
+    return res
+
+
+def _check_oracle(got, q, k, pos, top, init, local, queries):
+    for i in queries:
+        ref = obs.block_sparse_select(q[i], k, int(pos[i]), 128, top, init, local)
+        assert got[i] == ref, i
+
+
+@pytest.mark.parametrize("seed,Q,n_kv,L,top,init,local", [
+    (11, 70, 5, 5000, 12, 2, 1),       # 350 rows: two tiles, the second ragged; L not a multiple of 128
+    (12, 40, 8, 20000, 32, 1, 2),      # the MiniMax configuration, short context
+    (13, 1, 1, 9000, 4, 0, 0),         # one row
+    (14, 33, 3, 30000, 200, 0, 0),     # a large budget: many certain blocks, long candidate lists
+    (15, 25, 7, 16384, 512, 1, 1),     # the largest budget of the route
+])
+def test_tc_route_against_oracle(B, seed, Q, n_kv, L, top, init, local):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((Q, n_kv, 128)).astype(np.float32)
+    k = rng.standard_normal((L, 128)).astype(np.float32)
+    pos = rng.integers(0, L + 300, Q).astype(np.int32)   # unsorted, some past the end
+    pos[0] = min(5, L - 1)
+    o, c = _run(B, q, k, pos, top, init, local)
+    got = _lists(o, c)
+    _check_oracle(got, q, k, pos, top, init, local, range(Q))
+    o2, c2 = _run(B, q, k, pos, top, init, local, static=True)
+    assert np.array_equal(o, o2) and np.array_equal(c, c2)
+    assert B.device_error() == 0
+
+
+def test_tc_route_exact_ties(B):
+    """Duplicated key rows make whole blocks tie on their maxima; the order
+    (score desc, block asc) must still come out bit for bit."""
+    rng = np.random.default_rng(21)
+    Q, n_kv, L = 48, 4, 24000
+    q = rng.standard_normal((Q, n_kv, 128)).astype(np.float32)
+    k = rng.standard_normal((L, 128)).astype(np.float32)
+    src = k[:128].copy()
+    for b in rng.choice(L // 128, 40, replace=False):   # 40 blocks identical to block 0
+        k[b * 128:(b + 1) * 128] = src
+    k[rng.integers(0, L, L // 10)] = k[7]                # scattered duplicate rows
+    pos = rng.integers(200, L, Q).astype(np.int32)
+    o, c = _run(B, q, k, pos, 32, 1, 2)
+    got = _lists(o, c)
+    _check_oracle(got, q, k, pos, 32, 1, 2, range(0, Q, 3))
+    o2, c2 = _run(B, q, k, pos, 32, 1, 2, static=True)
+    assert np.array_equal(o, o2) and np.array_equal(c, c2)
+
+
+def test_tc_route_undecided_pairs(B):
+    """Zero queries (every block scores 0: nothing is decided by the bounds) and
+    a context made of one repeated block (all maxima equal) send pairs down the
+    path that rescores every non-forced block."""
+    rng = np.random.default_rng(22)
+    Q, n_kv, L = 12, 4, 40000
+    q = rng.standard_normal((Q, n_kv, 128)).astype(np.float32)
+    q[::3] = 0.0
+    k = rng.standard_normal((L, 128)).astype(np.float32)
+    pos = np.linspace(1000, L - 1, Q).astype(np.int32)
+    st = B.block_select_stats_tensor()
+    o, c = _run(B, q, k, pos, 32, 1, 2, stats=st)
+    got = _lists(o, c)
+    _check_oracle(got, q, k, pos, 32, 1, 2, range(Q))
+    s = B.block_select_stats_read(st)
+    assert s["fallback_pairs"] >= 3 * n_kv      # zero queries past the first (8 blocks: nothing to score)
+    kr = np.tile(rng.standard_normal((128, 128)).astype(np.float32), (L // 128 + 1, 1))[:L]
+    o, c = _run(B, q, kr, pos, 32, 1, 2)
+    got = _lists(o, c)
+    _check_oracle(got, q, kr, pos, 32, 1, 2, range(0, Q, 2))
+
+
+def test_tc_route_matches_core_route_many_queries(B):
+    """1000 random queries (unsorted) x 8 heads over 50000 keys: the two routes agree."""
+    rng = np.random.default_rng(23)
+    Q, n_kv, L = 1000, 8, 50000
+    q = rng.standard_normal((Q, n_kv, 128)).astype(np.float32)
+    k = rng.standard_normal((L, 128)).astype(np.float32)
+    pos = rng.integers(0, L, Q).astype(np.int32)
+    o, c = _run(B, q, k, pos, 32, 1, 2)
+    o2, c2 = _run(B, q, k, pos, 32, 1, 2, static=True)
+    assert np.array_equal(c, c2)
+    assert np.array_equal(o, o2)
+
+
+def test_tc_route_workload_stats(B):
+    """The MiniMax workload: bounded blocks, few rescored, none undecided, and
+    the measured error well inside the certified bound."""
+    bp = wl.block_select()
+    st = B.block_select_stats_tensor()
+    o, c = _run(B, bp.index_q, bp.index_k, bp.query_pos, bp.top_blocks, bp.init_blocks, bp.local_blocks, stats=st)
+    s = B.block_select_stats_read(st)
+    assert s["pairs"] > 0 and s["fallback_pairs"] == 0
+    assert s["blocks_rescored"] < 0.05 * s["blocks_bounded"]
+    assert 0.0 < s["max_bound_use"] < 0.5
+    got = _lists(o, c)
+    _check_oracle(got, bp.index_q, bp.index_k, bp.query_pos, bp.top_blocks, bp.init_blocks, bp.local_blocks,
+                  [3, 300, 777, 1023])
+    o2, c2 = _run(B, bp.index_q, bp.index_k, bp.query_pos, bp.top_blocks, bp.init_blocks, bp.local_blocks,
+                  static=True)
+    assert np.array_equal(o, o2) and np.array_equal(c, c2)
