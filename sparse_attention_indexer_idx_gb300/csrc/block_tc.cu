@@ -14,13 +14,17 @@
 //
 //  1. bt_prep_kernel: queries ordered by their number of visible blocks (a
 //     counting sort; a tile of 32 queries then scans about as many blocks as
-//     each of its queries needs); an upper bound of ||q|| per (query, head)
-//     and of max ||k_p|| per block.
+//     each of its queries needs); every query row and every key block written
+//     as fp16 under a power-of-two scale (sigma per row, s_b per block, so
+//     that the largest magnitude sits in [2^14, 2^15): 11 significant bits,
+//     as many as tf32, at half the bytes and twice the tensor rate); the
+//     norm factors of the bound.
 //  2. bt_max_kernel: A_b over every visible block of every pair, on
-//     tcgen05.mma kind::tf32.  A CTA holds 256 (query, head) rows (two M = 128
+//     tcgen05.mma kind::f16.  A CTA holds 256 (query, head) rows (two M = 128
 //     tiles, fetched by TMA gather4 in the sorted order) and streams key
-//     blocks (128 keys = N, four 32-float K chunks, one TMA box each) through a
-//     six-stage ring; each key chunk feeds eight MMAs (K = 8, both tiles).  The
+//     blocks (128 keys = N, two 64-element K chunks, one TMA box each) through
+//     a ten-stage ring; each key chunk feeds eight MMAs (K = 16, both tiles).
+//     A_b = sigma s_b max(acc) (exact power-of-two scaling).  The
 //     accumulators (two stages of 2 x 128 TMEM columns) are reduced by eight
 //     epilogue warps: a thread owns one (query, head) row, so the block max is
 //     a max over its own 128 columns (positions past the query's position or
@@ -40,15 +44,20 @@
 //     blocks has every non-forced block rescored and takes its whole top list
 //     here.
 //
-// The bound.  The tensor core reads an fp32 operand as tf32 (its top 19 bits),
-// an error below 2^-10 relative per operand; products of tf32 values are exact
-// in fp32, and the fp32 accumulation of 128 products (16 MMAs of K = 8) and the
-// page's own sequential sum each stay well inside 2^-14 of sum |q_d k_d|.  So
-// |A_p - E_p| <= (2^-9 + 2^-12) ||q|| ||k_p|| for every position p, and the
-// same holds for the block maxima.  ||q|| and max ||k_p|| are rounded up.
-// bt_exact_kernel measures |A_b - E_b| / e_b on every block it rescores and
-// reports the largest value through block_select_stats.
+// The bound.  The tensor core multiplies exactly q~ = sigma fp16(q / sigma)
+// and k~ = s_b fp16(k / s_b) (values this code rounded, so dq = q - q~ and
+// dk = k - k~ are known exactly); products of fp16 values are exact in fp32.
+// With E_p = q.k_p in the page's order and A_p the tensor-core value,
+//   |A_p - E_p| <= |q~.dk| + |dq.k| + (accumulation and page-order sum)
+//              <= ||q~|| ||dk_p|| + ||dq|| ||k_p|| + 2^-12 ||q|| ||k_p||,
+// the last term a wide allowance (16x) over fp32 accumulation of 128 products
+// in 8 MMAs of K = 16 plus the page's sequential sum, plus 2^-118 for products
+// below the normal range.  Per block the key factors are their maxima over
+// its positions; every factor is rounded up.  The same bound holds for the
+// block maxima.  bt_exact_kernel measures |A_b - E_b| / e_b on every block it
+// rescores and reports the largest value through block_select_stats.
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include "block_select.cuh"
 
@@ -57,11 +66,12 @@ namespace idx {
 bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
 
-constexpr float kBtErr = 0.001953125f + 0.000244140625f;   // 2^-9 + 2^-12
+constexpr float kBtGamma = 0.000244140625f;        // 2^-12: accumulation and page-order sum allowance
+constexpr float kBtAbs = 3.00926553e-36f;           // 2^-118: products below the normal range
 constexpr int kBtRowsT = 256;        // (query, head) rows per CTA tile: two MMA tiles of 128
-constexpr int kBtKStages = 6;        // key-chunk ring
-constexpr int kBtChunkBytes = 128 * 128;   // 128 keys x 32 floats
-constexpr int kBtATile = 4 * kBtChunkBytes;   // 128 rows x 128 floats
+constexpr int kBtKStages = 10;       // key-chunk ring
+constexpr int kBtChunkBytes = 128 * 128;   // 128 rows x 64 fp16 (one 128-byte swizzle span)
+constexpr int kBtATile = 2 * kBtChunkBytes;   // 128 rows x 128 fp16
 constexpr int kBtNE = 8;             // epilogue warps
 constexpr int kBtThreads = 32 * (2 + kBtNE);
 constexpr int kBtTmemCols = 512;     // two stages x two tiles x 128 keys
@@ -76,8 +86,12 @@ enum BtStatus { kBtDone = 0, kBtList = 1, kBtFallback = 2 };
 struct BtWs {
   int32_t* order;      // [Q] query rank -> query
   int32_t* nbT;        // [nT] blocks scanned by row tile pair T
-  float* qn;           // [Q*n_kv] upper bound of ||q|| (original pair order)
-  float* kmax;         // [nbm] upper bound of max ||k_p|| over the block
+  __half* q16;         // [Q*n_kv, 128] q / sigma as fp16 (original pair order)
+  float* qsig;         // [Q*n_kv] sigma: power-of-two row scale
+  float2* qab;         // [Q*n_kv] bound factors (||dq|| + 2^-12 (||q~|| + ||dq||), ||q~||), rounded up
+  __half* k16;         // [L, 128] k / s_b as fp16
+  float* ksc;          // [nbm] s_b: power-of-two block scale
+  float2* kb;          // [nbm] (max ||k_p||, max ||k_p - k~_p||) over the block, rounded up
   float* amax;         // [slots, nbm] A_b (float), overwritten by the exact ordered key when rescored
   int32_t* icnt;       // [nbm] listed pairs per block
   int32_t* ilist;      // [nbm, slots] slots listed per block
@@ -105,8 +119,12 @@ static BtWs bt_carve(void* base, const BtProblem& P) {
   BtWs s;
   s.order = w.take<int32_t>((size_t)P.Q);
   s.nbT = w.take<int32_t>((size_t)P.nT);
-  s.qn = w.take<float>((size_t)P.slots);
-  s.kmax = w.take<float>((size_t)P.nbm);
+  s.q16 = w.take<__half>((size_t)P.slots * 128);
+  s.qsig = w.take<float>((size_t)P.slots);
+  s.qab = w.take<float2>((size_t)P.slots);
+  s.k16 = w.take<__half>((size_t)P.L * 128);
+  s.ksc = w.take<float>((size_t)P.nbm);
+  s.kb = w.take<float2>((size_t)P.nbm);
   s.amax = w.take<float>((size_t)(P.slots * P.nbm));
   s.icnt = w.take<int32_t>((size_t)P.nbm);
   s.ilist = w.take<int32_t>((size_t)(P.nbm * P.slots));
@@ -119,8 +137,12 @@ static size_t bt_ws_bytes(const BtProblem& P) {
   WsCarver w(nullptr);
   w.take<int32_t>((size_t)P.Q);
   w.take<int32_t>((size_t)P.nT);
+  w.take<__half>((size_t)P.slots * 128);
   w.take<float>((size_t)P.slots);
+  w.take<float2>((size_t)P.slots);
+  w.take<__half>((size_t)P.L * 128);
   w.take<float>((size_t)P.nbm);
+  w.take<float2>((size_t)P.nbm);
   w.take<float>((size_t)(P.slots * P.nbm));
   w.take<int32_t>((size_t)P.nbm);
   w.take<int32_t>((size_t)(P.nbm * P.slots));
@@ -138,36 +160,157 @@ __device__ __forceinline__ int64_t bt_slot_query(const BtProblem& P, const BtWs&
   return (int64_t)W.order[slot / P.n_kv];
 }
 
-// Upper bound of the Euclidean norm of four 128-float rows r0..r0+3 (rows past
-// `rows` give 0): lanes 8g..8g+7 read row r0 + g, 16 floats each.
-__device__ __forceinline__ float bt_norm4(const float* base, int64_t r0, int64_t rows) {
-  const int lane = threadIdx.x & 31;
-  const int64_t r = r0 + (lane >> 3);
-  float ss = 0.0f;
-  if (r < rows) {
-    const float4* p = reinterpret_cast<const float4*>(base + r * 128) + (lane & 7) * 4;
+// sqrt of a sum of 128 squares accumulated in fp32 (relative error < 2^-16),
+// rounded up with 2^-14 on top: an upper bound of the exact norm.
+__device__ __forceinline__ float bt_norm_up(float ss) { return __fmul_ru(__fsqrt_ru(ss), 1.00006103515625f); }
+
+// Sum / max over the 8 lanes of a row group (lanes 8g..8g+7).
+__device__ __forceinline__ float bt_sum8(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  return v;
+}
+__device__ __forceinline__ float bt_max8(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  return v;
+}
+
+// Power-of-two scale s of a row or block with largest magnitude amax: amax / s
+// in [2^14, 2^15), so x / s is an fp16 value with 11 significant bits for every
+// element within a factor 2^14 of amax and never overflows; s >= 2^-100 keeps
+// every s * fp16 value an exact fp32 number.
+__device__ __forceinline__ float bt_scale(float amax) {
+  if (!(amax > 0.0f)) return 1.0f;
+  int ex;
+  frexpf(amax, &ex);   // amax = f 2^ex, f in [0.5, 1)
+  return ldexpf(1.0f, ex - 15 > -100 ? ex - 15 : -100);
+}
+
+// 16 floats -> 16 fp16 values of x / s (round to nearest even), stored to dst
+// (32-byte aligned) when `store`;
+// accumulates sum x~^2 and sum (x - x~)^2 with x~ = s * fp16(x / s) (both exact
+// in fp32: a power-of-two scaling and a difference of neighbours).
+__device__ __forceinline__ void bt_to_f16(const float4 (&v)[4], float s, float inv, __half* dst, bool store,
+                                          float& st, float& sd) {
+  uint32_t w[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 v = __ldg(p + i);
-      ss = __fmaf_rn(v.x, v.x, ss);
-      ss = __fmaf_rn(v.y, v.y, ss);
-      ss = __fmaf_rn(v.z, v.z, ss);
-      ss = __fmaf_rn(v.w, v.w, ss);
+  for (int i = 0; i < 4; ++i) {
+    const float x[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; j += 2) {
+      const __half2 h = __floats2half2_rn(x[j] * inv, x[j + 1] * inv);
+      const float2 back = __half22float2(h);
+      const float t0 = back.x * s, t1 = back.y * s;
+      const float d0 = x[j] - t0, d1 = x[j + 1] - t1;
+      st = __fmaf_rn(t0, t0, st);
+      st = __fmaf_rn(t1, t1, st);
+      sd = __fmaf_rn(d0, d0, sd);
+      sd = __fmaf_rn(d1, d1, sd);
+      w[2 * i + j / 2] = *reinterpret_cast<const uint32_t*>(&h);
     }
   }
-  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-  // 128 squares summed in fp32 are within 2^-16 of the exact sum; sqrt rounded up, then 2^-14 on top
-  return __fmul_ru(__fsqrt_ru(ss), 1.00006103515625f);
+  if (store) {
+    uint4* o = reinterpret_cast<uint4*>(dst);
+    o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// One key block (rows [128 t, min(128 t + 128, L))): its scale s_b, the fp16
+// rows of k / s_b, and (max ||k_p||, max ||k_p - k~_p||) over its rows.  Lanes
+// 8g..8g+7 take row r + g + 4j (16 floats each), 16 rows in flight per step;
+// the first pass finds max |k|, the second (L2-hot) converts.
+__device__ __forceinline__ void bt_key_block(const float* k, __half* k16, int64_t t, int64_t L, float2* kb,
+                                             float* ksc) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r_end = (t + 1) * 128 < L ? (t + 1) * 128 : L;
+  float am = 0.0f;
+  for (int64_t r = t * 128; r < r_end; r += 16) {
+    float4 v[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t row = r + (lane >> 3) + 4 * j;
+      const float4* p = reinterpret_cast<const float4*>(k + row * 128) + (lane & 7) * 4;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[j][i] = row < r_end ? __ldg(p + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        am = fmaxf(am, fmaxf(fmaxf(fabsf(v[j][i].x), fabsf(v[j][i].y)), fmaxf(fabsf(v[j][i].z), fabsf(v[j][i].w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  const float s = bt_scale(am), inv = 1.0f / s;   // exact: a power of two
+  float mk = 0.0f, md = 0.0f;
+  for (int64_t r = t * 128; r < r_end; r += 16) {
+    float4 v[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t row = r + (lane >> 3) + 4 * j;
+      const float4* p = reinterpret_cast<const float4*>(k + row * 128) + (lane & 7) * 4;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[j][i] = row < r_end ? __ldg(p + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t row = r + (lane >> 3) + 4 * j;
+      float st = 0.0f, sd = 0.0f;
+      bt_to_f16(v[j], s, inv, k16 + row * 128 + (lane & 7) * 16, row < r_end, st, sd);
+      // ||k|| from k~ and k - k~: ||k|| <= ||k~|| + ||k - k~||
+      const float nd = bt_norm_up(bt_sum8(sd));
+      mk = fmaxf(mk, __fadd_ru(bt_norm_up(bt_sum8(st)), nd));
+      md = fmaxf(md, nd);
+    }
+  }
+  mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, 8));
+  mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, 16));
+  md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, 8));
+  md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, 16));
+  if (lane == 0) {
+    kb[t] = make_float2(mk, md);
+    ksc[t] = s;
+  }
+}
+
+// Four query rows r0..r0+3: scale sigma per row, fp16 rows of q / sigma, and
+// the bound factors (||dq|| + 2^-12 (||q~|| + ||dq||), ||q~||), dq = q - q~.
+__device__ __forceinline__ void bt_query_rows(const float* q, __half* q16, float2* qab, float* qsig, int64_t r0,
+                                              int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = r0 + (lane >> 3);
+  float4 v[4];
+  const float4* p = reinterpret_cast<const float4*>(q + (r < rows ? r : 0) * 128) + (lane & 7) * 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = r < rows ? __ldg(p + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float am = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) am = fmaxf(am, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+  const float s = bt_scale(bt_max8(am)), inv = 1.0f / s;
+  float st = 0.0f, sd = 0.0f;
+  bt_to_f16(v, s, inv, q16 + r * 128 + (lane & 7) * 16, r < rows, st, sd);
+  const float nt = bt_norm_up(bt_sum8(st)), nd = bt_norm_up(bt_sum8(sd));
+  if ((lane & 7) == 0 && r < rows) {
+    qab[r] = make_float2(__fmaf_ru(kBtGamma, __fadd_ru(nt, nd), nd), nt);
+    qsig[r] = s;
+  }
+}
+
+// Certified bound of |A_b - E_b| for a pair and a block.
+__device__ __forceinline__ float bt_bound(float2 qab, float2 kb) {
+  return __fadd_ru(__fmaf_ru(qab.x, kb.x, __fmul_ru(qab.y, kb.y)), kBtAbs);
 }
 
 constexpr int kBtPrepThreads = 256;
 
 // CTA 0: counting sort of the queries by visible block count (rank -> query),
 // the block count of every row tile pair, and the per-block list counters set
-// to zero.  Other CTAs: the norm bounds (warp tasks: key blocks, then groups of
-// four (query, head) rows).
+// to zero.  Other CTAs (warp tasks): the key-block bound factors, then groups of
+// four (query, head) rows: tf32 copy and bound factors.
 __global__ void __launch_bounds__(kBtPrepThreads) bt_prep_kernel(BtProblem P, BtWs W) {
   if (blockIdx.x == 0) {
     __shared__ int32_t hist[kBtSortBins];
@@ -223,19 +366,8 @@ __global__ void __launch_bounds__(kBtPrepThreads) bt_prep_kernel(BtProblem P, Bt
   const int64_t n_tasks = P.nbm + (P.slots + 3) / 4;
   for (int64_t t = (int64_t)(blockIdx.x - 1) * warps + (threadIdx.x >> 5); t < n_tasks;
        t += (int64_t)(gridDim.x - 1) * warps) {
-    const int lane = threadIdx.x & 31;
-    if (t < P.nbm) {
-      const int64_t r_end = (t + 1) * 128 < P.L ? (t + 1) * 128 : P.L;
-      float mx = 0.0f;
-      for (int64_t r = t * 128; r < r_end; r += 4) mx = fmaxf(mx, bt_norm4(P.k, r, r_end));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      if (lane == 0) W.kmax[t] = mx;
-    } else {
-      const int64_t r0 = (t - P.nbm) * 4;
-      const float n = bt_norm4(P.q, r0, P.slots);
-      if ((lane & 7) == 0 && r0 + (lane >> 3) < P.slots) W.qn[r0 + (lane >> 3)] = n;
-    }
+    if (t < P.nbm) bt_key_block(P.k, W.k16, t, P.L, W.kb, W.ksc);
+    else bt_query_rows(P.q, W.q16, W.qab, W.qsig, (t - P.nbm) * 4, P.slots);
   }
 }
 
@@ -395,11 +527,11 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         bool ok = true;
         if (lane == 0) {
           ok = mbar_wait(a_empty, (na & 1) ^ 1, abort_flag);
-          if (ok) mbar_arrive_expect_tx(a_full, 2 * kBtATile);
+          if (ok) mbar_arrive_expect_tx(a_full, 2 * kBtATile);   // two tiles
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         __syncwarp();
-        // lane l: rows 8l .. 8l+7 of the tile pair, four at a time, four K chunks each
+        // lane l: rows 8l .. 8l+7 of the tile pair, four at a time, two K chunks each
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const int r0 = 8 * lane + 4 * g;
@@ -411,18 +543,18 @@ __global__ void __launch_bounds__(kBtThreads, 1)
           }
           uint8_t* dst = sA + (r0 >> 7) * kBtATile + (r0 & 127) * 128;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) bt_gather4(dst + c * kBtChunkBytes, &tmap_q, a_full, 32 * c, y[0], y[1], y[2], y[3]);
+          for (int c = 0; c < 2; ++c) bt_gather4(dst + c * kBtChunkBytes, &tmap_q, a_full, 64 * c, y[0], y[1], y[2], y[3]);
         }
         ++na;
       }
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         const int st = nk % kBtKStages;
         bool ok = true;
         if (lane == 0) {
           ok = mbar_wait(&k_empty[st], ((nk / kBtKStages) & 1) ^ 1, abort_flag);
           if (ok) {
             mbar_arrive_expect_tx(&k_full[st], kBtChunkBytes);
-            tma_load_2d(sK + st * kBtChunkBytes, &tmap_k, &k_full[st], 32 * c, (int32_t)(u.b * 128));
+            tma_load_2d(sK + st * kBtChunkBytes, &tmap_k, &k_full[st], 64 * c, (int32_t)(u.b * 128));
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -445,7 +577,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(128, 128, 2u);   // A, B tf32; D f32
+      constexpr uint32_t idesc = idesc_f16(128, 128, 0u);   // A, B fp16; D f32
       BtUnits u;
       u.init(W, s);
       int64_t cur_T = -1;
@@ -461,7 +593,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         if (!(ok = mbar_wait(&acc_empty[acc], ((nacc >> 1) & 1) ^ 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + (uint32_t)(acc * 256);
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           const int st = nk % kBtKStages;
           if (!(ok = mbar_wait(&k_full[st], (nk / kBtKStages) & 1, abort_flag))) break;
           tc_fence_after();
@@ -471,8 +603,8 @@ __global__ void __launch_bounds__(kBtThreads, 1)
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = smem_desc_sw128(kb + kk * 32);
             const uint32_t accum = (c | kk) ? 1u : 0u;
-            tc_mma_tf32(d0, smem_desc_sw128(a0 + kk * 32), bd, idesc, accum);
-            tc_mma_tf32(d0 + 128, smem_desc_sw128(a0 + kBtATile + kk * 32), bd, idesc, accum);
+            tc_mma_f16(d0, smem_desc_sw128(a0 + kk * 32), bd, idesc, accum);
+            tc_mma_f16(d0 + 128, smem_desc_sw128(a0 + kBtATile + kk * 32), bd, idesc, accum);
           }
           issued = true;
           tc_commit(&k_empty[st]);
@@ -499,6 +631,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
     BtUnits u;
     u.init(W, s);
     int64_t cur_T = -1, slot = 0, vis = 0;
+    float sig = 1.0f;
     uint32_t nacc = 0;
     const float ninf = -__int_as_float(0x7f800000);
     while (u.valid()) {
@@ -507,8 +640,10 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         slot = cur_T * kBtRowsT + row;
         vis = 0;
         if (slot < P.slots) {
-          const int64_t pos = P.qpos[bt_slot_query(P, W, slot)];
+          const int64_t qi = bt_slot_query(P, W, slot);
+          const int64_t pos = P.qpos[qi];
           if (pos >= 0) vis = pos + 1 < P.L ? pos + 1 : P.L;
+          sig = W.qsig[qi * P.n_kv + slot % P.n_kv];
         }
       }
       const int acc = nacc & 1;
@@ -547,7 +682,8 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             m3 = fmaxf(m3, i + 96 < nv ? __uint_as_float(v3[i]) : ninf);
           }
         }
-        W.amax[slot * P.nbm + u.b] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+        // A_b = sigma s_b max(acc): both scales are powers of two
+        W.amax[slot * P.nbm + u.b] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * (sig * W.ksc[u.b]);
       }
       ++nacc;
       u.advance();
@@ -621,6 +757,68 @@ __device__ uint32_t bt_warp_kth(const F& key, int64_t i0, int64_t i1, int64_t n,
   return prefix;
 }
 
+// The n-th largest of the keys key(i), i in [i0, i1) (n < i1 - i0).  For
+// n <= 32: the n-th largest of the 32 lanes' maxima is a lower threshold (n
+// lanes each hold a key at or above it); the answer is then the largest key k
+// of the (few) keys above that threshold with #{keys >= k} >= n, by rank
+// counting in shared memory.  Larger n, or too many keys above the threshold
+// (ties): radix select.  sbuf, skey, hist: per-warp scratch (kBtCapC, kBtCapC, 256).
+template <class F>
+__device__ uint32_t bt_lower_cut(const F& key, int64_t i0, int64_t i1, int64_t n, int32_t* sbuf, uint32_t* skey,
+                                 int32_t* hist) {
+  const int lane = threadIdx.x & 31;
+  if (n <= 32) {
+    uint32_t mx = 0;
+    for (int64_t i = i0 + lane; i < i1; i += 32) {
+      const uint32_t k = key(i);
+      mx = k > mx ? k : mx;
+    }
+    // rank of this lane's maximum among the 32 (ties: count every equal one)
+    int ge = 0;
+#pragma unroll
+    for (int o = 0; o < 32; ++o) ge += __shfl_sync(kFull, mx, o) >= mx ? 1 : 0;
+    uint32_t t0 = ge >= n ? mx : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint32_t u = __shfl_xor_sync(kFull, t0, o);
+      t0 = u > t0 ? u : t0;
+    }
+    // keys >= t0, compacted (their count is at least n)
+    int ns = 0;
+    for (int64_t b0 = i0; b0 < i1; b0 += 32) {
+      const int64_t i = b0 + lane;
+      const uint32_t k = i < i1 ? key(i) : 0u;
+      const bool in = i < i1 && k >= t0;
+      const unsigned bal = __ballot_sync(kFull, in);
+      if (in) {
+        const int p = ns + __popc(bal & ((1u << lane) - 1u));
+        if (p < kBtCapC) skey[p] = k;
+      }
+      ns += __popc(bal);
+    }
+    __syncwarp();
+    if (ns <= kBtCapC) {
+      uint32_t best = 0;
+      for (int i = lane; i < ns; i += 32) {
+        const uint32_t ki = skey[i];
+        int c = 0;
+        for (int j = 0; j < ns; ++j) c += skey[j] >= ki ? 1 : 0;
+        if (c >= n && ki > best) best = ki;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint32_t u = __shfl_xor_sync(kFull, best, o);
+        best = u > best ? u : best;
+      }
+      __syncwarp();
+      return best;
+    }
+    __syncwarp();
+  }
+  int64_t need_eq;
+  return bt_warp_kth(key, i0, i1, n, hist, &need_eq);
+}
+
 // Forced head [0, a), a middle of `mid` entries (written elsewhere) at [a, a+mid),
 // the forced tail zs..n-1 after it, -1 padding; returns the count.
 __device__ __forceinline__ int64_t bt_frame(int32_t* o, int Wd, int64_t a, int64_t mid, int64_t zs, int64_t n) {
@@ -679,12 +877,11 @@ __device__ void bt_classify_slot(const BtProblem& P, const BtWs& W, int64_t slot
       for (int j = lane; j < Wd; j += 32) o[j] = j < s.n ? j : -1;
       count = s.n;
     } else {
-      const float ce = __fmul_ru(kBtErr, W.qn[s.pair]);
+      const float2 qab = W.qab[s.pair];
       const float* arow = W.amax + slot * P.nbm;
-      const float* kmax = W.kmax;
-      auto lo_key = [&](int64_t b) { return score_key(__fsub_rd(arow[b], __fmul_ru(ce, kmax[b]))); };
-      int64_t need_eq;
-      const uint32_t T = bt_warp_kth(lo_key, s.a, s.zs, s.n_need, hist, &need_eq);
+      const float2* kbs = W.kb;
+      auto lo_key = [&](int64_t b) { return score_key(__fsub_rd(arow[b], bt_bound(qab, kbs[b]))); };
+      const uint32_t T = bt_lower_cut(lo_key, s.a, s.zs, s.n_need, cb, clo, hist);
       // candidates: upper bound >= T, ascending
       int nc = 0;
       for (int64_t b0 = s.a; b0 < s.zs; b0 += 32) {
@@ -692,7 +889,7 @@ __device__ void bt_classify_slot(const BtProblem& P, const BtWs& W, int64_t slot
         bool c = false;
         uint32_t lk = 0, hk = 0;
         if (b < s.zs) {
-          const float A = arow[b], e = __fmul_ru(ce, kmax[b]);
+          const float A = arow[b], e = bt_bound(qab, kbs[b]);
           lk = score_key(__fsub_rd(A, e));
           hk = score_key(__fadd_ru(A, e));
           c = hk >= T;
@@ -801,12 +998,13 @@ __global__ void __launch_bounds__(32 * kBtWarps) bt_classify_kernel(BtProblem P,
 
 // ------------------------------------------------------------ exact scores --
 constexpr int kBtExactThreads = 256;
-constexpr int kBtExactSmem = (128 * 128 + (kBtExactThreads / 32) * 128 * 2) * 4;
+constexpr int kBtExactSmem = (128 * 128 + (kBtExactThreads / 32) * 128 * 4) * 4;
 
 // One CTA per key block: its keys staged transposed ([d][key]), then each warp
-// takes two listed pairs at a time; lane l runs the page's chains of keys
-// 4l..4l+3 for both (packed: two keys of one pair per instruction).  The exact
-// block score replaces A_b in the pair's row as an ordered key.
+// takes four listed pairs at a time; lane l runs the page's chains of keys
+// 4l..4l+3 for all four (packed: two keys of one pair per instruction, each
+// half rounded as the scalar instruction rounds).  The exact block score
+// replaces A_b in the pair's row as an ordered key.
 __global__ void __launch_bounds__(kBtExactThreads) bt_exact_kernel(BtProblem P, BtWs W, block_select_stats* stats) {
   extern __shared__ __align__(16) float kt[];
   __shared__ float s_worst;
@@ -818,6 +1016,7 @@ __global__ void __launch_bounds__(kBtExactThreads) bt_exact_kernel(BtProblem P, 
   const int nk = (int)(P.L - k0 < 128 ? P.L - k0 : 128);
   {
     const float4* src = reinterpret_cast<const float4*>(P.k + k0 * 128);
+#pragma unroll 4
     for (int i = t; i < nk * 32; i += kBtExactThreads) {
       const int key = i % nk, d4 = i / nk;
       const float4 v = __ldg(src + key * 32 + d4);
@@ -829,48 +1028,57 @@ __global__ void __launch_bounds__(kBtExactThreads) bt_exact_kernel(BtProblem P, 
   }
   if (t == 0) s_worst = 0.0f;
   __syncthreads();
-  float2* qs = reinterpret_cast<float2*>(kt + 128 * 128) + wi * 128;
-  const float km = W.kmax[b];
+  float4* qs = reinterpret_cast<float4*>(kt + 128 * 128) + wi * 128;   // [d] = (q of the four pairs)
+  const float2 kb = W.kb[b];
   const float ninf = -__int_as_float(0x7f800000);
   float worst = 0.0f;
   const int32_t* items = W.ilist + b * P.slots;
-  for (int ip = wi; 2 * ip < cnt; ip += kBtExactThreads / 32) {
-    const int i0 = 2 * ip;
-    const bool two = i0 + 1 < cnt;
-    const int64_t s0 = items[i0], s1 = two ? items[i0 + 1] : s0;
-    const int64_t q0 = bt_slot_query(P, W, s0), q1 = bt_slot_query(P, W, s1);
-    const int64_t p0 = q0 * P.n_kv + s0 % P.n_kv, p1 = q1 * P.n_kv + s1 % P.n_kv;
+  for (int ip = wi; 4 * ip < cnt; ip += kBtExactThreads / 32) {
+    const int i0 = 4 * ip;
+    const int nit = cnt - i0 < 4 ? cnt - i0 : 4;
+    int64_t sl[4], pr[4];
+    int64_t vis[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      sl[it] = items[i0 + (it < nit ? it : 0)];
+      const int64_t qi = bt_slot_query(P, W, sl[it]);
+      pr[it] = qi * P.n_kv + sl[it] % P.n_kv;
+      const int64_t v = (int64_t)P.qpos[qi] + 1;
+      vis[it] = v < P.L ? v : P.L;
+    }
     {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(P.q + p0 * 128) + lane);
-      const float4 y = __ldg(reinterpret_cast<const float4*>(P.q + p1 * 128) + lane);
-      qs[4 * lane + 0] = make_float2(x.x, y.x);
-      qs[4 * lane + 1] = make_float2(x.y, y.y);
-      qs[4 * lane + 2] = make_float2(x.z, y.z);
-      qs[4 * lane + 3] = make_float2(x.w, y.w);
+      float4 x[4];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) x[it] = __ldg(reinterpret_cast<const float4*>(P.q + pr[it] * 128) + lane);
+      qs[4 * lane + 0] = make_float4(x[0].x, x[1].x, x[2].x, x[3].x);
+      qs[4 * lane + 1] = make_float4(x[0].y, x[1].y, x[2].y, x[3].y);
+      qs[4 * lane + 2] = make_float4(x[0].z, x[1].z, x[2].z, x[3].z);
+      qs[4 * lane + 3] = make_float4(x[0].w, x[1].w, x[2].w, x[3].w);
     }
     __syncwarp();
-    uint64_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;   // pair 0: keys (4l, 4l+1), (4l+2, 4l+3); pair 1: same
-#pragma unroll 8
+    uint64_t c[8];   // pair it: keys (4l, 4l+1) in c[2 it], (4l+2, 4l+3) in c[2 it + 1]
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c[j] = 0ull;
+#pragma unroll 4
     for (int d = 0; d < 128; ++d) {
       const float4 kv = *reinterpret_cast<const float4*>(kt + d * 128 + 4 * lane);
-      const float2 qq = qs[d];
+      const float4 qq = qs[d];
       const uint64_t k01 = f2_pack(kv.x, kv.y), k23 = f2_pack(kv.z, kv.w);
-      const uint64_t x0 = f2_pack(qq.x, qq.x), x1 = f2_pack(qq.y, qq.y);
-      c0 = f2_add(c0, f2_mul(x0, k01));
-      c1 = f2_add(c1, f2_mul(x0, k23));
-      c2 = f2_add(c2, f2_mul(x1, k01));
-      c3 = f2_add(c3, f2_mul(x1, k23));
+      const float qv[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const uint64_t x = f2_pack(qv[it], qv[it]);
+        c[2 * it] = f2_add(c[2 * it], f2_mul(x, k01));
+        c[2 * it + 1] = f2_add(c[2 * it + 1], f2_mul(x, k23));
+      }
     }
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
-      if (it == 1 && !two) break;
-      const int64_t sl = it ? s1 : s0, qi = it ? q1 : q0, pr = it ? p1 : p0;
-      int64_t vis = (int64_t)P.qpos[qi] + 1;
-      vis = vis < P.L ? vis : P.L;
-      const int nv = (int)(vis - k0);
+    for (int it = 0; it < 4; ++it) {
+      if (it >= nit) break;
+      const int nv = (int)(vis[it] - k0);   // >= 1 for a listed block
       float e[4];
-      f2_unpack(it ? c2 : c0, &e[0], &e[1]);
-      f2_unpack(it ? c3 : c1, &e[2], &e[3]);
+      f2_unpack(c[2 * it], &e[0], &e[1]);
+      f2_unpack(c[2 * it + 1], &e[2], &e[3]);
       float mx = ninf;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -878,9 +1086,9 @@ __global__ void __launch_bounds__(kBtExactThreads) bt_exact_kernel(BtProblem P, 
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
       if (lane == 0) {
-        uint32_t* cell = reinterpret_cast<uint32_t*>(W.amax) + sl * P.nbm + b;
+        uint32_t* cell = reinterpret_cast<uint32_t*>(W.amax) + sl[it] * P.nbm + b;
         const float A = __uint_as_float(*cell);
-        const float eb = __fmul_ru(__fmul_ru(kBtErr, W.qn[pr]), km);
+        const float eb = bt_bound(W.qab[pr[it]], kb);
         if (eb > 0.0f) worst = fmaxf(worst, fabsf(A - mx) / eb);
         *cell = score_key(mx);
       }
@@ -1019,8 +1227,8 @@ cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t
   }
   if (P.nbm > 0) {
     CUtensorMap tk, tq;
-    bool ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, k, 128, (uint64_t)L, 512, 32, 128);
-    ok = ok && make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q, 128, (uint64_t)P.slots, 512, 32, 1);
+    bool ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W.k16, 128, (uint64_t)L, 256, 64, 128);
+    ok = ok && make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W.q16, 128, (uint64_t)P.slots, 256, 64, 1);
     if (!ok) return cudaErrorInvalidValue;
     if ((e = cudaFuncSetAttribute(bt_max_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBtSmem)) !=
         cudaSuccess)
