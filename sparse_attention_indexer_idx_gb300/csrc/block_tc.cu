@@ -73,7 +73,11 @@ constexpr int kBtKStages = 10;       // key-chunk ring
 constexpr int kBtChunkBytes = 128 * 128;   // 128 rows x 64 fp16 (one 128-byte swizzle span)
 constexpr int kBtATile = 2 * kBtChunkBytes;   // 128 rows x 128 fp16
 constexpr int kBtNE = 8;             // epilogue warps
-constexpr int kBtThreads = 32 * (2 + kBtNE);
+// warp 0 TMA producer, warp 1 and the last warp MMA issue (alternate units:
+// tcgen05.mma issue blocks while the tensor pipe is busy, so one thread's waits
+// and commits overlap the other thread's MMAs), warps 2 .. 2 + kBtNE - 1 epilogue
+constexpr int kBtMma2Warp = 2 + kBtNE;
+constexpr int kBtThreads = 32 * (3 + kBtNE);
 constexpr int kBtTmemCols = 512;     // two stages x two tiles x 128 keys
 constexpr int kBtCapC = 256;         // candidates per pair held by the classifier
 constexpr int kBtCapU = 64;          // undecided blocks per pair resolved from a list
@@ -219,60 +223,62 @@ __device__ __forceinline__ void bt_to_f16(const float4 (&v)[4], float s, float i
   }
 }
 
-// One key block (rows [128 t, min(128 t + 128, L))): its scale s_b, the fp16
-// rows of k / s_b, and (max ||k_p||, max ||k_p - k~_p||) over its rows.  Lanes
-// 8g..8g+7 take row r + g + 4j (16 floats each), 16 rows in flight per step;
-// the first pass finds max |k|, the second (L2-hot) converts.
+// One key block (rows [128 t, min(128 t + 128, L))) per CTA of 8 warps: its
+// scale s_b, the fp16 rows of k / s_b, and (max ||k_p||, max ||k_p - k~_p||).
+// Warp w holds rows 16w .. 16w+15 in registers (lanes 8g..8g+7: row 16w + g +
+// 4j, 16 floats each), so the block is read once, every load in flight.
 __device__ __forceinline__ void bt_key_block(const float* k, __half* k16, int64_t t, int64_t L, float2* kb,
-                                             float* ksc) {
-  const int lane = threadIdx.x & 31;
+                                             float* ksc, float* red) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t r_end = (t + 1) * 128 < L ? (t + 1) * 128 : L;
+  float4 v[4][4];
   float am = 0.0f;
-  for (int64_t r = t * 128; r < r_end; r += 16) {
-    float4 v[4][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t row = r + (lane >> 3) + 4 * j;
-      const float4* p = reinterpret_cast<const float4*>(k + row * 128) + (lane & 7) * 4;
+  for (int j = 0; j < 4; ++j) {
+    const int64_t row = t * 128 + 16 * w + (lane >> 3) + 4 * j;
+    const float4* p = reinterpret_cast<const float4*>(k + row * 128) + (lane & 7) * 4;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v[j][i] = row < r_end ? __ldg(p + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        am = fmaxf(am, fmaxf(fmaxf(fabsf(v[j][i].x), fabsf(v[j][i].y)), fmaxf(fabsf(v[j][i].z), fabsf(v[j][i].w))));
+    for (int i = 0; i < 4; ++i) v[j][i] = row < r_end ? __ldg(p + i) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      am = fmaxf(am, fmaxf(fmaxf(fabsf(v[j][i].x), fabsf(v[j][i].y)), fmaxf(fabsf(v[j][i].z), fabsf(v[j][i].w))));
+#pragma unroll
   for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  if (lane == 0) red[w] = am;
+  __syncthreads();
+  am = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) am = fmaxf(am, red[i]);
   const float s = bt_scale(am), inv = 1.0f / s;   // exact: a power of two
   float mk = 0.0f, md = 0.0f;
-  for (int64_t r = t * 128; r < r_end; r += 16) {
-    float4 v[4][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t row = r + (lane >> 3) + 4 * j;
-      const float4* p = reinterpret_cast<const float4*>(k + row * 128) + (lane & 7) * 4;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[j][i] = row < r_end ? __ldg(p + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t row = r + (lane >> 3) + 4 * j;
-      float st = 0.0f, sd = 0.0f;
-      bt_to_f16(v[j], s, inv, k16 + row * 128 + (lane & 7) * 16, row < r_end, st, sd);
-      // ||k|| from k~ and k - k~: ||k|| <= ||k~|| + ||k - k~||
-      const float nd = bt_norm_up(bt_sum8(sd));
-      mk = fmaxf(mk, __fadd_ru(bt_norm_up(bt_sum8(st)), nd));
-      md = fmaxf(md, nd);
-    }
+  for (int j = 0; j < 4; ++j) {
+    const int64_t row = t * 128 + 16 * w + (lane >> 3) + 4 * j;
+    float st = 0.0f, sd = 0.0f;
+    bt_to_f16(v[j], s, inv, k16 + row * 128 + (lane & 7) * 16, row < r_end, st, sd);
+    // ||k|| <= ||k~|| + ||k - k~||
+    const float nd = bt_norm_up(bt_sum8(sd));
+    mk = fmaxf(mk, __fadd_ru(bt_norm_up(bt_sum8(st)), nd));
+    md = fmaxf(md, nd);
   }
   mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, 8));
   mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, 16));
   md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, 8));
   md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, 16));
   if (lane == 0) {
-    kb[t] = make_float2(mk, md);
+    red[8 + w] = mk;
+    red[16 + w] = md;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < 8; ++i) {
+      mk = fmaxf(mk, red[8 + i]);
+      md = fmaxf(md, red[16 + i]);
+    }
+    kb[t] = make_float2(fmaxf(mk, red[8]), fmaxf(md, red[16]));
     ksc[t] = s;
   }
 }
@@ -309,8 +315,8 @@ constexpr int kBtPrepThreads = 256;
 
 // CTA 0: counting sort of the queries by visible block count (rank -> query),
 // the block count of every row tile pair, and the per-block list counters set
-// to zero.  Other CTAs (warp tasks): the key-block bound factors, then groups of
-// four (query, head) rows: tf32 copy and bound factors.
+// to zero.  CTAs 1 .. nbm: one key block each.  The rest: 32 (query, head)
+// rows each (four per warp).
 __global__ void __launch_bounds__(kBtPrepThreads) bt_prep_kernel(BtProblem P, BtWs W) {
   if (blockIdx.x == 0) {
     __shared__ int32_t hist[kBtSortBins];
@@ -362,12 +368,13 @@ __global__ void __launch_bounds__(kBtPrepThreads) bt_prep_kernel(BtProblem P, Bt
     for (int64_t b = threadIdx.x; b < P.nbm; b += kBtPrepThreads) W.icnt[b] = 0;
     return;
   }
-  const int warps = kBtPrepThreads / 32;
-  const int64_t n_tasks = P.nbm + (P.slots + 3) / 4;
-  for (int64_t t = (int64_t)(blockIdx.x - 1) * warps + (threadIdx.x >> 5); t < n_tasks;
-       t += (int64_t)(gridDim.x - 1) * warps) {
-    if (t < P.nbm) bt_key_block(P.k, W.k16, t, P.L, W.kb, W.ksc);
-    else bt_query_rows(P.q, W.q16, W.qab, W.qsig, (t - P.nbm) * 4, P.slots);
+  __shared__ float red[24];
+  const int64_t cta = (int64_t)blockIdx.x - 1;
+  if (cta < P.nbm) {
+    bt_key_block(P.k, W.k16, cta, P.L, W.kb, W.ksc, red);
+  } else {
+    const int64_t r0 = (cta - P.nbm) * 32 + 4 * (threadIdx.x >> 5);
+    bt_query_rows(P.q, W.q16, W.qab, W.qsig, r0, P.slots);
   }
 }
 
@@ -458,7 +465,7 @@ __device__ __forceinline__ void bt_gather4(void* dst, const void* tmap, uint64_t
 constexpr int kBtOffA = 0;
 constexpr int kBtOffK = kBtOffA + 2 * kBtATile;
 constexpr int kBtOffBar = kBtOffK + kBtKStages * kBtChunkBytes;
-constexpr int kBtNBars = 2 + 2 * kBtKStages + 4 + 1;
+constexpr int kBtNBars = 2 + 2 * kBtKStages + 4 + 2;
 constexpr int kBtOffMisc = kBtOffBar + kBtNBars * 8;
 constexpr int kBtSmem = kBtOffMisc + 64 + 1024;
 static_assert(kBtSmem <= 232448, "shared memory");
@@ -487,7 +494,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(a_full, 1);
-    mbar_init(a_empty, 1);
+    mbar_init(a_empty, 2);   // both MMA-issuing threads, once per row tile pair
     for (int i = 0; i < kBtKStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -496,7 +503,8 @@ __global__ void __launch_bounds__(kBtThreads, 1)
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kBtNE);
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(&drain_bar[0], 1);
+    mbar_init(&drain_bar[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -574,14 +582,17 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         mbar_wait(&k_full[j % kBtKStages], (j / kBtKStages) & 1, no_abort);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kBtMma2Warp) {
     // ------------------------------------------------------------ MMA issue
+    // Both threads walk every unit; thread `me` issues the units of its parity
+    // into accumulator stage `me`.
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(128, 128, 0u);   // A, B fp16; D f32
+      const uint32_t me = warp == 1 ? 0u : 1u;
       BtUnits u;
       u.init(W, s);
       int64_t cur_T = -1;
-      uint32_t na = 0, nk = 0, nacc = 0;
+      uint32_t na = 0, nunit = 0;
       bool issued = false, ok = true;
       while (u.valid() && ok) {
         if (u.T != cur_T) {
@@ -589,40 +600,42 @@ __global__ void __launch_bounds__(kBtThreads, 1)
           if (!(ok = mbar_wait(a_full, na & 1, abort_flag))) break;
           ++na;
         }
-        const int acc = nacc & 1;
-        if (!(ok = mbar_wait(&acc_empty[acc], ((nacc >> 1) & 1) ^ 1, abort_flag))) break;
-        tc_fence_after();
-        const uint32_t d0 = tmem_base + (uint32_t)(acc * 256);
-        for (int c = 0; c < 2; ++c) {
-          const int st = nk % kBtKStages;
-          if (!(ok = mbar_wait(&k_full[st], (nk / kBtKStages) & 1, abort_flag))) break;
+        if ((nunit & 1u) == me) {
+          const uint32_t use = nunit >> 1;   // this thread's use count of its stage
+          if (!(ok = mbar_wait(&acc_empty[me], (use & 1) ^ 1, abort_flag))) break;
           tc_fence_after();
-          const uint32_t kb = smem_u32(sK + st * kBtChunkBytes);
-          const uint32_t a0 = smem_u32(sA + c * kBtChunkBytes);
+          const uint32_t d0 = tmem_base + me * 256u;
+          for (int c = 0; c < 2 && ok; ++c) {
+            const uint32_t nk = 2 * nunit + c;
+            const int st = nk % kBtKStages;
+            if (!(ok = mbar_wait(&k_full[st], (nk / kBtKStages) & 1, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t kb = smem_u32(sK + st * kBtChunkBytes);
+            const uint32_t a0 = smem_u32(sA + c * kBtChunkBytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = smem_desc_sw128(kb + kk * 32);
-            const uint32_t accum = (c | kk) ? 1u : 0u;
-            tc_mma_f16(d0, smem_desc_sw128(a0 + kk * 32), bd, idesc, accum);
-            tc_mma_f16(d0 + 128, smem_desc_sw128(a0 + kBtATile + kk * 32), bd, idesc, accum);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = smem_desc_sw128(kb + kk * 32);
+              const uint32_t accum = (c | kk) ? 1u : 0u;
+              tc_mma_f16(d0, smem_desc_sw128(a0 + kk * 32), bd, idesc, accum);
+              tc_mma_f16(d0 + 128, smem_desc_sw128(a0 + kBtATile + kk * 32), bd, idesc, accum);
+            }
+            issued = true;
+            tc_commit(&k_empty[st]);
           }
-          issued = true;
-          tc_commit(&k_empty[st]);
-          ++nk;
+          if (!ok) break;
+          tc_commit(&acc_full[me]);
         }
-        if (!ok) break;
-        tc_commit(&acc_full[acc]);
-        ++nacc;
+        ++nunit;
         const int64_t T_this = u.T;
         u.advance();
         if (!u.valid() || u.T != T_this) tc_commit(a_empty);
       }
       if (issued) {
-        tc_commit(drain_bar);
-        mbar_wait(drain_bar, 0, no_abort);
+        tc_commit(&drain_bar[me]);
+        mbar_wait(&drain_bar[me], 0, no_abort);
       }
     }
-  } else {
+  } else if (warp >= 2 && warp < 2 + kBtNE) {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;
     const int quarter = warp & 3;
@@ -757,68 +770,6 @@ __device__ uint32_t bt_warp_kth(const F& key, int64_t i0, int64_t i1, int64_t n,
   return prefix;
 }
 
-// The n-th largest of the keys key(i), i in [i0, i1) (n < i1 - i0).  For
-// n <= 32: the n-th largest of the 32 lanes' maxima is a lower threshold (n
-// lanes each hold a key at or above it); the answer is then the largest key k
-// of the (few) keys above that threshold with #{keys >= k} >= n, by rank
-// counting in shared memory.  Larger n, or too many keys above the threshold
-// (ties): radix select.  sbuf, skey, hist: per-warp scratch (kBtCapC, kBtCapC, 256).
-template <class F>
-__device__ uint32_t bt_lower_cut(const F& key, int64_t i0, int64_t i1, int64_t n, int32_t* sbuf, uint32_t* skey,
-                                 int32_t* hist) {
-  const int lane = threadIdx.x & 31;
-  if (n <= 32) {
-    uint32_t mx = 0;
-    for (int64_t i = i0 + lane; i < i1; i += 32) {
-      const uint32_t k = key(i);
-      mx = k > mx ? k : mx;
-    }
-    // rank of this lane's maximum among the 32 (ties: count every equal one)
-    int ge = 0;
-#pragma unroll
-    for (int o = 0; o < 32; ++o) ge += __shfl_sync(kFull, mx, o) >= mx ? 1 : 0;
-    uint32_t t0 = ge >= n ? mx : 0u;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint32_t u = __shfl_xor_sync(kFull, t0, o);
-      t0 = u > t0 ? u : t0;
-    }
-    // keys >= t0, compacted (their count is at least n)
-    int ns = 0;
-    for (int64_t b0 = i0; b0 < i1; b0 += 32) {
-      const int64_t i = b0 + lane;
-      const uint32_t k = i < i1 ? key(i) : 0u;
-      const bool in = i < i1 && k >= t0;
-      const unsigned bal = __ballot_sync(kFull, in);
-      if (in) {
-        const int p = ns + __popc(bal & ((1u << lane) - 1u));
-        if (p < kBtCapC) skey[p] = k;
-      }
-      ns += __popc(bal);
-    }
-    __syncwarp();
-    if (ns <= kBtCapC) {
-      uint32_t best = 0;
-      for (int i = lane; i < ns; i += 32) {
-        const uint32_t ki = skey[i];
-        int c = 0;
-        for (int j = 0; j < ns; ++j) c += skey[j] >= ki ? 1 : 0;
-        if (c >= n && ki > best) best = ki;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const uint32_t u = __shfl_xor_sync(kFull, best, o);
-        best = u > best ? u : best;
-      }
-      __syncwarp();
-      return best;
-    }
-    __syncwarp();
-  }
-  int64_t need_eq;
-  return bt_warp_kth(key, i0, i1, n, hist, &need_eq);
-}
-
 // Forced head [0, a), a middle of `mid` entries (written elsewhere) at [a, a+mid),
 // the forced tail zs..n-1 after it, -1 padding; returns the count.
 __device__ __forceinline__ int64_t bt_frame(int32_t* o, int Wd, int64_t a, int64_t mid, int64_t zs, int64_t n) {
@@ -855,9 +806,108 @@ __device__ __forceinline__ void bt_list(const BtProblem& P, const BtWs& W, int64
 }
 
 // counters: pairs scored, blocks bounded, blocks rescored, fallback pairs
+// Bit-by-bit search for the n-th largest of the values v[u] (u < U, lanes
+// hold lane + 32u; absent ones 0) starting from t with count(>= t) >= n and
+// from bit hb down.
+template <int U>
+__device__ __forceinline__ uint32_t bt_bit_search(const uint32_t (&v)[8], uint32_t t, int hb, int n) {
+  for (int bit = hb; bit >= 0; --bit) {
+    const uint32_t cand = t | (1u << bit);
+    int c = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) c += v[u] >= cand ? 1 : 0;
+    if (__reduce_add_sync(kFull, c) >= n) t = cand;
+  }
+  return t;
+}
+
+// Candidates of a row of at most 32 R non-forced blocks [a, zs) with n <= 32,
+// every bound key held in registers (lane holds blocks a + lane + 32 r): the
+// cut T (the n-th largest lower bound) from the lanes' maxima and a bit search
+// over the few keys above them, then the blocks with upper bound >= T written
+// ascending to cb/clo/chi.  Returns their count, or -1 when the keys above the
+// lanes' cut do not fit the scratch (heavy ties; the caller takes the general
+// path).
+template <int R>
+__device__ int bt_cands_regs(const float* arow, const float2* kbs, float2 qab, int a, int zs, int n, int32_t* cb,
+                             uint32_t* clo, uint32_t* chi, uint32_t* sk, uint32_t* T_out) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  uint32_t lo[R], hi[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int b = a + lane + 32 * r;
+    lo[r] = 0u;
+    hi[r] = 0u;
+    if (b < zs) {
+      const float A = arow[b], e = bt_bound(qab, kbs[b]);
+      lo[r] = score_key(__fsub_rd(A, e));
+      hi[r] = score_key(__fadd_ru(A, e));
+    }
+  }
+  uint32_t mx = 0u;
+#pragma unroll
+  for (int r = 0; r < R; ++r) mx = lo[r] > mx ? lo[r] : mx;
+  int ge = 0;
+#pragma unroll
+  for (int o = 0; o < 32; ++o) ge += __shfl_sync(kFull, mx, o) >= mx ? 1 : 0;
+  uint32_t t0 = ge >= n ? mx : 0u, top = mx;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint32_t u = __shfl_xor_sync(kFull, t0, o), w = __shfl_xor_sync(kFull, top, o);
+    t0 = u > t0 ? u : t0;
+    top = w > top ? w : top;
+  }
+  // the keys >= t0 (at least n of them; absent blocks hold 0 < t0 unless t0 is 0)
+  int ns = 0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const bool in = a + lane + 32 * r < zs && lo[r] >= t0;
+    const unsigned bal = __ballot_sync(kFull, in);
+    if (in) {
+      const int p = ns + __popc(bal & lt);
+      if (p < kBtCapC) sk[p] = lo[r];
+    }
+    ns += __popc(bal);
+  }
+  if (ns > kBtCapC) return -1;
+  __syncwarp();
+  uint32_t v[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int i = lane + 32 * u;
+    v[u] = i < ns ? sk[i] : 0u;
+  }
+  const int hb = (t0 ^ top) ? 31 - __clz(t0 ^ top) : -1;
+  uint32_t T = hb >= 0 ? (t0 & ~((2u << hb) - 1u)) : t0;
+  if (ns <= 64) T = bt_bit_search<2>(v, T, hb, n);
+  else if (ns <= 128) T = bt_bit_search<4>(v, T, hb, n);
+  else T = bt_bit_search<8>(v, T, hb, n);
+  *T_out = T;
+  // candidates: upper bound >= T, ascending
+  int nc = 0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int b = a + lane + 32 * r;
+    const bool c = b < zs && hi[r] >= T;
+    const unsigned bal = __ballot_sync(kFull, c);
+    if (c) {
+      const int p = nc + __popc(bal & lt);
+      if (p < kBtCapC) {
+        cb[p] = b;
+        clo[p] = lo[r];
+        chi[p] = hi[r];
+      }
+    }
+    nc += __popc(bal);
+  }
+  __syncwarp();
+  return nc;
+}
+
 __device__ void bt_classify_slot(const BtProblem& P, const BtWs& W, int64_t slot, int32_t* out, int Wd,
                                  int32_t* out_count, int32_t* cb, uint32_t* clo, uint32_t* chi, int32_t* hist,
-                                 unsigned long long* cnt) {
+                                 uint32_t* sk, unsigned long long* cnt) {
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   const BtSlotGeom s = bt_slot_geom(P, W, slot);
@@ -880,32 +930,44 @@ __device__ void bt_classify_slot(const BtProblem& P, const BtWs& W, int64_t slot
       const float2 qab = W.qab[s.pair];
       const float* arow = W.amax + slot * P.nbm;
       const float2* kbs = W.kb;
-      auto lo_key = [&](int64_t b) { return score_key(__fsub_rd(arow[b], bt_bound(qab, kbs[b]))); };
-      const uint32_t T = bt_lower_cut(lo_key, s.a, s.zs, s.n_need, cb, clo, hist);
-      // candidates: upper bound >= T, ascending
-      int nc = 0;
-      for (int64_t b0 = s.a; b0 < s.zs; b0 += 32) {
-        const int64_t b = b0 + lane;
-        bool c = false;
-        uint32_t lk = 0, hk = 0;
-        if (b < s.zs) {
-          const float A = arow[b], e = bt_bound(qab, kbs[b]);
-          lk = score_key(__fsub_rd(A, e));
-          hk = score_key(__fadd_ru(A, e));
-          c = hk >= T;
-        }
-        const unsigned bal = __ballot_sync(kFull, c);
-        if (c) {
-          const int p = nc + __popc(bal & lt);
-          if (p < kBtCapC) {
-            cb[p] = (int32_t)b;
-            clo[p] = lk;
-            chi[p] = hk;
-          }
-        }
-        nc += __popc(bal);
+      int nc = -1;
+      uint32_t T = 0;
+      if (s.n_need <= 32) {
+        if (m <= 512) nc = bt_cands_regs<16>(arow, kbs, qab, (int)s.a, (int)s.zs, (int)s.n_need, cb, clo, chi, sk, &T);
+        else if (m <= 1024)
+          nc = bt_cands_regs<32>(arow, kbs, qab, (int)s.a, (int)s.zs, (int)s.n_need, cb, clo, chi, sk, &T);
       }
-      __syncwarp();
+      if (nc < 0) {
+        // general rows: the cut by radix select over all blocks, then the candidates
+        auto keys_of = [&](int64_t b) {
+          const float A = arow[b], e = bt_bound(qab, kbs[b]);
+          return make_uint2(score_key(__fsub_rd(A, e)), score_key(__fadd_ru(A, e)));
+        };
+        auto lo_key = [&](int64_t b) { return keys_of(b).x; };
+        int64_t need_eq;
+        T = bt_warp_kth(lo_key, s.a, s.zs, s.n_need, hist, &need_eq);
+        nc = 0;
+        for (int64_t b0 = s.a; b0 < s.zs; b0 += 32) {
+          const int64_t b = b0 + lane;
+          bool c = false;
+          uint2 k2 = make_uint2(0u, 0u);
+          if (b < s.zs) {
+            k2 = keys_of(b);
+            c = k2.y >= T;
+          }
+          const unsigned bal = __ballot_sync(kFull, c);
+          if (c) {
+            const int p = nc + __popc(bal & lt);
+            if (p < kBtCapC) {
+              cb[p] = (int32_t)b;
+              clo[p] = k2.x;
+              chi[p] = k2.y;
+            }
+          }
+          nc += __popc(bal);
+        }
+        __syncwarp();
+      }
       bool fallback = nc > kBtCapC;
       if (!fallback) {
         // certainly in: fewer than n_need other candidates reach its lower bound
@@ -981,6 +1043,7 @@ constexpr int kBtWarps = 8;   // pairs per CTA in the per-pair kernels
 
 __global__ void __launch_bounds__(32 * kBtWarps) bt_classify_kernel(BtProblem P, BtWs W, int32_t* out, int Wd,
                                                                       int32_t* out_count, block_select_stats* stats) {
+  __shared__ uint32_t s_k[kBtWarps][kBtCapC];
   __shared__ int32_t s_b[kBtWarps][kBtCapC];
   __shared__ uint32_t s_lo[kBtWarps][kBtCapC];
   __shared__ uint32_t s_hi[kBtWarps][kBtCapC];
@@ -990,7 +1053,8 @@ __global__ void __launch_bounds__(32 * kBtWarps) bt_classify_kernel(BtProblem P,
   __syncthreads();
   const int wi = threadIdx.x >> 5;
   const int64_t slot = (int64_t)blockIdx.x * kBtWarps + wi;
-  if (slot < P.slots) bt_classify_slot(P, W, slot, out, Wd, out_count, s_b[wi], s_lo[wi], s_hi[wi], s_hist[wi], s_cnt);
+  if (slot < P.slots)
+    bt_classify_slot(P, W, slot, out, Wd, out_count, s_b[wi], s_lo[wi], s_hi[wi], s_hist[wi], s_k[wi], s_cnt);
   __syncthreads();
   if (stats && threadIdx.x < 4 && s_cnt[threadIdx.x])
     atomicAdd(&stats->pairs + threadIdx.x, s_cnt[threadIdx.x]);
@@ -1015,15 +1079,25 @@ __global__ void __launch_bounds__(kBtExactThreads) bt_exact_kernel(BtProblem P, 
   const int64_t k0 = b * 128;
   const int nk = (int)(P.L - k0 < 128 ? P.L - k0 : 128);
   {
+    // transposed staging, every load in flight: lanes take consecutive keys of one 16-byte column
     const float4* src = reinterpret_cast<const float4*>(P.k + k0 * 128);
-#pragma unroll 4
-    for (int i = t; i < nk * 32; i += kBtExactThreads) {
-      const int key = i % nk, d4 = i / nk;
-      const float4 v = __ldg(src + key * 32 + d4);
-      kt[(4 * d4 + 0) * 128 + key] = v.x;
-      kt[(4 * d4 + 1) * 128 + key] = v.y;
-      kt[(4 * d4 + 2) * 128 + key] = v.z;
-      kt[(4 * d4 + 3) * 128 + key] = v.w;
+    const int n4 = nk * 32;
+    float4 v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = t + kBtExactThreads * u;
+      v[u] = i < n4 ? __ldg(src + (i % nk) * 32 + i / nk) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = t + kBtExactThreads * u;
+      if (i < n4) {
+        const int key = i % nk, d4 = i / nk;
+        kt[(4 * d4 + 0) * 128 + key] = v[u].x;
+        kt[(4 * d4 + 1) * 128 + key] = v[u].y;
+        kt[(4 * d4 + 2) * 128 + key] = v[u].z;
+        kt[(4 * d4 + 3) * 128 + key] = v[u].w;
+      }
     }
   }
   if (t == 0) s_worst = 0.0f;
@@ -1218,11 +1292,8 @@ cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t
   const BtWs W = bt_carve(ws, P);
   cudaError_t e;
   {
-    const int64_t tasks = P.nbm + (P.slots + 3) / 4;
-    int64_t g = (tasks + 7) / 8;
-    const int64_t gmax = 8 * (int64_t)sm_count();
-    g = g < gmax ? g : gmax;
-    bt_prep_kernel<<<(unsigned)(1 + g), kBtPrepThreads, 0, st>>>(P, W);
+    const int64_t g = 1 + P.nbm + (P.slots + 31) / 32;
+    bt_prep_kernel<<<(unsigned)g, kBtPrepThreads, 0, st>>>(P, W);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (P.nbm > 0) {
