@@ -67,10 +67,12 @@ __global__ void __launch_bounds__(kBsThreads) block_score_kernel(const float* __
 }
 
 // ------------------------------------------------------------ D == 128 --
-// Same scores, at the packed fp32 rate and half the shared-memory traffic per
+// Same scores, with packed products and half the shared-memory traffic per
 // operation:
-//  * the packed f32x2 multiply and add round each half on its own exactly as the
-//    scalar instructions do, so two keys' chains advance in one instruction;
+//  * one packed f32x2 multiply forms two keys' products (each half rounded as
+//    the scalar instruction rounds); the two sums are scalar adds, since a
+//    packed multiply feeding a packed add is fused into a packed fma by code
+//    generation (see f2_add_halves);
 //  * lanes 2i and 2i+1 hold the two halves (d < 64, d >= 64) of the queries of
 //    two pairs, so every key value a lane loads serves two pairs.  Keys go in
 //    groups of 8: the even lane sums d = 0..63 of a group while the odd lane
@@ -93,14 +95,14 @@ __device__ __forceinline__ void bs128_group(const float* kcol, const float (&qa)
     const uint64_t k45 = f2_pack(v.x, v.y), k67 = f2_pack(v.z, v.w);
     const uint64_t xa = f2_pack(qa[dd], qa[dd]);
     const uint64_t xb = f2_pack(qb[dd], qb[dd]);
-    acc[0] = f2_add(acc[0], f2_mul(xa, k01));
-    acc[1] = f2_add(acc[1], f2_mul(xa, k23));
-    acc[2] = f2_add(acc[2], f2_mul(xa, k45));
-    acc[3] = f2_add(acc[3], f2_mul(xa, k67));
-    acc[4] = f2_add(acc[4], f2_mul(xb, k01));
-    acc[5] = f2_add(acc[5], f2_mul(xb, k23));
-    acc[6] = f2_add(acc[6], f2_mul(xb, k45));
-    acc[7] = f2_add(acc[7], f2_mul(xb, k67));
+    acc[0] = f2_add_halves(acc[0], f2_mul(xa, k01));
+    acc[1] = f2_add_halves(acc[1], f2_mul(xa, k23));
+    acc[2] = f2_add_halves(acc[2], f2_mul(xa, k45));
+    acc[3] = f2_add_halves(acc[3], f2_mul(xa, k67));
+    acc[4] = f2_add_halves(acc[4], f2_mul(xb, k01));
+    acc[5] = f2_add_halves(acc[5], f2_mul(xb, k23));
+    acc[6] = f2_add_halves(acc[6], f2_mul(xb, k45));
+    acc[7] = f2_add_halves(acc[7], f2_mul(xb, k67));
   }
 }
 

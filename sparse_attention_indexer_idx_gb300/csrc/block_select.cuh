@@ -36,16 +36,23 @@ __device__ __forceinline__ bool block_forced(int64_t b, int64_t n, const block_s
   return b < c.init_blocks || b >= (z < 0 ? 0 : z);
 }
 
-// Packed fp32 pairs: each half is the scalar IEEE operation, rounded on its own.
+// Packed fp32 multiply: each half is the scalar IEEE product, rounded on its own.
 __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
+// acc + p, each half by a scalar rounded add.  A packed multiply feeding a
+// packed add comes out of code generation as one packed fused multiply-add
+// (measured: the same bits as an fma chain, with the rn modifiers, with
+// contraction switched off, and with the product written as fma(a, b, -0)),
+// which is not the page's order; with the adds scalar, every product and every
+// sum is rounded on its own (measured bit-identical to the sequential fp32 sum).
+__device__ __forceinline__ uint64_t f2_add_halves(uint64_t acc, uint64_t p) {
+  float a0, a1, p0, p1;
+  f2_unpack(acc, &a0, &a1);
+  f2_unpack(p, &p0, &p1);
+  return f2_pack(__fadd_rn(a0, p0), __fadd_rn(a1, p1));
 }
 __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
   const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);

@@ -1061,118 +1061,210 @@ __global__ void __launch_bounds__(32 * kBtWarps) bt_classify_kernel(BtProblem P,
 }
 
 // ------------------------------------------------------------ exact scores --
-constexpr int kBtExactThreads = 256;
-constexpr int kBtExactSmem = (128 * 128 + (kBtExactThreads / 32) * 128 * 4) * 4;
+// One CTA (4 warps) per key block b.  The listed pairs go in rounds of 32:
+//  1. one MMA (M = 128 positions of the block, N = 32 pairs, K = 128; the
+//     same scaled fp16 operands as the block-max pass) gives A_p for every
+//     position and pair, within e_b of the page's E_p;
+//  2. per pair, A1 = max_p A_p; a position with A_p < A1 - 2 e_b has
+//     E_p <= A_p + e_b < A1 - e_b <= E_p1 (p1 the position of A1), so the
+//     block's exact maximum is among the positions with A_p >= A1 - 2 e_b
+//     (usually one);
+//  3. those positions are scored in the page's order (one thread per
+//     (pair, position), products and sums rounded one by one) and the block
+//     score E_b = max replaces A_b in the pair's row as an ordered key.
+constexpr int kBtExactThreads = 128;
+constexpr int kBtXN = 32;                          // pairs per round (MMA N)
+constexpr int kBtXOffK = 0;                        // fp16 keys: 2 chunks x 128 rows x 128 B
+constexpr int kBtXOffQ = kBtXOffK + 2 * kBtChunkBytes;   // fp16 query rows: 2 chunks x 32 rows x 128 B
+constexpr int kBtXOffT = kBtXOffQ + 2 * kBtXN * 128;     // A_p transposed: [32 pairs][128 positions] fp32
+constexpr int kBtXOffL = kBtXOffT + kBtXN * 128 * 4;     // (pair, position) list: 32 x 128 uint16
+constexpr int kBtXOffM = kBtXOffL + kBtXN * 128 * 2;     // misc
+constexpr int kBtExactSmem = kBtXOffM + 512 + 1024;
 
-// One CTA per key block: its keys staged transposed ([d][key]), then each warp
-// takes four listed pairs at a time; lane l runs the page's chains of keys
-// 4l..4l+3 for all four (packed: two keys of one pair per instruction, each
-// half rounded as the scalar instruction rounds).  The exact block score
-// replaces A_b in the pair's row as an ordered key.
-__global__ void __launch_bounds__(kBtExactThreads) bt_exact_kernel(BtProblem P, BtWs W, block_select_stats* stats) {
-  extern __shared__ __align__(16) float kt[];
-  __shared__ float s_worst;
+__global__ void __launch_bounds__(kBtExactThreads)
+    bt_exact_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                    const BtProblem P, const BtWs W, block_select_stats* stats) {
+  extern __shared__ uint8_t smem_raw[];
   const int64_t b = blockIdx.x;
   const int cnt = W.icnt[b];
   if (cnt == 0) return;
-  const int t = threadIdx.x, wi = t >> 5, lane = t & 31;
-  const int64_t k0 = b * 128;
-  const int nk = (int)(P.L - k0 < 128 ? P.L - k0 : 128);
-  {
-    // transposed staging, every load in flight: lanes take consecutive keys of one 16-byte column
-    const float4* src = reinterpret_cast<const float4*>(P.k + k0 * 128);
-    const int n4 = nk * 32;
-    float4 v[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int i = t + kBtExactThreads * u;
-      v[u] = i < n4 ? __ldg(src + (i % nk) * 32 + i / nk) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int i = t + kBtExactThreads * u;
-      if (i < n4) {
-        const int key = i % nk, d4 = i / nk;
-        kt[(4 * d4 + 0) * 128 + key] = v[u].x;
-        kt[(4 * d4 + 1) * 128 + key] = v[u].y;
-        kt[(4 * d4 + 2) * 128 + key] = v[u].z;
-        kt[(4 * d4 + 3) * 128 + key] = v[u].w;
-      }
-    }
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint8_t* sK = smem + kBtXOffK;
+  uint8_t* sQ = smem + kBtXOffQ;
+  float* tr = reinterpret_cast<float*>(smem + kBtXOffT);
+  uint16_t* lst = reinterpret_cast<uint16_t*>(smem + kBtXOffL);
+  uint8_t* misc = smem + kBtXOffM;
+  uint64_t* tma_bar = reinterpret_cast<uint64_t*>(misc);
+  uint64_t* mma_bar = tma_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 20);
+  int* n_lst = reinterpret_cast<int*>(misc + 24);
+  float* s_worst = reinterpret_cast<float*>(misc + 28);
+  uint32_t* ekey = reinterpret_cast<uint32_t*>(misc + 64);     // [32] exact block score keys
+  float* scl = reinterpret_cast<float*>(misc + 192);            // [32] sigma s_b per pair of the round
+  int32_t* nvis = reinterpret_cast<int32_t*>(misc + 320);       // [32] visible positions of the block
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  if (t == 0) {
+    mbar_init(tma_bar, 1);
+    mbar_init(mma_bar, 1);
+    *abort_flag = 0;
+    *s_worst = 0.0f;
+    fence_mbar_init();
   }
-  if (t == 0) s_worst = 0.0f;
+  if (warp == 0) tmem_alloc(tmem_slot, 32);
+  tc_fence_before();
   __syncthreads();
-  float4* qs = reinterpret_cast<float4*>(kt + 128 * 128) + wi * 128;   // [d] = (q of the four pairs)
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int32_t* items = W.ilist + b * P.slots;
   const float2 kb = W.kb[b];
+  const float sb = W.ksc[b];
+  const int64_t k0 = b * 128;
   const float ninf = -__int_as_float(0x7f800000);
   float worst = 0.0f;
-  const int32_t* items = W.ilist + b * P.slots;
-  for (int ip = wi; 4 * ip < cnt; ip += kBtExactThreads / 32) {
-    const int i0 = 4 * ip;
-    const int nit = cnt - i0 < 4 ? cnt - i0 : 4;
-    int64_t sl[4], pr[4];
-    int64_t vis[4];
+  bool ok = true;
+  for (int base = 0, round = 0; base < cnt && ok; base += kBtXN, ++round) {
+    const int ni = cnt - base < kBtXN ? cnt - base : kBtXN;
+    // ---- operands: the block's keys once, 32 query rows per round (gather4, rows of absent pairs: row 0)
+    if (warp == 0) {
+      int32_t y[4] = {0, 0, 0, 0};
+      if (lane < kBtXN / 4) {
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      sl[it] = items[i0 + (it < nit ? it : 0)];
-      const int64_t qi = bt_slot_query(P, W, sl[it]);
-      pr[it] = qi * P.n_kv + sl[it] % P.n_kv;
-      const int64_t v = (int64_t)P.qpos[qi] + 1;
-      vis[it] = v < P.L ? v : P.L;
-    }
-    {
-      float4 x[4];
-#pragma unroll
-      for (int it = 0; it < 4; ++it) x[it] = __ldg(reinterpret_cast<const float4*>(P.q + pr[it] * 128) + lane);
-      qs[4 * lane + 0] = make_float4(x[0].x, x[1].x, x[2].x, x[3].x);
-      qs[4 * lane + 1] = make_float4(x[0].y, x[1].y, x[2].y, x[3].y);
-      qs[4 * lane + 2] = make_float4(x[0].z, x[1].z, x[2].z, x[3].z);
-      qs[4 * lane + 3] = make_float4(x[0].w, x[1].w, x[2].w, x[3].w);
-    }
-    __syncwarp();
-    uint64_t c[8];   // pair it: keys (4l, 4l+1) in c[2 it], (4l+2, 4l+3) in c[2 it + 1]
-#pragma unroll
-    for (int j = 0; j < 8; ++j) c[j] = 0ull;
-#pragma unroll 4
-    for (int d = 0; d < 128; ++d) {
-      const float4 kv = *reinterpret_cast<const float4*>(kt + d * 128 + 4 * lane);
-      const float4 qq = qs[d];
-      const uint64_t k01 = f2_pack(kv.x, kv.y), k23 = f2_pack(kv.z, kv.w);
-      const float qv[4] = {qq.x, qq.y, qq.z, qq.w};
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const uint64_t x = f2_pack(qv[it], qv[it]);
-        c[2 * it] = f2_add(c[2 * it], f2_mul(x, k01));
-        c[2 * it + 1] = f2_add(c[2 * it + 1], f2_mul(x, k23));
+        for (int i = 0; i < 4; ++i) {
+          const int j = 4 * lane + i;
+          if (j < ni) {
+            const int64_t sl = items[base + j];
+            y[i] = (int32_t)(bt_slot_query(P, W, sl) * P.n_kv + sl % P.n_kv);
+          }
+        }
       }
-    }
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      if (it >= nit) break;
-      const int nv = (int)(vis[it] - k0);   // >= 1 for a listed block
-      float e[4];
-      f2_unpack(c[2 * it], &e[0], &e[1]);
-      f2_unpack(c[2 * it + 1], &e[2], &e[3]);
-      float mx = ninf;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (4 * lane + j < nv) mx = fmaxf(mx, __fadd_rn(e[j], 0.0f));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
       if (lane == 0) {
-        uint32_t* cell = reinterpret_cast<uint32_t*>(W.amax) + sl[it] * P.nbm + b;
-        const float A = __uint_as_float(*cell);
-        const float eb = bt_bound(W.qab[pr[it]], kb);
-        if (eb > 0.0f) worst = fmaxf(worst, fabsf(A - mx) / eb);
-        *cell = score_key(mx);
+        mbar_arrive_expect_tx(tma_bar, (round == 0 ? 2 * kBtChunkBytes : 0) + 2 * kBtXN * 128);
+        if (round == 0) {
+          tma_load_2d(sK, &tmap_k, tma_bar, 0, (int32_t)k0);
+          tma_load_2d(sK + kBtChunkBytes, &tmap_k, tma_bar, 64, (int32_t)k0);
+        }
+      }
+      __syncwarp();
+      if (lane < kBtXN / 4) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          bt_gather4(sQ + c * (kBtXN * 128) + lane * 512, &tmap_q, tma_bar, 64 * c, y[0], y[1], y[2], y[3]);
       }
     }
-    __syncwarp();
+    // per pair of the round: scale, visible positions; exact keys start at the smallest key
+    if (t < kBtXN) {
+      ekey[t] = 0u;
+      if (t < ni) {
+        const int64_t sl = items[base + t];
+        const int64_t qi = bt_slot_query(P, W, sl);
+        scl[t] = W.qsig[qi * P.n_kv + sl % P.n_kv] * sb;
+        int64_t v = (int64_t)P.qpos[qi] + 1;
+        v = v < P.L ? v : P.L;
+        nvis[t] = (int32_t)(v - k0);
+      } else {
+        scl[t] = 0.0f;
+        nvis[t] = 0;
+      }
+    }
+    if (t == 0) *n_lst = 0;
+    // ---- MMA
+    if (t == 0) {
+      ok = mbar_wait(tma_bar, round & 1, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        constexpr uint32_t idesc = idesc_f16(128, kBtXN, 0u);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t a0 = smem_u32(sK + c * kBtChunkBytes), b0 = smem_u32(sQ + c * (kBtXN * 128));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_f16(tmem_base, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
+                       (c | kk) ? 1u : 0u);
+        }
+        tc_commit(mma_bar);
+      }
+    }
+    __syncthreads();
+    const bool got = mbar_wait(mma_bar, round & 1, abort_flag);
+    if (!__syncthreads_and(got)) {   // every thread leaves together
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    // ---- A_p for this thread's position p = t and the 32 pairs, transposed to [pair][position]
+    {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(warp * 32) << 16), v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < kBtXN; ++j) tr[j * 128 + t] = t < nvis[j] ? __uint_as_float(v[j]) * scl[j] : ninf;
+    }
+    tc_fence_before();
+    __syncthreads();
+    // ---- per pair: A1, the threshold, the candidate positions
+    for (int j = warp; j < ni; j += kBtExactThreads / 32) {
+      const float4 a4 = *reinterpret_cast<const float4*>(tr + j * 128 + 4 * lane);
+      float m = fmaxf(fmaxf(a4.x, a4.y), fmaxf(a4.z, a4.w));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      const int64_t sl = items[base + j];
+      const int64_t pr = bt_slot_query(P, W, sl) * P.n_kv + sl % P.n_kv;
+      const float eb = bt_bound(W.qab[pr], kb);
+      const float thr = __fsub_rd(m, __fmul_ru(2.0f, eb));
+      const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (av[i] >= thr) {
+          const int pos = atomicAdd(n_lst, 1);
+          lst[pos] = (uint16_t)((j << 7) | (4 * lane + i));
+        }
+      }
+    }
+    __syncthreads();
+    // ---- the candidates in the page's order
+    const int nl = *n_lst;
+    for (int i = t; i < nl; i += kBtExactThreads) {
+      const int j = lst[i] >> 7, p = lst[i] & 127;
+      const int64_t sl = items[base + j];
+      const int64_t pr = bt_slot_query(P, W, sl) * P.n_kv + sl % P.n_kv;
+      const float4* qr = reinterpret_cast<const float4*>(P.q + pr * 128);
+      const float4* kr = reinterpret_cast<const float4*>(P.k + (k0 + p) * 128);
+      float acc = 0.0f;
+#pragma unroll 8
+      for (int d4 = 0; d4 < 32; ++d4) {
+        const float4 x = __ldg(qr + d4), y = __ldg(kr + d4);
+        acc = __fadd_rn(acc, __fmul_rn(x.x, y.x));
+        acc = __fadd_rn(acc, __fmul_rn(x.y, y.y));
+        acc = __fadd_rn(acc, __fmul_rn(x.z, y.z));
+        acc = __fadd_rn(acc, __fmul_rn(x.w, y.w));
+      }
+      atomicMax(&ekey[j], score_key(acc));   // score_key folds -0 onto +0
+    }
+    __syncthreads();
+    if (t < ni) {
+      const int64_t sl = items[base + t];
+      const int64_t pr = bt_slot_query(P, W, sl) * P.n_kv + sl % P.n_kv;
+      uint32_t* cell = reinterpret_cast<uint32_t*>(W.amax) + sl * P.nbm + b;
+      const float A = __uint_as_float(*cell);
+      const float E = key_score(ekey[t]);
+      const float eb = bt_bound(W.qab[pr], kb);
+      if (eb > 0.0f) worst = fmaxf(worst, fabsf(A - E) / eb);
+      *cell = ekey[t];
+    }
+    __syncthreads();
   }
-  if (lane == 0 && worst > 0.0f) atomicMax(reinterpret_cast<int*>(&s_worst), __float_as_int(worst));
+  if (worst > 0.0f) atomicMax(reinterpret_cast<int*>(s_worst), __float_as_int(worst));
+  tc_fence_before();
   __syncthreads();
-  if (t == 0 && stats && s_worst > 0.0f)
-    atomicMax(reinterpret_cast<int*>(&stats->max_bound_use), __float_as_int(s_worst));
+  if (t == 0 && stats && *s_worst > 0.0f)
+    atomicMax(reinterpret_cast<int*>(&stats->max_bound_use), __float_as_int(*s_worst));
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 32);
+  }
 }
 
 // ---------------------------------------------------------------- resolve --
@@ -1296,8 +1388,8 @@ cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t
     bt_prep_kernel<<<(unsigned)g, kBtPrepThreads, 0, st>>>(P, W);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  CUtensorMap tk, tq;
   if (P.nbm > 0) {
-    CUtensorMap tk, tq;
     bool ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W.k16, 128, (uint64_t)L, 256, 64, 128);
     ok = ok && make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W.q16, 128, (uint64_t)P.slots, 256, 64, 1);
     if (!ok) return cudaErrorInvalidValue;
@@ -1314,7 +1406,7 @@ cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t
     if ((e = cudaFuncSetAttribute(bt_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBtExactSmem)) !=
         cudaSuccess)
       return e;
-    bt_exact_kernel<<<(unsigned)P.nbm, kBtExactThreads, kBtExactSmem, st>>>(P, W, stats);
+    bt_exact_kernel<<<(unsigned)P.nbm, kBtExactThreads, kBtExactSmem, st>>>(tk, tq, P, W, stats);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   bt_resolve_kernel<<<gp, 32 * kBtWarps, 0, st>>>(P, W, out, out_width, out_count);

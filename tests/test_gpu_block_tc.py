@@ -150,3 +150,20 @@ def test_tc_route_workload_stats(B):
     o2, c2 = _run(B, bp.index_q, bp.index_k, bp.query_pos, bp.top_blocks, bp.init_blocks, bp.local_blocks,
                   static=True)
     assert np.array_equal(o, o2) and np.array_equal(c, c2)
+
+
+def test_page_order_one_ulp_tie_both_routes(B):
+    """Query 815, head 4 of the MiniMax workload: blocks 548 and 156 score
+    41.377743 and 41.37774 in the page's sequential fp32 sum (one ulp apart),
+    and a fused multiply-add chain swaps them.  Both routes must keep the
+    page's order (products and sums rounded one by one)."""
+    bp = wl.block_select()
+    sc = obs.block_scores(bp.index_q[815, 4], bp.index_k, int(bp.query_pos[815]), 128)
+    assert np.float32(sc[548]).view(np.int32) - np.float32(sc[156]).view(np.int32) == 1
+    q = bp.index_q[815:816]
+    pos = bp.query_pos[815:816]
+    ref = obs.block_sparse_select(q[0], bp.index_k, int(pos[0]), 128, 32, 1, 2)
+    assert 548 in ref[4] and 156 not in ref[4]
+    for static in (False, True):
+        o, c = _run(B, q, bp.index_k, pos, 32, 1, 2, static=static)
+        assert _lists(o, c)[0] == ref, "static" if static else "tensor"
