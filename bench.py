@@ -151,6 +151,9 @@ LARGE_INPUTS = ("decode", "ragged_fp8")
 # capture of a smaller batch of the same workload, scaled by the keys processed (traffic grows
 # in proportion).  Valid for the kernel as built with this file; None where not captured.
 SCORE_TRAFFIC = {"decode": 549.9e6, "ragged_fp8": 1158.7e6}
+# the same counters for one bt_max_kernel launch on the full block_select workload (one
+# ncu capture of the kernel as built with this file; the fp16 keys, 33.5 MB, dominate)
+BLOCK_MAX_TRAFFIC = 37.77e6
 
 WORKLOAD_TEXT = {
     "decode": "decode indexer bf16: 64 rows x 32768 own keys, H32 D128, top-2048, witness_merge S=16 (5% padding)",
@@ -281,22 +284,34 @@ class BlockSelectStep:
         self.cnt = torch.empty((Q, n_kv), dtype=torch.int32, device=dev)
         self.ws = torch.empty(B.block_select_workspace_size(Q, n_kv, bp.index_k.shape[0], self.cfg),
                               dtype=torch.uint8, device=dev)
-        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        self.score_ms = []
-        self.launches = 2
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        self.score_ms = []          # the block-maxima kernel (bt_max_kernel)
+        self.phase_ms = {k: [] for k in self.PHASES}
+        self.launches = 5           # prep, block maxima, classify, rescoring, resolve
+
+    PHASES = ("prep", "block_max", "classify", "rescore", "resolve")
 
     def run(self, timed=False):
         if timed:
-            self.ev[0].record()
-        self.B.block_select(self.q, self.k, self.pos, self.cfg, self.out, self.cnt, self.ws)
-        if timed:
-            self.ev[1].record()
+            # events between the kernels, recorded by the library on the current stream
+            self.B.block_select_events(self.q, self.k, self.pos, self.cfg, self.out, self.cnt, self.ws, self.ev,
+                                       stream=torch.cuda.current_stream())
+        else:
+            self.B.block_select(self.q, self.k, self.pos, self.cfg, self.out, self.cnt, self.ws)
 
     def collect(self):
-        self.score_ms.append(self.ev[0].elapsed_time(self.ev[1]))
+        for i, k in enumerate(self.PHASES):
+            self.phase_ms[k].append(self.ev[i].elapsed_time(self.ev[i + 1]))
+        self.score_ms.append(self.phase_ms["block_max"][-1])
 
     def step_ms(self):
-        return self.ev[0].elapsed_time(self.ev[1])
+        return self.ev[0].elapsed_time(self.ev[5])
+
+    def bound_stats(self):
+        st = self.B.block_select_stats_tensor()
+        self.B.block_select(self.q, self.k, self.pos, self.cfg, self.out, self.cnt, self.ws, stats=st)
+        torch.cuda.synchronize()
+        return self.B.block_select_stats_read(st)
 
     def pairs(self):
         bs = self.bp.block_size
@@ -461,7 +476,7 @@ def main():
         t_end = torch.cuda.Event(enable_timing=True)
         # one event pair per step around the dominant kernel, on the launching stream
         # (created and recorded once here, so no event is created inside the timed region)
-        per_step = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        per_step = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
         for evs in per_step + [[t_start, t_end]]:
             for e in evs:
                 e.record(stream)
@@ -509,17 +524,18 @@ def main():
                     "algorithmic_bytes": step.algorithmic_bytes()}
     elif isinstance(step, BlockSelectStep):
         k_ms = statistics.median(kernel_ms)
-        # fp32 ALU: a separately rounded multiply and add per multiply-add (no FMA, the
-        # page's order); the fp32 pipes retire 2 such operations per lane per clock
-        # with the packed f32x2 instructions: 152 SMs x 128 lanes x 2 x clock
-        macs = step.pairs() * wp.index_q.shape[2]
-        sm_mhz = clock_info.get("sm_mhz") or 2070.0
-        peak_alu = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
-        ach = 2.0 * macs / (k_ms * 1e-3) / 1e12
-        roof = {"kernel": "block_score128_kernel + block_pick_kernel", "bound": "alu", "achieved": ach,
-                "peak": peak_alu, "unit": "T fp32 ops/s", "frac": ach / peak_alu, "traffic": None,
-                "peak_source": "152 SMs x 128 fp32 lanes x 2 (packed f32x2) x median SM clock",
-                "kernel_ms": k_ms}
+        # the block maxima on the tensor cores: one multiply-add per visible (query, head,
+        # position) and dimension (fp16 operands, fp32 accumulate; the fp16 dense rate is
+        # the bf16 rate)
+        flops = 2.0 * step.pairs() * wp.index_q.shape[2]
+        ach = flops / (k_ms * 1e-3) / 1e12
+        roof = {"kernel": "bt_max_kernel", "bound": "tensor", "achieved": ach, "peak": bf16, "unit": "TFLOP/s",
+                "frac": ach / bf16, "traffic": BLOCK_MAX_TRAFFIC if not args.rows else None,
+                "peak_source": f"{peak_src} bf16 burst (fp16 = bf16 rate)", "kernel_ms": k_ms,
+                "algorithmic_flops": flops,
+                "phases_ms": {k: statistics.median(v) for k, v in step.phase_ms.items()}}
+        with torch.cuda.stream(stream):
+            roof["bound_stats"] = step.bound_stats()
     else:
         k_ms = statistics.median(kernel_ms)
         roof = {"kernel": "dosa_topk (all kernels)", "bound": "tensor", "achieved": None, "peak": bf16,

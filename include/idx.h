@@ -256,6 +256,17 @@ idx_status block_select(const float* index_q, const float* index_k, const int32_
                         int32_t out_width, int32_t* out_count, block_select_stats* stats, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* block_select, recording CUDA events (cudaEvent_t handles, host array of
+ * n_events >= 6, each created by the caller) on `stream` between its kernels,
+ * for profiling: events[0] before the first kernel; on the tensor-core route
+ * events[1..5] after the prep, block-maxima, classify, rescoring and resolve
+ * kernels; on the CUDA-core route only events[0] and events[5].  Same
+ * arguments and result as block_select otherwise. */
+idx_status block_select_events(const float* index_q, const float* index_k, const int32_t* query_pos, int64_t Q,
+                               int32_t n_kv, int32_t D, int64_t L, const block_sparse_config* cfg, int32_t* out,
+                               int32_t out_width, int32_t* out_count, block_select_stats* stats, void* ws,
+                               size_t ws_bytes, void* const* events, int32_t n_events, void* stream);
+
 /* ------------------------------------------------------ block_select_static
  * block_select for callers that cannot allocate device memory: code that runs
  * inside a host framework which owns every device allocation (and offers no

@@ -108,6 +108,11 @@ EXPORTS = {
                                       ctypes.POINTER(block_sparse_config), ctypes.c_void_p, ctypes.c_int32,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                       ctypes.c_void_p]),
+    "block_select_events": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                             ctypes.POINTER(block_sparse_config), ctypes.c_void_p, ctypes.c_int32,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                             ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
     "block_select_static": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                              ctypes.POINTER(block_sparse_config), ctypes.c_void_p, ctypes.c_int32,
@@ -268,6 +273,21 @@ def block_select(index_q: torch.Tensor, index_k: torch.Tensor, query_pos: torch.
     _check(lib().block_select(_ptr(index_q), _ptr(index_k), _ptr(query_pos), Q, n_kv, D, L, ctypes.byref(cfg),
                               _ptr(out), out.shape[-1], _ptr(out_count), _ptr(stats), _ptr(ws), ws_bytes,
                               _stream(stream)))
+    return out, out_count
+
+
+def block_select_events(index_q: torch.Tensor, index_k: torch.Tensor, query_pos: torch.Tensor,
+                        cfg: block_sparse_config, out: torch.Tensor, out_count: Optional[torch.Tensor],
+                        ws: Optional[torch.Tensor], events, stream=None, stats: Optional[torch.Tensor] = None):
+    """block_select recording 6 torch.cuda.Event (already created: recorded once)
+    between its kernels on `stream` (profiling)."""
+    Q, n_kv, D = index_q.shape
+    L = index_k.shape[0]
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    handles = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events[:6]])
+    _check(lib().block_select_events(_ptr(index_q), _ptr(index_k), _ptr(query_pos), Q, n_kv, D, L, ctypes.byref(cfg),
+                                     _ptr(out), out.shape[-1], _ptr(out_count), _ptr(stats), _ptr(ws), ws_bytes,
+                                     handles, 6, _stream(stream)))
     return out, out_count
 
 

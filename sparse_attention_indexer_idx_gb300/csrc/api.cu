@@ -213,10 +213,10 @@ size_t block_select_workspace_size(int64_t Q, int32_t n_kv, int64_t L, const blo
   return block_select_ws(Q, n_kv, L, *cfg);
 }
 
-idx_status block_select(const float* index_q, const float* index_k, const int32_t* query_pos, int64_t Q,
-                        int32_t n_kv, int32_t D, int64_t L, const block_sparse_config* cfg, int32_t* out,
-                        int32_t out_width, int32_t* out_count, block_select_stats* stats, void* ws,
-                        size_t ws_bytes, void* stream) {
+static idx_status block_select_impl(const float* index_q, const float* index_k, const int32_t* query_pos, int64_t Q,
+                                    int32_t n_kv, int32_t D, int64_t L, const block_sparse_config* cfg, int32_t* out,
+                                    int32_t out_width, int32_t* out_count, block_select_stats* stats, void* ws,
+                                    size_t ws_bytes, void* stream, const cudaEvent_t* ev) {
   if (!cfg) return fail(IDX_ERR_INVALID_ARG, "config is NULL");
   if (Q < 0 || n_kv < 0 || D <= 0 || L < 0 || cfg->block_size < 0 || cfg->top_blocks < 0 || cfg->init_blocks < 0 ||
       cfg->local_blocks < 0)
@@ -236,8 +236,27 @@ idx_status block_select(const float* index_q, const float* index_k, const int32_
     return fail(IDX_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
   if (block_select_workspace_size(Q, n_kv, L, cfg) > 0 && !ws) return fail(IDX_ERR_INVALID_ARG, "workspace is NULL");
   return cuda_status(launch_block_select(index_q, index_k, query_pos, Q, n_kv, D, L, *cfg, out, out_width, out_count,
-                                         ws, (cudaStream_t)stream, stats, true),
+                                         ws, (cudaStream_t)stream, stats, true, ev),
                      "block_select");
+}
+
+idx_status block_select(const float* index_q, const float* index_k, const int32_t* query_pos, int64_t Q,
+                        int32_t n_kv, int32_t D, int64_t L, const block_sparse_config* cfg, int32_t* out,
+                        int32_t out_width, int32_t* out_count, block_select_stats* stats, void* ws,
+                        size_t ws_bytes, void* stream) {
+  return block_select_impl(index_q, index_k, query_pos, Q, n_kv, D, L, cfg, out, out_width, out_count, stats, ws,
+                           ws_bytes, stream, nullptr);
+}
+
+idx_status block_select_events(const float* index_q, const float* index_k, const int32_t* query_pos, int64_t Q,
+                               int32_t n_kv, int32_t D, int64_t L, const block_sparse_config* cfg, int32_t* out,
+                               int32_t out_width, int32_t* out_count, block_select_stats* stats, void* ws,
+                               size_t ws_bytes, void* const* events, int32_t n_events, void* stream) {
+  if (!events || n_events < 6) return fail(IDX_ERR_INVALID_ARG, "block_select_events needs 6 events");
+  cudaEvent_t ev[6];
+  for (int i = 0; i < 6; ++i) ev[i] = (cudaEvent_t)events[i];
+  return block_select_impl(index_q, index_k, query_pos, Q, n_kv, D, L, cfg, out, out_width, out_count, stats, ws,
+                           ws_bytes, stream, ev);
 }
 
 }  // extern "C"

@@ -266,14 +266,16 @@ size_t block_select_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config
 cudaError_t launch_block_select(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv, int D,
                                 int64_t L, const block_sparse_config& c, int32_t* out, int out_width,
                                 int32_t* out_count, void* ws, cudaStream_t st, block_select_stats* stats,
-                                bool tensor_route) {
+                                bool tensor_route, const cudaEvent_t* ev) {
   const int64_t pairs = Q * n_kv;
   if (pairs <= 0) return cudaSuccess;
   if (tensor_route && block_select_tc_applies(D, c, Q, n_kv, L))
-    return launch_block_select_tc(q, k, pos, Q, n_kv, L, c, out, out_width, out_count, ws, stats, st);
+    return launch_block_select_tc(q, k, pos, Q, n_kv, L, c, out, out_width, out_count, ws, stats, st, ev);
+  cudaError_t e;
+  // CUDA-core route: events 0 and 5 only (before and after)
+  if (ev && ev[0] && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return e;
   const int64_t nbm = c.block_size > 0 ? (L + c.block_size - 1) / c.block_size : 0;
   uint32_t* bkey = (uint32_t*)ws;
-  cudaError_t e;
   if (nbm > 0) {
     dim3 grid((unsigned)((pairs + kBsThreads - 1) / kBsThreads), (unsigned)(nbm < 65535 ? nbm : 65535));
     if (D == 128) {
@@ -301,7 +303,9 @@ cudaError_t launch_block_select(const float* q, const float* k, const int32_t* p
   if (e != cudaSuccess) return e;
   block_pick_kernel<<<(unsigned)pairs, kPickThreads, smem, st>>>(pos, Q, n_kv, L, c, nbm, bkey, out, out_width,
                                                                 out_count);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess && ev && ev[5]) e = cudaEventRecord(ev[5], st);
+  return e;
 }
 
 }  // namespace idx

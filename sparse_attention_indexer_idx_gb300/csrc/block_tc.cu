@@ -1079,7 +1079,7 @@ constexpr int kBtXOffQ = kBtXOffK + 2 * kBtChunkBytes;   // fp16 query rows: 2 c
 constexpr int kBtXOffT = kBtXOffQ + 2 * kBtXN * 128;     // A_p transposed: [32 pairs][128 positions] fp32
 constexpr int kBtXOffL = kBtXOffT + kBtXN * 128 * 4;     // (pair, position) list: 32 x 128 uint16
 constexpr int kBtXOffM = kBtXOffL + kBtXN * 128 * 2;     // misc
-constexpr int kBtExactSmem = kBtXOffM + 512 + 1024;
+constexpr int kBtExactSmem = kBtXOffM + 1024 + 1024;
 
 __global__ void __launch_bounds__(kBtExactThreads)
     bt_exact_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
@@ -1095,22 +1095,33 @@ __global__ void __launch_bounds__(kBtExactThreads)
   float* tr = reinterpret_cast<float*>(smem + kBtXOffT);
   uint16_t* lst = reinterpret_cast<uint16_t*>(smem + kBtXOffL);
   uint8_t* misc = smem + kBtXOffM;
-  uint64_t* tma_bar = reinterpret_cast<uint64_t*>(misc);
-  uint64_t* mma_bar = tma_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 20);
-  int* n_lst = reinterpret_cast<int*>(misc + 24);
-  float* s_worst = reinterpret_cast<float*>(misc + 28);
-  uint32_t* ekey = reinterpret_cast<uint32_t*>(misc + 64);     // [32] exact block score keys
-  float* scl = reinterpret_cast<float*>(misc + 192);            // [32] sigma s_b per pair of the round
-  int32_t* nvis = reinterpret_cast<int32_t*>(misc + 320);       // [32] visible positions of the block
+  uint64_t* k_bar = reinterpret_cast<uint64_t*>(misc);
+  uint64_t* q_bar = k_bar + 1;
+  uint64_t* mma_bar = k_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 32);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 36);
+  int* n_lst = reinterpret_cast<int*>(misc + 40);
+  float* s_worst = reinterpret_cast<float*>(misc + 44);
+  // per pair of the round
+  uint32_t* ekey = reinterpret_cast<uint32_t*>(misc + 64);      // exact block score key
+  float* scl = reinterpret_cast<float*>(misc + 192);             // sigma s_b
+  int32_t* nvis = reinterpret_cast<int32_t*>(misc + 320);        // visible positions of the block
+  int32_t* slot_of = reinterpret_cast<int32_t*>(misc + 448);     // slot
+  int32_t* pair_of = reinterpret_cast<int32_t*>(misc + 576);     // pair (row of index_q, q16, qab)
+  float* eb_of = reinterpret_cast<float*>(misc + 704);           // e_b
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int64_t k0 = b * 128;
   if (t == 0) {
-    mbar_init(tma_bar, 1);
+    mbar_init(k_bar, 1);
+    mbar_init(q_bar, 1);
     mbar_init(mma_bar, 1);
     *abort_flag = 0;
     *s_worst = 0.0f;
     fence_mbar_init();
+    // the block's fp16 keys, needed by every round
+    mbar_arrive_expect_tx(k_bar, 2 * kBtChunkBytes);
+    tma_load_2d(sK, &tmap_k, k_bar, 0, (int32_t)k0);
+    tma_load_2d(sK + kBtChunkBytes, &tmap_k, k_bar, 64, (int32_t)k0);
   }
   if (warp == 0) tmem_alloc(tmem_slot, 32);
   tc_fence_before();
@@ -1120,80 +1131,66 @@ __global__ void __launch_bounds__(kBtExactThreads)
   const int32_t* items = W.ilist + b * P.slots;
   const float2 kb = W.kb[b];
   const float sb = W.ksc[b];
-  const int64_t k0 = b * 128;
   const float ninf = -__int_as_float(0x7f800000);
   float worst = 0.0f;
-  bool ok = true;
-  for (int base = 0, round = 0; base < cnt && ok; base += kBtXN, ++round) {
+  for (int base = 0, round = 0; base < cnt; base += kBtXN, ++round) {
     const int ni = cnt - base < kBtXN ? cnt - base : kBtXN;
-    // ---- operands: the block's keys once, 32 query rows per round (gather4, rows of absent pairs: row 0)
-    if (warp == 0) {
-      int32_t y[4] = {0, 0, 0, 0};
-      if (lane < kBtXN / 4) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j = 4 * lane + i;
-          if (j < ni) {
-            const int64_t sl = items[base + j];
-            y[i] = (int32_t)(bt_slot_query(P, W, sl) * P.n_kv + sl % P.n_kv);
-          }
-        }
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(tma_bar, (round == 0 ? 2 * kBtChunkBytes : 0) + 2 * kBtXN * 128);
-        if (round == 0) {
-          tma_load_2d(sK, &tmap_k, tma_bar, 0, (int32_t)k0);
-          tma_load_2d(sK + kBtChunkBytes, &tmap_k, tma_bar, 64, (int32_t)k0);
-        }
-      }
-      __syncwarp();
-      if (lane < kBtXN / 4) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          bt_gather4(sQ + c * (kBtXN * 128) + lane * 512, &tmap_q, tma_bar, 64 * c, y[0], y[1], y[2], y[3]);
-      }
-    }
-    // per pair of the round: scale, visible positions; exact keys start at the smallest key
+    // ---- the round's pairs, looked up once
     if (t < kBtXN) {
       ekey[t] = 0u;
       if (t < ni) {
         const int64_t sl = items[base + t];
         const int64_t qi = bt_slot_query(P, W, sl);
-        scl[t] = W.qsig[qi * P.n_kv + sl % P.n_kv] * sb;
+        const int64_t pr = qi * P.n_kv + sl % P.n_kv;
         int64_t v = (int64_t)P.qpos[qi] + 1;
         v = v < P.L ? v : P.L;
+        slot_of[t] = (int32_t)sl;
+        pair_of[t] = (int32_t)pr;
         nvis[t] = (int32_t)(v - k0);
+        scl[t] = W.qsig[pr] * sb;
+        eb_of[t] = bt_bound(W.qab[pr], kb);
       } else {
-        scl[t] = 0.0f;
+        slot_of[t] = -1;
+        pair_of[t] = 0;   // gathered but unused
         nvis[t] = 0;
+        scl[t] = 0.0f;
+        eb_of[t] = 0.0f;
       }
     }
     if (t == 0) *n_lst = 0;
-    // ---- MMA
-    if (t == 0) {
-      ok = mbar_wait(tma_bar, round & 1, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        constexpr uint32_t idesc = idesc_f16(128, kBtXN, 0u);
+    __syncthreads();
+    // ---- operands and the MMA (one thread)
+    if (warp == 0) {
+      if (lane == 0) mbar_arrive_expect_tx(q_bar, 2 * kBtXN * 128);
+      __syncwarp();
+      if (lane < kBtXN / 4) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t a0 = smem_u32(sK + c * kBtChunkBytes), b0 = smem_u32(sQ + c * (kBtXN * 128));
+        for (int c = 0; c < 2; ++c)
+          bt_gather4(sQ + c * (kBtXN * 128) + lane * 512, &tmap_q, q_bar, 64 * c, pair_of[4 * lane],
+                     pair_of[4 * lane + 1], pair_of[4 * lane + 2], pair_of[4 * lane + 3]);
+      }
+      if (lane == 0) {
+        bool ok = round > 0 || mbar_wait(k_bar, 0, abort_flag);
+        ok = ok && mbar_wait(q_bar, round & 1, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          constexpr uint32_t idesc = idesc_f16(128, kBtXN, 0u);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_f16(tmem_base, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
-                       (c | kk) ? 1u : 0u);
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t a0 = smem_u32(sK + c * kBtChunkBytes), b0 = smem_u32(sQ + c * (kBtXN * 128));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_f16(tmem_base, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
+                         (c | kk) ? 1u : 0u);
+          }
+          tc_commit(mma_bar);
         }
-        tc_commit(mma_bar);
       }
     }
-    __syncthreads();
     const bool got = mbar_wait(mma_bar, round & 1, abort_flag);
-    if (!__syncthreads_and(got)) {   // every thread leaves together
-      ok = false;
-      break;
-    }
+    if (!__syncthreads_and(got)) break;   // every thread leaves together
     tc_fence_after();
-    // ---- A_p for this thread's position p = t and the 32 pairs, transposed to [pair][position]
+    // ---- A_p for this thread's position p = t and the round's pairs, transposed to [pair][position]
     {
       uint32_t v[32];
       tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(warp * 32) << 16), v);
@@ -1209,10 +1206,7 @@ __global__ void __launch_bounds__(kBtExactThreads)
       float m = fmaxf(fmaxf(a4.x, a4.y), fmaxf(a4.z, a4.w));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-      const int64_t sl = items[base + j];
-      const int64_t pr = bt_slot_query(P, W, sl) * P.n_kv + sl % P.n_kv;
-      const float eb = bt_bound(W.qab[pr], kb);
-      const float thr = __fsub_rd(m, __fmul_ru(2.0f, eb));
+      const float thr = __fsub_rd(m, __fmul_ru(2.0f, eb_of[j]));
       const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -1223,34 +1217,38 @@ __global__ void __launch_bounds__(kBtExactThreads)
       }
     }
     __syncthreads();
-    // ---- the candidates in the page's order
+    // ---- the candidates in the page's order: one thread each, rows loaded 16 x 16 bytes at a time
     const int nl = *n_lst;
     for (int i = t; i < nl; i += kBtExactThreads) {
       const int j = lst[i] >> 7, p = lst[i] & 127;
-      const int64_t sl = items[base + j];
-      const int64_t pr = bt_slot_query(P, W, sl) * P.n_kv + sl % P.n_kv;
-      const float4* qr = reinterpret_cast<const float4*>(P.q + pr * 128);
+      const float4* qr = reinterpret_cast<const float4*>(P.q + (int64_t)pair_of[j] * 128);
       const float4* kr = reinterpret_cast<const float4*>(P.k + (k0 + p) * 128);
       float acc = 0.0f;
-#pragma unroll 8
-      for (int d4 = 0; d4 < 32; ++d4) {
-        const float4 x = __ldg(qr + d4), y = __ldg(kr + d4);
-        acc = __fadd_rn(acc, __fmul_rn(x.x, y.x));
-        acc = __fadd_rn(acc, __fmul_rn(x.y, y.y));
-        acc = __fadd_rn(acc, __fmul_rn(x.z, y.z));
-        acc = __fadd_rn(acc, __fmul_rn(x.w, y.w));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float4 x[16], y[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          x[u] = __ldg(qr + 16 * h + u);
+          y[u] = __ldg(kr + 16 * h + u);
+        }
+        asm volatile("" ::: "memory");   // all 32 loads issued before the serial sum consumes them
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          acc = __fadd_rn(acc, __fmul_rn(x[u].x, y[u].x));
+          acc = __fadd_rn(acc, __fmul_rn(x[u].y, y[u].y));
+          acc = __fadd_rn(acc, __fmul_rn(x[u].z, y[u].z));
+          acc = __fadd_rn(acc, __fmul_rn(x[u].w, y[u].w));
+        }
       }
       atomicMax(&ekey[j], score_key(acc));   // score_key folds -0 onto +0
     }
     __syncthreads();
     if (t < ni) {
-      const int64_t sl = items[base + t];
-      const int64_t pr = bt_slot_query(P, W, sl) * P.n_kv + sl % P.n_kv;
-      uint32_t* cell = reinterpret_cast<uint32_t*>(W.amax) + sl * P.nbm + b;
+      uint32_t* cell = reinterpret_cast<uint32_t*>(W.amax) + (int64_t)slot_of[t] * P.nbm + b;
       const float A = __uint_as_float(*cell);
       const float E = key_score(ekey[t]);
-      const float eb = bt_bound(W.qab[pr], kb);
-      if (eb > 0.0f) worst = fmaxf(worst, fabsf(A - E) / eb);
+      if (eb_of[t] > 0.0f) worst = fmaxf(worst, fabsf(A - E) / eb_of[t]);
       *cell = ekey[t];
     }
     __syncthreads();
@@ -1378,16 +1376,21 @@ size_t block_select_tc_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_con
 
 cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv,
                                    int64_t L, const block_sparse_config& c, int32_t* out, int out_width,
-                                   int32_t* out_count, void* ws, block_select_stats* stats, cudaStream_t st) {
+                                   int32_t* out_count, void* ws, block_select_stats* stats, cudaStream_t st,
+                                   const cudaEvent_t* ev) {
   const BtProblem P = bt_problem(q, k, pos, Q, n_kv, L, c);
   if (P.slots <= 0) return cudaSuccess;
   const BtWs W = bt_carve(ws, P);
   cudaError_t e;
+  // ev (optional, 6 events): before prep, then after each of the five kernels
+  auto mark = [&](int i) { return ev && ev[i] ? cudaEventRecord(ev[i], st) : cudaSuccess; };
+  if ((e = mark(0)) != cudaSuccess) return e;
   {
     const int64_t g = 1 + P.nbm + (P.slots + 31) / 32;
     bt_prep_kernel<<<(unsigned)g, kBtPrepThreads, 0, st>>>(P, W);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if ((e = mark(1)) != cudaSuccess) return e;
   CUtensorMap tk, tq;
   if (P.nbm > 0) {
     bool ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W.k16, 128, (uint64_t)L, 256, 64, 128);
@@ -1399,9 +1402,11 @@ cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t
     bt_max_kernel<<<sm_count(), kBtThreads, kBtSmem, st>>>(tk, tq, P, W);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if ((e = mark(2)) != cudaSuccess) return e;
   const unsigned gp = (unsigned)((P.slots + kBtWarps - 1) / kBtWarps);
   bt_classify_kernel<<<gp, 32 * kBtWarps, 0, st>>>(P, W, out, out_width, out_count, stats);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = mark(3)) != cudaSuccess) return e;
   if (P.nbm > 0) {
     if ((e = cudaFuncSetAttribute(bt_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBtExactSmem)) !=
         cudaSuccess)
@@ -1409,8 +1414,10 @@ cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t
     bt_exact_kernel<<<(unsigned)P.nbm, kBtExactThreads, kBtExactSmem, st>>>(tk, tq, P, W, stats);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if ((e = mark(4)) != cudaSuccess) return e;
   bt_resolve_kernel<<<gp, 32 * kBtWarps, 0, st>>>(P, W, out, out_width, out_count);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return mark(5);
 }
 
 }  // namespace idx

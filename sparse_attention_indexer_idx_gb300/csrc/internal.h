@@ -71,12 +71,13 @@ size_t block_select_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config
 cudaError_t launch_block_select(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv, int D,
                                 int64_t L, const block_sparse_config& c, int32_t* out, int out_width,
                                 int32_t* out_count, void* ws, cudaStream_t st, block_select_stats* stats,
-                                bool tensor_route);
+                                bool tensor_route, const cudaEvent_t* ev = nullptr);
 bool block_select_tc_applies(int D, const block_sparse_config& c, int64_t Q, int n_kv, int64_t L);
 size_t block_select_tc_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c);
 cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv,
                                    int64_t L, const block_sparse_config& c, int32_t* out, int out_width,
-                                   int32_t* out_count, void* ws, block_select_stats* stats, cudaStream_t st);
+                                   int32_t* out_count, void* ws, block_select_stats* stats, cudaStream_t st,
+                                   const cudaEvent_t* ev = nullptr);
 
 size_t dosa_ws(const idx_problem& p, int K, const dosa_params& dp, int seed_ld);
 cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, const int32_t* seed_ids, int seed_ld,

@@ -69,3 +69,19 @@ def test_block_select_refusals_before_launch(L):
     assert L.block_select(one, one, one, 4, 2, 128, 1024, ctypes.byref(bad), one, 32, nul, nul, one, 1 << 20, nul) == 4
     assert L.block_select(one, one, one, 4, 2, 128, 1024, ctypes.byref(cfg), one, 32, nul, nul, one, 0, nul) == 6
     assert L.block_select_workspace_size(4, 2, 1024, ctypes.byref(cfg)) >= 4 * 2 * 8 * 4
+
+
+def test_block_select_events_refusals(L):
+    from sparse_attention_indexer_idx_gb300 import binding as B
+    nul = ctypes.c_void_p(0)
+    cfg = B.block_sparse_config(128, 32, 1, 2)
+    one = ctypes.c_void_p(256)
+    ev = (ctypes.c_void_p * 6)()
+    # fewer than 6 events, or none, is refused before anything runs
+    assert L.block_select_events(one, one, one, 4, 2, 128, 1024, ctypes.byref(cfg), one, 32, nul, nul, one, 1 << 20,
+                                 ev, 5, nul) == 4
+    assert L.block_select_events(one, one, one, 4, 2, 128, 1024, ctypes.byref(cfg), one, 32, nul, nul, one, 1 << 20,
+                                 nul, 6, nul) == 4
+    # the same argument checks as block_select
+    assert L.block_select_events(one, one, one, 4, 2, 128, 1024, ctypes.byref(cfg), one, 31, nul, nul, one, 1 << 20,
+                                 ev, 6, nul) == 4
