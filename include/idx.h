@@ -267,6 +267,24 @@ idx_status block_select_events(const float* index_q, const float* index_k, const
                                int32_t out_width, int32_t* out_count, block_select_stats* stats, void* ws,
                                size_t ws_bytes, void* const* events, int32_t n_events, void* stream);
 
+/* --------------------------------------------------------- block_positions
+ * The positions a block selection covers ("ferrox_core/block_sparse.rs":
+ * positions_of_blocks): row r = i * n_kv + h (query i, KV head h) lists
+ * blocks[r * W + j] for j < counts[r] (counts NULL: all W); negative entries
+ * are ignored.  Its output is the union over those blocks b of the positions
+ * [b * block_size, min((b + 1) * block_size, L, query_pos[i] + 1)),
+ * ascending, without repeats -- the block_select output of one row maps to
+ * the positions sparse attention reads.
+ *   blocks device [Q * n_kv, W] int32 (W <= IDX_MAX_K); counts device
+ *   [Q * n_kv] int32 or NULL; query_pos device [Q] int32.
+ *   out device [Q * n_kv, out_width] int32, -1 padded, out_width >= W *
+ *   block_size (every block covers at most block_size positions);
+ *   out_count device [Q * n_kv] int32 or NULL.
+ * Block size 0 gives empty rows. */
+idx_status block_positions(const int32_t* blocks, const int32_t* counts, int64_t Q, int32_t n_kv, int32_t W,
+                           const int32_t* query_pos, int64_t L, int32_t block_size, int32_t* out, int32_t out_width,
+                           int32_t* out_count, void* stream);
+
 /* ------------------------------------------------------ block_select_static
  * block_select for callers that cannot allocate device memory: code that runs
  * inside a host framework which owns every device allocation (and offers no

@@ -113,6 +113,9 @@ EXPORTS = {
                                              ctypes.POINTER(block_sparse_config), ctypes.c_void_p, ctypes.c_int32,
                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                              ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
+    "block_positions": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                         ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
     "block_select_static": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                              ctypes.POINTER(block_sparse_config), ctypes.c_void_p, ctypes.c_int32,
@@ -288,6 +291,16 @@ def block_select_events(index_q: torch.Tensor, index_k: torch.Tensor, query_pos:
     _check(lib().block_select_events(_ptr(index_q), _ptr(index_k), _ptr(query_pos), Q, n_kv, D, L, ctypes.byref(cfg),
                                      _ptr(out), out.shape[-1], _ptr(out_count), _ptr(stats), _ptr(ws), ws_bytes,
                                      handles, 6, _stream(stream)))
+    return out, out_count
+
+
+def block_positions(blocks: torch.Tensor, counts: Optional[torch.Tensor], query_pos: torch.Tensor, L: int,
+                    block_size: int, out: torch.Tensor, out_count: Optional[torch.Tensor], stream=None):
+    """blocks [Q, n_kv, W] int32 (as block_select writes them) -> covered positions
+    [Q, n_kv, out_width] (ascending, -1 padded)."""
+    Q, n_kv, W = blocks.shape
+    _check(lib().block_positions(_ptr(blocks), _ptr(counts), Q, n_kv, W, _ptr(query_pos), L, block_size, _ptr(out),
+                                 out.shape[-1], _ptr(out_count), _stream(stream)))
     return out, out_count
 
 

@@ -259,4 +259,19 @@ idx_status block_select_events(const float* index_q, const float* index_k, const
                            ws_bytes, stream, ev);
 }
 
+idx_status block_positions(const int32_t* blocks, const int32_t* counts, int64_t Q, int32_t n_kv, int32_t W,
+                           const int32_t* query_pos, int64_t L, int32_t block_size, int32_t* out, int32_t out_width,
+                           int32_t* out_count, void* stream) {
+  if (Q < 0 || n_kv <= 0 || W < 0 || L < 0 || block_size < 0)
+    return fail(IDX_ERR_INVALID_ARG, "negative size, or n_kv <= 0");
+  if (W > IDX_MAX_K) return fail(IDX_ERR_INVALID_ARG, "W=%d above %d", W, IDX_MAX_K);
+  if ((int64_t)out_width < (int64_t)W * block_size || out_width < 0)
+    return fail(IDX_ERR_INVALID_ARG, "out_width=%d below W*block_size=%lld", out_width, (long long)W * block_size);
+  if (Q * n_kv == 0) return IDX_OK;
+  if ((W > 0 && !blocks) || !query_pos || (out_width > 0 && !out)) return fail(IDX_ERR_INVALID_ARG, "NULL pointer");
+  return cuda_status(launch_block_positions(blocks, counts, Q * n_kv, W, query_pos, n_kv, L, block_size, out,
+                                            out_width, out_count, (cudaStream_t)stream),
+                     "block_positions");
+}
+
 }  // extern "C"

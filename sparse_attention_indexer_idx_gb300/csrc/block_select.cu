@@ -308,6 +308,114 @@ cudaError_t launch_block_select(const float* q, const float* k, const int32_t* p
   return e;
 }
 
+// ------------------------------------------------------- block positions --
+// positions_of_blocks: one CTA per (query, head) row.  The row's block ids
+// (negative entries dropped) are sorted ascending in shared memory and
+// repeats removed; distinct blocks cover disjoint position ranges, ordered as
+// the blocks, so concatenating each block's clipped range [b bs, min((b+1) bs,
+// L, pos+1)) gives the covered positions ascending and without repeats.
+constexpr int kBpThreads = 256;
+
+__global__ void __launch_bounds__(kBpThreads) block_positions_kernel(const int32_t* __restrict__ blocks,
+                                                                      const int32_t* __restrict__ counts, int W,
+                                                                      int P2, const int32_t* __restrict__ qpos,
+                                                                      int n_kv, int64_t L, int bs,
+                                                                      int32_t* __restrict__ out, int ow,
+                                                                      int32_t* __restrict__ out_count) {
+  extern __shared__ int32_t sb[];   // [P2] block ids, then [P2 + 1] exclusive scan of the covered lengths
+  int32_t* off = sb + P2;
+  const int64_t row = blockIdx.x;
+  const int t = threadIdx.x;
+  int n = counts ? counts[row] : W;
+  n = n < 0 ? 0 : (n > W ? W : n);
+  const int64_t pos = qpos[row / n_kv];
+  int64_t end_all = pos + 1 < L ? pos + 1 : L;
+  end_all = end_all < 0 ? 0 : end_all;
+  const int32_t* brow = blocks + row * (int64_t)W;
+  for (int j = t; j < P2; j += kBpThreads) {
+    const int32_t b = j < n ? brow[j] : -1;
+    sb[j] = b >= 0 ? b : INT32_MAX;   // dropped entries sort last
+  }
+  __syncthreads();
+  // bitonic sort, ascending
+  for (int k = 2; k <= P2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = t; i < P2; i += kBpThreads) {
+        const int x = i ^ j;
+        if (x > i) {
+          const int32_t a = sb[i], c = sb[x];
+          const bool up = (i & k) == 0;
+          if ((a > c) == up) {
+            sb[i] = c;
+            sb[x] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // covered length per entry (0 for dropped entries and repeats), then an exclusive scan
+  // (a single warp over P2 <= 4096 entries, 128 per lane at most)
+  if (t < 32) {
+    const int per = P2 / 32;
+    int run = 0;
+    for (int q = 0; q < per; ++q) {
+      const int j = t * per + q;
+      const int32_t b = sb[j];
+      int len = 0;
+      if (b != INT32_MAX && (j == 0 || sb[j - 1] != b) && bs > 0) {
+        const int64_t st = (int64_t)b * bs;
+        int64_t en = st + bs;
+        en = en < end_all ? en : end_all;
+        len = en > st ? (int)(en - st) : 0;
+      }
+      off[j] = len;
+      run += len;
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (t >= o) incl += u;
+    }
+    int acc = incl - run;
+    for (int q = 0; q < per; ++q) {
+      const int j = t * per + q;
+      const int len = off[j];
+      off[j] = acc;
+      acc += len;
+    }
+    if (t == 31) off[P2] = acc;
+  }
+  __syncthreads();
+  const int total = off[P2];
+  int32_t* orow = out + row * (int64_t)ow;
+  // each warp writes whole blocks, lanes over consecutive positions
+  const int warp = t >> 5, lane = t & 31;
+  for (int j = warp; j < P2; j += kBpThreads / 32) {
+    const int len = off[j + 1] - off[j];
+    if (len <= 0) continue;
+    const int64_t st = (int64_t)sb[j] * bs;
+    for (int i = lane; i < len; i += 32) orow[off[j] + i] = (int32_t)(st + i);
+  }
+  for (int i = total + t; i < ow; i += kBpThreads) orow[i] = -1;
+  if (out_count && t == 0) out_count[row] = total;
+}
+
+cudaError_t launch_block_positions(const int32_t* blocks, const int32_t* counts, int64_t rows, int W,
+                                   const int32_t* qpos, int n_kv, int64_t L, int bs, int32_t* out, int ow,
+                                   int32_t* out_count, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  int P2 = 32;
+  while (P2 < W) P2 <<= 1;
+  const size_t smem = (size_t)(2 * P2 + 1) * sizeof(int32_t);
+  cudaError_t e = cudaFuncSetAttribute(block_positions_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  block_positions_kernel<<<(unsigned)rows, kBpThreads, smem, st>>>(blocks, counts, W, P2, qpos, n_kv, L, bs, out, ow,
+                                                                   out_count);
+  return cudaGetLastError();
+}
+
 }  // namespace idx
 
 // ---------------------------------------------------------------------------

@@ -159,9 +159,14 @@ __device__ __forceinline__ int64_t bt_nblocks(int64_t pos, const BtProblem& P) {
   return block_geom(pos, P.L, P.c).n_blocks;
 }
 
-// Query of a slot (sorted rank * n_kv + head) and its row of index_q.
+// Query of a slot (sorted rank * n_kv + head); slots fit 32 bits on this route.
 __device__ __forceinline__ int64_t bt_slot_query(const BtProblem& P, const BtWs& W, int64_t slot) {
-  return (int64_t)W.order[slot / P.n_kv];
+  return (int64_t)W.order[(uint32_t)slot / (uint32_t)P.n_kv];
+}
+// Row of index_q (pair index) of a slot.
+__device__ __forceinline__ int64_t bt_slot_pair(const BtProblem& P, const BtWs& W, int64_t slot) {
+  const uint32_t sl = (uint32_t)slot, nk = (uint32_t)P.n_kv, rank = sl / nk;
+  return (int64_t)W.order[rank] * P.n_kv + (int64_t)(sl - rank * nk);
 }
 
 // sqrt of a sum of 128 squares accumulated in fp32 (relative error < 2^-16),
@@ -348,24 +353,18 @@ __global__ void __launch_bounds__(kBtPrepThreads) bt_prep_kernel(BtProblem P, Bt
     }
     __syncthreads();
     for (int j = 0; j < PER; ++j) hist[threadIdx.x * PER + j] += part[threadIdx.x];
-    __syncthreads();
-    for (int64_t i = threadIdx.x; i < P.Q; i += kBtPrepThreads) {
-      const int r = atomicAdd(&hist[bt_nblocks(P.qpos[i], P) >> shift], 1);
-      W.order[r] = (int32_t)i;
-    }
-    __syncthreads();
-    for (int64_t T = threadIdx.x; T < P.nT; T += kBtPrepThreads) {
-      const int64_t r0 = T * kBtRowsT / P.n_kv;
-      int64_t r1 = ((T + 1) * kBtRowsT - 1) / P.n_kv;
-      r1 = r1 < P.Q - 1 ? r1 : P.Q - 1;
-      int64_t mx = 0;
-      for (int64_t r = r0; r <= r1; ++r) {
-        const int64_t nb = bt_nblocks(P.qpos[W.order[r]], P);
-        mx = nb > mx ? nb : mx;
-      }
-      W.nbT[T] = (int32_t)mx;
-    }
+    for (int64_t T = threadIdx.x; T < P.nT; T += kBtPrepThreads) W.nbT[T] = 0;
     for (int64_t b = threadIdx.x; b < P.nbm; b += kBtPrepThreads) W.icnt[b] = 0;
+    __syncthreads();
+    // scatter; a query's rank fixes the row tile pairs its heads land in, whose block count
+    // is the largest visible block count among their queries
+    for (int64_t i = threadIdx.x; i < P.Q; i += kBtPrepThreads) {
+      const int64_t nb = bt_nblocks(P.qpos[i], P);
+      const int64_t r = atomicAdd(&hist[nb >> shift], 1);
+      W.order[r] = (int32_t)i;
+      const int64_t T1 = (r * P.n_kv + P.n_kv - 1) / kBtRowsT;
+      for (int64_t T = r * P.n_kv / kBtRowsT; T <= T1; ++T) atomicMax(&W.nbT[T], (int32_t)nb);
+    }
     return;
   }
   __shared__ float red[24];
@@ -547,7 +546,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int64_t slot = cur_T * kBtRowsT + r0 + i;
-            y[i] = slot < P.slots ? (int32_t)(bt_slot_query(P, W, slot) * P.n_kv + slot % P.n_kv) : 0;
+            y[i] = slot < P.slots ? (int32_t)bt_slot_pair(P, W, slot) : 0;
           }
           uint8_t* dst = sA + (r0 >> 7) * kBtATile + (r0 & 127) * 128;
 #pragma unroll
@@ -656,7 +655,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
           const int64_t qi = bt_slot_query(P, W, slot);
           const int64_t pos = P.qpos[qi];
           if (pos >= 0) vis = pos + 1 < P.L ? pos + 1 : P.L;
-          sig = W.qsig[qi * P.n_kv + slot % P.n_kv];
+          sig = W.qsig[bt_slot_pair(P, W, slot)];
         }
       }
       const int acc = nacc & 1;
@@ -786,16 +785,31 @@ struct BtSlotGeom {
   BlockGeom g;
 };
 
+// The route's block size is 128 and every index fits 32 bits: the geometry of
+// block_geom in 32-bit arithmetic and shifts (no 64-bit division per pair).
 __device__ __forceinline__ BtSlotGeom bt_slot_geom(const BtProblem& P, const BtWs& W, int64_t slot) {
   BtSlotGeom s;
-  s.qi = bt_slot_query(P, W, slot);
-  s.pair = s.qi * P.n_kv + slot % P.n_kv;
-  s.g = block_geom(P.qpos[s.qi], P.L, P.c);
-  s.n = s.g.n_blocks;
-  s.a = P.c.init_blocks < s.n ? P.c.init_blocks : s.n;
-  s.zs = s.n - P.c.local_blocks;
-  s.zs = s.zs < s.a ? s.a : s.zs;   // non-forced blocks: [a, zs)
-  s.n_need = s.g.budget - s.g.n_forced;
+  const uint32_t sl = (uint32_t)slot, nk = (uint32_t)P.n_kv;
+  const uint32_t rank = sl / nk;
+  s.qi = W.order[rank];
+  s.pair = s.qi * P.n_kv + (int64_t)(sl - rank * nk);
+  const int32_t pos = P.qpos[s.qi];
+  const int32_t exist = (int32_t)P.nbm;
+  const int32_t n = pos < 0 ? 0 : ((pos >> 7) + 1 < exist ? (pos >> 7) + 1 : exist);
+  const int32_t init = P.c.init_blocks, local = P.c.local_blocks;
+  const int32_t a = init < n ? init : n;
+  int32_t zs = n - local;
+  zs = zs < a ? a : zs;   // non-forced blocks: [a, zs)
+  const int32_t n_forced = a + (n - zs);
+  const int32_t budget = P.c.top_blocks > n_forced ? P.c.top_blocks : n_forced;
+  s.g.n_blocks = n;
+  s.g.n_forced = n_forced;
+  s.g.budget = budget;
+  s.g.scoring = n > 0 && !(n_forced >= budget || n_forced == n);
+  s.n = n;
+  s.a = a;
+  s.zs = zs;
+  s.n_need = budget - n_forced;
   return s;
 }
 
@@ -1075,10 +1089,11 @@ __global__ void __launch_bounds__(32 * kBtWarps) bt_classify_kernel(BtProblem P,
 constexpr int kBtExactThreads = 128;
 constexpr int kBtXN = 32;                          // pairs per round (MMA N)
 constexpr int kBtXOffK = 0;                        // fp16 keys: 2 chunks x 128 rows x 128 B
-constexpr int kBtXOffQ = kBtXOffK + 2 * kBtChunkBytes;   // fp16 query rows: 2 chunks x 32 rows x 128 B
-constexpr int kBtXOffT = kBtXOffQ + 2 * kBtXN * 128;     // A_p transposed: [32 pairs][128 positions] fp32
-constexpr int kBtXOffL = kBtXOffT + kBtXN * 128 * 4;     // (pair, position) list: 32 x 128 uint16
-constexpr int kBtXOffM = kBtXOffL + kBtXN * 128 * 2;     // misc
+constexpr int kBtXOffQ = kBtXOffK + 2 * kBtChunkBytes;   // fp16 query rows: 2 chunks x 32 rows x 128 B,
+constexpr int kBtXOffT = kBtXOffQ;                       // then (the MMA done) A_p: [32 pairs][128 positions] fp32
+constexpr int kBtXCap = 2048;                            // (pair, position) candidates per round
+constexpr int kBtXOffL = kBtXOffT + kBtXN * 128 * 4;     // candidate list: kBtXCap x uint16
+constexpr int kBtXOffM = kBtXOffL + kBtXCap * 2;         // misc
 constexpr int kBtExactSmem = kBtXOffM + 1024 + 1024;
 
 __global__ void __launch_bounds__(kBtExactThreads)
@@ -1141,7 +1156,7 @@ __global__ void __launch_bounds__(kBtExactThreads)
       if (t < ni) {
         const int64_t sl = items[base + t];
         const int64_t qi = bt_slot_query(P, W, sl);
-        const int64_t pr = qi * P.n_kv + sl % P.n_kv;
+        const int64_t pr = bt_slot_pair(P, W, sl);
         int64_t v = (int64_t)P.qpos[qi] + 1;
         v = v < P.L ? v : P.L;
         slot_of[t] = (int32_t)sl;
@@ -1212,15 +1227,21 @@ __global__ void __launch_bounds__(kBtExactThreads)
       for (int i = 0; i < 4; ++i) {
         if (av[i] >= thr) {
           const int pos = atomicAdd(n_lst, 1);
-          lst[pos] = (uint16_t)((j << 7) | (4 * lane + i));
+          if (pos < kBtXCap) lst[pos] = (uint16_t)((j << 7) | (4 * lane + i));
         }
       }
     }
+    // A_p shares its bytes with the next round's query tile, written by TMA (the async proxy)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
-    // ---- the candidates in the page's order: one thread each, rows loaded 16 x 16 bytes at a time
+    // ---- the candidates in the page's order: one thread each, rows loaded 16 x 16 bytes at a time.
+    // More candidates than the list holds (heavy ties): every visible position of the round's pairs.
     const int nl = *n_lst;
-    for (int i = t; i < nl; i += kBtExactThreads) {
-      const int j = lst[i] >> 7, p = lst[i] & 127;
+    const bool every = nl > kBtXCap;
+    const int n_items = every ? ni * 128 : nl;
+    for (int i = t; i < n_items; i += kBtExactThreads) {
+      const int j = every ? i >> 7 : lst[i] >> 7, p = every ? i & 127 : lst[i] & 127;
+      if (p >= nvis[j]) continue;
       const float4* qr = reinterpret_cast<const float4*>(P.q + (int64_t)pair_of[j] * 128);
       const float4* kr = reinterpret_cast<const float4*>(P.k + (k0 + p) * 128);
       float acc = 0.0f;

@@ -72,6 +72,9 @@ cudaError_t launch_block_select(const float* q, const float* k, const int32_t* p
                                 int64_t L, const block_sparse_config& c, int32_t* out, int out_width,
                                 int32_t* out_count, void* ws, cudaStream_t st, block_select_stats* stats,
                                 bool tensor_route, const cudaEvent_t* ev = nullptr);
+cudaError_t launch_block_positions(const int32_t* blocks, const int32_t* counts, int64_t rows, int W,
+                                   const int32_t* qpos, int n_kv, int64_t L, int bs, int32_t* out, int ow,
+                                   int32_t* out_count, cudaStream_t st);
 bool block_select_tc_applies(int D, const block_sparse_config& c, int64_t Q, int n_kv, int64_t L);
 size_t block_select_tc_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c);
 cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t* pos, int64_t Q, int n_kv,

@@ -85,3 +85,14 @@ def test_block_select_events_refusals(L):
     # the same argument checks as block_select
     assert L.block_select_events(one, one, one, 4, 2, 128, 1024, ctypes.byref(cfg), one, 31, nul, nul, one, 1 << 20,
                                  ev, 6, nul) == 4
+
+
+def test_block_positions_refusals(L):
+    nul = ctypes.c_void_p(0)
+    one = ctypes.c_void_p(256)
+    # out_width below W * block_size, W above IDX_MAX_K, n_kv of 0
+    assert L.block_positions(one, nul, 4, 2, 32, one, 1024, 128, one, 4095, nul, nul) == 4
+    assert L.block_positions(one, nul, 4, 2, 4097, one, 1024, 1, one, 1 << 20, nul, nul) == 4
+    assert L.block_positions(one, nul, 4, 0, 32, one, 1024, 128, one, 4096, nul, nul) == 4
+    # no rows: nothing to do
+    assert L.block_positions(one, nul, 0, 2, 32, one, 1024, 128, one, 4096, nul, nul) == 0

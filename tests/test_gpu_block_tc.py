@@ -167,3 +167,50 @@ def test_page_order_one_ulp_tie_both_routes(B):
     for static in (False, True):
         o, c = _run(B, q, bp.index_k, pos, 32, 1, 2, static=static)
         assert _lists(o, c)[0] == ref, "static" if static else "tensor"
+
+
+def _positions(B, blocks, counts, pos, L, bs):
+    Q, n_kv, W = blocks.shape
+    out = torch.full((Q, n_kv, max(1, W * bs)), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((Q, n_kv), -7, dtype=torch.int32, device="cuda")
+    B.block_positions(torch.from_numpy(np.ascontiguousarray(blocks, dtype=np.int32)).cuda(),
+                      None if counts is None else torch.from_numpy(np.asarray(counts, dtype=np.int32)).cuda(),
+                      torch.from_numpy(np.asarray(pos, dtype=np.int32)).cuda(), L, bs, out, cnt)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), cnt.cpu().numpy()
+
+
+def test_block_positions_against_oracle(B):
+    """positions_of_blocks on arbitrary block lists: unsorted, repeated, -1 entries, blocks past
+    the keys, positions past L, counts given or not."""
+    rng = np.random.default_rng(31)
+    Q, n_kv, W, L, bs = 40, 3, 12, 3000, 128
+    blocks = rng.integers(-1, (L + bs - 1) // bs + 3, (Q, n_kv, W)).astype(np.int32)
+    blocks[0, 0, :] = 5                                   # one block repeated
+    counts = rng.integers(0, W + 1, (Q, n_kv)).astype(np.int32)
+    pos = rng.integers(0, L + 100, Q).astype(np.int32)
+    pos[1] = 0
+    for use_counts in (True, False):
+        o, c = _positions(B, blocks, counts if use_counts else None, pos, L, bs)
+        for i in range(Q):
+            for h in range(n_kv):
+                n = counts[i, h] if use_counts else W
+                ref = obs.positions_of_blocks([int(b) for b in blocks[i, h, :n] if b >= 0], int(pos[i]), L, bs)
+                assert c[i, h] == len(ref)
+                assert o[i, h, :c[i, h]].tolist() == ref
+                assert (o[i, h, c[i, h]:] == -1).all()
+    o, c = _positions(B, blocks, counts, pos, L, 0)        # block size 0: nothing covered
+    assert (c == 0).all()
+
+
+def test_block_positions_of_workload_selection(B):
+    """The MiniMax selection of sampled queries, expanded to positions."""
+    bp = wl.block_select()
+    o, c = _run(B, bp.index_q, bp.index_k, bp.query_pos, bp.top_blocks, bp.init_blocks, bp.local_blocks)
+    po, pc = _positions(B, o, c, bp.query_pos, bp.index_k.shape[0], 128)
+    for i in (0, 1, 500, 1023):
+        for h in range(8):
+            ref = obs.positions_of_blocks(o[i, h, :c[i, h]].tolist(), int(bp.query_pos[i]), bp.index_k.shape[0], 128)
+            assert po[i, h, :pc[i, h]].tolist() == ref
+    # a full selection covers top_blocks * 128 positions except in the last, partial block
+    assert (pc[100:] >= 31 * 128).all()
