@@ -130,7 +130,11 @@ def make_workload(name: str, rank: int, rows=None):
         if rows:
             kw["n_queries"] = rows
         return wl.prefill_bf16(seed=3 + seed_shift, q_noise=PREFILL_Q_NOISE, **kw)
-    if name in ("ragged_fp8", "ragged_fp8_dosa"):
+    if name == "decode_prior":
+        if rows:
+            kw["M"] = rows
+        return wl.decode_bf16(seed=2 + seed_shift, **kw)
+    if name in ("ragged_fp8", "ragged_fp8_dosa", "ragged_fp8_prior"):
         if rows:
             kw["M"] = rows
         return wl.ragged_fp8(seed=5 + seed_shift, **kw)
@@ -145,7 +149,7 @@ def make_workload(name: str, rank: int, rows=None):
 
 
 # workloads whose inputs exceed the 129 MB L2 (no flush between timed steps)
-LARGE_INPUTS = ("decode", "ragged_fp8")
+LARGE_INPUTS = ("decode", "ragged_fp8", "decode_prior", "ragged_fp8_prior")
 
 # dram__bytes_read.sum + dram__bytes_write.sum of the score kernel per full launch: one ncu
 # capture of a smaller batch of the same workload, scaled by the keys processed (traffic grows
@@ -162,6 +166,10 @@ WORKLOAD_TEXT = {
     "ragged_fp8_dosa": "ragged decode FP8 with DoSA pruning: 128 rows, L_r~U[4096,131072], H64 D128, K2048, 8192 seeds/row, R20",
     "ragged_fp8": "ragged decode FP8 e4m3 keys + scale: 128 rows, L_r~U[4096,131072], H64 D128, top-2048, witness_merge S=32",
     "tiny": "tiny fp32 indexer: 8 rows, H4 D16, L512, K32, witness_merge S=4",
+    "decode_prior": "decode indexer bf16 (as decode) ranked with a prior: the top-2048 of the two previous steps "
+                    "(queries q + 0.3 N(0,1), one key fewer)",
+    "ragged_fp8_prior": "ragged decode FP8 (as ragged_fp8) ranked with a prior: the top-2048 of the two previous "
+                        "steps (queries q + 0.3 N(0,1), one key fewer)",
     "block_select": "MiniMax block select fp32: 1024 queries, 8 KV heads, D128, L131072, block 128, top 32, init 1, local 2",
 }
 
@@ -319,6 +327,74 @@ class BlockSelectStep:
         return int(sum(min(int(p) + 1, L) for p in self.bp.query_pos)) * self.bp.index_q.shape[1]
 
 
+class PriorStep:
+    """Top-K with recent selections as a prior (idx_topk_prior) on device-resident inputs.
+    The prior (the top-K of the two previous decode steps) is computed once, outside the
+    timed region, by the unpruned top-K on the previous steps' queries."""
+
+    PHASES = ("check", "prior_scores", "filter", "candidate_topk", "rest")
+
+    def __init__(self, B, wp, dev, capacity):
+        self.B = B
+        self.wp = wp
+        self.p = B.problem_to_device(wp, dev)
+        self.K = K = wp.K
+        M = wp.M
+        priors = []
+        for seed in (8, 9):
+            prev = wl.previous_step(wp, seed=seed, noise=0.3)
+            q = torch.from_numpy(np.ascontiguousarray(prev.q).view(np.int16)).to(dev).view(torch.bfloat16)
+            pq = B.Problem(q, self.p.w, self.p.keys, torch.from_numpy(prev.key_len).to(dev), self.p.max_key_len,
+                           self.p.key_off, self.p.key_scale)
+            ids = torch.empty((M, K), dtype=torch.int32, device=dev)
+            B.idx_topk(pq, K, ids, None, torch.empty(B.idx_topk_workspace_size(pq, K), dtype=torch.uint8, device=dev))
+            priors.append(ids)
+        self.prior = torch.cat(priors, dim=1).contiguous()
+        self.cap = 4 * K
+        self.ids = torch.empty((M, K), dtype=torch.int32, device=dev)
+        self.sc = torch.empty((M, K), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(B.idx_topk_prior_workspace_size(self.p, K, self.prior.shape[1], self.cap),
+                              dtype=torch.uint8, device=dev)
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        self.score_ms = []          # the filtered score kernel
+        self.phase_ms = {k: [] for k in self.PHASES}
+        # check, prior scores, tau, filtered scores, route, candidate top-K (2), unpruned rows'
+        # score and top-K (3, masked), counters
+        self.launches = 11
+        torch.cuda.synchronize()
+
+    def run(self, timed=False):
+        if timed:
+            self.B.idx_topk_prior_events(self.p, self.K, self.prior, self.cap, self.ids, self.sc, self.ws, self.ev,
+                                         stream=torch.cuda.current_stream())
+        else:
+            self.B.idx_topk_prior(self.p, self.K, self.prior, self.cap, self.ids, self.sc, self.ws)
+
+    def collect(self):
+        for i, k in enumerate(self.PHASES):
+            self.phase_ms[k].append(self.ev[i].elapsed_time(self.ev[i + 1]))
+        self.score_ms.append(self.phase_ms["filter"][-1])
+
+    def step_ms(self):
+        return self.ev[0].elapsed_time(self.ev[5])
+
+    def algorithmic_bytes(self):
+        """Filtered score kernel: every visible key row once, queries, weights (the candidates it
+        writes are ~1% of that)."""
+        wp = self.wp
+        kb = {"bf16": 2, "fp8": 1}[wp.dtype] * wp.D + (4 if wp.dtype == "fp8" else 0)
+        return wp.pairs() * kb + wp.M * wp.H * wp.D * 2 + wp.M * wp.H * 4
+
+    def prior_stats(self):
+        st = torch.zeros(3, dtype=torch.int64, device=self.ids.device)
+        rs = torch.empty((self.wp.M,), dtype=torch.int32, device=self.ids.device)
+        self.B.idx_topk_prior(self.p, self.K, self.prior, self.cap, self.ids, self.sc, self.ws, row_status=rs,
+                              stats=st)
+        torch.cuda.synchronize()
+        s = st.cpu().tolist()
+        return {"rows_filtered": s[0], "candidates_per_row": s[1] / max(1, s[0]), "dense_rows": s[2]}
+
+
 def e2e_run(B, wp, dev, steps):
     """Same step through the C ABI from pinned host buffers: H2D of the step's
     inputs, score -> top-K -> witness merge, D2H of the top-K ids."""
@@ -454,6 +530,10 @@ def main():
             step = BlockSelectStep(B, wp, dev)
             pairs_per_step = step.pairs()
             rows_per_step = wp.index_q.shape[0] * wp.index_q.shape[1]
+        elif args.workload in ("decode_prior", "ragged_fp8_prior"):
+            step = PriorStep(B, wp, dev, args.capacity)
+            pairs_per_step = wp.pairs()
+            rows_per_step = wp.M
         elif args.workload in ("prefill_dosa", "ragged_fp8_dosa"):
             step = DosaStep(B, wp, dev, R=wp.extras["R"], n_seed=wp.extras.get("n_seed", wp.extras.get("seed_cap", 8192)),
                             capacity=args.capacity)
@@ -522,6 +602,15 @@ def main():
                     "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": traffic,
                     "peak_source": f"{peak_src} hbm copy", "kernel_ms": k_ms,
                     "algorithmic_bytes": step.algorithmic_bytes()}
+    elif isinstance(step, PriorStep):
+        k_ms = statistics.median(kernel_ms)
+        ach = step.algorithmic_bytes() / (k_ms * 1e-3) / 1e9
+        roof = {"kernel": "score_tc_kernel (kFilter)", "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "traffic": None, "peak_source": f"{peak_src} hbm copy", "kernel_ms": k_ms,
+                "algorithmic_bytes": step.algorithmic_bytes(),
+                "phases_ms": {k: statistics.median(v) for k, v in step.phase_ms.items()}}
+        with torch.cuda.stream(stream):
+            roof["prior_stats"] = step.prior_stats()
     elif isinstance(step, BlockSelectStep):
         k_ms = statistics.median(kernel_ms)
         # the block maxima on the tensor cores: one multiply-add per visible (query, head,

@@ -185,6 +185,43 @@ idx_status dosa_topk(const idx_problem* p, int32_t K, const dosa_params* dp, con
                      int32_t seed_ld, int32_t* out_ids, float* out_scores, int32_t* row_status,
                      dosa_stats* stats, void* ws, size_t ws_bytes, void* stream);
 
+/* ----------------------------------------------------------- idx_topk_prior
+ * Decode top-K with recent selections as a prior ("DoSA：用安全上界减少 Indexer 的
+ * 完整打分": the decode path keeps full scoring; the keys of recent selections
+ * set a threshold that shrinks the score write-back and the top-K input).
+ * prior_ids: device [M, prior_ld] int32, row m's recent selections (row-
+ * relative ids, e.g. the previous steps' top-K; negative, out-of-range and
+ * repeated entries are ignored).  With I the remaining ids, n = min(K, L_m)
+ * and tau_m the n-th largest current score over I, a row with |I| >= n has its
+ * top-K among {s >= tau_m}: every visible key is scored, only those are kept
+ * (up to candidate_capacity per row) and ranked.  Rows without such a prior,
+ * or whose candidates exceed the capacity, take the unpruned path.  A prior
+ * wider than K gives a tighter tau_m.  The output is identical to idx_topk's
+ * on the same inputs.
+ *   row_status: device [M] int32 or NULL: 0 ranked from candidates, 1 no
+ *   usable prior, 2 candidate overflow.  stats: device topk_prior_stats or
+ *   NULL (added to).  Tensor-core score shapes only use the prior (others run
+ *   the unpruned path for every row). */
+typedef struct topk_prior_stats {
+  unsigned long long rows_filtered; /* rows ranked from their candidates */
+  unsigned long long candidates;    /* candidates of those rows */
+  unsigned long long dense_rows;    /* rows that took the unpruned path */
+} topk_prior_stats;
+
+size_t idx_topk_prior_workspace_size(const idx_problem* p, int32_t K, int32_t prior_ld,
+                                     int32_t candidate_capacity);
+idx_status idx_topk_prior(const idx_problem* p, int32_t K, const int32_t* prior_ids, int32_t prior_ld,
+                          int32_t candidate_capacity, int32_t* out_ids, float* out_scores, int32_t* row_status,
+                          topk_prior_stats* stats, void* ws, size_t ws_bytes, void* stream);
+/* idx_topk_prior, recording CUDA events (cudaEvent_t handles, host array of
+ * n_events >= 6, created by the caller) on `stream` for profiling: before the
+ * prior check, after it, after the prior scores and tau, after the filtered
+ * scoring, after the candidate top-K, after the unpruned rows and counters. */
+idx_status idx_topk_prior_events(const idx_problem* p, int32_t K, const int32_t* prior_ids, int32_t prior_ld,
+                                 int32_t candidate_capacity, int32_t* out_ids, float* out_scores,
+                                 int32_t* row_status, topk_prior_stats* stats, void* ws, size_t ws_bytes,
+                                 void* const* events, int32_t n_events, void* stream);
+
 /* ------------------------------------------------------------ witness_merge
  * Segment-witness covering pass, in place ("Segment Witnesses", sections
  * "Object" and "Implementation rule and contracts").  Row r of topk_ids

@@ -54,6 +54,11 @@ class dosa_stats(ctypes.Structure):
                 ("skipped_rows", ctypes.c_ulonglong)]
 
 
+class topk_prior_stats(ctypes.Structure):
+    _fields_ = [("rows_filtered", ctypes.c_ulonglong), ("candidates", ctypes.c_ulonglong),
+                ("dense_rows", ctypes.c_ulonglong)]
+
+
 class block_select_stats(ctypes.Structure):
     _fields_ = [("pairs", ctypes.c_ulonglong), ("blocks_bounded", ctypes.c_ulonglong),
                 ("blocks_rescored", ctypes.c_ulonglong), ("fallback_pairs", ctypes.c_ulonglong),
@@ -113,6 +118,15 @@ EXPORTS = {
                                              ctypes.POINTER(block_sparse_config), ctypes.c_void_p, ctypes.c_int32,
                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                              ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
+    "idx_topk_prior_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(idx_problem), ctypes.c_int32, ctypes.c_int32,
+                                                        ctypes.c_int32]),
+    "idx_topk_prior": (ctypes.c_int32, [ctypes.POINTER(idx_problem), ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
+                                        ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "idx_topk_prior_events": (ctypes.c_int32, [ctypes.POINTER(idx_problem), ctypes.c_int32, ctypes.c_void_p,
+                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                               ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
     "block_positions": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
                                          ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
                                          ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
@@ -204,6 +218,34 @@ def idx_topk(p: Problem, K: int, out_ids: torch.Tensor, out_scores: Optional[tor
     cp = p.c()
     _check(lib().idx_topk(ctypes.byref(cp), K, _ptr(out_ids), _ptr(out_scores), _ptr(ws), ws.numel() * ws.element_size(),
                           _stream(stream)))
+    return out_ids, out_scores
+
+
+def idx_topk_prior_workspace_size(p: Problem, K: int, prior_ld: int, capacity: int) -> int:
+    cp = p.c()
+    return int(lib().idx_topk_prior_workspace_size(ctypes.byref(cp), K, prior_ld, capacity))
+
+
+def idx_topk_prior(p: Problem, K: int, prior_ids: torch.Tensor, capacity: int, out_ids: torch.Tensor,
+                   out_scores: Optional[torch.Tensor], ws: torch.Tensor, row_status: Optional[torch.Tensor] = None,
+                   stats: Optional[torch.Tensor] = None, stream=None):
+    """Top-K with the previous step's selection prior_ids [M, prior_ld] as a prior.
+    stats: torch.zeros(3, dtype=torch.int64) storage for topk_prior_stats, or None."""
+    cp = p.c()
+    _check(lib().idx_topk_prior(ctypes.byref(cp), K, _ptr(prior_ids), prior_ids.shape[1], capacity, _ptr(out_ids),
+                                _ptr(out_scores), _ptr(row_status), _ptr(stats), _ptr(ws),
+                                ws.numel() * ws.element_size(), _stream(stream)))
+    return out_ids, out_scores
+
+
+def idx_topk_prior_events(p: Problem, K: int, prior_ids: torch.Tensor, capacity: int, out_ids: torch.Tensor,
+                          out_scores: Optional[torch.Tensor], ws: torch.Tensor, events, stream=None):
+    """idx_topk_prior recording 6 torch.cuda.Event (already created) between its stages."""
+    cp = p.c()
+    handles = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events[:6]])
+    _check(lib().idx_topk_prior_events(ctypes.byref(cp), K, _ptr(prior_ids), prior_ids.shape[1], capacity,
+                                       _ptr(out_ids), _ptr(out_scores), None, None, _ptr(ws),
+                                       ws.numel() * ws.element_size(), handles, 6, _stream(stream)))
     return out_ids, out_scores
 
 

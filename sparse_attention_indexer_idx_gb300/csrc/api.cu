@@ -128,6 +128,50 @@ idx_status idx_topk(const idx_problem* p, int32_t K, int32_t* out_ids, float* ou
   return cuda_status(e, "idx_topk/select");
 }
 
+size_t idx_topk_prior_workspace_size(const idx_problem* p, int32_t K, int32_t prior_ld,
+                                     int32_t candidate_capacity) {
+  if (!p || p->M <= 0 || K < 1 || prior_ld < 1 || candidate_capacity < 1) return 0;
+  return topk_prior_ws(*p, K, prior_ld, candidate_capacity);
+}
+
+static idx_status topk_prior_impl(const idx_problem* p, int32_t K, const int32_t* prior_ids, int32_t prior_ld,
+                                  int32_t candidate_capacity, int32_t* out_ids, float* out_scores,
+                                  int32_t* row_status, topk_prior_stats* stats, void* ws, size_t ws_bytes,
+                                  void* stream, const cudaEvent_t* ev) {
+  idx_status st = check_problem(p);
+  if (st) return st;
+  if (K < 1 || K > IDX_MAX_K) return fail(IDX_ERR_INVALID_ARG, "K=%d outside [1, %d]", K, IDX_MAX_K);
+  if (prior_ld < 1) return fail(IDX_ERR_INVALID_ARG, "prior_ld=%d below 1", prior_ld);
+  if (candidate_capacity < K)
+    return fail(IDX_ERR_INVALID_ARG, "candidate_capacity=%d below K=%d", candidate_capacity, K);
+  if (p->M == 0) return IDX_OK;
+  if (!out_ids || !prior_ids) return fail(IDX_ERR_INVALID_ARG, "NULL pointer");
+  if (ws_bytes < idx_topk_prior_workspace_size(p, K, prior_ld, candidate_capacity))
+    return fail(IDX_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  if (!ws) return fail(IDX_ERR_INVALID_ARG, "workspace is NULL");
+  return cuda_status(launch_topk_prior(*p, K, prior_ids, prior_ld, candidate_capacity, out_ids, out_scores,
+                                       row_status, stats, ws, (cudaStream_t)stream, ev),
+                     "idx_topk_prior");
+}
+
+idx_status idx_topk_prior(const idx_problem* p, int32_t K, const int32_t* prior_ids, int32_t prior_ld,
+                          int32_t candidate_capacity, int32_t* out_ids, float* out_scores, int32_t* row_status,
+                          topk_prior_stats* stats, void* ws, size_t ws_bytes, void* stream) {
+  return topk_prior_impl(p, K, prior_ids, prior_ld, candidate_capacity, out_ids, out_scores, row_status, stats, ws,
+                         ws_bytes, stream, nullptr);
+}
+
+idx_status idx_topk_prior_events(const idx_problem* p, int32_t K, const int32_t* prior_ids, int32_t prior_ld,
+                                 int32_t candidate_capacity, int32_t* out_ids, float* out_scores,
+                                 int32_t* row_status, topk_prior_stats* stats, void* ws, size_t ws_bytes,
+                                 void* const* events, int32_t n_events, void* stream) {
+  if (!events || n_events < 6) return fail(IDX_ERR_INVALID_ARG, "idx_topk_prior_events needs 6 events");
+  cudaEvent_t ev[6];
+  for (int i = 0; i < 6; ++i) ev[i] = (cudaEvent_t)events[i];
+  return topk_prior_impl(p, K, prior_ids, prior_ld, candidate_capacity, out_ids, out_scores, row_status, stats, ws,
+                         ws_bytes, stream, ev);
+}
+
 size_t idx_topk_scores_workspace_size(int64_t M, int32_t max_len, int32_t K) {
   if (M <= 0 || max_len <= 0) return 0;
   return topk_dense_ws(M, max_len, K < 1 ? 1 : K);

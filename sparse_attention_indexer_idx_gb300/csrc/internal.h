@@ -82,6 +82,11 @@ cudaError_t launch_block_select_tc(const float* q, const float* k, const int32_t
                                    int32_t* out_count, void* ws, block_select_stats* stats, cudaStream_t st,
                                    const cudaEvent_t* ev = nullptr);
 
+size_t topk_prior_ws(const idx_problem& p, int K, int P, int64_t cap);
+cudaError_t launch_topk_prior(const idx_problem& p, int K, const int32_t* prior, int P, int64_t cap,
+                              int32_t* out_ids, float* out_scores, int32_t* row_status, topk_prior_stats* stats,
+                              void* ws, cudaStream_t st, const cudaEvent_t* ev = nullptr);
+
 size_t dosa_ws(const idx_problem& p, int K, const dosa_params& dp, int seed_ld);
 cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, const int32_t* seed_ids, int seed_ld,
                         int32_t* out_ids, float* out_scores, int32_t* row_status, dosa_stats* stats, void* ws,

@@ -62,7 +62,7 @@
 
 namespace idx {
 
-enum TcMode { kScore = 0, kGather = 1, kBound = 2 };
+enum TcMode { kScore = 0, kGather = 1, kBound = 2, kFilter = 3 };
 
 struct TcArgs {
   idx_problem p;              // p.q is the B source: queries, or prepared vectors (kBound)
@@ -83,6 +83,7 @@ struct TcArgs {
   int32_t* cand_cnt;          // [M]
   int64_t cap;
   int32_t* status;            // [M] bit 1: candidate overflow
+  float* cand_sc;             // kFilter: [M, cap] scores of the candidates (cand: their ids)
   const int32_t* row_mask;    // optional [M]: rows with row_mask[m] == 0 are skipped
   int R;
 };
@@ -101,12 +102,13 @@ struct TcCfg {
   static constexpr bool FP8 = (KDT == IDX_FP8_E4M3);
   static constexpr bool GATHER = (MODE == kGather);
   static constexpr bool BOUND = (MODE == kBound);
+  static constexpr bool FILTER = (MODE == kFilter);   // scores >= tau[m] appended as (id, score)
   static constexpr int NCOLX = FP8 ? 2 * NCOL : NCOL;   // MMA columns per query (hi, lo for FP8)
   static constexpr int N = NQ * NCOLX;
   // 128-key subtiles per work unit: FP8 per-row scoring takes 256 keys (32 KB,
   // one TMA box) per unit, so every barrier round trip, commit and schedule
   // step covers as many key bytes as a bf16 tile
-  static constexpr int SUB = (FP8 && MODE == kScore && NQ == 1 && N <= 128) ? 2 : 1;
+  static constexpr int SUB = (FP8 && (MODE == kScore || MODE == kFilter) && NQ == 1 && N <= 128) ? 2 : 1;
   static constexpr int UKEYS = 128 * SUB;
   static constexpr int A_BYTES = SUB * (FP8 ? 128 * 128 : 128 * 128 * 2);   // one unit of keys
   static constexpr int SUB_BYTES = A_BYTES / SUB;                           // one 128-key subtile
@@ -128,7 +130,7 @@ struct TcCfg {
   static constexpr int NE = 8;   // epilogue warps, two per TMEM lane quarter
   // bf16 score tiles with at least 4 queries: an epilogue warp walks its queries
   // two at a time, both chains in one packed fma.rn.f32x2 per head
-  static constexpr bool PAIR = (MODE != kBound) && !FP8 && NQ >= 4;
+  static constexpr bool PAIR = (MODE != kBound) && (MODE != kFilter) && !FP8 && NQ >= 4;
   // epilogue warps that read one unit: all 8 when a unit holds several queries
   // (alternating queries) or two subtiles (one warp of a quarter per subtile),
   // else 4 (the two warps of a quarter take alternate units)
@@ -158,6 +160,7 @@ struct TcCfg {
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N");
+  static_assert(MODE != kFilter || NQ == 1, "kFilter: one query per group");
   static_assert(SACC * SUB * N <= 512, "TMEM columns");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -688,10 +691,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           }
           sLen[lane] = len;
           sBase[lane] = off;
-          if (C::BOUND) {
-            sAux[4 * lane] = m < args.p.M ? args.coef[m] : 0.0f;
-            sAux[4 * lane + 1] = m < args.p.M ? args.tau[m] : 0.0f;
-          }
+          if (C::BOUND) sAux[4 * lane] = m < args.p.M ? args.coef[m] : 0.0f;
+          if (C::BOUND || C::FILTER) sAux[4 * lane + 1] = m < args.p.M ? args.tau[m] : 0.0f;
         }
         __syncwarp();
       }
@@ -867,7 +868,27 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
               }
             }
           }
-          if (key < len) args.scores[m * args.ld + key] = C::FP8 ? (sc * sAux[4 * qi + 2]) * kscale : sc;
+          const float val = C::FP8 ? (sc * sAux[4 * qi + 2]) * kscale : sc;
+          if constexpr (C::FILTER) {
+            // the same value the dense mode writes; kept iff >= tau (warp ballot, one atomic per warp)
+            const bool is_cand = key < len && !(val < sAux[4 * qi + 1]);
+            const unsigned mask = __ballot_sync(0xffffffffu, is_cand);
+            if (mask) {
+              int32_t basepos = 0;
+              if (lane == 0) basepos = atomicAdd(&args.cand_cnt[m], __popc(mask));
+              basepos = __shfl_sync(0xffffffffu, basepos, 0);
+              if (lane == 0 && basepos + __popc(mask) > args.cap) atomicOr(&args.status[m], 2);
+              if (is_cand) {
+                const int64_t pos = basepos + __popc(mask & ((1u << lane) - 1u));
+                if (pos < args.cap) {
+                  args.cand[m * args.cap + pos] = key;
+                  args.cand_sc[m * args.cap + pos] = val;
+                }
+              }
+            }
+          } else if (key < len) {
+            args.scores[m * args.ld + key] = val;
+          }
         } else {
           uint32_t v[32], vl[32];
           tmem_ld_32x32b_x32(tcol, v);

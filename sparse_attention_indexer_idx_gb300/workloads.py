@@ -301,6 +301,18 @@ def block_select(seed: int = 4, Q: int = 1024, n_kv: int = 8, D: int = 128, L: i
                               block_size, top_blocks, init_blocks, local_blocks)
 
 
+def previous_step(wp: IndexerProblem, seed: int = 11, noise: float = 0.3) -> IndexerProblem:
+    """The decode step before `wp`: every row saw one key fewer and its query
+    was q + noise * N(0, 1) (rounded as q is stored); keys, offsets and
+    weights are shared.  Its top-K is the prior of the step `wp`."""
+    rng = np.random.default_rng(seed)
+    qf = wp.q_f32() + np.float32(noise) * _normal(rng, wp.q.shape)
+    q = qf.astype(np.float32) if wp.dtype == "f32" else _bulk_bf16(qf.astype(np.float32))
+    key_len = np.maximum(np.asarray(wp.key_len, dtype=np.int32) - 1, 0).astype(np.int32)
+    return IndexerProblem(wp.name + "_previous", wp.dtype, q, wp.w, wp.keys, key_len, wp.key_off, wp.K,
+                          key_scale=wp.key_scale, extras=dict(wp.extras))
+
+
 def witness_rows(seed: int, rows: int, topk: int, L_min: int = 1, L_max: int = 4096,
                  pad_frac: float = 0.1, oob_frac: float = 0.01):
     """Random learned rows for the witness merge: distinct in-range offsets with

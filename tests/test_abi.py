@@ -96,3 +96,18 @@ def test_block_positions_refusals(L):
     assert L.block_positions(one, nul, 4, 0, 32, one, 1024, 128, one, 4096, nul, nul) == 4
     # no rows: nothing to do
     assert L.block_positions(one, nul, 0, 2, 32, one, 1024, 128, one, 4096, nul, nul) == 0
+
+
+def test_topk_prior_refusals(L):
+    from sparse_attention_indexer_idx_gb300 import binding as B
+    nul = ctypes.c_void_p(0)
+    one = ctypes.c_void_p(256)
+    p = B.idx_problem(one, B.IDX_BF16, one, 4, 32, 128, one, B.IDX_BF16, None, 1 << 20, None, one, 4096)
+    # K out of range, prior_ld < 1, capacity below K, NULL prior
+    assert L.idx_topk_prior(ctypes.byref(p), 0, one, 16, 64, one, nul, nul, nul, one, 1 << 30, nul) == 4
+    assert L.idx_topk_prior(ctypes.byref(p), 16, one, 0, 64, one, nul, nul, nul, one, 1 << 30, nul) == 4
+    assert L.idx_topk_prior(ctypes.byref(p), 16, one, 16, 8, one, nul, nul, nul, one, 1 << 30, nul) == 4
+    assert L.idx_topk_prior(ctypes.byref(p), 16, nul, 16, 64, one, nul, nul, nul, one, 1 << 30, nul) == 4
+    # workspace too small
+    assert L.idx_topk_prior(ctypes.byref(p), 16, one, 16, 64, one, nul, nul, nul, one, 16, nul) == 6
+    assert L.idx_topk_prior_workspace_size(ctypes.byref(p), 16, 16, 64) > 4 * 4096 * 4
