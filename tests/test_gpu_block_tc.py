@@ -214,3 +214,27 @@ def test_block_positions_of_workload_selection(B):
             assert po[i, h, :pc[i, h]].tolist() == ref
     # a full selection covers top_blocks * 128 positions except in the last, partial block
     assert (pc[100:] >= 31 * 128).all()
+
+
+def test_block_select_events_same_result(B):
+    """block_select_events records its six events and returns what block_select returns."""
+    rng = np.random.default_rng(41)
+    Q, n_kv, L = 30, 8, 9000
+    q = torch.from_numpy(rng.standard_normal((Q, n_kv, 128)).astype(np.float32)).cuda()
+    k = torch.from_numpy(rng.standard_normal((L, 128)).astype(np.float32)).cuda()
+    pos = torch.from_numpy(rng.integers(0, L, Q).astype(np.int32)).cuda()
+    cfg = B.block_sparse_config(128, 32, 1, 2)
+    ws = torch.empty(B.block_select_workspace_size(Q, n_kv, L, cfg), dtype=torch.uint8, device="cuda")
+    out1 = torch.empty((Q, n_kv, 32), dtype=torch.int32, device="cuda")
+    out2 = torch.empty_like(out1)
+    c1 = torch.empty((Q, n_kv), dtype=torch.int32, device="cuda")
+    c2 = torch.empty_like(c1)
+    B.block_select(q, k, pos, cfg, out1, c1, ws)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in ev:
+        e.record()
+    B.block_select_events(q, k, pos, cfg, out2, c2, ws, ev, stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2) and torch.equal(c1, c2)
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(5)]
+    assert all(t >= 0.0 for t in times)

@@ -145,3 +145,24 @@ def test_prior_full_size_ragged_fp8(B):
         _same((ids, sc), ref)
     assert (st == 0).sum() >= 120 and stats[1] < 0.05 * wp.pairs()
     assert B.device_error() == 0
+
+
+def test_prior_events_same_result(B):
+    """idx_topk_prior_events records its six events and returns what idx_topk_prior returns."""
+    K = 128
+    wp = wl.decode_bf16(seed=21, M=8, H=32, L=3000, K=K)
+    prev = wl.previous_step(wp, seed=22, noise=0.3)
+    prior = torch.from_numpy(_oracle_prior(prev, K)).cuda()
+    p = B.problem_to_device(wp)
+    ws = torch.empty(B.idx_topk_prior_workspace_size(p, K, K, 4 * K), dtype=torch.uint8, device="cuda")
+    i1 = torch.empty((8, K), dtype=torch.int32, device="cuda")
+    s1 = torch.empty((8, K), dtype=torch.float32, device="cuda")
+    i2, s2 = torch.empty_like(i1), torch.empty_like(s1)
+    B.idx_topk_prior(p, K, prior, 4 * K, i1, s1, ws)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in ev:
+        e.record()
+    B.idx_topk_prior_events(p, K, prior, 4 * K, i2, s2, ws, ev, stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2) and torch.equal(s1.view(torch.int32), s2.view(torch.int32))
+    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0.0 for i in range(5))
