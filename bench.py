@@ -130,6 +130,10 @@ def make_workload(name: str, rank: int, rows=None):
         if rows:
             kw["n_queries"] = rows
         return wl.prefill_bf16(seed=3 + seed_shift, q_noise=PREFILL_Q_NOISE, **kw)
+    if name == "prefill_dosa_aligned":
+        if rows:
+            kw["n_queries"] = rows
+        return wl.prefill_bf16(seed=3 + seed_shift, q_noise=0.001, q_run=16, positive_w=True, **kw)
     if name == "decode_prior":
         if rows:
             kw["M"] = rows
@@ -163,6 +167,9 @@ WORKLOAD_TEXT = {
     "decode": "decode indexer bf16: 64 rows x 32768 own keys, H32 D128, top-2048, witness_merge S=16 (5% padding)",
     "prefill": "causal prefill bf16: 4096 queries over 65536 shared keys, H64 D128, top-2048 (unpruned)",
     "prefill_dosa": "causal prefill bf16 with DoSA pruning: 4096 queries, 65536 keys, H64 D128, K2048, 12288 seeds, R16",
+    "prefill_dosa_aligned": "causal prefill bf16 with DoSA pruning, near-parallel heads: 4096 queries, 65536 keys, "
+                            "H64 D128, K2048, 12288 seeds, R16; q_h = |a_h| c_z + 0.001 N(0,1), runs of 16 "
+                            "queries share z, w = |N(0, 1/64)|",
     "ragged_fp8_dosa": "ragged decode FP8 with DoSA pruning: 128 rows, L_r~U[4096,131072], H64 D128, K2048, 8192 seeds/row, R20",
     "ragged_fp8": "ragged decode FP8 e4m3 keys + scale: 128 rows, L_r~U[4096,131072], H64 D128, top-2048, witness_merge S=32",
     "tiny": "tiny fp32 indexer: 8 rows, H4 D16, L512, K32, witness_merge S=4",
@@ -241,16 +248,17 @@ class IndexerStep:
 class DosaStep:
     """DoSA-pruned top-K (dosa_topk) on device-resident inputs."""
 
-    def __init__(self, B, wp, dev, R, n_seed, capacity=16384):
+    def __init__(self, B, wp, dev, R, n_seed, capacity=16384, group_stream=1):
         self.B = B
         self.wp = wp
         self.p = B.problem_to_device(wp, dev)
         self.K = wp.K
-        self.dp = B.make_dosa_params(n_seed=n_seed, retained_heads=R, candidate_capacity=capacity)
+        self.dp = B.make_dosa_params(n_seed=n_seed, retained_heads=R, candidate_capacity=capacity,
+                                     group_stream=group_stream)
         self.ids = torch.empty((wp.M, self.K), dtype=torch.int32, device=dev)
         self.sc = torch.empty((wp.M, self.K), dtype=torch.float32, device=dev)
         self.ws = torch.empty(B.dosa_topk_workspace_size(self.p, self.K, self.dp), dtype=torch.uint8, device=dev)
-        self.stats = torch.zeros(6, dtype=torch.int64, device=dev)
+        self.stats = torch.zeros(B.DOSA_STATS_FIELDS, dtype=torch.int64, device=dev)
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         self.score_ms = []
         # kernels dosa_topk enqueues per call: seeds, seed scores and top-K, planner,
@@ -260,7 +268,9 @@ class DosaStep:
         L = int(np.max(wp.key_len))
         NS = min(max(n_seed, wp.K), L)
         if wp.key_off is None:
-            self.launches = 20 + two(L) + two(NS) + two(wp.K + capacity) + two(L)
+            # + the group split and the shared-stream scoring (groups of four queries)
+            grp = 2 if group_stream and wp.M >= 2 and wp.q.shape[1] in (16, 32, 64) else 0
+            self.launches = 20 + grp + two(L) + two(NS) + two(wp.K + capacity) + two(L)
         else:
             self.launches = 13 + two(NS) + two(wp.K + capacity) + two(L)
 
@@ -482,6 +492,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=list(WORKLOAD_TEXT))
     ap.add_argument("--capacity", type=int, default=16384, help="DoSA candidate capacity per row")
+    ap.add_argument("--group-stream", type=int, default=1, choices=[0, 1],
+                    help="DoSA shared candidate stream for groups of four queries (shared keys)")
     ap.add_argument("--rows", type=int, default=0, help="smaller batch (query rows) for profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -534,9 +546,9 @@ def main():
             step = PriorStep(B, wp, dev, args.capacity)
             pairs_per_step = wp.pairs()
             rows_per_step = wp.M
-        elif args.workload in ("prefill_dosa", "ragged_fp8_dosa"):
+        elif args.workload in ("prefill_dosa", "prefill_dosa_aligned", "ragged_fp8_dosa"):
             step = DosaStep(B, wp, dev, R=wp.extras["R"], n_seed=wp.extras.get("n_seed", wp.extras.get("seed_cap", 8192)),
-                            capacity=args.capacity)
+                            capacity=args.capacity, group_stream=args.group_stream)
             pairs_per_step = wp.pairs()
             rows_per_step = wp.M
         else:
@@ -637,6 +649,7 @@ def main():
         nonseed = max(1, st[0] - st[1])
         dosa_info = {"pairs": st[0], "seed_pairs": st[1], "candidates": st[2], "survivors": st[3],
                      "fallback_rows": st[4], "skipped_rows": st[5],
+                     "group_keys": st[6], "solo_keys": st[7], "group_stream": int(step.dp.group_stream),
                      # rates over all non-seed pairs: only meaningful when no row skipped the scan
                      "candidate_rate": st[2] / nonseed if st[5] == 0 else None,
                      "survival_rate": st[3] / nonseed if st[5] == 0 else None}

@@ -160,6 +160,11 @@ idx_status idx_topk_scores(const float* scores, int64_t ld, const int32_t* lens,
  * visible keys, predicts more than 1.25 x candidate_capacity candidates: it
  * skips the bound scan (row_status 3).  The output does not depend on which
  * rows take the unpruned path.
+ * group_stream != 0 (shared keys, H 16/32/64 with bf16 keys or 16/32 with FP8
+ * keys; section 4 of the same page): rows in groups of four; a candidate kept
+ * by at least two rows of a group and visible to all four is scored once for
+ * the four (one tensor-core tile), the other candidates on their own rows;
+ * only scores >= tau are written.  Same output either way.
  * row_status: device [M] int32 or NULL.  stats: device dosa_stats or NULL
  * (counters are added to, not overwritten). */
 typedef struct dosa_params {
@@ -169,6 +174,7 @@ typedef struct dosa_params {
   float act_freq_min;         /* 0.5 */
   float margin_gamma;         /* relative rounding margin (2^-10) */
   int32_t candidate_capacity; /* per-row candidate list length */
+  int32_t group_stream;       /* 1: shared candidate stream for groups of four rows (shared keys) */
 } dosa_params;
 
 typedef struct dosa_stats {
@@ -178,6 +184,8 @@ typedef struct dosa_stats {
   unsigned long long survivors;   /* rescored keys with s >= tau */
   unsigned long long fallback_rows;
   unsigned long long skipped_rows;  /* rows whose bound scan was skipped (predicted overflow) */
+  unsigned long long group_keys;  /* shared stream: keys scored once for a group of four rows */
+  unsigned long long solo_keys;   /* shared stream: candidates scored on their own row */
 } dosa_stats;
 
 size_t dosa_topk_workspace_size(const idx_problem* p, int32_t K, const dosa_params* dp, int32_t seed_ld);

@@ -45,13 +45,16 @@ class idx_problem(ctypes.Structure):
 class dosa_params(ctypes.Structure):
     _fields_ = [("n_seed", ctypes.c_int32), ("retained_heads", ctypes.c_int32), ("n_sample", ctypes.c_int32),
                 ("act_freq_min", ctypes.c_float), ("margin_gamma", ctypes.c_float),
-                ("candidate_capacity", ctypes.c_int32)]
+                ("candidate_capacity", ctypes.c_int32), ("group_stream", ctypes.c_int32)]
 
 
 class dosa_stats(ctypes.Structure):
     _fields_ = [("pairs", ctypes.c_ulonglong), ("seeds", ctypes.c_ulonglong), ("candidates", ctypes.c_ulonglong),
                 ("survivors", ctypes.c_ulonglong), ("fallback_rows", ctypes.c_ulonglong),
-                ("skipped_rows", ctypes.c_ulonglong)]
+                ("skipped_rows", ctypes.c_ulonglong), ("group_keys", ctypes.c_ulonglong),
+                ("solo_keys", ctypes.c_ulonglong)]
+
+DOSA_STATS_FIELDS = len(dosa_stats._fields_)   # int64 counters of a device dosa_stats
 
 
 class topk_prior_stats(ctypes.Structure):
@@ -265,8 +268,9 @@ def idx_topk_scores(scores: torch.Tensor, lens: torch.Tensor, max_len: int, K: i
 
 
 def make_dosa_params(n_seed=12288, retained_heads=16, n_sample=128, act_freq_min=0.5, margin_gamma=2.0 ** -10,
-                     candidate_capacity=16384) -> dosa_params:
-    return dosa_params(n_seed, retained_heads, n_sample, act_freq_min, margin_gamma, candidate_capacity)
+                     candidate_capacity=16384, group_stream=1) -> dosa_params:
+    return dosa_params(n_seed, retained_heads, n_sample, act_freq_min, margin_gamma, candidate_capacity,
+                       group_stream)
 
 
 def dosa_topk_workspace_size(p: Problem, K: int, dp: dosa_params, seed_ld: int = 0) -> int:

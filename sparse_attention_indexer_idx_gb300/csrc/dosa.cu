@@ -21,7 +21,12 @@
 //              margin, plus gamma * (sum_h |w_h| ||q_h|| + ||a_A||);
 //   bound scan the tensor-core kernel in bound mode: U >= tau keeps a key;
 //   rescoring  the candidates scored exactly (gathered tiles, same MMA shape
-//              per pair); survivors have s >= tau (section 2 step 3);
+//              per pair); survivors have s >= tau (section 2 step 3).  With the
+//              shared stream (section 4, one key sequence): queries in groups
+//              of four; a candidate that at least two rows of the group kept
+//              and that all of them can see is scored once for the four (one
+//              MMA tile, N = 4H), the rest on their own rows' lists, and only
+//              records with s >= tau are written;
 //   merge      exact top-K of the seed top-K plus the survivors;
 //   fallback   rows with too few seeds or an overflowing candidate list are
 //              recomputed on the unpruned path.
@@ -589,16 +594,19 @@ __global__ void clamp_cnt_kernel(const int32_t* cand_cnt, const int32_t* status,
 }
 
 // Row m of the merge input: the seed top-K then the rescored candidates (those
-// below tau become -inf); also the fallback mask and the survivor count.
+// below tau become -inf); also the fallback mask and the survivor count.  With
+// the shared stream (app_cnt given) the row's own candidates are already in
+// place at K.. and the shared stream's survivors follow them up to app_cnt[m].
 __global__ void merge_rows_kernel(int64_t M, int K, int64_t cap, const int32_t* stop_ids, const float* stop_sc,
                                   const int32_t* cand, const int32_t* cand_n, const float* cand_sc, const float* tau,
-                                  const int32_t* status, float* mrg_sc, int32_t* mrg_id, int32_t* mrg_len,
-                                  int32_t* fbmask, unsigned long long* survivors) {
+                                  const int32_t* status, const int32_t* app_cnt, float* mrg_sc, int32_t* mrg_id,
+                                  int32_t* mrg_len, int32_t* fbmask, unsigned long long* survivors) {
   const int64_t m = blockIdx.x;
   const int64_t ld = K + cap;
   const bool ok = status[m] == 0;
+  const int64_t napp = app_cnt ? (app_cnt[m] < cap ? app_cnt[m] : cap) : cand_n[m];
   if (threadIdx.x == 0) {
-    mrg_len[m] = ok ? K + cand_n[m] : 0;
+    mrg_len[m] = ok ? (int32_t)(K + napp) : 0;
     fbmask[m] = ok ? 0 : 1;
   }
   if (!ok) return;
@@ -614,10 +622,150 @@ __global__ void merge_rows_kernel(int64_t M, int K, int64_t cap, const int32_t* 
     const bool keep = s >= t;
     surv += keep ? 1ull : 0ull;
     mrg_sc[m * ld + K + i] = keep ? s : -__int_as_float(0x7f800000);
-    mrg_id[m * ld + K + i] = cand[m * cap + i];
+    if (!app_cnt) mrg_id[m * ld + K + i] = cand[m * cap + i];
   }
+  if (app_cnt && threadIdx.x == 0) surv += (unsigned long long)(napp - n);
   for (int o = 16; o > 0; o >>= 1) surv += __shfl_xor_sync(0xffffffffu, surv, o);
   if ((threadIdx.x & 31) == 0 && surv) atomicAdd(survivors, surv);
+}
+
+// ---------------------------------------------------------- shared stream --
+
+constexpr int kGrpThreads = 1024;
+constexpr int kGrpWords = 2 * kGrpThreads;      // bitmap words per row and pass (two per thread)
+constexpr int kGrpChunk = 32 * kGrpWords;       // keys per pass
+
+// One block per group g (rows 4g..4g+3).  Over the key range, in passes of
+// kGrpChunk ids: each row's candidates as a bitmap; a key kept by at least two
+// rows and below every row's visible length goes to the group list (glist,
+// ascending), each row's other candidates to its own list (solo, ascending).
+// Rows with status != 0 take no part.  app_cnt[m] = solo_n[m]: where the
+// shared stream's survivors of row m start.
+__global__ void __launch_bounds__(kGrpThreads) group_split_kernel(
+    idx_problem p, int64_t cap, const int32_t* cand, const int32_t* cand_n, const int32_t* status, int32_t* solo,
+    int64_t solo_ld, int32_t* solo_n, int32_t* app_cnt, int32_t* glist, int32_t* gcnt, int64_t capg,
+    unsigned long long* st_group, unsigned long long* st_solo) {
+  __shared__ uint32_t bm[4][kGrpWords];
+  __shared__ int32_t s_warp[32][5];
+  __shared__ int32_t s_tot[5], s_base[5], s_n[4];
+  __shared__ int32_t s_common, s_maxlen;
+  const int64_t g = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid == 0) {
+    int common = 0x7fffffff, mx = 0;
+    for (int i = 0; i < 4; ++i) {
+      const int64_t m = 4 * g + i;
+      int n = 0;
+      if (m < p.M && status[m] == 0) {
+        int64_t off;
+        int len;
+        row_extent(p, m, &off, &len);
+        common = len < common ? len : common;
+        mx = len > mx ? len : mx;
+        n = cand_n[m];
+      }
+      s_n[i] = n;
+    }
+    s_common = common == 0x7fffffff ? 0 : common;
+    s_maxlen = mx;
+    for (int v = 0; v < 5; ++v) s_base[v] = 0;
+  }
+  __syncthreads();
+  const int common = s_common, maxlen = s_maxlen;
+  for (int c0 = 0; c0 < maxlen; c0 += kGrpChunk) {
+    for (int i = tid; i < 4 * kGrpWords; i += kGrpThreads) (&bm[0][0])[i] = 0u;
+    __syncthreads();
+    for (int i = 0; i < 4; ++i) {
+      const int64_t m = 4 * g + i;
+      const int n = s_n[i];
+      for (int j = tid; j < n; j += kGrpThreads) {
+        const int id = cand[m * cap + j];
+        if (id >= c0 && id - c0 < kGrpChunk) atomicOr(&bm[i][(id - c0) >> 5], 1u << (id & 31));
+      }
+    }
+    __syncthreads();
+    uint32_t sh[2], so[4][2];
+    int cnt[5] = {0, 0, 0, 0, 0};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int w = 2 * tid + e;
+      const uint32_t b0 = bm[0][w], b1 = bm[1][w], b2 = bm[2][w], b3 = bm[3][w];
+      const uint32_t two = (b0 & b1) | (b0 & b2) | (b0 & b3) | (b1 & b2) | (b1 & b3) | (b2 & b3);
+      const int nv = common - (c0 + 32 * w);   // keys of this word below the common length
+      const uint32_t vis = nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
+      sh[e] = two & vis;
+      so[0][e] = b0 & ~sh[e];
+      so[1][e] = b1 & ~sh[e];
+      so[2][e] = b2 & ~sh[e];
+      so[3][e] = b3 & ~sh[e];
+      cnt[0] += __popc(sh[e]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cnt[1 + i] += __popc(so[i][e]);
+    }
+    // block exclusive scan of the five counts (warp scans, then a scan of the warp totals)
+    int incl[5];
+#pragma unroll
+    for (int v = 0; v < 5; ++v) {
+      int x = cnt[v];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      incl[v] = x;
+      if (lane == 31) s_warp[wid][v] = x;
+    }
+    __syncthreads();
+    if (wid == 0) {
+#pragma unroll
+      for (int v = 0; v < 5; ++v) {
+        const int t = s_warp[lane][v];
+        int x = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        s_warp[lane][v] = x - t;
+        if (lane == 31) s_tot[v] = x;
+      }
+    }
+    __syncthreads();
+    int pos[5];
+#pragma unroll
+    for (int v = 0; v < 5; ++v) pos[v] = s_base[v] + s_warp[wid][v] + incl[v] - cnt[v];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int k0 = c0 + 32 * (2 * tid + e);
+      for (uint32_t b = sh[e]; b; b &= b - 1) {
+        if (pos[0] < capg) glist[g * capg + pos[0]] = k0 + __ffs(b) - 1;
+        ++pos[0];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t m = 4 * g + i;
+        for (uint32_t b = so[i][e]; b; b &= b - 1) solo[m * solo_ld + pos[1 + i]++] = k0 + __ffs(b) - 1;
+      }
+    }
+    __syncthreads();
+    if (tid == 0)
+      for (int v = 0; v < 5; ++v) s_base[v] += s_tot[v];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const int ng = s_base[0] < capg ? s_base[0] : (int)capg;
+    gcnt[g] = ng;
+    unsigned long long ns = 0;
+    for (int i = 0; i < 4; ++i) {
+      const int64_t m = 4 * g + i;
+      if (m >= p.M) break;
+      solo_n[m] = s_base[1 + i];
+      app_cnt[m] = s_base[1 + i];
+      ns += (unsigned long long)s_base[1 + i];
+    }
+    if (st_group) atomicAdd(st_group, (unsigned long long)ng);
+    if (st_solo) atomicAdd(st_solo, ns);
+  }
 }
 
 __global__ void stats_kernel(idx_problem p, const int32_t* seed_cnt, int shared_seeds, const int32_t* cand_cnt,
@@ -689,6 +837,10 @@ struct DosaWs {
   int32_t* fbmask;
   unsigned long long* surv;
   float* fb_scores;
+  int32_t* glist;          // shared stream: [G, 2 cap] group lists
+  int32_t* gcnt;           // [G]
+  int32_t* solo_n;         // [M] own-list lengths
+  int32_t* app_cnt;        // [M] merge-row fill after the shared stream
   char* tk_ws;
   // (surv is the survivor counter used when the caller passes no stats)
   size_t used;
@@ -696,6 +848,8 @@ struct DosaWs {
 
 struct DosaShape {
   bool shared_keys, shared_seeds;
+  bool group;         // shared candidate stream (groups of four rows)
+  int64_t G;          // groups
   int64_t W;          // bitmap words per row
   int64_t NS;         // seed list capacity per row
   int64_t cap;        // candidate capacity per row
@@ -713,6 +867,8 @@ static DosaShape dosa_shape(const idx_problem& p, int K, const dosa_params& dp, 
   s.NS = ns < s.ldmax ? ns : s.ldmax;
   if (s.NS < 1) s.NS = 1;
   s.cap = dp.candidate_capacity > 0 ? dp.candidate_capacity : 1;
+  s.group = dp.group_stream != 0 && p.M >= 2 && group_stream_supported(p);
+  s.G = s.group ? (p.M + 3) / 4 : 0;
   return s;
 }
 
@@ -755,6 +911,10 @@ static DosaWs carve(void* base, const idx_problem& p, int K, const dosa_params& 
   w.fbmask = c.take<int32_t>(M);
   w.surv = c.take<unsigned long long>(1);
   w.fb_scores = c.take<float>((size_t)M * s.ldmax);
+  w.glist = c.take<int32_t>(s.group ? (size_t)s.G * 2 * s.cap : 1);
+  w.gcnt = c.take<int32_t>(s.group ? (size_t)s.G : 1);
+  w.solo_n = c.take<int32_t>(s.group ? (size_t)M : 1);
+  w.app_cnt = c.take<int32_t>(s.group ? (size_t)M : 1);
   size_t tk = topk_dense_ws(M, (int)s.ldmax, K);
   size_t tk2 = topk_dense_ws(M, (int)(K + s.cap), K);
   size_t tk3 = topk_dense_ws(M, (int)s.NS, K);
@@ -895,10 +1055,26 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
 
   // ---- exact rescoring of the candidates, merge with the seed top-K
   clamp_cnt_kernel<<<grid_for(M, 256), 256, 0, st>>>(w.cand_cnt, w.status, w.cand_n, M, s.cap);
-  DOSA_CHECK(launch_score_gather(p, w.cand, w.cand_n, s.cap, w.cand_sc, s.cap, w.active, st));
-  merge_rows_kernel<<<(unsigned)M, 256, 0, st>>>(M, K, s.cap, w.stop_ids, w.stop_sc, w.cand, w.cand_n, w.cand_sc,
-                                                  w.tau, w.status, w.mrg_sc, w.mrg_id, w.mrg_len, w.fbmask,
-                                                  stats ? &stats->survivors : w.surv);
+  if (s.group) {
+    // shared stream: own lists straight into the merge rows (at K), group lists scored once per group,
+    // their survivors appended behind each row's own candidates
+    const int64_t mld = K + s.cap;
+    group_split_kernel<<<(unsigned)s.G, kGrpThreads, 0, st>>>(
+        p, s.cap, w.cand, w.cand_n, w.status, w.mrg_id + K, mld, w.solo_n, w.app_cnt, w.glist, w.gcnt, 2 * s.cap,
+        stats ? &stats->group_keys : nullptr, stats ? &stats->solo_keys : nullptr);
+    DOSA_CHECK(cudaGetLastError());
+    DOSA_CHECK(launch_score_gather(p, w.mrg_id + K, w.solo_n, mld, w.cand_sc, s.cap, w.active, st));
+    DOSA_CHECK(launch_score_group(p, w.glist, w.gcnt, 2 * s.cap, w.bits, s.shared_seeds ? 0 : s.W, w.tau, w.status,
+                                  w.mrg_id + K, w.mrg_sc + K, w.app_cnt, mld, s.cap, st));
+    merge_rows_kernel<<<(unsigned)M, 256, 0, st>>>(M, K, s.cap, w.stop_ids, w.stop_sc, nullptr, w.solo_n, w.cand_sc,
+                                                    w.tau, w.status, w.app_cnt, w.mrg_sc, w.mrg_id, w.mrg_len,
+                                                    w.fbmask, stats ? &stats->survivors : w.surv);
+  } else {
+    DOSA_CHECK(launch_score_gather(p, w.cand, w.cand_n, s.cap, w.cand_sc, s.cap, w.active, st));
+    merge_rows_kernel<<<(unsigned)M, 256, 0, st>>>(M, K, s.cap, w.stop_ids, w.stop_sc, w.cand, w.cand_n, w.cand_sc,
+                                                    w.tau, w.status, nullptr, w.mrg_sc, w.mrg_id, w.mrg_len,
+                                                    w.fbmask, stats ? &stats->survivors : w.surv);
+  }
   DOSA_CHECK(cudaGetLastError());
   DOSA_CHECK(launch_topk_dense(w.mrg_sc, K + s.cap, w.mrg_len, nullptr, M, (int)(K + s.cap), K, out_ids, out_scores,
                                w.tk_ws, st, w.mrg_id, K + s.cap));

@@ -60,6 +60,17 @@ cudaError_t launch_score_tc(const idx_problem& p, float* scores, int64_t ld, con
 // for list position i < cnt[m] of row m, keys key_off[m] + list[m*gld + i].
 cudaError_t launch_score_gather(const idx_problem& p, const int32_t* list, const int32_t* cnt, int64_t gld,
                                 float* scores, int64_t ld, const int32_t* row_mask, cudaStream_t st);
+// Shared candidate stream: group g = rows 4g..4g+3 over one key sequence scores
+// the keys list[g*gld + i], i < cnt[g]; row m keeps (id, score) when id is
+// visible to it, not a seed (seedbits, row stride seed_stride words, 0: shared)
+// and the score reaches tau[m], appending at out_*[m*out_ld + out_cnt[m]++]
+// (positions >= cap are dropped and set status bit 2); rows with status != 0
+// keep nothing.  Shared keys, tensor-core shapes with 4 queries per MMA tile.
+bool group_stream_supported(const idx_problem& p);
+cudaError_t launch_score_group(const idx_problem& p, const int32_t* list, const int32_t* cnt, int64_t gld,
+                               const uint32_t* seedbits, int64_t seed_stride, const float* tau, int32_t* status,
+                               int32_t* out_ids, float* out_sc, int32_t* out_cnt, int64_t out_ld, int64_t cap,
+                               cudaStream_t st);
 // DoSA bound scan over prepared vectors prep.q = [M, 32, 128] bf16.
 cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const float* coef, const float* tau,
                          const uint32_t* seedbits, int64_t seed_stride, int32_t* cand, int32_t* cand_cnt,

@@ -28,6 +28,14 @@
 //           keys list[m][t*128 + i], fetched by TMA tile::gather4 (four rows
 //           per instruction) straight into the swizzled tile.  Used to rescore
 //           DoSA candidates; output is indexed by list position.
+//  kGroup   the shared candidate stream of the same page (section 4): a group
+//           of four consecutive queries over one key sequence and one list of
+//           keys (list[g][i], ascending, visible to all four); every key of the
+//           list is scored for the four queries in one tile, and a query keeps
+//           (id, score) only when the key is visible to it, is not one of its
+//           seeds and its exact score reaches tau[m].
+//  kFilter  the dense score of every visible key of a row, kept as (id, score)
+//           only when it reaches tau[m] (decode with a prior).
 //  kBound   DoSA's safe upper bound (same page, sections 2, 3.1, 3.2): B holds
 //           per query R retained head vectors (rows 0..R-1) and the |w|-folded
 //           negative aggregate (row 31); the epilogue evaluates
@@ -62,7 +70,7 @@
 
 namespace idx {
 
-enum TcMode { kScore = 0, kGather = 1, kBound = 2, kFilter = 3 };
+enum TcMode { kScore = 0, kGather = 1, kBound = 2, kFilter = 3, kGroup = 4 };
 
 struct TcArgs {
   idx_problem p;              // p.q is the B source: queries, or prepared vectors (kBound)
@@ -70,6 +78,7 @@ struct TcArgs {
   int64_t ld;
   int64_t G;                  // groups
   // kGather: row m's keys are key_base(m) + list[m*gld + i], i < cnt[m]
+  // kGroup: group g's keys are list[g*gld + i], i < cnt[g]
   const int32_t* list;
   const int32_t* cnt;
   int64_t gld;
@@ -79,11 +88,12 @@ struct TcArgs {
   const float* tau;           // [M]
   const uint32_t* seedbits;   // seed bitmap, row stride seed_stride words (0: one shared bitmap)
   int64_t seed_stride;
-  int32_t* cand;              // [M, cap] candidate ids
-  int32_t* cand_cnt;          // [M]
+  int32_t* cand;              // [M, cand_ld] candidate ids (cand_ld 0: cap)
+  int32_t* cand_cnt;          // [M] (kGroup: starts at the row's first free slot)
   int64_t cap;
+  int64_t cand_ld;
   int32_t* status;            // [M] bit 1: candidate overflow
-  float* cand_sc;             // kFilter: [M, cap] scores of the candidates (cand: their ids)
+  float* cand_sc;             // kFilter, kGroup: scores of the kept keys (cand: their ids)
   const int32_t* row_mask;    // optional [M]: rows with row_mask[m] == 0 are skipped
   int R;
 };
@@ -100,9 +110,11 @@ struct TcCfg {
   static constexpr int NQ = NQ_;
   static constexpr int MODE = MODE_;
   static constexpr bool FP8 = (KDT == IDX_FP8_E4M3);
-  static constexpr bool GATHER = (MODE == kGather);
+  static constexpr bool GATHER = (MODE == kGather || MODE == kGroup);   // keys fetched by list entries
+  static constexpr bool GROUP = (MODE == kGroup);
   static constexpr bool BOUND = (MODE == kBound);
   static constexpr bool FILTER = (MODE == kFilter);   // scores >= tau[m] appended as (id, score)
+  static constexpr bool APPEND = FILTER || GROUP;       // the score modes whose output is a kept list
   static constexpr int NCOLX = FP8 ? 2 * NCOL : NCOL;   // MMA columns per query (hi, lo for FP8)
   static constexpr int N = NQ * NCOLX;
   // 128-key subtiles per work unit: FP8 per-row scoring takes 256 keys (32 KB,
@@ -175,7 +187,7 @@ struct TcSched {
 template <class C>
 __device__ __forceinline__ int64_t tc_group_tiles(const TcArgs& A, int64_t g, bool report = false) {
   if (C::GATHER) {
-    if (A.row_mask && !A.row_mask[g]) return 0;
+    if (!C::GROUP && A.row_mask && !A.row_mask[g]) return 0;
     const int32_t c = A.cnt[g];
     return c > 0 ? (c + 127) / 128 : 0;
   }
@@ -334,6 +346,32 @@ __device__ __forceinline__ float query_amax(const uint16_t* q) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   return mx;
+}
+
+// Warp-collective: the lanes with keep set append (id, val) to row m's list
+// (one atomic per warp); a list that would pass cap sets status bit 2.
+__device__ __forceinline__ void tc_append(const TcArgs& A, int64_t m, bool keep, int32_t id, float val) {
+  const int lane = threadIdx.x & 31;
+  const unsigned mask = __ballot_sync(0xffffffffu, keep);
+  if (!mask) return;
+  int32_t basepos = 0;
+  if (lane == 0) basepos = atomicAdd(&A.cand_cnt[m], __popc(mask));
+  basepos = __shfl_sync(0xffffffffu, basepos, 0);
+  if (lane == 0 && basepos + __popc(mask) > A.cap) atomicOr(&A.status[m], 2);
+  if (keep) {
+    const int64_t pos = basepos + __popc(mask & ((1u << lane) - 1u));
+    if (pos < A.cap) {
+      const int64_t at = m * (A.cand_ld ? A.cand_ld : A.cap) + pos;
+      A.cand[at] = id;
+      if (A.cand_sc) A.cand_sc[at] = val;
+    }
+  }
+}
+
+// Seed bit of key id in row m (seed_stride 0: one bitmap for all rows).
+__device__ __forceinline__ bool tc_is_seed(const TcArgs& A, int64_t m, int32_t id) {
+  const uint32_t word = A.seedbits[(A.seed_stride ? m * A.seed_stride : 0) + (id >> 5)];
+  return (word >> (id & 31)) & 1u;
 }
 
 // ------------------------------------------------------------- the kernel ---
@@ -645,6 +683,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     TcUnits<C> u;
     u.init(args, s);
     int64_t cur_g = -1;
+    int32_t gcnt_e = 0;                        // kGroup: the group's list length
     uint32_t nacc = 0, ngrp = 0;
     while (u.valid()) {
       if (u.g != cur_g) {
@@ -681,7 +720,11 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           int64_t off = 0;
           int len = 0;
           if (m < args.p.M) {
-            if (C::GATHER) {
+            if (C::GROUP) {
+              // visible extent; a row already sent to the unpruned path keeps nothing
+              row_extent(args.p, m, &off, &len);
+              if (args.status[m] != 0) len = 0;
+            } else if (C::GATHER) {
               len = args.cnt[m];
               off = tc_key_base(args, m);
             } else {
@@ -692,8 +735,9 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           sLen[lane] = len;
           sBase[lane] = off;
           if (C::BOUND) sAux[4 * lane] = m < args.p.M ? args.coef[m] : 0.0f;
-          if (C::BOUND || C::FILTER) sAux[4 * lane + 1] = m < args.p.M ? args.tau[m] : 0.0f;
+          if (C::BOUND || C::APPEND) sAux[4 * lane + 1] = m < args.p.M ? args.tau[m] : 0.0f;
         }
+        if (C::GROUP) gcnt_e = args.cnt[cur_g];
         __syncwarp();
       }
       if (C::NQ == 1 && C::SUB == 1 && (int)(nacc & 1) != tile_par) {
@@ -707,6 +751,9 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       // wait so that the load overlaps it (words cover max_key_len keys)
       uint32_t sword = 0;
       if (C::BOUND && args.seed_stride == 0 && key < args.p.max_key_len) sword = __ldg(args.seedbits + (key >> 5));
+      // kGroup: the key id at this list position (-1 past the list), read before the wait
+      int32_t kid = -1;
+      if (C::GROUP && key < gcnt_e) kid = __ldg(args.list + cur_g * args.gld + key);
       bool got = mbar_wait(&acc_full[acc], (nacc / C::SACC) & 1, abort_flag);
       // the key-tile slot of this unit (bound: read below for ||k||, so the slot is
       // held until this warp releases it) and its scale slot (FP8)
@@ -798,8 +845,17 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           }
           float sa, sb;
           f2_unpack(s2, &sa, &sb);
-          if (key < sLen[qi]) args.scores[ma * args.ld + key] = sa;
-          if (mb < args.p.M && key < sLen[qb]) args.scores[mb * args.ld + key] = sb;
+          if constexpr (C::GROUP) {
+            tc_append(args, ma,
+                      kid >= 0 && kid < sLen[qi] && !(sa < sAux[4 * qi + 1]) && !tc_is_seed(args, ma, kid), kid, sa);
+            if (mb < args.p.M)
+              tc_append(args, mb,
+                        kid >= 0 && kid < sLen[qb] && !(sb < sAux[4 * qb + 1]) && !tc_is_seed(args, mb, kid), kid,
+                        sb);
+          } else {
+            if (key < sLen[qi]) args.scores[ma * args.ld + key] = sa;
+            if (mb < args.p.M && key < sLen[qb]) args.scores[mb * args.ld + key] = sb;
+          }
         }
       } else
 #pragma unroll 1
@@ -871,21 +927,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           const float val = C::FP8 ? (sc * sAux[4 * qi + 2]) * kscale : sc;
           if constexpr (C::FILTER) {
             // the same value the dense mode writes; kept iff >= tau (warp ballot, one atomic per warp)
-            const bool is_cand = key < len && !(val < sAux[4 * qi + 1]);
-            const unsigned mask = __ballot_sync(0xffffffffu, is_cand);
-            if (mask) {
-              int32_t basepos = 0;
-              if (lane == 0) basepos = atomicAdd(&args.cand_cnt[m], __popc(mask));
-              basepos = __shfl_sync(0xffffffffu, basepos, 0);
-              if (lane == 0 && basepos + __popc(mask) > args.cap) atomicOr(&args.status[m], 2);
-              if (is_cand) {
-                const int64_t pos = basepos + __popc(mask & ((1u << lane) - 1u));
-                if (pos < args.cap) {
-                  args.cand[m * args.cap + pos] = key;
-                  args.cand_sc[m * args.cap + pos] = val;
-                }
-              }
-            }
+            tc_append(args, m, key < len && !(val < sAux[4 * qi + 1]), key, val);
+          } else if constexpr (C::GROUP) {
+            tc_append(args, m, kid >= 0 && kid < len && !(val < sAux[4 * qi + 1]) && !tc_is_seed(args, m, kid), kid,
+                      val);
           } else if (key < len) {
             args.scores[m * args.ld + key] = val;
           }
@@ -913,17 +958,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
             const bool seed = (word >> (key & 31)) & 1u;
             is_cand = !seed && !(ub < sAux[4 * qi + 1]);
           }
-          const unsigned mask = __ballot_sync(0xffffffffu, is_cand);
-          if (mask) {
-            int32_t basepos = 0;
-            if (lane == 0) basepos = atomicAdd(&args.cand_cnt[m], __popc(mask));
-            basepos = __shfl_sync(0xffffffffu, basepos, 0);
-            if (lane == 0 && basepos + __popc(mask) > args.cap) atomicOr(&args.status[m], 2);
-            if (is_cand) {
-              const int64_t pos = basepos + __popc(mask & ((1u << lane) - 1u));
-              if (pos < args.cap) args.cand[m * args.cap + pos] = key;
-            }
-          }
+          tc_append(args, m, is_cand, key, 0.0f);
         }
       }
       tc_fence_before();

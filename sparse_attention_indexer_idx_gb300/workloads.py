@@ -225,7 +225,8 @@ def decode_bf16(seed: int = 2, M: int = 64, H: int = 32, D: int = 128, L: int = 
 
 def prefill_bf16(seed: int = 3, n_queries: int = 4096, H: int = 64, D: int = 128,
                  L: int = 65536, K: int = 2048, n_centres: int = 64, sigma: float = 0.3,
-                 n_seed: int = 12288, R: int = 16, q_noise: Optional[float] = None) -> IndexerProblem:
+                 n_seed: int = 12288, R: int = 16, q_noise: Optional[float] = None,
+                 q_run: int = 1, positive_w: bool = False) -> IndexerProblem:
     """Causal prefill: queries at positions L-n..L-1 over one shared key sequence.
 
     Keys: with probability 1/2 a cluster key c_z + sigma*eps (z uniform over
@@ -234,6 +235,8 @@ def prefill_bf16(seed: int = 3, n_queries: int = 4096, H: int = 64, D: int = 128
     share one direction, q_{m,h} = a_{m,h} c_{z_m} + q_noise * eps with
     a = |N(0, 1)| and z_m uniform over the centres (heads of a trained indexer
     are strongly correlated; this is the structure the anchor bound uses).
+    q_run > 1: runs of q_run consecutive queries share their centre (neighbouring
+    positions of a prompt look for the same content).  positive_w: w = |w|.
     """
     rng = np.random.default_rng(seed)
     centres = _normal(rng, (n_centres, D))
@@ -245,11 +248,16 @@ def prefill_bf16(seed: int = 3, n_queries: int = 4096, H: int = 64, D: int = 128
     if q_noise is None:
         q = _bulk_bf16(_normal(rng, (n_queries, H, D)))
     else:
-        zq = rng.integers(0, n_centres, n_queries)
+        if q_run > 1:
+            zq = np.repeat(rng.integers(0, n_centres, -(-n_queries // q_run)), q_run)[:n_queries]
+        else:
+            zq = rng.integers(0, n_centres, n_queries)
         amp = np.abs(_normal(rng, (n_queries, H)))
         qf = amp[:, :, None] * centres[zq][:, None, :] + np.float32(q_noise) * _normal(rng, (n_queries, H, D))
         q = _bulk_bf16(qf.astype(np.float32))
     w = _normal(rng, (n_queries, H), std=float(np.sqrt(1.0 / H)))
+    if positive_w:
+        w = np.abs(w)
     pos = np.arange(L - n_queries, L, dtype=np.int64)
     key_len = (pos + 1).astype(np.int32)
     return IndexerProblem("prefill_bf16", "bf16", q, w, keys, key_len, None, K,

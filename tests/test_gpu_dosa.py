@@ -35,7 +35,7 @@ def _pruned(B, p, K, seed_ids=None, **kw):
     ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
     sc = torch.empty((M, K), dtype=torch.float32, device="cuda")
     st = torch.full((M,), -7, dtype=torch.int32, device="cuda")
-    stats = torch.zeros(6, dtype=torch.int64, device="cuda")
+    stats = torch.zeros(B.DOSA_STATS_FIELDS, dtype=torch.int64, device="cuda")
     sld = 0 if seed_ids is None else seed_ids.shape[1]
     ws = torch.empty(B.dosa_topk_workspace_size(p, K, dp, sld), dtype=torch.uint8, device="cuda")
     B.dosa_topk(p, K, dp, ids, sc, ws, seed_ids=seed_ids, row_status=st, stats=stats)
@@ -152,3 +152,83 @@ def test_unsupported_shape_takes_the_exact_path(B):
     d_ids, d_sc, st, _ = _pruned(B, p, wp.K, n_seed=64, retained_heads=2)
     _same(*u, d_ids, d_sc)
     assert (st == 1).all()
+
+
+def _as_fp8_keys(wp):
+    """The same problem with its keys quantised per token to e4m3 codes and a scale."""
+    k = wp.keys_f32()
+    amax = np.abs(k).max(axis=1)
+    sc = np.where(amax > 0, amax / np.float32(wl.E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    codes = wl.f32_to_e4m3_bits(np.clip(k / sc[:, None], -wl.E4M3_MAX, wl.E4M3_MAX))
+    return wl.IndexerProblem(wp.name + "_fp8", "fp8", wp.q, wp.w, codes, wp.key_len, None, wp.K, key_scale=sc,
+                             extras=dict(wp.extras))
+
+
+def _stream_counts_hold(on_stats, off_stats):
+    """Every candidate is scored once on its row or once for its group: a group key was kept by two to four
+    rows; both modes see the same candidates and survivors."""
+    cands, group, solo = int(on_stats[2]), int(on_stats[6]), int(on_stats[7])
+    assert group > 0 and solo > 0, on_stats
+    assert solo + 2 * group <= cands <= solo + 4 * group, on_stats
+    assert on_stats[2] == off_stats[2] and on_stats[3] == off_stats[3], (on_stats, off_stats)
+    assert off_stats[6] == 0 and off_stats[7] == 0
+
+
+@pytest.mark.parametrize("H,n_queries", [(64, 40), (32, 23), (16, 18)])
+def test_shared_stream_groups_of_four(B, H, n_queries):
+    """DoSA page section 4: groups of four queries share one exact pass over the keys that at least two of
+    them kept.  Runs of three queries share a direction, so a group holds keys that several rows kept (shared)
+    and keys that one row kept (its own list); a partial last group when n_queries % 4 != 0.  The output stays bit-identical to the unpruned top-K."""
+    wp = wl.prefill_bf16(seed=13 + H, n_queries=n_queries, H=H, D=128, L=8000, K=256, n_seed=1024, R=min(16, H // 2),
+                         q_noise=0.001, q_run=3, positive_w=True)
+    p = B.problem_to_device(wp)
+    u = _unpruned(B, p, wp.K)
+    R = min(16, H // 2)
+    on = _pruned(B, p, wp.K, n_seed=1024, retained_heads=R, candidate_capacity=8000, group_stream=1)
+    off = _pruned(B, p, wp.K, n_seed=1024, retained_heads=R, candidate_capacity=8000, group_stream=0)
+    _same(*u, on[0], on[1])
+    _same(*u, off[0], off[1])
+    assert (on[2] == 0).all() and (off[2] == 0).all()
+    _stream_counts_hold(on[3], off[3])
+    assert B.device_error() == 0
+
+
+def test_shared_stream_fp8_keys(B):
+    """The shared stream over e4m3 keys with a per-token scale (H 32: four queries' hi and lo rows fill
+    N = 256)."""
+    wp = _as_fp8_keys(wl.prefill_bf16(seed=31, n_queries=21, H=32, D=128, L=6000, K=192, n_seed=1024, R=16,
+                                      q_noise=0.001, q_run=3, positive_w=True))
+    p = B.problem_to_device(wp)
+    u = _unpruned(B, p, wp.K)
+    on = _pruned(B, p, wp.K, n_seed=1024, retained_heads=16, candidate_capacity=6000, group_stream=1)
+    off = _pruned(B, p, wp.K, n_seed=1024, retained_heads=16, candidate_capacity=6000, group_stream=0)
+    _same(*u, on[0], on[1])
+    _same(*u, off[0], off[1])
+    assert (on[2] == 0).all()
+    _stream_counts_hold(on[3], off[3])
+    _check_oracle(wp, on[0], on[1], [0, 20])
+    assert B.device_error() == 0
+
+
+def test_shared_stream_per_row_seeds_and_fallback_rows(B):
+    """Caller seeds per row over shared keys: a key can be a seed of one row of a group and a candidate of the
+    others, and the shared pass must not hand it back to the row that already has it.  Rows 5 and 6 get fewer
+    than K seeds and take the unpruned path; their groups still share among the other rows."""
+    wp = wl.prefill_bf16(seed=41, n_queries=16, H=64, D=128, L=7000, K=200, n_seed=1024, R=16, q_noise=0.001,
+                         q_run=4, positive_w=True)
+    rng = np.random.default_rng(41)
+    seeds = np.full((wp.M, 1500), -1, dtype=np.int32)
+    for m in range(wp.M):
+        n = 100 if m in (5, 6) else 1500
+        seeds[m, :n] = rng.choice(int(wp.key_len[m]), n, replace=False)
+    p = B.problem_to_device(wp)
+    u = _unpruned(B, p, wp.K)
+    sd = torch.from_numpy(seeds).cuda()
+    on = _pruned(B, p, wp.K, seed_ids=sd, retained_heads=16, candidate_capacity=7000, group_stream=1)
+    off = _pruned(B, p, wp.K, seed_ids=sd, retained_heads=16, candidate_capacity=7000, group_stream=0)
+    _same(*u, on[0], on[1])
+    _same(*u, off[0], off[1])
+    assert on[2][5] == 1 and on[2][6] == 1
+    assert (np.delete(on[2], [5, 6]) == 0).all()
+    _stream_counts_hold(on[3], off[3])
+    assert B.device_error() == 0

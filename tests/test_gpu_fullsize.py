@@ -37,7 +37,7 @@ def _dosa(B, p, K, **kw):
     ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
     sc = torch.empty((M, K), dtype=torch.float32, device="cuda")
     st = torch.empty((M,), dtype=torch.int32, device="cuda")
-    stats = torch.zeros(6, dtype=torch.int64, device="cuda")
+    stats = torch.zeros(B.DOSA_STATS_FIELDS, dtype=torch.int64, device="cuda")
     ws = torch.empty(B.dosa_topk_workspace_size(p, K, dp), dtype=torch.uint8, device="cuda")
     B.dosa_topk(p, K, dp, ids, sc, ws, row_status=st, stats=stats)
     torch.cuda.synchronize()
