@@ -19,14 +19,17 @@
 //              seed samples and their |w|-weighted aggregate a_A (section 3.2),
 //              a_A rounded to bf16 with the rounding distance added to the
 //              margin, plus gamma * (sum_h |w_h| ||q_h|| + ||a_A||);
-//   bound scan the tensor-core kernel in bound mode: U >= tau keeps a key;
+//   bound scan the tensor-core kernel in bound mode: U >= tau sets the key's
+//              bit in the row's candidate bitmap; compaction turns the bitmap
+//              into an ascending id list (a row over its capacity falls back);
 //   rescoring  the candidates scored exactly (gathered tiles, same MMA shape
 //              per pair); survivors have s >= tau (section 2 step 3).  With the
 //              shared stream (section 4, one key sequence): queries in groups
 //              of four; a candidate that at least two rows of the group kept
 //              and that all of them can see is scored once for the four (one
-//              MMA tile, N = 4H), the rest on their own rows' lists, and only
-//              records with s >= tau are written;
+//              MMA tile, N = 4H), the rest on their own rows' lists; a row
+//              keeps the group records that it can see, that are not its seeds
+//              and whose s >= tau;
 //   merge      exact top-K of the seed top-K plus the survivors;
 //   fallback   rows with too few seeds or an overflowing candidate list are
 //              recomputed on the unpruned path.
@@ -185,14 +188,10 @@ __global__ void caller_seeds_kernel(idx_problem p, const int32_t* seed_ids, int 
   }
 }
 
-// Seed bitmap row -> ascending id list (at most cap entries) and its count.
+// Bitmap row b[0..W) -> ascending id list out[0..cap) (block of kListThreads
+// threads, wsum: 32 words of shared memory); returns the number of set bits.
 constexpr int kListThreads = 1024;
-__global__ void __launch_bounds__(kListThreads) bits_to_list_kernel(const uint32_t* bits, int64_t W, int32_t* list,
-                                                                     int64_t cap, int32_t* cnt) {
-  __shared__ uint32_t wsum[32];
-  const int64_t r = blockIdx.x;
-  const uint32_t* b = bits + r * W;
-  int32_t* out = list + r * cap;
+__device__ int64_t bits_row_to_list(const uint32_t* b, int64_t W, int32_t* out, int64_t cap, uint32_t* wsum) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   int64_t run = 0;
   for (int64_t w0 = 0; w0 < W; w0 += kListThreads) {
@@ -222,7 +221,44 @@ __global__ void __launch_bounds__(kListThreads) bits_to_list_kernel(const uint32
     run += tot;
     __syncthreads();
   }
+  return run;
+}
+
+// Seed bitmap row -> ascending id list (at most cap entries) and its count.
+__global__ void __launch_bounds__(kListThreads) bits_to_list_kernel(const uint32_t* bits, int64_t W, int32_t* list,
+                                                                     int64_t cap, int32_t* cnt) {
+  __shared__ uint32_t wsum[32];
+  const int64_t r = blockIdx.x;
+  const int64_t run = bits_row_to_list(bits + r * W, W, list + r * cap, cap, wsum);
   if (threadIdx.x == 0) cnt[r] = (int32_t)(run < cap ? run : cap);
+}
+
+// Candidate bitmap row m (the words below its visible length) -> ascending id
+// list; cand_cnt = all candidates, cand_n = those to rescore (0 for a row on
+// the unpruned path; a row over cap joins it with status bit 2).
+__global__ void __launch_bounds__(kListThreads) cand_compact_kernel(idx_problem p, const uint32_t* bits, int64_t W,
+                                                                     int32_t* status, int32_t* cand, int64_t cap,
+                                                                     int32_t* cand_cnt, int32_t* cand_n) {
+  __shared__ uint32_t wsum[32];
+  const int64_t m = blockIdx.x;
+  if (status[m] != 0) {
+    if (threadIdx.x == 0) {
+      cand_cnt[m] = 0;
+      cand_n[m] = 0;
+    }
+    return;
+  }
+  int64_t off;
+  int len;
+  row_extent(p, m, &off, &len);
+  int64_t nw = ((int64_t)len + 31) / 32;
+  nw = nw < W ? nw : W;
+  const int64_t run = bits_row_to_list(bits + m * W, nw, cand + m * cap, cap, wsum);
+  if (threadIdx.x == 0) {
+    cand_cnt[m] = (int32_t)run;
+    if (run > cap) status[m] |= 2;
+    cand_n[m] = run > cap ? 0 : (int32_t)run;
+  }
 }
 
 // Copies the shared seed keys (and scales) into a contiguous buffer.
@@ -583,33 +619,37 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
 
 // --------------------------------------------------------------- merging --
 
-// Candidates to rescore per row: none for a row that will take the unpruned
-// path anyway (too few seeds, predicted or actual overflow).
-__global__ void clamp_cnt_kernel(const int32_t* cand_cnt, const int32_t* status, int32_t* cand_n, int64_t M,
-                                 int64_t cap) {
-  for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < M; m += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t c = cand_cnt[m];
-    cand_n[m] = status[m] != 0 ? 0 : (c < cap ? c : (int32_t)cap);
-  }
-}
+// The shared stream's output for the merge: group g's list and the scores of
+// its four rows by list position.
+struct GroupRecs {
+  const int32_t* glist;      // [G, capg] ascending ids (nullptr: no shared stream)
+  const int32_t* gcnt;       // [G]
+  const float* gsc;          // [M, capg]
+  int64_t capg;
+  const uint32_t* seedbits;  // seed bitmap, row stride seed_stride words (0: one for all rows)
+  int64_t seed_stride;
+  idx_problem p;
+};
 
 // Row m of the merge input: the seed top-K then the rescored candidates (those
 // below tau become -inf); also the fallback mask and the survivor count.  With
-// the shared stream (app_cnt given) the row's own candidates are already in
-// place at K.. and the shared stream's survivors follow them up to app_cnt[m].
-__global__ void merge_rows_kernel(int64_t M, int K, int64_t cap, const int32_t* stop_ids, const float* stop_sc,
-                                  const int32_t* cand, const int32_t* cand_n, const float* cand_sc, const float* tau,
-                                  const int32_t* status, const int32_t* app_cnt, float* mrg_sc, int32_t* mrg_id,
-                                  int32_t* mrg_len, int32_t* fbmask, unsigned long long* survivors) {
+// the shared stream the row's own candidates are already in place at K.., and
+// the group records that the row can see, that are not its seeds and whose
+// score reaches tau follow them (in list order).
+constexpr int kMergeThreads = 256;
+__global__ void __launch_bounds__(kMergeThreads) merge_rows_kernel(
+    int64_t M, int K, int64_t cap, const int32_t* stop_ids, const float* stop_sc, const int32_t* cand,
+    const int32_t* cand_n, const float* cand_sc, const float* tau, const int32_t* status, GroupRecs gr, float* mrg_sc,
+    int32_t* mrg_id, int32_t* mrg_len, int32_t* fbmask, unsigned long long* survivors) {
+  __shared__ int32_t s_wcnt[kMergeThreads / 32];
   const int64_t m = blockIdx.x;
   const int64_t ld = K + cap;
   const bool ok = status[m] == 0;
-  const int64_t napp = app_cnt ? (app_cnt[m] < cap ? app_cnt[m] : cap) : cand_n[m];
-  if (threadIdx.x == 0) {
-    mrg_len[m] = ok ? (int32_t)(K + napp) : 0;
-    fbmask[m] = ok ? 0 : 1;
+  if (threadIdx.x == 0) fbmask[m] = ok ? 0 : 1;
+  if (!ok) {
+    if (threadIdx.x == 0) mrg_len[m] = 0;
+    return;
   }
-  if (!ok) return;
   for (int j = threadIdx.x; j < K; j += blockDim.x) {
     mrg_sc[m * ld + j] = stop_sc[m * K + j];
     mrg_id[m * ld + j] = stop_ids[m * K + j];
@@ -622,9 +662,54 @@ __global__ void merge_rows_kernel(int64_t M, int K, int64_t cap, const int32_t* 
     const bool keep = s >= t;
     surv += keep ? 1ull : 0ull;
     mrg_sc[m * ld + K + i] = keep ? s : -__int_as_float(0x7f800000);
-    if (!app_cnt) mrg_id[m * ld + K + i] = cand[m * cap + i];
+    if (!gr.glist) mrg_id[m * ld + K + i] = cand[m * cap + i];
   }
-  if (app_cnt && threadIdx.x == 0) surv += (unsigned long long)(napp - n);
+  int64_t fill = n;
+  if (gr.glist) {
+    // the group's records, compacted in list order behind the row's own candidates
+    const int64_t g = m >> 2;
+    const int gn = gr.gcnt[g];
+    int64_t off;
+    int len;
+    row_extent(gr.p, m, &off, &len);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int i0 = 0; i0 < gn; i0 += kMergeThreads) {
+      const int i = i0 + threadIdx.x;
+      bool keep = false;
+      int32_t id = 0;
+      float s = 0.0f;
+      if (i < gn) {
+        id = gr.glist[g * gr.capg + i];
+        s = gr.gsc[m * gr.capg + i];
+        if (id < len && s >= t) {
+          const uint32_t word = gr.seedbits[(gr.seed_stride ? m * gr.seed_stride : 0) + (id >> 5)];
+          keep = !((word >> (id & 31)) & 1u);
+        }
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (lane == 0) s_wcnt[wid] = __popc(bal);
+      __syncthreads();
+      int64_t pos = fill + __popc(bal & ((1u << lane) - 1u));
+      int tot = 0;
+      for (int w = 0; w < kMergeThreads / 32; ++w) {
+        if (w < wid) pos += s_wcnt[w];
+        tot += s_wcnt[w];
+      }
+      if (keep && pos < cap) {
+        mrg_id[m * ld + K + pos] = id;
+        mrg_sc[m * ld + K + pos] = s;
+      }
+      fill += tot;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) surv += (unsigned long long)(fill - n);
+  }
+  if (threadIdx.x == 0) {
+    // more records than places can only come from a bound that failed: the row then takes the unpruned path
+    const bool over = fill > cap;
+    mrg_len[m] = over ? 0 : (int32_t)(K + fill);
+    if (over) fbmask[m] = 1;
+  }
   for (int o = 16; o > 0; o >>= 1) surv += __shfl_xor_sync(0xffffffffu, surv, o);
   if ((threadIdx.x & 31) == 0 && surv) atomicAdd(survivors, surv);
 }
@@ -632,75 +717,95 @@ __global__ void merge_rows_kernel(int64_t M, int K, int64_t cap, const int32_t* 
 // ---------------------------------------------------------- shared stream --
 
 constexpr int kGrpThreads = 1024;
-constexpr int kGrpWords = 2 * kGrpThreads;      // bitmap words per row and pass (two per thread)
-constexpr int kGrpChunk = 32 * kGrpWords;       // keys per pass
+constexpr int kGrpChunk = 64 * kGrpThreads;     // keys per pass (two bitmap words per thread)
 
-// One block per group g (rows 4g..4g+3).  Over the key range, in passes of
-// kGrpChunk ids: each row's candidates as a bitmap; a key kept by at least two
-// rows and below every row's visible length goes to the group list (glist,
-// ascending), each row's other candidates to its own list (solo, ascending).
-// Rows with status != 0 take no part.  app_cnt[m] = solo_n[m]: where the
-// shared stream's survivors of row m start.
+// One block per group g (rows 4g..4g+3) over the rows' candidate bitmaps (row
+// stride W words, the words below each row's visible length).  A row on the
+// unpruned path (status != 0) takes no part; a row with more than cap
+// candidates joins that path (status bit 2).  Then, in passes of kGrpChunk
+// ids: a key kept by at least two of the remaining rows and below all of their
+// visible lengths goes to the group list (glist, ascending), each row's other
+// candidates to its own list (solo, ascending).  cand_cnt[m] = the row's
+// candidates, solo_n[m] = its own-list length.
 __global__ void __launch_bounds__(kGrpThreads) group_split_kernel(
-    idx_problem p, int64_t cap, const int32_t* cand, const int32_t* cand_n, const int32_t* status, int32_t* solo,
-    int64_t solo_ld, int32_t* solo_n, int32_t* app_cnt, int32_t* glist, int32_t* gcnt, int64_t capg,
-    unsigned long long* st_group, unsigned long long* st_solo) {
-  __shared__ uint32_t bm[4][kGrpWords];
+    idx_problem p, int64_t cap, const uint32_t* bits, int64_t W, int32_t* status, int32_t* cand_cnt, int32_t* solo,
+    int64_t solo_ld, int32_t* solo_n, int32_t* glist, int32_t* gcnt, int64_t capg, unsigned long long* st_group,
+    unsigned long long* st_solo) {
   __shared__ int32_t s_warp[32][5];
-  __shared__ int32_t s_tot[5], s_base[5], s_n[4];
+  __shared__ int32_t s_tot[5], s_base[5];
+  __shared__ int32_t s_len[4], s_nw[4], s_cnt[4];
   __shared__ int32_t s_common, s_maxlen;
   const int64_t g = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid < 4) {
+    const int64_t m = 4 * g + tid;
+    int len = 0, nw = 0;
+    if (m < p.M && status[m] == 0) {
+      int64_t off;
+      row_extent(p, m, &off, &len);
+      const int64_t w = ((int64_t)len + 31) / 32;
+      nw = (int)(w < W ? w : W);
+    }
+    s_len[tid] = len;
+    s_nw[tid] = nw;
+    s_cnt[tid] = 0;
+  }
+  if (tid < 5) s_base[tid] = 0;
+  __syncthreads();
+  // each row's candidate count
+  {
+    int c[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      for (int w = tid; w < s_nw[i]; w += kGrpThreads) c[i] += __popc(bits[(4 * g + i) * W + w]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c[i] += __shfl_xor_sync(0xffffffffu, c[i], o);
+      if (lane == 0 && c[i]) atomicAdd(&s_cnt[i], c[i]);
+    }
+  }
+  __syncthreads();
   if (tid == 0) {
     int common = 0x7fffffff, mx = 0;
     for (int i = 0; i < 4; ++i) {
       const int64_t m = 4 * g + i;
-      int n = 0;
-      if (m < p.M && status[m] == 0) {
-        int64_t off;
-        int len;
-        row_extent(p, m, &off, &len);
-        common = len < common ? len : common;
-        mx = len > mx ? len : mx;
-        n = cand_n[m];
+      if (m >= p.M) break;
+      cand_cnt[m] = s_cnt[i];
+      if (s_nw[i] == 0 && s_len[i] == 0) continue;   // not taking part (or nothing visible)
+      if (s_cnt[i] > cap) {
+        status[m] |= 2;
+        s_nw[i] = 0;
+        s_len[i] = 0;
+        continue;
       }
-      s_n[i] = n;
+      common = s_len[i] < common ? s_len[i] : common;
+      mx = s_len[i] > mx ? s_len[i] : mx;
     }
     s_common = common == 0x7fffffff ? 0 : common;
     s_maxlen = mx;
-    for (int v = 0; v < 5; ++v) s_base[v] = 0;
   }
   __syncthreads();
   const int common = s_common, maxlen = s_maxlen;
   for (int c0 = 0; c0 < maxlen; c0 += kGrpChunk) {
-    for (int i = tid; i < 4 * kGrpWords; i += kGrpThreads) (&bm[0][0])[i] = 0u;
-    __syncthreads();
-    for (int i = 0; i < 4; ++i) {
-      const int64_t m = 4 * g + i;
-      const int n = s_n[i];
-      for (int j = tid; j < n; j += kGrpThreads) {
-        const int id = cand[m * cap + j];
-        if (id >= c0 && id - c0 < kGrpChunk) atomicOr(&bm[i][(id - c0) >> 5], 1u << (id & 31));
-      }
-    }
-    __syncthreads();
     uint32_t sh[2], so[4][2];
     int cnt[5] = {0, 0, 0, 0, 0};
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int w = 2 * tid + e;
-      const uint32_t b0 = bm[0][w], b1 = bm[1][w], b2 = bm[2][w], b3 = bm[3][w];
-      const uint32_t two = (b0 & b1) | (b0 & b2) | (b0 & b3) | (b1 & b2) | (b1 & b3) | (b2 & b3);
-      const int nv = common - (c0 + 32 * w);   // keys of this word below the common length
+      const int w = c0 / 32 + 2 * tid + e;
+      uint32_t b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) b[i] = w < s_nw[i] ? bits[(4 * g + i) * W + w] : 0u;
+      const uint32_t two = (b[0] & b[1]) | (b[0] & b[2]) | (b[0] & b[3]) | (b[1] & b[2]) | (b[1] & b[3]) | (b[2] & b[3]);
+      const int nv = common - 32 * w;          // keys of this word below the common length
       const uint32_t vis = nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
       sh[e] = two & vis;
-      so[0][e] = b0 & ~sh[e];
-      so[1][e] = b1 & ~sh[e];
-      so[2][e] = b2 & ~sh[e];
-      so[3][e] = b3 & ~sh[e];
       cnt[0] += __popc(sh[e]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) cnt[1 + i] += __popc(so[i][e]);
+      for (int i = 0; i < 4; ++i) {
+        so[i][e] = b[i] & ~sh[e];
+        cnt[1 + i] += __popc(so[i][e]);
+      }
     }
     // block exclusive scan of the five counts (warp scans, then a scan of the warp totals)
     int incl[5];
@@ -760,7 +865,6 @@ __global__ void __launch_bounds__(kGrpThreads) group_split_kernel(
       const int64_t m = 4 * g + i;
       if (m >= p.M) break;
       solo_n[m] = s_base[1 + i];
-      app_cnt[m] = s_base[1 + i];
       ns += (unsigned long long)s_base[1 + i];
     }
     if (st_group) atomicAdd(st_group, (unsigned long long)ng);
@@ -837,10 +941,11 @@ struct DosaWs {
   int32_t* fbmask;
   unsigned long long* surv;
   float* fb_scores;
+  uint32_t* candbits;      // [M, cbW] candidate bitmaps of the bound scan
   int32_t* glist;          // shared stream: [G, 2 cap] group lists
   int32_t* gcnt;           // [G]
+  float* gsc;              // [M, 2 cap] scores of the group lists, by position
   int32_t* solo_n;         // [M] own-list lengths
-  int32_t* app_cnt;        // [M] merge-row fill after the shared stream
   char* tk_ws;
   // (surv is the survivor counter used when the caller passes no stats)
   size_t used;
@@ -851,6 +956,7 @@ struct DosaShape {
   bool group;         // shared candidate stream (groups of four rows)
   int64_t G;          // groups
   int64_t W;          // bitmap words per row
+  int64_t cbW;        // candidate bitmap words per row (whole 128-key tiles)
   int64_t NS;         // seed list capacity per row
   int64_t cap;        // candidate capacity per row
   int64_t ldmax;      // max_key_len (>= 1)
@@ -862,6 +968,7 @@ static DosaShape dosa_shape(const idx_problem& p, int K, const dosa_params& dp, 
   s.shared_seeds = s.shared_keys && seed_ld == 0;
   s.ldmax = p.max_key_len > 0 ? p.max_key_len : 1;
   s.W = (s.ldmax + 31) / 32;
+  s.cbW = (s.ldmax + 127) / 128 * 4;
   int64_t ns = seed_ld > 0 ? seed_ld : dp.n_seed;
   if (ns < K) ns = K;
   s.NS = ns < s.ldmax ? ns : s.ldmax;
@@ -911,10 +1018,11 @@ static DosaWs carve(void* base, const idx_problem& p, int K, const dosa_params& 
   w.fbmask = c.take<int32_t>(M);
   w.surv = c.take<unsigned long long>(1);
   w.fb_scores = c.take<float>((size_t)M * s.ldmax);
+  w.candbits = c.take<uint32_t>((size_t)M * s.cbW);
   w.glist = c.take<int32_t>(s.group ? (size_t)s.G * 2 * s.cap : 1);
   w.gcnt = c.take<int32_t>(s.group ? (size_t)s.G : 1);
+  w.gsc = c.take<float>(s.group ? (size_t)M * 2 * s.cap : 1);
   w.solo_n = c.take<int32_t>(s.group ? (size_t)M : 1);
-  w.app_cnt = c.take<int32_t>(s.group ? (size_t)M : 1);
   size_t tk = topk_dense_ws(M, (int)s.ldmax, K);
   size_t tk2 = topk_dense_ws(M, (int)(K + s.cap), K);
   size_t tk3 = topk_dense_ws(M, (int)s.NS, K);
@@ -1045,35 +1153,38 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
   dosa_plan_kernel<<<(unsigned)M, kPlanThreads, psmem, st>>>(pa);
   DOSA_CHECK(cudaGetLastError());
 
-  // ---- bound scan
-  DOSA_CHECK(fill_i32(w.cand_cnt, M, 0, st));
+  // ---- bound scan: candidate bitmaps
   idx_problem prep = p;
   prep.q = w.qprep;
   prep.H = kVec;
-  DOSA_CHECK(launch_bound(prep, w.wfold, w.coef, w.tau, w.bits, s.shared_seeds ? 0 : s.W, w.cand, w.cand_cnt, s.cap,
-                          w.status, dp.retained_heads, w.active, st));
+  DOSA_CHECK(launch_bound(prep, w.wfold, w.coef, w.tau, w.bits, s.shared_seeds ? 0 : s.W, w.candbits, s.cbW,
+                          dp.retained_heads, w.active, st));
 
   // ---- exact rescoring of the candidates, merge with the seed top-K
-  clamp_cnt_kernel<<<grid_for(M, 256), 256, 0, st>>>(w.cand_cnt, w.status, w.cand_n, M, s.cap);
+  GroupRecs gr{};
   if (s.group) {
-    // shared stream: own lists straight into the merge rows (at K), group lists scored once per group,
-    // their survivors appended behind each row's own candidates
-    const int64_t mld = K + s.cap;
+    // shared stream: own lists straight into the merge rows (at K), group lists scored once per group
+    const int64_t mld = K + s.cap, capg = 2 * s.cap;
     group_split_kernel<<<(unsigned)s.G, kGrpThreads, 0, st>>>(
-        p, s.cap, w.cand, w.cand_n, w.status, w.mrg_id + K, mld, w.solo_n, w.app_cnt, w.glist, w.gcnt, 2 * s.cap,
+        p, s.cap, w.candbits, s.cbW, w.status, w.cand_cnt, w.mrg_id + K, mld, w.solo_n, w.glist, w.gcnt, capg,
         stats ? &stats->group_keys : nullptr, stats ? &stats->solo_keys : nullptr);
     DOSA_CHECK(cudaGetLastError());
     DOSA_CHECK(launch_score_gather(p, w.mrg_id + K, w.solo_n, mld, w.cand_sc, s.cap, w.active, st));
-    DOSA_CHECK(launch_score_group(p, w.glist, w.gcnt, 2 * s.cap, w.bits, s.shared_seeds ? 0 : s.W, w.tau, w.status,
-                                  w.mrg_id + K, w.mrg_sc + K, w.app_cnt, mld, s.cap, st));
-    merge_rows_kernel<<<(unsigned)M, 256, 0, st>>>(M, K, s.cap, w.stop_ids, w.stop_sc, nullptr, w.solo_n, w.cand_sc,
-                                                    w.tau, w.status, w.app_cnt, w.mrg_sc, w.mrg_id, w.mrg_len,
-                                                    w.fbmask, stats ? &stats->survivors : w.surv);
+    DOSA_CHECK(launch_score_group(p, w.glist, w.gcnt, capg, w.gsc, capg, st));
+    gr = GroupRecs{w.glist, w.gcnt, w.gsc, capg, w.bits, s.shared_seeds ? 0 : s.W, p};
+    merge_rows_kernel<<<(unsigned)M, kMergeThreads, 0, st>>>(M, K, s.cap, w.stop_ids, w.stop_sc, nullptr, w.solo_n,
+                                                              w.cand_sc, w.tau, w.status, gr, w.mrg_sc, w.mrg_id,
+                                                              w.mrg_len, w.fbmask,
+                                                              stats ? &stats->survivors : w.surv);
   } else {
+    cand_compact_kernel<<<(unsigned)M, kListThreads, 0, st>>>(p, w.candbits, s.cbW, w.status, w.cand, s.cap,
+                                                               w.cand_cnt, w.cand_n);
+    DOSA_CHECK(cudaGetLastError());
     DOSA_CHECK(launch_score_gather(p, w.cand, w.cand_n, s.cap, w.cand_sc, s.cap, w.active, st));
-    merge_rows_kernel<<<(unsigned)M, 256, 0, st>>>(M, K, s.cap, w.stop_ids, w.stop_sc, w.cand, w.cand_n, w.cand_sc,
-                                                    w.tau, w.status, nullptr, w.mrg_sc, w.mrg_id, w.mrg_len,
-                                                    w.fbmask, stats ? &stats->survivors : w.surv);
+    merge_rows_kernel<<<(unsigned)M, kMergeThreads, 0, st>>>(M, K, s.cap, w.stop_ids, w.stop_sc, w.cand, w.cand_n,
+                                                              w.cand_sc, w.tau, w.status, gr, w.mrg_sc, w.mrg_id,
+                                                              w.mrg_len, w.fbmask,
+                                                              stats ? &stats->survivors : w.surv);
   }
   DOSA_CHECK(cudaGetLastError());
   DOSA_CHECK(launch_topk_dense(w.mrg_sc, K + s.cap, w.mrg_len, nullptr, M, (int)(K + s.cap), K, out_ids, out_scores,

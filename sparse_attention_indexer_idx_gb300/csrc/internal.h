@@ -61,20 +61,17 @@ cudaError_t launch_score_tc(const idx_problem& p, float* scores, int64_t ld, con
 cudaError_t launch_score_gather(const idx_problem& p, const int32_t* list, const int32_t* cnt, int64_t gld,
                                 float* scores, int64_t ld, const int32_t* row_mask, cudaStream_t st);
 // Shared candidate stream: group g = rows 4g..4g+3 over one key sequence scores
-// the keys list[g*gld + i], i < cnt[g]; row m keeps (id, score) when id is
-// visible to it, not a seed (seedbits, row stride seed_stride words, 0: shared)
-// and the score reaches tau[m], appending at out_*[m*out_ld + out_cnt[m]++]
-// (positions >= cap are dropped and set status bit 2); rows with status != 0
-// keep nothing.  Shared keys, tensor-core shapes with 4 queries per MMA tile.
+// the keys list[g*gld + i], i < cnt[g], for its four rows: scores[m*ld + i]
+// (m = 4g + q).  Shared keys, tensor-core shapes with 4 queries per MMA tile.
 bool group_stream_supported(const idx_problem& p);
 cudaError_t launch_score_group(const idx_problem& p, const int32_t* list, const int32_t* cnt, int64_t gld,
-                               const uint32_t* seedbits, int64_t seed_stride, const float* tau, int32_t* status,
-                               int32_t* out_ids, float* out_sc, int32_t* out_cnt, int64_t out_ld, int64_t cap,
-                               cudaStream_t st);
-// DoSA bound scan over prepared vectors prep.q = [M, 32, 128] bf16.
+                               float* scores, int64_t ld, cudaStream_t st);
+// DoSA bound scan over prepared vectors prep.q = [M, 32, 128] bf16: bit k of
+// candbits row m (cb_stride words, at least ceil(max_key_len / 128) * 4) is set
+// iff key k is a candidate; words of tiles past a row's group are not written.
 cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const float* coef, const float* tau,
-                         const uint32_t* seedbits, int64_t seed_stride, int32_t* cand, int32_t* cand_cnt,
-                         int64_t cap, int32_t* status, int R, const int32_t* row_mask, cudaStream_t st);
+                         const uint32_t* seedbits, int64_t seed_stride, uint32_t* candbits, int64_t cb_stride,
+                         int R, const int32_t* row_mask, cudaStream_t st);
 
 size_t block_select_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c);
 // tensor_route: allow the tensor-core route (block_tc.cu) when it applies; ws

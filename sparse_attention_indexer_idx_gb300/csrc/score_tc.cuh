@@ -30,10 +30,10 @@
 //           DoSA candidates; output is indexed by list position.
 //  kGroup   the shared candidate stream of the same page (section 4): a group
 //           of four consecutive queries over one key sequence and one list of
-//           keys (list[g][i], ascending, visible to all four); every key of the
-//           list is scored for the four queries in one tile, and a query keeps
-//           (id, score) only when the key is visible to it, is not one of its
-//           seeds and its exact score reaches tau[m].
+//           keys (list[g][i], ascending); every key of the list is scored for
+//           the four queries in one tile, output indexed by list position
+//           (row m = 4g + q: scores[m*ld + i]); which records a row keeps is
+//           decided when the rows are merged.
 //  kFilter  the dense score of every visible key of a row, kept as (id, score)
 //           only when it reaches tau[m] (decode with a prior).
 //  kBound   DoSA's safe upper bound (same page, sections 2, 3.1, 3.2): B holds
@@ -41,8 +41,9 @@
 //           negative aggregate (row 31); the epilogue evaluates
 //             U = sum_j w'_j ReLU(q_j . k) + coef ||k|| - ReLU(a . k)
 //           (times the FP8 scale), with ||k|| read from the key tile in shared
-//           memory, and appends every visible non-seed key with U >= tau to the
-//           row's candidate list (drop only when U < tau).
+//           memory, and sets the bit of every visible non-seed key with U >= tau
+//           in the row's candidate bitmap (drop only when U < tau): one warp
+//           ballot is one 32-key word, stored whole, so the scan needs no atomics.
 //
 // Work units are (query group g, key tile t).  Shared keys (causal prefill): a
 // group is NQ consecutive rows over one key sequence.  Per-row keys (decode,
@@ -88,12 +89,13 @@ struct TcArgs {
   const float* tau;           // [M]
   const uint32_t* seedbits;   // seed bitmap, row stride seed_stride words (0: one shared bitmap)
   int64_t seed_stride;
-  int32_t* cand;              // [M, cand_ld] candidate ids (cand_ld 0: cap)
-  int32_t* cand_cnt;          // [M] (kGroup: starts at the row's first free slot)
+  uint32_t* candbits;         // kBound: [M, cb_stride] candidate bitmap words
+  int64_t cb_stride;
+  int32_t* cand;              // kFilter: [M, cap] kept ids
+  int32_t* cand_cnt;          // [M]
   int64_t cap;
-  int64_t cand_ld;
   int32_t* status;            // [M] bit 1: candidate overflow
-  float* cand_sc;             // kFilter, kGroup: scores of the kept keys (cand: their ids)
+  float* cand_sc;             // kFilter: [M, cap] scores of the kept keys (cand: their ids)
   const int32_t* row_mask;    // optional [M]: rows with row_mask[m] == 0 are skipped
   int R;
 };
@@ -114,7 +116,6 @@ struct TcCfg {
   static constexpr bool GROUP = (MODE == kGroup);
   static constexpr bool BOUND = (MODE == kBound);
   static constexpr bool FILTER = (MODE == kFilter);   // scores >= tau[m] appended as (id, score)
-  static constexpr bool APPEND = FILTER || GROUP;       // the score modes whose output is a kept list
   static constexpr int NCOLX = FP8 ? 2 * NCOL : NCOL;   // MMA columns per query (hi, lo for FP8)
   static constexpr int N = NQ * NCOLX;
   // 128-key subtiles per work unit: FP8 per-row scoring takes 256 keys (32 KB,
@@ -361,17 +362,10 @@ __device__ __forceinline__ void tc_append(const TcArgs& A, int64_t m, bool keep,
   if (keep) {
     const int64_t pos = basepos + __popc(mask & ((1u << lane) - 1u));
     if (pos < A.cap) {
-      const int64_t at = m * (A.cand_ld ? A.cand_ld : A.cap) + pos;
-      A.cand[at] = id;
-      if (A.cand_sc) A.cand_sc[at] = val;
+      A.cand[m * A.cap + pos] = id;
+      A.cand_sc[m * A.cap + pos] = val;
     }
   }
-}
-
-// Seed bit of key id in row m (seed_stride 0: one bitmap for all rows).
-__device__ __forceinline__ bool tc_is_seed(const TcArgs& A, int64_t m, int32_t id) {
-  const uint32_t word = A.seedbits[(A.seed_stride ? m * A.seed_stride : 0) + (id >> 5)];
-  return (word >> (id & 31)) & 1u;
 }
 
 // ------------------------------------------------------------- the kernel ---
@@ -683,7 +677,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     TcUnits<C> u;
     u.init(args, s);
     int64_t cur_g = -1;
-    int32_t gcnt_e = 0;                        // kGroup: the group's list length
     uint32_t nacc = 0, ngrp = 0;
     while (u.valid()) {
       if (u.g != cur_g) {
@@ -721,9 +714,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           int len = 0;
           if (m < args.p.M) {
             if (C::GROUP) {
-              // visible extent; a row already sent to the unpruned path keeps nothing
-              row_extent(args.p, m, &off, &len);
-              if (args.status[m] != 0) len = 0;
+              len = args.cnt[cur_g];               // every row of the group: the group's list
             } else if (C::GATHER) {
               len = args.cnt[m];
               off = tc_key_base(args, m);
@@ -735,9 +726,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           sLen[lane] = len;
           sBase[lane] = off;
           if (C::BOUND) sAux[4 * lane] = m < args.p.M ? args.coef[m] : 0.0f;
-          if (C::BOUND || C::APPEND) sAux[4 * lane + 1] = m < args.p.M ? args.tau[m] : 0.0f;
+          if (C::BOUND || C::FILTER) sAux[4 * lane + 1] = m < args.p.M ? args.tau[m] : 0.0f;
         }
-        if (C::GROUP) gcnt_e = args.cnt[cur_g];
         __syncwarp();
       }
       if (C::NQ == 1 && C::SUB == 1 && (int)(nacc & 1) != tile_par) {
@@ -751,9 +741,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       // wait so that the load overlaps it (words cover max_key_len keys)
       uint32_t sword = 0;
       if (C::BOUND && args.seed_stride == 0 && key < args.p.max_key_len) sword = __ldg(args.seedbits + (key >> 5));
-      // kGroup: the key id at this list position (-1 past the list), read before the wait
-      int32_t kid = -1;
-      if (C::GROUP && key < gcnt_e) kid = __ldg(args.list + cur_g * args.gld + key);
       bool got = mbar_wait(&acc_full[acc], (nacc / C::SACC) & 1, abort_flag);
       // the key-tile slot of this unit (bound: read below for ||k||, so the slot is
       // held until this warp releases it) and its scale slot (FP8)
@@ -845,17 +832,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           }
           float sa, sb;
           f2_unpack(s2, &sa, &sb);
-          if constexpr (C::GROUP) {
-            tc_append(args, ma,
-                      kid >= 0 && kid < sLen[qi] && !(sa < sAux[4 * qi + 1]) && !tc_is_seed(args, ma, kid), kid, sa);
-            if (mb < args.p.M)
-              tc_append(args, mb,
-                        kid >= 0 && kid < sLen[qb] && !(sb < sAux[4 * qb + 1]) && !tc_is_seed(args, mb, kid), kid,
-                        sb);
-          } else {
-            if (key < sLen[qi]) args.scores[ma * args.ld + key] = sa;
-            if (mb < args.p.M && key < sLen[qb]) args.scores[mb * args.ld + key] = sb;
-          }
+          if (key < sLen[qi]) args.scores[ma * args.ld + key] = sa;
+          if (mb < args.p.M && key < sLen[qb]) args.scores[mb * args.ld + key] = sb;
         }
       } else
 #pragma unroll 1
@@ -928,9 +906,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           if constexpr (C::FILTER) {
             // the same value the dense mode writes; kept iff >= tau (warp ballot, one atomic per warp)
             tc_append(args, m, key < len && !(val < sAux[4 * qi + 1]), key, val);
-          } else if constexpr (C::GROUP) {
-            tc_append(args, m, kid >= 0 && kid < len && !(val < sAux[4 * qi + 1]) && !tc_is_seed(args, m, kid), kid,
-                      val);
           } else if (key < len) {
             args.scores[m * args.ld + key] = val;
           }
@@ -958,7 +933,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
             const bool seed = (word >> (key & 31)) & 1u;
             is_cand = !seed && !(ub < sAux[4 * qi + 1]);
           }
-          tc_append(args, m, is_cand, key, 0.0f);
+          // the warp's 32 keys are one bitmap word (key - lane is a multiple of 32)
+          const unsigned mask = __ballot_sync(0xffffffffu, is_cand);
+          const int64_t wd = key >> 5;
+          if (lane == 0 && wd < args.cb_stride) args.candbits[m * args.cb_stride + wd] = mask;
         }
       }
       tc_fence_before();

@@ -6,8 +6,8 @@
 namespace idx {
 
 cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const float* coef, const float* tau,
-                         const uint32_t* seedbits, int64_t seed_stride, int32_t* cand, int32_t* cand_cnt,
-                         int64_t cap, int32_t* status, int R, const int32_t* row_mask, cudaStream_t st) {
+                         const uint32_t* seedbits, int64_t seed_stride, uint32_t* candbits, int64_t cb_stride,
+                         int R, const int32_t* row_mask, cudaStream_t st) {
   TcArgs a{};
   a.p = prep;
   a.wfold = wfold;
@@ -15,10 +15,8 @@ cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const floa
   a.tau = tau;
   a.seedbits = seedbits;
   a.seed_stride = seed_stride;
-  a.cand = cand;
-  a.cand_cnt = cand_cnt;
-  a.cap = cap;
-  a.status = status;
+  a.candbits = candbits;
+  a.cb_stride = cb_stride;
   a.R = R;
   a.row_mask = row_mask;
   const bool shared = prep.key_off == nullptr;

@@ -2,7 +2,7 @@
 // (score_tc.cuh, kGroup): four consecutive queries over one key sequence score
 // one list of keys together (N = 4 x H for bf16 keys, 4 x 2H for FP8), with
 // the same MMA shape and epilogue chain per (query, key) pair as every other
-// instantiation, and keep (id, score) per query when the score reaches tau.
+// instantiation; scores are written by list position.
 #include "score_tc.cuh"
 
 namespace idx {
@@ -14,23 +14,14 @@ bool group_stream_supported(const idx_problem& p) {
 }
 
 cudaError_t launch_score_group(const idx_problem& p, const int32_t* list, const int32_t* cnt, int64_t gld,
-                               const uint32_t* seedbits, int64_t seed_stride, const float* tau, int32_t* status,
-                               int32_t* out_ids, float* out_sc, int32_t* out_cnt, int64_t out_ld, int64_t cap,
-                               cudaStream_t st) {
+                               float* scores, int64_t ld, cudaStream_t st) {
   TcArgs a{};
   a.p = p;
   a.list = list;
   a.cnt = cnt;
   a.gld = gld;
-  a.seedbits = seedbits;
-  a.seed_stride = seed_stride;
-  a.tau = tau;
-  a.status = status;
-  a.cand = out_ids;
-  a.cand_sc = out_sc;
-  a.cand_cnt = out_cnt;
-  a.cand_ld = out_ld;
-  a.cap = cap;
+  a.scores = scores;
+  a.ld = ld;
   if (!group_stream_supported(p)) return cudaErrorInvalidValue;
   if (p.k_dtype == IDX_FP8_E4M3) {
     return p.H == 16 ? launch_tc<TcCfg<IDX_FP8_E4M3, 16, 4, kGroup>>(a, st)
