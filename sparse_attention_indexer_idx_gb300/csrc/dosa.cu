@@ -714,6 +714,40 @@ __global__ void __launch_bounds__(kMergeThreads) merge_rows_kernel(
   if ((threadIdx.x & 31) == 0 && surv) atomicAdd(survivors, surv);
 }
 
+// ||k|| of every key of one shared key sequence (e4m3 codes for FP8 keys),
+// squares summed by fmaf in d order, square root rounded up: the bound's
+// c ||k|| term, computed once instead of in every epilogue warp.
+__global__ void key_norm_kernel(idx_problem p, float* knorm) {
+  const int D = p.D;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < p.n_keys;
+       k += (int64_t)gridDim.x * blockDim.x) {
+    float ss = 0.0f;
+    if (p.k_dtype == IDX_FP8_E4M3) {
+      const uint8_t* row = (const uint8_t*)p.keys + k * D;
+      for (int d = 0; d < D; d += 16) {
+        const uint4 c = *reinterpret_cast<const uint4*>(row + d);
+        const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+        for (int e = 0; e < 16; ++e) {
+          const float x = e4m3_to_f((uint8_t)(w4[e >> 2] >> (8 * (e & 3))));
+          ss = __fmaf_rn(x, x, ss);
+        }
+      }
+    } else {
+      const uint16_t* row = (const uint16_t*)p.keys + k * D;
+      for (int d = 0; d < D; d += 8) {
+        const uint4 c = *reinterpret_cast<const uint4*>(row + d);
+        const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+        for (int e = 0; e < 4; ++e) {
+          const float lo = bf16_to_f((uint16_t)(w4[e] & 0xffffu)), hi = bf16_to_f((uint16_t)(w4[e] >> 16));
+          ss = __fmaf_rn(lo, lo, ss);
+          ss = __fmaf_rn(hi, hi, ss);
+        }
+      }
+    }
+    knorm[k] = __fsqrt_ru(ss);
+  }
+}
+
 // ---------------------------------------------------------- shared stream --
 
 constexpr int kGrpThreads = 1024;
@@ -942,6 +976,7 @@ struct DosaWs {
   unsigned long long* surv;
   float* fb_scores;
   uint32_t* candbits;      // [M, cbW] candidate bitmaps of the bound scan
+  float* knorm;            // shared keys: [n_keys] ||k||
   int32_t* glist;          // shared stream: [G, 2 cap] group lists
   int32_t* gcnt;           // [G]
   float* gsc;              // [M, 2 cap] scores of the group lists, by position
@@ -1019,6 +1054,7 @@ static DosaWs carve(void* base, const idx_problem& p, int K, const dosa_params& 
   w.surv = c.take<unsigned long long>(1);
   w.fb_scores = c.take<float>((size_t)M * s.ldmax);
   w.candbits = c.take<uint32_t>((size_t)M * s.cbW);
+  w.knorm = c.take<float>(s.shared_keys ? (size_t)p.n_keys : 1);
   w.glist = c.take<int32_t>(s.group ? (size_t)s.G * 2 * s.cap : 1);
   w.gcnt = c.take<int32_t>(s.group ? (size_t)s.G : 1);
   w.gsc = c.take<float>(s.group ? (size_t)M * 2 * s.cap : 1);
@@ -1157,8 +1193,12 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
   idx_problem prep = p;
   prep.q = w.qprep;
   prep.H = kVec;
-  DOSA_CHECK(launch_bound(prep, w.wfold, w.coef, w.tau, w.bits, s.shared_seeds ? 0 : s.W, w.candbits, s.cbW,
-                          dp.retained_heads, w.active, st));
+  if (s.shared_keys) {
+    key_norm_kernel<<<grid_for(p.n_keys, 256), 256, 0, st>>>(p, w.knorm);
+    DOSA_CHECK(cudaGetLastError());
+  }
+  DOSA_CHECK(launch_bound(prep, w.wfold, w.coef, w.tau, s.shared_keys ? w.knorm : nullptr, w.bits,
+                          s.shared_seeds ? 0 : s.W, w.candbits, s.cbW, dp.retained_heads, w.active, st));
 
   // ---- exact rescoring of the candidates, merge with the seed top-K
   GroupRecs gr{};

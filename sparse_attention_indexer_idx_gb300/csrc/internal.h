@@ -69,9 +69,12 @@ cudaError_t launch_score_group(const idx_problem& p, const int32_t* list, const 
 // DoSA bound scan over prepared vectors prep.q = [M, 32, 128] bf16: bit k of
 // candbits row m (cb_stride words, at least ceil(max_key_len / 128) * 4) is set
 // iff key k is a candidate; words of tiles past a row's group are not written.
+// Shared keys (key_off == NULL) need knorm [n_keys] = ||k|| rounded up (codes
+// for FP8); per-row keys take ||k|| from the key tile (knorm unused).
+// Prepared rows R..30 and their folded weights must be zero.
 cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const float* coef, const float* tau,
-                         const uint32_t* seedbits, int64_t seed_stride, uint32_t* candbits, int64_t cb_stride,
-                         int R, const int32_t* row_mask, cudaStream_t st);
+                         const float* knorm, const uint32_t* seedbits, int64_t seed_stride, uint32_t* candbits,
+                         int64_t cb_stride, int R, const int32_t* row_mask, cudaStream_t st);
 
 size_t block_select_ws(int64_t Q, int n_kv, int64_t L, const block_sparse_config& c);
 // tensor_route: allow the tensor-core route (block_tc.cu) when it applies; ws

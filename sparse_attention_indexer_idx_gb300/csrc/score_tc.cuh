@@ -25,9 +25,13 @@
 //           wherever it is computed -- same instruction shape, same K order,
 //           same chain.
 //  kGather  the same score over per-row key lists: tile t of row m holds the
-//           keys list[m][t*128 + i], fetched by TMA tile::gather4 (four rows
-//           per instruction) straight into the swizzled tile.  Used to rescore
-//           DoSA candidates; output is indexed by list position.
+//           keys list[m][t*128 + i], copied by the producer warp's lanes (16-byte
+//           cp.async, four rows per lane) straight into the swizzled tile; each
+//           lane waits for its own copies a few tiles later, fences them for the
+//           async proxy and arrives on the tile's barrier.  (TMA tile::gather4
+//           moves 512 bytes per instruction and its issue rate, not bandwidth,
+//           set the pace.)  Used to rescore DoSA candidates; output is indexed
+//           by list position.
 //  kGroup   the shared candidate stream of the same page (section 4): a group
 //           of four consecutive queries over one key sequence and one list of
 //           keys (list[g][i], ascending); every key of the list is scored for
@@ -41,7 +45,8 @@
 //           negative aggregate (row 31); the epilogue evaluates
 //             U = sum_j w'_j ReLU(q_j . k) + coef ||k|| - ReLU(a . k)
 //           (times the FP8 scale), with ||k|| read from the key tile in shared
-//           memory, and sets the bit of every visible non-seed key with U >= tau
+//           memory (one query per tile) or from a per-key array (shared keys,
+//           where every epilogue warp would otherwise redo it), and sets the bit of every visible non-seed key with U >= tau
 //           in the row's candidate bitmap (drop only when U < tau): one warp
 //           ballot is one 32-key word, stored whole, so the scan needs no atomics.
 //
@@ -87,6 +92,7 @@ struct TcArgs {
   const float* wfold;         // [M, 32] folded retained weights (j < R)
   const float* coef;          // [M] c + margin, multiplies ||k||
   const float* tau;           // [M]
+  const float* knorm;         // kBound over shared keys: [n_keys] ||k|| (codes for FP8), rounded up
   const uint32_t* seedbits;   // seed bitmap, row stride seed_stride words (0: one shared bitmap)
   int64_t seed_stride;
   uint32_t* candbits;         // kBound: [M, cb_stride] candidate bitmap words
@@ -115,6 +121,10 @@ struct TcCfg {
   static constexpr bool GATHER = (MODE == kGather || MODE == kGroup);   // keys fetched by list entries
   static constexpr bool GROUP = (MODE == kGroup);
   static constexpr bool BOUND = (MODE == kBound);
+  // kBound: ||k|| from the key tile (one query per tile: one epilogue warp reads a
+  // unit) or from the per-key array (several queries per tile)
+  static constexpr bool KN_TILE = BOUND && NQ_ == 1;
+  static constexpr bool KN_GLOBAL = BOUND && NQ_ > 1;
   static constexpr bool FILTER = (MODE == kFilter);   // scores >= tau[m] appended as (id, score)
   static constexpr int NCOLX = FP8 ? 2 * NCOL : NCOL;   // MMA columns per query (hi, lo for FP8)
   static constexpr int N = NQ * NCOLX;
@@ -138,6 +148,9 @@ struct TcCfg {
   static constexpr int SA = FP8 ? (SA_FIT > 12 ? 12 : SA_FIT) : ((BQ_BYTES * SB <= 32768) ? 5 : 4);
   static constexpr int SSC = FP8 ? SA + SACC + 2 : 0;
   static constexpr int SSC_MOD = SSC > 0 ? SSC : 1;
+  // gathered tiles: key copies a producer lane keeps in flight before it waits
+  // (at most SA - 1, so the slot it waits to reuse never depends on its own arrival)
+  static constexpr int GD = SA - 1;
   static constexpr int IL = (SUB == 1 && N <= 128) ? 2 : 1;   // units whose MMA chains are interleaved
   static constexpr int TMEM_COLS = tc_pow2_cols(SACC * SUB * N);
   static constexpr int NE = 8;   // epilogue warps, two per TMEM lane quarter
@@ -406,9 +419,9 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::SA; ++i) {
-      mbar_init(&a_full[i], 1);
+      mbar_init(&a_full[i], C::GATHER ? 32 : 1);   // gathered: every producer lane arrives
       // the bound epilogue reads ||k|| from the key tile, so its warps also release the slot
-      mbar_init(&a_empty[i], C::BOUND ? 1 + C::EPT : 1);
+      mbar_init(&a_empty[i], C::KN_TILE ? 1 + C::EPT : 1);
     }
     for (int i = 0; i < C::SB; ++i) {
       // FP8: every lane of the split warps arrives once its rows are written
@@ -458,6 +471,20 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     int32_t pf[4] = {0, 0, 0, 0};
     int64_t pf_g = -1, pf_t = -1;
     uint32_t na = 0, nb = 0;
+    uint32_t arrived = 0;                      // gathered: units whose copies this lane has arrived for
+    // Gathered tiles: a lane arrives for a unit only a few units after issuing its
+    // copies, so before the warp blocks on a barrier that the MMA or the epilogue
+    // frees, every unit still in flight is finished and counted (those may be the
+    // very units the MMA needs first).  probe: one non-blocking test by lane 0.
+    auto flush_if_blocked = [&](uint64_t* bar, uint32_t parity) {
+      if (!C::GATHER) return;
+      bool rdy = false;
+      if (lane == 0) rdy = mbar_try_wait(bar, parity);
+      if (__shfl_sync(0xffffffffu, rdy, 0) || arrived == na) return;
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      fence_proxy_async_smem();
+      for (; arrived < na; ++arrived) mbar_arrive(&a_full[arrived % C::SA]);
+    };
     while (u.valid()) {
       if (u.g != cur_g) {
         cur_g = u.g;
@@ -467,6 +494,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           // bf16: the group's query rows (FP8: the split warps read them from global memory)
           const int bs = nb % C::SB;
           bool ok = true;
+          flush_if_blocked(&b_empty[bs], ((nb / C::SB) & 1) ^ 1);
           if (lane == 0) {
             ok = mbar_wait(&b_empty[bs], ((nb / C::SB) & 1) ^ 1, abort_flag);
             if (ok) {
@@ -483,6 +511,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       }
       const int as = na % C::SA;
       bool ok = true;
+      flush_if_blocked(&a_empty[as], ((na / C::SA) & 1) ^ 1);
       if (lane == 0) ok = mbar_wait(&a_empty[as], ((na / C::SA) & 1) ^ 1, abort_flag);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       uint8_t* dst = sA + as * C::A_BYTES;
@@ -503,6 +532,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         // the buffer; a scale past the row's end is never used)
         const int ss = na % C::SSC_MOD;
         bool sok = true;
+        flush_if_blocked(&sc_empty[ss], ((na / C::SSC_MOD) & 1) ^ 1);
         if (lane == 0) sok = mbar_wait(&sc_empty[ss], ((na / C::SSC_MOD) & 1) ^ 1, abort_flag);
         if (!__shfl_sync(0xffffffffu, sok, 0)) break;
         float* sdst = sScale + ss * C::UKEYS + 4 * lane;
@@ -517,18 +547,23 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         cp_async_arrive_noinc(&sc_full[ss]);
       }
       if (C::GATHER) {
-        // lane l fetches tile rows 4l..4l+3 (list positions t*128 + 4l + i)
-        int32_t y[4];
+        // lane l copies tile rows 4l..4l+3 (list positions t*128 + 4l + i), 16 bytes
+        // at a time, into the 128-byte-swizzled halves; rows past the list are left
+        // as they are (their accumulator rows are never read)
+        constexpr int RB = C::FP8 ? 128 : 256;   // bytes of one key row
+        const char* kb = static_cast<const char*>(args.p.keys);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
+          const int r = 4 * lane + i;
+          if ((int)(u.t * 128) + r >= gcnt) continue;
           int64_t row = gbase + (int64_t)graw[i];
           row = row < 0 ? 0 : (row >= args.p.n_keys ? args.p.n_keys - 1 : row);
-          y[i] = (int32_t)row;
+          const char* src = kb + row * RB;
+#pragma unroll
+          for (int cc = 0; cc < RB / 16; ++cc)
+            cp_async_16(dst + (cc >> 3) * (C::A_BYTES / 2) + r * 128 + (((cc & 7) ^ (r & 7)) << 4), src + cc * 16);
         }
-        if (lane == 0) mbar_arrive_expect_tx(fbar, C::A_BYTES);
-        __syncwarp();
-        tma_gather4(dst + lane * 512, &tmap_k, fbar, 0, y[0], y[1], y[2], y[3]);
-        if (!C::FP8) tma_gather4(dst + C::A_BYTES / 2 + lane * 512, &tmap_k, fbar, 64, y[0], y[1], y[2], y[3]);
+        cp_async_commit();
         // the next unit's entries
         TcUnits<C> nx = u;
         nx.advance();
@@ -546,12 +581,24 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         tma_load_2d(dst, &tmap_k, fbar, 0, y);
         if (!C::FP8) tma_load_2d(dst + C::A_BYTES / 2, &tmap_k, fbar, 64, y);
       }
+      if (C::GATHER && na + 1 - arrived > (uint32_t)C::GD) {
+        // the oldest unit in flight: this lane's copies are done; make them visible
+        // to the tensor cores and count this lane in
+        cp_async_wait_group<C::GD>();
+        fence_proxy_async_smem();
+        mbar_arrive(&a_full[arrived % C::SA]);
+        ++arrived;
+      }
       __syncwarp();
       ++na;
       u.advance();
     }
     // drain: the last phase issued on every ring slot has landed
-    if (C::FP8) asm volatile("cp.async.wait_all;" ::: "memory");
+    if (C::FP8 || C::GATHER) asm volatile("cp.async.wait_all;" ::: "memory");
+    if (C::GATHER) {
+      fence_proxy_async_smem();
+      for (; arrived < na; ++arrived) mbar_arrive(&a_full[arrived % C::SA]);
+    }
     if (lane == 0) {
       for (uint32_t i = 0; i < (uint32_t)C::SB && i < nb; ++i) {
         uint32_t j = nb - 1 - i;
@@ -741,20 +788,21 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       // wait so that the load overlaps it (words cover max_key_len keys)
       uint32_t sword = 0;
       if (C::BOUND && args.seed_stride == 0 && key < args.p.max_key_len) sword = __ldg(args.seedbits + (key >> 5));
+      float knorm = 0.0f;
+      if (C::KN_GLOBAL && key < args.p.max_key_len) knorm = __ldg(args.knorm + key);
       bool got = mbar_wait(&acc_full[acc], (nacc / C::SACC) & 1, abort_flag);
       // the key-tile slot of this unit (bound: read below for ||k||, so the slot is
       // held until this warp releases it) and its scale slot (FP8)
       const int slot = nacc % C::SA;
       const int sslot = nacc % C::SSC_MOD;
-      if (C::BOUND && got) got = mbar_wait(&a_full[slot], (nacc / C::SA) & 1, abort_flag);
+      if (C::KN_TILE && got) got = mbar_wait(&a_full[slot], (nacc / C::SA) & 1, abort_flag);
       if (C::FP8 && got) got = mbar_wait(&sc_full[sslot], (nacc / C::SSC_MOD) & 1, abort_flag);
       __syncwarp();                           // tcgen05.ld below is warp-collective
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       // FP8: all queries of a group read the same key sequence, so one scale serves them all
       const float kscale = C::FP8 ? sScale[sslot * C::UKEYS + sub * 128 + row_in_tile] : 1.0f;
-      float knorm = 0.0f;
-      if (C::BOUND) {
+      if (C::KN_TILE) {
         // ||k|| of this lane's key (codes for FP8) from the MMA-ready tile
         const uint8_t* at = sA + slot * C::A_BYTES;
         float ss = 0.0f;
@@ -787,10 +835,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         }
         knorm = __fsqrt_ru(ss);
       }
-      if (C::BOUND || C::FP8) {
+      if (C::KN_TILE || C::FP8) {
         __syncwarp();
         if (lane == 0) {
-          if (C::BOUND) mbar_arrive(&a_empty[slot]);
+          if (C::KN_TILE) mbar_arrive(&a_empty[slot]);
           if (C::FP8) mbar_arrive(&sc_empty[sslot]);
         }
       }
@@ -918,11 +966,19 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(vl[j]));
           }
-          const int R = args.R;
+          // rows R..30 of the prepared vectors and their folded weights are zero, so
+          // the chain over all 31 adds nothing past R: no per-row predicate
           float ub = 0.0f;
+          const float4* w4 = reinterpret_cast<const float4*>(wq);
 #pragma unroll
-          for (int j = 0; j < 31; ++j)
-            if (j < R) ub = __fmaf_rn(wq[j], fmaxf(__uint_as_float(v[j]), 0.0f), ub);
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 ww = w4[j4];
+            const int j = 4 * j4;
+            ub = __fmaf_rn(ww.x, fmaxf(__uint_as_float(v[j]), 0.0f), ub);
+            ub = __fmaf_rn(ww.y, fmaxf(__uint_as_float(v[j + 1]), 0.0f), ub);
+            ub = __fmaf_rn(ww.z, fmaxf(__uint_as_float(v[j + 2]), 0.0f), ub);
+            if (j4 < 7) ub = __fmaf_rn(ww.w, fmaxf(__uint_as_float(v[j + 3]), 0.0f), ub);
+          }
           ub = ub - fmaxf(__uint_as_float(v[31]), 0.0f);
           if (C::FP8) ub = ub * sAux[4 * qi + 2];
           ub = __fmaf_rn(sAux[4 * qi], knorm, ub);

@@ -6,13 +6,14 @@
 namespace idx {
 
 cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const float* coef, const float* tau,
-                         const uint32_t* seedbits, int64_t seed_stride, uint32_t* candbits, int64_t cb_stride,
-                         int R, const int32_t* row_mask, cudaStream_t st) {
+                         const float* knorm, const uint32_t* seedbits, int64_t seed_stride, uint32_t* candbits,
+                         int64_t cb_stride, int R, const int32_t* row_mask, cudaStream_t st) {
   TcArgs a{};
   a.p = prep;
   a.wfold = wfold;
   a.coef = coef;
   a.tau = tau;
+  a.knorm = knorm;
   a.seedbits = seedbits;
   a.seed_stride = seed_stride;
   a.candbits = candbits;
@@ -20,6 +21,7 @@ cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const floa
   a.R = R;
   a.row_mask = row_mask;
   const bool shared = prep.key_off == nullptr;
+  if (shared && !knorm) return cudaErrorInvalidValue;
   if (prep.k_dtype == IDX_FP8_E4M3)
     return shared ? launch_tc<TcCfg<IDX_FP8_E4M3, 32, 4, kBound>>(a, st)
                   : launch_tc<TcCfg<IDX_FP8_E4M3, 32, 1, kBound>>(a, st);
