@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
       u.init(W, s);
       int64_t cur_T = -1;
       uint32_t na = 0, nunit = 0;
-      bool issued = false, ok = true;
+      bool ok = true;
       while (u.valid() && ok) {
         if (u.T != cur_T) {
           cur_T = u.T;
@@ -618,7 +618,6 @@ __global__ void __launch_bounds__(kBtThreads, 1)
               tc_mma_f16(d0, smem_desc_sw128(a0 + kk * 32), bd, idesc, accum);
               tc_mma_f16(d0 + 128, smem_desc_sw128(a0 + kBtATile + kk * 32), bd, idesc, accum);
             }
-            issued = true;
             tc_commit(&k_empty[st]);
           }
           if (!ok) break;
@@ -629,9 +628,19 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         u.advance();
         if (!u.valid() || u.T != T_this) tc_commit(a_empty);
       }
-      if (issued) {
-        tc_commit(&drain_bar[me]);
-        mbar_wait(&drain_bar[me], 0, no_abort);
+      // No commit may still be in flight when the CTA exits (its arrive would land
+      // in the next kernel's shared memory): each thread waits for its drain
+      // commit, also one that issued nothing but committed the query-tile barrier,
+      // and warp 1 waits for the last phases of the barriers the commits target.
+      tc_commit(&drain_bar[me]);
+      mbar_wait(&drain_bar[me], 0, no_abort);
+      if (me == 0 && ok && !*abort_flag) {
+        if (na > 0) mbar_wait(a_empty, (na - 1) & 1, no_abort);
+        const uint32_t nk = 2 * nunit;
+        for (uint32_t i = 0; i < (uint32_t)kBtKStages && i < nk; ++i) {
+          const uint32_t j = nk - 1 - i;
+          mbar_wait(&k_empty[j % kBtKStages], (j / kBtKStages) & 1, no_abort);
+        }
       }
     }
   } else if (warp >= 2 && warp < 2 + kBtNE) {

@@ -619,7 +619,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       int64_t cur_g = -1;
       int cur_bs = 0;
       uint32_t na = 0, nb = 0, nacc = 0, round = 0;
-      bool issued = false;
       while (u.valid()) {
         if (u.g != cur_g) {
           cur_g = u.g;
@@ -690,7 +689,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
             if (n > 1) tc_mma_f16(d[1], smem_desc_sw128(a0[1] + ao), bd, idesc, k > 0 ? 1u : 0u);
           }
         }
-        issued = true;
         if (C::SUB > 1) n = 1;                 // one unit
         for (int i = 0; i < n; ++i) {
           tc_commit(&a_empty[(na + i) % C::SA]);
@@ -703,9 +701,23 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         u.advance();
         if (!u.valid() || u.g != g_this) tc_commit(&b_empty[cur_bs]);
       }
-      if (issued) {
-        tc_commit(&drain_bar[me]);
-        mbar_wait(&drain_bar[me], 0, no_abort);
+      // No commit of this thread may still be in flight when the CTA exits: its
+      // arrive would land on whatever the next kernel on this SM keeps at that
+      // shared-memory address.  So each thread commits the drain barrier and waits
+      // for it (also a thread that issued nothing but committed the query-buffer
+      // barrier at a group end), and warp 1 waits for the last phases of the slot
+      // and query-buffer barriers, which both threads commit to.
+      tc_commit(&drain_bar[me]);
+      mbar_wait(&drain_bar[me], 0, no_abort);
+      if (me == 0 && !*abort_flag) {
+        for (uint32_t i = 0; i < (uint32_t)C::SA && i < na; ++i) {
+          const uint32_t j = na - 1 - i;
+          mbar_wait(&a_empty[j % C::SA], (j / C::SA) & 1, no_abort);
+        }
+        for (uint32_t i = 0; i < (uint32_t)C::SB && i < nb; ++i) {
+          const uint32_t j = nb - 1 - i;
+          mbar_wait(&b_empty[j % C::SB], (j / C::SB) & 1, no_abort);
+        }
       }
     }
   } else if (warp >= 2 && warp < 2 + C::NE) {
@@ -842,7 +854,55 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           if (C::FP8) mbar_arrive(&sc_empty[sslot]);
         }
       }
-      if constexpr (C::PAIR) {
+      // kBound: U of this lane's key for query qi (row m) from its 32 accumulator
+      // columns, and the warp's 32 candidate bits as one bitmap word
+      auto bound_word = [&](int qi, int64_t m, const uint32_t (&v)[32]) {
+        const float* wq = sW + qi * C::NCOL;
+        // rows R..30 of the prepared vectors and their folded weights are zero, so
+        // the chain over all 31 adds nothing past R: no per-row predicate
+        float ub = 0.0f;
+        const float4* w4 = reinterpret_cast<const float4*>(wq);
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 ww = w4[j4];
+          const int j = 4 * j4;
+          ub = __fmaf_rn(ww.x, fmaxf(__uint_as_float(v[j]), 0.0f), ub);
+          ub = __fmaf_rn(ww.y, fmaxf(__uint_as_float(v[j + 1]), 0.0f), ub);
+          ub = __fmaf_rn(ww.z, fmaxf(__uint_as_float(v[j + 2]), 0.0f), ub);
+          if (j4 < 7) ub = __fmaf_rn(ww.w, fmaxf(__uint_as_float(v[j + 3]), 0.0f), ub);
+        }
+        ub = ub - fmaxf(__uint_as_float(v[31]), 0.0f);
+        if (C::FP8) ub = ub * sAux[4 * qi + 2];
+        ub = __fmaf_rn(sAux[4 * qi], knorm, ub);
+        bool is_cand = false;
+        if (key < sLen[qi]) {
+          if (C::FP8) ub = ub * kscale;
+          const uint32_t word = args.seed_stride ? args.seedbits[m * args.seed_stride + (key >> 5)] : sword;
+          const bool seed = (word >> (key & 31)) & 1u;
+          is_cand = !seed && !(ub < sAux[4 * qi + 1]);
+        }
+        // the warp's 32 keys are one bitmap word (key - lane is a multiple of 32)
+        const unsigned mask = __ballot_sync(0xffffffffu, is_cand);
+        const int64_t wd = key >> 5;
+        if (lane == 0 && wd < args.cb_stride) args.candbits[m * args.cb_stride + wd] = mask;
+      };
+      if constexpr (C::BOUND && !C::FP8 && C::NQ >= 2 * QSTEP) {
+        // several queries per tile: two queries' columns per TMEM wait
+#pragma unroll 1
+        for (int qi = qfirst; qi < C::NQ; qi += 2 * QSTEP) {
+          const int64_t ma = cur_g * C::NQ + qi;
+          if (ma >= args.p.M) break;
+          const int qb = qi + QSTEP;
+          const int64_t mb = cur_g * C::NQ + qb;
+          const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::SUB * C::N);
+          uint32_t va[32], vb[32];
+          tmem_ld_32x32b_x32(tbase + (uint32_t)(qi * C::NCOLX), va);
+          tmem_ld_32x32b_x32(tbase + (uint32_t)(qb * C::NCOLX), vb);
+          tmem_ld_wait();
+          bound_word(qi, ma, va);
+          if (mb < args.p.M) bound_word(qb, mb, vb);
+        }
+      } else if constexpr (C::PAIR) {
         // queries qi and qi + QSTEP, chains packed (a in the low half, b in the high half)
 #pragma unroll 1
         for (int qi = qfirst, r = 0; qi < C::NQ; qi += 2 * QSTEP, r += 2) {
@@ -966,33 +1026,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(vl[j]));
           }
-          // rows R..30 of the prepared vectors and their folded weights are zero, so
-          // the chain over all 31 adds nothing past R: no per-row predicate
-          float ub = 0.0f;
-          const float4* w4 = reinterpret_cast<const float4*>(wq);
-#pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 ww = w4[j4];
-            const int j = 4 * j4;
-            ub = __fmaf_rn(ww.x, fmaxf(__uint_as_float(v[j]), 0.0f), ub);
-            ub = __fmaf_rn(ww.y, fmaxf(__uint_as_float(v[j + 1]), 0.0f), ub);
-            ub = __fmaf_rn(ww.z, fmaxf(__uint_as_float(v[j + 2]), 0.0f), ub);
-            if (j4 < 7) ub = __fmaf_rn(ww.w, fmaxf(__uint_as_float(v[j + 3]), 0.0f), ub);
-          }
-          ub = ub - fmaxf(__uint_as_float(v[31]), 0.0f);
-          if (C::FP8) ub = ub * sAux[4 * qi + 2];
-          ub = __fmaf_rn(sAux[4 * qi], knorm, ub);
-          bool is_cand = false;
-          if (key < len) {
-            if (C::FP8) ub = ub * kscale;
-            const uint32_t word = args.seed_stride ? args.seedbits[m * args.seed_stride + (key >> 5)] : sword;
-            const bool seed = (word >> (key & 31)) & 1u;
-            is_cand = !seed && !(ub < sAux[4 * qi + 1]);
-          }
-          // the warp's 32 keys are one bitmap word (key - lane is a multiple of 32)
-          const unsigned mask = __ballot_sync(0xffffffffu, is_cand);
-          const int64_t wd = key >> 5;
-          if (lane == 0 && wd < args.cb_stride) args.candbits[m * args.cb_stride + wd] = mask;
+          bound_word(qi, m, v);
         }
       }
       tc_fence_before();
