@@ -856,22 +856,11 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       }
       // kBound: U of this lane's key for query qi (row m) from its 32 accumulator
       // columns, and the warp's 32 candidate bits as one bitmap word
-      auto bound_word = [&](int qi, int64_t m, const uint32_t (&v)[32]) {
-        const float* wq = sW + qi * C::NCOL;
-        // rows R..30 of the prepared vectors and their folded weights are zero, so
-        // the chain over all 31 adds nothing past R: no per-row predicate
-        float ub = 0.0f;
-        const float4* w4 = reinterpret_cast<const float4*>(wq);
-#pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 ww = w4[j4];
-          const int j = 4 * j4;
-          ub = __fmaf_rn(ww.x, fmaxf(__uint_as_float(v[j]), 0.0f), ub);
-          ub = __fmaf_rn(ww.y, fmaxf(__uint_as_float(v[j + 1]), 0.0f), ub);
-          ub = __fmaf_rn(ww.z, fmaxf(__uint_as_float(v[j + 2]), 0.0f), ub);
-          if (j4 < 7) ub = __fmaf_rn(ww.w, fmaxf(__uint_as_float(v[j + 3]), 0.0f), ub);
-        }
-        ub = ub - fmaxf(__uint_as_float(v[31]), 0.0f);
+      // (the retained-head chain sum_j w'_j ReLU(acc_j) is computed by the callers:
+      // rows R..30 of the prepared vectors and their folded weights are zero, so a
+      // chain that stops anywhere at or past R has the same value)
+      auto bound_finish = [&](int qi, int64_t m, float chain, uint32_t agg) {
+        float ub = chain - fmaxf(__uint_as_float(agg), 0.0f);
         if (C::FP8) ub = ub * sAux[4 * qi + 2];
         ub = __fmaf_rn(sAux[4 * qi], knorm, ub);
         bool is_cand = false;
@@ -886,21 +875,77 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         const int64_t wd = key >> 5;
         if (lane == 0 && wd < args.cb_stride) args.candbits[m * args.cb_stride + wd] = mask;
       };
-      if constexpr (C::BOUND && !C::FP8 && C::NQ >= 2 * QSTEP) {
-        // several queries per tile: two queries' columns per TMEM wait
-#pragma unroll 1
-        for (int qi = qfirst; qi < C::NQ; qi += 2 * QSTEP) {
-          const int64_t ma = cur_g * C::NQ + qi;
-          if (ma >= args.p.M) break;
-          const int qb = qi + QSTEP;
-          const int64_t mb = cur_g * C::NQ + qb;
-          const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::SUB * C::N);
-          uint32_t va[32], vb[32];
-          tmem_ld_32x32b_x32(tbase + (uint32_t)(qi * C::NCOLX), va);
-          tmem_ld_32x32b_x32(tbase + (uint32_t)(qb * C::NCOLX), vb);
+      auto bound_word = [&](int qi, int64_t m, const uint32_t (&v)[32]) {
+        float ub = 0.0f;
+        const float4* w4 = reinterpret_cast<const float4*>(sW + qi * C::NCOL);
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 ww = w4[j4];
+          const int j = 4 * j4;
+          ub = __fmaf_rn(ww.x, fmaxf(__uint_as_float(v[j]), 0.0f), ub);
+          ub = __fmaf_rn(ww.y, fmaxf(__uint_as_float(v[j + 1]), 0.0f), ub);
+          ub = __fmaf_rn(ww.z, fmaxf(__uint_as_float(v[j + 2]), 0.0f), ub);
+          if (j4 < 7) ub = __fmaf_rn(ww.w, fmaxf(__uint_as_float(v[j + 3]), 0.0f), ub);
+        }
+        bound_finish(qi, m, ub, v[31]);
+      };
+      if constexpr (C::BOUND && !C::FP8 && C::NQ == 4 * QSTEP) {
+        const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::SUB * C::N);
+        if (args.R <= 16) {
+          // at most 16 retained heads: columns 0..15 and the aggregate (31) of this
+          // warp's four queries, one TMEM wait; two packed chains (queries 0|1 and
+          // 2|3 of the warp in the halves of fma.rn.f32x2, each rounding as fmaf)
+          uint32_t v[4][32], agg[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t col = tbase + (uint32_t)((qfirst + b * QSTEP) * C::NCOLX);
+            tmem_ld_32x32b_x16(col, v[b]);
+            agg[b] = tmem_ld_32x32b_x1(col + 31);
+          }
           tmem_ld_wait();
-          bound_word(qi, ma, va);
-          if (mb < args.p.M) bound_word(qb, mb, vb);
+          const float4* w0 = reinterpret_cast<const float4*>(sW + (qfirst + 0 * QSTEP) * C::NCOL);
+          const float4* w1 = reinterpret_cast<const float4*>(sW + (qfirst + 1 * QSTEP) * C::NCOL);
+          const float4* w2 = reinterpret_cast<const float4*>(sW + (qfirst + 2 * QSTEP) * C::NCOL);
+          const float4* w3 = reinterpret_cast<const float4*>(sW + (qfirst + 3 * QSTEP) * C::NCOL);
+          uint64_t s01 = f2_pack(0.0f, 0.0f), s23 = f2_pack(0.0f, 0.0f);
+#pragma unroll
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const float4 a = w0[j4], b = w1[j4], c = w2[j4], d = w3[j4];
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+            const float cv[4] = {c.x, c.y, c.z, c.w}, dv[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 4 * j4 + e;
+              s01 = f2_fma(f2_pack(av[e], bv[e]),
+                           f2_pack(fmaxf(__uint_as_float(v[0][j]), 0.0f), fmaxf(__uint_as_float(v[1][j]), 0.0f)), s01);
+              s23 = f2_fma(f2_pack(cv[e], dv[e]),
+                           f2_pack(fmaxf(__uint_as_float(v[2][j]), 0.0f), fmaxf(__uint_as_float(v[3][j]), 0.0f)), s23);
+            }
+          }
+          float u[4];
+          f2_unpack(s01, &u[0], &u[1]);
+          f2_unpack(s23, &u[2], &u[3]);
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int qi = qfirst + b * QSTEP;
+            const int64_t m = cur_g * C::NQ + qi;
+            if (m < args.p.M) bound_finish(qi, m, u[b], agg[b]);
+          }
+        } else {
+          // more retained heads: the whole 31-column chain, two queries per TMEM wait
+#pragma unroll 1
+          for (int qi = qfirst; qi < C::NQ; qi += 2 * QSTEP) {
+            const int64_t ma = cur_g * C::NQ + qi;
+            if (ma >= args.p.M) break;
+            const int qb = qi + QSTEP;
+            const int64_t mb = cur_g * C::NQ + qb;
+            uint32_t va[32], vb[32];
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(qi * C::NCOLX), va);
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(qb * C::NCOLX), vb);
+            tmem_ld_wait();
+            bound_word(qi, ma, va);
+            if (mb < args.p.M) bound_word(qb, mb, vb);
+          }
         }
       } else if constexpr (C::PAIR) {
         // queries qi and qi + QSTEP, chains packed (a in the low half, b in the high half)
