@@ -339,25 +339,43 @@ __device__ __forceinline__ float e4m3_to_f(uint8_t b) {
   return s ? -v : v;
 }
 
-// One key or query row (D values, bf16 or e4m3 codes) into dst[0..D) as fp32:
-// the warp loads it with one 8-byte (bf16) or 4-byte (e4m3) load per lane.
-__device__ __forceinline__ void warp_load_row(const void* base, int dtype, int64_t row, int D, float* dst) {
-  const int lane = threadIdx.x & 31;
-  for (int d = 4 * lane; d < D; d += 128) {
-    float v[4];
-    if (dtype == IDX_FP8_E4M3) {
-      const uint32_t c = *reinterpret_cast<const uint32_t*>((const uint8_t*)base + row * D + d);
+// Rows row_of(i), i < n, of `base` (D values each: bf16, or e4m3 codes) into
+// dst[i * DP + d] as fp32, by the whole block: every thread issues up to four
+// 16-byte loads before it stores any, so the rows arrive in about one memory
+// latency rather than one per row and warp.
+template <class RowOf>
+__device__ void block_load_rows(const void* base, int dtype, int n, int D, float* dst, int DP, RowOf row_of) {
+  const int esz = dtype == IDX_FP8_E4M3 ? 1 : 2;
+  const int per = 16 / esz;                 // values per 16-byte chunk
+  const int cpr = D / per;                  // chunks per row
+  const int total = n * cpr;
+  for (int c0 = 0; c0 < total; c0 += 4 * kPlanThreads) {
+    uint4 v[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = e4m3_to_f((uint8_t)(c >> (8 * e)));
-    } else {
-      const uint2 c = *reinterpret_cast<const uint2*>((const uint16_t*)base + row * D + d);
-      v[0] = bf16_to_f((uint16_t)(c.x & 0xffffu));
-      v[1] = bf16_to_f((uint16_t)(c.x >> 16));
-      v[2] = bf16_to_f((uint16_t)(c.y & 0xffffu));
-      v[3] = bf16_to_f((uint16_t)(c.y >> 16));
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * kPlanThreads + threadIdx.x;
+      if (c < total) {
+        const int64_t row = row_of(c / cpr);
+        v[u] = *reinterpret_cast<const uint4*>(static_cast<const char*>(base) + (row * D + (c % cpr) * per) * esz);
+      }
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) dst[d + e] = v[e];
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * kPlanThreads + threadIdx.x;
+      if (c >= total) continue;
+      float* o = dst + (c / cpr) * DP + (c % cpr) * per;
+      const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      if (dtype == IDX_FP8_E4M3) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[e] = e4m3_to_f((uint8_t)(w4[e >> 2] >> (8 * (e & 3))));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          o[2 * e] = bf16_to_f((uint16_t)(w4[e] & 0xffffu));
+          o[2 * e + 1] = bf16_to_f((uint16_t)(w4[e] >> 16));
+        }
+      }
+    }
   }
 }
 
@@ -381,6 +399,8 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   int* ret_pos = anchor + H;           // H: position among retained, -1 if omitted
   int* act = ret_pos + H;              // H: activation counts
   int* rlist = act + H;                // 32: retained heads ascending
+  float* wq = (float*)(rlist + 32);    // H: w_h (read many times below)
+  float* wfs = wq + H;                 // 32: folded weights, for the estimate
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nw = kPlanThreads / 32;
 
@@ -393,16 +413,16 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     return;
   }
   const uint16_t* qsrc = (const uint16_t*)p.q + m * (int64_t)H * D;
-  for (int h = wid; h < H; h += nw) warp_load_row(p.q, IDX_BF16, m * H + h, D, q + h * DP);
+  for (int h = tid; h < H; h += kPlanThreads) wq[h] = p.w[m * H + h];
+  block_load_rows(p.q, IDX_BF16, H, D, q, DP, [&](int h) { return (int64_t)(m * H + h); });
   // sample keys: seed[floor(i n / ns)], i < ns = min(n_sample, n)
   const int32_t* sl = a.seed_list + (a.shared_seeds ? 0 : m * a.list_ld);
   const int n = a.seed_cnt[a.shared_seeds ? 0 : m];
   const int ns = n < a.n_sample ? n : a.n_sample;
   const int64_t kbase = p.key_off ? p.key_off[m] : 0;
-  for (int si = wid; si < ns; si += nw) {
-    const int64_t id = sl[n <= a.n_sample ? si : (int)(((int64_t)si * n) / a.n_sample)];
-    warp_load_row(p.keys, p.k_dtype, kbase + id, D, ks + si * DP);
-  }
+  block_load_rows(p.keys, p.k_dtype, ns, D, ks, DP, [&](int si) {
+    return kbase + (int64_t)sl[n <= a.n_sample ? si : (int)(((int64_t)si * n) / a.n_sample)];
+  });
   __syncthreads();
   // ||q_h||^2, one warp per head, fixed order
   for (int h = wid; h < H; h += nw) {
@@ -414,10 +434,10 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   __syncthreads();
   // retained heads: the R largest |w_h| ||q_h||, ties to the lower head
   for (int h = tid; h < H; h += kPlanThreads) {
-    const float mh = fabsf(p.w[m * H + h]) * sqrtf(qn2[h]);
+    const float mh = fabsf(wq[h]) * sqrtf(qn2[h]);
     int rank = 0;
     for (int g = 0; g < H; ++g) {
-      const float mg = fabsf(p.w[m * H + g]) * sqrtf(qn2[g]);
+      const float mg = fabsf(wq[g]) * sqrtf(qn2[g]);
       rank += (mg > mh || (mg == mh && g < h)) ? 1 : 0;
     }
     ret_pos[h] = rank < R ? 1 : -1;
@@ -435,7 +455,7 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   // anchors of the omitted positive heads (section 3.1): one warp per head, the
   // dot products with the lanes across d (consecutive words: no bank conflicts)
   for (int h = wid; h < H; h += nw) {
-    const float wh = p.w[m * H + h];
+    const float wh = wq[h];
     int bj = -1;
     float bb = 0.0f, dnh = 0.0f;
     if (ret_pos[h] < 0 && wh > 0.0f) {
@@ -476,7 +496,7 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   const int NSQ = (ns + 3) / 4;
   for (int t = tid; t < H * NSQ; t += kPlanThreads) {
     const int h = t / NSQ, sq = t % NSQ;
-    const float wh = p.w[m * H + h];
+    const float wh = wq[h];
     if (!(ret_pos[h] < 0 && wh < 0.0f)) continue;
     const float* x = q + h * DP;
     int rows[4];
@@ -499,7 +519,7 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   for (int d = tid; d < D; d += kPlanThreads) {
     float s = 0.0f;
     for (int h = 0; h < H; ++h) {
-      const float wh = p.w[m * H + h];
+      const float wh = wq[h];
       if (ret_pos[h] < 0 && wh < 0.0f && ns > 0 && (float)act[h] >= need_act) s = __fmaf_rn(-wh, q[h * DP + d], s);
     }
     aggv[d] = s;
@@ -513,11 +533,12 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     float wf = 0.0f;
     if (r < R) {
       const int j = rlist[r];
-      wf = p.w[m * H + j];
+      wf = wq[j];
       for (int h = 0; h < H; ++h)
-        if (anchor[h] == j) wf = __fmaf_rn(p.w[m * H + h], beta[h], wf);
+        if (anchor[h] == j) wf = __fmaf_rn(wq[h], beta[h], wf);
     }
     wout[r] = wf;
+    wfs[r] = wf;
   }
   __syncthreads();
   // margin: bf16 rounding distance of a_A, plus gamma * (sum |w_h| ||q_h|| + ||a_A||)
@@ -545,7 +566,7 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     }
     float c = 0.0f, W = 0.0f;
     for (int h = 0; h < H; ++h) {
-      const float wh = p.w[m * H + h];
+      const float wh = wq[h];
       if (anchor[h] >= 0) c = __fmaf_rn(wh, dn[h], c);
       W = __fmaf_rn(fabsf(wh), sqrtf(qn2[h]), W);
     }
@@ -559,7 +580,7 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
       float qmax = 0.0f, sw = 0.0f, swf = 1.0f;
       for (int h = 0; h < H; ++h) {
         qmax = fmaxf(qmax, sqrtf(qn2[h]));
-        sw += fabsf(p.w[m * H + h]);
+        sw += fabsf(wq[h]);
       }
       for (int r = 0; r < kVec; ++r) swf += fabsf(wout[r]);
       const float vmax = fmaxf(qmax, sqrtf(A2) * 1.01f + sqrtf(E2) * 1.01f);
@@ -579,29 +600,39 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   row_extent(p, m, &off, &len);
   const int ne = len < a.n_sample ? len : a.n_sample;   // the sample area holds n_sample keys
   if (ne <= 0) return;
-  for (int si = wid; si < ne; si += nw) warp_load_row(p.keys, p.k_dtype, off + ((int64_t)si * len) / ne, D, ks + si * DP);
+  block_load_rows(p.keys, p.k_dtype, ne, D, ks, DP, [&](int si) { return off + ((int64_t)si * len) / ne; });
   __syncthreads();
   const float t = a.tau[m];
-  // U of every estimate key, one key per thread (the lanes walk different key rows)
+  // U of every estimate key, two threads per key (ne <= n_sample <= 128): one
+  // takes the first half of the retained vectors and the aggregate, the other
+  // the second half and ||k|| (an estimate: the split sum rounds differently)
   int pass = 0;
-  for (int si = tid; si < ne; si += kPlanThreads) {
-    const float* k = ks + si * DP;
-    float u = 0.0f;
-    for (int r = 0; r < R; ++r) {
-      const float* x = q + rlist[r] * DP;
-      float dot = 0.0f;
-      for (int d = 0; d < D; ++d) dot = __fmaf_rn(x[d], k[d], dot);
-      u = __fmaf_rn(wout[r], fmaxf(dot, 0.0f), u);
+  {
+    const int si = tid >> 1, half = tid & 1;
+    float part = 0.0f, dx = 0.0f;
+    if (si < ne) {
+      const float* k = ks + si * DP;
+      const int r0 = half ? R / 2 : 0, r1 = half ? R : R / 2;
+      for (int r = r0; r < r1; ++r) {
+        const float* x = q + rlist[r] * DP;
+        float dot = 0.0f;
+        for (int d = 0; d < D; ++d) dot = __fmaf_rn(x[d], k[d], dot);
+        part = __fmaf_rn(wfs[r], fmaxf(dot, 0.0f), part);
+      }
+      if (half == 0)
+        for (int d = 0; d < D; ++d) dx = __fmaf_rn(aggv[d], k[d], dx);   // a_A . k
+      else
+        for (int d = 0; d < D; ++d) dx = __fmaf_rn(k[d], k[d], dx);      // ||k||^2
     }
-    float da = 0.0f, dk = 0.0f;
-    for (int d = 0; d < D; ++d) {
-      da = __fmaf_rn(aggv[d], k[d], da);
-      dk = __fmaf_rn(k[d], k[d], dk);
+    const float part_o = __shfl_xor_sync(0xffffffffu, part, 1);
+    const float dx_o = __shfl_xor_sync(0xffffffffu, dx, 1);
+    if (si < ne && half == 0) {
+      float u = part + part_o;
+      u = u - fmaxf(dx, 0.0f);
+      u = __fmaf_rn(coef, sqrtf(dx_o), u);
+      if (p.k_dtype == IDX_FP8_E4M3) u *= p.key_scale[off + ((int64_t)si * len) / ne];
+      pass = u >= t ? 1 : 0;
     }
-    u = u - fmaxf(da, 0.0f);
-    u = __fmaf_rn(coef, sqrtf(dk), u);
-    if (p.k_dtype == IDX_FP8_E4M3) u *= p.key_scale[off + ((int64_t)si * len) / ne];
-    pass += u >= t ? 1 : 0;
   }
   for (int o = 16; o > 0; o >>= 1) pass += __shfl_xor_sync(0xffffffffu, pass, o);
   if (lane == 0) act[wid] = pass;   // the activation counts are no longer needed
@@ -1184,7 +1215,7 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
   pa.wfold = w.wfold;
   pa.coef = w.coef;
   const size_t psmem = ((size_t)p.H * (p.D + 1) + (size_t)dp.n_sample * (p.D + 1) + 4 * (size_t)p.H + p.D) * sizeof(float) +
-                       (3 * (size_t)p.H + 32) * sizeof(int);
+                       (3 * (size_t)p.H + 32) * sizeof(int) + ((size_t)p.H + 32) * sizeof(float);
   DOSA_CHECK(cudaFuncSetAttribute(dosa_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem));
   dosa_plan_kernel<<<(unsigned)M, kPlanThreads, psmem, st>>>(pa);
   DOSA_CHECK(cudaGetLastError());
