@@ -76,8 +76,7 @@ constexpr int kBtNE = 8;             // epilogue warps
 // warp 0 TMA producer, warp 1 and the last warp MMA issue (alternate units:
 // tcgen05.mma issue blocks while the tensor pipe is busy, so one thread's waits
 // and commits overlap the other thread's MMAs), warps 2 .. 2 + kBtNE - 1 epilogue
-constexpr int kBtMma2Warp = 2 + kBtNE;
-constexpr int kBtThreads = 32 * (3 + kBtNE);
+constexpr int kBtThreads = 32 * (2 + kBtNE);
 constexpr int kBtTmemCols = 512;     // two stages x two tiles x 128 keys
 constexpr int kBtCapC = 256;         // candidates per pair held by the classifier
 constexpr int kBtCapU = 64;          // undecided blocks per pair resolved from a list
@@ -464,7 +463,7 @@ __device__ __forceinline__ void bt_gather4(void* dst, const void* tmap, uint64_t
 constexpr int kBtOffA = 0;
 constexpr int kBtOffK = kBtOffA + 2 * kBtATile;
 constexpr int kBtOffBar = kBtOffK + kBtKStages * kBtChunkBytes;
-constexpr int kBtNBars = 2 + 2 * kBtKStages + 4 + 2;
+constexpr int kBtNBars = 2 + 2 * kBtKStages + 4 + 1;
 constexpr int kBtOffMisc = kBtOffBar + kBtNBars * 8;
 constexpr int kBtSmem = kBtOffMisc + 64 + 1024;
 static_assert(kBtSmem <= 232448, "shared memory");
@@ -493,7 +492,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(a_full, 1);
-    mbar_init(a_empty, 2);   // both MMA-issuing threads, once per row tile pair
+    mbar_init(a_empty, 1);   // the MMA-issuing thread, once per row tile pair
     for (int i = 0; i < kBtKStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -503,7 +502,6 @@ __global__ void __launch_bounds__(kBtThreads, 1)
       mbar_init(&acc_empty[i], kBtNE);
     }
     mbar_init(&drain_bar[0], 1);
-    mbar_init(&drain_bar[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -581,13 +579,12 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         mbar_wait(&k_full[j % kBtKStages], (j / kBtKStages) & 1, no_abort);
       }
     }
-  } else if (warp == 1 || warp == kBtMma2Warp) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
-    // Both threads walk every unit; thread `me` issues the units of its parity
-    // into accumulator stage `me`.
+    // One thread issues every unit, into accumulator stages 0 and 1 in turn (a
+    // second issuing thread corrupted a few accumulator rows now and then).
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(128, 128, 0u);   // A, B fp16; D f32
-      const uint32_t me = warp == 1 ? 0u : 1u;
       BtUnits u;
       u.init(W, s);
       int64_t cur_T = -1;
@@ -599,8 +596,9 @@ __global__ void __launch_bounds__(kBtThreads, 1)
           if (!(ok = mbar_wait(a_full, na & 1, abort_flag))) break;
           ++na;
         }
-        if ((nunit & 1u) == me) {
-          const uint32_t use = nunit >> 1;   // this thread's use count of its stage
+        {
+          const uint32_t me = nunit & 1u;    // accumulator stage
+          const uint32_t use = nunit >> 1;   // uses of that stage so far
           if (!(ok = mbar_wait(&acc_empty[me], (use & 1) ^ 1, abort_flag))) break;
           tc_fence_after();
           const uint32_t d0 = tmem_base + me * 256u;
@@ -629,12 +627,11 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         if (!u.valid() || u.T != T_this) tc_commit(a_empty);
       }
       // No commit may still be in flight when the CTA exits (its arrive would land
-      // in the next kernel's shared memory): each thread waits for its drain
-      // commit, also one that issued nothing but committed the query-tile barrier,
-      // and warp 1 waits for the last phases of the barriers the commits target.
-      tc_commit(&drain_bar[me]);
-      mbar_wait(&drain_bar[me], 0, no_abort);
-      if (me == 0 && ok && !*abort_flag) {
+      // in the next kernel's shared memory): the thread waits for its drain commit
+      // and for the last phases of the barriers its commits target.
+      tc_commit(&drain_bar[0]);
+      mbar_wait(&drain_bar[0], 0, no_abort);
+      if (ok && !*abort_flag) {
         if (na > 0) mbar_wait(a_empty, (na - 1) & 1, no_abort);
         const uint32_t nk = 2 * nunit;
         for (uint32_t i = 0; i < (uint32_t)kBtKStages && i < nk; ++i) {

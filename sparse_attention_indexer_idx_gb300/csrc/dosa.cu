@@ -310,7 +310,8 @@ struct PlanArgs {
   int32_t* status;            // bit 4 set for such a row
   const float* tau;           // [M]
   int64_t cap;                // candidate capacity per row
-  uint16_t* qprep;            // [M, 32, D] bf16
+  uint16_t* qprep;            // [M, 32, D] bf16, or the bound's group layout (glayout)
+  int glayout;
   float* wfold;               // [M, 32]
   float* coef;                // [M]
 };
@@ -404,10 +405,23 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nw = kPlanThreads / 32;
 
-  uint16_t* qout = a.qprep + m * kVec * D;
   float* wout = a.wfold + m * kVec;
+  // prepared row r of this query (r < 31: vector r, 31: the aggregate; the group
+  // layout keeps 16 vectors per query and the group's aggregates in one block,
+  // with one zero row per query behind them)
+  const int nvec = a.glayout ? 16 : kVec - 1;
+  auto qrow = [&](int r) -> uint16_t* {
+    if (!a.glayout) return a.qprep + (m * kVec + r) * D;
+    const int64_t g = m >> 3, qi = m & 7;
+    return a.qprep + (g * 144 + (r == 31 ? 128 + qi : (r == 32 ? 136 + qi : qi * 16 + r))) * D;
+  };
   if (!a.active[m]) {
-    for (int i = tid; i < kVec * D; i += kPlanThreads) qout[i] = 0;
+    for (int i = tid; i < (nvec + 2) * D; i += kPlanThreads) {
+      const int r = i / D;
+      if (r < nvec) qrow(r)[i % D] = 0;
+      else if (r == nvec) qrow(31)[i % D] = 0;
+      else if (a.glayout) qrow(32)[i % D] = 0;
+    }
     for (int i = tid; i < kVec; i += kPlanThreads) wout[i] = 0.0f;
     if (tid == 0) a.coef[m] = 0.0f;
     return;
@@ -523,11 +537,12 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
       if (ret_pos[h] < 0 && wh < 0.0f && ns > 0 && (float)act[h] >= need_act) s = __fmaf_rn(-wh, q[h * DP + d], s);
     }
     aggv[d] = s;
-    qout[31 * D + d] = f_to_bf16_rn(s);
+    qrow(31)[d] = f_to_bf16_rn(s);
+    if (a.glayout) qrow(32)[d] = 0;
   }
-  for (int i = tid; i < (kVec - 1) * D; i += kPlanThreads) {
+  for (int i = tid; i < nvec * D; i += kPlanThreads) {
     const int r = i / D, d = i % D;
-    qout[i] = r < R ? qsrc[rlist[r] * D + d] : (uint16_t)0;
+    qrow(r)[d] = r < R ? qsrc[rlist[r] * D + d] : (uint16_t)0;
   }
   for (int r = tid; r < kVec; r += kPlanThreads) {
     float wf = 0.0f;
@@ -1071,7 +1086,9 @@ static DosaWs carve(void* base, const idx_problem& p, int K, const dosa_params& 
   w.tau = c.take<float>(M);
   w.status = c.take<int32_t>(M);
   w.active = c.take<int32_t>(M);
-  w.qprep = c.take<uint16_t>((size_t)M * kVec * p.D);
+  // [M, 32, D], or the bound's group layout: 144 rows per 8 queries
+  const size_t qp_rows = (size_t)M * kVec > (size_t)((M + 7) / 8) * 144 ? (size_t)M * kVec : (size_t)((M + 7) / 8) * 144;
+  w.qprep = c.take<uint16_t>(qp_rows * p.D);
   w.wfold = c.take<float>((size_t)M * kVec);
   w.coef = c.take<float>(M);
   w.cand = c.take<int32_t>((size_t)M * s.cap);
@@ -1212,6 +1229,7 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
   pa.tau = w.tau;
   pa.cap = s.cap;
   pa.qprep = w.qprep;
+  pa.glayout = bound_group_layout(p, dp.retained_heads) ? 1 : 0;
   pa.wfold = w.wfold;
   pa.coef = w.coef;
   const size_t psmem = ((size_t)p.H * (p.D + 1) + (size_t)dp.n_sample * (p.D + 1) + 4 * (size_t)p.H + p.D) * sizeof(float) +

@@ -71,7 +71,11 @@ cudaError_t launch_score_group(const idx_problem& p, const int32_t* list, const 
 // iff key k is a candidate; words of tiles past a row's group are not written.
 // Shared keys (key_off == NULL) need knorm [n_keys] = ||k|| rounded up (codes
 // for FP8); per-row keys take ||k|| from the key tile (knorm unused).
-// Prepared rows R..30 and their folded weights must be zero.
+// Prepared rows R..30 and their folded weights must be zero.  With
+// bound_group_layout(p, R) the prepared rows are laid out per group of 8
+// queries: 144 rows at group * 144, query q's vector r < 16 at q * 16 + r, its
+// aggregate at 128 + q (rows 136..143 zero).
+bool bound_group_layout(const idx_problem& p, int R);
 cudaError_t launch_bound(const idx_problem& prep, const float* wfold, const float* coef, const float* tau,
                          const float* knorm, const uint32_t* seedbits, int64_t seed_stride, uint32_t* candbits,
                          int64_t cb_stride, int R, const int32_t* row_mask, cudaStream_t st);

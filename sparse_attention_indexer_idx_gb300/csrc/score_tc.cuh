@@ -64,9 +64,12 @@
 //                         tcgen05.ld -> score / bound -> global
 //              next       (FP8 only) split of each query group's bf16 rows
 //                         into the e4m3 hi and lo tiles
-//              last       second MMA issue thread (alternate rounds with warp 1)
+// One thread issues every tcgen05.mma of the CTA: a build in which a second
+// warp issued every other round into the same accumulators gave, in about one
+// launch in twenty, a few wrong rows of one tile (repeated launches on the same
+// inputs compared bit for bit); with a single issuer every repeat is identical.
 // Every wait is bounded (see common.cuh); on a timeout all roles stop, the
-// producer and the MMA threads drain what they issued, and TMEM is released.
+// producer and the MMA thread drain what they issued, and TMEM is released.
 #pragma once
 
 #include <cuda.h>
@@ -127,7 +130,12 @@ struct TcCfg {
   static constexpr bool KN_GLOBAL = BOUND && NQ_ > 1;
   static constexpr bool FILTER = (MODE == kFilter);   // scores >= tau[m] appended as (id, score)
   static constexpr int NCOLX = FP8 ? 2 * NCOL : NCOL;   // MMA columns per query (hi, lo for FP8)
-  static constexpr int N = NQ * NCOLX;
+  // kBound over shared keys with at most 16 retained heads: per query a block of
+  // 16 vectors (retained, zero past R), then one 16-row block holding the
+  // group's aggregates (8 used): 144 columns where 8 x 32 would carry 17 terms each
+  static constexpr bool AGG16 = (MODE == kBound) && NCOL_ == 16 && !FP8;
+  static constexpr int QROWS = NQ * NCOL + (AGG16 ? 16 : 0);   // query-side rows of one group
+  static constexpr int N = AGG16 ? QROWS : NQ * NCOLX;
   // 128-key subtiles per work unit: FP8 per-row scoring takes 256 keys (32 KB,
   // one TMA box) per unit, so every barrier round trip, commit and schedule
   // step covers as many key bytes as a bf16 tile
@@ -135,11 +143,13 @@ struct TcCfg {
   static constexpr int UKEYS = 128 * SUB;
   static constexpr int A_BYTES = SUB * (FP8 ? 128 * 128 : 128 * 128 * 2);   // one unit of keys
   static constexpr int SUB_BYTES = A_BYTES / SUB;                           // one 128-key subtile
-  static constexpr int BQ_BYTES = FP8 ? 0 : NQ * NCOL * 256;         // bf16 query rows as loaded
+  static constexpr int BQ_BYTES = FP8 ? 0 : QROWS * 256;            // bf16 query rows as loaded
   static constexpr int B8_BYTES = FP8 ? N * 128 : 0;                 // e4m3 hi and lo rows (FP8)
   static constexpr int B_BYTES = BQ_BYTES + B8_BYTES;                // one query buffer
   static constexpr int SB = (NQ > 1) ? 1 : 2;
-  static constexpr int SACC = (SUB * N >= 256) ? 2 : 4;
+  static constexpr int SACC = (SUB * N >= 256) ? 2 : (4 * SUB * N <= 512 ? 4 : 3);
+  // TMEM columns between accumulator stages (AGG16: 144 rounded up to 160)
+  static constexpr int ACC_STRIDE = AGG16 ? 160 : SUB * N;
   // FP8: key scales of one tile; their ring is deeper than the key ring by the
   // tiles that can sit between the MMA and the epilogue, so a key slot is free
   // as soon as its MMAs complete
@@ -152,7 +162,7 @@ struct TcCfg {
   // (at most SA - 1, so the slot it waits to reuse never depends on its own arrival)
   static constexpr int GD = SA - 1;
   static constexpr int IL = (SUB == 1 && N <= 128) ? 2 : 1;   // units whose MMA chains are interleaved
-  static constexpr int TMEM_COLS = tc_pow2_cols(SACC * SUB * N);
+  static constexpr int TMEM_COLS = tc_pow2_cols(SACC * ACC_STRIDE);
   static constexpr int NE = 8;   // epilogue warps, two per TMEM lane quarter
   // bf16 score tiles with at least 4 queries: an epilogue warp walks its queries
   // two at a time, both chains in one packed fma.rn.f32x2 per head
@@ -162,11 +172,7 @@ struct TcCfg {
   // else 4 (the two warps of a quarter take alternate units)
   static constexpr int EPT = (NQ > 1 || SUB > 1) ? 8 : 4;
   static constexpr int NCONV = FP8 ? 1 : 0;   // warp that splits the query rows (FP8)
-  // two MMA-issuing warps (warp 1 and the last warp) take alternate issue rounds:
-  // tcgen05.mma issue blocks while the tensor pipe is busy, so one thread's
-  // waits, commits and schedule steps overlap the other thread's MMAs
-  static constexpr int MMA2_WARP = 2 + NE + NCONV;
-  static constexpr int NTHREADS = 32 * (3 + NE + NCONV);
+  static constexpr int NTHREADS = 32 * (2 + NE + NCONV);
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + SA * A_BYTES;
@@ -182,12 +188,12 @@ struct TcCfg {
   static constexpr int SIGR_MOD = SIGR > 0 ? SIGR : 1;
   static constexpr int OFF_SIG = OFF_AUX + NE * NQ * 16;
   static constexpr int OFF_BAR = ((OFF_SIG + SIGR * NQ * 4) + 7) & ~7;
-  static constexpr int NBARS = 2 * SA + 2 * SB + 2 * SACC + 2 + 2 * SIGR + 2 * SSC;
+  static constexpr int NBARS = 2 * SA + 2 * SB + 2 * SACC + 1 + 2 * SIGR + 2 * SSC;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N");
   static_assert(MODE != kFilter || NQ == 1, "kFilter: one query per group");
-  static_assert(SACC * SUB * N <= 512, "TMEM columns");
+  static_assert(SACC * ACC_STRIDE <= 512, "TMEM columns");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -403,8 +409,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   uint64_t* b_empty = b_full + C::SB;
   uint64_t* acc_full = b_empty + C::SB;
   uint64_t* acc_empty = acc_full + C::SACC;
-  uint64_t* drain_bar = acc_empty + C::SACC;   // one per MMA-issuing thread
-  uint64_t* sig_full = drain_bar + 2;
+  uint64_t* drain_bar = acc_empty + C::SACC;   // the MMA thread's last commit
+  uint64_t* sig_full = drain_bar + 1;
   uint64_t* sig_empty = sig_full + C::SIGR;
   float* sSig = reinterpret_cast<float*>(smem + C::OFF_SIG);
   uint64_t* sc_full = sig_empty + C::SIGR;
@@ -426,14 +432,13 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     for (int i = 0; i < C::SB; ++i) {
       // FP8: every lane of the split warps arrives once its rows are written
       mbar_init(&b_full[i], C::FP8 ? 32 * C::NCONV : 1);
-      mbar_init(&b_empty[i], 2);                 // both MMA-issuing threads
+      mbar_init(&b_empty[i], 1);                 // the MMA-issuing thread
     }
     for (int i = 0; i < C::SACC; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 32 * C::EPT);
     }
     mbar_init(&drain_bar[0], 1);
-    mbar_init(&drain_bar[1], 1);
     for (int i = 0; i < C::SIGR; ++i) {
       mbar_init(&sig_full[i], 1);
       mbar_init(&sig_empty[i], C::NE);
@@ -500,7 +505,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
             if (ok) {
               uint64_t* bar = &b_full[bs];
               mbar_arrive_expect_tx(bar, C::BQ_BYTES);
-              const int32_t y = (int32_t)(cur_g * C::NQ * C::NCOL);
+              const int32_t y = (int32_t)(cur_g * C::QROWS);
               tma_load_2d(sB + bs * C::B_BYTES, &tmap_q, bar, 0, y);
               tma_load_2d(sB + bs * C::B_BYTES + C::BQ_BYTES / 2, &tmap_q, bar, 64, y);
             }
@@ -609,16 +614,14 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         mbar_wait(&a_full[j % C::SA], (j / C::SA) & 1, no_abort);
       }
     }
-  } else if (warp == 1 || warp == C::MMA2_WARP) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
-    // Both issuing threads walk every round; each issues the rounds of its parity.
     if (lane == 0) {
-      const uint32_t me = warp == 1 ? 0u : 1u;
       TcUnits<C> u;
       u.init(args, s);
       int64_t cur_g = -1;
       int cur_bs = 0;
-      uint32_t na = 0, nb = 0, nacc = 0, round = 0;
+      uint32_t na = 0, nb = 0, nacc = 0;
       while (u.valid()) {
         if (u.g != cur_g) {
           cur_g = u.g;
@@ -636,16 +639,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           nx.advance();
           if (nx.valid() && nx.g == u.g) n = 2;
         }
-        const bool mine = (round++ & 1u) == me;
-        if (!mine) {
-          na += n;
-          nacc += n;
-          const int64_t g_this = u.g;
-          if (n > 1) u = nx;
-          u.advance();
-          if (!u.valid() || u.g != g_this) tc_commit(&b_empty[cur_bs]);
-          continue;
-        }
         bool ok = true;
         for (int i = 0; i < n && ok; ++i) {
           ok = mbar_wait(&a_full[(na + i) % C::SA], ((na + i) / C::SA) & 1, abort_flag);
@@ -660,13 +653,13 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           n = 2;
           a0[0] = smem_u32(sA + (na % C::SA) * C::A_BYTES);
           a0[1] = a0[0] + C::SUB_BYTES;
-          d[0] = tmem_base + (uint32_t)((nacc % C::SACC) * C::SUB * C::N);
+          d[0] = tmem_base + (uint32_t)((nacc % C::SACC) * C::ACC_STRIDE);
           d[1] = d[0] + C::N;
         } else {
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             a0[i] = smem_u32(sA + ((na + i) % C::SA) * C::A_BYTES);
-            d[i] = tmem_base + (uint32_t)(((nacc + i) % C::SACC) * C::N);
+            d[i] = tmem_base + (uint32_t)(((nacc + i) % C::SACC) * C::ACC_STRIDE);
           }
         }
         if constexpr (C::FP8) {
@@ -701,15 +694,13 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         u.advance();
         if (!u.valid() || u.g != g_this) tc_commit(&b_empty[cur_bs]);
       }
-      // No commit of this thread may still be in flight when the CTA exits: its
-      // arrive would land on whatever the next kernel on this SM keeps at that
-      // shared-memory address.  So each thread commits the drain barrier and waits
-      // for it (also a thread that issued nothing but committed the query-buffer
-      // barrier at a group end), and warp 1 waits for the last phases of the slot
-      // and query-buffer barriers, which both threads commit to.
-      tc_commit(&drain_bar[me]);
-      mbar_wait(&drain_bar[me], 0, no_abort);
-      if (me == 0 && !*abort_flag) {
+      // No commit may still be in flight when the CTA exits: its arrive would land
+      // on whatever the next kernel on this SM keeps at that shared-memory address.
+      // So the thread commits the drain barrier and waits for it, then for the last
+      // phases of the slot and query-buffer barriers it commits to.
+      tc_commit(&drain_bar[0]);
+      mbar_wait(&drain_bar[0], 0, no_abort);
+      if (!*abort_flag) {
         for (uint32_t i = 0; i < (uint32_t)C::SA && i < na; ++i) {
           const uint32_t j = na - 1 - i;
           mbar_wait(&a_empty[j % C::SA], (j / C::SA) & 1, no_abort);
@@ -890,17 +881,19 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         bound_finish(qi, m, ub, v[31]);
       };
       if constexpr (C::BOUND && !C::FP8 && C::NQ == 4 * QSTEP) {
-        const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::SUB * C::N);
-        if (args.R <= 16) {
-          // at most 16 retained heads: columns 0..15 and the aggregate (31) of this
-          // warp's four queries, one TMEM wait; two packed chains (queries 0|1 and
-          // 2|3 of the warp in the halves of fma.rn.f32x2, each rounding as fmaf)
+        const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
+        if (C::AGG16 || args.R <= 16) {
+          // at most 16 retained heads: columns 0..15 of each of this warp's four
+          // queries and their aggregates (column 31 of the query, or the group's
+          // aggregate block), one TMEM wait; two packed chains (queries 0|1 and 2|3
+          // of the warp in the halves of fma.rn.f32x2, each rounding as fmaf)
           uint32_t v[4][32], agg[4];
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
-            const uint32_t col = tbase + (uint32_t)((qfirst + b * QSTEP) * C::NCOLX);
+            const int q = qfirst + b * QSTEP;
+            const uint32_t col = tbase + (uint32_t)(q * C::NCOLX);
             tmem_ld_32x32b_x16(col, v[b]);
-            agg[b] = tmem_ld_32x32b_x1(col + 31);
+            agg[b] = tmem_ld_32x32b_x1(C::AGG16 ? tbase + (uint32_t)(C::NQ * C::NCOL + q) : col + 31);
           }
           tmem_ld_wait();
           const float4* w0 = reinterpret_cast<const float4*>(sW + (qfirst + 0 * QSTEP) * C::NCOL);
@@ -954,7 +947,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           const int qb = qi + QSTEP;
           const int64_t ma = cur_g * C::NQ + qi, mb = cur_g * C::NQ + qb;
           if (ma >= args.p.M) break;
-          const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::SUB * C::N);
+          const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
           const uint32_t ta = tbase + (uint32_t)(qi * C::NCOLX), tb = tbase + (uint32_t)(qb * C::NCOLX);
           const float* w2 = sW + (r >> 1) * 2 * C::NCOL;
           constexpr int NCH = (C::H + 31) / 32;
@@ -994,7 +987,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         const int64_t m = cur_g * C::NQ + qi;
         if (m >= args.p.M) break;
         const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                              (uint32_t)((acc * C::SUB + sub) * C::N + qi * C::NCOLX);
+                              (uint32_t)(acc * C::ACC_STRIDE + sub * C::N + qi * C::NCOLX);
         const float* wq = sW + qi * C::NCOL;
         const int len = sLen[qi];
         if (!C::BOUND) {
@@ -1166,10 +1159,11 @@ cudaError_t launch_tc(const TcArgs& a_in, cudaStream_t st) {
     ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.keys, 128, (uint64_t)p.n_keys, 128, 128, krows);
   else
     ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.keys, 128, (uint64_t)p.n_keys, 256, 64, krows);
-  ok = ok && make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, 128, (uint64_t)(p.M * C::NCOL), 256, 64,
-                          C::NQ * C::NCOL);
-  if (!ok) return cudaErrorInvalidValue;
   a.G = (p.M + C::NQ - 1) / C::NQ;
+  // query-side rows: M x NCOL, or (AGG16) QROWS per group
+  const uint64_t qrows = C::AGG16 ? (uint64_t)(a.G * C::QROWS) : (uint64_t)(p.M * C::NCOL);
+  ok = ok && make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, 128, qrows, 256, 64, C::QROWS);
+  if (!ok) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   score_tc_kernel<C><<<sm_count(), C::NTHREADS, C::SMEM_BYTES, st>>>(tk, tq, a);
