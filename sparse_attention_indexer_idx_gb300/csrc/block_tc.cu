@@ -73,9 +73,8 @@ constexpr int kBtKStages = 10;       // key-chunk ring
 constexpr int kBtChunkBytes = 128 * 128;   // 128 rows x 64 fp16 (one 128-byte swizzle span)
 constexpr int kBtATile = 2 * kBtChunkBytes;   // 128 rows x 128 fp16
 constexpr int kBtNE = 8;             // epilogue warps
-// warp 0 TMA producer, warp 1 and the last warp MMA issue (alternate units:
-// tcgen05.mma issue blocks while the tensor pipe is busy, so one thread's waits
-// and commits overlap the other thread's MMAs), warps 2 .. 2 + kBtNE - 1 epilogue
+// warp 0 TMA producer, warp 1 MMA issue (one thread, every unit, the two
+// accumulator stages in turn), warps 2 .. 2 + kBtNE - 1 epilogue
 constexpr int kBtThreads = 32 * (2 + kBtNE);
 constexpr int kBtTmemCols = 512;     // two stages x two tiles x 128 keys
 constexpr int kBtCapC = 256;         // candidates per pair held by the classifier
