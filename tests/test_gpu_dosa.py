@@ -232,3 +232,19 @@ def test_shared_stream_per_row_seeds_and_fallback_rows(B):
     assert (np.delete(on[2], [5, 6]) == 0).all()
     _stream_counts_hold(on[3], off[3])
     assert B.device_error() == 0
+
+
+def test_bound_with_more_than_16_retained_heads(B):
+    """Shared bf16 keys with R = 20: the bound keeps 32 prepared rows per query (8 queries per tile);
+    with R <= 16 it takes the group layout (16 rows per query, one block of aggregates).  Both
+    layouts must leave the output equal to the unpruned top-K; 21 queries end on a partial group."""
+    wp = wl.prefill_bf16(seed=51, n_queries=21, H=64, D=128, L=5000, K=200, n_seed=1024, R=20, q_noise=0.001,
+                         q_run=3, positive_w=True)
+    p = B.problem_to_device(wp)
+    u = _unpruned(B, p, wp.K)
+    for R in (20, 16, 9):
+        d_ids, d_sc, st, stats = _pruned(B, p, wp.K, n_seed=1024, retained_heads=R, candidate_capacity=5000)
+        _same(*u, d_ids, d_sc)
+        assert (st == 0).all(), (R, st)
+        assert stats[2] < stats[0] - stats[1], (R, stats)
+    assert B.device_error() == 0
