@@ -7,7 +7,8 @@ learned slots are set to -1 padding.  One step = score every visible key
 (idx_score) -> exact top-K (idx_topk_scores) -> padding -> witness_merge.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode|prefill|prefill_dosa|ragged_fp8|block_select|tiny]
+                  [--workload decode|prefill|prefill_dosa|prefill_dosa_aligned|ragged_fp8|ragged_fp8_dosa|
+                              decode_prior|ragged_fp8_prior|block_select|tiny]
 
 Prints ONE JSON line (rank 0).  `value` is queries*keys scored per second over
 the whole job (inputs resident in HBM); `e2e` is the same metric through the
