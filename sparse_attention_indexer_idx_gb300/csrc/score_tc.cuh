@@ -163,14 +163,16 @@ struct TcCfg {
   static constexpr int GD = SA - 1;
   static constexpr int IL = (SUB == 1 && N <= 128) ? 2 : 1;   // units whose MMA chains are interleaved
   static constexpr int TMEM_COLS = tc_pow2_cols(SACC * ACC_STRIDE);
-  static constexpr int NE = 8;   // epilogue warps, two per TMEM lane quarter
+  // epilogue warps, two per TMEM lane quarter (four for the bf16 bound over
+  // several queries, whose dependent chains leave two warps per quarter idle)
+  static constexpr int NE = (MODE == kBound && NQ_ > 1 && KDT_ != IDX_FP8_E4M3) ? 16 : 8;
   // bf16 score tiles with at least 4 queries: an epilogue warp walks its queries
   // two at a time, both chains in one packed fma.rn.f32x2 per head
   static constexpr bool PAIR = (MODE != kBound) && (MODE != kFilter) && !FP8 && NQ >= 4;
   // epilogue warps that read one unit: all 8 when a unit holds several queries
   // (alternating queries) or two subtiles (one warp of a quarter per subtile),
   // else 4 (the two warps of a quarter take alternate units)
-  static constexpr int EPT = (NQ > 1 || SUB > 1) ? 8 : 4;
+  static constexpr int EPT = (NQ > 1 || SUB > 1) ? NE : 4;
   static constexpr int NCONV = FP8 ? 1 : 0;   // warp that splits the query rows (FP8)
   static constexpr int NTHREADS = 32 * (2 + NE + NCONV);
   // shared memory layout (offsets from a 1024-aligned base)
@@ -716,7 +718,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     const int ew = warp - 2;                   // epilogue warp index
     const int quarter = warp & 3;              // TMEM lanes this warp may read
     const int qfirst = C::NQ > 1 ? (ew >> 2) : 0;   // first query of this warp in a tile
-    constexpr int QSTEP = C::NQ > 1 ? 2 : 1;
+    constexpr int QSTEP = C::NQ > 1 ? C::NE / 4 : 1;  // warps per lane quarter
     const int tile_par = ew >> 2;              // one query per tile: the parity of the tiles this warp takes
     const int sub = C::SUB > 1 ? (ew >> 2) : 0;   // two subtiles per unit: the one this warp reads
     const int row_in_tile = quarter * 32 + lane;
@@ -880,46 +882,49 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         }
         bound_finish(qi, m, ub, v[31]);
       };
-      if constexpr (C::BOUND && !C::FP8 && C::NQ == 4 * QSTEP) {
+      if constexpr (C::BOUND && !C::FP8 && C::NQ > 1 && (C::NQ == 4 * QSTEP || C::NQ == 2 * QSTEP)) {
+        constexpr int QPW = C::NQ / QSTEP;     // queries of this warp in a tile
         const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
         if (C::AGG16 || args.R <= 16) {
           // at most 16 retained heads: columns 0..15 of each of this warp's four
           // queries and their aggregates (column 31 of the query, or the group's
           // aggregate block), one TMEM wait; two packed chains (queries 0|1 and 2|3
           // of the warp in the halves of fma.rn.f32x2, each rounding as fmaf)
-          uint32_t v[4][32], agg[4];
+          uint32_t v[QPW][32], agg[QPW];
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
+          for (int b = 0; b < QPW; ++b) {
             const int q = qfirst + b * QSTEP;
             const uint32_t col = tbase + (uint32_t)(q * C::NCOLX);
             tmem_ld_32x32b_x16(col, v[b]);
             agg[b] = tmem_ld_32x32b_x1(C::AGG16 ? tbase + (uint32_t)(C::NQ * C::NCOL + q) : col + 31);
           }
           tmem_ld_wait();
-          const float4* w0 = reinterpret_cast<const float4*>(sW + (qfirst + 0 * QSTEP) * C::NCOL);
-          const float4* w1 = reinterpret_cast<const float4*>(sW + (qfirst + 1 * QSTEP) * C::NCOL);
-          const float4* w2 = reinterpret_cast<const float4*>(sW + (qfirst + 2 * QSTEP) * C::NCOL);
-          const float4* w3 = reinterpret_cast<const float4*>(sW + (qfirst + 3 * QSTEP) * C::NCOL);
-          uint64_t s01 = f2_pack(0.0f, 0.0f), s23 = f2_pack(0.0f, 0.0f);
+          // queries 2c and 2c + 1 of this warp in the halves of chain c
+          uint64_t sc2[QPW / 2];
+#pragma unroll
+          for (int c = 0; c < QPW / 2; ++c) sc2[c] = f2_pack(0.0f, 0.0f);
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4) {
-            const float4 a = w0[j4], b = w1[j4], c = w2[j4], d = w3[j4];
-            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-            const float cv[4] = {c.x, c.y, c.z, c.w}, dv[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 4 * j4 + e;
-              s01 = f2_fma(f2_pack(av[e], bv[e]),
-                           f2_pack(fmaxf(__uint_as_float(v[0][j]), 0.0f), fmaxf(__uint_as_float(v[1][j]), 0.0f)), s01);
-              s23 = f2_fma(f2_pack(cv[e], dv[e]),
-                           f2_pack(fmaxf(__uint_as_float(v[2][j]), 0.0f), fmaxf(__uint_as_float(v[3][j]), 0.0f)), s23);
+            for (int c = 0; c < QPW / 2; ++c) {
+              const float4 a = reinterpret_cast<const float4*>(sW + (qfirst + (2 * c) * QSTEP) * C::NCOL)[j4];
+              const float4 b = reinterpret_cast<const float4*>(sW + (qfirst + (2 * c + 1) * QSTEP) * C::NCOL)[j4];
+              const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int j = 4 * j4 + e;
+                sc2[c] = f2_fma(f2_pack(av[e], bv[e]),
+                                f2_pack(fmaxf(__uint_as_float(v[2 * c][j]), 0.0f),
+                                        fmaxf(__uint_as_float(v[2 * c + 1][j]), 0.0f)),
+                                sc2[c]);
+              }
             }
           }
-          float u[4];
-          f2_unpack(s01, &u[0], &u[1]);
-          f2_unpack(s23, &u[2], &u[3]);
+          float u[QPW];
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
+          for (int c = 0; c < QPW / 2; ++c) f2_unpack(sc2[c], &u[2 * c], &u[2 * c + 1]);
+#pragma unroll
+          for (int b = 0; b < QPW; ++b) {
             const int qi = qfirst + b * QSTEP;
             const int64_t m = cur_g * C::NQ + qi;
             if (m < args.p.M) bound_finish(qi, m, u[b], agg[b]);
