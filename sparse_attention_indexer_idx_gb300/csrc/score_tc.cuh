@@ -310,15 +310,6 @@ __device__ __forceinline__ int64_t tc_key_base(const TcArgs& A, int64_t m) {
   return off;
 }
 
-__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y0,
-                                            int32_t y1, int32_t y2, int32_t y3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
-      "%5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
-      : "memory");
-}
-
 // ----------------------------------------------------------- FP8 helpers ---
 // Power-of-two scale of a query row: max|q| / sigma lies in [128, 256).
 __device__ __forceinline__ void row_sigma(float amax, float* sigma, float* inv) {
@@ -1159,7 +1150,8 @@ cudaError_t launch_tc(const TcArgs& a_in, cudaStream_t st) {
   if (p.n_keys >= ((int64_t)1 << 31) || p.M * C::NCOL >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
   CUtensorMap tk, tq;
   bool ok;
-  const uint32_t krows = C::GATHER ? 1u : (uint32_t)C::UKEYS;     // gather4 wants a one-row box
+  // gathered modes copy key rows with cp.async and never read through this map
+  const uint32_t krows = C::GATHER ? 1u : (uint32_t)C::UKEYS;
   if (C::FP8)
     ok = make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.keys, 128, (uint64_t)p.n_keys, 128, 128, krows);
   else
