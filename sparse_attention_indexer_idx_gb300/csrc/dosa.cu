@@ -318,16 +318,6 @@ struct PlanArgs {
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
-// x . y over D floats in shared memory, the lanes across d; every lane gets the sum.
-__device__ __forceinline__ float warp_dot(const float* x, const float* y, int D) {
-  const int lane = threadIdx.x & 31;
-  float s = 0.0f;
-  for (int d = lane; d < D; d += 32) s = __fmaf_rn(x[d], y[d], s);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  return s;
-}
-
 __device__ __forceinline__ uint16_t f_to_bf16_rn(float x) {
   uint32_t u = __float_as_uint(x);
   u += 0x7fffu + ((u >> 16) & 1u);
@@ -402,6 +392,7 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   int* rlist = act + H;                // 32: retained heads ascending
   float* wq = (float*)(rlist + 32);    // H: w_h (read many times below)
   float* wfs = wq + H;                 // 32: folded weights, for the estimate
+  float* gram = wfs + 32;              // H x 32: q_h . q_j for the retained heads j
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nw = kPlanThreads / 32;
 
@@ -466,8 +457,18 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
       }
   }
   __syncthreads();
-  // anchors of the omitted positive heads (section 3.1): one warp per head, the
-  // dot products with the lanes across d (consecutive words: no bank conflicts)
+  // anchors of the omitted positive heads (section 3.1): the dot products of
+  // every head with every retained head first, one thread per pair (d in order),
+  // then one warp per head picks its anchor and forms the residual norm
+  for (int t = tid; t < H * R; t += kPlanThreads) {
+    const int h = t / R, r = t - h * R;
+    const float* x = q + h * DP;
+    const float* y = q + rlist[r] * DP;
+    float dot = 0.0f;
+    for (int d = 0; d < D; ++d) dot = __fmaf_rn(x[d], y[d], dot);
+    gram[h * 32 + r] = dot;
+  }
+  __syncthreads();
   for (int h = wid; h < H; h += nw) {
     const float wh = wq[h];
     int bj = -1;
@@ -476,7 +477,7 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
       float best = 0.0f;
       for (int r = 0; r < R; ++r) {
         const int j = rlist[r];
-        const float dot = warp_dot(q + h * DP, q + j * DP, D);
+        const float dot = gram[h * 32 + r];
         const float b = qn2[j] > 0.0f ? fmaxf(0.0f, dot / qn2[j]) : 0.0f;
         const float r2 = qn2[h] - 2.0f * b * dot + b * b * qn2[j];
         if (bj < 0 || r2 < best) {
@@ -1233,7 +1234,7 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
   pa.wfold = w.wfold;
   pa.coef = w.coef;
   const size_t psmem = ((size_t)p.H * (p.D + 1) + (size_t)dp.n_sample * (p.D + 1) + 4 * (size_t)p.H + p.D) * sizeof(float) +
-                       (3 * (size_t)p.H + 32) * sizeof(int) + ((size_t)p.H + 32) * sizeof(float);
+                       (3 * (size_t)p.H + 32) * sizeof(int) + ((size_t)p.H + 32 + (size_t)p.H * 32) * sizeof(float);
   DOSA_CHECK(cudaFuncSetAttribute(dosa_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem));
   dosa_plan_kernel<<<(unsigned)M, kPlanThreads, psmem, st>>>(pa);
   DOSA_CHECK(cudaGetLastError());
