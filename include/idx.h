@@ -272,11 +272,18 @@ idx_status witness_indices(const int32_t* learned, int64_t rows, int32_t topk, c
  * Block size 0 gives empty selections.
  *
  * With block_size 128, D = 128 and top_blocks <= 512 the block maxima are
- * first computed on the tensor cores (tf32 operands, fp32 accumulate) with a
- * certified error bound e_b = (2^-9 + 2^-12) ||q|| max_p ||k_p||; a block
- * whose bound interval lies clear of the selection cut is decided by it, the
- * others are scored in the page's order.  The selection is the same either
- * way.  stats: device block_select_stats or NULL, added to (that route only).
+ * first computed on the tensor cores: every query row q and key block are
+ * rounded to fp16 under exact power-of-two scales (q~ = sigma fp16(q/sigma),
+ * k~ = s_b fp16(k/s_b), the largest magnitude in [2^14, 2^15)), multiplied on
+ * tcgen05 kind::f16 with fp32 accumulation, and each block maximum A_b
+ * carries the certified error bound
+ *   e_b = ||q~|| max_p ||k_p - k~_p|| + ||q - q~|| max_p ||k_p||
+ *         + 2^-12 ||q|| max_p ||k_p|| (+ 2^-118),
+ * the maxima over the block's visible positions, every factor rounded up (the
+ * last term covers the fp32 accumulation and the page's sequential sum).  A
+ * block whose interval [A_b - e_b, A_b + e_b] lies clear of the selection cut
+ * is decided by it, the others are scored in the page's order.  The selection
+ * is the same either way.  stats: device block_select_stats or NULL, added to (that route only).
  * Workspace: block_select_workspace_size(), about Q * n_kv * ceil(L/bs) * 8
  * bytes. */
 typedef struct block_sparse_config {

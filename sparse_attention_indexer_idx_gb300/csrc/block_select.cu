@@ -475,11 +475,15 @@ extern "C" idx_status block_select_static(const float* index_q, const float* ind
   if (D > 256) return fail(IDX_ERR_UNSUPPORTED, "D=%d above 256", D);
   if (D == 128 && (((uintptr_t)index_q | (uintptr_t)index_k) & 15))
     return fail(IDX_ERR_INVALID_ARG, "index_q/index_k must be 16-byte aligned");
-  const int64_t words = (int64_t)(block_select_core_ws(Q, n_kv, L, *cfg) / sizeof(uint32_t));
-  if (words > kStaticBlockScores)
+  // Q * n_kv * ceil(L / block_size) against the fixed array, by division so that
+  // no product can wrap before it is compared
+  const int64_t nbm = cfg->block_size > 0 ? (L + cfg->block_size - 1) / cfg->block_size : 0;
+  const bool too_big = Q > 0 && n_kv > 0 && nbm > 0 &&
+                       (Q > kStaticBlockScores / n_kv || nbm > kStaticBlockScores / (Q * n_kv));
+  if (too_big)
     return fail(IDX_ERR_WORKSPACE_TOO_SMALL,
-                "block_select_static: Q*n_kv*ceil(L/block_size) = %lld block scores exceed the fixed %lld",
-                (long long)words, (long long)kStaticBlockScores);
+                "block_select_static: Q=%lld x n_kv=%d x %lld blocks exceed the fixed %lld block scores",
+                (long long)Q, n_kv, (long long)nbm, (long long)kStaticBlockScores);
   if (Q * n_kv == 0) return IDX_OK;
   if (!index_q || !query_pos || !out || (L > 0 && !index_k)) return fail(IDX_ERR_INVALID_ARG, "NULL pointer");
   void* scratch = nullptr;
