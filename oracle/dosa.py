@@ -142,9 +142,10 @@ def choose_retained(q_m, w_m, R: int) -> np.ndarray:
 
 
 def choose_anchor(q_h, q_m, retained):
-    """(j, beta, ||q_h - beta q_j||) for the retained j with the smallest residual."""
+    """(j, beta, ||q_h - beta q_j||) for the retained j with the smallest residual;
+    among equal residuals the lowest j (the heads are visited in ascending order)."""
     best, best_j, best_beta = None, -1, 0.0
-    for j in retained:
+    for j in sorted(int(x) for x in retained):
         beta = anchor_coefficient(q_h, q_m[j])
         r = float(np.linalg.norm(np.asarray(q_h, np.float64) - beta * np.asarray(q_m[j], np.float64)))
         if best is None or r < best:
