@@ -193,6 +193,43 @@ idx_status dosa_topk(const idx_problem* p, int32_t K, const dosa_params* dp, con
                      int32_t seed_ld, int32_t* out_ids, float* out_scores, int32_t* row_status,
                      dosa_stats* stats, void* ws, size_t ws_bytes, void* stream);
 
+/* Where dosa_topk leaves the intermediate results of the pruned path inside
+ * its workspace (after the call completes), for tests and diagnostics: byte
+ * offsets from the workspace start.  Layouts, with M rows and H heads:
+ *   seed_list   int32 [seed_rows, seed_ld] ascending seed ids (seed_rows = 1
+ *               for the shared cold-rule seeds, else M), seed_count int32
+ *               [seed_rows];
+ *   rep_count   uint32 [rep_ld] (cold rule only): per key, how many
+ *               representative top-K lists hold it; rep_scores float32
+ *               [n_reps, rep_ld] the representatives' scores, n_reps = the
+ *               distinct floor(i (M-1) / 3), i = 0..3;
+ *   tau         float32 [M]; status int32 [M] (bit 0: too few seeds, bit 1:
+ *               candidate overflow, bit 2: bound scan skipped);
+ *   plan_head   int32 [M, H]: r >= 0 the head's position among the retained
+ *               heads, 1024 + j an omitted positive head anchored on head j,
+ *               -2 an omitted negative head in the aggregate set A, -1 any
+ *               other omitted head; plan_beta, plan_dnorm float32 [M, H]: beta
+ *               and ||q_h - beta q_j|| (rounded up) of the anchored heads;
+ *   wfold       float32 [M, 32] folded retained weights; coef float32 [M] =
+ *               c + rounding margin;
+ *   qprep       bf16 [M, 32, D] prepared vectors (row r < R: the retained head
+ *               at position r, row 31: the aggregate a_A rounded to bf16), or
+ *               with group_layout the bound's layout: per group of 8 rows 144
+ *               rows, row m's vector r at (m/8)*144 + (m%8)*16 + r and its
+ *               aggregate at (m/8)*144 + 128 + m%8.
+ * Rows whose status has bit 0 set have no plan.  Returns IDX_ERR_UNSUPPORTED
+ * for shapes where dosa_topk runs the unpruned path for every row. */
+typedef struct dosa_ws_layout {
+  int64_t seed_list, seed_count, rep_count, rep_scores, tau, status;
+  int64_t plan_head, plan_beta, plan_dnorm, wfold, coef, qprep;
+  int64_t seed_ld, rep_ld, seed_rows;
+  int32_t group_layout;
+  int32_t reserved;
+} dosa_ws_layout;
+
+idx_status dosa_workspace_layout(const idx_problem* p, int32_t K, const dosa_params* dp, int32_t seed_ld,
+                                 dosa_ws_layout* out);
+
 /* ----------------------------------------------------------- idx_topk_prior
  * Decode top-K with recent selections as a prior ("DoSA：用安全上界减少 Indexer 的
  * 完整打分": the decode path keeps full scoring; the keys of recent selections

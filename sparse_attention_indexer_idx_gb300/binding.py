@@ -57,6 +57,13 @@ class dosa_stats(ctypes.Structure):
 DOSA_STATS_FIELDS = len(dosa_stats._fields_)   # int64 counters of a device dosa_stats
 
 
+class dosa_ws_layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("seed_list", "seed_count", "rep_count", "rep_scores", "tau", "status",
+                                             "plan_head", "plan_beta", "plan_dnorm", "wfold", "coef", "qprep",
+                                             "seed_ld", "rep_ld", "seed_rows")] + \
+               [("group_layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 class topk_prior_stats(ctypes.Structure):
     _fields_ = [("rows_filtered", ctypes.c_ulonglong), ("candidates", ctypes.c_ulonglong),
                 ("dense_rows", ctypes.c_ulonglong)]
@@ -104,6 +111,9 @@ EXPORTS = {
                                    ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                    ctypes.c_void_p]),
+    "dosa_workspace_layout": (ctypes.c_int32, [ctypes.POINTER(idx_problem), ctypes.c_int32,
+                                               ctypes.POINTER(dosa_params), ctypes.c_int32,
+                                               ctypes.POINTER(dosa_ws_layout)]),
     "witness_merge": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
                                        ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_void_p]),
@@ -287,6 +297,14 @@ def dosa_topk(p: Problem, K: int, dp: dosa_params, out_ids: torch.Tensor, out_sc
                            _ptr(out_scores), _ptr(row_status), _ptr(stats), _ptr(ws),
                            ws.numel() * ws.element_size(), _stream(stream)))
     return out_ids, out_scores
+
+
+def dosa_workspace_layout(p: Problem, K: int, dp: dosa_params, seed_ld: int = 0) -> dict:
+    """Byte offsets (and row strides) of dosa_topk's intermediate arrays in its workspace."""
+    cp = p.c()
+    out = dosa_ws_layout()
+    _check(lib().dosa_workspace_layout(ctypes.byref(cp), K, ctypes.byref(dp), seed_ld, ctypes.byref(out)))
+    return {n: int(getattr(out, n)) for n, _ in dosa_ws_layout._fields_}
 
 
 def witness_merge(topk_ids: torch.Tensor, context_lens: torch.Tensor, keep: int, num_segments: int,

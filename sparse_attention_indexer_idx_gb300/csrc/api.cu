@@ -218,6 +218,17 @@ idx_status dosa_topk(const idx_problem* p, int32_t K, const dosa_params* dp, con
                      "dosa_topk");
 }
 
+idx_status dosa_workspace_layout(const idx_problem* p, int32_t K, const dosa_params* dp, int32_t seed_ld,
+                                 dosa_ws_layout* out) {
+  idx_status st = check_problem(p);
+  if (st) return st;
+  if (!dp || !out) return fail(IDX_ERR_INVALID_ARG, "NULL pointer");
+  if (K < 1 || K > IDX_MAX_K) return fail(IDX_ERR_INVALID_ARG, "K=%d outside [1, %d]", K, IDX_MAX_K);
+  if (!dosa_layout(*p, K, *dp, seed_ld > 0 ? seed_ld : 0, out))
+    return fail(IDX_ERR_UNSUPPORTED, "dosa_topk takes the unpruned path for this shape");
+  return IDX_OK;
+}
+
 idx_status witness_merge(int32_t* topk_ids, int64_t rows, int32_t topk, const int32_t* context_lens,
                          int64_t n_context_lens, int32_t keep, int32_t num_segments, int32_t max_replacements,
                          void* stream) {

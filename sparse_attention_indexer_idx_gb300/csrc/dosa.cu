@@ -314,6 +314,12 @@ struct PlanArgs {
   int glayout;
   float* wfold;               // [M, 32]
   float* coef;                // [M]
+  // per (row, head) record of the plan: the head's role (position r >= 0 among
+  // the retained heads; 1024 + j for an omitted positive head anchored on head
+  // j; -2 for an omitted negative head in A; -1 otherwise), beta and ||d_h||
+  int32_t* plan_head;         // [M, H]
+  float* plan_beta;           // [M, H]
+  float* plan_dn;             // [M, H]
 };
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
@@ -540,6 +546,16 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     aggv[d] = s;
     qrow(31)[d] = f_to_bf16_rn(s);
     if (a.glayout) qrow(32)[d] = 0;
+  }
+  for (int h = tid; h < H; h += kPlanThreads) {
+    const float wh = wq[h];
+    int code = -1;
+    if (ret_pos[h] >= 0) code = ret_pos[h];
+    else if (anchor[h] >= 0) code = 1024 + anchor[h];
+    else if (wh < 0.0f && ns > 0 && (float)act[h] >= need_act) code = -2;
+    a.plan_head[m * H + h] = code;
+    a.plan_beta[m * H + h] = beta[h];
+    a.plan_dn[m * H + h] = dn[h];
   }
   for (int i = tid; i < nvec * D; i += kPlanThreads) {
     const int r = i / D, d = i % D;
@@ -1012,6 +1028,9 @@ struct DosaWs {
   uint16_t* qprep;
   float* wfold;
   float* coef;
+  int32_t* plan_head;      // [M, H] the planner's record (see PlanArgs)
+  float* plan_beta;        // [M, H]
+  float* plan_dn;          // [M, H]
   int32_t* cand;
   int32_t* cand_cnt;
   int32_t* cand_n;
@@ -1092,6 +1111,9 @@ static DosaWs carve(void* base, const idx_problem& p, int K, const dosa_params& 
   w.qprep = c.take<uint16_t>(qp_rows * p.D);
   w.wfold = c.take<float>((size_t)M * kVec);
   w.coef = c.take<float>(M);
+  w.plan_head = c.take<int32_t>((size_t)M * p.H);
+  w.plan_beta = c.take<float>((size_t)M * p.H);
+  w.plan_dn = c.take<float>((size_t)M * p.H);
   w.cand = c.take<int32_t>((size_t)M * s.cap);
   w.cand_cnt = c.take<int32_t>(M);
   w.cand_n = c.take<int32_t>(M);
@@ -1125,6 +1147,32 @@ bool dosa_supported(const idx_problem& p, const dosa_params& dp) {
 size_t dosa_ws(const idx_problem& p, int K, const dosa_params& dp, int seed_ld) {
   if (!dosa_supported(p, dp)) return idx_topk_workspace_size(&p, K);
   return carve(nullptr, p, K, dp, seed_ld).used;
+}
+
+bool dosa_layout(const idx_problem& p, int K, const dosa_params& dp, int seed_ld, dosa_ws_layout* out) {
+  if (!dosa_supported(p, dp) || p.M <= 0) return false;
+  const DosaShape s = dosa_shape(p, K, dp, seed_ld);
+  // carved against a nominal 256-aligned base, offsets relative to it
+  const uintptr_t base = (uintptr_t)1 << 20;
+  const DosaWs w = carve(reinterpret_cast<void*>(base), p, K, dp, seed_ld);
+  auto off = [&](const void* x) { return (int64_t)(reinterpret_cast<uintptr_t>(x) - base); };
+  out->seed_list = off(w.list);
+  out->seed_count = off(w.seed_cnt);
+  out->rep_count = off(w.rep_count);
+  out->rep_scores = off(w.rep_sc);
+  out->tau = off(w.tau);
+  out->status = off(w.status);
+  out->plan_head = off(w.plan_head);
+  out->plan_beta = off(w.plan_beta);
+  out->plan_dnorm = off(w.plan_dn);
+  out->wfold = off(w.wfold);
+  out->coef = off(w.coef);
+  out->qprep = off(w.qprep);
+  out->seed_ld = s.NS;
+  out->rep_ld = s.ldmax;
+  out->seed_rows = s.shared_seeds ? 1 : p.M;
+  out->group_layout = bound_group_layout(p, dp.retained_heads) ? 1 : 0;
+  return true;
 }
 
 static int grid_for(int64_t n, int threads) {
@@ -1233,6 +1281,9 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
   pa.glayout = bound_group_layout(p, dp.retained_heads) ? 1 : 0;
   pa.wfold = w.wfold;
   pa.coef = w.coef;
+  pa.plan_head = w.plan_head;
+  pa.plan_beta = w.plan_beta;
+  pa.plan_dn = w.plan_dn;
   const size_t psmem = ((size_t)p.H * (p.D + 1) + (size_t)dp.n_sample * (p.D + 1) + 4 * (size_t)p.H + p.D) * sizeof(float) +
                        (3 * (size_t)p.H + 32) * sizeof(int) + ((size_t)p.H + 32 + (size_t)p.H * 32) * sizeof(float);
   DOSA_CHECK(cudaFuncSetAttribute(dosa_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem));

@@ -103,6 +103,9 @@ cudaError_t launch_topk_prior(const idx_problem& p, int K, const int32_t* prior,
                               void* ws, cudaStream_t st, const cudaEvent_t* ev = nullptr);
 
 size_t dosa_ws(const idx_problem& p, int K, const dosa_params& dp, int seed_ld);
+// Byte offsets of the pruned path's intermediate arrays in the workspace
+// (false where dosa_topk takes the unpruned path for every row).
+bool dosa_layout(const idx_problem& p, int K, const dosa_params& dp, int seed_ld, dosa_ws_layout* out);
 cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, const int32_t* seed_ids, int seed_ld,
                         int32_t* out_ids, float* out_scores, int32_t* row_status, dosa_stats* stats, void* ws,
                         size_t ws_bytes, cudaStream_t st);
