@@ -1,21 +1,29 @@
 """Benchmark of the indexer hot path on GB300.
 
-Default workload (the decode indexer batch): 64 query rows, each with its own
-32768 bf16 index keys, H=32 heads, D=128, exact top-K=2048, then the
-segment-witness merge (S=16, keep=K-S, max_replacements=S) after 5% of the
-learned slots are set to -1 padding.  One step = score every visible key
-(idx_score) -> exact top-K (idx_topk_scores) -> padding -> witness_merge.
+Default workload (the causal prefill indexer, the largest single-GPU
+configuration): 4096 queries at positions 61440..65535 over 65536 shared bf16
+index keys, H=64 heads, D=128, exact top-K=2048.  One step = score every
+visible key (idx_score, 260 M (query, key) pairs) -> exact top-K
+(idx_topk_scores).  The same line carries, as a nested `dosa` object, the
+DoSA-pruned top-K (dosa_topk, 12288 cold-rule seeds, 16 retained heads) on
+the same inputs: its step time, its speed-up over the unpruned step, its
+candidate and survival rates, how many rows stayed pruned, and whether its
+output equals the unpruned one bit for bit; `dosa_aligned` does the same on
+the near-parallel-heads prefill, where the bound prunes.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode|prefill|prefill_dosa|prefill_dosa_aligned|ragged_fp8|ragged_fp8_dosa|
-                              decode_prior|ragged_fp8_prior|block_select|tiny]
+                  [--workload prefill|decode|ragged_fp8|prefill_dosa|prefill_dosa_aligned|
+                              ragged_fp8_dosa|decode_prior|ragged_fp8_prior|block_select|tiny]
 
 Prints ONE JSON line (rank 0).  `value` is queries*keys scored per second over
 the whole job (inputs resident in HBM); `e2e` is the same metric through the
-C ABI with the inputs copied from pinned host memory and the top-K ids copied
-back inside the timed region.  `roofline` is for the dominant kernel, timed
-with CUDA events on its own stream inside the timed region.  `cpu_baseline`
-times the CPU oracle on a bounded sample of the same workload on this host.
+C ABI (idx_topk) with the inputs copied from pinned host memory and the top-K
+ids copied back inside the timed region.  `roofline` is for the dominant
+kernel, timed with CUDA events on its own stream inside the timed region.
+`cpu_baseline` times the CPU oracle on a bounded sample of the same workload
+on this host's cores (a process pool over every core this process may run
+on, and one core).  `witness_vs_memcpy` times witness_merge against a
+device-to-device copy of the same [rows, 2048] int32 buffer.
 --impl reference times the oracle alone (the reference arm of this build).
 Multi-GPU (torchrun): every rank runs its own independent batch (weak
 scaling, no data-path collective); the time is the max over ranks.
@@ -24,12 +32,14 @@ from __future__ import annotations
 
 import os
 
-# the CPU oracle leg runs single-threaded so its core count is exact
+# every CPU oracle process runs its BLAS on one thread, so a pool of N
+# processes uses exactly N cores
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse
 import json
+import multiprocessing as mp
 import statistics
 import subprocess
 import sys
@@ -203,12 +213,15 @@ class IndexerStep:
         pm = wp.extras.get("pad_mask")
         self.pad = None if pm is None else torch.from_numpy(pm).to(dev)
         self.ctx = self.p.key_len
-        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
         self.score_ms = []
         # score + top-K (filter and finish kernels) + witness merge
         self.launches = 1 + 2 + (1 if self.S else 0)
 
     def run(self, timed=False):
+        """score -> top-K [-> padding -> witness merge].  The padding (5% of the
+        learned slots set to -1, a torch op standing in for the learned
+        selection's padding) lies between events 2 and 3, outside the step."""
         B, p = self.B, self.p
         if timed:
             self.ev[0].record()
@@ -216,18 +229,25 @@ class IndexerStep:
         if timed:
             self.ev[1].record()
         B.idx_topk_scores(self.scores, p.key_len, self.ld, self.K, self.ids, None, ld=self.ld, ws=self.tk_ws)
+        if timed:
+            self.ev[2].record()
         if self.S:
             if self.pad is not None:
                 self.ids.masked_fill_(self.pad, -1)
+            if timed:
+                self.ev[3].record()
             B.witness_merge(self.ids, self.ctx, max(self.K - self.S, 0), self.S, self.S)
-        if timed:
-            self.ev[2].record()
+            if timed:
+                self.ev[4].record()
 
     def collect(self):
         self.score_ms.append(self.ev[0].elapsed_time(self.ev[1]))
 
     def step_ms(self):
-        return self.ev[0].elapsed_time(self.ev[2])
+        ms = self.ev[0].elapsed_time(self.ev[2])
+        if self.S:
+            ms += self.ev[3].elapsed_time(self.ev[4])
+        return ms
 
     def algorithmic_bytes(self):
         """Score kernel: every visible key row once, queries, weights, one fp32 score per pair."""
@@ -288,6 +308,29 @@ class DosaStep:
 
     def step_ms(self):
         return self.ev[0].elapsed_time(self.ev[1])
+
+    def info(self, stream, ref_ids=None, ref_sc=None):
+        """One more call with fresh counters: candidate / survival rates, rows that
+        stayed pruned, and (given the unpruned output) bit identity with it."""
+        self.stats.zero_()
+        rs = torch.full((self.wp.M,), -1, dtype=torch.int32, device=self.ids.device)
+        with torch.cuda.stream(stream):
+            self.B.dosa_topk(self.p, self.K, self.dp, self.ids, self.sc, self.ws, stats=self.stats, row_status=rs)
+        torch.cuda.synchronize()
+        st = self.stats.cpu().tolist()
+        nonseed = max(1, st[0] - st[1])
+        rs = rs.cpu().numpy()
+        out = {"pairs": st[0], "seed_pairs": st[1], "candidates": st[2], "survivors": st[3],
+               "fallback_rows": st[4], "skipped_rows": st[5], "group_keys": st[6], "solo_keys": st[7],
+               "group_stream": int(self.dp.group_stream),
+               "rows_pruned": int((rs == 0).sum()), "rows": int(self.wp.M),
+               # rates over all non-seed pairs: only meaningful when no row skipped the scan
+               "candidate_rate": st[2] / nonseed if st[5] == 0 else None,
+               "survival_rate": st[3] / nonseed if st[5] == 0 else None}
+        if ref_ids is not None:
+            out["identical_to_unpruned"] = bool(torch.equal(self.ids, ref_ids) and
+                                               torch.equal(self.sc.view(torch.int32), ref_sc.view(torch.int32)))
+        return out
 
 
 class BlockSelectStep:
@@ -448,43 +491,260 @@ def e2e_run(B, wp, dev, steps):
 
 
 # ------------------------------------------------------------- CPU baseline --
+# The oracle as it stands, run by a pool of worker processes (spawned, so that
+# no worker inherits a CUDA context), one core each.  A worker holds a
+# sub-problem with only the sampled rows (and the keys they read).
 
-def cpu_baseline(wl_name, wp, budget_s=12.0):
-    """The oracle as it stands, single-threaded, on a bounded sample of rows."""
+_ORACLE = None
+
+
+def _oracle_init(problem):
+    global _ORACLE
+    _ORACLE = problem
+
+
+def _oracle_indexer_row(task):
+    """Score + exact top-K (+ witness merge) of one row: row `task` of the worker's
+    problem, or row 0 of the one-row problem `task` (rows with their own keys)."""
     from oracle import dsa as odsa
     from oracle import witness as ow
-    if wl_name == "block_select":
-        from oracle import block_select as obs
-        bp = wp
-        t0 = time.perf_counter()
-        done_pairs, done_q = 0, 0
-        for i in range(bp.index_q.shape[0] - 1, -1, -37):
-            obs.block_sparse_select(bp.index_q[i], bp.index_k, int(bp.query_pos[i]), bp.block_size,
-                                    bp.top_blocks, bp.init_blocks, bp.local_blocks)
-            done_pairs += min(int(bp.query_pos[i]) + 1, bp.index_k.shape[0]) * bp.index_q.shape[1]
-            done_q += 1
-            if time.perf_counter() - t0 > budget_s:
-                break
-        dt = time.perf_counter() - t0
-        return {"value": done_pairs / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-                "sample": f"{done_q} queries (all 8 KV heads) of the workload, oracle.block_select"}
-    t0 = time.perf_counter()
-    pairs, rows = 0, 0
+    wp, m = (_ORACLE, task) if isinstance(task, int) else (task, 0)
+    ids, _, _, _ = odsa.row_topk(wp, m, wp.K)
     S = wp.extras.get("S", 0)
-    for m in range(wp.M):
-        ids, _, _, _ = odsa.row_topk(wp, m, wp.K)
-        if S:
-            ow.apply_topology_witnesses(ids, wp.K, [int(wp.key_len[m])], max(wp.K - S, 0), S, S)
-        pairs += int(wp.key_len[m])
-        rows += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": pairs / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{rows} of {wp.M} rows (score + top-K{' + witness merge' if S else ''}), oracle.dsa fp64"}
+    if S:
+        ow.apply_topology_witnesses(ids, wp.K, [int(wp.key_len[m])], max(wp.K - S, 0), S, S)
+    return int(wp.key_len[m])
+
+
+def _oracle_block_query(i):
+    """MiniMax selection of query i (all KV heads) of the worker's problem."""
+    from oracle import block_select as obs
+    bp = _ORACLE
+    obs.block_sparse_select(bp.index_q[i], bp.index_k, int(bp.query_pos[i]), bp.block_size, bp.top_blocks,
+                            bp.init_blocks, bp.local_blocks)
+    return min(int(bp.query_pos[i]) + 1, bp.index_k.shape[0]) * bp.index_q.shape[1]
+
+
+def _sub_indexer(wp, rows):
+    """The rows `rows` of an indexer problem as a problem of their own (row i of it
+    is row rows[i]); per-row keys are gathered, shared keys cut to what they see."""
+    rows = np.asarray(rows, dtype=np.int64)
+    key_len = np.asarray(wp.key_len)[rows].astype(np.int32)
+    scale = None
+    if wp.key_off is None:
+        n = int(key_len.max()) if rows.size else 0
+        keys, key_off = wp.keys[:n], None
+        if wp.key_scale is not None:
+            scale = wp.key_scale[:n]
+    else:
+        offs = np.asarray(wp.key_off)[rows]
+        keys = np.concatenate([wp.keys[o:o + l] for o, l in zip(offs, key_len)])
+        if wp.key_scale is not None:
+            scale = np.concatenate([wp.key_scale[o:o + l] for o, l in zip(offs, key_len)])
+        key_off = np.concatenate([[0], np.cumsum(key_len.astype(np.int64))[:-1]]).astype(np.int64)
+    extras = {k: v for k, v in wp.extras.items() if k != "pad_mask"}
+    return wl.IndexerProblem(wp.name, wp.dtype, wp.q[rows], wp.w[rows], keys, key_len, key_off, wp.K,
+                             key_scale=scale, extras=extras)
+
+
+def _sub_block(bp, queries):
+    queries = np.asarray(queries, dtype=np.int64)
+    pos = bp.query_pos[queries]
+    n = min(int(pos.max()) + 1, bp.index_k.shape[0])
+    return wl.BlockSelectProblem(bp.name, bp.index_q[queries], bp.index_k[:n], pos, bp.block_size, bp.top_blocks,
+                                 bp.init_blocks, bp.local_blocks)
+
+
+class OraclePool:
+    """A bounded sample of the workload and the processes that run the oracle on it."""
+
+    def __init__(self, wl_name, wp, cores):
+        self.block = wl_name == "block_select"
+        if self.block:
+            Q = wp.index_q.shape[0]
+            self.units = list(range(Q - 1, -1, -max(1, Q // 64)))          # 64 queries spread over [0, L)
+            self.sub = _sub_block(wp, self.units)
+            self.fn = _oracle_block_query
+            self.sample = (f"{len(self.units)} of {Q} queries (all {wp.index_q.shape[1]} KV heads), "
+                           "oracle.block_select (the page's sequential f32 dots)")
+        else:
+            stride = 16 if wp.M >= 1024 else 1                               # the prefill: every 16th query
+            self.units = list(range(0, wp.M, stride))
+            # shared keys travel to every worker once; rows with their own keys carry them in the task
+            self.wp = wp
+            self.per_row = wp.key_off is not None
+            self.sub = None if self.per_row else _sub_indexer(wp, self.units)
+            self.fn = _oracle_indexer_row
+            S = wp.extras.get("S", 0)
+            self.sample = (f"{'every 16th' if stride > 1 else 'every'} row ({len(self.units)} of {wp.M}): score + "
+                           f"top-K{' + witness merge' if S else ''}, oracle.dsa fp64")
+        self.cores = cores
+        self.pool = None
+        if cores > 1:
+            self.pool = mp.get_context("spawn").Pool(cores, initializer=_oracle_init, initargs=(self.sub,))
+
+    def _tasks(self, idx):
+        if not self.block and self.per_row:
+            return [_sub_indexer(self.wp, [self.units[i]]) for i in idx]
+        return list(idx)
+
+    def run(self, idx):
+        """Runs the sample's units `idx`; returns (pairs, seconds)."""
+        tasks = self._tasks(idx)
+        t0 = time.perf_counter()
+        if self.pool is None:
+            _oracle_init(self.sub)
+            pairs = sum(self.fn(t) for t in tasks)
+        else:
+            pairs = sum(self.pool.map(self.fn, tasks, chunksize=1))
+        return pairs, time.perf_counter() - t0
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.close()
+            self.pool.join()
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl_name, wp, one_core_units=None):
+    """The oracle as it stands on the sample, on every core of this host (a process
+    pool) and on one core (the first `one_core_units` units of the sample)."""
+    n = host_cores()
+    pool = OraclePool(wl_name, wp, n)
+    try:
+        idx = list(range(len(pool.units)))
+        pool.run(idx[:n])                       # workers started and warm
+        pairs, dt = pool.run(idx)
+    finally:
+        pool.close()
+    one = OraclePool(wl_name, wp, 1)
+    k1 = one_core_units or max(1, len(one.units) // 8)
+    p1, d1 = one.run(list(range(min(k1, len(one.units)))))
+    return {"value": pairs / dt, "unit": UNIT, "cores": n, "kind": "oracle", "sample": pool.sample,
+            "seconds": dt,
+            "single_core": {"value": p1 / d1, "unit": UNIT, "cores": 1, "seconds": d1,
+                            "sample": f"the first {min(k1, len(one.units))} units of the same sample"}}
+
+
+# ------------------------------------------------------- witness vs memcpy --
+
+def witness_vs_memcpy(B, dev, stream, reps=30):
+    """witness_merge (S = 64, topk 2048, keep = topk - S, B = S: the page's
+    setting) against a device-to-device copy of the same [rows, 2048] int32
+    buffer (cudaMemcpyAsync through torch), each timed by CUDA events on the
+    stream, median of `reps`; the merge runs on a fresh copy of the learned
+    rows every time (the refresh lies outside its events)."""
+    out = {}
+    topk, S = 2048, 64
+    for rows in (32, 64, 128, 256, 512, 65536):
+        learned, ctx = wl.witness_rows(seed=70 + rows, rows=rows, topk=topk, L_min=topk, L_max=131072)
+        with torch.cuda.stream(stream):
+            src = torch.from_numpy(learned).to(dev)
+            work = torch.empty_like(src)
+            dst = torch.empty_like(src)
+            c = torch.from_numpy(ctx).to(dev)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            tw, tc = [], []
+            for i in range(reps + 3):
+                work.copy_(src)
+                ev[0].record(stream)
+                B.witness_merge(work, c, topk - S, S, S, stream=stream)
+                ev[1].record(stream)
+                ev[2].record(stream)
+                dst.copy_(src)
+                ev[3].record(stream)
+                torch.cuda.synchronize()
+                if i >= 3:
+                    tw.append(ev[0].elapsed_time(ev[1]))
+                    tc.append(ev[2].elapsed_time(ev[3]))
+        mw, mc = statistics.median(tw), statistics.median(tc)
+        out[str(rows)] = {"witness_us": mw * 1e3, "memcpy_us": mc * 1e3, "ratio": mw / mc}
+    return out
 
 
 # --------------------------------------------------------------------- main --
+
+def _timed_steps(step, stream, steps, flush):
+    """`steps` calls of step.run(timed=True) on `stream`, each with its own events
+    (created and recorded once before, so none is created in the timed region);
+    returns the summed per-step milliseconds and the wall-clock region's."""
+    per_step = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    for evs in per_step + [[t_start, t_end]]:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        step.ev = per_step[i]
+        step.run(timed=True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    total = 0.0
+    for i in range(steps):
+        step.ev = per_step[i]
+        step.collect()
+        total += step.step_ms()
+    return total, t_start.elapsed_time(t_end)
+
+
+def dosa_nested(B, wp, dev, stream, steps, warmup, unpruned_ms, ref_ids, ref_sc, flush, capacity, group_stream):
+    """The DoSA-pruned top-K on the same inputs as the unpruned step."""
+    with torch.cuda.stream(stream):
+        d = DosaStep(B, wp, dev, R=wp.extras["R"], n_seed=wp.extras["n_seed"], capacity=capacity,
+                     group_stream=group_stream)
+        for _ in range(warmup):
+            d.run()
+        torch.cuda.synchronize()
+        total, _ = _timed_steps(d, stream, steps, flush)
+    ms = total / steps
+    out = {"ms_per_step": ms, "speedup_vs_unpruned": unpruned_ms / ms,
+           "pairs_per_s": wp.pairs() / (ms * 1e-3)}
+    out.update(d.info(stream, ref_ids, ref_sc))
+    return out
+
+
+def reference_arm(args):
+    """The CPU oracle on the machine's host cores, the same workload, metric and unit:
+    W warm-up steps and K timed steps, each a bounded part of the sample."""
+    wp = make_workload(args.workload, 0)
+    n = host_cores()
+    pool = OraclePool(args.workload, wp, n)
+    units = list(range(len(pool.units)))
+    per = max(n, min(len(units), 2 * n))       # units per step
+    samples = []
+    try:
+        for i in range(args.warmup + args.steps):
+            lo = (i * per) % len(units)
+            idx = (units[lo:] + units[:lo])[:per]
+            pairs, dt = pool.run(idx)
+            if i >= args.warmup:
+                samples.append(pairs / dt)
+    finally:
+        pool.close()
+    v = statistics.median(samples)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "l2": _l2_text(args.workload)},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": n, "kind": "oracle",
+                             "sample": f"{per} units per step of: {pool.sample}"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _l2_text(name):
+    return ("inputs larger than L2 (no flush)" if name in LARGE_INPUTS else
+            "L2 flushed before every timed step (256 MB write outside the step's events)")
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -492,52 +752,43 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=list(WORKLOAD_TEXT))
+    ap.add_argument("--workload", default="prefill", choices=list(WORKLOAD_TEXT))
     ap.add_argument("--capacity", type=int, default=16384, help="DoSA candidate capacity per row")
     ap.add_argument("--group-stream", type=int, default=1, choices=[0, 1],
                     help="DoSA shared candidate stream for groups of four queries (shared keys)")
     ap.add_argument("--rows", type=int, default=0, help="smaller batch (query rows) for profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the nested DoSA runs, the witness/memcpy leg and e2e (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        # rank 0 alone; the other ranks of a torchrun launch exit at once
+        if rank == 0:
+            print(json.dumps(reference_arm(args)))
+        return
+
     dist = None
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+        dist.init_process_group("nccl")
 
-    if args.impl == "reference":
-        if rank != 0:
-            if dist:
-                dist.destroy_process_group()
-            return
-        wp = make_workload(args.workload, 0)
-        samples = []
-        for _ in range(args.warmup):
-            pass
-        for _ in range(args.steps):
-            samples.append(cpu_baseline(args.workload, wp, budget_s=4.0))
-        v = statistics.median(s["value"] for s in samples)
-        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": WORKLOAD_TEXT[args.workload]},
-                "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                 "sample": samples[0]["sample"] + " per step"},
-                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
-        if dist:
-            dist.destroy_process_group()
-        return
+    # the CPU baseline first: its worker processes are spawned before this
+    # process touches the GPU
+    wp = make_workload(args.workload, rank, args.rows or None)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.rows:
+        cpu = cpu_baseline(args.workload, wp)
 
     from sparse_attention_indexer_idx_gb300 import binding as B
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     B.lib()
-    wp = make_workload(args.workload, rank, args.rows or None)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         if args.workload == "block_select":
@@ -561,54 +812,31 @@ def main():
             step.run()
         torch.cuda.synchronize()
         assert B.device_error() == 0, "device error during warm-up"
+        # inputs smaller than L2: a 256 MB write before every timed step evicts them; the
+        # step is then timed by its own events, which the flush lies outside of
+        flush = None if args.workload in LARGE_INPUTS else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         clocks = Clocks(torch.cuda.current_device())
         clocks.start()
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        # one event pair per step around the dominant kernel, on the launching stream
-        # (created and recorded once here, so no event is created inside the timed region)
-        per_step = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-        for evs in per_step + [[t_start, t_end]]:
-            for e in evs:
-                e.record(stream)
-        # inputs smaller than L2: a 256 MB write before every timed step evicts them; the
-        # step is then timed by its own events, which the flush lies outside of
-        flush = None if args.workload in LARGE_INPUTS else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-        torch.cuda.synchronize()
-        t_start.record(stream)
-        for i in range(args.steps):
-            if flush is not None:
-                flush.zero_()
-            step.ev = per_step[i]
-            step.run(timed=True)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        ms_total = t_start.elapsed_time(t_end)
+        ms_total, _ = _timed_steps(step, stream, args.steps, flush)
         clock_info = clocks.stop()
-    for i in range(args.steps):
-        step.ev = per_step[i]
-        step.collect()
-    if flush is not None:
-        ms_total = 0.0
-        for i in range(args.steps):
-            step.ev = per_step[i]
-            ms_total += step.step_ms()
     kernel_ms = step.score_ms
     ms_step = job_step_ms(ms_total / args.steps, device=dev)
     value = job_value(pairs_per_step, ms_step, world)
 
     hbm, bf16, bf16_sus, peak_src = _peaks()
     roof = None
+    extra = {}
     if isinstance(step, IndexerStep):
         k_ms = statistics.median(kernel_ms)
         if wp.dtype in ("bf16", "fp8") and wp.key_off is None:
             ach = step.flops() / (k_ms * 1e-3) / 1e12
             roof = {"kernel": "score_tc_kernel", "bound": "tensor", "achieved": ach, "peak": bf16, "unit": "TFLOP/s",
-                    "frac": ach / bf16, "traffic": None, "peak_source": f"{peak_src} bf16 burst",
-                    "kernel_ms": k_ms}
+                    "frac": ach / bf16, "traffic": SCORE_TRAFFIC.get(args.workload) if not args.rows else None,
+                    "peak_source": f"{peak_src} bf16 burst", "kernel_ms": k_ms,
+                    "algorithmic_flops": step.flops()}
         else:
             ach = step.algorithmic_bytes() / (k_ms * 1e-3) / 1e9
             traffic = SCORE_TRAFFIC.get(args.workload) if not args.rows else None
@@ -643,25 +871,35 @@ def main():
         k_ms = statistics.median(kernel_ms)
         roof = {"kernel": "dosa_topk (all kernels)", "bound": "tensor", "achieved": None, "peak": bf16,
                 "unit": "TFLOP/s", "frac": None, "traffic": None, "kernel_ms": k_ms}
-        step.stats.zero_()
-        with torch.cuda.stream(stream):
-            step.run()
-        torch.cuda.synchronize()
-        st = step.stats.cpu().tolist()
-        nonseed = max(1, st[0] - st[1])
-        dosa_info = {"pairs": st[0], "seed_pairs": st[1], "candidates": st[2], "survivors": st[3],
-                     "fallback_rows": st[4], "skipped_rows": st[5],
-                     "group_keys": st[6], "solo_keys": st[7], "group_stream": int(step.dp.group_stream),
-                     # rates over all non-seed pairs: only meaningful when no row skipped the scan
-                     "candidate_rate": st[2] / nonseed if st[5] == 0 else None,
-                     "survival_rate": st[3] / nonseed if st[5] == 0 else None}
+        extra["dosa"] = step.info(stream)
 
     e2e = None
-    if isinstance(step, IndexerStep):
+    if isinstance(step, IndexerStep) and not args.no_extras:
         with torch.cuda.stream(stream):
             e_ms, h2d, d2h = e2e_run(B, wp, dev, max(3, min(args.steps, 10)))
         e2e = {"value": pairs_per_step * world / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms, "api": "idx_topk"}
+
+    if isinstance(step, IndexerStep) and not args.no_extras and rank == 0:
+        # the pruned path on the same inputs, and on the near-parallel-heads prefill
+        if args.workload == "prefill" and not args.rows:
+            ref_ids, ref_sc = _unpruned_topk(B, step, stream)
+            extra["dosa"] = dosa_nested(B, wp, dev, stream, args.steps, args.warmup, ms_step, ref_ids, ref_sc,
+                                        flush, args.capacity, args.group_stream)
+            wa = make_workload("prefill_dosa_aligned", rank)
+            sa = IndexerStep(B, wa, dev)
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    sa.run()
+                torch.cuda.synchronize()
+                ua, _ = _timed_steps(sa, stream, args.steps, flush)
+            ra_ids, ra_sc = _unpruned_topk(B, sa, stream)
+            extra["dosa_aligned"] = dosa_nested(B, wa, dev, stream, args.steps, args.warmup, ua / args.steps,
+                                                ra_ids, ra_sc, flush, args.capacity, args.group_stream)
+            extra["dosa_aligned"]["unpruned_ms_per_step"] = ua / args.steps
+            extra["dosa_aligned"]["workload"] = WORKLOAD_TEXT["prefill_dosa_aligned"]
+            del sa, wa
+        extra["witness_vs_memcpy"] = witness_vs_memcpy(B, dev, stream)
 
     assert B.device_error() == 0, "device error during the timed region"
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -669,20 +907,30 @@ def main():
             "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "fp8": "fp8e4m3"}.get(
                 getattr(wp, "dtype", "f32"), "f32"),
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[args.workload], "l2": "inputs larger than L2 (no flush)"
-                       if args.workload in LARGE_INPUTS else
-                       "L2 flushed before every timed step (256 MB write outside the step's events)"},
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "l2": _l2_text(args.workload)},
             "rows_per_s": rows_per_step * world / (ms_step * 1e-3),
             "roofline": roof, "e2e": e2e, "clocks": clock_info,
             "gpu_launches": step.launches * args.steps}
-    if isinstance(step, DosaStep):
-        line["dosa"] = dosa_info
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, wp)
+    line.update(extra)
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
+
+
+def _unpruned_topk(B, step, stream):
+    """The unpruned top-K ids and scores of an IndexerStep's inputs (idx_topk)."""
+    wp = step.wp
+    with torch.cuda.stream(stream):
+        ids = torch.empty((wp.M, wp.K), dtype=torch.int32, device=step.dev)
+        sc = torch.empty((wp.M, wp.K), dtype=torch.float32, device=step.dev)
+        ws = torch.empty(B.idx_topk_workspace_size(step.p, wp.K), dtype=torch.uint8, device=step.dev)
+        B.idx_topk(step.p, wp.K, ids, sc, ws)
+    torch.cuda.synchronize()
+    del ws
+    return ids, sc
 
 
 if __name__ == "__main__":

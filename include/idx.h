@@ -65,6 +65,18 @@ const char* idx_last_error_string(void);
 /* Synchronises the device, returns the device error word and clears it. */
 uint32_t idx_device_error(void);
 
+/* Every wait inside a tensor-core pipeline (a warp waiting for a tile, an
+ * accumulator or a free slot) gives up after a time limit: the kernel then
+ * stops its pipeline, waits (with a fixed 2 s limit) for the copies and MMAs
+ * it has in flight, frees its tensor memory, returns, and sets
+ * IDX_DEVERR_WAIT_TIMEOUT; that call's output is undefined and later calls
+ * are unaffected.  This sets the limit, in nanoseconds, for every kernel of
+ * the library on the current device (after synchronising it); 0 gives up at
+ * the first wait that is not already complete (for tests of the failure
+ * path).  IDX_DEFAULT_WAIT_LIMIT_NS is the default. */
+#define IDX_DEFAULT_WAIT_LIMIT_NS 2000000000ull
+idx_status idx_set_wait_limit_ns(uint64_t ns);
+
 /* ----------------------------------------------------------- the problem ---
  * One batch of indexer rows ("DoSA：用安全上界减少 Indexer 的完整打分",
  * section 3: one index key per position, shared by every head of a query).

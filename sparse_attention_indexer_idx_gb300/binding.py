@@ -97,6 +97,7 @@ class block_sparse_config(ctypes.Structure):
 EXPORTS = {
     "idx_last_error_string": (ctypes.c_char_p, []),
     "idx_device_error": (ctypes.c_uint32, []),
+    "idx_set_wait_limit_ns": (ctypes.c_int32, [ctypes.c_uint64]),
     "idx_score": (ctypes.c_int32, [ctypes.POINTER(idx_problem), ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
     "idx_topk_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(idx_problem), ctypes.c_int32]),
     "idx_topk": (ctypes.c_int32, [ctypes.POINTER(idx_problem), ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
@@ -212,6 +213,14 @@ class Problem:
 def device_error() -> int:
     """Synchronise and return (then clear) the library's device error word."""
     return int(lib().idx_device_error())
+
+
+DEFAULT_WAIT_LIMIT_NS = 2_000_000_000
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of every pipeline wait in the library's kernels (current device)."""
+    _check(lib().idx_set_wait_limit_ns(int(ns)))
 
 
 def idx_score(p: Problem, scores: torch.Tensor, ld: Optional[int] = None, stream=None) -> torch.Tensor:

@@ -22,6 +22,16 @@ void register_error_word(uint32_t (*take)()) {
   error_words().push_back(take);
 }
 
+static std::vector<cudaError_t (*)(uint64_t)>& wait_limit_setters() {
+  static std::vector<cudaError_t (*)(uint64_t)> v;
+  return v;
+}
+
+void register_wait_limit_setter(cudaError_t (*set)(uint64_t)) {
+  std::lock_guard<std::mutex> lk(g_error_words_mu);
+  wait_limit_setters().push_back(set);
+}
+
 static thread_local std::string g_last_error;
 
 idx_status fail(idx_status st, const char* fmt, ...) {
@@ -90,6 +100,17 @@ uint32_t idx_device_error(void) {
   std::lock_guard<std::mutex> lk(g_error_words_mu);
   for (auto take : error_words()) v |= take();
   return v;
+}
+
+idx_status idx_set_wait_limit_ns(uint64_t ns) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_status(e, "idx_set_wait_limit_ns");
+  std::lock_guard<std::mutex> lk(g_error_words_mu);
+  for (auto set : wait_limit_setters()) {
+    e = set(ns);
+    if (e != cudaSuccess) return cuda_status(e, "idx_set_wait_limit_ns");
+  }
+  return IDX_OK;
 }
 
 idx_status idx_score(const idx_problem* p, float* scores, int64_t ld_scores, void* stream) {

@@ -515,8 +515,6 @@ __global__ void __launch_bounds__(kBtThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const BtSched s = *sched;
-  volatile int no_abort_storage = 0;
-  volatile int* no_abort = &no_abort_storage;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -572,10 +570,10 @@ __global__ void __launch_bounds__(kBtThreads, 1)
     }
     // drain: the last phase issued on every barrier has landed
     if (lane == 0) {
-      if (na > 0) mbar_wait(a_full, (na - 1) & 1, no_abort);
+      if (na > 0) mbar_wait_drain(a_full, (na - 1) & 1);
       for (uint32_t i = 0; i < (uint32_t)kBtKStages && i < nk; ++i) {
         const uint32_t j = nk - 1 - i;
-        mbar_wait(&k_full[j % kBtKStages], (j / kBtKStages) & 1, no_abort);
+        mbar_wait_drain(&k_full[j % kBtKStages], (j / kBtKStages) & 1);
       }
     }
   } else if (warp == 1) {
@@ -629,13 +627,13 @@ __global__ void __launch_bounds__(kBtThreads, 1)
       // in the next kernel's shared memory): the thread waits for its drain commit
       // and for the last phases of the barriers its commits target.
       tc_commit(&drain_bar[0]);
-      mbar_wait(&drain_bar[0], 0, no_abort);
+      mbar_wait_drain(&drain_bar[0], 0);
       if (ok && !*abort_flag) {
-        if (na > 0) mbar_wait(a_empty, (na - 1) & 1, no_abort);
+        if (na > 0) mbar_wait_drain(a_empty, (na - 1) & 1);
         const uint32_t nk = 2 * nunit;
         for (uint32_t i = 0; i < (uint32_t)kBtKStages && i < nk; ++i) {
           const uint32_t j = nk - 1 - i;
-          mbar_wait(&k_empty[j % kBtKStages], (j / kBtKStages) & 1, no_abort);
+          mbar_wait_drain(&k_empty[j % kBtKStages], (j / kBtKStages) & 1);
         }
       }
     }

@@ -43,8 +43,24 @@ static struct IdxErrorWordRegistrar {
 
 namespace idx {
 
-// Wait limit of a single mbarrier wait, in globaltimer nanoseconds.
+// Default limit of a single mbarrier wait, in globaltimer nanoseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Setter of this translation unit's pipeline wait limit (see idx_set_wait_limit_ns).
+void register_wait_limit_setter(cudaError_t (*set)(uint64_t));
+}  // namespace idx
+
+// The pipeline wait limit of the kernels of this translation unit (one copy per
+// unit, like the error word); idx_set_wait_limit_ns() sets every copy.
+static __device__ uint64_t g_wait_limit_ns = idx::kWaitLimitNs;
+
+static cudaError_t idx_set_unit_wait_limit(uint64_t ns) {
+  return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns));
+}
+static struct IdxWaitLimitRegistrar {
+  IdxWaitLimitRegistrar() { idx::register_wait_limit_setter(&idx_set_unit_wait_limit); }
+} idx_wait_limit_registrar;
+
+namespace idx {
 
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
@@ -108,16 +124,32 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
       : "memory");
   return ok != 0;
 }
-// Bounded wait: returns false (and flags the CTA and the device) when the
-// phase did not complete within the limit or another warp already aborted.
+// Bounded pipeline wait: returns false (and flags the CTA and the device) when
+// the phase did not complete within the unit's wait limit (g_wait_limit_ns,
+// 2 s unless the host set another) or another warp already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t limit = *(volatile uint64_t*)&g_wait_limit_ns;
   uint64_t t0 = global_ns();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit) {
       *abort_flag = 1;
+      atomicOr(&g_device_error, DEVERR_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+// Drain wait at the end of a kernel (copies and MMAs this thread issued that
+// must land before the CTA exits): always the fixed 2 s limit, whatever the
+// pipeline limit, so that an aborted CTA still waits for its work in flight.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
       atomicOr(&g_device_error, DEVERR_WAIT_TIMEOUT);
       return false;
     }

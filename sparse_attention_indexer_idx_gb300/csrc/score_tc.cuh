@@ -454,8 +454,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const TcSched s = *sched;
-  volatile int no_abort_storage = 0;
-  volatile int* no_abort = &no_abort_storage;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -600,11 +598,11 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     if (lane == 0) {
       for (uint32_t i = 0; i < (uint32_t)C::SB && i < nb; ++i) {
         uint32_t j = nb - 1 - i;
-        mbar_wait(&b_full[j % C::SB], (j / C::SB) & 1, no_abort);
+        mbar_wait_drain(&b_full[j % C::SB], (j / C::SB) & 1);
       }
       for (uint32_t i = 0; i < (uint32_t)C::SA && i < na; ++i) {
         uint32_t j = na - 1 - i;
-        mbar_wait(&a_full[j % C::SA], (j / C::SA) & 1, no_abort);
+        mbar_wait_drain(&a_full[j % C::SA], (j / C::SA) & 1);
       }
     }
   } else if (warp == 1) {
@@ -692,15 +690,15 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       // So the thread commits the drain barrier and waits for it, then for the last
       // phases of the slot and query-buffer barriers it commits to.
       tc_commit(&drain_bar[0]);
-      mbar_wait(&drain_bar[0], 0, no_abort);
+      mbar_wait_drain(&drain_bar[0], 0);
       if (!*abort_flag) {
         for (uint32_t i = 0; i < (uint32_t)C::SA && i < na; ++i) {
           const uint32_t j = na - 1 - i;
-          mbar_wait(&a_empty[j % C::SA], (j / C::SA) & 1, no_abort);
+          mbar_wait_drain(&a_empty[j % C::SA], (j / C::SA) & 1);
         }
         for (uint32_t i = 0; i < (uint32_t)C::SB && i < nb; ++i) {
           const uint32_t j = nb - 1 - i;
-          mbar_wait(&b_empty[j % C::SB], (j / C::SB) & 1, no_abort);
+          mbar_wait_drain(&b_empty[j % C::SB], (j / C::SB) & 1);
         }
       }
     }

@@ -55,3 +55,71 @@ def check_topk_row(g_ids, g_sc, s_ref, a_ref, K, eps):
     diff = set(real.tolist()) ^ set(o_ids.tolist())
     for x in diff:
         assert abs(s_ref[x] - s_k) <= eps * (a_ref[x] + a_k) + 1e-30, f"id {x} differs and is not near the K-th score"
+
+
+# ---------------------------------------------------------------------------
+# The oracle on every host core: a pool of spawned worker processes (spawned,
+# so that no worker inherits the test process's CUDA context), each running
+# its BLAS on one thread.  A worker holds one problem (the pool initializer's);
+# a task names a row of it, or carries a one-row problem of its own.
+
+_POOL_PROBLEM = None
+
+
+def _pool_init(problem):
+    global _POOL_PROBLEM
+    _POOL_PROBLEM = problem
+
+
+def oracle_pool(problem=None):
+    import multiprocessing as mp
+    import os
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return mp.get_context("spawn").Pool(n, initializer=_pool_init, initargs=(problem,))
+
+
+def row_check_task(task):
+    """(problem or None, row, gpu ids, gpu scores, eps): check_topk_row of that
+    row against oracle.dsa (None: the worker's problem)."""
+    from oracle import dsa as odsa
+    prob, m, ids, sc, eps = task
+    wp = _POOL_PROBLEM if prob is None else prob
+    s_ref, a_ref = odsa.row_scores(wp, m)
+    check_topk_row(ids, sc, s_ref, a_ref, wp.K, eps)
+    return m
+
+
+def block_select_task(i):
+    """oracle.block_select's selection of query i of the worker's problem."""
+    from oracle import block_select as obs
+    bp = _POOL_PROBLEM
+    return i, obs.block_sparse_select(bp.index_q[i], bp.index_k, int(bp.query_pos[i]), bp.block_size,
+                                      bp.top_blocks, bp.init_blocks, bp.local_blocks)
+
+
+def sub_problem(wp, rows):
+    """Rows `rows` of an indexer problem as a problem of their own; per-row keys
+    are gathered, a shared key sequence is cut to what those rows see."""
+    from sparse_attention_indexer_idx_gb300 import workloads as wl
+    rows = np.asarray(rows, dtype=np.int64)
+    key_len = np.asarray(wp.key_len)[rows].astype(np.int32)
+    scale = None
+    if wp.key_off is None:
+        n = int(key_len.max())
+        keys, key_off = wp.keys[:n], None
+        if wp.key_scale is not None:
+            scale = wp.key_scale[:n]
+    else:
+        offs = np.asarray(wp.key_off)[rows]
+        keys = np.concatenate([wp.keys[o:o + l] for o, l in zip(offs, key_len)])
+        if wp.key_scale is not None:
+            scale = np.concatenate([wp.key_scale[o:o + l] for o, l in zip(offs, key_len)])
+        key_off = np.concatenate([[0], np.cumsum(key_len.astype(np.int64))[:-1]]).astype(np.int64)
+    extras = {k: v for k, v in wp.extras.items() if k != "pad_mask"}
+    return wl.IndexerProblem(wp.name, wp.dtype, wp.q[rows], wp.w[rows], keys, key_len, key_off, wp.K,
+                             key_scale=scale, extras=extras)

@@ -90,15 +90,23 @@ def test_random_against_oracle(B, seed, Q, n_kv, D, L, bs, top, init, local):
     assert B.device_error() == 0
 
 
-def test_minimax_workload_sampled_queries(B):
+def test_minimax_workload_every_selection(B):
     """1024 queries x 8 KV heads over 131072 keys (block 128, top 32, init 1,
-    local 2); the oracle checks 12 sampled queries bit for bit."""
+    local 2): every (query, KV head) selection bit for bit against the oracle
+    (run on every host core)."""
+    from helpers import block_select_task, oracle_pool
     bp = wl.block_select()
     got = _gpu_select(B, bp.index_q, bp.index_k, bp.query_pos, bp.block_size, bp.top_blocks, bp.init_blocks,
                       bp.local_blocks)
-    for i in [0, 1, 2, 64, 511, 1000, 1022, 1023]:
-        ref = obs.block_sparse_select(bp.index_q[i], bp.index_k, int(bp.query_pos[i]), bp.block_size,
-                                      bp.top_blocks, bp.init_blocks, bp.local_blocks)
+    pool = oracle_pool(bp)
+    try:
+        # the late (long) queries first so the pool stays busy to the end
+        refs = pool.map(block_select_task, list(range(1023, -1, -1)), chunksize=1)
+    finally:
+        pool.close()
+        pool.join()
+    assert len(refs) == 1024
+    for i, ref in refs:
         assert got[i] == ref, i
     for i in range(1024):
         for h in range(8):

@@ -1,13 +1,17 @@
 """Parity at the full workload sizes, in the launch configuration the
-benchmark times: sampled rows against the fp64 oracle (scores within
-tolerance, top-K sets equal away from the K-th score), every row of the
-integer witness merge bit-exact, and the DoSA-pruned top-K bit-identical to
-the unpruned one on every row."""
+benchmark times, against the oracle run on every host core: every row of the
+decode batch (64) and of the ragged FP8 batch (128), every 16th query of the
+causal prefill (256 of 4096) and every (query, KV head) selection of the
+MiniMax workload (1024 x 8) -- scores within tolerance, top-K sets equal away
+from the K-th score, block indices bit-exact -- plus every row of the integer
+witness merge bit-exact, and the DoSA-pruned top-K bit-identical to the
+unpruned one on every row, with the number of rows that stayed on the pruned
+path asserted (the near-parallel-heads prefill: at least 99%)."""
 import numpy as np
 import pytest
 import torch
 
-from helpers import EPS, check_topk_row
+from helpers import EPS, check_topk_row, oracle_pool, row_check_task, sub_problem
 from oracle import dsa as odsa
 from oracle import witness as ow
 from sparse_attention_indexer_idx_gb300 import workloads as wl
@@ -50,9 +54,7 @@ def test_decode_bf16_full(B):
     p = B.problem_to_device(wp)
     ids, sc = _topk(B, p, wp.K)
     g_ids, g_sc = ids.cpu().numpy(), sc.cpu().numpy()
-    for m in (0, 31, 63):
-        s_ref, a_ref = odsa.row_scores(wp, m)
-        check_topk_row(g_ids[m], g_sc[m], s_ref, a_ref, wp.K, EPS["bf16"])
+    _check_rows_pooled(wp, g_ids, g_sc, range(wp.M), EPS["bf16"])
     learned = g_ids.copy()
     learned[wp.extras["pad_mask"]] = -1
     t = torch.from_numpy(learned).cuda()
@@ -63,9 +65,35 @@ def test_decode_bf16_full(B):
     assert B.device_error() == 0
 
 
+def _check_rows_pooled(wp, g_ids, g_sc, rows, eps):
+    """check_topk_row on `rows` by the oracle on every host core."""
+    rows = list(rows)
+    if wp.key_off is None:
+        sub = sub_problem(wp, rows)
+        tasks = [(None, i, g_ids[m], g_sc[m], eps) for i, m in enumerate(rows)]
+    else:
+        sub = None
+        tasks = [(sub_problem(wp, [m]), 0, g_ids[m], g_sc[m], eps) for m in rows]
+    pool = oracle_pool(sub)
+    try:
+        done = pool.map(row_check_task, tasks, chunksize=1)
+    finally:
+        pool.close()
+        pool.join()
+    assert len(done) == len(rows)
+
+
+def _pruned_rows(st, stats, M):
+    """Rows that stayed on the pruned path; consistent with the counters."""
+    pruned = int((st == 0).sum())
+    assert pruned == M - int(stats[4]), (pruned, stats)
+    return pruned
+
+
 @pytest.mark.parametrize("q_noise", [None, 0.05])
 def test_prefill_full_pruned_equals_unpruned(B, q_noise):
-    """4096 causal queries over 65536 keys, H64, K2048, 12288 seeds, R16."""
+    """4096 causal queries over 65536 keys, H64, K2048, 12288 seeds, R16; every
+    16th query against the oracle."""
     wp = wl.prefill_bf16(q_noise=q_noise)
     p = B.problem_to_device(wp)
     ids, sc = _topk(B, p, wp.K)
@@ -74,9 +102,29 @@ def test_prefill_full_pruned_equals_unpruned(B, q_noise):
     assert np.array_equal(u_ids, d_ids)
     assert np.array_equal(u_sc.view(np.uint32), d_sc.view(np.uint32))
     assert stats[0] == wp.pairs()
-    for m in (0, 2047, 4095):
-        s_ref, a_ref = odsa.row_scores(wp, m)
-        check_topk_row(u_ids[m], u_sc[m], s_ref, a_ref, wp.K, EPS["bf16"])
+    pruned = _pruned_rows(st, stats, wp.M)
+    print(f"prefill q_noise={q_noise}: {pruned} of {wp.M} rows pruned, {int(stats[5])} skipped the scan, "
+          f"{int(stats[2])} candidates, {int(stats[3])} survivors")
+    _check_rows_pooled(wp, u_ids, u_sc, range(0, wp.M, 16), EPS["bf16"])
+    assert B.device_error() == 0
+
+
+def test_prefill_aligned_full_pruned_equals_unpruned(B):
+    """The near-parallel-heads prefill (the benchmark's DoSA workload): the bound
+    prunes, so the identity covers the pruned path itself on nearly every row."""
+    wp = wl.prefill_bf16(seed=3, q_noise=0.001, q_run=16, positive_w=True)
+    p = B.problem_to_device(wp)
+    ids, sc = _topk(B, p, wp.K)
+    u_ids, u_sc = ids.cpu().numpy(), sc.cpu().numpy()
+    d_ids, d_sc, st, stats = _dosa(B, p, wp.K, n_seed=12288, retained_heads=16)
+    assert np.array_equal(u_ids, d_ids)
+    assert np.array_equal(u_sc.view(np.uint32), d_sc.view(np.uint32))
+    pruned = _pruned_rows(st, stats, wp.M)
+    print(f"aligned prefill: {pruned} of {wp.M} rows pruned, {int(stats[2])} candidates, "
+          f"{int(stats[3])} survivors, {int(stats[6])} group keys")
+    assert pruned >= 0.99 * wp.M
+    assert stats[2] > 0 and stats[3] > 0
+    assert stats[2] < 0.5 * (stats[0] - stats[1])      # the bound dropped most non-seed pairs
     assert B.device_error() == 0
 
 
@@ -86,12 +134,12 @@ def test_ragged_fp8_full(B):
     p = B.problem_to_device(wp)
     ids, sc = _topk(B, p, wp.K)
     u_ids, u_sc = ids.cpu().numpy(), sc.cpu().numpy()
-    for m in (0, 77, 127):
-        s_ref, a_ref = odsa.row_scores(wp, m)
-        check_topk_row(u_ids[m], u_sc[m], s_ref, a_ref, wp.K, EPS["fp8"])
+    _check_rows_pooled(wp, u_ids, u_sc, range(wp.M), EPS["fp8"])
     d_ids, d_sc, st, stats = _dosa(B, p, wp.K, n_seed=8192, retained_heads=20)
     assert np.array_equal(u_ids, d_ids)
     assert np.array_equal(u_sc.view(np.uint32), d_sc.view(np.uint32))
+    pruned = _pruned_rows(st, stats, wp.M)
+    print(f"ragged FP8: {pruned} of {wp.M} rows pruned, {int(stats[5])} skipped the scan")
     S = wp.extras["S"]
     t = torch.from_numpy(u_ids.copy()).cuda()
     B.witness_merge(t, p.key_len, wp.K - S, S, S)
