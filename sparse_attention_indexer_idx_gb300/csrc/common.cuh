@@ -127,18 +127,20 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // Bounded pipeline wait: returns false (and flags the CTA and the device) when
 // the phase did not complete within the unit's wait limit (g_wait_limit_ns,
 // 2 s unless the host set another) or another warp already aborted.
+// The limit is checked before every sleep, so a limit of 0 gives up at the
+// first wait whose phase is not already complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t limit = *(volatile uint64_t*)&g_wait_limit_ns;
-  uint64_t t0 = global_ns();
+  const uint64_t t0 = global_ns();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     if (*abort_flag) return false;
-    if (global_ns() - t0 > limit) {
+    if (global_ns() - t0 >= limit) {
       *abort_flag = 1;
       atomicOr(&g_device_error, DEVERR_WAIT_TIMEOUT);
       return false;
     }
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
   }
 }
 // Drain wait at the end of a kernel (copies and MMAs this thread issued that
