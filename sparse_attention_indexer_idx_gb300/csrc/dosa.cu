@@ -336,71 +336,121 @@ __device__ __forceinline__ float e4m3_to_f(uint8_t b) {
   return s ? -v : v;
 }
 
-// Rows row_of(i), i < n, of `base` (D values each: bf16, or e4m3 codes) into
-// dst[i * DP + d] as fp32, by the whole block: every thread issues up to four
-// 16-byte loads before it stores any, so the rows arrive in about one memory
-// latency rather than one per row and warp.
+// The planner's tiles: rows of D = 128 bf16 values, kPS elements apart (the
+// 8 extra elements put the 8 rows x 4 words of an mma fragment load in 32
+// different banks).
+constexpr int kPS = 136;
+
+// Rows row_of(i), i < n, of `base` (128 values each: bf16, or e4m3 codes --
+// which bf16 holds exactly) into dst[i * kPS + d] as bf16; rows n..n_pad-1 are
+// zero.  By the whole block: every thread issues up to four 16-byte loads
+// before it stores any, so the rows arrive in about one memory latency.
 template <class RowOf>
-__device__ void block_load_rows(const void* base, int dtype, int n, int D, float* dst, int DP, RowOf row_of) {
+__device__ void block_load_rows_bf16(const void* base, int dtype, int n, int n_pad, uint16_t* dst, RowOf row_of) {
   const int esz = dtype == IDX_FP8_E4M3 ? 1 : 2;
   const int per = 16 / esz;                 // values per 16-byte chunk
-  const int cpr = D / per;                  // chunks per row
-  const int total = n * cpr;
+  const int cpr = 128 / per;                // chunks per row
+  const int total = n_pad * cpr;
   for (int c0 = 0; c0 < total; c0 += 4 * kPlanThreads) {
     uint4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int c = c0 + u * kPlanThreads + threadIdx.x;
-      if (c < total) {
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < total && c / cpr < n) {
         const int64_t row = row_of(c / cpr);
-        v[u] = *reinterpret_cast<const uint4*>(static_cast<const char*>(base) + (row * D + (c % cpr) * per) * esz);
+        v[u] = *reinterpret_cast<const uint4*>(static_cast<const char*>(base) + (row * 128 + (c % cpr) * per) * esz);
       }
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int c = c0 + u * kPlanThreads + threadIdx.x;
       if (c >= total) continue;
-      float* o = dst + (c / cpr) * DP + (c % cpr) * per;
-      const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint16_t* o = dst + (c / cpr) * kPS + (c % cpr) * per;
       if (dtype == IDX_FP8_E4M3) {
+        const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t ow[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) o[e] = e4m3_to_f((uint8_t)(w4[e >> 2] >> (8 * (e & 3))));
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          o[2 * e] = bf16_to_f((uint16_t)(w4[e] & 0xffffu));
-          o[2 * e + 1] = bf16_to_f((uint16_t)(w4[e] >> 16));
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t lo = f_to_bf16_rn(e4m3_to_f((uint8_t)(w4[(2 * e) >> 2] >> (8 * ((2 * e) & 3)))));
+          const uint32_t hi = f_to_bf16_rn(e4m3_to_f((uint8_t)(w4[(2 * e + 1) >> 2] >> (8 * ((2 * e + 1) & 3)))));
+          ow[e] = lo | (hi << 16);
         }
+        reinterpret_cast<uint4*>(o)[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        reinterpret_cast<uint4*>(o)[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+      } else {
+        *reinterpret_cast<uint4*>(o) = v[u];
       }
     }
   }
 }
 
-// One thread block per query.  Shared memory: q [H][D+1] f32, sample keys
-// [ns][D+1] f32, and per-head scratch.
+// Two bf16 (elements col, col + 1 of a tile row; col even) as one word.
+__device__ __forceinline__ uint32_t tile_word(const uint16_t* t, int row, int col) {
+  return *reinterpret_cast<const uint32_t*>(t + row * kPS + col);
+}
+
+// d += A (16 x 16, rows of `a` from row a0) times B (16 x 8, B[k][n] = row
+// n of `b`, entry k; b_ok false: that column is zero), over D = 128 in eight
+// K steps, on the warp's tensor core (bf16 products are exact in the fp32
+// accumulator).  Fragment positions: lane = 4 g + t holds d[0], d[1] at row
+// g, columns 2t, 2t + 1 and d[2], d[3] at row g + 8.
+__device__ __forceinline__ void warp_mma_rows(float (&d)[4], const uint16_t* a, int a0, const uint16_t* brow,
+                                              bool b_ok) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int k0 = 0; k0 < 128; k0 += 16) {
+    const uint32_t x0 = tile_word(a, a0 + g, k0 + 2 * t), x1 = tile_word(a, a0 + g + 8, k0 + 2 * t);
+    const uint32_t x2 = tile_word(a, a0 + g, k0 + 2 * t + 8), x3 = tile_word(a, a0 + g + 8, k0 + 2 * t + 8);
+    const uint32_t y0 = b_ok ? *reinterpret_cast<const uint32_t*>(brow + k0 + 2 * t) : 0u;
+    const uint32_t y1 = b_ok ? *reinterpret_cast<const uint32_t*>(brow + k0 + 2 * t + 8) : 0u;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(x0), "r"(x1), "r"(x2), "r"(x3), "r"(y0), "r"(y1));
+  }
+}
+
+// Shared memory of the planner for H heads and n_sample samples.
+__host__ __device__ constexpr size_t plan_smem_bytes(int H, int n_sample) {
+  return (size_t)2 * kPS * ((size_t)H + (size_t)((n_sample + 15) / 16 * 16) + 32) +
+         (size_t)4 * ((size_t)H * 33 + 5 * (size_t)H + 128 + 32 + (size_t)((n_sample + 15) / 16 * 16) +
+                      3 * (size_t)H + 32 + 24);
+}
+
+// One thread block per query (8 warps).  The three small contractions of the
+// plan -- q_h . q_j for every head and retained head, q_h . k over the seed
+// samples, and the prepared vectors against the estimate keys -- run as warp
+// tensor-core tiles (mma.sync m16n8k16, bf16 in, fp32 out) over bf16 tiles in
+// shared memory; the rest is per head or per key.
 __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
-  extern __shared__ __align__(16) float pl[];
+  extern __shared__ __align__(16) uint8_t pl_raw[];
   const idx_problem& p = a.p;
   const int64_t m = blockIdx.x;
-  const int H = p.H, D = p.D, R = a.R;
-  float* q = pl;                       // H*D
-  // rows of q and of the sample keys are DP = D + 1 floats apart, so threads
-  // that walk different rows at the same d hit different banks
-  const int DP = D + 1;
-  float* ks = q + H * DP;              // n_sample rows
-  float* qn2 = ks + a.n_sample * DP;   // H: ||q_h||^2
-  float* beta = qn2 + H;               // H
-  float* dn = beta + H;                // H: ||d_h||
-  float* aggv = dn + H;                // D: a_A
-  int* anchor = (int*)(aggv + D);      // H
-  int* ret_pos = anchor + H;           // H: position among retained, -1 if omitted
-  int* act = ret_pos + H;              // H: activation counts
-  int* rlist = act + H;                // 32: retained heads ascending
-  float* wq = (float*)(rlist + 32);    // H: w_h (read many times below)
-  float* wfs = wq + H;                 // 32: folded weights, for the estimate
-  float* gram = wfs + 32;              // H x 32: q_h . q_j for the retained heads j
+  const int H = p.H, R = a.R;
+  constexpr int D = 128;
+  const int NSP = (a.n_sample + 15) / 16 * 16;   // sample rows (padded to whole tiles)
+  uint16_t* qs = reinterpret_cast<uint16_t*>(pl_raw);   // H rows: q_h
+  uint16_t* ks = qs + H * kPS;                   // NSP rows: seed samples, later the estimate keys
+  uint16_t* vs = ks + NSP * kPS;                 // 32 rows: the prepared vectors (retained, zero, a_A at 31)
+  float* gram = reinterpret_cast<float*>(vs + 32 * kPS);   // [H][33]: q_h . q_{rlist[r]}
+  float* qn2 = gram + H * 33;                    // H: ||q_h||^2
+  float* mag = qn2 + H;                          // H: |w_h| ||q_h||
+  float* beta = mag + H;                         // H
+  float* dn = beta + H;                          // H: ||d_h||
+  float* wq = dn + H;                            // H: w_h
+  float* aggv = wq + H;                          // D: a_A
+  float* wfs = aggv + D;                         // 32: folded weights
+  float* kn2 = wfs + 32;                         // NSP: ||k||^2 of the estimate keys
+  int* anchor = reinterpret_cast<int*>(kn2 + NSP);   // H
+  int* ret_pos = anchor + H;                     // H: position among retained, -1 if omitted
+  int* act = ret_pos + H;                        // H: activation counts
+  int* rlist = act + H;                          // 32: retained heads ascending
+  float* red = reinterpret_cast<float*>(rlist + 32);   // 2 x 8 partial sums, coef, pass count
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int nw = kPlanThreads / 32;
+  const int g = lane >> 2, t = lane & 3;
+  constexpr int nw = kPlanThreads / 32;
 
   float* wout = a.wfold + m * kVec;
   // prepared row r of this query (r < 31: vector r, 31: the aggregate; the group
@@ -409,8 +459,8 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   const int nvec = a.glayout ? 16 : kVec - 1;
   auto qrow = [&](int r) -> uint16_t* {
     if (!a.glayout) return a.qprep + (m * kVec + r) * D;
-    const int64_t g = m >> 3, qi = m & 7;
-    return a.qprep + (g * 144 + (r == 31 ? 128 + qi : (r == 32 ? 136 + qi : qi * 16 + r))) * D;
+    const int64_t gg = m >> 3, qi = m & 7;
+    return a.qprep + (gg * 144 + (r == 31 ? 128 + qi : (r == 32 ? 136 + qi : qi * 16 + r))) * D;
   };
   if (!a.active[m]) {
     for (int i = tid; i < (nvec + 2) * D; i += kPlanThreads) {
@@ -423,33 +473,42 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     if (tid == 0) a.coef[m] = 0.0f;
     return;
   }
-  const uint16_t* qsrc = (const uint16_t*)p.q + m * (int64_t)H * D;
-  for (int h = tid; h < H; h += kPlanThreads) wq[h] = p.w[m * H + h];
-  block_load_rows(p.q, IDX_BF16, H, D, q, DP, [&](int h) { return (int64_t)(m * H + h); });
+  for (int h = tid; h < H; h += kPlanThreads) {
+    wq[h] = p.w[m * H + h];
+    act[h] = 0;
+  }
+  block_load_rows_bf16(p.q, IDX_BF16, H, H, qs, [&](int h) { return (int64_t)(m * H + h); });
   // sample keys: seed[floor(i n / ns)], i < ns = min(n_sample, n)
   const int32_t* sl = a.seed_list + (a.shared_seeds ? 0 : m * a.list_ld);
   const int n = a.seed_cnt[a.shared_seeds ? 0 : m];
   const int ns = n < a.n_sample ? n : a.n_sample;
   const int64_t kbase = p.key_off ? p.key_off[m] : 0;
-  block_load_rows(p.keys, p.k_dtype, ns, D, ks, DP, [&](int si) {
+  block_load_rows_bf16(p.keys, p.k_dtype, ns, NSP, ks, [&](int si) {
     return kbase + (int64_t)sl[n <= a.n_sample ? si : (int)(((int64_t)si * n) / a.n_sample)];
   });
   __syncthreads();
-  // ||q_h||^2, one warp per head, fixed order
+  // ||q_h||^2 and |w_h| ||q_h||, one warp per head (lane: elements 4 lane .. 4 lane + 3)
   for (int h = wid; h < H; h += nw) {
+    const uint32_t w0 = tile_word(qs, h, 4 * lane), w1 = tile_word(qs, h, 4 * lane + 2);
+    const float x[4] = {bf16_to_f((uint16_t)w0), bf16_to_f((uint16_t)(w0 >> 16)), bf16_to_f((uint16_t)w1),
+                        bf16_to_f((uint16_t)(w1 >> 16))};
     float s = 0.0f;
-    for (int d = lane; d < D; d += 32) s = __fmaf_rn(q[h * DP + d], q[h * DP + d], s);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s = __fmaf_rn(x[e], x[e], s);
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) qn2[h] = s;
+    if (lane == 0) {
+      qn2[h] = s;
+      mag[h] = fabsf(wq[h]) * sqrtf(s);
+    }
   }
   __syncthreads();
   // retained heads: the R largest |w_h| ||q_h||, ties to the lower head
   for (int h = tid; h < H; h += kPlanThreads) {
-    const float mh = fabsf(wq[h]) * sqrtf(qn2[h]);
+    const float mh = mag[h];
     int rank = 0;
-    for (int g = 0; g < H; ++g) {
-      const float mg = fabsf(wq[g]) * sqrtf(qn2[g]);
-      rank += (mg > mh || (mg == mh && g < h)) ? 1 : 0;
+    for (int q = 0; q < H; ++q) {
+      const float mq = mag[q];
+      rank += (mq > mh || (mq == mh && q < h)) ? 1 : 0;
     }
     ret_pos[h] = rank < R ? 1 : -1;
   }
@@ -463,27 +522,60 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
       }
   }
   __syncthreads();
-  // anchors of the omitted positive heads (section 3.1): the dot products of
-  // every head with every retained head first, one thread per pair (d in order),
-  // then one warp per head picks its anchor and forms the residual norm
-  for (int t = tid; t < H * R; t += kPlanThreads) {
-    const int h = t / R, r = t - h * R;
-    const float* x = q + h * DP;
-    const float* y = q + rlist[r] * DP;
-    float dot = 0.0f;
-    for (int d = 0; d < D; ++d) dot = __fmaf_rn(x[d], y[d], dot);
-    gram[h * 32 + r] = dot;
+  // q_h . q_j for every head h and retained head j (section 3.1's beta needs them)
+  {
+    const int mt = H / 16, nt = (R + 7) / 8;
+    for (int tile = wid; tile < mt * nt; tile += nw) {
+      const int r0 = (tile / nt) * 16, c0 = (tile % nt) * 8;
+      const bool ok = c0 + g < R;
+      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      warp_mma_rows(d, qs, r0, qs + (ok ? rlist[c0 + g] : 0) * kPS, ok);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int col = c0 + 2 * t + j;
+        if (col < R) {
+          gram[(r0 + g) * 33 + col] = d[j];
+          gram[(r0 + g + 8) * 33 + col] = d[2 + j];
+        }
+      }
+    }
+  }
+  // activation counts of every head on the samples (section 3.2: "active" is
+  // q_h . k > 0; only the omitted negative heads' counts are used)
+  {
+    const int mt = H / 16, nt = NSP / 8;
+    for (int tile = wid; tile < mt * nt; tile += nw) {
+      const int r0 = (tile / nt) * 16, c0 = (tile % nt) * 8;
+      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      warp_mma_rows(d, qs, r0, ks + (c0 + g) * kPS, true);
+      int lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (c0 + 2 * t + j < ns) {
+          lo += d[j] > 0.0f ? 1 : 0;
+          hi += d[2 + j] > 0.0f ? 1 : 0;
+        }
+      }
+      lo += __shfl_xor_sync(0xffffffffu, lo, 1);
+      lo += __shfl_xor_sync(0xffffffffu, lo, 2);
+      hi += __shfl_xor_sync(0xffffffffu, hi, 1);
+      hi += __shfl_xor_sync(0xffffffffu, hi, 2);
+      if (t == 0) {
+        if (lo) atomicAdd(&act[r0 + g], lo);
+        if (hi) atomicAdd(&act[r0 + g + 8], hi);
+      }
+    }
   }
   __syncthreads();
-  for (int h = wid; h < H; h += nw) {
-    const float wh = wq[h];
+  // anchors of the omitted positive heads: the retained j with the smallest
+  // ||q_h - beta q_j||^2 = ||q_h||^2 - 2 beta q_h.q_j + beta^2 ||q_j||^2, ties to the lower j
+  for (int h = tid; h < H; h += kPlanThreads) {
     int bj = -1;
-    float bb = 0.0f, dnh = 0.0f;
-    if (ret_pos[h] < 0 && wh > 0.0f) {
-      float best = 0.0f;
+    float bb = 0.0f, best = 0.0f;
+    if (ret_pos[h] < 0 && wq[h] > 0.0f) {
       for (int r = 0; r < R; ++r) {
         const int j = rlist[r];
-        const float dot = gram[h * 32 + r];
+        const float dot = gram[h * 33 + r];
         const float b = qn2[j] > 0.0f ? fmaxf(0.0f, dot / qn2[j]) : 0.0f;
         const float r2 = qn2[h] - 2.0f * b * dot + b * b * qn2[j];
         if (bj < 0 || r2 < best) {
@@ -492,61 +584,55 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
           bb = b;
         }
       }
-      // residual norm of the chosen decomposition, computed directly and rounded up
+    }
+    anchor[h] = bj;
+    beta[h] = bb;
+  }
+  __syncthreads();
+  // residual norm of the chosen decomposition, computed directly and rounded up
+  for (int h = wid; h < H; h += nw) {
+    float dnh = 0.0f;
+    const int j = anchor[h];
+    if (j >= 0) {
+      const float bb = beta[h];
       float sres = 0.0f;
-      for (int d = lane; d < D; d += 32) {
-        const float x = q[h * DP + d] - bb * q[bj * DP + d];
-        sres = __fmaf_rn(x, x, sres);
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        const uint32_t wh = tile_word(qs, h, 4 * lane + e), wj = tile_word(qs, j, 4 * lane + e);
+        const float x0 = __fmaf_rn(-bb, bf16_to_f((uint16_t)wj), bf16_to_f((uint16_t)wh));
+        const float x1 = __fmaf_rn(-bb, bf16_to_f((uint16_t)(wj >> 16)), bf16_to_f((uint16_t)(wh >> 16)));
+        sres = __fmaf_rn(x0, x0, sres);
+        sres = __fmaf_rn(x1, x1, sres);
       }
       for (int o = 16; o > 0; o >>= 1) sres += __shfl_xor_sync(0xffffffffu, sres, o);
       dnh = __fsqrt_ru(sres) * (1.0f + 1.0e-6f);
     }
-    if (lane == 0) {
-      anchor[h] = bj;
-      beta[h] = bb;
-      dn[h] = dnh;
-    }
+    if (lane == 0) dn[h] = dnh;
   }
-  // activation counts of the omitted negative heads on the samples (section
-  // 3.2): one whole dot product per thread and task (head, sample); the lanes of
-  // a warp share the head and walk different sample rows
-  for (int h = tid; h < H; h += kPlanThreads) act[h] = 0;
-  __syncthreads();
-  // (a thread takes samples sq, sq + NSQ, sq + 2 NSQ, sq + 3 NSQ of one head, so
-  // every q value it loads serves four dot products)
-  const int NSQ = (ns + 3) / 4;
-  for (int t = tid; t < H * NSQ; t += kPlanThreads) {
-    const int h = t / NSQ, sq = t % NSQ;
-    const float wh = wq[h];
-    if (!(ret_pos[h] < 0 && wh < 0.0f)) continue;
-    const float* x = q + h * DP;
-    int rows[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) rows[j] = sq + j * NSQ < ns ? sq + j * NSQ : sq;
-    float dot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int d = 0; d < D; ++d) {
-      const float xd = x[d];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) dot[j] = __fmaf_rn(xd, ks[rows[j] * DP + d], dot[j]);
-    }
-    int c = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) c += (sq + j * NSQ < ns && dot[j] > 0.0f) ? 1 : 0;
-    if (c) atomicAdd(&act[h], c);
-  }
-  __syncthreads();
-  // aggregate a_A = sum_{h in A} |w_h| q_h, prepared rows, folded weights
+  // aggregate a_A = sum_{h in A} |w_h| q_h (heads in order), prepared rows
   const float need_act = a.act_min * (float)ns;
   for (int d = tid; d < D; d += kPlanThreads) {
-    float s = 0.0f;
+    float sa = 0.0f;
     for (int h = 0; h < H; ++h) {
       const float wh = wq[h];
-      if (ret_pos[h] < 0 && wh < 0.0f && ns > 0 && (float)act[h] >= need_act) s = __fmaf_rn(-wh, q[h * DP + d], s);
+      if (ret_pos[h] < 0 && wh < 0.0f && ns > 0 && (float)act[h] >= need_act)
+        sa = __fmaf_rn(-wh, bf16_to_f(qs[h * kPS + d]), sa);
     }
-    aggv[d] = s;
-    qrow(31)[d] = f_to_bf16_rn(s);
+    aggv[d] = sa;
+    const uint16_t ab = f_to_bf16_rn(sa);
+    qrow(31)[d] = ab;
+    vs[31 * kPS + d] = ab;
     if (a.glayout) qrow(32)[d] = 0;
   }
+  for (int i = tid; i < nvec * D; i += kPlanThreads) {
+    const int r = i / D, d = i % D;
+    qrow(r)[d] = r < R ? qs[rlist[r] * kPS + d] : (uint16_t)0;
+  }
+  for (int i = tid; i < 31 * D; i += kPlanThreads) {
+    const int r = i / D, d = i % D;
+    vs[r * kPS + d] = r < R ? qs[rlist[r] * kPS + d] : (uint16_t)0;
+  }
+  __syncthreads();   // dn complete
   for (int h = tid; h < H; h += kPlanThreads) {
     const float wh = wq[h];
     int code = -1;
@@ -556,10 +642,6 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     a.plan_head[m * H + h] = code;
     a.plan_beta[m * H + h] = beta[h];
     a.plan_dn[m * H + h] = dn[h];
-  }
-  for (int i = tid; i < nvec * D; i += kPlanThreads) {
-    const int r = i / D, d = i % D;
-    qrow(r)[d] = r < R ? qsrc[rlist[r] * D + d] : (uint16_t)0;
   }
   for (int r = tid; r < kVec; r += kPlanThreads) {
     float wf = 0.0f;
@@ -572,7 +654,6 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     wout[r] = wf;
     wfs[r] = wf;
   }
-  __syncthreads();
   // margin: bf16 rounding distance of a_A, plus gamma * (sum |w_h| ||q_h|| + ||a_A||)
   float e2 = 0.0f, a2 = 0.0f;
   for (int d = tid; d < D; d += kPlanThreads) {
@@ -584,17 +665,16 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     e2 += __shfl_xor_sync(0xffffffffu, e2, o);
     a2 += __shfl_xor_sync(0xffffffffu, a2, o);
   }
-  __shared__ float e2s[kPlanThreads / 32], a2s[kPlanThreads / 32];
   if (lane == 0) {
-    e2s[wid] = e2;
-    a2s[wid] = a2;
+    red[wid] = e2;
+    red[nw + wid] = a2;
   }
   __syncthreads();
   if (tid == 0) {
     float E2 = 0.0f, A2 = 0.0f;
     for (int w = 0; w < nw; ++w) {
-      E2 += e2s[w];
-      A2 += a2s[w];
+      E2 += red[w];
+      A2 += red[nw + w];
     }
     float c = 0.0f, W = 0.0f;
     for (int h = 0; h < H; ++h) {
@@ -614,64 +694,92 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
         qmax = fmaxf(qmax, sqrtf(qn2[h]));
         sw += fabsf(wq[h]);
       }
-      for (int r = 0; r < kVec; ++r) swf += fabsf(wout[r]);
+      for (int r = 0; r < kVec; ++r) swf += fabsf(wfs[r]);
       const float vmax = fmaxf(qmax, sqrtf(A2) * 1.01f + sqrtf(E2) * 1.01f);
       margin += 2.0f * sqrtf((float)D) * 7.62939453125e-6f * (sw * qmax + swf * vmax);
     }
     a.coef[m] = (c + margin) * (1.0f + 1.0e-6f);
-    e2s[0] = (c + margin) * (1.0f + 1.0e-6f);   // coef, for the estimate below
+    red[2 * nw] = (c + margin) * (1.0f + 1.0e-6f);   // coef, for the estimate below
+    reinterpret_cast<int*>(red)[2 * nw + 1] = 0;     // the estimate's pass count
   }
-  // Overflow estimate: the bound U of n_sample evenly spaced visible keys of the row
-  // against tau.  A row whose candidates would clearly exceed the capacity
-  // skips the bound scan and is computed on the unpruned path (as an
-  // overflowing row would be); the output is the same either way.
+  // Overflow estimate: the bound U of n_sample evenly spaced visible keys of the
+  // row against tau, from the same bf16 vectors the bound scan multiplies.  A
+  // row whose candidates would clearly exceed the capacity skips the bound scan
+  // and is computed on the unpruned path (as an overflowing row would be); the
+  // output is the same either way.
   __syncthreads();
-  const float coef = e2s[0];
+  const float coef = red[2 * nw];
   int64_t off;
   int len;
   row_extent(p, m, &off, &len);
   const int ne = len < a.n_sample ? len : a.n_sample;   // the sample area holds n_sample keys
   if (ne <= 0) return;
-  block_load_rows(p.keys, p.k_dtype, ne, D, ks, DP, [&](int si) { return off + ((int64_t)si * len) / ne; });
+  const int NEP = (ne + 15) / 16 * 16;
+  block_load_rows_bf16(p.keys, p.k_dtype, ne, NEP, ks, [&](int si) { return off + ((int64_t)si * len) / ne; });
   __syncthreads();
-  const float t = a.tau[m];
-  // U of every estimate key, two threads per key (ne <= n_sample <= 128): one
-  // takes the first half of the retained vectors and the aggregate, the other
-  // the second half and ||k|| (an estimate: the split sum rounds differently)
-  int pass = 0;
-  {
-    const int si = tid >> 1, half = tid & 1;
-    float part = 0.0f, dx = 0.0f;
-    if (si < ne) {
-      const float* k = ks + si * DP;
-      const int r0 = half ? R / 2 : 0, r1 = half ? R : R / 2;
-      for (int r = r0; r < r1; ++r) {
-        const float* x = q + rlist[r] * DP;
-        float dot = 0.0f;
-        for (int d = 0; d < D; ++d) dot = __fmaf_rn(x[d], k[d], dot);
-        part = __fmaf_rn(wfs[r], fmaxf(dot, 0.0f), part);
-      }
-      if (half == 0)
-        for (int d = 0; d < D; ++d) dx = __fmaf_rn(aggv[d], k[d], dx);   // a_A . k
-      else
-        for (int d = 0; d < D; ++d) dx = __fmaf_rn(k[d], k[d], dx);      // ||k||^2
+  for (int k = tid; k < ne; k += kPlanThreads) {
+    float s2 = 0.0f;
+    for (int c = 0; c < D; c += 2) {
+      const uint32_t w = tile_word(ks, k, c);
+      const float x0 = bf16_to_f((uint16_t)w), x1 = bf16_to_f((uint16_t)(w >> 16));
+      s2 = __fmaf_rn(x0, x0, s2);
+      s2 = __fmaf_rn(x1, x1, s2);
     }
-    const float part_o = __shfl_xor_sync(0xffffffffu, part, 1);
-    const float dx_o = __shfl_xor_sync(0xffffffffu, dx, 1);
-    if (si < ne && half == 0) {
-      float u = part + part_o;
-      u = u - fmaxf(dx, 0.0f);
-      u = __fmaf_rn(coef, sqrtf(dx_o), u);
-      if (p.k_dtype == IDX_FP8_E4M3) u *= p.key_scale[off + ((int64_t)si * len) / ne];
-      pass = u >= t ? 1 : 0;
+    kn2[k] = s2;
+  }
+  __syncthreads();
+  const float tau = a.tau[m];
+  int pass = 0;
+  if (wid * 16 < NEP) {
+    // this warp's 16 keys against the 32 prepared vectors (four n-tiles)
+    float acc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[nt][j] = 0.0f;
+      warp_mma_rows(acc[nt], ks, wid * 16, vs + (nt * 8 + g) * kPS, true);
+    }
+    float plo = 0.0f, phi = 0.0f, alo = 0.0f, ahi = 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int col = nt * 8 + 2 * t + j;
+        if (col < R) {
+          plo = __fmaf_rn(wfs[col], fmaxf(acc[nt][j], 0.0f), plo);
+          phi = __fmaf_rn(wfs[col], fmaxf(acc[nt][2 + j], 0.0f), phi);
+        }
+        if (col == 31) {
+          alo = acc[nt][j];
+          ahi = acc[nt][2 + j];
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      plo += __shfl_xor_sync(0xffffffffu, plo, o);
+      phi += __shfl_xor_sync(0xffffffffu, phi, o);
+      alo += __shfl_xor_sync(0xffffffffu, alo, o);
+      ahi += __shfl_xor_sync(0xffffffffu, ahi, o);
+    }
+    if (t == 0) {
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int k = wid * 16 + g + 8 * hlf;
+        if (k < ne) {
+          float u = (hlf ? phi : plo) - fmaxf(hlf ? ahi : alo, 0.0f);
+          u = __fmaf_rn(coef, sqrtf(kn2[k]), u);
+          if (p.k_dtype == IDX_FP8_E4M3) u *= p.key_scale[off + ((int64_t)k * len) / ne];
+          pass += u >= tau ? 1 : 0;
+        }
+      }
     }
   }
   for (int o = 16; o > 0; o >>= 1) pass += __shfl_xor_sync(0xffffffffu, pass, o);
-  if (lane == 0) act[wid] = pass;   // the activation counts are no longer needed
+  if (lane == 0 && pass) atomicAdd(reinterpret_cast<int*>(red) + 2 * nw + 1, pass);
   __syncthreads();
   if (tid == 0) {
-    int total = 0;
-    for (int w = 0; w < nw; ++w) total += act[w];
+    const int total = reinterpret_cast<int*>(red)[2 * nw + 1];
     const float nonseed = (float)(len - (n < len ? n : len));
     if ((float)total / (float)ne * nonseed > 1.25f * (float)a.cap) {
       a.active[m] = 0;
@@ -1284,8 +1392,7 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
   pa.plan_head = w.plan_head;
   pa.plan_beta = w.plan_beta;
   pa.plan_dn = w.plan_dn;
-  const size_t psmem = ((size_t)p.H * (p.D + 1) + (size_t)dp.n_sample * (p.D + 1) + 4 * (size_t)p.H + p.D) * sizeof(float) +
-                       (3 * (size_t)p.H + 32) * sizeof(int) + ((size_t)p.H + 32 + (size_t)p.H * 32) * sizeof(float);
+  const size_t psmem = plan_smem_bytes(p.H, dp.n_sample);
   DOSA_CHECK(cudaFuncSetAttribute(dosa_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem));
   dosa_plan_kernel<<<(unsigned)M, kPlanThreads, psmem, st>>>(pa);
   DOSA_CHECK(cudaGetLastError());

@@ -599,6 +599,429 @@ __global__ void __launch_bounds__(TK_NT, 1)
   emit(order_desc(sh, sh.cand, want, P, best), want);
 }
 
+// ------------------------------------------------- many long rows, fused --
+// When there are at least two rows per SM and the rows are long (the causal
+// prefill: 4096 rows of up to 65536 scores; DoSA's seed and merge rows), one
+// thread block of 512 threads per row does both passes, two blocks per SM so
+// that one block's scan overlaps the other's sort: the row threshold once
+// (the filter's rule, from 1024 evenly spaced samples), one coalesced stream
+// over the row that collects the keys >= T in shared memory (a per-warp
+// reservation, no global slots), then the same bucket sort and rank placement
+// as the finish pass over those candidates, and the first min(K, n) written.
+// Heavy ties take the two radix selects and a bitonic sort; a threshold that
+// missed (fewer than min(K, n) candidates, or more than the candidate space)
+// takes the exact radix select over the row's scores.  The output is the
+// same as the two-pass path's (the exact top-K under (score desc, id asc)).
+constexpr int TR_NT = 512;
+constexpr int TR_NW = TR_NT / 32;
+constexpr int TR_CAP = 7168;                // candidates a row may collect
+constexpr int TR_KMAX = 2048;               // largest K this kernel takes
+constexpr uint32_t kTrBucketMax = 256;      // a larger bucket: heavy ties
+constexpr int TR_DST = TR_KMAX + 256;       // scatter space: the first K places plus one bucket
+constexpr int TR_NB = 4096;                 // buckets of the sort
+constexpr int TR_V = 8;                     // 4-score vectors per thread and round (loads in flight)
+constexpr int TR_NS = 1024;                 // threshold samples
+
+struct TrShared {
+  uint64_t cand[TR_CAP];
+  uint64_t dst[TR_DST];
+  union {
+    struct {
+      uint32_t cur[TR_NB];                  // count, then scatter cursor, per bucket
+      uint32_t start[TR_NB];                // first slot per bucket
+    } b;
+    uint32_t hist[kTopkBins];               // radix histograms (never live with the buckets)
+  } u;
+  uint32_t red[TR_NW];
+  uint32_t found_bin, found_above;
+  uint32_t kmin, kmax, bmax, kend, ncand;
+};
+
+// Exclusive prefix sum over the block in thread order; *total = block sum.
+__device__ __forceinline__ uint32_t tr_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  __syncthreads();
+  if (lane == 31) red[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t x = lane < TR_NW ? red[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += u;
+    }
+    if (lane < TR_NW) red[lane] = x;
+  }
+  __syncthreads();
+  *total = red[TR_NW - 1];
+  return (wid ? red[wid - 1] : 0u) + incl - v;
+}
+
+// Suffix search over u.hist[0..nb) (bins high to low): the bin b with
+// (#in bins > b) < remaining <= (#in bins >= b) -> found_bin / found_above.
+__device__ __forceinline__ void tr_suffix_find(TrShared& sh, int nb, uint32_t remaining) {
+  constexpr int PER = kTopkBins / TR_NT;
+  uint32_t loc[PER], sum = 0;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int bin = nb - 1 - (threadIdx.x * PER + q);
+    loc[q] = bin >= 0 ? sh.u.hist[bin] : 0u;
+    sum += loc[q];
+  }
+  uint32_t total;
+  uint32_t run = tr_excl_scan(sum, sh.red, &total);
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int bin = nb - 1 - (threadIdx.x * PER + q);
+    if (bin >= 0 && run < remaining && run + loc[q] >= remaining) {
+      sh.found_bin = (uint32_t)bin;
+      sh.found_above = run;
+    }
+    run += loc[q];
+  }
+  __syncthreads();
+}
+
+// The filter's row threshold (n > K), once per row: 1024 samples i n / 1024.
+__device__ uint32_t tr_threshold(TrShared& sh, const float* row, int n, int K) {
+  const int tid = threadIdx.x;
+  uint32_t sv[TR_NS / TR_NT];
+#pragma unroll
+  for (int j = 0; j < TR_NS / TR_NT; ++j)
+    sv[j] = score_key(__ldg(row + (int)(((int64_t)(tid + j * TR_NT) * n) / TR_NS)));
+  const float expect = (float)TR_NS * (float)K / (float)n;
+  int r = (int)ceilf(1.15f * expect + 3.5f * sqrtf(expect)) + 1;
+  r = r < 1 ? 1 : (r > TR_NS ? TR_NS : r);
+  for (int b = tid; b < kTopkBins; b += TR_NT) sh.u.hist[b] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < TR_NS / TR_NT; ++j) atomicAdd(&sh.u.hist[sv[j] >> 21], 1u);
+  __syncthreads();
+  tr_suffix_find(sh, kTopkBins, (uint32_t)r);
+  const uint32_t b1 = sh.found_bin, a1 = sh.found_above;
+  __syncthreads();
+  for (int b = tid; b < kTopkBins; b += TR_NT) sh.u.hist[b] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < TR_NS / TR_NT; ++j)
+    if ((sv[j] >> 21) == b1) atomicAdd(&sh.u.hist[(sv[j] >> 10) & 0x7ffu], 1u);
+  __syncthreads();
+  tr_suffix_find(sh, kTopkBins, (uint32_t)r - a1);
+  const uint32_t T = (b1 << 21) | (sh.found_bin << 10);
+  __syncthreads();
+  return T ? T : 1u;
+}
+
+// Exact radix select over cn elements: the want-th largest f(i) among the
+// flagged ones (11 + 11 + 10 bits); *eq_out = how many flagged equal it.
+template <class F, class Flag>
+__device__ uint32_t tr_radix_select(TrShared& sh, int cn, uint32_t want, F f, Flag flag, uint32_t* above_out,
+                                    uint32_t* eq_out) {
+  uint32_t prefix = 0, mask = 0, remaining = want, eq = 0;
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const uint32_t dmask = pass == 2 ? 0x3ffu : 0x7ffu;
+    for (int b = threadIdx.x; b < kTopkBins; b += TR_NT) sh.u.hist[b] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < cn; i += TR_NT) {
+      if (flag(i)) {
+        const uint32_t k = f(i);
+        if ((k & mask) == prefix) atomicAdd(&sh.u.hist[(k >> shift) & dmask], 1u);
+      }
+    }
+    __syncthreads();
+    tr_suffix_find(sh, (int)dmask + 1, remaining);
+    remaining -= sh.found_above;
+    eq = sh.u.hist[sh.found_bin];
+    prefix |= sh.found_bin << shift;
+    mask |= dmask << shift;
+    __syncthreads();
+  }
+  *above_out = want - remaining;
+  *eq_out = eq;
+  return prefix;
+}
+
+// Sorts the first `limit` places of the n nonzero, distinct composites src
+// descending (the finish pass's bucket sort, 4096 buckets): src[0, limit) ends
+// up in order.  dst takes the scattered elements (at most limit + 255).
+// Returns false, src untouched, when a bucket holds more than kTrBucketMax.
+__device__ bool tr_bucket_sort(TrShared& sh, uint64_t* src, int n, uint64_t* dst, int limit) {
+  const int tid = threadIdx.x;
+  uint32_t* bh = sh.u.b.cur;
+  uint32_t* bs = sh.u.b.start;
+  constexpr int PER = TR_NB / TR_NT;
+  static_assert(PER == 8, "two 16-byte vectors per thread");
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  reinterpret_cast<uint4*>(bh)[2 * tid] = z;
+  reinterpret_cast<uint4*>(bh)[2 * tid + 1] = z;
+  if (tid == 0) {
+    sh.kmin = 0xffffffffu;
+    sh.kmax = 0u;
+    sh.bmax = 0u;
+    sh.kend = (uint32_t)n;
+  }
+  __syncthreads();
+  uint32_t mn = 0xffffffffu, mx = 0u;
+  for (int i = tid; i < n; i += TR_NT) {
+    const uint32_t k = (uint32_t)(src[i] >> 32);
+    mn = min(mn, k);
+    mx = max(mx, k);
+  }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if ((tid & 31) == 0) {
+    atomicMin(&sh.kmin, mn);
+    atomicMax(&sh.kmax, mx);
+  }
+  __syncthreads();
+  const uint32_t kmin = sh.kmin;
+  const float scale = (float)TR_NB / ((float)(sh.kmax - kmin) + 1.0f);
+  auto bucket = [&](uint64_t v) {
+    uint32_t b = (uint32_t)((float)((uint32_t)(v >> 32) - kmin) * scale);
+    b = b < (uint32_t)TR_NB ? b : (uint32_t)TR_NB - 1u;
+    return (uint32_t)TR_NB - 1u - b;   // largest keys first
+  };
+  for (int i = tid; i < n; i += TR_NT) atomicAdd(&bh[bucket(src[i])], 1u);
+  __syncthreads();
+  const uint4 c0 = reinterpret_cast<const uint4*>(bh)[2 * tid];
+  const uint4 c1 = reinterpret_cast<const uint4*>(bh)[2 * tid + 1];
+  const uint32_t cnt8[PER] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  uint32_t sum = 0, big = 0;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    sum += cnt8[q];
+    big = max(big, cnt8[q]);
+  }
+  uint32_t total;
+  uint32_t run = tr_excl_scan(sum, sh.red, &total);
+  big = __reduce_max_sync(0xffffffffu, big);
+  if ((tid & 31) == 0) atomicMax(&sh.bmax, big);
+  const uint32_t lim = (uint32_t)(limit < n ? limit : n);
+  uint32_t st8[PER], kend = 0xffffffffu;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    st8[q] = run;
+    if (run >= lim && cnt8[q]) kend = min(kend, run);   // first bucket left out
+    run += cnt8[q];
+  }
+  kend = __reduce_min_sync(0xffffffffu, kend);
+  if ((tid & 31) == 0 && kend != 0xffffffffu) atomicMin(&sh.kend, kend);
+  reinterpret_cast<uint4*>(bs)[2 * tid] = make_uint4(st8[0], st8[1], st8[2], st8[3]);
+  reinterpret_cast<uint4*>(bs)[2 * tid + 1] = make_uint4(st8[4], st8[5], st8[6], st8[7]);
+  reinterpret_cast<uint4*>(bh)[2 * tid] = make_uint4(st8[0], st8[1], st8[2], st8[3]);   // scatter cursors
+  reinterpret_cast<uint4*>(bh)[2 * tid + 1] = make_uint4(st8[4], st8[5], st8[6], st8[7]);
+  __syncthreads();
+  if (sh.bmax > kTrBucketMax) return false;
+  for (int i = tid; i < n; i += TR_NT) {
+    const uint64_t v = src[i];
+    const uint32_t b = bucket(v);
+    if (bs[b] >= lim) continue;
+    const uint32_t pos = atomicAdd(&bh[b], 1u);
+    dst[pos] = v;
+  }
+  __syncthreads();
+  const int used = (int)sh.kend;
+  for (int i = tid; i < used; i += TR_NT) {
+    const uint64_t v = dst[i];
+    const uint32_t b = bucket(v);
+    const int b0 = (int)bs[b], b1 = (int)bh[b];
+    int r = b0;
+    for (int q = b0; q < b1; ++q) r += dst[q] > v ? 1 : 0;
+    src[r] = v;
+  }
+  __syncthreads();
+  return true;
+}
+
+// Bitonic sort of buf[0..S) descending (S a power of two).
+__device__ void tr_bitonic_desc(uint64_t* v, int S) {
+  for (int size = 2; size <= S; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = threadIdx.x; t < (S >> 1); t += TR_NT) {
+        const int lo = 2 * t - (t & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = ((lo & size) == 0);
+        const uint64_t a = v[lo], b = v[hi];
+        if ((a < b) == desc) {
+          v[lo] = b;
+          v[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// The `want` largest of the n composites src[0..n) (want <= n), sorted, in
+// src[0..want) or dst[0..want): returns where.  Bucket sort, else (heavy ties)
+// two radix selects cut exactly `want` into dst and a bitonic sort orders them.
+__device__ const uint64_t* tr_order_top(TrShared& sh, uint64_t* src, int n, int want, int P, uint64_t* dst) {
+  if (n <= 1) return src;
+  if (tr_bucket_sort(sh, src, n, dst, want)) return src;
+  int c = n;
+  if (n > want) {
+    uint32_t above, eq;
+    auto hi = [&](int i) { return (uint32_t)(src[i] >> 32); };
+    auto real = [&](int i) { return src[i] != 0ull; };
+    const uint32_t KT = tr_radix_select(sh, n, (uint32_t)want, hi, real, &above, &eq);
+    const uint32_t need = (uint32_t)want - above;
+    uint32_t IT = 0;
+    if (eq != need) {
+      auto lo = [&](int i) { return (uint32_t)src[i]; };
+      auto tie = [&](int i) { return src[i] != 0ull && (uint32_t)(src[i] >> 32) == KT; };
+      uint32_t above2, eq2;
+      IT = tr_radix_select(sh, n, need, lo, tie, &above2, &eq2);
+    }
+    auto take = [&](int i) {
+      const uint64_t v = src[i];
+      const uint32_t k = (uint32_t)(v >> 32);
+      return v != 0ull && (k > KT || (k == KT && (uint32_t)v >= IT));
+    };
+    uint32_t local = 0;
+    for (int i = threadIdx.x; i < n; i += TR_NT) local += take(i) ? 1u : 0u;
+    uint32_t total;
+    uint32_t off = tr_excl_scan(local, sh.red, &total);
+    for (int i = threadIdx.x; i < n; i += TR_NT)
+      if (take(i)) dst[off++] = src[i];
+    c = want;
+  } else {
+    for (int i = threadIdx.x; i < n; i += TR_NT) dst[i] = src[i];
+  }
+  for (int i = c + threadIdx.x; i < P; i += TR_NT) dst[i] = 0ull;
+  __syncthreads();
+  tr_bitonic_desc(dst, P);
+  return dst;
+}
+
+__global__ void __launch_bounds__(TR_NT, 2)
+    topk_rows_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ lens, idx_problem p,
+                     int use_p, int max_len, int K, int P, const int32_t* __restrict__ id_map, int64_t id_ld,
+                     const int32_t* __restrict__ row_mask, int32_t* __restrict__ out_ids,
+                     float* __restrict__ out_scores, int vec4) {
+  extern __shared__ __align__(16) uint8_t tr_smem[];
+  TrShared& sh = *reinterpret_cast<TrShared*>(tr_smem);
+  const int64_t m = blockIdx.x;
+  if (row_mask && !row_mask[m]) return;
+  const int n = row_length(lens, p, use_p, max_len, m);
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int want = n < K ? n : K;
+  auto emit = [&](const uint64_t* sorted, int have) {
+    for (int j = tid; j < K; j += TR_NT) {
+      const uint64_t v = j < have ? sorted[j] : 0ull;
+      out_ids[m * K + j] = v ? key_id((uint32_t)v) : -1;
+      if (out_scores) out_scores[m * K + j] = v ? key_score((uint32_t)(v >> 32)) : -__int_as_float(0x7f800000);
+    }
+  };
+  if (want <= 0) {
+    emit(nullptr, 0);
+    return;
+  }
+  const float* row = scores + m * ld;
+  const int32_t* idm = id_map ? id_map + m * id_ld : nullptr;
+  auto idof = [&](int i) { return idm ? idm[i] : (int32_t)i; };
+  // every visible key when the row has at most K of them (ordered keys are >= 1)
+  const uint32_t T = n <= K ? 1u : tr_threshold(sh, row, n, K);
+  if (tid == 0) sh.ncand = 0;
+  __syncthreads();
+  // one stream over the row: keys >= T into the candidate space, one
+  // reservation per warp and round; thread tid reads the four scores at
+  // c0 + 4 (v TR_NT + tid) .. + 3 (one 16-byte load when the rows allow it:
+  // ld a multiple of 4 and an aligned base, checked by the host)
+#pragma unroll 1
+  for (int c0 = 0; c0 < n; c0 += TR_NT * 4 * TR_V) {
+    uint32_t kv[4 * TR_V];
+#pragma unroll
+    for (int v = 0; v < TR_V; ++v) {
+      const int i0 = c0 + 4 * (v * TR_NT + tid);
+      float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (i0 < n) {
+        if (vec4) {
+          // i0 < n <= ld and ld % 4 == 0, so the vector lies inside the row's storage
+          const float4 f = __ldg(reinterpret_cast<const float4*>(row + i0));
+          x[0] = f.x;
+          x[1] = f.y;
+          x[2] = f.z;
+          x[3] = f.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (i0 + e < n) x[e] = __ldg(row + i0 + e);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) kv[4 * v + e] = i0 + e < n ? score_key(x[e]) : 0u;
+    }
+    uint32_t c = 0;
+#pragma unroll
+    for (int u = 0; u < 4 * TR_V; ++u) c += kv[u] >= T ? 1u : 0u;
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t base = 0;
+    if (wtot) {
+      if (lane == 31) base = atomicAdd(&sh.ncand, wtot);
+      base = __shfl_sync(0xffffffffu, base, 31);
+    }
+    uint32_t pos = base + incl - c;
+#pragma unroll
+    for (int u = 0; u < 4 * TR_V; ++u) {
+      if (kv[u] >= T) {
+        if (pos < (uint32_t)TR_CAP) sh.cand[pos] = composite(kv[u], idof(c0 + 4 * ((u >> 2) * TR_NT + tid) + (u & 3)));
+        ++pos;
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t total = sh.ncand;
+  if (total >= (uint32_t)want && total <= (uint32_t)TR_CAP) {
+    emit(tr_order_top(sh, sh.cand, (int)total, want, P, sh.dst), want);
+    return;
+  }
+  // the threshold missed: exact radix select over the row's scores
+  auto key_f = [&](int i) { return score_key(__ldg(row + i)); };
+  auto all = [&](int) { return true; };
+  uint32_t above, eq;
+  const uint32_t KT = tr_radix_select(sh, n, (uint32_t)want, key_f, all, &above, &eq);
+  const uint32_t need = (uint32_t)want - above;
+  uint32_t IT = 0;
+  if (eq != need) {
+    auto tie = [&](int i) { return key_f(i) == KT; };
+    auto idk = [&](int i) { return id_key(idof(i)); };
+    uint32_t above2, eq2;
+    IT = tr_radix_select(sh, n, need, idk, tie, &above2, &eq2);
+  }
+  auto take = [&](int i) {
+    const uint32_t kk = key_f(i);
+    return kk > KT || (kk == KT && id_key(idof(i)) >= IT);
+  };
+  uint32_t local = 0;
+  for (int i = tid; i < n; i += TR_NT) local += take(i) ? 1u : 0u;
+  uint32_t tot2;
+  uint32_t off = tr_excl_scan(local, sh.red, &tot2);
+  for (int i = tid; i < n; i += TR_NT)
+    if (take(i)) sh.cand[off++] = composite(key_f(i), idof(i));
+  __syncthreads();
+  emit(tr_order_top(sh, sh.cand, want, want, P, sh.dst), want);
+}
+
+// The fused kernel takes a launch when the rows are long, there are at least
+// two per SM and K fits its sort space.
+static bool topk_rows_applies(int64_t M, int max_len, int K) {
+  return K <= TR_KMAX && max_len > 4096 && M >= 2 * (int64_t)sm_count();
+}
+
 static int pow2_at_least(int x) {
   int p = 1;
   while (p < x) p <<= 1;
@@ -623,6 +1046,18 @@ cudaError_t launch_topk_dense(const float* scores, int64_t ld, const int32_t* le
                               cudaStream_t st, const int32_t* id_map, int64_t id_ld, const int32_t* row_mask) {
   if (M <= 0) return cudaSuccess;
   const int P = pow2_at_least(K);
+  if (topk_rows_applies(M, max_len, K)) {
+    if (M > 0x7fffffff) return cudaErrorInvalidValue;
+    idx_problem p{};
+    if (p_or_null) p = *p_or_null;
+    const size_t smem = sizeof(TrShared);
+    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int vec4 = (ld % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0) ? 1 : 0;
+    topk_rows_kernel<<<(unsigned)M, TR_NT, smem, st>>>(scores, ld, lens, p, p_or_null ? 1 : 0, max_len, K, P, id_map,
+                                                       id_ld, row_mask, out_ids, out_scores, vec4);
+    return cudaGetLastError();
+  }
   const int n_chunks = filter_chunks(max_len);
   if (n_chunks > 65535 || M > 0x7fffffff) return cudaErrorInvalidValue;
   idx_problem p{};

@@ -153,3 +153,47 @@ def test_topk_heavy_ties_among_candidates(B):
         assert g_ids[m].tolist() == o_ids.tolist(), m
         assert np.array_equal(g_sc[m], o_sc.astype(np.float32)), m
     assert B.device_error() == 0
+
+
+def _many_rows(seed, M, L, K, ties):
+    """Score rows for the many-long-rows top-K: random (or small-integer) rows of
+    ragged lengths plus special rows (empty, shorter than K, all equal, -0.0 /
+    +0.0, two-valued, heavy ties among the best ~1.2 K)."""
+    s, lens = wl.score_rows(seed, M, L, ties=ties)
+    rng = np.random.default_rng(seed + 100)
+    lens[0], lens[1], lens[2], lens[3] = 0, 1, min(K - 1, L), min(K, L)
+    lens[4] = min(K + 1, L)
+    lens[5:12] = L
+    s[5] = 0.0
+    s[6] = -0.0
+    s[6, ::7] = 0.0
+    s[7] = 1.0
+    s[7, ::3] = 2.0
+    top = rng.choice(L, min(L, K + K // 5), replace=False)
+    s[8] = rng.random(L, dtype=np.float32)
+    s[8, top] = rng.choice(np.array([10.0, 11.0, 12.0], dtype=np.float32), top.size)
+    s[9] = np.float32(3.0)
+    s[9, rng.choice(L, 5, replace=False)] = np.float32(4.0)
+    return s, lens
+
+
+@pytest.mark.parametrize("seed,L,K,ties", [(41, 65536, 2048, False), (42, 65536, 2048, True), (43, 9000, 100, False),
+                                           (44, 20001, 1, True), (45, 18432, 2048, False),
+                                           (46, 16387, 2048, False)])
+def test_topk_many_long_rows(B, seed, L, K, ties):
+    """More rows than two per SM, longer than 4096: the one-block-per-row top-K
+    (threshold, one stream, shared-memory sort), bit-exact against the oracle's
+    lexicographic top-K on every row."""
+    M = 2 * torch.cuda.get_device_properties(0).multi_processor_count + 16
+    s, lens = _many_rows(seed, M, L, K, ties)
+    ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    sc = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(1, B.idx_topk_scores_workspace_size(M, L, K)), dtype=torch.uint8, device="cuda")
+    B.idx_topk_scores(_dev(s, torch.float32), _dev(lens), L, K, ids, sc, ws=ws)
+    g_ids, g_sc = ids.cpu().numpy(), sc.cpu().numpy()
+    for m in range(M):
+        o_ids, o_sc = odsa.topk(s[m, :lens[m]].astype(np.float64), K)
+        assert g_ids[m].tolist() == o_ids.tolist(), m
+        o32 = o_sc.astype(np.float32) + np.float32(0.0)    # the kernel reports -0.0 as +0.0
+        assert np.array_equal(g_sc[m].view(np.uint32), o32.view(np.uint32)), m
+    assert B.device_error() == 0
