@@ -238,3 +238,53 @@ def test_block_select_events_same_result(B):
     assert torch.equal(out1, out2) and torch.equal(c1, c2)
     times = [ev[i].elapsed_time(ev[i + 1]) for i in range(5)]
     assert all(t >= 0.0 for t in times)
+
+
+def test_tc_route_adversarial_bounds(B):
+    """Inputs aimed at the certified bound of the tensor-core block maxima
+    ("ferrox_core/block_sparse.rs", dot and select_for_head: the selection
+    rests on the exact sequential f32 block maxima): query and key elements
+    spread over many binades (fp16 under a per-row / per-block power-of-two
+    scale loses the small ones), keys k = 1000 u + v with u orthogonal to one
+    query head (large products cancelling to a small dot), and copies of the
+    block at the selection cut (exact ties and one-ulp nudges).  Every
+    selection must equal the oracle's and the CUDA-core route's, and the
+    measured error of every rescored block must stay inside its bound."""
+    rng = np.random.default_rng(31)
+    Q, n_kv, L, D = 16, 4, 20000, 128
+    q = rng.standard_normal((Q, n_kv, D)).astype(np.float32)
+    q[::2] *= (2.0 ** rng.integers(-12, 13, (Q // 2, n_kv, D))).astype(np.float32)
+    k = rng.standard_normal((L, D)).astype(np.float32)
+    k[:L // 4] *= (2.0 ** rng.integers(-20, 21, (L // 4, D))).astype(np.float32)
+    pos = np.linspace(8000, L - 1, Q).astype(np.int32)
+    # cancellation: blocks 70..89 orthogonal to query 1 head 0, 100..119 to query 3 head 1
+    for (qi, h, b0) in ((1, 0, 70), (3, 1, 100), (5, 2, 40)):
+        qv = q[qi, h].astype(np.float64)
+        for b in range(b0, b0 + 20):
+            r = rng.standard_normal((128, D))
+            u = r - np.outer(r @ qv / (qv @ qv), qv)
+            k[b * 128:(b + 1) * 128] = (1000.0 * u + rng.standard_normal((128, D))).astype(np.float32)
+    # copies of the block at the cut of query 0, head 0 (32 places, 3 forced)
+    sc = obs.block_scores(q[0, 0], k, int(pos[0]), 128)
+    n_blocks = sc.shape[0]
+    free = [b for b in range(1, n_blocks - 2)]
+    order = sorted(free, key=lambda b: (-float(sc[b]), b))
+    cut = order[28]
+    src = k[cut * 128:(cut + 1) * 128].copy()
+    for b in rng.choice([x for x in free if x != cut], 4, replace=False):
+        k[b * 128:(b + 1) * 128] = src                           # exact ties with the cut block
+    nudged = src.copy()
+    nudged.view(np.uint32)[:, 0] ^= 1                              # one-ulp changes of one element
+    b = [x for x in free if x != cut][5]
+    k[b * 128:(b + 1) * 128] = nudged
+    st = B.block_select_stats_tensor()
+    o, c = _run(B, q, k, pos, 32, 1, 2, stats=st)
+    got = _lists(o, c)
+    _check_oracle(got, q, k, pos, 32, 1, 2, range(Q))
+    o2, c2 = _run(B, q, k, pos, 32, 1, 2, static=True)
+    assert np.array_equal(o, o2) and np.array_equal(c, c2)
+    s = B.block_select_stats_read(st)
+    print("adversarial bound stats", s)
+    assert s["blocks_rescored"] > 0
+    assert 0.0 <= s["max_bound_use"] < 1.0
+    assert B.device_error() == 0

@@ -65,6 +65,43 @@ def test_merge_random_rows(B, seed, rows, topk, S, keep_mode):
     assert B.device_error() == 0
 
 
+@pytest.mark.parametrize("S", [3, 16, 64])
+def test_merge_large_contexts_at_segment_edges(B, S):
+    """Context lengths up to 2^31 - 1 and entries at the segment edges e_s - 1,
+    e_s, e_s + 1 (where floor(x S_eff / L) changes): bit-exact occupancy and
+    witnesses against the oracle's integer arithmetic."""
+    rng = np.random.default_rng(90 + S)
+    rows, topk = 40, 96
+    ctx = rng.integers(2 ** 30, 2 ** 31, rows).astype(np.int64)
+    ctx[0] = 2 ** 31 - 1
+    ctx[1] = S + 1
+    learned = np.full((rows, topk), -1, dtype=np.int64)
+    for r in range(rows):
+        L = int(ctx[r])
+        s_eff = min(S, L)
+        edges = [(s * L + s_eff - 1) // s_eff for s in range(s_eff)]
+        pick = rng.choice(s_eff, size=min(s_eff, 12), replace=False)
+        vals = []
+        for s in pick:
+            for d in (-1, 0, 1):
+                x = edges[s] + d
+                if 0 <= x < L:
+                    vals.append(x)
+        vals += [L - 1, L, L + 5] if L < 2 ** 31 - 6 else [L - 1]
+        vals = vals[:topk - 8]
+        learned[r, :len(vals)] = vals
+    learned = learned.astype(np.int32)
+    ctx = ctx.astype(np.int32)
+    ids = _dev(learned)
+    B.witness_merge(ids, _dev(ctx), topk - S if topk > S else 0, S, S)
+    ref = ow.apply_topology_witnesses(learned, topk, ctx, topk - S if topk > S else 0, S, S)
+    assert np.array_equal(ids.cpu().numpy(), ref)
+    tab = torch.empty((rows, S), dtype=torch.int32, device="cuda")
+    B.witness_indices(_dev(learned), _dev(ctx), S, tab)
+    assert np.array_equal(tab.cpu().numpy(), ow.topology_witness_indices(learned, topk, ctx, S))
+    assert B.device_error() == 0
+
+
 def test_decode_shaped_rows_with_padding(B):
     """64 rows x 2048 with 5% of slots set to -1, S = 16, serving form."""
     wp = wl.decode_bf16(M=64, H=2, D=8, L=32768, K=2048)
