@@ -48,6 +48,17 @@ __device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* red) {
   return t;
 }
 
+// Adds one to hist[bin] for every lane with `active` set, one shared-memory
+// atomic per distinct bin of the warp (lanes with equal bins are grouped by
+// match.any): rows with thousands of equal scores would otherwise serialise
+// their atomics on one address.  Every lane of the warp must call it.
+__device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool active) {
+  const unsigned act = __ballot_sync(0xffffffffu, active);
+  if (!active) return;
+  const unsigned peers = __match_any_sync(act, bin);
+  if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+}
+
 // Exclusive prefix sum over the block (thread order); *total = block sum.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* red, uint32_t* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -384,11 +395,16 @@ __device__ uint32_t smem_radix_select(TkShared& sh, int cn, uint32_t want, F f, 
     const uint32_t dmask = pass == 2 ? 0x3ffu : 0x7ffu;
     for (int b = threadIdx.x; b < kTopkBins; b += TK_NT) sh.hist[b] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < cn; i += TK_NT) {
-      if (flag(i)) {
+    for (int i0 = (int)(threadIdx.x & ~31u); i0 < cn; i0 += TK_NT) {
+      const int i = i0 + (int)(threadIdx.x & 31);
+      bool on = false;
+      uint32_t bin = 0;
+      if (i < cn && flag(i)) {
         const uint32_t k = f(i);
-        if ((k & mask) == prefix) atomicAdd(&sh.hist[(k >> shift) & dmask], 1u);
+        on = (k & mask) == prefix;
+        bin = (k >> shift) & dmask;
       }
+      hist_add_warp(sh.hist, bin, on);
     }
     __syncthreads();
     hist_suffix_find(sh, (int)dmask + 1, remaining);
@@ -447,14 +463,14 @@ __device__ uint32_t row_threshold(TfShared& sh, const float* row, int n, int K) 
   r = r < 1 ? 1 : (r > NS ? NS : r);
   for (int b = tid; b < kTopkBins; b += TF_NT) sh.hist[b] = 0;
   __syncthreads();
-  atomicAdd(&sh.hist[sv >> 21], 1u);
+  hist_add_warp(sh.hist, sv >> 21, true);
   __syncthreads();
   hist_suffix_find(sh, kTopkBins, (uint32_t)r);
   const uint32_t b1 = sh.found_bin, a1 = sh.found_above;
   __syncthreads();
   for (int b = tid; b < kTopkBins; b += TF_NT) sh.hist[b] = 0;
   __syncthreads();
-  if ((sv >> 21) == b1) atomicAdd(&sh.hist[(sv >> 10) & 0x7ffu], 1u);
+  hist_add_warp(sh.hist, (sv >> 10) & 0x7ffu, (sv >> 21) == b1);
   __syncthreads();
   hist_suffix_find(sh, kTopkBins, (uint32_t)r - a1);
   const uint32_t T = (b1 << 21) | (sh.found_bin << 10);
@@ -701,7 +717,7 @@ __device__ uint32_t tr_threshold(TrShared& sh, const float* row, int n, int K) {
   for (int b = tid; b < kTopkBins; b += TR_NT) sh.u.hist[b] = 0;
   __syncthreads();
 #pragma unroll
-  for (int j = 0; j < TR_NS / TR_NT; ++j) atomicAdd(&sh.u.hist[sv[j] >> 21], 1u);
+  for (int j = 0; j < TR_NS / TR_NT; ++j) hist_add_warp(sh.u.hist, sv[j] >> 21, true);
   __syncthreads();
   tr_suffix_find(sh, kTopkBins, (uint32_t)r);
   const uint32_t b1 = sh.found_bin, a1 = sh.found_above;
@@ -709,8 +725,7 @@ __device__ uint32_t tr_threshold(TrShared& sh, const float* row, int n, int K) {
   for (int b = tid; b < kTopkBins; b += TR_NT) sh.u.hist[b] = 0;
   __syncthreads();
 #pragma unroll
-  for (int j = 0; j < TR_NS / TR_NT; ++j)
-    if ((sv[j] >> 21) == b1) atomicAdd(&sh.u.hist[(sv[j] >> 10) & 0x7ffu], 1u);
+  for (int j = 0; j < TR_NS / TR_NT; ++j) hist_add_warp(sh.u.hist, (sv[j] >> 10) & 0x7ffu, (sv[j] >> 21) == b1);
   __syncthreads();
   tr_suffix_find(sh, kTopkBins, (uint32_t)r - a1);
   const uint32_t T = (b1 << 21) | (sh.found_bin << 10);
@@ -730,11 +745,16 @@ __device__ uint32_t tr_radix_select(TrShared& sh, int cn, uint32_t want, F f, Fl
     const uint32_t dmask = pass == 2 ? 0x3ffu : 0x7ffu;
     for (int b = threadIdx.x; b < kTopkBins; b += TR_NT) sh.u.hist[b] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < cn; i += TR_NT) {
-      if (flag(i)) {
+    for (int i0 = (int)(threadIdx.x & ~31u); i0 < cn; i0 += TR_NT) {
+      const int i = i0 + (int)(threadIdx.x & 31);
+      bool on = false;
+      uint32_t bin = 0;
+      if (i < cn && flag(i)) {
         const uint32_t k = f(i);
-        if ((k & mask) == prefix) atomicAdd(&sh.u.hist[(k >> shift) & dmask], 1u);
+        on = (k & mask) == prefix;
+        bin = (k >> shift) & dmask;
       }
+      hist_add_warp(sh.u.hist, bin, on);
     }
     __syncthreads();
     tr_suffix_find(sh, (int)dmask + 1, remaining);
