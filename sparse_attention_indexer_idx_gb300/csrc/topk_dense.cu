@@ -395,16 +395,19 @@ __device__ uint32_t smem_radix_select(TkShared& sh, int cn, uint32_t want, F f, 
     const uint32_t dmask = pass == 2 ? 0x3ffu : 0x7ffu;
     for (int b = threadIdx.x; b < kTopkBins; b += TK_NT) sh.hist[b] = 0;
     __syncthreads();
-    for (int i0 = (int)(threadIdx.x & ~31u); i0 < cn; i0 += TK_NT) {
-      const int i = i0 + (int)(threadIdx.x & 31);
-      bool on = false;
-      uint32_t bin = 0;
-      if (i < cn && flag(i)) {
-        const uint32_t k = f(i);
-        on = (k & mask) == prefix;
-        bin = (k >> shift) & dmask;
+    // eight elements per thread and iteration (their loads in flight together),
+    // warp-uniform trip counts for the aggregated adds
+    for (int i0 = (int)(threadIdx.x & ~31u); i0 < cn; i0 += 8 * TK_NT) {
+      uint32_t kk[8];
+      bool on[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * TK_NT + (int)(threadIdx.x & 31);
+        on[u] = i < cn && flag(i);
+        kk[u] = on[u] ? f(i) : 0u;
       }
-      hist_add_warp(sh.hist, bin, on);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) hist_add_warp(sh.hist, (kk[u] >> shift) & dmask, on[u] && (kk[u] & mask) == prefix);
     }
     __syncthreads();
     hist_suffix_find(sh, (int)dmask + 1, remaining);
@@ -463,14 +466,14 @@ __device__ uint32_t row_threshold(TfShared& sh, const float* row, int n, int K) 
   r = r < 1 ? 1 : (r > NS ? NS : r);
   for (int b = tid; b < kTopkBins; b += TF_NT) sh.hist[b] = 0;
   __syncthreads();
-  hist_add_warp(sh.hist, sv >> 21, true);
+  atomicAdd(&sh.hist[sv >> 21], 1u);
   __syncthreads();
   hist_suffix_find(sh, kTopkBins, (uint32_t)r);
   const uint32_t b1 = sh.found_bin, a1 = sh.found_above;
   __syncthreads();
   for (int b = tid; b < kTopkBins; b += TF_NT) sh.hist[b] = 0;
   __syncthreads();
-  hist_add_warp(sh.hist, (sv >> 10) & 0x7ffu, (sv >> 21) == b1);
+  if ((sv >> 21) == b1) atomicAdd(&sh.hist[(sv >> 10) & 0x7ffu], 1u);
   __syncthreads();
   hist_suffix_find(sh, kTopkBins, (uint32_t)r - a1);
   const uint32_t T = (b1 << 21) | (sh.found_bin << 10);
@@ -704,7 +707,14 @@ __device__ __forceinline__ void tr_suffix_find(TrShared& sh, int nb, uint32_t re
   __syncthreads();
 }
 
-// The filter's row threshold (n > K), once per row: 1024 samples i n / 1024.
+// The row threshold (n > K), once per row, from 1024 samples i n / 1024: v =
+// the key of the sample ranked r (the filter's rank: ~1.15 K + 3.5 sigma keys
+// expected above it), found exactly by three histogram levels (11, 11 and 10
+// bits).  T = v rounded down to its 22-bit prefix, as in the filter -- unless
+// v is a heavily repeated value (a plateau of equal scores, e.g. the exact
+// zeros of rows whose heads all clip) and enough samples lie strictly above
+// it (the expected K-sample count + 2 sigma): then T = v + 1, which leaves the
+// plateau out instead of collecting all of it.
 __device__ uint32_t tr_threshold(TrShared& sh, const float* row, int n, int K) {
   const int tid = threadIdx.x;
   uint32_t sv[TR_NS / TR_NT];
@@ -714,22 +724,29 @@ __device__ uint32_t tr_threshold(TrShared& sh, const float* row, int n, int K) {
   const float expect = (float)TR_NS * (float)K / (float)n;
   int r = (int)ceilf(1.15f * expect + 3.5f * sqrtf(expect)) + 1;
   r = r < 1 ? 1 : (r > TR_NS ? TR_NS : r);
-  for (int b = tid; b < kTopkBins; b += TR_NT) sh.u.hist[b] = 0;
-  __syncthreads();
+  uint32_t prefix = 0, mask = 0, remaining = (uint32_t)r, eq = 0;
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const uint32_t dmask = pass == 2 ? 0x3ffu : 0x7ffu;
+    for (int b = tid; b < kTopkBins; b += TR_NT) sh.u.hist[b] = 0;
+    __syncthreads();
 #pragma unroll
-  for (int j = 0; j < TR_NS / TR_NT; ++j) hist_add_warp(sh.u.hist, sv[j] >> 21, true);
-  __syncthreads();
-  tr_suffix_find(sh, kTopkBins, (uint32_t)r);
-  const uint32_t b1 = sh.found_bin, a1 = sh.found_above;
-  __syncthreads();
-  for (int b = tid; b < kTopkBins; b += TR_NT) sh.u.hist[b] = 0;
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < TR_NS / TR_NT; ++j) hist_add_warp(sh.u.hist, (sv[j] >> 10) & 0x7ffu, (sv[j] >> 21) == b1);
-  __syncthreads();
-  tr_suffix_find(sh, kTopkBins, (uint32_t)r - a1);
-  const uint32_t T = (b1 << 21) | (sh.found_bin << 10);
-  __syncthreads();
+    for (int j = 0; j < TR_NS / TR_NT; ++j)
+      if ((sv[j] & mask) == prefix) atomicAdd(&sh.u.hist[(sv[j] >> shift) & dmask], 1u);
+    __syncthreads();
+    tr_suffix_find(sh, (int)dmask + 1, remaining);
+    remaining -= sh.found_above;
+    eq = sh.u.hist[sh.found_bin];
+    prefix |= sh.found_bin << shift;
+    mask |= dmask << shift;
+    __syncthreads();
+  }
+  const uint32_t v = prefix;                                   // the r-th sample's key
+  const uint32_t above = (uint32_t)r - remaining;              // samples > v
+  const uint32_t safe = (uint32_t)ceilf(expect + 2.0f * sqrtf(expect)) + 1u;
+  uint32_t T = v & ~0x3ffu;
+  if (eq >= 8u && above >= safe && v < 0xffffffffu) T = v + 1u;
   return T ? T : 1u;
 }
 
@@ -745,16 +762,19 @@ __device__ uint32_t tr_radix_select(TrShared& sh, int cn, uint32_t want, F f, Fl
     const uint32_t dmask = pass == 2 ? 0x3ffu : 0x7ffu;
     for (int b = threadIdx.x; b < kTopkBins; b += TR_NT) sh.u.hist[b] = 0;
     __syncthreads();
-    for (int i0 = (int)(threadIdx.x & ~31u); i0 < cn; i0 += TR_NT) {
-      const int i = i0 + (int)(threadIdx.x & 31);
-      bool on = false;
-      uint32_t bin = 0;
-      if (i < cn && flag(i)) {
-        const uint32_t k = f(i);
-        on = (k & mask) == prefix;
-        bin = (k >> shift) & dmask;
+    // eight elements per thread and iteration (their loads in flight together),
+    // warp-uniform trip counts for the aggregated adds
+    for (int i0 = (int)(threadIdx.x & ~31u); i0 < cn; i0 += 8 * TR_NT) {
+      uint32_t kk[8];
+      bool on[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * TR_NT + (int)(threadIdx.x & 31);
+        on[u] = i < cn && flag(i);
+        kk[u] = on[u] ? f(i) : 0u;
       }
-      hist_add_warp(sh.u.hist, bin, on);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) hist_add_warp(sh.u.hist, (kk[u] >> shift) & dmask, on[u] && (kk[u] & mask) == prefix);
     }
     __syncthreads();
     tr_suffix_find(sh, (int)dmask + 1, remaining);

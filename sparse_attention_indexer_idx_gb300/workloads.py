@@ -331,8 +331,8 @@ def witness_rows(seed: int, rows: int, topk: int, L_min: int = 1, L_max: int = 4
     for r in range(rows):
         L = int(ctx[r])
         n = min(topk, L)
-        vals = rng.choice(L, size=n, replace=False).astype(np.int32)
-        out[r, :n] = vals
+        if n > 0:
+            out[r, :n] = rng.choice(L, size=n, replace=False).astype(np.int32)
         pad = rng.random(topk) < pad_frac
         out[r, pad] = -1
         oob = rng.random(topk) < oob_frac

@@ -47,7 +47,8 @@ def test_printed_examples(B):
 
 @pytest.mark.parametrize("seed,rows,topk,S,keep_mode", [
     (1, 64, 2048, 16, "serving"), (2, 128, 2048, 32, "serving"), (3, 37, 100, 64, "serving"),
-    (4, 50, 33, 7, "random"), (5, 300, 8, 4, "random"), (6, 20, 64, 64, "random"), (7, 9, 5, 40, "serving")])
+    (4, 50, 33, 7, "random"), (5, 300, 8, 4, "random"), (6, 20, 64, 64, "random"), (7, 9, 5, 40, "serving"),
+    (8, 5000, 64, 16, "serving"), (9, 6000, 37, 64, "random")])     # many rows: one warp per row
 def test_merge_random_rows(B, seed, rows, topk, S, keep_mode):
     learned, ctx = wl.witness_rows(seed, rows, topk, L_min=-2, L_max=5000)
     rng = np.random.default_rng(seed + 100)
