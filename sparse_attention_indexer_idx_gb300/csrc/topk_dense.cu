@@ -707,47 +707,63 @@ __device__ __forceinline__ void tr_suffix_find(TrShared& sh, int nb, uint32_t re
   __syncthreads();
 }
 
-// The row threshold (n > K), once per row, from 1024 samples i n / 1024: v =
-// the key of the sample ranked r (the filter's rank: ~1.15 K + 3.5 sigma keys
-// expected above it), found exactly by three histogram levels (11, 11 and 10
-// bits).  T = v rounded down to its 22-bit prefix, as in the filter -- unless
-// v is a heavily repeated value (a plateau of equal scores, e.g. the exact
-// zeros of rows whose heads all clip) and enough samples lie strictly above
-// it (the expected K-sample count + 2 sigma): then T = v + 1, which leaves the
-// plateau out instead of collecting all of it.
-__device__ uint32_t tr_threshold(TrShared& sh, const float* row, int n, int K) {
-  const int tid = threadIdx.x;
-  uint32_t sv[TR_NS / TR_NT];
+// Row thresholds, one warp per row, before the fused kernel: from 1024 samples
+// i n / 1024 (32 per lane), v = the key of the sample ranked r (the filter's
+// rank: ~1.15 K + 3.5 sigma keys expected above it), found exactly by a search
+// over its 32 bits (the largest key with at least r samples at or above it).
+// thr[m] = v rounded down to its 22-bit prefix, as in the filter -- unless v
+// is a heavily repeated value (8 or more samples equal to it: a plateau of
+// equal scores, e.g. the exact zeros of rows whose heads all clip), then
+// thr[m] = v + 1 and piv[m] = v: the plateau is left out of the candidates and
+// the fused kernel takes from it only what the top-K needs.  Rows with at most
+// K visible keys get thr = 1 (everything).
+constexpr int TT_WARPS = 8;
+
+__global__ void __launch_bounds__(32 * TT_WARPS)
+    topk_thresh_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ lens, idx_problem p,
+                       int use_p, int max_len, int K, const int32_t* __restrict__ row_mask, int64_t M,
+                       uint32_t* __restrict__ thr, uint32_t* __restrict__ piv) {
+  const int64_t m = (int64_t)blockIdx.x * TT_WARPS + (threadIdx.x >> 5);
+  if (m >= M) return;
+  const int lane = threadIdx.x & 31;
+  if (row_mask && !row_mask[m]) return;
+  const int n = row_length(lens, p, use_p, max_len, m);
+  if (n <= K) {
+    if (lane == 0) {
+      thr[m] = 1u;
+      piv[m] = 0u;
+    }
+    return;
+  }
+  const float* row = scores + m * ld;
+  uint32_t kv[32];
 #pragma unroll
-  for (int j = 0; j < TR_NS / TR_NT; ++j)
-    sv[j] = score_key(__ldg(row + (int)(((int64_t)(tid + j * TR_NT) * n) / TR_NS)));
+  for (int j = 0; j < 32; ++j) kv[j] = score_key(__ldg(row + (int)(((int64_t)(lane + 32 * j) * n) / TR_NS)));
   const float expect = (float)TR_NS * (float)K / (float)n;
   int r = (int)ceilf(1.15f * expect + 3.5f * sqrtf(expect)) + 1;
   r = r < 1 ? 1 : (r > TR_NS ? TR_NS : r);
-  uint32_t prefix = 0, mask = 0, remaining = (uint32_t)r, eq = 0;
+  uint32_t v = 0;
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const uint32_t dmask = pass == 2 ? 0x3ffu : 0x7ffu;
-    for (int b = tid; b < kTopkBins; b += TR_NT) sh.u.hist[b] = 0;
-    __syncthreads();
+  for (int b = 31; b >= 0; --b) {
+    const uint32_t trial = v | (1u << b);
+    uint32_t c = 0;
 #pragma unroll
-    for (int j = 0; j < TR_NS / TR_NT; ++j)
-      if ((sv[j] & mask) == prefix) atomicAdd(&sh.u.hist[(sv[j] >> shift) & dmask], 1u);
-    __syncthreads();
-    tr_suffix_find(sh, (int)dmask + 1, remaining);
-    remaining -= sh.found_above;
-    eq = sh.u.hist[sh.found_bin];
-    prefix |= sh.found_bin << shift;
-    mask |= dmask << shift;
-    __syncthreads();
+    for (int j = 0; j < 32; ++j) c += kv[j] >= trial ? 1u : 0u;
+    if (__reduce_add_sync(0xffffffffu, c) >= (uint32_t)r) v = trial;
   }
-  const uint32_t v = prefix;                                   // the r-th sample's key
-  const uint32_t above = (uint32_t)r - remaining;              // samples > v
-  const uint32_t safe = (uint32_t)ceilf(expect + 2.0f * sqrtf(expect)) + 1u;
-  uint32_t T = v & ~0x3ffu;
-  if (eq >= 8u && above >= safe && v < 0xffffffffu) T = v + 1u;
-  return T ? T : 1u;
+  uint32_t eq = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) eq += kv[j] == v ? 1u : 0u;
+  eq = __reduce_add_sync(0xffffffffu, eq);
+  uint32_t T = v & ~0x3ffu, pv = 0u;
+  if (eq >= 8u && v < 0xffffffffu) {
+    T = v + 1u;
+    pv = v;
+  }
+  if (lane == 0) {
+    thr[m] = T ? T : 1u;
+    piv[m] = pv;
+  }
 }
 
 // Exact radix select over cn elements: the want-th largest f(i) among the
@@ -945,7 +961,8 @@ __global__ void __launch_bounds__(TR_NT, 2)
     topk_rows_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ lens, idx_problem p,
                      int use_p, int max_len, int K, int P, const int32_t* __restrict__ id_map, int64_t id_ld,
                      const int32_t* __restrict__ row_mask, int32_t* __restrict__ out_ids,
-                     float* __restrict__ out_scores, int vec4) {
+                     float* __restrict__ out_scores, int vec4, const uint32_t* __restrict__ thr,
+                     const uint32_t* __restrict__ piv) {
   extern __shared__ __align__(16) uint8_t tr_smem[];
   TrShared& sh = *reinterpret_cast<TrShared*>(tr_smem);
   const int64_t m = blockIdx.x;
@@ -967,8 +984,12 @@ __global__ void __launch_bounds__(TR_NT, 2)
   const float* row = scores + m * ld;
   const int32_t* idm = id_map ? id_map + m * id_ld : nullptr;
   auto idof = [&](int i) { return idm ? idm[i] : (int32_t)i; };
-  // every visible key when the row has at most K of them (ordered keys are >= 1)
-  const uint32_t T = n <= K ? 1u : tr_threshold(sh, row, n, K);
+  // keys >= T (T = 1: every visible key), compared as floats: x >= key_score(T)
+  // is key(x) >= T for every finite x (a T below every finite key maps to a NaN
+  // float, and then everything is kept)
+  const uint32_t T = thr[m], pv = piv[m];
+  const float Tf = key_score(T);
+  const bool keep_all = T <= 1u || !(Tf == Tf);
   if (tid == 0) sh.ncand = 0;
   __syncthreads();
   // one stream over the row: keys >= T into the candidate space, one
@@ -977,7 +998,9 @@ __global__ void __launch_bounds__(TR_NT, 2)
   // ld a multiple of 4 and an aligned base, checked by the host)
 #pragma unroll 1
   for (int c0 = 0; c0 < n; c0 += TR_NT * 4 * TR_V) {
-    uint32_t kv[4 * TR_V];
+    float xs[4 * TR_V];
+    uint32_t kmask = 0;                          // bit u: score u is kept
+    static_assert(4 * TR_V == 32, "one mask word per round");
 #pragma unroll
     for (int v = 0; v < TR_V; ++v) {
       const int i0 = c0 + 4 * (v * TR_NT + tid);
@@ -997,11 +1020,12 @@ __global__ void __launch_bounds__(TR_NT, 2)
         }
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) kv[4 * v + e] = i0 + e < n ? score_key(x[e]) : 0u;
+      for (int e = 0; e < 4; ++e) {
+        xs[4 * v + e] = x[e];
+        if (i0 + e < n && (keep_all || x[e] >= Tf)) kmask |= 1u << (4 * v + e);
+      }
     }
-    uint32_t c = 0;
-#pragma unroll
-    for (int u = 0; u < 4 * TR_V; ++u) c += kv[u] >= T ? 1u : 0u;
+    const uint32_t c = (uint32_t)__popc(kmask);
     uint32_t incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1017,8 +1041,9 @@ __global__ void __launch_bounds__(TR_NT, 2)
     uint32_t pos = base + incl - c;
 #pragma unroll
     for (int u = 0; u < 4 * TR_V; ++u) {
-      if (kv[u] >= T) {
-        if (pos < (uint32_t)TR_CAP) sh.cand[pos] = composite(kv[u], idof(c0 + 4 * ((u >> 2) * TR_NT + tid) + (u & 3)));
+      if ((kmask >> u) & 1u) {
+        if (pos < (uint32_t)TR_CAP)
+          sh.cand[pos] = composite(score_key(xs[u]), idof(c0 + 4 * ((u >> 2) * TR_NT + tid) + (u & 3)));
         ++pos;
       }
     }
@@ -1028,6 +1053,41 @@ __global__ void __launch_bounds__(TR_NT, 2)
   if (total >= (uint32_t)want && total <= (uint32_t)TR_CAP) {
     emit(tr_order_top(sh, sh.cand, (int)total, want, P, sh.dst), want);
     return;
+  }
+  if (pv && !idm && total < (uint32_t)want) {
+    // The plateau at pv was left out and the keys above it are fewer than
+    // min(K, n): if the row has enough keys equal to pv, the K-th key is pv and
+    // the rest of the top-K are the keys equal to pv with the smallest ids --
+    // the first ones in row order (ids are positions here).  One ordered scan:
+    // thread t takes four consecutive positions of each 2048-position chunk.
+    const uint32_t need = (uint32_t)want - total;
+    uint32_t found = 0;
+#pragma unroll 1
+    for (int c0 = 0; c0 < n && found < need; c0 += 4 * TR_NT) {
+      const int i0 = c0 + 4 * tid;
+      uint32_t ek[4];
+      uint32_t c = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ek[e] = i0 + e < n ? score_key(__ldg(row + i0 + e)) : 0u;
+        c += ek[e] == pv ? 1u : 0u;
+      }
+      uint32_t chunk;
+      uint32_t rank = found + tr_excl_scan(c, sh.red, &chunk);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (ek[e] == pv) {
+          if (rank < need) sh.cand[total + rank] = composite(pv, i0 + e);
+          ++rank;
+        }
+      }
+      found += chunk;
+    }
+    __syncthreads();
+    if (found >= need) {
+      emit(tr_order_top(sh, sh.cand, want, want, P, sh.dst), want);
+      return;
+    }
   }
   // the threshold missed: exact radix select over the row's scores
   auto key_f = [&](int i) { return score_key(__ldg(row + i)); };
@@ -1094,8 +1154,15 @@ cudaError_t launch_topk_dense(const float* scores, int64_t ld, const int32_t* le
     cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int vec4 = (ld % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0) ? 1 : 0;
+    WsCarver c(ws);
+    uint32_t* thr = c.take<uint32_t>((size_t)M);
+    uint32_t* piv = c.take<uint32_t>((size_t)M);
+    topk_thresh_kernel<<<(unsigned)((M + TT_WARPS - 1) / TT_WARPS), 32 * TT_WARPS, 0, st>>>(
+        scores, ld, lens, p, p_or_null ? 1 : 0, max_len, K, row_mask, M, thr, piv);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     topk_rows_kernel<<<(unsigned)M, TR_NT, smem, st>>>(scores, ld, lens, p, p_or_null ? 1 : 0, max_len, K, P, id_map,
-                                                       id_ld, row_mask, out_ids, out_scores, vec4);
+                                                       id_ld, row_mask, out_ids, out_scores, vec4, thr, piv);
     return cudaGetLastError();
   }
   const int n_chunks = filter_chunks(max_len);

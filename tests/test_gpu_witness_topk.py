@@ -212,6 +212,21 @@ def _many_rows(seed, M, L, K, ties):
     s[8, top] = rng.choice(np.array([10.0, 11.0, 12.0], dtype=np.float32), top.size)
     s[9] = np.float32(3.0)
     s[9, rng.choice(L, 5, replace=False)] = np.float32(4.0)
+    # a plateau of exact zeros under the top-K (rows whose heads all clip):
+    # ~1.25 K positives (the K-th key above the plateau), ~0.75 K positives (the
+    # K-th key on it: the smallest ids among the zeros complete the top-K)
+    for row, npos in ((10, min(L // 3, K + K // 4)), (11, min(L // 3, (3 * K) // 4))):
+        s[row] = -rng.random(L, dtype=np.float32) - np.float32(1.0)
+        z = rng.choice(L, L // 3, replace=False)
+        s[row, z] = np.float32(0.0)
+        s[row, rng.choice(z, npos, replace=False)] = rng.random(npos, dtype=np.float32) + np.float32(0.5)
+        lens[row] = L
+    # a plateau of -inf (dropped entries) with finite scores above and below K
+    s[12] = -np.inf
+    s[12, rng.choice(L, min(L, K + 10), replace=False)] = rng.standard_normal(min(L, K + 10), dtype=np.float32)
+    s[13] = -np.inf
+    s[13, rng.choice(L, max(1, K // 2), replace=False)] = rng.standard_normal(max(1, K // 2), dtype=np.float32)
+    lens[12] = lens[13] = L
     return s, lens
 
 
