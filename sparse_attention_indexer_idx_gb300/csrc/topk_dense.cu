@@ -638,7 +638,7 @@ constexpr int TR_KMAX = 2048;               // largest K this kernel takes
 constexpr uint32_t kTrBucketMax = 256;      // a larger bucket: heavy ties
 constexpr int TR_DST = TR_KMAX + 256;       // scatter space: the first K places plus one bucket
 constexpr int TR_NB = 4096;                 // buckets of the sort
-constexpr int TR_V = 8;                     // 4-score vectors per thread and round (loads in flight)
+constexpr int TR_V = 4;                     // 4-score vectors per thread, round and register buffer
 constexpr int TR_NS = 1024;                 // threshold samples
 
 struct TrShared {
@@ -992,45 +992,47 @@ __global__ void __launch_bounds__(TR_NT, 2)
   const bool keep_all = T <= 1u || !(Tf == Tf);
   if (tid == 0) sh.ncand = 0;
   __syncthreads();
-  // one stream over the row: keys >= T into the candidate space, one
-  // reservation per warp and round; thread tid reads the four scores at
-  // c0 + 4 (v TR_NT + tid) .. + 3 (one 16-byte load when the rows allow it:
-  // ld a multiple of 4 and an aligned base, checked by the host)
-#pragma unroll 1
-  for (int c0 = 0; c0 < n; c0 += TR_NT * 4 * TR_V) {
-    float xs[4 * TR_V];
-    uint32_t kmask = 0;                          // bit u: score u is kept
-    static_assert(4 * TR_V == 32, "one mask word per round");
+  // one stream over the row: keys >= T into the candidate space.  Rounds of
+  // 4 x TR_NT x TR_V scores, thread tid reading the four at c0 + 4 (v TR_NT +
+  // tid) .. + 3 (one 16-byte load when the rows allow it: ld a multiple of 4
+  // and an aligned base, checked by the host); two register buffers, so that
+  // one round's loads are in flight while the previous round is processed; one
+  // shared-memory reservation per warp and round.
+  auto load_round = [&](float4 (&buf)[TR_V], int c0) {
 #pragma unroll
     for (int v = 0; v < TR_V; ++v) {
       const int i0 = c0 + 4 * (v * TR_NT + tid);
-      float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       if (i0 < n) {
         if (vec4) {
           // i0 < n <= ld and ld % 4 == 0, so the vector lies inside the row's storage
-          const float4 f = __ldg(reinterpret_cast<const float4*>(row + i0));
-          x[0] = f.x;
-          x[1] = f.y;
-          x[2] = f.z;
-          x[3] = f.w;
+          f = __ldg(reinterpret_cast<const float4*>(row + i0));
         } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (i0 + e < n) x[e] = __ldg(row + i0 + e);
+          f.x = __ldg(row + i0);
+          if (i0 + 1 < n) f.y = __ldg(row + i0 + 1);
+          if (i0 + 2 < n) f.z = __ldg(row + i0 + 2);
+          if (i0 + 3 < n) f.w = __ldg(row + i0 + 3);
         }
       }
+      buf[v] = f;
+    }
+  };
+  auto process_round = [&](const float4 (&buf)[TR_V], int c0) {
+    uint32_t kmask = 0;                        // bit 4 v + e: score e of vector v is kept
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        xs[4 * v + e] = x[e];
+    for (int v = 0; v < TR_V; ++v) {
+      const int i0 = c0 + 4 * (v * TR_NT + tid);
+      const float x[4] = {buf[v].x, buf[v].y, buf[v].z, buf[v].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
         if (i0 + e < n && (keep_all || x[e] >= Tf)) kmask |= 1u << (4 * v + e);
-      }
     }
     const uint32_t c = (uint32_t)__popc(kmask);
     uint32_t incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
     }
     const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
     uint32_t base = 0;
@@ -1040,13 +1042,27 @@ __global__ void __launch_bounds__(TR_NT, 2)
     }
     uint32_t pos = base + incl - c;
 #pragma unroll
-    for (int u = 0; u < 4 * TR_V; ++u) {
-      if ((kmask >> u) & 1u) {
-        if (pos < (uint32_t)TR_CAP)
-          sh.cand[pos] = composite(score_key(xs[u]), idof(c0 + 4 * ((u >> 2) * TR_NT + tid) + (u & 3)));
+    for (int v = 0; v < TR_V; ++v) {
+      uint32_t m4 = (kmask >> (4 * v)) & 0xfu;
+      while (m4) {
+        const int e = __ffs(m4) - 1;
+        m4 &= m4 - 1u;
+        const float4 f = buf[v];
+        const float xv = e == 0 ? f.x : (e == 1 ? f.y : (e == 2 ? f.z : f.w));
+        if (pos < (uint32_t)TR_CAP) sh.cand[pos] = composite(score_key(xv), idof(c0 + 4 * (v * TR_NT + tid) + e));
         ++pos;
       }
     }
+  };
+  constexpr int kStep = 4 * TR_NT * TR_V;
+  float4 ba[TR_V], bb[TR_V];
+  load_round(ba, 0);
+#pragma unroll 1
+  for (int c0 = 0; c0 < n; c0 += 2 * kStep) {
+    load_round(bb, c0 + kStep);
+    process_round(ba, c0);
+    load_round(ba, c0 + 2 * kStep);
+    process_round(bb, c0 + kStep);
   }
   __syncthreads();
   const uint32_t total = sh.ncand;
