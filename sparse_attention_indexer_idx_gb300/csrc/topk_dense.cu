@@ -708,7 +708,7 @@ __device__ __forceinline__ void tr_suffix_find(TrShared& sh, int nb, uint32_t re
 }
 
 // Row thresholds, one warp per row, before the fused kernel: from 1024 samples
-// i n / 1024 (32 per lane), v = the key of the sample ranked r (the filter's
+// (32 per lane, in runs of 8 evenly spread), v = the key of the sample ranked r (the filter's
 // rank: ~1.15 K + 3.5 sigma keys expected above it), found exactly by a search
 // over its 32 bits (the largest key with at least r samples at or above it).
 // thr[m] = v rounded down to its 22-bit prefix, as in the filter -- unless v
@@ -719,7 +719,7 @@ __device__ __forceinline__ void tr_suffix_find(TrShared& sh, int nb, uint32_t re
 // K visible keys get thr = 1 (everything).
 constexpr int TT_WARPS = 8;
 
-__global__ void __launch_bounds__(32 * TT_WARPS)
+__global__ void __launch_bounds__(32 * TT_WARPS, 1)
     topk_thresh_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ lens, idx_problem p,
                        int use_p, int max_len, int K, const int32_t* __restrict__ row_mask, int64_t M,
                        uint32_t* __restrict__ thr, uint32_t* __restrict__ piv) {
@@ -735,10 +735,19 @@ __global__ void __launch_bounds__(32 * TT_WARPS)
     }
     return;
   }
+  // samples in 128 runs of 8 consecutive scores (one 32-byte sector each) spread
+  // evenly over the row: sample s sits at run_start(s / 8) + s % 8.  A lone
+  // 4-byte sample costs a whole 128-byte line of DRAM traffic, so runs cut
+  // the threshold's traffic about eightfold.
   const float* row = scores + m * ld;
   uint32_t kv[32];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) kv[j] = score_key(__ldg(row + (int)(((int64_t)(lane + 32 * j) * n) / TR_NS)));
+  for (int j = 0; j < 32; ++j) {
+    const int smp = lane + 32 * j;
+    int pos = (int)(((int64_t)(smp >> 3) * n) / (TR_NS / 8)) + (smp & 7);
+    pos = pos < n ? pos : n - 1;
+    kv[j] = score_key(__ldg(row + pos));
+  }
   const float expect = (float)TR_NS * (float)K / (float)n;
   int r = (int)ceilf(1.15f * expect + 3.5f * sqrtf(expect)) + 1;
   r = r < 1 ? 1 : (r > TR_NS ? TR_NS : r);
