@@ -174,7 +174,13 @@ struct TcCfg {
   // else 4 (the two warps of a quarter take alternate units)
   static constexpr int EPT = (NQ > 1 || SUB > 1) ? NE : 4;
   static constexpr int NCONV = FP8 ? 1 : 0;   // warp that splits the query rows (FP8)
-  static constexpr int NTHREADS = 32 * (2 + NE + NCONV);
+  // producer warps: gathered tiles take two (two tile rows per lane: the copies
+  // of one warp alone could not keep the tensor core fed; a third or fourth
+  // warp would cut the registers per thread below what the epilogue needs),
+  // TMA tiles one
+  static constexpr int NP = GATHER ? 2 : 1;
+  static constexpr int RPL = 4 / NP;          // tile rows per producer lane
+  static constexpr int NTHREADS = 32 * (2 + NE + NCONV + (NP - 1));
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + SA * A_BYTES;
@@ -418,7 +424,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::SA; ++i) {
-      mbar_init(&a_full[i], C::GATHER ? 32 : 1);   // gathered: every producer lane arrives
+      mbar_init(&a_full[i], C::GATHER ? 32 * C::NP : 1);   // gathered: every producer lane arrives
       // the bound epilogue reads ||k|| from the key tile, so its warps also release the slot
       mbar_init(&a_empty[i], C::KN_TILE ? 1 + C::EPT : 1);
     }
@@ -437,7 +443,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       mbar_init(&sig_empty[i], C::NE);
     }
     for (int i = 0; i < C::SSC; ++i) {
-      mbar_init(&sc_full[i], 32);               // each producer lane, once its copies landed
+      mbar_init(&sc_full[i], 32 * C::NP);       // each producer lane, once its copies landed
       mbar_init(&sc_empty[i], C::EPT);
     }
     *abort_flag = 0;
@@ -455,8 +461,12 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const TcSched s = *sched;
 
-  if (warp == 0) {
+  if (warp == 0 || (C::NP > 1 && warp >= 2 + C::NE + C::NCONV)) {
     // ------------------------------------------------------------ producer
+    // producer warp pidx (warp 0 is producer 0, the only one that loads query
+    // tiles) copies tile rows RPL (32 pidx + lane) .. + RPL - 1
+    const int pidx = warp == 0 ? 0 : warp - (2 + C::NE + C::NCONV) + 1;
+    const int rbase = C::RPL * (32 * pidx + lane);
     TcUnits<C> u;
     u.init(args, s);
     int64_t cur_g = -1;
@@ -464,7 +474,9 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     int32_t gcnt = 0;                          // kGather: list length of the group
     // kGather: this lane's four list entries of the next unit, loaded one unit
     // ahead so that the list read overlaps the previous unit's gather
-    int32_t pf[4] = {0, 0, 0, 0};
+    int32_t pf[C::RPL];
+#pragma unroll
+    for (int i = 0; i < C::RPL; ++i) pf[i] = 0;
     int64_t pf_g = -1, pf_t = -1;
     uint32_t na = 0, nb = 0;
     uint32_t arrived = 0;                      // gathered: units whose copies this lane has arrived for
@@ -486,7 +498,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         cur_g = u.g;
         gbase = tc_key_base(args, cur_g);
         if (C::GATHER) gcnt = args.cnt[cur_g];
-        if (!C::FP8) {
+        if (!C::FP8 && pidx == 0) {
           // bf16: the group's query rows (FP8: the split warps read them from global memory)
           const int bs = nb % C::SB;
           bool ok = true;
@@ -512,15 +524,17 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       uint8_t* dst = sA + as * C::A_BYTES;
       uint64_t* fbar = &a_full[as];
-      int32_t graw[4] = {0, 0, 0, 0};   // kGather: list entries of tile rows 4 lane .. 4 lane + 3
+      int32_t graw[C::RPL];   // gathered: list entries of this lane's tile rows rbase .. rbase + RPL - 1
+#pragma unroll
+      for (int i = 0; i < C::RPL; ++i) graw[i] = 0;
       if (C::GATHER) {
         if (pf_g == u.g && pf_t == u.t) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) graw[i] = pf[i];
+          for (int i = 0; i < C::RPL; ++i) graw[i] = pf[i];
         } else {
           const int32_t* lst = args.list + u.g * args.gld + u.t * 128;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) graw[i] = (int)(u.t * 128) + 4 * lane + i < gcnt ? lst[4 * lane + i] : 0;
+          for (int i = 0; i < C::RPL; ++i) graw[i] = (int)(u.t * 128) + rbase + i < gcnt ? lst[rbase + i] : 0;
         }
       }
       if constexpr (C::FP8) {
@@ -531,26 +545,26 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         flush_if_blocked(&sc_empty[ss], ((na / C::SSC_MOD) & 1) ^ 1);
         if (lane == 0) sok = mbar_wait(&sc_empty[ss], ((na / C::SSC_MOD) & 1) ^ 1, abort_flag);
         if (!__shfl_sync(0xffffffffu, sok, 0)) break;
-        float* sdst = sScale + ss * C::UKEYS + 4 * lane;
+        float* sdst = sScale + ss * C::UKEYS + rbase;
 #pragma unroll
-        for (int i = 0; i < 4 * C::SUB; ++i) {
-          const int pos = (int)(u.t * C::UKEYS) + 128 * (i >> 2) + 4 * lane + (i & 3);
+        for (int i = 0; i < C::RPL * C::SUB; ++i) {
+          const int pos = (int)(u.t * C::UKEYS) + 128 * (i / C::RPL) + rbase + (i % C::RPL);
           int64_t row = gbase + pos;
-          if (C::GATHER) row = gbase + (int64_t)graw[i & 3];
+          if (C::GATHER) row = gbase + (int64_t)graw[i % C::RPL];
           row = row < 0 ? 0 : (row >= args.p.n_keys ? args.p.n_keys - 1 : row);
-          cp_async_4(sdst + 128 * (i >> 2) + (i & 3), args.p.key_scale + row);
+          cp_async_4(sdst + 128 * (i / C::RPL) + (i % C::RPL), args.p.key_scale + row);
         }
         cp_async_arrive_noinc(&sc_full[ss]);
       }
       if (C::GATHER) {
-        // lane l copies tile rows 4l..4l+3 (list positions t*128 + 4l + i), 16 bytes
-        // at a time, into the 128-byte-swizzled halves; rows past the list are left
-        // as they are (their accumulator rows are never read)
+        // this lane's tile rows (list positions t*128 + r), 16 bytes at a time, into
+        // the 128-byte-swizzled halves; rows past the list are left as they are
+        // (their accumulator rows are never read)
         constexpr int RB = C::FP8 ? 128 : 256;   // bytes of one key row
         const char* kb = static_cast<const char*>(args.p.keys);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 4 * lane + i;
+        for (int i = 0; i < C::RPL; ++i) {
+          const int r = rbase + i;
           if ((int)(u.t * 128) + r >= gcnt) continue;
           int64_t row = gbase + (int64_t)graw[i];
           row = row < 0 ? 0 : (row >= args.p.n_keys ? args.p.n_keys - 1 : row);
@@ -567,11 +581,11 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           const int32_t cn = nx.g == u.g ? gcnt : args.cnt[nx.g];
           const int32_t* l2 = args.list + nx.g * args.gld + nx.t * 128;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) pf[i] = (int)(nx.t * 128) + 4 * lane + i < cn ? l2[4 * lane + i] : 0;
+          for (int i = 0; i < C::RPL; ++i) pf[i] = (int)(nx.t * 128) + rbase + i < cn ? l2[rbase + i] : 0;
           pf_g = nx.g;
           pf_t = nx.t;
         }
-      } else if (lane == 0) {
+      } else if (lane == 0 && pidx == 0) {
         const int32_t y = (int32_t)(gbase + u.t * C::UKEYS);
         mbar_arrive_expect_tx(fbar, C::A_BYTES);
         tma_load_2d(dst, &tmap_k, fbar, 0, y);
@@ -595,7 +609,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       fence_proxy_async_smem();
       for (; arrived < na; ++arrived) mbar_arrive(&a_full[arrived % C::SA]);
     }
-    if (lane == 0) {
+    if (lane == 0 && pidx == 0) {
       for (uint32_t i = 0; i < (uint32_t)C::SB && i < nb; ++i) {
         uint32_t j = nb - 1 - i;
         mbar_wait_drain(&b_full[j % C::SB], (j / C::SB) & 1);
@@ -1066,7 +1080,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       ++nacc;
       u.advance();
     }
-  } else if (C::FP8) {
+  } else if (C::FP8 && warp < 2 + C::NE + C::NCONV) {
     // ------------------------------------------------------------ query split
     // Per query group, once the MMA has released the buffer: bf16 row v of query
     // qi (global memory, 256 bytes, one coalesced warp load) -> e4m3 B rows
