@@ -103,22 +103,29 @@ __global__ void rep_count_kernel(const int32_t* rep_ids, int nrep, int K, uint32
   }
 }
 
+// The best representative score of every key of [0, Lc), as an ordered key.
+__global__ void rep_best_kernel(const float* rep_sc, int64_t ld, int nrep, const int32_t* common_len,
+                                uint32_t* best) {
+  const int Lc = *common_len;
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < Lc; k += gridDim.x * blockDim.x) {
+    float b = rep_sc[k];
+    for (int r = 1; r < nrep; ++r) b = fmaxf(b, rep_sc[r * ld + k]);
+    best[k] = score_key(b);
+  }
+}
+
 // Cold rule: the n_seed best keys of [0, Lc) by (count desc, best rep score
 // desc, id asc) are marked in the shared seed bitmap.
 constexpr int kColdThreads = 1024;
 struct DummyRow {};
 
-__global__ void __launch_bounds__(kColdThreads) cold_select_kernel(const uint32_t* count, const float* rep_sc,
-                                                                   int64_t ld, int nrep, const int32_t* common_len,
-                                                                   int n_seed, uint32_t* seedbits) {
+__global__ void __launch_bounds__(kColdThreads) cold_select_kernel(const uint32_t* count, const uint32_t* best,
+                                                                   const int32_t* common_len, int n_seed,
+                                                                   uint32_t* seedbits) {
   __shared__ TopkShared<kColdThreads> sh;
   __shared__ uint32_t cnt_hist[8];
   const int Lc = *common_len;
-  auto best_key = [&](int k) {
-    float b = rep_sc[k];
-    for (int r = 1; r < nrep; ++r) b = fmaxf(b, rep_sc[r * ld + k]);
-    return score_key(b);
-  };
+  auto best_key = [&](int k) { return best[k]; };
   if (Lc <= n_seed) {
     for (int k = threadIdx.x; k < Lc; k += kColdThreads) atomicOr(&seedbits[k >> 5], 1u << (k & 31));
     return;
@@ -1125,6 +1132,7 @@ struct DosaWs {
   float* rep_sc;
   int32_t* rep_ids;
   uint32_t* rep_count;
+  uint32_t* rep_best;      // [ldmax] best representative score per key (ordered key)
   void* seed_keys;
   float* seed_scale;
   float* seed_sc;
@@ -1205,6 +1213,7 @@ static DosaWs carve(void* base, const idx_problem& p, int K, const dosa_params& 
   w.rep_sc = c.take<float>((size_t)4 * s.ldmax);
   w.rep_ids = c.take<int32_t>((size_t)4 * K);
   w.rep_count = c.take<uint32_t>(s.ldmax);
+  w.rep_best = c.take<uint32_t>(s.ldmax);
   const int row_bytes = p.k_dtype == IDX_FP8_E4M3 ? 128 : 256;
   w.seed_keys = c.take<char>(s.shared_seeds ? (size_t)s.NS * row_bytes : 16);
   w.seed_scale = c.take<float>(s.shared_seeds ? (size_t)s.NS : 1);
@@ -1341,7 +1350,8 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
                                  w.tk_ws, st));
     DOSA_CHECK(fill_i32(w.rep_count, s.ldmax, 0, st));
     rep_count_kernel<<<grid_for((int64_t)r.n * K, 256), 256, 0, st>>>(w.rep_ids, r.n, K, w.rep_count);
-    cold_select_kernel<<<1, kColdThreads, 0, st>>>(w.rep_count, w.rep_sc, s.ldmax, r.n, w.common, dp.n_seed, w.bits);
+    rep_best_kernel<<<grid_for(s.ldmax, 256), 256, 0, st>>>(w.rep_sc, s.ldmax, r.n, w.common, w.rep_best);
+    cold_select_kernel<<<1, kColdThreads, 0, st>>>(w.rep_count, w.rep_best, w.common, dp.n_seed, w.bits);
   }
   DOSA_CHECK(cudaGetLastError());
   bits_to_list_kernel<<<(unsigned)seed_rows, kListThreads, 0, st>>>(w.bits, s.W, w.list, s.NS, w.seed_cnt);

@@ -85,10 +85,19 @@ __device__ uint32_t topk_radix_select(TopkShared<NT>& sh, const Row& row, int n,
     const uint32_t dmask = (1u << widths[pass]) - 1u;
     for (int b = threadIdx.x; b < kTopkBins; b += NT) sh.hist[b] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += NT) {
-      if (!filter(i)) continue;
-      uint32_t k = f(i);
-      if ((k & mask) == prefix) atomicAdd(&sh.hist[(k >> shift) & dmask], 1u);
+    // eight elements per thread and iteration, their loads in flight together
+    for (int i0 = threadIdx.x; i0 < n; i0 += 8 * NT) {
+      uint32_t kk[8];
+      bool on[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * NT;
+        on[u] = i < n && filter(i);
+        kk[u] = on[u] ? f(i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (on[u] && (kk[u] & mask) == prefix) atomicAdd(&sh.hist[(kk[u] >> shift) & dmask], 1u);
     }
     __syncthreads();
     topk_find_bin<NT>(sh, dmask + 1u, remaining);
