@@ -851,31 +851,52 @@ __global__ void __launch_bounds__(kMergeThreads) merge_rows_kernel(
     int len;
     row_extent(gr.p, m, &off, &len);
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int i0 = 0; i0 < gn; i0 += kMergeThreads) {
-      const int i = i0 + threadIdx.x;
-      bool keep = false;
-      int32_t id = 0;
-      float s = 0.0f;
-      if (i < gn) {
-        id = gr.glist[g * gr.capg + i];
-        s = gr.gsc[m * gr.capg + i];
-        if (id < len && s >= t) {
-          const uint32_t word = gr.seedbits[(gr.seed_stride ? m * gr.seed_stride : 0) + (id >> 5)];
-          keep = !((word >> (id & 31)) & 1u);
+    const uint32_t* sbits = gr.seedbits + (gr.seed_stride ? m * gr.seed_stride : 0);
+    // rounds of kMergeThreads x 8 records, thread t taking records 8 t .. 8 t + 7
+    // of the round (their loads in flight together); one block scan places them
+    constexpr int RPT = 8;
+    for (int i0 = 0; i0 < gn; i0 += kMergeThreads * RPT) {
+      int32_t id[RPT];
+      float sv[RPT];
+#pragma unroll
+      for (int u = 0; u < RPT; ++u) {
+        const int i = i0 + RPT * (int)threadIdx.x + u;
+        id[u] = i < gn ? gr.glist[g * gr.capg + i] : 0x7fffffff;
+        sv[u] = i < gn ? gr.gsc[m * gr.capg + i] : 0.0f;
+      }
+      uint32_t keepm = 0;
+#pragma unroll
+      for (int u = 0; u < RPT; ++u) {
+        if (id[u] < len && sv[u] >= t) {
+          const uint32_t word = sbits[id[u] >> 5];
+          if (!((word >> (id[u] & 31)) & 1u)) keepm |= 1u << u;
         }
       }
-      const unsigned bal = __ballot_sync(0xffffffffu, keep);
-      if (lane == 0) s_wcnt[wid] = __popc(bal);
+      const int c = __popc(keepm);
+      // exclusive scan of c over the block, in thread order
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) s_wcnt[wid] = incl;
       __syncthreads();
-      int64_t pos = fill + __popc(bal & ((1u << lane) - 1u));
+      int64_t pos = fill + incl - c;
       int tot = 0;
       for (int w = 0; w < kMergeThreads / 32; ++w) {
         if (w < wid) pos += s_wcnt[w];
         tot += s_wcnt[w];
       }
-      if (keep && pos < cap) {
-        mrg_id[m * ld + K + pos] = id;
-        mrg_sc[m * ld + K + pos] = s;
+#pragma unroll
+      for (int u = 0; u < RPT; ++u) {
+        if ((keepm >> u) & 1u) {
+          if (pos < cap) {
+            mrg_id[m * ld + K + pos] = id[u];
+            mrg_sc[m * ld + K + pos] = sv[u];
+          }
+          ++pos;
+        }
       }
       fill += tot;
       __syncthreads();
