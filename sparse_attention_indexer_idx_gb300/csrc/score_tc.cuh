@@ -480,10 +480,14 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     int64_t pf_g = -1, pf_t = -1;
     uint32_t na = 0, nb = 0;
     uint32_t arrived = 0;                      // gathered: units whose copies this lane has arrived for
-    // Gathered tiles: a lane arrives for a unit only a few units after issuing its
-    // copies, so before the warp blocks on a barrier that the MMA or the epilogue
-    // frees, every unit still in flight is finished and counted (those may be the
-    // very units the MMA needs first).  probe: one non-blocking test by lane 0.
+    // Gathered tiles: a lane arrives for a unit only GD = SA - 1 units after issuing
+    // its copies.  A wait for a free key slot or scale slot needs the MMA (and the
+    // epilogue) to finish a unit issued SA or more units ago, which every lane has
+    // already counted, so those waits go ahead with the copies in flight.  The wait
+    // for the query buffer at a group change needs the whole previous group, whose
+    // last units may still be in flight here: before that wait (producer 0 only)
+    // every unit in flight is finished and counted.  probe: one non-blocking test
+    // by lane 0.
     auto flush_if_blocked = [&](uint64_t* bar, uint32_t parity) {
       if (!C::GATHER) return;
       bool rdy = false;
@@ -519,7 +523,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       }
       const int as = na % C::SA;
       bool ok = true;
-      flush_if_blocked(&a_empty[as], ((na / C::SA) & 1) ^ 1);
       if (lane == 0) ok = mbar_wait(&a_empty[as], ((na / C::SA) & 1) ^ 1, abort_flag);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       uint8_t* dst = sA + as * C::A_BYTES;
@@ -542,7 +545,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         // the buffer; a scale past the row's end is never used)
         const int ss = na % C::SSC_MOD;
         bool sok = true;
-        flush_if_blocked(&sc_empty[ss], ((na / C::SSC_MOD) & 1) ^ 1);
         if (lane == 0) sok = mbar_wait(&sc_empty[ss], ((na / C::SSC_MOD) & 1) ^ 1, abort_flag);
         if (!__shfl_sync(0xffffffffu, sok, 0)) break;
         float* sdst = sScale + ss * C::UKEYS + rbase;
