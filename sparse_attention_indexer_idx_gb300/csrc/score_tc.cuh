@@ -158,10 +158,12 @@ struct TcCfg {
   static constexpr int SA = FP8 ? (SA_FIT > 12 ? 12 : SA_FIT) : ((BQ_BYTES * SB <= 32768) ? 5 : 4);
   static constexpr int SSC = FP8 ? SA + SACC + 2 : 0;
   static constexpr int SSC_MOD = SSC > 0 ? SSC : 1;
-  // gathered tiles: key copies a producer lane keeps in flight before it waits
-  // (at most SA - 1, so the slot it waits to reuse never depends on its own arrival)
-  static constexpr int GD = SA - 1;
   static constexpr int IL = (SUB == 1 && N <= 128) ? 2 : 1;   // units whose MMA chains are interleaved
+  // gathered tiles: units a producer lane keeps in flight before it counts the
+  // oldest one in.  A wait for the slot of unit x needs the MMA to finish unit
+  // x - SA, which it issues together with the next IL - 1 units, so those must
+  // already be counted: at most SA - IL units in flight.
+  static constexpr int GD = SA - IL;
   static constexpr int TMEM_COLS = tc_pow2_cols(SACC * ACC_STRIDE);
   // epilogue warps, two per TMEM lane quarter (four for the bf16 bound over
   // several queries, whose dependent chains leave two warps per quarter idle)
@@ -203,6 +205,7 @@ struct TcCfg {
   static_assert(MODE != kFilter || NQ == 1, "kFilter: one query per group");
   static_assert(SACC * ACC_STRIDE <= 512, "TMEM columns");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(!GATHER || GD >= 1, "gathered tiles need a key ring deeper than the interleave");
 };
 
 struct TcSched {
@@ -480,10 +483,11 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     int64_t pf_g = -1, pf_t = -1;
     uint32_t na = 0, nb = 0;
     uint32_t arrived = 0;                      // gathered: units whose copies this lane has arrived for
-    // Gathered tiles: a lane arrives for a unit only GD = SA - 1 units after issuing
-    // its copies.  A wait for a free key slot or scale slot needs the MMA (and the
-    // epilogue) to finish a unit issued SA or more units ago, which every lane has
-    // already counted, so those waits go ahead with the copies in flight.  The wait
+    // Gathered tiles: a lane arrives for a unit only GD = SA - IL units after
+    // issuing its copies.  A wait for a free key slot or scale slot needs the MMA
+    // (and the epilogue) to finish a unit issued SA or more units ago, together
+    // with the IL - 1 units the MMA interleaves with it, all of which every lane
+    // has already counted, so those waits go ahead with the copies in flight.  The wait
     // for the query buffer at a group change needs the whole previous group, whose
     // last units may still be in flight here: before that wait (producer 0 only)
     // every unit in flight is finished and counted.  probe: one non-blocking test
