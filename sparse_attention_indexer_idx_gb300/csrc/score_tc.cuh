@@ -159,11 +159,6 @@ struct TcCfg {
   static constexpr int SSC = FP8 ? SA + SACC + 2 : 0;
   static constexpr int SSC_MOD = SSC > 0 ? SSC : 1;
   static constexpr int IL = (SUB == 1 && N <= 128) ? 2 : 1;   // units whose MMA chains are interleaved
-  // gathered tiles: units a producer lane keeps in flight before it counts the
-  // oldest one in.  A wait for the slot of unit x needs the MMA to finish unit
-  // x - SA, which it issues together with the next IL - 1 units, so those must
-  // already be counted: at most SA - IL units in flight.
-  static constexpr int GD = SA - IL;
   static constexpr int TMEM_COLS = tc_pow2_cols(SACC * ACC_STRIDE);
   // epilogue warps, two per TMEM lane quarter (four for the bf16 bound over
   // several queries, whose dependent chains leave two warps per quarter idle)
@@ -205,7 +200,6 @@ struct TcCfg {
   static_assert(MODE != kFilter || NQ == 1, "kFilter: one query per group");
   static_assert(SACC * ACC_STRIDE <= 512, "TMEM columns");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
-  static_assert(!GATHER || GD >= 1, "gathered tiles need a key ring deeper than the interleave");
 };
 
 struct TcSched {
@@ -482,25 +476,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     for (int i = 0; i < C::RPL; ++i) pf[i] = 0;
     int64_t pf_g = -1, pf_t = -1;
     uint32_t na = 0, nb = 0;
-    uint32_t arrived = 0;                      // gathered: units whose copies this lane has arrived for
-    // Gathered tiles: a lane arrives for a unit only GD = SA - IL units after
-    // issuing its copies.  A wait for a free key slot or scale slot needs the MMA
-    // (and the epilogue) to finish a unit issued SA or more units ago, together
-    // with the IL - 1 units the MMA interleaves with it, all of which every lane
-    // has already counted, so those waits go ahead with the copies in flight.  The wait
-    // for the query buffer at a group change needs the whole previous group, whose
-    // last units may still be in flight here: before that wait (producer 0 only)
-    // every unit in flight is finished and counted.  probe: one non-blocking test
-    // by lane 0.
-    auto flush_if_blocked = [&](uint64_t* bar, uint32_t parity) {
-      if (!C::GATHER) return;
-      bool rdy = false;
-      if (lane == 0) rdy = mbar_try_wait(bar, parity);
-      if (__shfl_sync(0xffffffffu, rdy, 0) || arrived == na) return;
-      asm volatile("cp.async.wait_all;" ::: "memory");
-      fence_proxy_async_smem();
-      for (; arrived < na; ++arrived) mbar_arrive(&a_full[arrived % C::SA]);
-    };
+    // Gathered tiles: every producer lane arrives on the tile's barrier through
+    // cp.async.mbarrier.arrive.noinc, which fires once that lane's copies have
+    // landed, so the producer never waits for its own copies; the MMA thread
+    // fences the async proxy after the barrier and before its MMAs read the tile.
     while (u.valid()) {
       if (u.g != cur_g) {
         cur_g = u.g;
@@ -510,7 +489,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           // bf16: the group's query rows (FP8: the split warps read them from global memory)
           const int bs = nb % C::SB;
           bool ok = true;
-          flush_if_blocked(&b_empty[bs], ((nb / C::SB) & 1) ^ 1);
           if (lane == 0) {
             ok = mbar_wait(&b_empty[bs], ((nb / C::SB) & 1) ^ 1, abort_flag);
             if (ok) {
@@ -579,7 +557,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           for (int cc = 0; cc < RB / 16; ++cc)
             cp_async_16(dst + (cc >> 3) * (C::A_BYTES / 2) + r * 128 + (((cc & 7) ^ (r & 7)) << 4), src + cc * 16);
         }
-        cp_async_commit();
+        cp_async_arrive_noinc(fbar);            // counts this lane in once its copies landed
         // the next unit's entries
         TcUnits<C> nx = u;
         nx.advance();
@@ -597,24 +575,12 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         tma_load_2d(dst, &tmap_k, fbar, 0, y);
         if (!C::FP8) tma_load_2d(dst + C::A_BYTES / 2, &tmap_k, fbar, 64, y);
       }
-      if (C::GATHER && na + 1 - arrived > (uint32_t)C::GD) {
-        // the oldest unit in flight: this lane's copies are done; make them visible
-        // to the tensor cores and count this lane in
-        cp_async_wait_group<C::GD>();
-        fence_proxy_async_smem();
-        mbar_arrive(&a_full[arrived % C::SA]);
-        ++arrived;
-      }
       __syncwarp();
       ++na;
       u.advance();
     }
     // drain: the last phase issued on every ring slot has landed
     if (C::FP8 || C::GATHER) asm volatile("cp.async.wait_all;" ::: "memory");
-    if (C::GATHER) {
-      fence_proxy_async_smem();
-      for (; arrived < na; ++arrived) mbar_arrive(&a_full[arrived % C::SA]);
-    }
     if (lane == 0 && pidx == 0) {
       for (uint32_t i = 0; i < (uint32_t)C::SB && i < nb; ++i) {
         uint32_t j = nb - 1 - i;
@@ -657,6 +623,9 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         }
         if (!ok) break;
         tc_fence_after();
+        // gathered tiles were written through the generic proxy (cp.async); make
+        // them visible to the tensor core's async-proxy reads
+        if (C::GATHER) fence_proxy_async_smem();
         const uint32_t b0 = smem_u32(sB + cur_bs * C::B_BYTES);
         // two independent chains: two units (IL), or the two subtiles of one unit
         uint32_t a0[2], d[2];
