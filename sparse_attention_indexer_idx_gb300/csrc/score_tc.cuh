@@ -166,6 +166,9 @@ struct TcCfg {
   // bf16 score tiles with at least 4 queries: an epilogue warp walks its queries
   // two at a time, both chains in one packed fma.rn.f32x2 per head
   static constexpr bool PAIR = (MODE != kBound) && (MODE != kFilter) && !FP8 && NQ >= 4;
+  // the bound over 16-vector blocks keeps its warp's two queries' folded weights
+  // interleaved the same way, (w_a[j], w_b[j]) adjacent, for the packed chain
+  static constexpr bool BPAIR = AGG16 && NQ == 8 && NE == 16;
   // epilogue warps that read one unit: all 8 when a unit holds several queries
   // (alternating queries) or two subtiles (one warp of a quarter per subtile),
   // else 4 (the two warps of a quarter take alternate units)
@@ -728,7 +731,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           const int64_t m = cur_g * C::NQ + qi;
           float wv = 0.0f;
           if (m < args.p.M) wv = C::BOUND ? args.wfold[m * 32 + h] : args.p.w[m * C::H + h];
-          if constexpr (C::PAIR) {
+          if constexpr (C::PAIR || C::BPAIR) {
             // this warp's r-th query goes to pair r/2, half r%2: [pair][h][2]
             if ((qi - qfirst) % QSTEP != 0) continue;
             const int r = (qi - qfirst) / QSTEP;
@@ -881,6 +884,23 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           uint64_t sc2[QPW / 2];
 #pragma unroll
           for (int c = 0; c < QPW / 2; ++c) sc2[c] = f2_pack(0.0f, 0.0f);
+          if constexpr (C::BPAIR) {
+            // weights stored (w_a[j], w_b[j]) adjacent: one 16-byte load gives two
+            // ready operand pairs
+            const float4* w4 = reinterpret_cast<const float4*>(sW);
+#pragma unroll
+            for (int j2 = 0; j2 < 8; ++j2) {
+              const float4 ww = w4[j2];
+              const int j = 2 * j2;
+              sc2[0] = f2_fma(f2_pack(ww.x, ww.y),
+                              f2_pack(fmaxf(__uint_as_float(v[0][j]), 0.0f), fmaxf(__uint_as_float(v[1][j]), 0.0f)),
+                              sc2[0]);
+              sc2[0] = f2_fma(f2_pack(ww.z, ww.w),
+                              f2_pack(fmaxf(__uint_as_float(v[0][j + 1]), 0.0f),
+                                      fmaxf(__uint_as_float(v[1][j + 1]), 0.0f)),
+                              sc2[0]);
+            }
+          } else {
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4) {
 #pragma unroll
@@ -897,6 +917,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
                                 sc2[c]);
               }
             }
+          }
           }
           float u[QPW];
 #pragma unroll
