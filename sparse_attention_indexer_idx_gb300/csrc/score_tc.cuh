@@ -166,13 +166,19 @@ struct TcCfg {
   // bf16 score tiles with at least 4 queries: an epilogue warp walks its queries
   // two at a time, both chains in one packed fma.rn.f32x2 per head
   static constexpr bool PAIR = (MODE != kBound) && (MODE != kFilter) && !FP8 && NQ >= 4;
-  // the bound over 16-vector blocks keeps its warp's two queries' folded weights
-  // interleaved the same way, (w_a[j], w_b[j]) adjacent, for the packed chain
-  static constexpr bool BPAIR = AGG16 && NQ == 8 && NE == 16;
-  // epilogue warps that read one unit: all 8 when a unit holds several queries
-  // (alternating queries) or two subtiles (one warp of a quarter per subtile),
-  // else 4 (the two warps of a quarter take alternate units)
-  static constexpr int EPT = (NQ > 1 || SUB > 1) ? NE : 4;
+  // the bound over 16-vector blocks keeps the folded weights of its warp's
+  // queries the same way, a pair's (w_a[j], w_b[j]) adjacent, for packed chains
+  static constexpr bool BPAIR = AGG16 && NQ == 8;
+  // epilogue warps in two sets that take alternate units: one query per unit
+  // (each set one warp per lane quarter), and the bound over 16-vector blocks
+  // (each set two warps per quarter, four rows each), where one warp's
+  // dependent chain from the TMEM load to the bitmap store would otherwise
+  // set the pace of every unit
+  static constexpr bool ALT = (NQ == 1 && SUB == 1) || (BPAIR && NE == 16);
+  // epilogue warps that read one unit: half of them with alternate units, else
+  // all (several queries per unit, alternating queries, or two subtiles, one
+  // warp of a quarter per subtile)
+  static constexpr int EPT = ALT ? NE / 2 : NE;
   static constexpr int NCONV = FP8 ? 1 : 0;   // warp that splits the query rows (FP8)
   // producer warps: gathered tiles take two (two tile rows per lane: the copies
   // of one warp alone could not keep the tensor core fed; a third or fourth
@@ -435,7 +441,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     }
     for (int i = 0; i < C::SACC; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 32 * C::EPT);
+      mbar_init(&acc_empty[i], C::EPT);          // one arrival per epilogue warp that read the stage
     }
     mbar_init(&drain_bar[0], 1);
     for (int i = 0; i < C::SIGR; ++i) {
@@ -698,9 +704,11 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;                   // epilogue warp index
     const int quarter = warp & 3;              // TMEM lanes this warp may read
-    const int qfirst = C::NQ > 1 ? (ew >> 2) : 0;   // first query of this warp in a tile
-    constexpr int QSTEP = C::NQ > 1 ? C::NE / 4 : 1;  // warps per lane quarter
-    const int tile_par = ew >> 2;              // one query per tile: the parity of the tiles this warp takes
+    // first query of this warp in a tile, and the warps per lane quarter that
+    // read one unit (its queries are qfirst, qfirst + QSTEP, ...)
+    const int qfirst = C::NQ > 1 ? ((ew % C::EPT) >> 2) : 0;
+    constexpr int QSTEP = C::NQ > 1 ? C::EPT / 4 : 1;
+    const int tile_par = ew / C::EPT;          // alternate units: the parity of the units this warp takes
     const int sub = C::SUB > 1 ? (ew >> 2) : 0;   // two subtiles per unit: the one this warp reads
     const int row_in_tile = quarter * 32 + lane;
     float* sW = sW_all + ew * C::NQ * C::NCOL;
@@ -711,6 +719,16 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     u.init(args, s);
     int64_t cur_g = -1;
     uint32_t nacc = 0, ngrp = 0;
+    // bound over 16-vector blocks: the length, coefficient and threshold of this
+    // warp's rows, copied to registers at each group change
+    constexpr int BQ = C::BPAIR ? C::NQ / QSTEP : 1;   // rows of a group this warp reads
+    int bq_len[BQ];
+    float bq_coef[BQ], bq_tau[BQ];
+#pragma unroll
+    for (int b = 0; b < BQ; ++b) {
+      bq_len[b] = 0;
+      bq_coef[b] = bq_tau[b] = 0.0f;
+    }
     while (u.valid()) {
       if (u.g != cur_g) {
         cur_g = u.g;
@@ -762,8 +780,17 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           if (C::BOUND || C::FILTER) sAux[4 * lane + 1] = m < args.p.M ? args.tau[m] : 0.0f;
         }
         __syncwarp();
+        if constexpr (C::BPAIR) {
+#pragma unroll
+          for (int b = 0; b < BQ; ++b) {
+            const int qi = qfirst + b * QSTEP;
+            bq_len[b] = sLen[qi];
+            bq_coef[b] = sAux[4 * qi];
+            bq_tau[b] = sAux[4 * qi + 1];
+          }
+        }
       }
-      if (C::NQ == 1 && C::SUB == 1 && (int)(nacc & 1) != tile_par) {
+      if (C::ALT && (int)(nacc & 1) != tile_par) {
         ++nacc;
         u.advance();
         continue;
@@ -776,6 +803,19 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       if (C::BOUND && args.seed_stride == 0 && key < args.p.max_key_len) sword = __ldg(args.seedbits + (key >> 5));
       float knorm = 0.0f;
       if (C::KN_GLOBAL && key < args.p.max_key_len) knorm = __ldg(args.knorm + key);
+      // per-row seed bitmaps: the words of this warp's rows, also before the wait
+      uint32_t sw2[BQ];
+#pragma unroll
+      for (int b = 0; b < BQ; ++b) sw2[b] = 0u;
+      if constexpr (C::BPAIR) {
+        if (args.seed_stride != 0) {
+#pragma unroll
+          for (int b = 0; b < BQ; ++b) {
+            const int64_t m = cur_g * C::NQ + qfirst + b * QSTEP;
+            if (key < bq_len[b]) sw2[b] = __ldg(args.seedbits + m * args.seed_stride + (key >> 5));
+          }
+        }
+      }
       bool got = mbar_wait(&acc_full[acc], (nacc / C::SACC) & 1, abort_flag);
       // the key-tile slot of this unit (bound: read below for ||k||, so the slot is
       // held until this warp releases it) and its scale slot (FP8)
@@ -863,44 +903,87 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         }
         bound_finish(qi, m, ub, v[31]);
       };
-      if constexpr (C::BOUND && !C::FP8 && C::NQ > 1 && (C::NQ == 4 * QSTEP || C::NQ == 2 * QSTEP)) {
+      if constexpr (C::BPAIR) {
+        // 16 retained vectors per query, rows qfirst + b * QSTEP of the group, taken
+        // in pairs (2c, 2c + 1): the halves of packed chains, two per pair (heads
+        // 2i and 2i + 1) so that each dependent sequence is 8 deep, then their sum.
+        // The summation order differs from the scalar chain by a few ulp, far
+        // inside the margin coef[m] already carries for the bf16 operands.
+        constexpr int NPR = BQ / 2;
+        const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
+        float chain[BQ];
+        uint32_t agg[BQ];
+#pragma unroll
+        for (int c = 0; c < NPR; ++c) {
+          // rows 2c and 2c + 1: columns 0..15 of each (one TMEM wait per pair, so
+          // that only one pair's values are live)
+          uint32_t v[2][32];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int q = qfirst + (2 * c + e) * QSTEP;
+            tmem_ld_32x32b_x16(tbase + (uint32_t)(q * C::NCOL), v[e]);
+            agg[2 * c + e] = tmem_ld_32x32b_x1(tbase + (uint32_t)(C::NQ * C::NCOL + q));
+          }
+          tmem_ld_wait();
+          // weights of pair c stored (w_a[h], w_b[h]) adjacent: one 16-byte load
+          // gives the operand pairs of heads j and j + 1
+          const float4* w4 = reinterpret_cast<const float4*>(sW + c * 2 * C::NCOL);
+          uint64_t se = f2_pack(0.0f, 0.0f), so = f2_pack(0.0f, 0.0f);
+#pragma unroll
+          for (int j2 = 0; j2 < 8; ++j2) {
+            const float4 ww = w4[j2];
+            const int j = 2 * j2;
+            se = f2_fma(f2_pack(ww.x, ww.y),
+                        f2_pack(fmaxf(__uint_as_float(v[0][j]), 0.0f), fmaxf(__uint_as_float(v[1][j]), 0.0f)), se);
+            so = f2_fma(f2_pack(ww.z, ww.w),
+                        f2_pack(fmaxf(__uint_as_float(v[0][j + 1]), 0.0f), fmaxf(__uint_as_float(v[1][j + 1]), 0.0f)),
+                        so);
+          }
+          float e0, e1, o0, o1;
+          f2_unpack(se, &e0, &e1);
+          f2_unpack(so, &o0, &o1);
+          chain[2 * c] = e0 + o0;
+          chain[2 * c + 1] = e1 + o1;
+        }
+        unsigned mask[BQ];
+#pragma unroll
+        for (int b = 0; b < BQ; ++b) {
+          float ub = chain[b] - fmaxf(__uint_as_float(agg[b]), 0.0f);
+          ub = __fmaf_rn(bq_coef[b], knorm, ub);
+          const uint32_t word = args.seed_stride ? sw2[b] : sword;
+          const bool is_cand = key < bq_len[b] && !((word >> (key & 31)) & 1u) && !(ub < bq_tau[b]);
+          mask[b] = __ballot_sync(0xffffffffu, is_cand);
+        }
+        // the warp's 32 keys are one bitmap word (key - lane is a multiple of 32)
+        const int64_t wd = key >> 5;
+        if (lane == 0 && wd < args.cb_stride) {
+#pragma unroll
+          for (int b = 0; b < BQ; ++b) {
+            const int64_t m = cur_g * C::NQ + qfirst + b * QSTEP;
+            if (m < args.p.M) args.candbits[m * args.cb_stride + wd] = mask[b];
+          }
+        }
+      } else if constexpr (C::BOUND && !C::FP8 && C::NQ > 1 && (C::NQ == 4 * QSTEP || C::NQ == 2 * QSTEP)) {
         constexpr int QPW = C::NQ / QSTEP;     // queries of this warp in a tile
         const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
-        if (C::AGG16 || args.R <= 16) {
+        if (args.R <= 16) {
           // at most 16 retained heads: columns 0..15 of each of this warp's four
-          // queries and their aggregates (column 31 of the query, or the group's
-          // aggregate block), one TMEM wait; two packed chains (queries 0|1 and 2|3
-          // of the warp in the halves of fma.rn.f32x2, each rounding as fmaf)
+          // queries and their aggregates (column 31 of the query), one TMEM wait;
+          // two packed chains (queries 0|1 and 2|3 of the warp in the halves of
+          // fma.rn.f32x2, each rounding as fmaf)
           uint32_t v[QPW][32], agg[QPW];
 #pragma unroll
           for (int b = 0; b < QPW; ++b) {
             const int q = qfirst + b * QSTEP;
             const uint32_t col = tbase + (uint32_t)(q * C::NCOLX);
             tmem_ld_32x32b_x16(col, v[b]);
-            agg[b] = tmem_ld_32x32b_x1(C::AGG16 ? tbase + (uint32_t)(C::NQ * C::NCOL + q) : col + 31);
+            agg[b] = tmem_ld_32x32b_x1(col + 31);
           }
           tmem_ld_wait();
           // queries 2c and 2c + 1 of this warp in the halves of chain c
           uint64_t sc2[QPW / 2];
 #pragma unroll
           for (int c = 0; c < QPW / 2; ++c) sc2[c] = f2_pack(0.0f, 0.0f);
-          if constexpr (C::BPAIR) {
-            // weights stored (w_a[j], w_b[j]) adjacent: one 16-byte load gives two
-            // ready operand pairs
-            const float4* w4 = reinterpret_cast<const float4*>(sW);
-#pragma unroll
-            for (int j2 = 0; j2 < 8; ++j2) {
-              const float4 ww = w4[j2];
-              const int j = 2 * j2;
-              sc2[0] = f2_fma(f2_pack(ww.x, ww.y),
-                              f2_pack(fmaxf(__uint_as_float(v[0][j]), 0.0f), fmaxf(__uint_as_float(v[1][j]), 0.0f)),
-                              sc2[0]);
-              sc2[0] = f2_fma(f2_pack(ww.z, ww.w),
-                              f2_pack(fmaxf(__uint_as_float(v[0][j + 1]), 0.0f),
-                                      fmaxf(__uint_as_float(v[1][j + 1]), 0.0f)),
-                              sc2[0]);
-            }
-          } else {
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4) {
 #pragma unroll
@@ -917,7 +1000,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
                                 sc2[c]);
               }
             }
-          }
           }
           float u[QPW];
 #pragma unroll
@@ -1072,7 +1154,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&acc_empty[acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
       ++nacc;
       u.advance();
     }
