@@ -423,7 +423,7 @@ __device__ __forceinline__ void warp_mma_rows(float (&d)[4], const uint16_t* a, 
 __host__ __device__ constexpr size_t plan_smem_bytes(int H, int n_sample) {
   return (size_t)2 * kPS * ((size_t)H + (size_t)((n_sample + 15) / 16 * 16) + 32) +
          (size_t)4 * ((size_t)H * 33 + 5 * (size_t)H + 128 + 32 + (size_t)((n_sample + 15) / 16 * 16) +
-                      3 * (size_t)H + 32 + 24);
+                      4 * (size_t)H + 33 + 24);
 }
 
 // One thread block per query (8 warps).  The three small contractions of the
@@ -454,7 +454,8 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   int* ret_pos = anchor + H;                     // H: position among retained, -1 if omitted
   int* act = ret_pos + H;                        // H: activation counts
   int* rlist = act + H;                          // 32: retained heads ascending
-  float* red = reinterpret_cast<float*>(rlist + 32);   // 2 x 8 partial sums, coef, pass count
+  int* a_list = rlist + 32;                      // H + 1: A's heads ascending, then their count
+  float* red = reinterpret_cast<float*>(a_list + H + 1);   // 2 x 8 partial sums, coef, pass count
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   constexpr int nw = kPlanThreads / 32;
@@ -509,24 +510,33 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     }
   }
   __syncthreads();
-  // retained heads: the R largest |w_h| ||q_h||, ties to the lower head
-  for (int h = tid; h < H; h += kPlanThreads) {
+  // retained heads: the R largest |w_h| ||q_h||, ties to the lower head (the
+  // rank of head h counted by one warp, its lanes over the other heads)
+  for (int h = wid; h < H; h += nw) {
     const float mh = mag[h];
-    int rank = 0;
-    for (int q = 0; q < H; ++q) {
+    unsigned rank = 0;
+    for (int q = lane; q < H; q += 32) {
       const float mq = mag[q];
-      rank += (mq > mh || (mq == mh && q < h)) ? 1 : 0;
+      rank += (mq > mh || (mq == mh && q < h)) ? 1u : 0u;
     }
-    ret_pos[h] = rank < R ? 1 : -1;
+    rank = __reduce_add_sync(0xffffffffu, rank);
+    if (lane == 0) ret_pos[h] = (int)rank < R ? 1 : -1;
   }
   __syncthreads();
-  if (tid == 0) {
+  if (wid == 0) {
+    // their list, ascending: one ballot per 32 heads places them
     int c = 0;
-    for (int h = 0; h < H; ++h)
-      if (ret_pos[h] > 0) {
-        rlist[c] = h;
-        ret_pos[h] = c++;
+    for (int h0 = 0; h0 < H; h0 += 32) {
+      const int h = h0 + lane;
+      const bool r = h < H && ret_pos[h] > 0;
+      const unsigned bal = __ballot_sync(0xffffffffu, r);
+      if (r) {
+        const int at = c + __popc(bal & ((1u << lane) - 1u));
+        rlist[at] = h;
+        ret_pos[h] = at;
       }
+      c += __popc(bal);
+    }
   }
   __syncthreads();
   // q_h . q_j for every head h and retained head j (section 3.1's beta needs them)
@@ -575,12 +585,15 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   }
   __syncthreads();
   // anchors of the omitted positive heads: the retained j with the smallest
-  // ||q_h - beta q_j||^2 = ||q_h||^2 - 2 beta q_h.q_j + beta^2 ||q_j||^2, ties to the lower j
-  for (int h = tid; h < H; h += kPlanThreads) {
+  // ||q_h - beta q_j||^2 = ||q_h||^2 - 2 beta q_h.q_j + beta^2 ||q_j||^2, ties to
+  // the lower j; four threads per head (retained positions r = sub (mod 4)),
+  // their bests combined in order of (r2, j)
+  for (int hb = 0; hb < H; hb += kPlanThreads / 4) {
+    const int h = hb + (tid >> 2), sub = tid & 3;
     int bj = -1;
     float bb = 0.0f, best = 0.0f;
-    if (ret_pos[h] < 0 && wq[h] > 0.0f) {
-      for (int r = 0; r < R; ++r) {
+    if (h < H && ret_pos[h] < 0 && wq[h] > 0.0f) {
+      for (int r = sub; r < R; r += 4) {
         const int j = rlist[r];
         const float dot = gram[h * 33 + r];
         const float b = qn2[j] > 0.0f ? fmaxf(0.0f, dot / qn2[j]) : 0.0f;
@@ -592,8 +605,20 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
         }
       }
     }
-    anchor[h] = bj;
-    beta[h] = bb;
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+      const float ob = __shfl_xor_sync(0xffffffffu, bb, o), obest = __shfl_xor_sync(0xffffffffu, best, o);
+      if (oj >= 0 && (bj < 0 || obest < best || (obest == best && oj < bj))) {
+        bj = oj;
+        bb = ob;
+        best = obest;
+      }
+    }
+    if (h < H && sub == 0) {
+      anchor[h] = bj;
+      beta[h] = bb;
+    }
   }
   __syncthreads();
   // residual norm of the chosen decomposition, computed directly and rounded up
@@ -616,14 +641,27 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     }
     if (lane == 0) dn[h] = dnh;
   }
-  // aggregate a_A = sum_{h in A} |w_h| q_h (heads in order), prepared rows
+  // aggregate a_A = sum_{h in A} |w_h| q_h (heads in order), prepared rows; A's
+  // heads listed first (ascending, one ballot per 32 heads)
   const float need_act = a.act_min * (float)ns;
+  if (wid == 0) {
+    int c = 0;
+    for (int h0 = 0; h0 < H; h0 += 32) {
+      const int h = h0 + lane;
+      const bool inA = h < H && ret_pos[h] < 0 && wq[h] < 0.0f && ns > 0 && (float)act[h] >= need_act;
+      const unsigned bal = __ballot_sync(0xffffffffu, inA);
+      if (inA) a_list[c + __popc(bal & ((1u << lane) - 1u))] = h;
+      c += __popc(bal);
+    }
+    if (lane == 0) a_list[H] = c;
+  }
+  __syncthreads();
+  const int nA = a_list[H];
   for (int d = tid; d < D; d += kPlanThreads) {
     float sa = 0.0f;
-    for (int h = 0; h < H; ++h) {
-      const float wh = wq[h];
-      if (ret_pos[h] < 0 && wh < 0.0f && ns > 0 && (float)act[h] >= need_act)
-        sa = __fmaf_rn(-wh, bf16_to_f(qs[h * kPS + d]), sa);
+    for (int i = 0; i < nA; ++i) {
+      const int h = a_list[i];
+      sa = __fmaf_rn(-wq[h], bf16_to_f(qs[h * kPS + d]), sa);
     }
     aggv[d] = sa;
     const uint16_t ab = f_to_bf16_rn(sa);
@@ -650,16 +688,21 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     a.plan_beta[m * H + h] = beta[h];
     a.plan_dn[m * H + h] = dn[h];
   }
-  for (int r = tid; r < kVec; r += kPlanThreads) {
+  // folded weights w'_r = w_j + sum of w_h beta_h over the heads anchored on
+  // j = rlist[r]: one warp per position, its lanes over the heads
+  for (int r = wid; r < kVec; r += nw) {
     float wf = 0.0f;
     if (r < R) {
       const int j = rlist[r];
-      wf = wq[j];
-      for (int h = 0; h < H; ++h)
+      for (int h = lane; h < H; h += 32)
         if (anchor[h] == j) wf = __fmaf_rn(wq[h], beta[h], wf);
+      for (int o = 16; o > 0; o >>= 1) wf += __shfl_xor_sync(0xffffffffu, wf, o);
+      wf += wq[j];
     }
-    wout[r] = wf;
-    wfs[r] = wf;
+    if (lane == 0) {
+      wout[r] = wf;
+      wfs[r] = wf;
+    }
   }
   // margin: bf16 rounding distance of a_A, plus gamma * (sum |w_h| ||q_h|| + ||a_A||)
   float e2 = 0.0f, a2 = 0.0f;
@@ -677,17 +720,23 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
     red[nw + wid] = a2;
   }
   __syncthreads();
-  if (tid == 0) {
+  if (wid == 0) {
+    // c = sum w_h ||d_h|| over the anchored heads and W = sum |w_h| ||q_h||, lanes
+    // over the heads
+    float c = 0.0f, W = 0.0f;
+    for (int h = lane; h < H; h += 32) {
+      const float wh = wq[h];
+      if (anchor[h] >= 0) c = __fmaf_rn(wh, dn[h], c);
+      W = __fmaf_rn(fabsf(wh), sqrtf(qn2[h]), W);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      c += __shfl_xor_sync(0xffffffffu, c, o);
+      W += __shfl_xor_sync(0xffffffffu, W, o);
+    }
     float E2 = 0.0f, A2 = 0.0f;
     for (int w = 0; w < nw; ++w) {
       E2 += red[w];
       A2 += red[nw + w];
-    }
-    float c = 0.0f, W = 0.0f;
-    for (int h = 0; h < H; ++h) {
-      const float wh = wq[h];
-      if (anchor[h] >= 0) c = __fmaf_rn(wh, dn[h], c);
-      W = __fmaf_rn(fabsf(wh), sqrtf(qn2[h]), W);
     }
     float margin = __fsqrt_ru(E2) * (1.0f + 0.0009765625f) + a.gamma * (W + sqrtf(A2) * 1.01f);
     if (p.k_dtype == IDX_FP8_E4M3) {
@@ -705,9 +754,11 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
       const float vmax = fmaxf(qmax, sqrtf(A2) * 1.01f + sqrtf(E2) * 1.01f);
       margin += 2.0f * sqrtf((float)D) * 7.62939453125e-6f * (sw * qmax + swf * vmax);
     }
-    a.coef[m] = (c + margin) * (1.0f + 1.0e-6f);
-    red[2 * nw] = (c + margin) * (1.0f + 1.0e-6f);   // coef, for the estimate below
-    reinterpret_cast<int*>(red)[2 * nw + 1] = 0;     // the estimate's pass count
+    if (lane == 0) {
+      a.coef[m] = (c + margin) * (1.0f + 1.0e-6f);
+      red[2 * nw] = (c + margin) * (1.0f + 1.0e-6f);   // coef, for the estimate below
+      reinterpret_cast<int*>(red)[2 * nw + 1] = 0;     // the estimate's pass count
+    }
   }
   // Overflow estimate: the bound U of n_sample evenly spaced visible keys of the
   // row against tau, from the same bf16 vectors the bound scan multiplies.  A
@@ -724,15 +775,21 @@ __global__ void __launch_bounds__(kPlanThreads) dosa_plan_kernel(PlanArgs a) {
   const int NEP = (ne + 15) / 16 * 16;
   block_load_rows_bf16(p.keys, p.k_dtype, ne, NEP, ks, [&](int si) { return off + ((int64_t)si * len) / ne; });
   __syncthreads();
-  for (int k = tid; k < ne; k += kPlanThreads) {
+  // ||k||^2 of the estimate keys: two threads per key (halves of the row, the
+  // partner's sum added by a shuffle)
+  for (int k0 = 0; k0 < ne; k0 += kPlanThreads / 2) {
+    const int k = k0 + (tid >> 1), half = tid & 1;
     float s2 = 0.0f;
-    for (int c = 0; c < D; c += 2) {
-      const uint32_t w = tile_word(ks, k, c);
-      const float x0 = bf16_to_f((uint16_t)w), x1 = bf16_to_f((uint16_t)(w >> 16));
-      s2 = __fmaf_rn(x0, x0, s2);
-      s2 = __fmaf_rn(x1, x1, s2);
+    if (k < ne) {
+      for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 2) {
+        const uint32_t w = tile_word(ks, k, c);
+        const float x0 = bf16_to_f((uint16_t)w), x1 = bf16_to_f((uint16_t)(w >> 16));
+        s2 = __fmaf_rn(x0, x0, s2);
+        s2 = __fmaf_rn(x1, x1, s2);
+      }
     }
-    kn2[k] = s2;
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+    if (k < ne && half == 0) kn2[k] = s2;
   }
   __syncthreads();
   const float tau = a.tau[m];
