@@ -75,6 +75,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 
 namespace idx {
@@ -603,6 +605,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
+      const uint64_t descA0 = smem_desc_sw128(smem_u32(sA)), descB0 = smem_desc_sw128(smem_u32(sB));
       TcUnits<C> u;
       u.init(args, s);
       int64_t cur_g = -1;
@@ -635,42 +638,55 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         // gathered tiles were written through the generic proxy (cp.async); make
         // them visible to the tensor core's async-proxy reads
         if (C::GATHER) fence_proxy_async_smem();
-        const uint32_t b0 = smem_u32(sB + cur_bs * C::B_BYTES);
+        // descriptors: the ring's base descriptors plus offsets (the start-address
+        // field is the byte address >> 4 and every offset stays inside shared
+        // memory, so adding offset >> 4 moves the operand), built once per unit
+        // so that each MMA costs one add per operand
+        const uint64_t bdesc = descB0 + (uint64_t)((cur_bs * C::B_BYTES) >> 4);
         // two independent chains: two units (IL), or the two subtiles of one unit
-        uint32_t a0[2], d[2];
+        uint64_t adesc[2];
+        uint32_t d[2];
         if (C::SUB > 1) {
           n = 2;
-          a0[0] = smem_u32(sA + (na % C::SA) * C::A_BYTES);
-          a0[1] = a0[0] + C::SUB_BYTES;
+          adesc[0] = descA0 + (uint64_t)(((na % C::SA) * C::A_BYTES) >> 4);
+          adesc[1] = adesc[0] + (uint64_t)(C::SUB_BYTES >> 4);
           d[0] = tmem_base + (uint32_t)((nacc % C::SACC) * C::ACC_STRIDE);
           d[1] = d[0] + C::N;
         } else {
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            a0[i] = smem_u32(sA + ((na + i) % C::SA) * C::A_BYTES);
+            adesc[i] = descA0 + (uint64_t)((((na + i) % C::SA) * C::A_BYTES) >> 4);
             d[i] = tmem_base + (uint32_t)(((nacc + i) % C::SACC) * C::ACC_STRIDE);
           }
         }
-        if constexpr (C::FP8) {
-          // e4m3 x e4m3, K = 32 per instruction: four steps of 32 bytes along the 128-byte rows
-          constexpr uint32_t idesc = idesc_f16(128, C::N, 0u);   // same layout; format 0 = E4M3 here
-          const uint32_t b8 = b0 + C::BQ_BYTES;
+        // the unit's MMAs, one chain or two interleaved (no branch between MMAs)
+        auto issue = [&](auto two) {
+          constexpr bool TWO = decltype(two)::value;
+          if constexpr (C::FP8) {
+            // e4m3 x e4m3, K = 32 per instruction: four steps of 32 bytes along the 128-byte rows
+            constexpr uint32_t idesc = idesc_f16(128, C::N, 0u);   // same layout; format 0 = E4M3 here
+            const uint64_t b8 = bdesc + (uint64_t)(C::BQ_BYTES >> 4);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t bd = smem_desc_sw128(b8 + k * 32);
-            tc_mma_f8(d[0], smem_desc_sw128(a0[0] + k * 32), bd, idesc, k > 0 ? 1u : 0u);
-            if (n > 1) tc_mma_f8(d[1], smem_desc_sw128(a0[1] + k * 32), bd, idesc, k > 0 ? 1u : 0u);
-          }
-        } else {
-          constexpr uint32_t idesc = idesc_f16(128, C::N, 1u);
+            for (int k = 0; k < 4; ++k) {
+              tc_mma_f8(d[0], adesc[0] + (uint64_t)(2 * k), b8 + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
+              if constexpr (TWO)
+                tc_mma_f8(d[1], adesc[1] + (uint64_t)(2 * k), b8 + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
+            }
+          } else {
+            constexpr uint32_t idesc = idesc_f16(128, C::N, 1u);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t ao = (k >> 2) * (C::A_BYTES / 2) + (k & 3) * 32;
-            const uint64_t bd = smem_desc_sw128(b0 + (k >> 2) * (C::BQ_BYTES / 2) + (k & 3) * 32);
-            tc_mma_f16(d[0], smem_desc_sw128(a0[0] + ao), bd, idesc, k > 0 ? 1u : 0u);
-            if (n > 1) tc_mma_f16(d[1], smem_desc_sw128(a0[1] + ao), bd, idesc, k > 0 ? 1u : 0u);
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t ao = (uint64_t)(((k >> 2) * (C::A_BYTES / 2) + (k & 3) * 32) >> 4);
+              const uint64_t bo = (uint64_t)(((k >> 2) * (C::BQ_BYTES / 2) + (k & 3) * 32) >> 4);
+              tc_mma_f16(d[0], adesc[0] + ao, bdesc + bo, idesc, k > 0 ? 1u : 0u);
+              if constexpr (TWO) tc_mma_f16(d[1], adesc[1] + ao, bdesc + bo, idesc, k > 0 ? 1u : 0u);
+            }
           }
-        }
+        };
+        if (n > 1)
+          issue(std::true_type{});
+        else
+          issue(std::false_type{});
         if (C::SUB > 1) n = 1;                 // one unit
         for (int i = 0; i < n; ++i) {
           tc_commit(&a_empty[(na + i) % C::SA]);
