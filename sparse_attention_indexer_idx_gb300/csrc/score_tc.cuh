@@ -188,7 +188,17 @@ struct TcCfg {
   // TMA tiles one
   static constexpr int NP = GATHER ? 2 : 1;
   static constexpr int RPL = 4 / NP;          // tile rows per producer lane
-  static constexpr int NTHREADS = 32 * (2 + NE + NCONV + (NP - 1));
+  // Two-query epilogue with its weights in registers: 2 x H per warp query pair
+  // (128 for H = 64), read from shared memory in every unit they took more of its
+  // bandwidth than the tensor core's operands.  The block then has twelve warps:
+  // warpgroup 0 holds the producer (warp 0), the MMA thread (warp 1), the second
+  // gather producer (warp 2) and an idle warp, and gives registers to the two
+  // epilogue warpgroups (warps 4..11) with setmaxnreg: 80 each against 208.
+  static constexpr bool WREG = PAIR;
+  static constexpr int EPI0 = WREG ? 4 : 2;                  // first epilogue warp
+  static constexpr int PROD1 = WREG ? 2 : 2 + NE + NCONV;    // second producer warp (NP = 2)
+  static constexpr int NTHREADS = WREG ? 32 * 12 : 32 * (2 + NE + NCONV + (NP - 1));
+  static constexpr int WG0_REGS = 80, EPI_REGS = 208;        // after setmaxnreg (WREG)
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + SA * A_BYTES;
@@ -210,6 +220,7 @@ struct TcCfg {
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA N");
   static_assert(MODE != kFilter || NQ == 1, "kFilter: one query per group");
   static_assert(SACC * ACC_STRIDE <= 512, "TMEM columns");
+  static_assert(!WREG || (NE == 8 && NP <= 2 && NCONV == 0), "register-weight layout: warpgroups 0, 1, 2");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -468,12 +479,19 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const TcSched s = *sched;
+  if constexpr (C::WREG) {
+    // the launch's registers (checked on the host: 168 a thread) move from
+    // warpgroup 0 to the epilogue warpgroups (their increase opens the epilogue
+    // branch, so that the compiler allocates that code for it); each warpgroup
+    // executes its instruction together
+    if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::WG0_REGS) : "memory");
+  }
 
-  if (warp == 0 || (C::NP > 1 && warp >= 2 + C::NE + C::NCONV)) {
+  if (warp == 0 || (C::NP > 1 && warp == C::PROD1)) {
     // ------------------------------------------------------------ producer
     // producer warp pidx (warp 0 is producer 0, the only one that loads query
     // tiles) copies tile rows RPL (32 pidx + lane) .. + RPL - 1
-    const int pidx = warp == 0 ? 0 : warp - (2 + C::NE + C::NCONV) + 1;
+    const int pidx = warp == 0 ? 0 : 1;
     const int rbase = C::RPL * (32 * pidx + lane);
     TcUnits<C> u;
     u.init(args, s);
@@ -716,9 +734,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         }
       }
     }
-  } else if (warp >= 2 && warp < 2 + C::NE) {
+  } else if (warp >= C::EPI0 && warp < C::EPI0 + C::NE) {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;                   // epilogue warp index
+    if constexpr (C::WREG) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::EPI_REGS) : "memory");
+    const int ew = warp - C::EPI0;             // epilogue warp index
     const int quarter = warp & 3;              // TMEM lanes this warp may read
     // first query of this warp in a tile, and the warps per lane quarter that
     // read one unit (its queries are qfirst, qfirst + QSTEP, ...)
@@ -745,6 +764,12 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       bq_len[b] = 0;
       bq_coef[b] = bq_tau[b] = 0.0f;
     }
+    // two-query epilogue: this warp's query pairs' weights, (w_a[h], w_b[h]) packed
+    constexpr int PPW = C::PAIR ? C::NQ / QSTEP / 2 : 1;   // query pairs of this warp
+    static_assert(!C::PAIR || C::H % 16 == 0, "two-query epilogue: whole TMEM loads");
+    uint64_t wreg[C::PAIR ? PPW * C::H : 1];
+#pragma unroll
+    for (int i = 0; i < (C::PAIR ? PPW * C::H : 1); ++i) wreg[i] = 0;
     while (u.valid()) {
       if (u.g != cur_g) {
         cur_g = u.g;
@@ -796,6 +821,11 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           if (C::BOUND || C::FILTER) sAux[4 * lane + 1] = m < args.p.M ? args.tau[m] : 0.0f;
         }
         __syncwarp();
+        if constexpr (C::PAIR) {
+#pragma unroll
+          for (int i = 0; i < PPW * C::H; ++i)
+            wreg[i] = reinterpret_cast<const uint64_t*>(sW + (i / C::H) * 2 * C::NCOL)[i % C::H];
+        }
         if constexpr (C::BPAIR) {
 #pragma unroll
           for (int b = 0; b < BQ; ++b) {
@@ -1043,40 +1073,27 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           }
         }
       } else if constexpr (C::PAIR) {
-        // queries qi and qi + QSTEP, chains packed (a in the low half, b in the high half)
-#pragma unroll 1
-        for (int qi = qfirst, r = 0; qi < C::NQ; qi += 2 * QSTEP, r += 2) {
-          const int qb = qi + QSTEP;
+        // queries qi and qi + QSTEP, chains packed (a in the low half, b in the
+        // high half), the weight pairs from registers (loaded at the group change)
+        const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
+#pragma unroll
+        for (int pp = 0; pp < PPW; ++pp) {
+          const int qi = qfirst + 2 * pp * QSTEP, qb = qi + QSTEP;
           const int64_t ma = cur_g * C::NQ + qi, mb = cur_g * C::NQ + qb;
           if (ma >= args.p.M) break;
-          const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
           const uint32_t ta = tbase + (uint32_t)(qi * C::NCOLX), tb = tbase + (uint32_t)(qb * C::NCOLX);
-          const float* w2 = sW + (r >> 1) * 2 * C::NCOL;
-          constexpr int NCH = (C::H + 31) / 32;
-          constexpr int CW = C::H < 32 ? C::H : 32;
+          constexpr int CW = 16;                        // heads per TMEM wait
           uint64_t s2 = 0;
 #pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            uint32_t va[32], vb[32];
-            if (C::H >= 32) {
-              tmem_ld_32x32b_x32(ta + 32 * c, va);
-              tmem_ld_32x32b_x32(tb + 32 * c, vb);
-            } else {
-              tmem_ld_32x32b_x16(ta, va);
-              tmem_ld_32x32b_x16(tb, vb);
-            }
+          for (int c = 0; c < C::H / CW; ++c) {
+            uint32_t va[32], vb[32];   // columns 0..CW-1 used
+            tmem_ld_32x32b_x16(ta + CW * c, va);
+            tmem_ld_32x32b_x16(tb + CW * c, vb);
             tmem_ld_wait();
-            const float4* w4 = reinterpret_cast<const float4*>(w2 + 2 * 32 * c);
 #pragma unroll
-            for (int j2 = 0; j2 < CW / 2; ++j2) {
-              const float4 ww = w4[j2];      // (wa[h], wb[h], wa[h+1], wb[h+1]), h = 32c + 2 j2
-              const int j = 2 * j2;
-              s2 = f2_fma(f2_pack(ww.x, ww.y),
+            for (int j = 0; j < CW; ++j)
+              s2 = f2_fma(wreg[pp * C::H + CW * c + j],
                           f2_pack(fmaxf(__uint_as_float(va[j]), 0.0f), fmaxf(__uint_as_float(vb[j]), 0.0f)), s2);
-              s2 = f2_fma(f2_pack(ww.z, ww.w),
-                          f2_pack(fmaxf(__uint_as_float(va[j + 1]), 0.0f), fmaxf(__uint_as_float(vb[j + 1]), 0.0f)),
-                          s2);
-            }
           }
           float sa, sb;
           f2_unpack(s2, &sa, &sb);
@@ -1270,6 +1287,14 @@ cudaError_t launch_tc(const TcArgs& a_in, cudaStream_t st) {
   if (!ok) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if constexpr (C::WREG) {
+    // setmaxnreg moves registers within the block: the epilogue warpgroups'
+    // increase must not exceed what warpgroup 0 gives back from the launch count
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, score_tc_kernel<C>);
+    if (e != cudaSuccess) return e;
+    if (4 * C::WG0_REGS + 8 * C::EPI_REGS > 12 * fa.numRegs || fa.numRegs > C::EPI_REGS) return cudaErrorInvalidConfiguration;
+  }
   score_tc_kernel<C><<<sm_count(), C::NTHREADS, C::SMEM_BYTES, st>>>(tk, tq, a);
   return cudaGetLastError();
 }
