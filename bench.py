@@ -168,12 +168,12 @@ def make_workload(name: str, rank: int, rows=None):
 LARGE_INPUTS = ("decode", "ragged_fp8", "decode_prior", "ragged_fp8_prior")
 
 # dram__bytes_read.sum + dram__bytes_write.sum of the score kernel per full launch: one ncu
-# capture of a smaller batch of the same workload, scaled by the keys processed (traffic grows
-# in proportion).  Valid for the kernel as built with this file; None where not captured.
-SCORE_TRAFFIC = {"decode": 550.9e6, "ragged_fp8": 1159.0e6}
-# the same counters for one bt_max_kernel launch on the full block_select workload (one
-# ncu capture of the kernel as built with this file; the fp16 keys, 33.5 MB, dominate)
-BLOCK_MAX_TRAFFIC = 37.60e6
+# capture (a single pass) of the full-size workload, the kernel as built with this file
+# (profiles/dram_traffic_full_size.md).  None where not captured.
+SCORE_TRAFFIC = {"decode": 547.73e6, "ragged_fp8": 1158.98e6, "prefill": 1083.81e6}
+# the same counters for one bt_max_kernel launch on the full block_select workload (the
+# fp16 keys, 33.5 MB, dominate)
+BLOCK_MAX_TRAFFIC = 37.66e6
 
 WORKLOAD_TEXT = {
     "decode": "decode indexer bf16: 64 rows x 32768 own keys, H32 D128, top-2048, witness_merge S=16 (5% padding)",
