@@ -639,6 +639,7 @@ constexpr uint32_t kTrBucketMax = 256;      // a larger bucket: heavy ties
 constexpr int TR_DST = TR_KMAX + 256;       // scatter space: the first K places plus one bucket
 constexpr int TR_NB = 4096;                 // buckets of the sort
 constexpr int TR_V = 4;                     // 4-score vectors per thread, round and register buffer
+constexpr int TR_PD = 2;                    // rounds prefetched into L2 ahead of the loads
 constexpr int TR_NS = 1024;                 // threshold samples
 
 struct TrShared {
@@ -1064,12 +1065,27 @@ __global__ void __launch_bounds__(TR_NT, 2)
     }
   };
   constexpr int kStep = 4 * TR_NT * TR_V;
+  // The register buffers hold two rounds (64 KB a block); an L2 prefetch of the
+  // rounds TR_PD ahead (one bulk request by thread 0 per round, aligned rows
+  // only) lets those loads find their data in L2.  Each request covers the
+  // round's scores rounded up to 16 bytes, inside the row's storage (ld is a
+  // multiple of 4 when vec4).
+  auto prefetch_round = [&](int c0p) {
+    if (vec4 && tid == 0 && c0p < n) {
+      const int cnt = n - c0p < kStep ? n - c0p : kStep;
+      l2_prefetch_bulk(row + c0p, (uint32_t)(((cnt + 3) & ~3) * 4));
+    }
+  };
+#pragma unroll
+  for (int r = 1; r <= TR_PD; ++r) prefetch_round(r * kStep);
   float4 ba[TR_V], bb[TR_V];
   load_round(ba, 0);
 #pragma unroll 1
   for (int c0 = 0; c0 < n; c0 += 2 * kStep) {
+    prefetch_round(c0 + (TR_PD + 1) * kStep);
     load_round(bb, c0 + kStep);
     process_round(ba, c0);
+    prefetch_round(c0 + (TR_PD + 2) * kStep);
     load_round(ba, c0 + 2 * kStep);
     process_round(bb, c0 + kStep);
   }
