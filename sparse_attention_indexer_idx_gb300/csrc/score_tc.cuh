@@ -629,6 +629,69 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       int64_t cur_g = -1;
       int cur_bs = 0;
       uint32_t na = 0, nb = 0, nacc = 0;
+      if constexpr (C::IL == 1 && C::SUB == 1) {
+        // One unit per step: ring slots and accumulator stages as 32-bit counters
+        // with their phase bits, the (group, tile) walk of TcUnits inline, one
+        // descriptor add per operand and unit -- the issuing thread's own work
+        // between two units is what the tensor core waits for.
+        uint32_t slot = 0, a_ph = 0, st = 0, e_ph = 1;
+        int64_t g = u.g, t = u.t, left = u.left, tiles_g = u.tiles_g;
+        while (left > 0) {
+          if (g != cur_g) {
+            cur_g = g;
+            cur_bs = nb % C::SB;
+            if (!mbar_wait(&b_full[cur_bs], (nb / C::SB) & 1, abort_flag)) break;
+            ++nb;
+          }
+          if (!mbar_wait(&a_full[slot], a_ph, abort_flag)) break;
+          if (!mbar_wait(&acc_empty[st], e_ph, abort_flag)) break;
+          tc_fence_after();
+          // gathered tiles were written through the generic proxy (cp.async)
+          if (C::GATHER) fence_proxy_async_smem();
+          const uint64_t adesc = descA0 + (uint64_t)((slot * (uint32_t)C::A_BYTES) >> 4);
+          const uint64_t bdesc = descB0 + (uint64_t)((cur_bs * C::B_BYTES) >> 4);
+          const uint32_t d = tmem_base + st * (uint32_t)C::ACC_STRIDE;
+          if constexpr (C::FP8) {
+            constexpr uint32_t idesc = idesc_f16(128, C::N, 0u);
+            const uint64_t b8 = bdesc + (uint64_t)(C::BQ_BYTES >> 4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc_mma_f8(d, adesc + (uint64_t)(2 * k), b8 + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
+          } else {
+            constexpr uint32_t idesc = idesc_f16(128, C::N, 1u);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t ao = (uint64_t)(((k >> 2) * (C::A_BYTES / 2) + (k & 3) * 32) >> 4);
+              const uint64_t bo = (uint64_t)(((k >> 2) * (C::BQ_BYTES / 2) + (k & 3) * 32) >> 4);
+              tc_mma_f16(d, adesc + ao, bdesc + bo, idesc, k > 0 ? 1u : 0u);
+            }
+          }
+          tc_commit(&a_empty[slot]);
+          tc_commit(&acc_full[st]);
+          ++na;
+          ++nacc;
+          if (++slot == (uint32_t)C::SA) {
+            slot = 0;
+            a_ph ^= 1u;
+          }
+          if (++st == (uint32_t)C::SACC) {
+            st = 0;
+            e_ph ^= 1u;
+          }
+          // the next unit (groups without tiles are skipped)
+          const int64_t g_this = g;
+          if (--left > 0) {
+            ++t;
+            while (t >= tiles_g) {
+              ++g;
+              t = 0;
+              tiles_g = tc_group_tiles<C>(args, g);
+            }
+          }
+          if (left <= 0 || g != g_this) tc_commit(&b_empty[cur_bs]);
+        }
+        u.left = 0;   // the general loop below does not run
+      }
       while (u.valid()) {
         if (u.g != cur_g) {
           cur_g = u.g;
