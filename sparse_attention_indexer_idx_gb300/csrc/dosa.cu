@@ -870,34 +870,40 @@ struct GroupRecs {
 // below tau become -inf); also the fallback mask and the survivor count.  With
 // the shared stream the row's own candidates are already in place at K.., and
 // the group records that the row can see, that are not its seeds and whose
-// score reaches tau follow them (in list order).
+// score reaches tau follow them (in list order).  One warp per row (eight rows
+// a block): the records are compacted 32 at a time by a ballot, in list order,
+// with four such steps' loads in flight per lane -- no block-wide scans.
 constexpr int kMergeThreads = 256;
+constexpr int kMergeRows = kMergeThreads / 32;
 __global__ void __launch_bounds__(kMergeThreads) merge_rows_kernel(
     int64_t M, int K, int64_t cap, const int32_t* stop_ids, const float* stop_sc, const int32_t* cand,
     const int32_t* cand_n, const float* cand_sc, const float* tau, const int32_t* status, GroupRecs gr, float* mrg_sc,
     int32_t* mrg_id, int32_t* mrg_len, int32_t* fbmask, unsigned long long* survivors) {
-  __shared__ int32_t s_wcnt[kMergeThreads / 32];
-  const int64_t m = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * kMergeRows + (threadIdx.x >> 5);
+  if (m >= M) return;
   const int64_t ld = K + cap;
   const bool ok = status[m] == 0;
-  if (threadIdx.x == 0) fbmask[m] = ok ? 0 : 1;
+  if (lane == 0) fbmask[m] = ok ? 0 : 1;
   if (!ok) {
-    if (threadIdx.x == 0) mrg_len[m] = 0;
+    if (lane == 0) mrg_len[m] = 0;
     return;
   }
-  for (int j = threadIdx.x; j < K; j += blockDim.x) {
-    mrg_sc[m * ld + j] = stop_sc[m * K + j];
-    mrg_id[m * ld + j] = stop_ids[m * K + j];
+  float* osc = mrg_sc + m * ld;
+  int32_t* oid = mrg_id + m * ld;
+  for (int j = lane; j < K; j += 32) {
+    osc[j] = stop_sc[m * K + j];
+    oid[j] = stop_ids[m * K + j];
   }
   const float t = tau[m];
   const int n = cand_n[m];
-  unsigned long long surv = 0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const float s = cand_sc[m * cap + i];
-    const bool keep = s >= t;
-    surv += keep ? 1ull : 0ull;
-    mrg_sc[m * ld + K + i] = keep ? s : -__int_as_float(0x7f800000);
-    if (!gr.glist) mrg_id[m * ld + K + i] = cand[m * cap + i];
+  uint32_t surv = 0;
+  for (int i = lane; i < n; i += 32) {
+    const float sv = cand_sc[m * cap + i];
+    const bool keep = sv >= t;
+    surv += keep ? 1u : 0u;
+    osc[K + i] = keep ? sv : -__int_as_float(0x7f800000);
+    if (!gr.glist) oid[K + i] = cand[m * cap + i];
   }
   int64_t fill = n;
   if (gr.glist) {
@@ -907,67 +913,47 @@ __global__ void __launch_bounds__(kMergeThreads) merge_rows_kernel(
     int64_t off;
     int len;
     row_extent(gr.p, m, &off, &len);
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const uint32_t* sbits = gr.seedbits + (gr.seed_stride ? m * gr.seed_stride : 0);
-    // rounds of kMergeThreads x 8 records, thread t taking records 8 t .. 8 t + 7
-    // of the round (their loads in flight together); one block scan places them
-    constexpr int RPT = 8;
-    for (int i0 = 0; i0 < gn; i0 += kMergeThreads * RPT) {
-      int32_t id[RPT];
-      float sv[RPT];
+    const int32_t* gl = gr.glist + g * gr.capg;
+    const float* gs = gr.gsc + m * gr.capg;
+    const uint32_t lt = (1u << lane) - 1u;
+    constexpr int ST = 4;   // ballot steps per round
+    for (int i0 = 0; i0 < gn; i0 += 32 * ST) {
+      int32_t id[ST];
+      float sv[ST];
 #pragma unroll
-      for (int u = 0; u < RPT; ++u) {
-        const int i = i0 + RPT * (int)threadIdx.x + u;
-        id[u] = i < gn ? gr.glist[g * gr.capg + i] : 0x7fffffff;
-        sv[u] = i < gn ? gr.gsc[m * gr.capg + i] : 0.0f;
+      for (int u = 0; u < ST; ++u) {
+        const int i = i0 + 32 * u + lane;
+        id[u] = i < gn ? gl[i] : 0x7fffffff;
+        sv[u] = i < gn ? gs[i] : 0.0f;
       }
-      uint32_t keepm = 0;
+      uint32_t word[ST];
 #pragma unroll
-      for (int u = 0; u < RPT; ++u) {
-        if (id[u] < len && sv[u] >= t) {
-          const uint32_t word = sbits[id[u] >> 5];
-          if (!((word >> (id[u] & 31)) & 1u)) keepm |= 1u << u;
-        }
-      }
-      const int c = __popc(keepm);
-      // exclusive scan of c over the block, in thread order
-      int incl = c;
+      for (int u = 0; u < ST; ++u) word[u] = id[u] < len ? sbits[id[u] >> 5] : 0xffffffffu;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (lane == 31) s_wcnt[wid] = incl;
-      __syncthreads();
-      int64_t pos = fill + incl - c;
-      int tot = 0;
-      for (int w = 0; w < kMergeThreads / 32; ++w) {
-        if (w < wid) pos += s_wcnt[w];
-        tot += s_wcnt[w];
-      }
-#pragma unroll
-      for (int u = 0; u < RPT; ++u) {
-        if ((keepm >> u) & 1u) {
+      for (int u = 0; u < ST; ++u) {
+        const bool keep = id[u] < len && sv[u] >= t && !((word[u] >> (id[u] & 31)) & 1u);
+        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          const int64_t pos = fill + __popc(bal & lt);
           if (pos < cap) {
-            mrg_id[m * ld + K + pos] = id[u];
-            mrg_sc[m * ld + K + pos] = sv[u];
+            oid[K + pos] = id[u];
+            osc[K + pos] = sv[u];
           }
-          ++pos;
         }
+        fill += __popc(bal);
       }
-      fill += tot;
-      __syncthreads();
     }
-    if (threadIdx.x == 0) surv += (unsigned long long)(fill - n);
+    if (lane == 0) surv += (uint32_t)(fill - n);
   }
-  if (threadIdx.x == 0) {
+  if (lane == 0) {
     // more records than places can only come from a bound that failed: the row then takes the unpruned path
     const bool over = fill > cap;
     mrg_len[m] = over ? 0 : (int32_t)(K + fill);
     if (over) fbmask[m] = 1;
   }
   for (int o = 16; o > 0; o >>= 1) surv += __shfl_xor_sync(0xffffffffu, surv, o);
-  if ((threadIdx.x & 31) == 0 && surv) atomicAdd(survivors, surv);
+  if (lane == 0 && surv) atomicAdd(survivors, (unsigned long long)surv);
 }
 
 // ||k|| of every key of one shared key sequence (e4m3 codes for FP8 keys),
@@ -1508,7 +1494,8 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
     DOSA_CHECK(launch_score_gather(p, w.mrg_id + K, w.solo_n, mld, w.cand_sc, s.cap, w.active, st));
     DOSA_CHECK(launch_score_group(p, w.glist, w.gcnt, capg, w.gsc, capg, st));
     gr = GroupRecs{w.glist, w.gcnt, w.gsc, capg, w.bits, s.shared_seeds ? 0 : s.W, p};
-    merge_rows_kernel<<<(unsigned)M, kMergeThreads, 0, st>>>(M, K, s.cap, w.stop_ids, w.stop_sc, nullptr, w.solo_n,
+    merge_rows_kernel<<<(unsigned)((M + kMergeRows - 1) / kMergeRows), kMergeThreads, 0, st>>>(
+        M, K, s.cap, w.stop_ids, w.stop_sc, nullptr, w.solo_n,
                                                               w.cand_sc, w.tau, w.status, gr, w.mrg_sc, w.mrg_id,
                                                               w.mrg_len, w.fbmask,
                                                               stats ? &stats->survivors : w.surv);
@@ -1517,7 +1504,8 @@ cudaError_t launch_dosa(const idx_problem& p, int K, const dosa_params& dp, cons
                                                                w.cand_cnt, w.cand_n);
     DOSA_CHECK(cudaGetLastError());
     DOSA_CHECK(launch_score_gather(p, w.cand, w.cand_n, s.cap, w.cand_sc, s.cap, w.active, st));
-    merge_rows_kernel<<<(unsigned)M, kMergeThreads, 0, st>>>(M, K, s.cap, w.stop_ids, w.stop_sc, w.cand, w.cand_n,
+    merge_rows_kernel<<<(unsigned)((M + kMergeRows - 1) / kMergeRows), kMergeThreads, 0, st>>>(
+        M, K, s.cap, w.stop_ids, w.stop_sc, w.cand, w.cand_n,
                                                               w.cand_sc, w.tau, w.status, gr, w.mrg_sc, w.mrg_id,
                                                               w.mrg_len, w.fbmask,
                                                               stats ? &stats->survivors : w.surv);
