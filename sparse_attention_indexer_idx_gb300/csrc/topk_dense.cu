@@ -1027,15 +1027,27 @@ __global__ void __launch_bounds__(TR_NT, 2)
       buf[v] = f;
     }
   };
+  constexpr int kStep = 4 * TR_NT * TR_V;
   auto process_round = [&](const float4 (&buf)[TR_V], int c0) {
     uint32_t kmask = 0;                        // bit 4 v + e: score e of vector v is kept
+    if (c0 + kStep <= n && !keep_all) {
+      // a whole round of visible scores (all rounds but a row's last): one
+      // compare per score
 #pragma unroll
-    for (int v = 0; v < TR_V; ++v) {
-      const int i0 = c0 + 4 * (v * TR_NT + tid);
-      const float x[4] = {buf[v].x, buf[v].y, buf[v].z, buf[v].w};
+      for (int v = 0; v < TR_V; ++v) {
+        const float x[4] = {buf[v].x, buf[v].y, buf[v].z, buf[v].w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (i0 + e < n && (keep_all || x[e] >= Tf)) kmask |= 1u << (4 * v + e);
+        for (int e = 0; e < 4; ++e) kmask |= (x[e] >= Tf ? 1u : 0u) << (4 * v + e);
+      }
+    } else {
+#pragma unroll
+      for (int v = 0; v < TR_V; ++v) {
+        const int i0 = c0 + 4 * (v * TR_NT + tid);
+        const float x[4] = {buf[v].x, buf[v].y, buf[v].z, buf[v].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (i0 + e < n && (keep_all || x[e] >= Tf)) kmask |= 1u << (4 * v + e);
+      }
     }
     const uint32_t c = (uint32_t)__popc(kmask);
     uint32_t incl = c;
@@ -1064,7 +1076,6 @@ __global__ void __launch_bounds__(TR_NT, 2)
       }
     }
   };
-  constexpr int kStep = 4 * TR_NT * TR_V;
   // The register buffers hold two rounds (64 KB a block); an L2 prefetch of the
   // rounds TR_PD ahead (one bulk request by thread 0 per round, aligned rows
   // only) lets those loads find their data in L2.  Each request covers the
