@@ -170,7 +170,7 @@ LARGE_INPUTS = ("decode", "ragged_fp8", "decode_prior", "ragged_fp8_prior")
 # dram__bytes_read.sum + dram__bytes_write.sum of the score kernel per full launch: one ncu
 # capture (a single pass) of the full-size workload, the kernel as built with this file
 # (profiles/dram_traffic_full_size.md).  None where not captured.
-SCORE_TRAFFIC = {"decode": 547.73e6, "ragged_fp8": 1158.98e6, "prefill": 1083.81e6}
+SCORE_TRAFFIC = {"decode": 547.86e6, "ragged_fp8": 1158.60e6, "prefill": 1084.21e6}
 # the same counters for one bt_max_kernel launch on the full block_select workload (the
 # fp16 keys, 33.5 MB, dominate)
 BLOCK_MAX_TRAFFIC = 37.66e6
