@@ -872,7 +872,7 @@ struct GroupRecs {
 // the group records that the row can see, that are not its seeds and whose
 // score reaches tau follow them (in list order).  One warp per row (eight rows
 // a block): the records are compacted 32 at a time by a ballot, in list order,
-// with four such steps' loads in flight per lane -- no block-wide scans.
+// with eight such steps' loads in flight per lane -- no block-wide scans.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeRows = kMergeThreads / 32;
 __global__ void __launch_bounds__(kMergeThreads) merge_rows_kernel(
@@ -891,9 +891,19 @@ __global__ void __launch_bounds__(kMergeThreads) merge_rows_kernel(
   }
   float* osc = mrg_sc + m * ld;
   int32_t* oid = mrg_id + m * ld;
-  for (int j = lane; j < K; j += 32) {
-    osc[j] = stop_sc[m * K + j];
-    oid[j] = stop_ids[m * K + j];
+  if ((K & 3) == 0 && (ld & 3) == 0) {
+    // 16-byte copies (rows of K and of ld elements start 16-byte aligned)
+    const float4* ss = reinterpret_cast<const float4*>(stop_sc + m * K);
+    const int4* si = reinterpret_cast<const int4*>(stop_ids + m * K);
+    for (int j = lane; j < K / 4; j += 32) {
+      reinterpret_cast<float4*>(osc)[j] = ss[j];
+      reinterpret_cast<int4*>(oid)[j] = si[j];
+    }
+  } else {
+    for (int j = lane; j < K; j += 32) {
+      osc[j] = stop_sc[m * K + j];
+      oid[j] = stop_ids[m * K + j];
+    }
   }
   const float t = tau[m];
   const int n = cand_n[m];
@@ -917,7 +927,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_rows_kernel(
     const int32_t* gl = gr.glist + g * gr.capg;
     const float* gs = gr.gsc + m * gr.capg;
     const uint32_t lt = (1u << lane) - 1u;
-    constexpr int ST = 4;   // ballot steps per round
+    constexpr int ST = 8;   // ballot steps per round
     for (int i0 = 0; i0 < gn; i0 += 32 * ST) {
       int32_t id[ST];
       float sv[ST];
