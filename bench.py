@@ -318,15 +318,19 @@ class DosaStep:
             self.B.dosa_topk(self.p, self.K, self.dp, self.ids, self.sc, self.ws, stats=self.stats, row_status=rs)
         torch.cuda.synchronize()
         st = self.stats.cpu().tolist()
-        nonseed = max(1, st[0] - st[1])
         rs = rs.cpu().numpy()
+        # rates over the non-seed pairs of the rows that ran the bound scan (row_status 0,
+        # or 2: candidates over capacity), the seed pairs taken as evenly spread over the rows
+        scanned = (rs == 0) | (rs == 2)
+        lens = np.asarray(self.wp.key_len, dtype=np.int64)
+        nonseed = float(lens[scanned].sum()) - float(st[1]) * float(scanned.sum()) / max(1, self.wp.M)
+        rate = (lambda x: x / nonseed) if nonseed > 0 else (lambda x: None)
         out = {"pairs": st[0], "seed_pairs": st[1], "candidates": st[2], "survivors": st[3],
                "fallback_rows": st[4], "skipped_rows": st[5], "group_keys": st[6], "solo_keys": st[7],
                "group_stream": int(self.dp.group_stream),
                "rows_pruned": int((rs == 0).sum()), "rows": int(self.wp.M),
-               # rates over all non-seed pairs: only meaningful when no row skipped the scan
-               "candidate_rate": st[2] / nonseed if st[5] == 0 else None,
-               "survival_rate": st[3] / nonseed if st[5] == 0 else None}
+               "candidate_rate": rate(st[2]), "survival_rate": rate(st[3]),
+               "rates_over": "non-seed pairs of the rows that ran the bound scan"}
         if ref_ids is not None:
             out["identical_to_unpruned"] = bool(torch.equal(self.ids, ref_ids) and
                                                torch.equal(self.sc.view(torch.int32), ref_sc.view(torch.int32)))
