@@ -221,6 +221,7 @@ struct TcCfg {
   static_assert(MODE != kFilter || NQ == 1, "kFilter: one query per group");
   static_assert(SACC * ACC_STRIDE <= 512, "TMEM columns");
   static_assert(!WREG || (NE == 8 && NP <= 2 && NCONV == 0), "register-weight layout: warpgroups 0, 1, 2");
+  static_assert(!BPAIR || (ALT && SUB == 1 && SACC >= 2), "bound over 16-vector blocks: every other unit, one subtile");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -817,23 +818,160 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     u.init(args, s);
     int64_t cur_g = -1;
     uint32_t nacc = 0, ngrp = 0;
-    // bound over 16-vector blocks: the length, coefficient and threshold of this
-    // warp's rows, copied to registers at each group change
-    constexpr int BQ = C::BPAIR ? C::NQ / QSTEP : 1;   // rows of a group this warp reads
-    int bq_len[BQ];
-    float bq_coef[BQ], bq_tau[BQ];
-#pragma unroll
-    for (int b = 0; b < BQ; ++b) {
-      bq_len[b] = 0;
-      bq_coef[b] = bq_tau[b] = 0.0f;
-    }
     // two-query epilogue: this warp's query pairs' weights, (w_a[h], w_b[h]) packed
     constexpr int PPW = C::PAIR ? C::NQ / QSTEP / 2 : 1;   // query pairs of this warp
     static_assert(!C::PAIR || C::H % 16 == 0, "two-query epilogue: whole TMEM loads");
     uint64_t wreg[C::PAIR ? PPW * C::H : 1];
 #pragma unroll
     for (int i = 0; i < (C::PAIR ? PPW * C::H : 1); ++i) wreg[i] = 0;
-    while (u.valid()) {
+    if constexpr (C::BPAIR) {
+      // The bound over 16-vector blocks.  This warp's set takes every other unit
+      // of the CTA's range (those of parity tile_par), so the walk of TcUnits
+      // steps two units at a time, on 32-bit counters like the stage and its
+      // phase, and lanes 0..BQ-1 store the bitmap words of the warp's BQ rows.
+      constexpr int BQ = C::NQ / QSTEP;        // rows of a group this warp reads
+      static_assert(BQ % 2 == 0 && BQ <= 32, "rows in pairs, one storing lane each");
+      int bq_len[BQ];
+      float bq_coef[BQ], bq_tau[BQ];
+      int32_t g = (int32_t)u.g, t = (int32_t)u.t, tiles_g = (int32_t)u.tiles_g, gcur = -1;
+      int64_t left = u.left;
+      if (tile_par == 1 && left > 0 && --left > 0) {
+        // the set's first unit is the range's second
+        ++t;
+        while (t >= tiles_g) {
+          ++g;
+          t = 0;
+          tiles_g = (int32_t)tc_group_tiles<C>(args, g);
+        }
+      }
+      uint32_t st = (uint32_t)tile_par, f_ph = 0;   // accumulator stage of the unit, its phase
+      uint32_t* cb_row = nullptr;                   // lane b < BQ: row b's candidate bitmap
+      while (left > 0) {
+        if (g != gcur) {
+          gcur = g;
+          __syncwarp();
+          // folded weights of the warp's rows, pair c = rows 2c, 2c + 1 stored
+          // (w_a[h], w_b[h]) adjacent
+          for (int i = lane; i < BQ * C::NCOL; i += 32) {
+            const int r = i / C::NCOL, h = i % C::NCOL;
+            const int64_t m = (int64_t)g * C::NQ + qfirst + r * QSTEP;
+            sW[(r >> 1) * 2 * C::NCOL + 2 * h + (r & 1)] = m < args.p.M ? args.wfold[m * 32 + h] : 0.0f;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int b = 0; b < BQ; ++b) {
+            const int64_t m = (int64_t)g * C::NQ + qfirst + b * QSTEP;
+            int64_t off = 0;
+            int len = 0;
+            if (m < args.p.M) {
+              row_extent(args.p, m, &off, &len);
+              if (args.row_mask && !args.row_mask[m]) len = 0;
+            }
+            bq_len[b] = len;
+            bq_coef[b] = m < args.p.M ? args.coef[m] : 0.0f;
+            bq_tau[b] = m < args.p.M ? args.tau[m] : 0.0f;
+          }
+          const int64_t ml = (int64_t)g * C::NQ + qfirst + lane * QSTEP;
+          cb_row = (lane < BQ && ml < args.p.M) ? args.candbits + ml * args.cb_stride : nullptr;
+        }
+        const int key = t * C::UKEYS + row_in_tile;
+        const uint32_t kbit = 1u << (key & 31);
+        // ||k|| and the seed words of this lane's key, read before the wait so that
+        // the loads overlap it (words cover max_key_len keys)
+        float knorm = 0.0f;
+        uint32_t sword = 0u, sw2[BQ];
+#pragma unroll
+        for (int b = 0; b < BQ; ++b) sw2[b] = 0u;
+        if (key < args.p.max_key_len) {
+          knorm = __ldg(args.knorm + key);
+          if (args.seed_stride == 0) sword = __ldg(args.seedbits + (key >> 5));
+        }
+        if (args.seed_stride != 0) {
+#pragma unroll
+          for (int b = 0; b < BQ; ++b) {
+            const int64_t m = (int64_t)g * C::NQ + qfirst + b * QSTEP;
+            if (key < bq_len[b]) sw2[b] = __ldg(args.seedbits + m * args.seed_stride + (key >> 5));
+          }
+        }
+        const bool got = mbar_wait(&acc_full[st], f_ph, abort_flag);
+        __syncwarp();                         // tcgen05.ld below is warp-collective
+        if (!__all_sync(0xffffffffu, got)) break;
+        tc_fence_after();
+        // 16 retained vectors per query, rows qfirst + b * QSTEP of the group, taken
+        // in pairs (2c, 2c + 1): the halves of packed chains, two per pair (heads
+        // 2i and 2i + 1) so that each dependent sequence is 8 deep, then their sum.
+        // The summation order differs from the scalar chain by a few ulp, far
+        // inside the margin coef[m] already carries for the bf16 operands.
+        constexpr int NPR = BQ / 2;
+        const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + st * (uint32_t)C::ACC_STRIDE;
+        float chain[BQ];
+        uint32_t agg[BQ];
+#pragma unroll
+        for (int c = 0; c < NPR; ++c) {
+          // rows 2c and 2c + 1: columns 0..15 of each (one TMEM wait per pair, so
+          // that only one pair's values are live)
+          uint32_t v[2][32];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int q = qfirst + (2 * c + e) * QSTEP;
+            tmem_ld_32x32b_x16(tbase + (uint32_t)(q * C::NCOL), v[e]);
+            agg[2 * c + e] = tmem_ld_32x32b_x1(tbase + (uint32_t)(C::NQ * C::NCOL + q));
+          }
+          tmem_ld_wait();
+          // weights of pair c stored (w_a[h], w_b[h]) adjacent: one 16-byte load
+          // gives the operand pairs of heads j and j + 1
+          const float4* w4 = reinterpret_cast<const float4*>(sW + c * 2 * C::NCOL);
+          uint64_t se = f2_pack(0.0f, 0.0f), so = f2_pack(0.0f, 0.0f);
+#pragma unroll
+          for (int j2 = 0; j2 < 8; ++j2) {
+            const float4 ww = w4[j2];
+            const int j = 2 * j2;
+            se = f2_fma(f2_pack(ww.x, ww.y),
+                        f2_pack(fmaxf(__uint_as_float(v[0][j]), 0.0f), fmaxf(__uint_as_float(v[1][j]), 0.0f)), se);
+            so = f2_fma(f2_pack(ww.z, ww.w),
+                        f2_pack(fmaxf(__uint_as_float(v[0][j + 1]), 0.0f), fmaxf(__uint_as_float(v[1][j + 1]), 0.0f)),
+                        so);
+          }
+          float e0, e1, o0, o1;
+          f2_unpack(se, &e0, &e1);
+          f2_unpack(so, &o0, &o1);
+          chain[2 * c] = e0 + o0;
+          chain[2 * c + 1] = e1 + o1;
+        }
+        unsigned mine = 0u;
+#pragma unroll
+        for (int b = 0; b < BQ; ++b) {
+          float ub = chain[b] - fmaxf(__uint_as_float(agg[b]), 0.0f);
+          ub = __fmaf_rn(bq_coef[b], knorm, ub);
+          const uint32_t word = args.seed_stride ? sw2[b] : sword;
+          const bool is_cand = key < bq_len[b] && !(word & kbit) && !(ub < bq_tau[b]);
+          const unsigned mk = __ballot_sync(0xffffffffu, is_cand);
+          if (lane == b) mine = mk;
+        }
+        // the warp's 32 keys are one bitmap word (key - lane is a multiple of 32)
+        const int64_t wd = (int64_t)t * (C::UKEYS / 32) + quarter;
+        if (cb_row && wd < args.cb_stride) cb_row[wd] = mine;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[st]);
+        // this set's next unit, two on (groups without tiles are skipped)
+        st += 2;
+        if (st >= (uint32_t)C::SACC) {
+          st -= C::SACC;
+          f_ph ^= 1u;
+        }
+        left -= 2;
+        if (left > 0) {
+          t += 2;
+          while (t >= tiles_g) {
+            t -= tiles_g;
+            ++g;
+            tiles_g = (int32_t)tc_group_tiles<C>(args, g);
+          }
+        }
+      }
+    }
+    while (!C::BPAIR && u.valid()) {
       if (u.g != cur_g) {
         cur_g = u.g;
         __syncwarp();
@@ -853,7 +991,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           const int64_t m = cur_g * C::NQ + qi;
           float wv = 0.0f;
           if (m < args.p.M) wv = C::BOUND ? args.wfold[m * 32 + h] : args.p.w[m * C::H + h];
-          if constexpr (C::PAIR || C::BPAIR) {
+          if constexpr (C::PAIR) {
             // this warp's r-th query goes to pair r/2, half r%2: [pair][h][2]
             if ((qi - qfirst) % QSTEP != 0) continue;
             const int r = (qi - qfirst) / QSTEP;
@@ -889,15 +1027,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           for (int i = 0; i < PPW * C::H; ++i)
             wreg[i] = reinterpret_cast<const uint64_t*>(sW + (i / C::H) * 2 * C::NCOL)[i % C::H];
         }
-        if constexpr (C::BPAIR) {
-#pragma unroll
-          for (int b = 0; b < BQ; ++b) {
-            const int qi = qfirst + b * QSTEP;
-            bq_len[b] = sLen[qi];
-            bq_coef[b] = sAux[4 * qi];
-            bq_tau[b] = sAux[4 * qi + 1];
-          }
-        }
       }
       if (C::ALT && (int)(nacc & 1) != tile_par) {
         ++nacc;
@@ -912,19 +1041,6 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       if (C::BOUND && args.seed_stride == 0 && key < args.p.max_key_len) sword = __ldg(args.seedbits + (key >> 5));
       float knorm = 0.0f;
       if (C::KN_GLOBAL && key < args.p.max_key_len) knorm = __ldg(args.knorm + key);
-      // per-row seed bitmaps: the words of this warp's rows, also before the wait
-      uint32_t sw2[BQ];
-#pragma unroll
-      for (int b = 0; b < BQ; ++b) sw2[b] = 0u;
-      if constexpr (C::BPAIR) {
-        if (args.seed_stride != 0) {
-#pragma unroll
-          for (int b = 0; b < BQ; ++b) {
-            const int64_t m = cur_g * C::NQ + qfirst + b * QSTEP;
-            if (key < bq_len[b]) sw2[b] = __ldg(args.seedbits + m * args.seed_stride + (key >> 5));
-          }
-        }
-      }
       bool got = mbar_wait(&acc_full[acc], (nacc / C::SACC) & 1, abort_flag);
       // the key-tile slot of this unit (bound: read below for ||k||, so the slot is
       // held until this warp releases it) and its scale slot (FP8)
@@ -1012,67 +1128,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         }
         bound_finish(qi, m, ub, v[31]);
       };
-      if constexpr (C::BPAIR) {
-        // 16 retained vectors per query, rows qfirst + b * QSTEP of the group, taken
-        // in pairs (2c, 2c + 1): the halves of packed chains, two per pair (heads
-        // 2i and 2i + 1) so that each dependent sequence is 8 deep, then their sum.
-        // The summation order differs from the scalar chain by a few ulp, far
-        // inside the margin coef[m] already carries for the bf16 operands.
-        constexpr int NPR = BQ / 2;
-        const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
-        float chain[BQ];
-        uint32_t agg[BQ];
-#pragma unroll
-        for (int c = 0; c < NPR; ++c) {
-          // rows 2c and 2c + 1: columns 0..15 of each (one TMEM wait per pair, so
-          // that only one pair's values are live)
-          uint32_t v[2][32];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int q = qfirst + (2 * c + e) * QSTEP;
-            tmem_ld_32x32b_x16(tbase + (uint32_t)(q * C::NCOL), v[e]);
-            agg[2 * c + e] = tmem_ld_32x32b_x1(tbase + (uint32_t)(C::NQ * C::NCOL + q));
-          }
-          tmem_ld_wait();
-          // weights of pair c stored (w_a[h], w_b[h]) adjacent: one 16-byte load
-          // gives the operand pairs of heads j and j + 1
-          const float4* w4 = reinterpret_cast<const float4*>(sW + c * 2 * C::NCOL);
-          uint64_t se = f2_pack(0.0f, 0.0f), so = f2_pack(0.0f, 0.0f);
-#pragma unroll
-          for (int j2 = 0; j2 < 8; ++j2) {
-            const float4 ww = w4[j2];
-            const int j = 2 * j2;
-            se = f2_fma(f2_pack(ww.x, ww.y),
-                        f2_pack(fmaxf(__uint_as_float(v[0][j]), 0.0f), fmaxf(__uint_as_float(v[1][j]), 0.0f)), se);
-            so = f2_fma(f2_pack(ww.z, ww.w),
-                        f2_pack(fmaxf(__uint_as_float(v[0][j + 1]), 0.0f), fmaxf(__uint_as_float(v[1][j + 1]), 0.0f)),
-                        so);
-          }
-          float e0, e1, o0, o1;
-          f2_unpack(se, &e0, &e1);
-          f2_unpack(so, &o0, &o1);
-          chain[2 * c] = e0 + o0;
-          chain[2 * c + 1] = e1 + o1;
-        }
-        unsigned mask[BQ];
-#pragma unroll
-        for (int b = 0; b < BQ; ++b) {
-          float ub = chain[b] - fmaxf(__uint_as_float(agg[b]), 0.0f);
-          ub = __fmaf_rn(bq_coef[b], knorm, ub);
-          const uint32_t word = args.seed_stride ? sw2[b] : sword;
-          const bool is_cand = key < bq_len[b] && !((word >> (key & 31)) & 1u) && !(ub < bq_tau[b]);
-          mask[b] = __ballot_sync(0xffffffffu, is_cand);
-        }
-        // the warp's 32 keys are one bitmap word (key - lane is a multiple of 32)
-        const int64_t wd = key >> 5;
-        if (lane == 0 && wd < args.cb_stride) {
-#pragma unroll
-          for (int b = 0; b < BQ; ++b) {
-            const int64_t m = cur_g * C::NQ + qfirst + b * QSTEP;
-            if (m < args.p.M) args.candbits[m * args.cb_stride + wd] = mask[b];
-          }
-        }
-      } else if constexpr (C::BOUND && !C::FP8 && C::NQ > 1 && (C::NQ == 4 * QSTEP || C::NQ == 2 * QSTEP)) {
+      if constexpr (C::BOUND && !C::FP8 && C::NQ > 1 && (C::NQ == 4 * QSTEP || C::NQ == 2 * QSTEP)) {
         constexpr int QPW = C::NQ / QSTEP;     // queries of this warp in a tile
         const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
         if (args.R <= 16) {
