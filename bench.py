@@ -643,7 +643,10 @@ def witness_vs_memcpy(B, dev, stream, reps=30):
     setting) against a device-to-device copy of the same [rows, 2048] int32
     buffer (cudaMemcpyAsync through torch), each timed by CUDA events on the
     stream, median of `reps`; the merge runs on a fresh copy of the learned
-    rows every time (the refresh lies outside its events)."""
+    rows every time (the refresh lies outside its events).  A spin of the GPU
+    (torch.cuda._sleep, outside the events) holds the stream while the host
+    enqueues both timed calls, so that at a few rows the events measure the
+    device time and not the host's submission gap."""
     out = {}
     topk, S = 2048, 64
     for rows in (32, 64, 128, 256, 512, 65536):
@@ -657,6 +660,7 @@ def witness_vs_memcpy(B, dev, stream, reps=30):
             tw, tc = [], []
             for i in range(reps + 3):
                 work.copy_(src)
+                torch.cuda._sleep(200_000)
                 ev[0].record(stream)
                 B.witness_merge(work, c, topk - S, S, S, stream=stream)
                 ev[1].record(stream)
