@@ -1,5 +1,6 @@
 // C-ABI entry points of libidx: argument validation on the host, workspace
 // carving and dispatch to the kernels.  Nothing here computes on the host.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -49,14 +50,21 @@ static idx_status cuda_status(cudaError_t e, const char* where) {
   return fail(IDX_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }
 
+// SM count of the calling thread's current device, cached per device (the
+// kernels size their grids by it, and a process may switch devices).
 int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
   }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (cached) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
