@@ -111,3 +111,48 @@ def test_topk_prior_refusals(L):
     # workspace too small
     assert L.idx_topk_prior(ctypes.byref(p), 16, one, 16, 64, one, nul, nul, nul, one, 16, nul) == 6
     assert L.idx_topk_prior_workspace_size(ctypes.byref(p), 16, 16, 64) > 4 * 4096 * 4
+
+
+def test_dosa_refusals_and_layout(L):
+    """dosa_topk refuses bad arguments before any launch; the workspace layout
+    is host arithmetic: every region lies inside the workspace size."""
+    from sparse_attention_indexer_idx_gb300 import binding as B
+    nul = ctypes.c_void_p(0)
+    one = ctypes.c_void_p(256)
+    big = 1 << 40
+    # 64 queries over 65536 shared bf16 keys (key_off NULL), H64 D128
+    p = B.idx_problem(one, B.IDX_BF16, one, 64, 64, 128, one, B.IDX_BF16, None, 65536, None, one, 65536)
+    dp = B.make_dosa_params(n_seed=4096, retained_heads=16)
+
+    def call(K=256, params=dp, seeds=nul, seed_ld=0, out=one, ws_bytes=big, prob=p):
+        pp = ctypes.byref(params) if params is not None else None
+        return L.dosa_topk(ctypes.byref(prob), K, pp, seeds, seed_ld, out, nul, nul, nul, one, ws_bytes, nul)
+
+    assert call(params=None) == 4                                   # NULL params
+    assert call(K=0) == 4 and call(K=4097) == 4                     # K outside [1, 4096]
+    for field, bad in (("n_seed", -1), ("retained_heads", 0), ("n_sample", 0), ("candidate_capacity", -1),
+                       ("act_freq_min", 1.5), ("act_freq_min", float("nan")), ("margin_gamma", -1.0)):
+        q = B.make_dosa_params(n_seed=4096, retained_heads=16)
+        setattr(q, field, bad)
+        assert call(params=q) == 4, field
+    assert call(seeds=one, seed_ld=0) == 4                          # caller seeds without a row stride
+    assert call(out=nul) == 4                                       # NULL output ids
+    need = L.dosa_topk_workspace_size(ctypes.byref(p), 256, ctypes.byref(dp), 0)
+    assert need > 64 * 65536 // 8                                   # at least the candidate bitmaps
+    assert call(ws_bytes=need - 1) == 6                             # workspace too small
+    p0 = B.idx_problem(one, B.IDX_BF16, one, 0, 64, 128, one, B.IDX_BF16, None, 65536, None, one, 65536)
+    assert call(prob=p0, ws_bytes=0) == 0                           # no rows: nothing to do
+    # the size grows with the rows
+    p2 = B.idx_problem(one, B.IDX_BF16, one, 128, 64, 128, one, B.IDX_BF16, None, 65536, None, one, 65536)
+    assert L.dosa_topk_workspace_size(ctypes.byref(p2), 256, ctypes.byref(dp), 0) > need
+
+    lay = B.dosa_ws_layout()
+    assert L.dosa_workspace_layout(ctypes.byref(p), 256, ctypes.byref(dp), 0, None) == 4
+    assert L.dosa_workspace_layout(ctypes.byref(p), 0, ctypes.byref(dp), 0, ctypes.byref(lay)) == 4
+    assert L.dosa_workspace_layout(ctypes.byref(p), 256, ctypes.byref(dp), 0, ctypes.byref(lay)) == 0
+    offs = [getattr(lay, n) for n in ("seed_list", "seed_count", "rep_count", "rep_scores", "tau", "status",
+                                      "plan_head", "plan_beta", "plan_dnorm", "wfold", "coef", "qprep")]
+    assert all(0 <= o < need for o in offs)
+    assert len(set(offs)) == len(offs)                              # distinct regions
+    assert lay.seed_rows == 1                                       # shared keys: one seed list for all rows
+    assert lay.seed_ld >= 4096 and lay.rep_ld >= 65536
