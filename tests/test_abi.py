@@ -156,3 +156,37 @@ def test_dosa_refusals_and_layout(L):
     assert len(set(offs)) == len(offs)                              # distinct regions
     assert lay.seed_rows == 1                                       # shared keys: one seed list for all rows
     assert lay.seed_ld >= 4096 and lay.rep_ld >= 65536
+
+
+def test_topk_scores_refusals(L):
+    nul = ctypes.c_void_p(0)
+    one = ctypes.c_void_p(256)
+    # ld below max_len, negative rows, K outside [1, 4096], NULL lengths
+    assert L.idx_topk_scores(one, 100, one, 4, 128, 16, one, nul, one, 1 << 30, nul) == 4
+    assert L.idx_topk_scores(one, 128, one, -1, 128, 16, one, nul, one, 1 << 30, nul) == 4
+    assert L.idx_topk_scores(one, 128, one, 4, 128, 0, one, nul, one, 1 << 30, nul) == 4
+    assert L.idx_topk_scores(one, 128, one, 4, 128, 4097, one, nul, one, 1 << 30, nul) == 4
+    assert L.idx_topk_scores(one, 128, nul, 4, 128, 16, one, nul, one, 1 << 30, nul) == 4
+    need = L.idx_topk_scores_workspace_size(4, 1 << 16, 16)
+    if need > 0:
+        assert L.idx_topk_scores(one, 1 << 16, one, 4, 1 << 16, 16, one, nul, one, need - 1, nul) == 6
+    assert L.idx_topk_scores(nul, 0, nul, 0, 0, 16, nul, nul, nul, 0, nul) == 0      # no rows
+
+
+def test_block_select_static_refusals(L):
+    """The fixed-array entry point checks Q x n_kv x blocks against its 2^23
+    block scores by division, so sizes whose product would wrap are refused
+    too; all before any device work."""
+    from sparse_attention_indexer_idx_gb300 import binding as B
+    nul = ctypes.c_void_p(0)
+    one = ctypes.c_void_p(256)
+    cfg = B.block_sparse_config(128, 32, 1, 2)
+    assert L.block_select_static(one, one, one, 4, 2, 128, 1024, None, one, 32, nul, nul) == 4      # NULL config
+    assert L.block_select_static(one, one, one, 4, 2, 128, 1024, ctypes.byref(cfg), one, 31, nul, nul) == 4
+    assert L.block_select_static(one, one, one, 4, 2, 512, 1024, ctypes.byref(cfg), one, 32, nul, nul) == 5
+    big = 1 << 23
+    assert L.block_select_static(one, one, one, big, 2, 128, 1024, ctypes.byref(cfg), one, 32, nul, nul) == 6
+    # Q * n_kv * blocks far past 2^63 (a product computed first would wrap)
+    assert L.block_select_static(one, one, one, 1 << 40, 1 << 20, 128, 1 << 62, ctypes.byref(cfg), one, 32,
+                                 nul, nul) == 6
+    assert L.block_select_static(one, one, one, 0, 2, 128, 1024, ctypes.byref(cfg), one, 32, nul, nul) == 0
