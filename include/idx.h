@@ -95,6 +95,10 @@ idx_status idx_set_wait_limit_ns(uint64_t ns);
  *   key_len  device [M] int32, L_r >= 0; key ids are row-relative, 0..L_r-1.
  *   max_key_len host-side bound on every key_len[m] (sizes grids/workspaces).
  *
+ * Sizes: M <= 2^40, n_keys <= 2^46 and M * max_key_len <= 2^56, so that every
+ * size derived from them stays inside 64-bit arithmetic; larger problems are
+ * refused with IDX_ERR_UNSUPPORTED before any device work.
+ *
  * Supported: (F32 q, F32 keys) any H <= 128, D <= 256 on CUDA cores;
  * (BF16 q, BF16 keys) and (BF16 q, FP8 keys) with D = 128 and H in
  * {16, 32, 64, 128} on the tensor cores; (BF16 q, BF16 keys) other shapes on

@@ -73,6 +73,13 @@ static idx_status check_problem(const idx_problem* p) {
   if (p->M < 0 || p->H <= 0 || p->D <= 0 || p->n_keys < 0 || p->max_key_len < 0)
     return fail(IDX_ERR_INVALID_ARG, "negative or zero size (M=%lld H=%d D=%d n_keys=%lld max_key_len=%d)",
                 (long long)p->M, p->H, p->D, (long long)p->n_keys, p->max_key_len);
+  // bounds that keep every size derived from the problem (the M x max_key_len
+  // scores, workspaces, key offsets) far inside 64-bit arithmetic (checked by
+  // division, so the check itself cannot wrap)
+  if (p->M > ((int64_t)1 << 40) || p->n_keys > ((int64_t)1 << 46) ||
+      (p->max_key_len > 0 && p->M > ((int64_t)1 << 56) / p->max_key_len))
+    return fail(IDX_ERR_UNSUPPORTED, "problem too large (M=%lld max_key_len=%d n_keys=%lld)", (long long)p->M,
+                p->max_key_len, (long long)p->n_keys);
   if (p->M > 0 && (!p->q || !p->w || !p->key_len))
     return fail(IDX_ERR_INVALID_ARG, "q, w and key_len must be non-NULL");
   if (p->n_keys > 0 && !p->keys) return fail(IDX_ERR_INVALID_ARG, "keys is NULL");

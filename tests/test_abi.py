@@ -190,3 +190,17 @@ def test_block_select_static_refusals(L):
     assert L.block_select_static(one, one, one, 1 << 40, 1 << 20, 128, 1 << 62, ctypes.byref(cfg), one, 32,
                                  nul, nul) == 6
     assert L.block_select_static(one, one, one, 0, 2, 128, 1024, ctypes.byref(cfg), one, 32, nul, nul) == 0
+
+
+def test_problem_size_bounds(L):
+    """Problems whose derived sizes would leave 64-bit arithmetic are refused."""
+    from sparse_attention_indexer_idx_gb300 import binding as B
+    nul = ctypes.c_void_p(0)
+    one = ctypes.c_void_p(256)
+    huge_m = B.idx_problem(one, B.IDX_F32, one, (1 << 40) + 1, 4, 16, one, B.IDX_F32, one, 1 << 20, None, one, 16)
+    assert L.idx_score(ctypes.byref(huge_m), one, 16, nul) == 5
+    wide = B.idx_problem(one, B.IDX_F32, one, 1 << 30, 4, 16, one, B.IDX_F32, one, 1 << 40, None, one, 1 << 30)
+    assert L.idx_score(ctypes.byref(wide), one, 1 << 30, nul) == 5
+    many_keys = B.idx_problem(one, B.IDX_F32, one, 4, 4, 16, one, B.IDX_F32, one, (1 << 46) + 1, None, one, 16)
+    assert L.idx_score(ctypes.byref(many_keys), one, 16, nul) == 5
+    assert b"too large" in L.idx_last_error_string()
