@@ -63,11 +63,18 @@
 //                         tile) or alternate tiles (one query per tile):
 //                         tcgen05.ld -> score / bound -> global
 //              next       (FP8 only) split of each query group's bf16 rows
-//                         into the e4m3 hi and lo tiles
+//                         into the e4m3 hi and lo tiles; (gathered tiles)
+//                         the second producer warp
+// Two layouts differ (TcCfg): the bf16 bound over several queries has sixteen
+// epilogue warps (warps 2..17; over 16-vector blocks, two sets of eight taking
+// alternate units), and the two-query score epilogue with its weights in
+// registers has twelve warps, the epilogue being warps 4..11 (WREG).
 // One thread issues every tcgen05.mma of the CTA: a build in which a second
 // warp issued every other round into the same accumulators gave, in about one
 // launch in twenty, a few wrong rows of one tile (repeated launches on the same
-// inputs compared bit for bit); with a single issuer every repeat is identical.
+// inputs compared bit for bit): the two threads shared the query buffer's
+// release barrier, which one thread's commit could complete while the other's
+// MMAs still read the buffer.  With a single issuer every repeat is identical.
 // Every wait is bounded (see common.cuh); on a timeout all roles stop, the
 // producer and the MMA thread drain what they issued, and TMEM is released.
 #pragma once
