@@ -183,6 +183,19 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _buf(t: Optional[torch.Tensor], dtype: torch.dtype, numel: int, name: str):
+    """A caller's device buffer that the library writes or reads as `numel`
+    elements of `dtype` (the C ABI takes plain pointers, so this is the last
+    place where a short or mistyped buffer can be caught)."""
+    if t is None:
+        return None
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: {t.numel()} elements, the call needs {numel}")
+    return _ptr(t)
+
+
 def _stream(stream: Optional[torch.cuda.Stream]):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
@@ -238,7 +251,9 @@ def idx_topk_workspace_size(p: Problem, K: int) -> int:
 def idx_topk(p: Problem, K: int, out_ids: torch.Tensor, out_scores: Optional[torch.Tensor], ws: torch.Tensor,
              stream=None):
     cp = p.c()
-    _check(lib().idx_topk(ctypes.byref(cp), K, _ptr(out_ids), _ptr(out_scores), _ptr(ws), ws.numel() * ws.element_size(),
+    MK = p.q.shape[0] * K
+    _check(lib().idx_topk(ctypes.byref(cp), K, _buf(out_ids, torch.int32, MK, "out_ids"),
+                          _buf(out_scores, torch.float32, MK, "out_scores"), _ptr(ws), ws.numel() * ws.element_size(),
                           _stream(stream)))
     return out_ids, out_scores
 
@@ -254,9 +269,12 @@ def idx_topk_prior(p: Problem, K: int, prior_ids: torch.Tensor, capacity: int, o
     """Top-K with the previous step's selection prior_ids [M, prior_ld] as a prior.
     stats: torch.zeros(3, dtype=torch.int64) storage for topk_prior_stats, or None."""
     cp = p.c()
-    _check(lib().idx_topk_prior(ctypes.byref(cp), K, _ptr(prior_ids), prior_ids.shape[1], capacity, _ptr(out_ids),
-                                _ptr(out_scores), _ptr(row_status), _ptr(stats), _ptr(ws),
-                                ws.numel() * ws.element_size(), _stream(stream)))
+    M = p.q.shape[0]
+    _check(lib().idx_topk_prior(ctypes.byref(cp), K, _buf(prior_ids, torch.int32, M * prior_ids.shape[1], "prior_ids"),
+                                prior_ids.shape[1], capacity, _buf(out_ids, torch.int32, M * K, "out_ids"),
+                                _buf(out_scores, torch.float32, M * K, "out_scores"),
+                                _buf(row_status, torch.int32, M, "row_status"), _buf(stats, torch.int64, 3, "stats"),
+                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
     return out_ids, out_scores
 
 
@@ -264,9 +282,12 @@ def idx_topk_prior_events(p: Problem, K: int, prior_ids: torch.Tensor, capacity:
                           out_scores: Optional[torch.Tensor], ws: torch.Tensor, events, stream=None):
     """idx_topk_prior recording 6 torch.cuda.Event (already created) between its stages."""
     cp = p.c()
+    M = p.q.shape[0]
     handles = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events[:6]])
-    _check(lib().idx_topk_prior_events(ctypes.byref(cp), K, _ptr(prior_ids), prior_ids.shape[1], capacity,
-                                       _ptr(out_ids), _ptr(out_scores), None, None, _ptr(ws),
+    _check(lib().idx_topk_prior_events(ctypes.byref(cp), K,
+                                       _buf(prior_ids, torch.int32, M * prior_ids.shape[1], "prior_ids"),
+                                       prior_ids.shape[1], capacity, _buf(out_ids, torch.int32, M * K, "out_ids"),
+                                       _buf(out_scores, torch.float32, M * K, "out_scores"), None, None, _ptr(ws),
                                        ws.numel() * ws.element_size(), handles, 6, _stream(stream)))
     return out_ids, out_scores
 
@@ -301,9 +322,13 @@ def dosa_topk(p: Problem, K: int, dp: dosa_params, out_ids: torch.Tensor, out_sc
               ws: torch.Tensor, seed_ids: Optional[torch.Tensor] = None, row_status: Optional[torch.Tensor] = None,
               stats: Optional[torch.Tensor] = None, stream=None):
     cp = p.c()
+    M = p.q.shape[0]
     seed_ld = int(seed_ids.shape[1]) if seed_ids is not None else 0
-    _check(lib().dosa_topk(ctypes.byref(cp), K, ctypes.byref(dp), _ptr(seed_ids), seed_ld, _ptr(out_ids),
-                           _ptr(out_scores), _ptr(row_status), _ptr(stats), _ptr(ws),
+    _check(lib().dosa_topk(ctypes.byref(cp), K, ctypes.byref(dp), _buf(seed_ids, torch.int32, M * seed_ld, "seed_ids"),
+                           seed_ld, _buf(out_ids, torch.int32, M * K, "out_ids"),
+                           _buf(out_scores, torch.float32, M * K, "out_scores"),
+                           _buf(row_status, torch.int32, M, "row_status"),
+                           _buf(stats, torch.int64, DOSA_STATS_FIELDS, "stats"), _ptr(ws),
                            ws.numel() * ws.element_size(), _stream(stream)))
     return out_ids, out_scores
 

@@ -204,3 +204,17 @@ def test_problem_size_bounds(L):
     many_keys = B.idx_problem(one, B.IDX_F32, one, 4, 4, 16, one, B.IDX_F32, one, (1 << 46) + 1, None, one, 16)
     assert L.idx_score(ctypes.byref(many_keys), one, 16, nul) == 5
     assert b"too large" in L.idx_last_error_string()
+
+
+def test_binding_checks_buffers():
+    """The binding checks each output buffer's dtype and size before the call
+    (the C ABI takes plain pointers): a short or mistyped buffer raises."""
+    import torch
+    from sparse_attention_indexer_idx_gb300 import binding as B
+    with pytest.raises(ValueError, match="expected torch.int32"):
+        B._buf(torch.zeros(8, dtype=torch.int64), torch.int32, 8, "out_ids")
+    with pytest.raises(ValueError, match="the call needs 8"):
+        B._buf(torch.zeros(7, dtype=torch.int32), torch.int32, 8, "out_ids")
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        B._buf(torch.zeros(8, dtype=torch.int32), torch.int32, 8, "out_ids")
+    assert B._buf(None, torch.int32, 8, "out_scores") is None
