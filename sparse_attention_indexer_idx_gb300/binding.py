@@ -236,10 +236,16 @@ def set_wait_limit_ns(ns: int) -> None:
     _check(lib().idx_set_wait_limit_ns(int(ns)))
 
 
+def _rows_need(M: int, ld: int, width: int) -> int:
+    """Elements that M rows of `width` values at row stride `ld` span."""
+    return 0 if M <= 0 or width <= 0 else (M - 1) * ld + width
+
+
 def idx_score(p: Problem, scores: torch.Tensor, ld: Optional[int] = None, stream=None) -> torch.Tensor:
     cp = p.c()
-    _check(lib().idx_score(ctypes.byref(cp), _ptr(scores), int(ld if ld is not None else scores.shape[-1]),
-                           _stream(stream)))
+    ld = int(ld if ld is not None else scores.shape[-1])
+    need = _rows_need(p.q.shape[0], ld, int(p.max_key_len))
+    _check(lib().idx_score(ctypes.byref(cp), _buf(scores, torch.float32, need, "scores"), ld, _stream(stream)))
     return scores
 
 
@@ -300,9 +306,12 @@ def idx_topk_scores(scores: torch.Tensor, lens: torch.Tensor, max_len: int, K: i
                     out_scores: Optional[torch.Tensor] = None, ld: Optional[int] = None,
                     ws: Optional[torch.Tensor] = None, stream=None):
     M = lens.shape[0]
+    ld = int(ld if ld is not None else scores.shape[-1])
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
-    _check(lib().idx_topk_scores(_ptr(scores), int(ld if ld is not None else scores.shape[-1]), _ptr(lens), M,
-                                 int(max_len), K, _ptr(out_ids), _ptr(out_scores), _ptr(ws), ws_bytes,
+    _check(lib().idx_topk_scores(_buf(scores, torch.float32, _rows_need(M, ld, int(max_len)), "scores"), ld,
+                                 _buf(lens, torch.int32, M, "lens"), M, int(max_len), K,
+                                 _buf(out_ids, torch.int32, M * K, "out_ids"),
+                                 _buf(out_scores, torch.float32, M * K, "out_scores"), _ptr(ws), ws_bytes,
                                  _stream(stream)))
     return out_ids, out_scores
 

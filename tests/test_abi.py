@@ -218,3 +218,12 @@ def test_binding_checks_buffers():
     with pytest.raises(ValueError, match="CUDA tensor"):
         B._buf(torch.zeros(8, dtype=torch.int32), torch.int32, 8, "out_ids")
     assert B._buf(None, torch.int32, 8, "out_scores") is None
+
+
+def test_binding_row_span():
+    from sparse_attention_indexer_idx_gb300 import binding as B
+    assert B._rows_need(0, 100, 50) == 0
+    assert B._rows_need(4, 100, 0) == 0
+    assert B._rows_need(1, 100, 50) == 50
+    assert B._rows_need(4, 100, 100) == 400
+    assert B._rows_need(4, 128, 100) == 3 * 128 + 100
